@@ -1,0 +1,167 @@
+"""Chunkwise form of the gated delta rule in numpy fp64 (test-side restatement).
+
+This is the chunk algorithm the CUDA kernels implement, written as plainly as
+possible so that the tests can pin it against the token-by-token oracle:
+forward for every chunk size (including a ragged tail), and the reverse chunk
+scan for the backward pass.  It does not import the oracle or the library.
+
+Per sequence and chunk of n tokens, with gamma = within-chunk cumulative sum
+of the log gate (per key dimension for KDA, broadcast over it for GDN) and
+Gam[r,j,d] = exp(gamma[r,d] - gamma[j,d]) for j <= r (0 above the diagonal):
+
+    A = strict_lower( beta_r * sum_d k_rd k_jd Gam[r,j,d] )
+    R = V - (K * E) H_in,           E = exp(gamma)
+    U = (I + A)^-1 diag(beta) R     (the WY / UT transform)
+    P = lower_incl( sum_d q_rd k_jd Gam[r,j,d] )
+    O = (Q * E) H_in + P U
+    H_out = diag(exp(gamma_last)) H_in + (K * exp(gamma_last - gamma))^T U
+
+The backward pass walks the chunks in reverse, given dO and the gradient of
+H_out, and returns the gradient of H_in for the previous chunk.  Log-gate
+gradients are accumulated per position as d(gamma) and turned into d(g) by a
+reverse cumulative sum inside the chunk.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _chunk_gates(g_chunk, dk, kda):
+    gam = np.cumsum(g_chunk, axis=0)
+    if not kda:
+        gam = np.repeat(gam[:, None], dk, axis=1)
+    n = gam.shape[0]
+    diff = gam[:, None, :] - gam[None, :, :]          # [r, j, d]
+    mask = np.tril(np.ones((n, n), dtype=bool))
+    Gam = np.where(mask[:, :, None], np.exp(np.where(mask[:, :, None], diff, 0.0)), 0.0)
+    return gam, Gam, mask
+
+
+def chunk_forward(Q, K, V, g, beta, H_in, kda):
+    dk = K.shape[1]
+    n = K.shape[0]
+    gam, Gam, mask = _chunk_gates(g, dk, kda)
+    E = np.exp(gam)
+    F = np.exp(gam[-1][None, :] - gam)
+    KKg = np.einsum("rd,jd,rjd->rj", K, K, Gam)
+    A = np.tril(beta[:, None] * KKg, -1)
+    L = np.eye(n) + A
+    R = V - (K * E) @ H_in
+    U = np.linalg.solve(L, beta[:, None] * R)
+    P = np.einsum("rd,jd,rjd->rj", Q, K, Gam) * mask
+    O = (Q * E) @ H_in + P @ U
+    H_out = np.exp(gam[-1])[:, None] * H_in + (K * F).T @ U
+    return O, H_out
+
+
+def forward(q, k, v, g, beta, h0, chunk, kda=False):
+    """Chunked forward over [B,T,H,*] inputs; returns (o, ht)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[3]
+    o = np.zeros((B, T, H, dv))
+    ht = np.zeros((B, H, dk, dv))
+    for b in range(B):
+        for h in range(H):
+            S = np.zeros((dk, dv)) if h0 is None else h0[b, h].astype(np.float64)
+            for c0 in range(0, T, chunk):
+                c1 = min(T, c0 + chunk)
+                o[b, c0:c1, h], S = chunk_forward(q[b, c0:c1, h], k[b, c0:c1, h], v[b, c0:c1, h],
+                                                  g[b, c0:c1, h], beta[b, c0:c1, h], S, kda)
+            ht[b, h] = S
+    return o, ht
+
+
+def chunk_backward(Q, K, V, g, beta, H_in, dO, dH_out, kda):
+    """Gradients of one chunk; returns (dQ, dK, dV, dg, dbeta, dH_in)."""
+    dk = K.shape[1]
+    n = K.shape[0]
+    gam, Gam, mask = _chunk_gates(g, dk, kda)
+    E = np.exp(gam)
+    eC = np.exp(gam[-1])
+    F = np.exp(gam[-1][None, :] - gam)
+    KKg = np.einsum("rd,jd,rjd->rj", K, K, Gam)
+    A = np.tril(beta[:, None] * KKg, -1)
+    L = np.eye(n) + A
+    R = V - (K * E) @ H_in
+    U = np.linalg.solve(L, beta[:, None] * R)
+    P = np.einsum("rd,jd,rjd->rj", Q, K, Gam) * mask
+
+    dgam = np.zeros((n, dk))
+    # H_out = diag(eC) H_in + (K*F)^T U
+    dH_in = eC[:, None] * dH_out
+    dgam[-1] += eC * np.sum(dH_out * H_in, axis=1)
+    UdH = U @ dH_out.T                                   # [n, dk]
+    dK = F * UdH
+    dF = K * UdH
+    dgam[-1] += np.sum(dF * F, axis=0)
+    dgam -= dF * F
+    dU = (K * F) @ dH_out
+    # O = (Q*E) H_in + P U
+    dQE = dO @ H_in.T
+    dQ = E * dQE
+    dgam += Q * E * dQE
+    dH_in += (Q * E).T @ dO
+    dP = (dO @ U.T) * mask
+    dU += P.T @ dO
+    # P[r,j] = sum_d q_rd k_jd Gam[r,j,d]
+    dQP = np.einsum("rj,jd,rjd->rd", dP, K, Gam)
+    dKP = np.einsum("rj,rd,rjd->jd", dP, Q, Gam)
+    dQ += dQP
+    dK += dKP
+    dgam += Q * dQP - K * dKP
+    # U = L^-1 diag(beta) R
+    dZ = np.linalg.solve(L.T, dU)
+    dA = np.tril(-dZ @ U.T, -1)
+    dbeta = np.sum(dZ * R, axis=1) + np.sum(dA * KKg, axis=1)
+    dR = beta[:, None] * dZ
+    # R = V - (K*E) H_in
+    dV = dR
+    dKE = -dR @ H_in.T
+    dK += E * dKE
+    dgam += K * E * dKE
+    dH_in -= (K * E).T @ dR
+    # A[r,j] = beta_r sum_d k_rd k_jd Gam[r,j,d]   (j < r)
+    dAt = dA * beta[:, None]
+    X = np.einsum("rj,jd,rjd->rd", dAt, K, Gam)
+    Y = np.einsum("rj,rd,rjd->jd", dAt, K, Gam)
+    dK += X + Y
+    dgam += K * X - K * Y
+    # gamma = cumsum(g)
+    dg = np.cumsum(dgam[::-1], axis=0)[::-1]
+    if not kda:
+        dg = dg.sum(axis=1)
+    return dQ, dK, dV, dg, dbeta, dH_in
+
+
+def backward(q, k, v, g, beta, h0, do, dht, chunk, kda=False):
+    """Chunked backward (state recompute, then reverse chunk scan)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[3]
+    out = {n: np.zeros(x.shape) for n, x in (("dq", q), ("dk", k), ("dv", v), ("dg", g),
+                                               ("dbeta", beta))}
+    out["dh0"] = np.zeros((B, H, dk, dv))
+    for b in range(B):
+        for h in range(H):
+            S = np.zeros((dk, dv)) if h0 is None else h0[b, h].astype(np.float64)
+            starts = list(range(0, T, chunk))
+            states = []
+            for c0 in starts:
+                c1 = min(T, c0 + chunk)
+                states.append(S)
+                _, S = chunk_forward(q[b, c0:c1, h], k[b, c0:c1, h], v[b, c0:c1, h],
+                                     g[b, c0:c1, h], beta[b, c0:c1, h], S, kda)
+            dS = np.zeros((dk, dv)) if dht is None else dht[b, h].astype(np.float64)
+            for ci in reversed(range(len(starts))):
+                c0 = starts[ci]
+                c1 = min(T, c0 + chunk)
+                sl = slice(c0, c1)
+                dQ, dK, dV, dg, db, dS = chunk_backward(q[b, sl, h], k[b, sl, h], v[b, sl, h],
+                                                        g[b, sl, h], beta[b, sl, h], states[ci],
+                                                        do[b, sl, h], dS, kda)
+                out["dq"][b, sl, h] = dQ
+                out["dk"][b, sl, h] = dK
+                out["dv"][b, sl, h] = dV
+                out["dg"][b, sl, h] = dg
+                out["dbeta"][b, sl, h] = db
+            out["dh0"][b, h] = dS
+    return out
