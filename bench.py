@@ -1,0 +1,435 @@
+#!/usr/bin/env python3
+"""GDN / KDA mixer forward + backward throughput on GB300, and its roofline.
+
+One step = one forward and one backward pass of the mixer over one batch of
+synthetic inputs (every step of the chunkwise method: gate prep, decayed
+K K^T, the triangular solve, WY factors, outputs, the inter-chunk state
+recurrence, the recomputed reverse chunk scan and the gate gradients).
+
+Default workload: GDN, B=16, T=2048, H=8, dk=dv=128, chunk 64, bf16 inputs
+with fp32 state (the 300M-model pre-training shape).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+With N > 1 (launched by torch.distributed.run) every rank runs its own batch
+(independent sequences, no exchange: weak scaling) and rank 0 reports the
+aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from gated_delta_rule_bwd_gb300 import workloads as W  # noqa: E402
+
+METRIC = "GDN/KDA mixer fwd+bwd tokens/s on 1 GB300; fraction of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+WORKLOADS = {"gdn_300m": W.GDN_300M_BF16, "kda_300m": W.KDA_300M_BF16, "gdn_1b": W.GDN_1B_BF16_H0,
+             "gdn_tiny": W.GDN_TINY_FP32}
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+def algorithmic(w):
+    """Per token-head algorithmic FLOPs and bytes of forward and backward.
+
+    FLOPs count the chunk algorithm's own matrix products (forward: decayed
+    K K^T, the two WY products, W H, Q H, Q K^T, P U and the state update;
+    backward: the recomputed forward products plus the gradient products),
+    C^2/3 for the triangular solve; the state recompute is not counted.
+    Bytes count each input read once and each output written once."""
+    dk, dv, C = w.dk, w.dv, w.chunk
+    e = 2 if w.dtype == "bf16" else 4
+    sg = 4 * dk if w.kda else 4
+    sb = 4
+    fwd_flops = 2 * C * (3 * dk + 2 * dv) + 6 * dk * dv + C * C / 3
+    bwd_flops = 2 * C * (7 * dk + 5 * dv) + 14 * dk * dv + C * C / 3
+    fwd_bytes = e * (2 * dk + 2 * dv) + sg + sb
+    bwd_bytes = e * (2 * dk + 2 * dv) + sg + sb + e * (2 * dk + dv) + sg + sb
+    return {"fwd_flops": fwd_flops, "bwd_flops": bwd_flops, "fwd_bytes": fwd_bytes,
+            "bwd_bytes": bwd_bytes}
+
+
+def state_bytes(w, kernel):
+    """Per-sequence state traffic of a kernel (h0 reads, final state write, dh0)."""
+    s = 4 * w.dk * w.dv
+    h0 = w.h0_std is not None
+    if kernel.endswith("_fwd"):
+        return s * (1 + h0)             # ht write (+ h0 read)
+    if kernel.endswith("_bwd"):
+        return s * (1 + h0)             # dh0 write (+ h0 read in the recompute)
+    return 0
+
+
+def kernel_work(w, kernel):
+    """(algorithmic bytes, FLOPs) of one launch of ``kernel`` on workload ``w``.
+
+    The forward kernel carries the forward op's work; the backward op's work
+    is carried by its main reverse-scan kernel (the state recompute and the
+    partial-sum reduction are implementation overhead and carry none)."""
+    a = algorithmic(w)
+    th = w.B * w.T * w.H
+    seqs = w.B * w.H
+    if kernel.endswith("_fwd"):
+        return a["fwd_bytes"] * th + state_bytes(w, kernel) * seqs, a["fwd_flops"] * th
+    if kernel.endswith("_bwd"):
+        return a["bwd_bytes"] * th + state_bytes(w, kernel) * seqs, a["bwd_flops"] * th
+    return 0.0, 0.0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) >= 9 and f[1].replace(".", "").isdigit():
+                    rows.append(f)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = [n for i, n in enumerate(names) if any(r[5 + i].lower() == "active" for r in rows)]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
+                if any(r[3].replace(".", "").isdigit() for r in rows) else None}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def cpu_oracle_run(w, rows, seed=0):
+    """Oracle forward + backward over ``rows`` batch rows of workload ``w``."""
+    import oracle
+    x = w.make(device="cpu", seed=seed, B=rows)
+    nthreads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.fwd(x.q, x.k, x.v, x.g, x.beta, x.h0, kda=w.kda, nthreads=nthreads)
+    if not w.fwd_only:
+        oracle.bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do, None, kda=w.kda, nthreads=nthreads)
+    return time.perf_counter() - t0, nthreads
+
+
+def cpu_baseline(w, min_s=10.0, max_s=30.0):
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    rows = max(1, cores // w.H)
+    elapsed, tokens, batches = 0.0, 0, 0
+    while elapsed < min_s and (elapsed == 0.0 or elapsed + elapsed / batches <= max_s):
+        dt, nthreads = cpu_oracle_run(w, rows, seed=batches)
+        elapsed += dt
+        tokens += rows * w.T
+        batches += 1
+    return {"value": tokens / elapsed, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{batches} x ({rows} batch rows x {w.H} heads x {w.T} tokens) of {w.name}, "
+                      f"fp64 token recurrence fwd+bwd, {elapsed:.1f} s"}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws, backend):
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import gated_delta_rule_bwd_gb300 as gdn
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init(ws, "nccl")
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    fwd = gdn.kda_fwd if w.kda else gdn.gdn_fwd
+    bwd = gdn.kda_bwd if w.kda else gdn.gdn_bwd
+
+    x = w.make(device=dev, seed=rank)
+    wsb = torch.empty(max(16, gdn.bwd_workspace_bytes(x.q, x.v, w.chunk, w.kda)),
+                      dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        o, ht = fwd(x.q, x.k, x.v, x.g, x.beta, x.h0, chunk=w.chunk)
+        gr = bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do, None, chunk=w.chunk, workspace=wsb)
+        return o, ht, gr
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        wall0 = time.perf_counter()
+        with gdn.KernelTimer(cap=64 * K) as timer:
+            for i in range(K):
+                flush.fill_(i & 0xFF)  # evict L2 between timed steps (outside the events)
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+        barrier(ws)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    dev_s = sum(step_ms) / 1e3
+    dev_s_max = max_over_ranks(dev_s, ws, dev)
+
+    # per-kernel live timing (events recorded on the launch stream)
+    per = {}
+    for name, ms in timer.records():
+        per.setdefault(name, []).append(ms)
+    totals = {k: sum(v) for k, v in per.items()}
+    dom = max(totals, key=totals.get)
+    dom_ms = statistics.mean(per[dom])
+    peaks, peak_src = load_peaks()
+    nbytes, flops = kernel_work(w, dom)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": nbytes / (dom_ms * 1e-3) / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / (dom_ms * 1e-3) / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = args.traffic
+    roof.update({"kernel": dom, "kernel_ms": dom_ms, "peak_source": peak_src,
+                 "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
+                 "kernel_share": totals[dom] / sum(totals.values()),
+                 "per_kernel_ms": {k: statistics.mean(v) for k, v in per.items()}})
+    # whole-step roofline (every kernel of fwd + bwd against the op's algorithmic work)
+    a = algorithmic(w)
+    th = w.B * w.T * w.H
+    step_bytes = (a["fwd_bytes"] + a["bwd_bytes"]) * th
+    step_flops = (a["fwd_flops"] + a["bwd_flops"]) * th
+    roof_step_s = max(step_bytes / (peaks["hbm_gbs"] * 1e9), step_flops / (peaks["bf16_tflops"] * 1e12))
+
+    tokens_step = w.B * w.T
+    value = tokens_step * K * ws / dev_s_max
+    ms_step = dev_s_max * 1e3 / K
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(gdn, w, x, wsb, dev, stream, K, args.warmup, ws)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds, 3 * args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "op": ("kda" if w.kda else "gdn") + " fwd+bwd",
+                       "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
+                       "tokens_per_step": tokens_step, "global_batch": w.B * ws,
+                       "parallelism": f"replicas x{ws} (independent sequences)",
+                       "l2": "flushed between timed steps (2 x L2 buffer written outside the events)",
+                       "roofline_step_us": roof_step_s * 1e6,
+                       "step_frac_of_roofline": roof_step_s / (ms_step * 1e-3),
+                       "wall_s": wall},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": timer.launches * ws, "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(gdn, w, x, wsb, dev, stream, K, warmup, ws):
+    """Same step through the public API with pinned host buffers: host-to-device
+    copies of the inputs and device-to-host copies of every result are inside
+    the timed region."""
+    fwd = gdn.kda_fwd if w.kda else gdn.gdn_fwd
+    bwd = gdn.kda_bwd if w.kda else gdn.gdn_bwd
+    names = ["q", "k", "v", "g", "beta", "do"] + (["h0"] if x.h0 is not None else [])
+    host_in = {n: getattr(x, n).cpu().pin_memory() for n in names}
+    dev_in = {n: torch.empty_like(getattr(x, n)) for n in names}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    host_out = None
+
+    def step():
+        nonlocal host_out
+        for n in names:
+            dev_in[n].copy_(host_in[n], non_blocking=True)
+        d = dev_in
+        o, ht = fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0"), chunk=w.chunk)
+        gr = bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0"), d["do"], None,
+                 chunk=w.chunk, workspace=wsb)
+        outs = {"o": o, "ht": ht, **{k: v for k, v in gr.items() if v is not None}}
+        if host_out is None:
+            host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+        for k, v in outs.items():
+            host_out[k].copy_(v, non_blocking=True)
+
+    for _ in range(max(1, warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(K):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    s = max_over_ranks(t0.elapsed_time(t1) / 1e3, ws, dev)
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    return {"value": w.B * w.T * K * ws / s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    rows = max(1, cores // w.H)
+    for i in range(args.warmup):
+        cpu_oracle_run(w, rows, seed=1000 + i)
+    times = []
+    nthreads = cores
+    for i in range(args.steps):
+        dt, nthreads = cpu_oracle_run(w, rows, seed=i)
+        times.append(dt)
+    total = sum(times)
+    value = rows * w.T * args.steps / total
+    sample = (f"each step: {rows} batch rows x {w.H} heads x {w.T} tokens of {w.name} "
+              f"(fp64 token recurrence fwd+bwd on {nthreads} threads)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "op": ("kda" if w.kda else "gdn") + " fwd+bwd",
+                       "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nthreads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gdn_300m")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

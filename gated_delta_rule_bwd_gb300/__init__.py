@@ -1,0 +1,251 @@
+"""GB300 (sm_103a) Gated DeltaNet / Kimi Delta Attention token mixer.
+
+Thin ctypes binding over the C ABI in ``include/gdn.h`` (``libgdn.so``).  The
+functions here only marshal arguments: they check dtypes and devices, allocate
+the outputs and the backward workspace with PyTorch, and pass raw device
+pointers and the current CUDA stream to the library.  Every step of the
+computation runs in the library's CUDA kernels; there is no other path.  If
+the library has not been built, every call raises.
+
+Names follow the ABI: ``gdn_fwd``, ``gdn_bwd``, ``kda_fwd``, ``kda_bwd``.
+Token tensors are ``[B, T, H, D]`` (fp32 or bf16, all the same dtype), ``g``
+is ``[B, T, H]`` (GDN) or ``[B, T, H, dk]`` (KDA) fp32, ``beta`` ``[B, T, H]``
+fp32, states ``[B, H, dk, dv]`` fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgdn.so")
+
+GDN_F32, GDN_BF16 = 0, 1
+_DTYPES = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}
+
+
+class GdnShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
+                ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("chunk", ctypes.c_int),
+                ("dtype", ctypes.c_int)]
+
+
+class GdnError(RuntimeError):
+    pass
+
+
+_lock = threading.Lock()
+_lib = None
+EXPORTS = ("gdn_fwd", "gdn_bwd", "kda_fwd", "kda_bwd", "gdn_bwd_workspace", "kda_bwd_workspace",
+           "gdn_status_str", "gdn_last_cuda_error", "gdn_device_status", "gdn_uses_tensor_cores",
+           "gdn_profile_begin", "gdn_profile_end", "gdn_profile_read", "gdn_kernel_name")
+
+
+def lib():
+    """The loaded ``libgdn.so``; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise GdnError(f"{LIB_PATH} is missing: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, sz, fp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p
+            sp = ctypes.POINTER(GdnShape)
+            for name in ("gdn_bwd_workspace", "kda_bwd_workspace"):
+                getattr(L, name).argtypes = [sp]
+                getattr(L, name).restype = sz
+            for name in ("gdn_fwd", "kda_fwd"):
+                getattr(L, name).argtypes = [sp] + [vp] * 8 + [vp, sz, vp]
+                getattr(L, name).restype = ctypes.c_int
+            for name in ("gdn_bwd", "kda_bwd"):
+                getattr(L, name).argtypes = [sp] + [vp] * 14 + [vp, sz, vp]
+                getattr(L, name).restype = ctypes.c_int
+            L.gdn_status_str.argtypes = [ctypes.c_int]
+            L.gdn_status_str.restype = ctypes.c_char_p
+            L.gdn_last_cuda_error.argtypes = []
+            L.gdn_last_cuda_error.restype = ctypes.c_int
+            L.gdn_device_status.argtypes = []
+            L.gdn_device_status.restype = ctypes.c_int
+            L.gdn_uses_tensor_cores.argtypes = [sp]
+            L.gdn_uses_tensor_cores.restype = ctypes.c_int
+            L.gdn_profile_begin.argtypes = [ctypes.c_int]
+            L.gdn_profile_begin.restype = ctypes.c_int
+            L.gdn_profile_end.argtypes = []
+            L.gdn_profile_end.restype = ctypes.c_int
+            L.gdn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_int),
+                                           ctypes.POINTER(ctypes.c_float), ctypes.c_int]
+            L.gdn_profile_read.restype = ctypes.c_int
+            L.gdn_kernel_name.argtypes = [ctypes.c_int]
+            L.gdn_kernel_name.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def _ptr(x):
+    return None if x is None else ctypes.c_void_p(x.data_ptr())
+
+
+def _check(rc):
+    if rc != 0:
+        L = lib()
+        msg = L.gdn_status_str(rc).decode()
+        if rc == -6:
+            msg += f" (cudaError {L.gdn_last_cuda_error()})"
+        raise GdnError(msg)
+
+
+def make_shape(q, v, chunk) -> GdnShape:
+    B, T, H, dk = q.shape
+    return GdnShape(B, T, H, dk, v.shape[3], chunk, _DTYPES[q.dtype])
+
+
+def _validate(q, k, v, g, beta, kda, extra=()):
+    if q.dtype not in _DTYPES:
+        raise GdnError(f"unsupported dtype {q.dtype}")
+    dev = q.device
+    if dev.type != "cuda":
+        raise GdnError("inputs must be CUDA tensors (the library has no CPU path)")
+    B, T, H, dk = q.shape
+    dv = v.shape[3]
+    want = {"k": (k, (B, T, H, dk), q.dtype), "v": (v, (B, T, H, dv), q.dtype),
+            "g": (g, (B, T, H, dk) if kda else (B, T, H), torch.float32),
+            "beta": (beta, (B, T, H), torch.float32)}
+    for name, (x, shape, dt) in list(want.items()) + list(extra):
+        if x is None:
+            continue
+        if tuple(x.shape) != tuple(shape) or x.dtype != dt or x.device != dev:
+            raise GdnError(f"{name}: expected {tuple(shape)} {dt} on {dev}, got "
+                           f"{tuple(x.shape)} {x.dtype} on {x.device}")
+        if not x.is_contiguous():
+            raise GdnError(f"{name} must be contiguous")
+
+
+def _stream(dev):
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def bwd_workspace_bytes(q, v, chunk=64, kda=False) -> int:
+    L = lib()
+    s = make_shape(q, v, chunk)
+    return int((L.kda_bwd_workspace if kda else L.gdn_bwd_workspace)(ctypes.byref(s)))
+
+
+def uses_tensor_cores(q, v, chunk=64) -> bool:
+    s = make_shape(q, v, chunk)
+    return bool(lib().gdn_uses_tensor_cores(ctypes.byref(s)))
+
+
+def _fwd(kda, q, k, v, g, beta, h0=None, chunk=64, output_final_state=True, out=None):
+    B, T, H, dk = q.shape
+    dv = v.shape[3]
+    _validate(q, k, v, g, beta, kda, [("h0", (h0, (B, H, dk, dv), torch.float32))])
+    o = out if out is not None else torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    ht = (torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+          if output_final_state else None)
+    s = make_shape(q, v, chunk)
+    fn = lib().kda_fwd if kda else lib().gdn_fwd
+    _check(fn(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
+              _ptr(ht), None, 0, _stream(q.device)))
+    return o, ht
+
+
+def _bwd(kda, q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, workspace=None):
+    B, T, H, dk = q.shape
+    dv = v.shape[3]
+    _validate(q, k, v, g, beta, kda, [("h0", (h0, (B, H, dk, dv), torch.float32)),
+                                      ("do", (do, (B, T, H, dv), q.dtype)),
+                                      ("dht", (dht, (B, H, dk, dv), torch.float32))])
+    e = lambda x: torch.empty_like(x)
+    dq, dk_, dv_, dg, dbeta = e(q), e(k), e(v), e(g), e(beta)
+    dh0 = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device) if want_dh0 else None
+    need = bwd_workspace_bytes(q, v, chunk, kda)
+    ws = workspace
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    s = make_shape(q, v, chunk)
+    fn = lib().kda_bwd if kda else lib().gdn_bwd
+    _check(fn(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(do),
+              _ptr(dht), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(dbeta), _ptr(dh0),
+              _ptr(ws), ws.numel(), _stream(q.device)))
+    return {"dq": dq, "dk": dk_, "dv": dv_, "dg": dg, "dbeta": dbeta, "dh0": dh0}
+
+
+def gdn_fwd(q, k, v, g, beta, h0=None, chunk=64, output_final_state=True):
+    """GDN forward.  Returns ``(o, ht)`` (``ht`` None if not requested)."""
+    return _fwd(False, q, k, v, g, beta, h0, chunk, output_final_state)
+
+
+def kda_fwd(q, k, v, g, beta, h0=None, chunk=64, output_final_state=True):
+    """KDA forward (``g`` is ``[B,T,H,dk]``).  Returns ``(o, ht)``."""
+    return _fwd(True, q, k, v, g, beta, h0, chunk, output_final_state)
+
+
+def gdn_bwd(q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, workspace=None):
+    """GDN backward.  Returns a dict ``dq, dk, dv, dg, dbeta, dh0``."""
+    return _bwd(False, q, k, v, g, beta, h0, do, dht, chunk, want_dh0, workspace)
+
+
+def kda_bwd(q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, workspace=None):
+    """KDA backward.  Returns a dict ``dq, dk, dv, dg, dbeta, dh0``."""
+    return _bwd(True, q, k, v, g, beta, h0, do, dht, chunk, want_dh0, workspace)
+
+
+def device_status() -> int:
+    """Reads and clears the device status word (0 = OK, -7 = a wait timed out)."""
+    return int(lib().gdn_device_status())
+
+
+class KernelTimer:
+    """Times every kernel the library launches from this thread with CUDA
+    events recorded on the launch stream (the ABI's gdn_profile_* hook).
+
+    ``with KernelTimer(cap) as t: ...`` then ``t.records()`` gives a list of
+    ``(kernel_name, ms)`` in launch order and ``t.launches`` the launch count."""
+
+    def __init__(self, cap=4096):
+        self.cap = cap
+        self.launches = 0
+
+    def __enter__(self):
+        _check(lib().gdn_profile_begin(self.cap))
+        return self
+
+    def __exit__(self, *exc):
+        self.launches = int(lib().gdn_profile_end())
+        return False
+
+    def records(self):
+        ids = (ctypes.c_int * self.cap)()
+        ms = (ctypes.c_float * self.cap)()
+        n = lib().gdn_profile_read(ids, ms, self.cap)
+        if n < 0:
+            _check(n)
+        return [(lib().gdn_kernel_name(ids[i]).decode(), float(ms[i])) for i in range(n)]
+
+
+class GatedDeltaRule(torch.autograd.Function):
+    """Autograd wrapper: forward via ``gdn_fwd``/``kda_fwd``, backward via
+    ``gdn_bwd``/``kda_bwd`` (inputs are saved; the library recomputes)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, h0, chunk, kda):
+        o, ht = _fwd(kda, q, k, v, g, beta, h0, chunk, True)
+        ctx.save_for_backward(q, k, v, g, beta, h0)
+        ctx.chunk, ctx.kda = chunk, kda
+        return o, ht
+
+    @staticmethod
+    def backward(ctx, do, dht):
+        q, k, v, g, beta, h0 = ctx.saved_tensors
+        gr = _bwd(ctx.kda, q, k, v, g, beta, h0, do.contiguous(),
+                  None if dht is None else dht.contiguous(), ctx.chunk, h0 is not None)
+        return gr["dq"], gr["dk"], gr["dv"], gr["dg"], gr["dbeta"], gr["dh0"], None, None
+
+
+def gated_delta_rule(q, k, v, g, beta, h0=None, chunk=64, kda=False):
+    """Differentiable mixer: returns ``(o, final_state)``."""
+    return GatedDeltaRule.apply(q, k, v, g, beta, h0, chunk, kda)

@@ -1,0 +1,248 @@
+// C ABI of the GDN / KDA mixer: argument checks, kernel selection, launch.
+// The operations, layouts and error rules are stated in include/gdn.h.
+
+#include <vector>
+
+#include "gdn.h"
+#include "gdn_internal.cuh"
+
+namespace {
+
+struct ProfileState {
+  bool on = false;
+  int cap = 0, n = 0, launches = 0;
+  std::vector<cudaEvent_t> ev;  // 2 per recorded launch
+  std::vector<int> ids;
+};
+thread_local ProfileState g_prof;
+
+thread_local int g_last_cuda_error = 0;
+
+int fail_cuda(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  return GDN_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Validates the shape; fills the size fields of a Problem.
+int check_shape(const gdn_shape* s, bool kda, gdn::Problem* p) {
+  if (!s) return GDN_ERR_ARG;
+  if (s->dtype != GDN_F32 && s->dtype != GDN_BF16) return GDN_ERR_DTYPE;
+  if (s->B < 0 || s->T < 0 || s->H < 0) return GDN_ERR_SHAPE;
+  if (s->dk < 1 || s->dk > 128 || s->dv < 1 || s->dv > 128) return GDN_ERR_SHAPE;
+  if (s->chunk != 16 && s->chunk != 32 && s->chunk != 64) return GDN_ERR_SHAPE;
+  *p = gdn::Problem{};
+  p->B = s->B;
+  p->T = s->T;
+  p->H = s->H;
+  p->dk = s->dk;
+  p->dv = s->dv;
+  p->C = s->chunk;
+  p->N = (s->T + s->chunk - 1) / s->chunk;
+  p->kda = kda;
+  p->bf16 = s->dtype == GDN_BF16;
+  return GDN_OK;
+}
+
+bool empty(const gdn::Problem& p) { return p.B == 0 || p.H == 0; }
+
+size_t bwd_ws(const gdn::Problem& p) {
+  if (empty(p) || p.T == 0) return 0;
+  return gdn::tc_supported(p) ? gdn::tc_bwd_workspace(p) : gdn::simt_bwd_workspace(p);
+}
+
+// Zero-length sequences: the final state is the initial one and every
+// gradient of the (empty) token tensors is empty.
+cudaError_t copy_state_or_zero(float* dst, const float* src, const gdn::Problem& p,
+                               cudaStream_t st) {
+  const size_t bytes = (size_t)p.B * p.H * p.dk * p.dv * sizeof(float);
+  if (!dst) return cudaSuccess;
+  if (src) return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st);
+  return cudaMemsetAsync(dst, 0, bytes, st);
+}
+
+int run_fwd(const gdn_shape* shape, bool kda, const void* q, const void* k, const void* v,
+            const float* g, const float* beta, const float* h0, void* o, float* ht, void* ws,
+            size_t ws_bytes, void* stream) {
+  gdn::Problem p;
+  int rc = check_shape(shape, kda, &p);
+  if (rc != GDN_OK) return rc;
+  if (empty(p)) return GDN_OK;
+  // token tensors of an empty sequence hold no data and may be NULL
+  if (p.T > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_ARG;
+  const void* ptrs[] = {q, k, v, g, beta, h0, o, ht};
+  for (const void* x : ptrs)
+    if (x && !aligned16(x)) return GDN_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p.T == 0) {
+    cudaError_t e = copy_state_or_zero(ht, h0, p, st);
+    return e == cudaSuccess ? GDN_OK : fail_cuda(e);
+  }
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.o = o; p.ht = ht;
+  p.ws = ws; p.ws_bytes = ws_bytes;
+  cudaError_t e = gdn::tc_supported(p) ? gdn::tc_fwd(p, st) : gdn::simt_fwd(p, st);
+  return e == cudaSuccess ? GDN_OK : fail_cuda(e);
+}
+
+int run_bwd(const gdn_shape* shape, bool kda, const void* q, const void* k, const void* v,
+            const float* g, const float* beta, const float* h0, const void* do_,
+            const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+            float* dh0, void* ws, size_t ws_bytes, void* stream) {
+  gdn::Problem p;
+  int rc = check_shape(shape, kda, &p);
+  if (rc != GDN_OK) return rc;
+  if (empty(p)) return GDN_OK;
+  if (p.T > 0 && (!q || !k || !v || !g || !beta || !do_ || !dq || !dk || !dv || !dg || !dbeta))
+    return GDN_ERR_ARG;
+  const void* ptrs[] = {q, k, v, g, beta, h0, do_, dht, dq, dk, dv, dg, dbeta, dh0, ws};
+  for (const void* x : ptrs)
+    if (x && !aligned16(x)) return GDN_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p.T == 0) {
+    cudaError_t e = copy_state_or_zero(dh0, dht, p, st);
+    return e == cudaSuccess ? GDN_OK : fail_cuda(e);
+  }
+  const size_t need = bwd_ws(p);
+  if (need > 0 && (!ws || ws_bytes < need)) return GDN_ERR_WORKSPACE;
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.do_ = do_; p.dht = dht;
+  p.dq = dq; p.dk_ = dk; p.dv_ = dv; p.dg = dg; p.dbeta = dbeta; p.dh0 = dh0;
+  p.ws = ws; p.ws_bytes = ws_bytes;
+  cudaError_t e = gdn::tc_supported(p) ? gdn::tc_bwd(p, st) : gdn::simt_bwd(p, st);
+  return e == cudaSuccess ? GDN_OK : fail_cuda(e);
+}
+
+size_t query_ws(const gdn_shape* shape, bool kda) {
+  gdn::Problem p;
+  if (check_shape(shape, kda, &p) != GDN_OK) return 0;
+  return bwd_ws(p);
+}
+
+}  // namespace
+
+namespace gdn {
+
+const char* kernel_name(int id) {
+  static const char* names[kNumKernelIds] = {
+      "simt_fwd", "simt_states", "simt_bwd", "simt_bwd_reduce",
+      "tc_fwd", "tc_states", "tc_bwd", "tc_bwd_reduce"};
+  return (id >= 0 && id < kNumKernelIds) ? names[id] : "unknown";
+}
+
+void prof_before(cudaStream_t s) {
+  ProfileState& P = g_prof;
+  if (P.on && P.n < P.cap) cudaEventRecord(P.ev[2 * P.n], s);
+}
+
+void prof_after(cudaStream_t s, int kernel_id) {
+  ProfileState& P = g_prof;
+  if (!P.on) return;
+  if (P.n < P.cap) {
+    cudaEventRecord(P.ev[2 * P.n + 1], s);
+    P.ids[P.n] = kernel_id;
+    ++P.n;
+  }
+  ++P.launches;
+}
+
+}  // namespace gdn
+
+extern "C" {
+
+int gdn_profile_begin(int cap) {
+  ProfileState& P = g_prof;
+  if (cap < 0) return GDN_ERR_ARG;
+  while ((int)P.ev.size() < 2 * cap) {
+    cudaEvent_t e;
+    cudaError_t err = cudaEventCreate(&e);
+    if (err != cudaSuccess) return fail_cuda(err);
+    P.ev.push_back(e);
+  }
+  P.ids.assign(cap, -1);
+  P.cap = cap;
+  P.n = 0;
+  P.launches = 0;
+  P.on = true;
+  return GDN_OK;
+}
+
+int gdn_profile_end(void) {
+  g_prof.on = false;
+  return g_prof.launches;
+}
+
+int gdn_profile_read(int* kernel_ids, float* ms, int max) {
+  ProfileState& P = g_prof;
+  const int n = P.n < max ? P.n : max;
+  for (int i = 0; i < n; ++i) {
+    cudaError_t e = cudaEventSynchronize(P.ev[2 * i + 1]);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms[i], P.ev[2 * i], P.ev[2 * i + 1]);
+    if (e != cudaSuccess) return fail_cuda(e);
+    kernel_ids[i] = P.ids[i];
+  }
+  return n;
+}
+
+const char* gdn_kernel_name(int kernel_id) { return gdn::kernel_name(kernel_id); }
+
+size_t gdn_bwd_workspace(const gdn_shape* shape) { return query_ws(shape, false); }
+size_t kda_bwd_workspace(const gdn_shape* shape) { return query_ws(shape, true); }
+
+int gdn_fwd(const gdn_shape* shape, const void* q, const void* k, const void* v, const float* g,
+            const float* beta, const float* h0, void* o, float* ht, void* ws, size_t ws_bytes,
+            void* stream) {
+  return run_fwd(shape, false, q, k, v, g, beta, h0, o, ht, ws, ws_bytes, stream);
+}
+
+int kda_fwd(const gdn_shape* shape, const void* q, const void* k, const void* v, const float* g,
+            const float* beta, const float* h0, void* o, float* ht, void* ws, size_t ws_bytes,
+            void* stream) {
+  return run_fwd(shape, true, q, k, v, g, beta, h0, o, ht, ws, ws_bytes, stream);
+}
+
+int gdn_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v, const float* g,
+            const float* beta, const float* h0, const void* do_, const float* dht, void* dq,
+            void* dk, void* dv, float* dg, float* dbeta, float* dh0, void* ws, size_t ws_bytes,
+            void* stream) {
+  return run_bwd(shape, false, q, k, v, g, beta, h0, do_, dht, dq, dk, dv, dg, dbeta, dh0, ws,
+                 ws_bytes, stream);
+}
+
+int kda_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v, const float* g,
+            const float* beta, const float* h0, const void* do_, const float* dht, void* dq,
+            void* dk, void* dv, float* dg, float* dbeta, float* dh0, void* ws, size_t ws_bytes,
+            void* stream) {
+  return run_bwd(shape, true, q, k, v, g, beta, h0, do_, dht, dq, dk, dv, dg, dbeta, dh0, ws,
+                 ws_bytes, stream);
+}
+
+const char* gdn_status_str(int status) {
+  switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_ARG: return "GDN_ERR_ARG: a required pointer is NULL";
+    case GDN_ERR_SHAPE: return "GDN_ERR_SHAPE: invalid B/T/H, head dimension or chunk size";
+    case GDN_ERR_DTYPE: return "GDN_ERR_DTYPE: dtype must be GDN_F32 or GDN_BF16";
+    case GDN_ERR_ALIGN: return "GDN_ERR_ALIGN: pointers must be 16-byte aligned";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing or too small";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA call failed (see gdn_last_cuda_error)";
+    case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT: a device-side wait ran out";
+    default: return "unknown gdn_status";
+  }
+}
+
+int gdn_last_cuda_error(void) { return g_last_cuda_error; }
+
+int gdn_device_status(void) {
+  int status = GDN_OK;
+  cudaError_t e = gdn::read_and_clear_device_status(&status);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return status;
+}
+
+int gdn_uses_tensor_cores(const gdn_shape* shape) {
+  gdn::Problem p;
+  if (check_shape(shape, false, &p) != GDN_OK) return 0;
+  return gdn::tc_supported(p) ? 1 : 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// Internal declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+// Everything one launch of the mixer needs.  Token tensors are [B,T,H,D],
+// states [B,H,dk,dv]; see include/gdn.h.
+struct Problem {
+  int B, T, H, dk, dv, C, N;  // N = ceil(T / C) chunks per sequence
+  bool kda, bf16;
+  const void *q, *k, *v, *do_;
+  const float *g, *beta, *h0, *dht;
+  void *o, *dq, *dk_, *dv_;
+  float *ht, *dg, *dbeta, *dh0;
+  void* ws;
+  size_t ws_bytes;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// CUDA-core fp32 kernels (any dk, dv <= 128; chunk 16/32/64).
+size_t simt_bwd_workspace(const Problem& p);
+cudaError_t simt_fwd(const Problem& p, cudaStream_t s);
+cudaError_t simt_bwd(const Problem& p, cudaStream_t s);
+
+// Tensor-core kernels (bf16, dk = dv = 128, chunk = 64).
+bool tc_supported(const Problem& p);
+size_t tc_bwd_workspace(const Problem& p);
+cudaError_t tc_fwd(const Problem& p, cudaStream_t s);
+cudaError_t tc_bwd(const Problem& p, cudaStream_t s);
+
+// Kernel ids reported by the timing hook (gdn_profile_*).
+enum KernelId {
+  kSimtFwd = 0,
+  kSimtStates = 1,
+  kSimtBwd = 2,
+  kSimtBwdReduce = 3,
+  kTcFwd = 4,
+  kTcStates = 5,
+  kTcBwd = 6,
+  kTcBwdReduce = 7,
+  kNumKernelIds = 8
+};
+const char* kernel_name(int id);
+
+// Called around every kernel launch of the library (no-ops unless the calling
+// thread enabled the timing hook).
+void prof_before(cudaStream_t s);
+void prof_after(cudaStream_t s, int kernel_id);
+
+// Per-device status word written by bounded device-side waits.
+cudaError_t read_and_clear_device_status(int* status);
+
+}  // namespace gdn

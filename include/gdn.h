@@ -1,0 +1,154 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) Gated DeltaNet / Kimi Delta Attention
+ * token mixer, forward and backward.
+ *
+ * The operation.  The Primus hybrid-LLM pretraining blog (MI355X), section
+ * "How hybrid models are defined in Primus", names the two linear-recurrent
+ * mixers built here: Gated DeltaNet (GDN), which adds the delta rule -- the
+ * state rewrites the value stored under the current key rather than only
+ * accumulating -- to a state with one scalar forget gate per head, and Kimi
+ * Delta Attention (KDA), which refines that gate to one value per key
+ * dimension.  Per batch row b and head h, over tokens t, with the state kept
+ * as H (dk x dv, fp32; H = S^T of the usual S_t = a_t S_{t-1}(I - b_t k_t
+ * k_t^T) + b_t v_t k_t^T, o_t = S_t q_t):
+ *
+ *   GDN:  H_t = exp(g_t) (I - beta_t k_t k_t^T) H_{t-1} + beta_t k_t v_t^T
+ *   KDA:  H_t = (I - beta_t k_t k_t^T) diag(exp(g_t)) H_{t-1} + beta_t k_t v_t^T
+ *   o_t = H_t^T q_t,   H_{-1} = initial state (or 0),   final state = H_{T-1}.
+ *
+ * The backward entry points return the gradients of a scalar loss with
+ * respect to q, k, v, g, beta and the initial state, given dL/do and
+ * (optionally) dL/d(final state).  They take the forward inputs again and
+ * recompute what they need; no context is saved between calls.
+ *
+ * Layout (all row-major, innermost dimension contiguous):
+ *   q, k, dq, dk          [B, T, H, dk]   dtype per gdn_shape.dtype
+ *   v, o, do_, dv         [B, T, H, dv]   dtype per gdn_shape.dtype
+ *   g, dg (GDN)           [B, T, H]       fp32, log forget gate (a = exp(g))
+ *   g, dg (KDA)           [B, T, H, dk]   fp32
+ *   beta, dbeta           [B, T, H]       fp32, used as given
+ *   h0, ht, dht, dh0      [B, H, dk, dv]  fp32
+ * No query scale and no normalisation is applied inside: gradients are with
+ * respect to the tensors passed.
+ *
+ * Memory and streams.  Every pointer is a device pointer owned by the
+ * caller and must be 16-byte aligned.  The library allocates nothing: the
+ * backward pass needs a caller-provided device workspace of at least
+ * *_bwd_workspace() bytes (the forward pass needs none; pass NULL/0).  All
+ * work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ * stream); the calls do not synchronise.  Outputs are overwritten, never
+ * accumulated.  Results are deterministic (no atomics).
+ *
+ * Errors.  Arguments are validated on the host before anything is launched;
+ * a failed check returns a negative gdn_status and launches nothing.  A
+ * launch failure returns GDN_ERR_CUDA; gdn_last_cuda_error() then gives the
+ * cudaError_t value.  Device-side waits are bounded: a wait that runs out
+ * records GDN_ERR_DEVICE_TIMEOUT in a per-device status word that
+ * gdn_device_status() reads (and clears).
+ *
+ * Kernel selection.  dtype BF16 with dk = dv = 128 and chunk = 64 runs the
+ * tensor-core (tcgen05/TMEM, TMA-fed) kernels; every other valid shape runs
+ * the CUDA-core fp32 kernels (chunk in {16, 32, 64}, 1 <= dk, dv <= 128).
+ * T need not be a multiple of chunk.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_ARG = -1,            /* NULL required pointer, bad enum value        */
+  GDN_ERR_SHAPE = -2,          /* B,T,H < 0, dk/dv outside [1,128], bad chunk  */
+  GDN_ERR_DTYPE = -3,          /* dtype not GDN_F32 / GDN_BF16                 */
+  GDN_ERR_ALIGN = -4,          /* a pointer is not 16-byte aligned             */
+  GDN_ERR_WORKSPACE = -5,      /* workspace NULL or smaller than required      */
+  GDN_ERR_CUDA = -6,           /* a CUDA call failed; see gdn_last_cuda_error  */
+  GDN_ERR_DEVICE_TIMEOUT = -7  /* a bounded device-side wait ran out           */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* Problem shape.  dtype is the element type of q, k, v, o, do_, dq, dk, dv. */
+typedef struct {
+  int B, T, H;  /* batch, tokens per sequence, heads; each >= 0 (0 = no work) */
+  int dk, dv;   /* key / value head dimension, 1..128                         */
+  int chunk;    /* tokens per chunk of the chunkwise algorithm: 16, 32 or 64  */
+  int dtype;    /* gdn_dtype                                                  */
+} gdn_shape;
+
+/* With T = 0 the token pointers may be NULL: the forward pass copies h0 to ht
+ * (or zeroes ht), the backward pass copies dht to dh0 (or zeroes dh0).
+ *
+ * Workspace bytes the backward entry points need for this shape (0 if the
+ * shape is invalid).  The forward entry points need none. */
+GDN_API size_t gdn_bwd_workspace(const gdn_shape* shape);
+GDN_API size_t kda_bwd_workspace(const gdn_shape* shape);
+
+/* GDN forward: o (and ht if non-NULL) from q, k, v, g [B,T,H], beta and h0
+ * (NULL = zero initial state).  ws/ws_bytes are unused (may be NULL/0). */
+GDN_API int gdn_fwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
+            const float* g, const float* beta, const float* h0, void* o, float* ht,
+            void* ws, size_t ws_bytes, void* stream);
+
+/* GDN backward: gradients with respect to every forward input.  dht may be
+ * NULL (zero gradient of the final state); dh0 may be NULL (not wanted). */
+GDN_API int gdn_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
+            const float* g, const float* beta, const float* h0, const void* do_,
+            const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+            float* dh0, void* ws, size_t ws_bytes, void* stream);
+
+/* KDA forward / backward: as GDN, with g and dg of shape [B,T,H,dk]. */
+GDN_API int kda_fwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
+            const float* g, const float* beta, const float* h0, void* o, float* ht,
+            void* ws, size_t ws_bytes, void* stream);
+
+GDN_API int kda_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
+            const float* g, const float* beta, const float* h0, const void* do_,
+            const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+            float* dh0, void* ws, size_t ws_bytes, void* stream);
+
+/* Human-readable name of a gdn_status value. */
+GDN_API const char* gdn_status_str(int status);
+
+/* cudaError_t of the most recent GDN_ERR_CUDA on the calling thread. */
+GDN_API int gdn_last_cuda_error(void);
+
+/* Reads and clears the device status word of the current device: GDN_OK or
+ * GDN_ERR_DEVICE_TIMEOUT.  Synchronises the current device.  Returns
+ * GDN_ERR_CUDA if the read itself fails. */
+GDN_API int gdn_device_status(void);
+
+/* 1 if the tensor-core kernels would run for this shape, else 0. */
+GDN_API int gdn_uses_tensor_cores(const gdn_shape* shape);
+
+/* Per-kernel timing without a profiler (calling thread only).
+ * gdn_profile_begin(cap) starts recording: every kernel the library launches
+ * from this thread is bracketed by a pair of CUDA events recorded on the
+ * launch stream, for the first `cap` launches (the library creates the events
+ * once and keeps them; it allocates no device memory).  gdn_profile_end()
+ * stops recording and returns the number of launches seen since begin (also
+ * those beyond cap).  gdn_profile_read() waits for the recorded events and
+ * writes, for each recorded launch in order, its kernel id and its duration
+ * in ms; it returns the number written (<= max).  gdn_kernel_name() names a
+ * kernel id.  Returns GDN_ERR_CUDA if an event call fails. */
+GDN_API int gdn_profile_begin(int cap);
+GDN_API int gdn_profile_end(void);
+GDN_API int gdn_profile_read(int* kernel_ids, float* ms, int max);
+GDN_API const char* gdn_kernel_name(int kernel_id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

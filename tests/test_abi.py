@@ -1,0 +1,129 @@
+"""C-ABI library: loads, exports every declared symbol, validates on the host.
+
+These run without a GPU: every call here returns from host-side argument
+validation before anything is enqueued (or has no work: B = 0).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_delta_rule_bwd_gb300 as gdn
+from gated_delta_rule_bwd_gb300 import build as gbuild
+
+HEADER = os.path.join(gbuild.INCLUDE, "gdn.h")
+
+GDN_OK, GDN_ERR_ARG, GDN_ERR_SHAPE, GDN_ERR_DTYPE, GDN_ERR_ALIGN, GDN_ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
+
+
+@pytest.fixture(scope="module")
+def L():
+    gbuild.build()
+    return gdn.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"GDN_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_abi():
+    names = set(declared_symbols())
+    assert {"gdn_fwd", "gdn_bwd", "kda_fwd", "kda_bwd", "gdn_bwd_workspace",
+            "kda_bwd_workspace", "gdn_status_str"} <= names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+
+
+def test_only_the_abi_is_exported(L):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", gdn.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert exported == set(declared_symbols())
+
+
+def shape(B=1, T=64, H=2, dk=16, dv=16, chunk=16, dtype=0):
+    return gdn.GdnShape(B, T, H, dk, dv, chunk, dtype)
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails or B = 0 first
+
+
+def call_fwd(L, s, kda=False, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, h0=None, o=FAKE, ht=None)
+    args.update(over)
+    fn = L.kda_fwd if kda else L.gdn_fwd
+    return fn(ctypes.byref(s), args["q"], args["k"], args["v"], args["g"], args["beta"],
+              args["h0"], args["o"], args["ht"], None, 0, None)
+
+
+def call_bwd(L, s, ws=None, ws_bytes=0, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, h0=None, do=FAKE, dht=None, dq=FAKE,
+             dk=FAKE, dv=FAKE, dg=FAKE, dbeta=FAKE, dh0=None)
+    a.update(over)
+    return L.gdn_bwd(ctypes.byref(s), a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], a["do"],
+                     a["dht"], a["dq"], a["dk"], a["dv"], a["dg"], a["dbeta"], a["dh0"], ws,
+                     ws_bytes, None)
+
+
+def test_shape_validation(L):
+    assert call_fwd(L, shape(chunk=17)) == GDN_ERR_SHAPE
+    assert call_fwd(L, shape(chunk=128)) == GDN_ERR_SHAPE
+    assert call_fwd(L, shape(dk=0)) == GDN_ERR_SHAPE
+    assert call_fwd(L, shape(dv=129)) == GDN_ERR_SHAPE
+    assert call_fwd(L, shape(T=-1)) == GDN_ERR_SHAPE
+    assert call_fwd(L, shape(dtype=7)) == GDN_ERR_DTYPE
+    assert L.gdn_fwd(None, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, None, 0, None) == GDN_ERR_ARG
+
+
+def test_null_and_alignment_checks(L):
+    assert call_fwd(L, shape(), q=None) == GDN_ERR_ARG
+    assert call_fwd(L, shape(), o=None) == GDN_ERR_ARG
+    assert call_fwd(L, shape(), kda=True, beta=None) == GDN_ERR_ARG
+    assert call_fwd(L, shape(), v=ctypes.c_void_p(0x10008)) == GDN_ERR_ALIGN
+    assert call_bwd(L, shape(), dg=ctypes.c_void_p(0x10004)) == GDN_ERR_ALIGN
+    assert call_bwd(L, shape(), do=None) == GDN_ERR_ARG
+
+
+def test_workspace_query_and_check(L):
+    s = shape()
+    need = L.gdn_bwd_workspace(ctypes.byref(s))
+    assert need > 0
+    assert L.gdn_bwd_workspace(ctypes.byref(shape(chunk=3))) == 0
+    assert call_bwd(L, s) == GDN_ERR_WORKSPACE
+    assert call_bwd(L, s, ws=FAKE, ws_bytes=need - 1) == GDN_ERR_WORKSPACE
+    # states of the recompute pass: B*H*N*dk*dv fp32 at least
+    big = shape(B=2, T=2048, H=4, dk=128, dv=128, chunk=64, dtype=1)
+    assert L.gdn_bwd_workspace(ctypes.byref(big)) >= 2 * 4 * 32 * 128 * 128 * 4
+    assert L.kda_bwd_workspace(ctypes.byref(big)) >= L.gdn_bwd_workspace(ctypes.byref(big))
+
+
+def test_empty_batch_is_a_no_op(L):
+    assert call_fwd(L, shape(B=0)) == GDN_OK
+    assert call_fwd(L, shape(H=0), q=None) == GDN_OK
+    assert call_bwd(L, shape(B=0)) == GDN_OK
+
+
+def test_status_strings(L):
+    for code in range(-7, 1):
+        assert L.gdn_status_str(code).startswith(b"GDN_")
+    assert b"unknown" in L.gdn_status_str(5)
+
+
+def test_tensor_core_selection_rule(L):
+    # only bf16, dk = dv = 128, chunk 64 may take the tensor-core kernels
+    for s in (shape(dtype=0, dk=128, dv=128, chunk=64), shape(dtype=1, dk=64, dv=128, chunk=64),
+              shape(dtype=1, dk=128, dv=128, chunk=32)):
+        assert L.gdn_uses_tensor_cores(ctypes.byref(s)) == 0
+
+
+def test_binding_refuses_cpu_tensors(L):
+    import torch
+    x = torch.zeros(1, 4, 1, 16)
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_fwd(x, x, x, torch.zeros(1, 4, 1), torch.zeros(1, 4, 1), chunk=16)

@@ -1,0 +1,214 @@
+"""GPU kernels against the fp64 oracle, element by element, through the C ABI.
+
+Tolerances (per output tensor: o, final state, dq, dk, dv, dg, dbeta, dh0):
+* fp32 inputs: relative L2 error <= 1e-5 and max |x - ref| <= 1e-4 * rms(ref);
+* bf16 inputs (fp32 state and accumulation): relative L2 error <= 2e-2.
+The oracle sees exactly the bytes the GPU sees (bf16 values upcast to fp64).
+Full-size workloads are checked on sampled (b, h) sequences, which are
+independent problems the oracle solves one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_bwd_gb300 as gdn
+import oracle
+from gated_delta_rule_bwd_gb300 import workloads as W
+from gated_delta_rule_bwd_gb300.inputs import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+FP32_REL, FP32_MAXABS, BF16_REL = 1e-5, 1e-4, 2e-2
+
+
+def rel_l2(x, ref):
+    ref = np.asarray(ref, dtype=np.float64)
+    x = np.asarray(x, dtype=np.float64)
+    den = np.linalg.norm(ref)
+    return np.linalg.norm(x - ref) / den if den > 0 else np.linalg.norm(x)
+
+
+def check(name, got, ref, fp32):
+    got = got.detach().double().cpu().numpy() if torch.is_tensor(got) else got
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    r = rel_l2(got, ref)
+    if fp32:
+        rms = np.sqrt(np.mean(np.square(ref))) if ref.size else 0.0
+        m = np.max(np.abs(got - ref)) if ref.size else 0.0
+        assert r <= FP32_REL, f"{name}: rel-L2 {r:.3e} > {FP32_REL}"
+        assert m <= FP32_MAXABS * rms, f"{name}: max-abs {m:.3e} > {FP32_MAXABS} * rms {rms:.3e}"
+    else:
+        assert r <= BF16_REL, f"{name}: rel-L2 {r:.3e} > {BF16_REL}"
+    return r
+
+
+def run_gpu(x, chunk, fwd_only=False):
+    d = x.to("cuda")
+    fwd = gdn.kda_fwd if x.kda else gdn.gdn_fwd
+    bwd = gdn.kda_bwd if x.kda else gdn.gdn_bwd
+    o, ht = fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, chunk=chunk)
+    gr = None
+    if not fwd_only:
+        gr = bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, d.dht, chunk=chunk)
+    torch.cuda.synchronize()
+    return o, ht, gr
+
+
+def compare(x, o, ht, gr, fp32, pairs=None):
+    """Compare GPU results for the sequences in ``pairs`` (default: all)."""
+    if pairs is not None:
+        sub = x.select(pairs)
+        pick_tok = lambda t: torch.stack([t[b, :, h] for b, h in pairs], 0).unsqueeze(2)
+        pick_st = lambda t: torch.stack([t[b, h] for b, h in pairs], 0).unsqueeze(1)
+    else:
+        sub = x
+        pick_tok = pick_st = lambda t: t
+    o_ref, ht_ref = oracle.fwd(sub.q, sub.k, sub.v, sub.g, sub.beta, sub.h0, kda=x.kda)
+    errs = {"o": check("o", pick_tok(o.cpu()), o_ref, fp32),
+            "ht": check("ht", pick_st(ht.cpu()), ht_ref, fp32)}
+    if gr is not None:
+        ref = oracle.bwd(sub.q, sub.k, sub.v, sub.g, sub.beta, sub.h0, sub.do, sub.dht, kda=x.kda)
+        for n in ("dq", "dk", "dv", "dg", "dbeta"):
+            errs[n] = check(n, pick_tok(gr[n].cpu()), ref[n], fp32)
+        errs["dh0"] = check("dh0", pick_st(gr["dh0"].cpu()), ref["dh0"], fp32)
+    return errs
+
+
+# ----------------------------------------------------------- small cases, every output
+
+SMALL = [
+    # B, T, H, dk, dv, chunk, dtype, kda, h0, dht
+    (1, 64, 2, 16, 16, 16, "f32", False, False, False),   # the tiny fp32 workload
+    (1, 64, 2, 16, 16, 16, "f32", True, False, False),
+    (2, 100, 3, 32, 48, 32, "f32", False, True, True),     # ragged tail, dk != dv
+    (2, 100, 3, 32, 48, 16, "f32", True, True, True),
+    (1, 37, 2, 24, 40, 64, "f32", False, True, True),      # T < chunk, odd sizes
+    (1, 1, 1, 8, 8, 16, "f32", True, True, True),          # one token
+    (2, 200, 2, 64, 64, 64, "bf16", False, True, True),
+    (2, 200, 2, 64, 64, 64, "bf16", True, True, True),
+    (1, 300, 2, 128, 128, 64, "f32", False, True, True),   # full head dims on CUDA cores
+    (1, 300, 2, 128, 128, 64, "f32", True, True, True),
+    (2, 192, 2, 128, 128, 32, "bf16", False, True, False),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "x".join(map(str, c)))
+def test_small_cases_match_oracle(case):
+    B, T, H, dk, dv, chunk, dtype, kda, h0, dht = case
+    x = make_inputs(B, T, H, dk, dv, kda=kda, dtype=dtype, h0_std=0.3 if h0 else None,
+                    with_dht=dht, seed=1)
+    o, ht, gr = run_gpu(x, chunk)
+    compare(x, o, ht, gr, fp32=dtype == "f32")
+
+
+def test_tiny_fp32_workload():
+    w = W.GDN_TINY_FP32
+    x = w.make()
+    o, ht, gr = run_gpu(x, w.chunk)
+    compare(x, o, ht, gr, fp32=True)
+
+
+@pytest.mark.parametrize("w", [W.GDN_300M_BF16, W.KDA_300M_BF16, W.GDN_1B_BF16_H0],
+                         ids=lambda w: w.name)
+def test_training_workloads_sampled(w):
+    x = w.make()
+    o, ht, gr = run_gpu(x, w.chunk)
+    rng = np.random.default_rng(0)
+    pairs = [(0, 0), (w.B - 1, w.H - 1)] + [(int(rng.integers(w.B)), int(rng.integers(w.H)))
+                                              for _ in range(2)]
+    compare(x, o, ht, gr, fp32=False, pairs=pairs)
+
+
+def test_long_context_forward_sampled():
+    """1M-token forward: final state and outputs of two heads vs the oracle."""
+    w = W.GDN_1M_FWD_BF16
+    x = w.make(device="cuda")
+    fwd = gdn.gdn_fwd
+    o, ht = fwd(x.q, x.k, x.v, x.g, x.beta, x.h0, chunk=w.chunk)
+    torch.cuda.synchronize()
+    heads = [0, w.H - 1]
+    pairs = [(0, h) for h in heads]
+    sub = x.select(pairs).to("cpu")
+    o_ref, ht_ref = oracle.fwd(sub.q, sub.k, sub.v, sub.g, sub.beta, None)
+    got_o = torch.stack([o[0, :, h] for h in heads], 0).unsqueeze(2).cpu()
+    got_ht = torch.stack([ht[0, h] for h in heads], 0).unsqueeze(1).cpu()
+    check("ht", got_ht, ht_ref, fp32=False)
+    check("o", got_o, o_ref, fp32=False)
+
+
+# ----------------------------------------------------------- invariants on the GPU
+
+def test_kda_with_broadcast_gate_equals_gdn():
+    x = make_inputs(2, 130, 2, 128, 128, dtype="bf16", h0_std=0.1, with_dht=True, seed=3)
+    d = x.to("cuda")
+    gk = d.g[..., None].expand(*d.g.shape, 128).contiguous()
+    o1, h1 = gdn.gdn_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0)
+    o2, h2 = gdn.kda_fwd(d.q, d.k, d.v, gk, d.beta, d.h0)
+    g1 = gdn.gdn_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, d.dht)
+    g2 = gdn.kda_bwd(d.q, d.k, d.v, gk, d.beta, d.h0, d.do, d.dht)
+    assert rel_l2(o2.float().cpu(), o1.float().cpu()) < 1e-2
+    assert rel_l2(h2.cpu(), h1.cpu()) < 1e-3
+    for n in ("dq", "dk", "dv", "dbeta", "dh0"):
+        assert rel_l2(g2[n].float().cpu(), g1[n].float().cpu()) < 1e-2, n
+    assert rel_l2(g2["dg"].sum(-1).cpu(), g1["dg"].cpu()) < 1e-2
+
+
+@pytest.mark.parametrize("kda", [False, True])
+def test_split_sequence_hands_over_state(kda):
+    T, tau = 256, 128
+    x = make_inputs(2, T, 2, 128, 128, kda=kda, dtype="bf16", h0_std=0.1, with_dht=True, seed=4)
+    d = x.to("cuda")
+    fwd = gdn.kda_fwd if kda else gdn.gdn_fwd
+    bwd = gdn.kda_bwd if kda else gdn.gdn_bwd
+    sl = lambda t, a, b: t[:, a:b].contiguous()
+    o, ht = fwd(d.q, d.k, d.v, d.g, d.beta, d.h0)
+    oa, ha = fwd(*(sl(t, 0, tau) for t in (d.q, d.k, d.v, d.g, d.beta)), d.h0)
+    ob, hb = fwd(*(sl(t, tau, T) for t in (d.q, d.k, d.v, d.g, d.beta)), ha)
+    assert rel_l2(torch.cat([oa, ob], 1).float().cpu(), o.float().cpu()) < 1e-2
+    assert rel_l2(hb.cpu(), ht.cpu()) < 1e-3
+    full = bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, d.dht)
+    gb = bwd(*(sl(t, tau, T) for t in (d.q, d.k, d.v, d.g, d.beta)), ha, sl(d.do, tau, T), d.dht)
+    ga = bwd(*(sl(t, 0, tau) for t in (d.q, d.k, d.v, d.g, d.beta)), d.h0, sl(d.do, 0, tau),
+             gb["dh0"])
+    for n in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert rel_l2(torch.cat([ga[n], gb[n]], 1).float().cpu(), full[n].float().cpu()) < 1e-2, n
+    assert rel_l2(ga["dh0"].cpu(), full["dh0"].cpu()) < 1e-2
+
+
+@pytest.mark.parametrize("kda", [False, True])
+def test_results_are_deterministic(kda):
+    x = make_inputs(2, 200, 2, 128, 128, kda=kda, dtype="bf16", h0_std=0.1, with_dht=True, seed=5)
+    r1 = run_gpu(x, 64)
+    r2 = run_gpu(x, 64)
+    assert torch.equal(r1[0], r2[0]) and torch.equal(r1[1], r2[1])
+    for n in r1[2]:
+        assert torch.equal(r1[2][n], r2[2][n]), n
+
+
+def test_beta_zero_gives_pure_decay_on_gpu():
+    x = make_inputs(1, 96, 2, 128, 128, dtype="bf16", h0_std=0.5, seed=6)
+    x.beta.zero_()
+    d = x.to("cuda")
+    o, ht = gdn.gdn_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0)
+    gam = torch.cumsum(x.g.double(), 1)                       # [B,T,H]
+    ht_ref = torch.exp(gam[:, -1])[..., None, None] * x.h0.double()
+    assert rel_l2(ht.cpu(), ht_ref) < 1e-5
+
+
+def test_empty_sequence_copies_state():
+    x = make_inputs(2, 0, 2, 16, 16, dtype="f32", h0_std=1.0, with_dht=True, seed=7)
+    d = x.to("cuda")
+    o, ht = gdn.gdn_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, chunk=16)
+    gr = gdn.gdn_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, d.dht, chunk=16)
+    torch.cuda.synchronize()
+    assert o.shape[1] == 0
+    assert torch.equal(ht, d.h0) and torch.equal(gr["dh0"], d.dht)
+
+
+def test_autograd_wrapper_matches_direct_calls():
+    x = make_inputs(1, 128, 2, 128, 128, dtype="bf16", h0_std=0.1, seed=8).to("cuda")
+    q, k, v = (t.clone().requires_grad_() for t in (x.q, x.k, x.v))
+    o, ht = gdn.gated_delta_rule(q, k, v, x.g, x.beta, x.h0)
+    (o.float() * x.do.float()).sum().backward()
+    ref = gdn.gdn_bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do)
+    assert torch.equal(q.grad, ref["dq"]) and torch.equal(v.grad, ref["dv"])
