@@ -90,6 +90,34 @@ def kernel_work(w, kernel):
     return 0.0, 0.0
 
 
+KERNEL_SOURCES = {"tc": "gdn_tc.cu", "simt": "gdn_simt.cu"}
+
+
+def recorded_traffic(kernel, workload_key):
+    """DRAM bytes per launch of ``kernel`` from the committed ncu summary
+    ``profiles/<kernel>_<workload_key>_*.md``, or None when there is none or
+    when the kernel source has changed since it was captured."""
+    import glob
+    import hashlib
+    files = glob.glob(os.path.join(ROOT, "profiles", f"{kernel}_{workload_key}*.md"))
+    if not files:
+        return None
+    fields = {}
+    for line in open(files[0]):
+        if ":" in line and not line.startswith(("|", "#", " ")):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip().split()[0] if v.strip() else ""
+    src = os.path.join(ROOT, "gated_delta_rule_bwd_gb300", "csrc",
+                       KERNEL_SOURCES.get(kernel.split("_")[0], ""))
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if sha != fields.get("kernel_source_sha256_16"):
+            return None
+        return float(fields["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -287,7 +315,8 @@ def run_ours(args):
         roof = {"bound": "tensor", "achieved": flops / (dom_ms * 1e-3) / 1e12,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = args.traffic
+    wkey = next((k for k, v in WORKLOADS.items() if v is w), w.name)
+    roof["traffic"] = args.traffic if args.traffic is not None else recorded_traffic(dom, wkey)
     roof.update({"kernel": dom, "kernel_ms": dom_ms, "peak_source": peak_src,
                  "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
                  "kernel_share": totals[dom] / sum(totals.values()),

@@ -97,10 +97,13 @@ def test_workspace_query_and_check(L):
     assert L.gdn_bwd_workspace(ctypes.byref(shape(chunk=3))) == 0
     assert call_bwd(L, s) == GDN_ERR_WORKSPACE
     assert call_bwd(L, s, ws=FAKE, ws_bytes=need - 1) == GDN_ERR_WORKSPACE
-    # states of the recompute pass: B*H*N*dk*dv fp32 at least
+    # chunk-entry states of the recompute pass: B*H*N*dk*dv values at least
+    # (bf16 on the tensor-core path, fp32 on the CUDA-core path)
     big = shape(B=2, T=2048, H=4, dk=128, dv=128, chunk=64, dtype=1)
-    assert L.gdn_bwd_workspace(ctypes.byref(big)) >= 2 * 4 * 32 * 128 * 128 * 4
-    assert L.kda_bwd_workspace(ctypes.byref(big)) >= L.gdn_bwd_workspace(ctypes.byref(big))
+    assert L.gdn_bwd_workspace(ctypes.byref(big)) >= 2 * 4 * 32 * 128 * 128 * 2
+    assert L.kda_bwd_workspace(ctypes.byref(big)) >= 2 * 4 * 32 * 128 * 128 * 4
+    f32 = shape(B=2, T=2048, H=4, dk=128, dv=128, chunk=64, dtype=0)
+    assert L.gdn_bwd_workspace(ctypes.byref(f32)) >= 2 * 4 * 32 * 128 * 128 * 4
 
 
 def test_empty_batch_is_a_no_op(L):
@@ -116,10 +119,11 @@ def test_status_strings(L):
 
 
 def test_tensor_core_selection_rule(L):
-    # only bf16, dk = dv = 128, chunk 64 may take the tensor-core kernels
+    # only bf16, dk = dv = 128, chunk 64 takes the tensor-core kernels
     for s in (shape(dtype=0, dk=128, dv=128, chunk=64), shape(dtype=1, dk=64, dv=128, chunk=64),
               shape(dtype=1, dk=128, dv=128, chunk=32)):
         assert L.gdn_uses_tensor_cores(ctypes.byref(s)) == 0
+    assert L.gdn_uses_tensor_cores(ctypes.byref(shape(dtype=1, dk=128, dv=128, chunk=64))) == 1
 
 
 def test_binding_refuses_cpu_tensors(L):

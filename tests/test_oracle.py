@@ -319,3 +319,23 @@ def test_chunked_form_equals_token_form(kda, chunk, T):
     gc = chunk_reference.backward(q, k, v, g, beta, h0, do, dht, chunk, kda)
     for n in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
         np.testing.assert_allclose(gc[n], gr[n], rtol=1e-10, atol=1e-11, err_msg=n)
+
+
+# ------------------------------------------------- scaling identity of the scalar gate
+
+def test_gdn_gate_gradient_scaling_identity():
+    """With one scalar gate per head, H_t = c_t Hhat_t (c_t = prod of the gates)
+    turns the gates into a rescaling of q (by c_t) and v (by 1/c_t), so
+    dL/dlog c_t = q_t.dq_t - v_t.dv_t (+ <dht, ht> at the last token) and
+    dg is its reverse cumulative sum over the sequence."""
+    T = 21
+    q, k, v, g, beta, h0 = rand_inputs(2, T, 3, 5, 4, rng=np.random.default_rng(21))
+    rng = np.random.default_rng(22)
+    do = rng.standard_normal((2, T, 3, 4))
+    dht = rng.standard_normal((2, 3, 5, 4))
+    _, ht = oracle.fwd(q, k, v, g, beta, h0)
+    gr = oracle.bwd(q, k, v, g, beta, h0, do, dht)
+    dlogc = (q * gr["dq"]).sum(-1) - (v * gr["dv"]).sum(-1)
+    dlogc[:, -1] += (dht * ht).sum((-1, -2))
+    want = np.cumsum(dlogc[:, ::-1], axis=1)[:, ::-1]
+    np.testing.assert_allclose(gr["dg"], want, rtol=1e-11, atol=1e-12)

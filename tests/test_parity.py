@@ -139,6 +139,9 @@ def test_long_context_forward_sampled():
 # ----------------------------------------------------------- invariants on the GPU
 
 def test_kda_with_broadcast_gate_equals_gdn():
+    """KDA (CUDA-core kernels) with one gate value repeated over the key
+    dimension against GDN (tensor-core kernels): equal within the bf16
+    tolerance; dg of GDN is the sum of KDA's over the key dimension."""
     x = make_inputs(2, 130, 2, 128, 128, dtype="bf16", h0_std=0.1, with_dht=True, seed=3)
     d = x.to("cuda")
     gk = d.g[..., None].expand(*d.g.shape, 128).contiguous()
@@ -146,11 +149,11 @@ def test_kda_with_broadcast_gate_equals_gdn():
     o2, h2 = gdn.kda_fwd(d.q, d.k, d.v, gk, d.beta, d.h0)
     g1 = gdn.gdn_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, d.dht)
     g2 = gdn.kda_bwd(d.q, d.k, d.v, gk, d.beta, d.h0, d.do, d.dht)
-    assert rel_l2(o2.float().cpu(), o1.float().cpu()) < 1e-2
-    assert rel_l2(h2.cpu(), h1.cpu()) < 1e-3
+    assert rel_l2(o2.float().cpu(), o1.float().cpu()) < BF16_REL
+    assert rel_l2(h2.cpu(), h1.cpu()) < BF16_REL
     for n in ("dq", "dk", "dv", "dbeta", "dh0"):
-        assert rel_l2(g2[n].float().cpu(), g1[n].float().cpu()) < 1e-2, n
-    assert rel_l2(g2["dg"].sum(-1).cpu(), g1["dg"].cpu()) < 1e-2
+        assert rel_l2(g2[n].float().cpu(), g1[n].float().cpu()) < BF16_REL, n
+    assert rel_l2(g2["dg"].sum(-1).cpu(), g1["dg"].cpu()) < BF16_REL
 
 
 @pytest.mark.parametrize("kda", [False, True])
