@@ -132,6 +132,24 @@ GDN_API int gdn_device_status(void);
 /* 1 if the tensor-core kernels would run for this shape, else 0. */
 GDN_API int gdn_uses_tensor_cores(const gdn_shape* shape);
 
+/* GDN backward for callers that cannot allocate device memory (an allocator
+ * callback that must not re-enter the allocator, a framework thread that only
+ * receives tensors, a path that forbids allocation after start-up).  The
+ * paper has no counterpart: this is a library convenience.  It is gdn_bwd
+ * with the workspace taken from a fixed 32 MiB device array built into the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  Arguments and results are those of gdn_bwd without ws/ws_bytes.
+ * Shapes whose gdn_bwd_workspace() exceeds 32 MiB return GDN_ERR_WORKSPACE
+ * and launch nothing.  All calls share the array: calls whose GPU work
+ * overlaps (other streams, unordered host threads) race and give wrong
+ * results.  The first call on each device looks up the array's address
+ * (cudaGetSymbolAddress); make it before any stream capture.  A failure of
+ * that set-up returns GDN_ERR_CUDA. */
+GDN_API int gdn_bwd_noalloc(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                            const float* g, const float* beta, const float* h0,
+                            const void* do_, const float* dht, void* dq, void* dk, void* dv,
+                            float* dg, float* dbeta, float* dh0, void* stream);
+
 /* Per-kernel timing without a profiler (calling thread only).
  * gdn_profile_begin(cap) starts recording: every kernel the library launches
  * from this thread is bracketed by a pair of CUDA events recorded on the
