@@ -53,7 +53,6 @@ using namespace tc;
 
 constexpr int C = 64;     // chunk
 constexpr int D = 128;    // dk = dv
-constexpr int NT = 128;   // threads per CTA
 
 // ---------------------------------------------------------------- shared memory map
 // Offsets in bytes from a 1024-aligned base.  Stage s (double buffer) holds
@@ -72,8 +71,7 @@ constexpr int kOffUf = kOffU + 16384;           // (U diag f)^T [c][j]         (
 // The fp32 solve scratch (A, T [64][65] and S [3][16][16]) aliases W / U / Uf:
 // those are written only after the solve and its T', T'' outputs are done.
 constexpr int kOffSolve = kOffW;
-constexpr int kLdA = 65;
-constexpr int kSolveBytes = (2 * 64 * kLdA + 3 * 256) * 4;
+constexpr int kSolveBytes = (2 * 64 * 68 + 3 * 256) * 4;   // A, T [64][68] fp32 + S
 static_assert(kSolveBytes <= 3 * 16384, "solve scratch must fit in W/U/Uf");
 constexpr int kOffGate = kOffUf + 16384;         // gam, e, f, beta [64] each, eC
 constexpr int kOffBar = kOffGate + 4 * 64 * 4 + 64;
@@ -102,45 +100,6 @@ __device__ __forceinline__ int sw_row_off(int row, int chunk16) {
   return row * 128 + ((chunk16 ^ (row & 7)) << 4);
 }
 
-// Writes 64 fp32 values as one 128-byte swizzled bf16 row.
-__device__ __forceinline__ void store_row64(unsigned char* tile, int row, const float* v) {
-#pragma unroll
-  for (int c8 = 0; c8 < 8; ++c8) {
-    uint4 pk;
-    uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 b2 = __floats2bfloat162_rn(v[c8 * 8 + 2 * i], v[c8 * 8 + 2 * i + 1]);
-      w[i] = *reinterpret_cast<uint32_t*>(&b2);
-    }
-    *reinterpret_cast<uint4*>(tile + sw_row_off(row, c8)) = pk;
-  }
-}
-
-// Writes thread c's fp32 state row as row c of the bf16 G tile (two 64-wide
-// column blocks of 16 KB) and, if dst is set, the same bytes to dst (a 32 KB
-// global copy of the tile in its shared-memory layout).
-__device__ __forceinline__ void store_g_tile(unsigned char* tile, const float* G, int row,
-                                             unsigned char* dst) {
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) {
-      uint4 pk;
-      uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(G[half * 64 + c8 * 8 + 2 * i],
-                                                  G[half * 64 + c8 * 8 + 2 * i + 1]);
-        w[i] = *reinterpret_cast<uint32_t*>(&b2);
-      }
-      const int off = half * 16384 + sw_row_off(row, c8);
-      *reinterpret_cast<uint4*>(tile + off) = pk;
-      if (dst) *reinterpret_cast<uint4*>(dst + off) = pk;
-    }
-  }
-}
-
 __device__ __forceinline__ void cta_sync() {
   tc_fence_before();
   __syncthreads();
@@ -149,13 +108,36 @@ __device__ __forceinline__ void cta_sync() {
 
 __device__ __forceinline__ void report_timeout() { atomicExch(&g_device_status, GDN_ERR_DEVICE_TIMEOUT); }
 
-// Unit-lower-triangular inverse T = (I + A)^-1 of a 64 x 64 strictly lower A
-// (fp32, row stride kLdA), blocked in 16 x 16: diagonal blocks by forward
-// substitution, off-diagonal blocks by T_ib,jb = -T_ib,ib sum_kb A_ib,kb T_kb,jb.
-__device__ void solve_unit_lower(const float* A, float* T, float* S) {
+// ---------------------------------------------------------------- forward kernel
+//
+// 512 threads: warp w reads TMEM lane quadrant q = w % 4 (lanes 32q..32q+31)
+// and handles column group cg = w / 4 of every tile, so each epilogue is split
+// four ways and every scheduler has four warps.  Thread (row, cg) owns
+// columns [32 cg, 32 cg + 32) of state row `row`.
+
+constexpr int FT = 512;              // forward threads
+constexpr int kLdF = 68;             // fp32 row stride of the solve scratch (16-byte rows)
+
+// 64-element row chunk helpers: write n16 groups of 8 bf16 (16 B) of a
+// swizzled 128-byte row, starting at 16-byte chunk c0.
+__device__ __forceinline__ void store_chunks(unsigned char* tile, int row, int c0, const float* v,
+                                             int nchunks) {
+  for (int k = 0; k < nchunks; ++k) {
+    uint4 pk;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(v[k * 8 + 2 * i], v[k * 8 + 2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&b2);
+    }
+    *reinterpret_cast<uint4*>(tile + sw_row_off(row, c0 + k)) = pk;
+  }
+}
+
+// T = (I + A)^-1 for a 64 x 64 strictly lower A (fp32, row stride kLdF), by
+// 16 x 16 blocks; all FT threads take part.
+__device__ void solve_unit_lower_f(const float* A, float* T, float* S) {
   const int tid = threadIdx.x;
-  for (int i = tid; i < 64 * 64; i += NT) T[(i / 64) * kLdA + (i % 64)] = 0.f;
-  __syncthreads();
   if (tid < 64) {
     const int ib = tid / 16, jj = tid % 16, o = ib * 16;
     float x[16];
@@ -165,44 +147,50 @@ __device__ void solve_unit_lower(const float* A, float* T, float* S) {
       if (r > jj) {
 #pragma unroll
         for (int i = 0; i < r; ++i)
-          if (i >= jj) s -= A[(o + r) * kLdA + o + i] * x[i];
+          if (i >= jj) s -= A[(o + r) * kLdF + o + i] * x[i];
       }
       x[r] = (r >= jj) ? s : 0.f;
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) T[(o + r) * kLdA + o + jj] = x[r];
+    for (int r = 0; r < 16; ++r) T[(o + r) * kLdF + o + jj] = x[r];
+  } else {
+    // zero the strictly upper blocks (never read as T, but keep T well defined)
+    for (int i = tid - 64; i < 64 * 64; i += FT - 64) {
+      const int r = i / 64, c = i % 64;
+      if ((c / 16) > (r / 16)) T[r * kLdF + c] = 0.f;
+    }
   }
   __syncthreads();
   for (int L = 1; L < 4; ++L) {
     const int nb = 4 - L;
-    // S_b = sum_{kb=jb}^{ib-1} A[ib][kb] T[kb][jb],  block b: jb = b, ib = b + L
-    for (int i = tid; i < nb * 256; i += NT) {
+    for (int i = tid; i < nb * 256; i += FT) {
       const int b = i / 256, r = (i / 16) % 16, c = i % 16;
       const int ib = b + L, jb = b;
       float s = 0.f;
-      for (int k = jb * 16; k < ib * 16; ++k) s += A[(ib * 16 + r) * kLdA + k] * T[k * kLdA + jb * 16 + c];
+      for (int k = jb * 16; k < ib * 16; ++k) s += A[(ib * 16 + r) * kLdF + k] * T[k * kLdF + jb * 16 + c];
       S[b * 256 + r * 16 + c] = s;
     }
     __syncthreads();
-    for (int i = tid; i < nb * 256; i += NT) {
+    for (int i = tid; i < nb * 256; i += FT) {
       const int b = i / 256, r = (i / 16) % 16, c = i % 16;
       const int ib = b + L, jb = b;
       float s = 0.f;
-      for (int k = 0; k <= r; ++k) s += T[(ib * 16 + r) * kLdA + ib * 16 + k] * S[b * 256 + k * 16 + c];
-      T[(ib * 16 + r) * kLdA + jb * 16 + c] = -s;
+      for (int k = 0; k <= r; ++k) s += T[(ib * 16 + r) * kLdF + ib * 16 + k] * S[b * 256 + k * 16 + c];
+      T[(ib * 16 + r) * kLdF + jb * 16 + c] = -s;
     }
     __syncthreads();
   }
 }
 
-// ---------------------------------------------------------------- forward kernel
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(FT, 1)
 gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, FwdParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int tid = threadIdx.x, warp = tid / 32;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
+  const int quad = warp & 3, cg = warp >> 2;
+  const int row = quad * 32 + lane;    // TMEM lane / tile row owned by this thread
   const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
 
   float* gam = reinterpret_cast<float*>(sm + kOffGate);
@@ -213,16 +201,14 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   uint64_t* bar_load = reinterpret_cast<uint64_t*>(sm + kOffBar);  // [2]
   uint64_t* bar_mma = bar_load + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma + 1);
-  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   float* Am = reinterpret_cast<float*>(sm + kOffSolve);
-  float* Tm = Am + 64 * kLdA;
-  float* Sm = Tm + 64 * kLdA;
+  float* Tm = Am + 64 * kLdF;
+  float* Sm = Tm + 64 * kLdF;
 
   if (tid == 0) {
     mbar_init(&bar_load[0], 1);
     mbar_init(&bar_load[1], 1);
     mbar_init(bar_mma, 1);
-    *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -234,7 +220,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
   cta_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
 
   auto issue_load = [&](int ci) {
     unsigned char* st = sm + kOffStage0 + (ci & 1) * kStageBytes;
@@ -248,22 +234,47 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tma_load_4d(st + kStageV + 0, &tm_v, bar, 0, h, t0, b);
     tma_load_4d(st + kStageV + 8192, &tm_v, bar, 64, h, t0, b);
   };
-
   auto state_dst = [&](int ci) -> unsigned char* {
     return p.states ? reinterpret_cast<unsigned char*>(p.states) +
                           ((size_t)bh * p.N + ci) * (size_t)(2 * 16384)
                     : nullptr;
   };
   const bool want_o = p.o != nullptr;
-
-  // state: thread c owns row c of G = H^T
-  float G[D];
-  {
+  // this thread's 32 state columns: d in [32 cg, 32 cg + 32) = tile region cg/2, chunks 4(cg%2)..
+  const int g_region = cg >> 1, g_chunk0 = (cg & 1) * 4;
+  auto write_g = [&](const float* Gv, unsigned char* dst) {
+    unsigned char* tile = sm + kOffG + g_region * 16384;
+    for (int k = 0; k < 4; ++k) {
+      uint4 pk;
+      uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
 #pragma unroll
-    for (int d = 0; d < D; ++d)
-      G[d] = p.h0 ? p.h0[((size_t)bh * D + d) * D + tid] : 0.f;
-    store_g_tile(sm + kOffG, G, tid, state_dst(0));
-  }
+      for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(Gv[k * 8 + 2 * i], Gv[k * 8 + 2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+      const int off = sw_row_off(row, g_chunk0 + k);
+      *reinterpret_cast<uint4*>(tile + off) = pk;
+      if (dst) *reinterpret_cast<uint4*>(dst + g_region * 16384 + off) = pk;
+    }
+  };
+
+  float G[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    G[i] = p.h0 ? p.h0[((size_t)bh * D + cg * 32 + i) * D + row] : 0.f;
+  write_g(G, state_dst(0));
+
+  // gate prefetch (warp 0): registers for the next chunk
+  float pg0 = 0.f, pg1 = 0.f, pb0 = 0.f, pb1 = 0.f;
+  auto load_gates = [&](int ci) {
+    const int t0 = ci * C, n = min(C, p.T - t0);
+    const size_t base = ((size_t)b * p.T + t0) * p.H + h;
+    pg0 = lane < n ? p.g[base + (size_t)lane * p.H] : 0.f;
+    pg1 = lane + 32 < n ? p.g[base + (size_t)(lane + 32) * p.H] : 0.f;
+    pb0 = lane < n ? p.beta[base + (size_t)lane * p.H] : 0.f;
+    pb1 = lane + 32 < n ? p.beta[base + (size_t)(lane + 32) * p.H] : 0.f;
+  };
+  if (warp == 0) load_gates(0);
   fence_async_shared();
   if (tid == 0) issue_load(0);
   cta_sync();
@@ -271,40 +282,42 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   uint32_t mma_phase = 0;
   uint32_t load_phase[2] = {0, 0};
   bool ok = true;
+  auto mma_wait = [&]() {
+    ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
+    mma_phase ^= 1;
+    tc_fence_after();
+  };
 
   for (int ci = 0; ci < p.N && ok; ++ci) {
     const int s = ci & 1, t0 = ci * C, n = min(C, p.T - t0);
     unsigned char* st = sm + kOffStage0 + s * kStageBytes;
     const uint32_t st_kq = smem_u32(st + kStageKQ), st_v = smem_u32(st + kStageV);
 
-    // gates of this chunk (warp 0): gamma = cumsum(g), e, f, eC
     if (warp == 0) {
-      const int l = threadIdx.x;
-      const size_t base = ((size_t)b * p.T + t0) * p.H + h;
-      float g0 = l < n ? p.g[base + (size_t)l * p.H] : 0.f;
-      float g1 = l + 32 < n ? p.g[base + (size_t)(l + 32) * p.H] : 0.f;
-      bt[l] = l < n ? p.beta[base + (size_t)l * p.H] : 0.f;
-      bt[l + 32] = l + 32 < n ? p.beta[base + (size_t)(l + 32) * p.H] : 0.f;
+      float g0 = pg0, g1 = pg1;
+      bt[lane] = pb0;
+      bt[lane + 32] = pb1;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         float a0 = __shfl_up_sync(0xffffffffu, g0, off);
         float a1 = __shfl_up_sync(0xffffffffu, g1, off);
-        if (l >= off) g0 += a0, g1 += a1;
+        if (lane >= off) g0 += a0, g1 += a1;
       }
       g1 += __shfl_sync(0xffffffffu, g0, 31);
       const float gl = __shfl_sync(0xffffffffu, g1, 31);
-      gam[l] = g0;
-      gam[l + 32] = g1;
-      ee[l] = expf(g0);
-      ee[l + 32] = expf(g1);
-      ff[l] = expf(gl - g0);
-      ff[l + 32] = expf(gl - g1);
-      if (l == 0) *eC = expf(gl);
+      gam[lane] = g0;
+      gam[lane + 32] = g1;
+      ee[lane] = __expf(g0);
+      ee[lane + 32] = __expf(g1);
+      ff[lane] = __expf(gl - g0);
+      ff[lane + 32] = __expf(gl - g1);
+      if (lane == 0) *eC = __expf(gl);
+      if (ci + 1 < p.N) load_gates(ci + 1);
     }
-    // tiles of this chunk
     ok = __syncthreads_and(mbar_wait(&bar_load[s], load_phase[s]));
     load_phase[s] ^= 1;
-    if (tid == 0 && ok) {
+    if (!ok) break;
+    if (tid == 0) {
       // MMA1: [K;Q] K^T, M=128 N=64 K=128
       const uint32_t idesc = idesc_bf16(128, 64, false, false);
       for (int ks = 0; ks < 8; ++ks) {
@@ -315,66 +328,53 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mma_commit(bar_mma);
       if (ci + 1 < p.N) issue_load(ci + 1);
     }
-    if (!ok) break;
-    ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
-    mma_phase ^= 1;
-    tc_fence_after();
+    mma_wait();
     if (!ok) break;
 
-    // E1: A (lanes 0-63) and P (lanes 64-127)
+    // E1: rows 0-63: A (fp32); rows 64-127: P (bf16); this thread: 16 columns
     {
-      float kk[64];
-      float v32[32];
-      tmem_ld32(tmem + lane_base + kTmKQ, v32);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) kk[i] = v32[i];
-      tmem_ld32(tmem + lane_base + kTmKQ + 32, v32);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) kk[32 + i] = v32[i];
-      if (tid < 64) {
-        const int r = tid;
+      float v[16];
+      tmem_ld16(tmem + lane_base + kTmKQ + cg * 16, v);
+      if (row < 64) {
+        const int r = row;
         const float gr = gam[r], br = bt[r];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) Am[r * kLdA + j] = (j < r) ? br * kk[j] * expf(gr - gam[j]) : 0.f;
+        for (int i = 0; i < 16; ++i) {
+          const int j = cg * 16 + i;
+          v[i] = (j < r) ? br * v[i] * __expf(gr - gam[j]) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          *reinterpret_cast<float4*>(Am + r * kLdF + cg * 16 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
       } else {
-        const int r = tid - 64;
+        const int r = row - 64;
         const float gr = gam[r];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) kk[j] = (j <= r) ? kk[j] * expf(gr - gam[j]) : 0.f;
-        store_row64(sm + kOffP, r, kk);
+        for (int i = 0; i < 16; ++i) {
+          const int j = cg * 16 + i;
+          v[i] = (j <= r) ? v[i] * __expf(gr - gam[j]) : 0.f;
+        }
+        store_chunks(sm + kOffP, r, cg * 2, v, 2);
       }
     }
     cta_sync();
-    solve_unit_lower(Am, Tm, Sm);
-    // T' = T diag(beta e), T'' = T diag(beta): thread -> (row r = tid/2, half)
+    solve_unit_lower_f(Am, Tm, Sm);
+    // T' = T diag(beta e), T'' = T diag(beta): one 16-byte chunk per thread
     {
-      const int r = tid >> 1, hf = tid & 1;
-      float v1[32], v2[32];
+      const int r = tid >> 3, c8 = tid & 7;
+      float v1[8], v2[8];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int j = hf * 32 + i;
-        const float t = (j <= r) ? Tm[r * kLdA + j] : 0.f;
+      for (int i = 0; i < 8; ++i) {
+        const int j = c8 * 8 + i;
+        const float t = (j <= r) ? Tm[r * kLdF + j] : 0.f;
         v2[i] = t * bt[j];
         v1[i] = v2[i] * ee[j];
       }
-#pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        uint4 p1, p2;
-        uint32_t* w1 = reinterpret_cast<uint32_t*>(&p1);
-        uint32_t* w2 = reinterpret_cast<uint32_t*>(&p2);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          __nv_bfloat162 a = __floats2bfloat162_rn(v1[c8 * 8 + 2 * i], v1[c8 * 8 + 2 * i + 1]);
-          __nv_bfloat162 c2 = __floats2bfloat162_rn(v2[c8 * 8 + 2 * i], v2[c8 * 8 + 2 * i + 1]);
-          w1[i] = *reinterpret_cast<uint32_t*>(&a);
-          w2[i] = *reinterpret_cast<uint32_t*>(&c2);
-        }
-        *reinterpret_cast<uint4*>(sm + kOffT1 + sw_row_off(r, hf * 4 + c8)) = p1;
-        *reinterpret_cast<uint4*>(sm + kOffT2 + sw_row_off(r, hf * 4 + c8)) = p2;
-      }
+      store_chunks(sm + kOffT1, r, c8, v1, 1);
+      store_chunks(sm + kOffT2, r, c8, v2, 1);
     }
-    // scale Q rows in place by e_r (Q is done as an MMA1 operand)
-    for (int i = tid; i < 2 * 64 * 8; i += NT) {
+    // scale Q rows in place by e_r (Q is done as an MMA1 operand): 2 chunks per thread
+    for (int i = tid; i < 2 * 64 * 8; i += FT) {
       const int half = i / 512, r = (i / 8) % 64, c8 = i % 8;
       uint4* ptr = reinterpret_cast<uint4*>(st + kStageKQ + half * 16384 + 8192 + r * 128 + c8 * 16);
       uint4 val = *ptr;
@@ -401,20 +401,13 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                  sw128_desc(smem_u32(sm + kOffT2) + ks * 32, 16, 1024), id2, ks > 0);
       mma_commit(bar_mma);
     }
-    ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
-    mma_phase ^= 1;
-    tc_fence_after();
+    mma_wait();
     if (!ok) break;
     // E2: W^T row d -> W tile (MN-major: row d holds 64 r)
     {
-      float w[64], v32[32];
-      tmem_ld32(tmem + lane_base + kTmW, v32);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) w[i] = v32[i];
-      tmem_ld32(tmem + lane_base + kTmW + 32, v32);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) w[32 + i] = v32[i];
-      store_row64(sm + kOffW, tid, w);
+      float w[16];
+      tmem_ld16(tmem + lane_base + kTmW + cg * 16, w);
+      store_chunks(sm + kOffW, row, cg * 2, w, 2);
     }
     fence_async_shared();
     cta_sync();
@@ -433,23 +426,16 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       mma_commit(bar_mma);
     }
-    ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
-    mma_phase ^= 1;
-    tc_fence_after();
+    mma_wait();
     if (!ok) break;
     // E3: U^T row c -> U^T tile and (U diag f)^T tile
     {
-      float u[64], v32[32];
-      tmem_ld32(tmem + lane_base + kTmU, v32);
+      float u[16];
+      tmem_ld16(tmem + lane_base + kTmU + cg * 16, u);
+      store_chunks(sm + kOffU, row, cg * 2, u, 2);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) u[i] = v32[i];
-      tmem_ld32(tmem + lane_base + kTmU + 32, v32);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) u[32 + i] = v32[i];
-      store_row64(sm + kOffU, tid, u);
-#pragma unroll
-      for (int j = 0; j < 64; ++j) u[j] *= ff[j];
-      store_row64(sm + kOffUf, tid, u);
+      for (int i = 0; i < 16; ++i) u[i] *= ff[cg * 16 + i];
+      store_chunks(sm + kOffUf, row, cg * 2, u, 2);
     }
     fence_async_shared();
     cta_sync();
@@ -466,36 +452,26 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                  sw128_desc(st_kq + ks * 2048, 16384, 1024), id5, ks > 0);
       mma_commit(bar_mma);
     }
-    ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
-    mma_phase ^= 1;
-    tc_fence_after();
+    mma_wait();
     if (!ok) break;
-    // E4: O^T row c -> o[b, t0 + r, h, c]
+    // E4: O^T row c, columns r in [16 cg, 16 cg + 16) -> o[b, t0 + r, h, c]
     if (want_o) {
-      float v32[32];
+      float v[16];
+      tmem_ld16(tmem + lane_base + kTmO + cg * 16, v);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        tmem_ld32(tmem + lane_base + kTmO + half * 32, v32);
-        {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int r = half * 32 + i;
-            if (r < n) p.o[(((size_t)b * p.T + t0 + r) * p.H + h) * D + tid] = __float2bfloat16_rn(v32[i]);
-          }
-        }
+      for (int i = 0; i < 16; ++i) {
+        const int r = cg * 16 + i;
+        if (r < n) p.o[(((size_t)b * p.T + t0 + r) * p.H + h) * D + row] = __float2bfloat16_rn(v[i]);
       }
     }
-    // E5: G = eC G + dG; bf16 copy for the next chunk
+    // E5: G = eC G + dG on this thread's 32 columns; bf16 copy for the next chunk
     {
       const float ec = *eC;
       float v32[32];
+      tmem_ld32(tmem + lane_base + kTmG + cg * 32, v32);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        tmem_ld32(tmem + lane_base + kTmG + q4 * 32, v32);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) G[q4 * 32 + i] = fmaf(ec, G[q4 * 32 + i], v32[i]);
-      }
-      store_g_tile(sm + kOffG, G, tid, ci + 1 < p.N ? state_dst(ci + 1) : nullptr);
+      for (int i = 0; i < 32; ++i) G[i] = fmaf(ec, G[i], v32[i]);
+      write_g(G, ci + 1 < p.N ? state_dst(ci + 1) : nullptr);
     }
     fence_async_shared();
     cta_sync();
@@ -508,22 +484,25 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   } else {
     if (p.ht) {
 #pragma unroll
-      for (int d = 0; d < D; ++d) p.ht[((size_t)bh * D + d) * D + tid] = G[d];
+      for (int i = 0; i < 32; ++i) p.ht[((size_t)bh * D + cg * 32 + i) * D + row] = G[i];
     }
     if (p.dht_dot) {
-      // <dht, ht> over the sequence's whole state (row c = tid here)
       float acc = 0.f;
       if (p.dht) {
 #pragma unroll
-        for (int d = 0; d < D; ++d) acc += p.dht[((size_t)bh * D + d) * D + tid] * G[d];
+        for (int i = 0; i < 32; ++i) acc += p.dht[((size_t)bh * D + cg * 32 + i) * D + row] * G[i];
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
       float* red = reinterpret_cast<float*>(sm + kOffGate);  // gates are no longer needed
       __syncthreads();
-      if ((tid & 31) == 0) red[warp] = acc;
+      if (lane == 0) red[warp] = acc;
       __syncthreads();
-      if (tid == 0) p.dht_dot[bh] = red[0] + red[1] + red[2] + red[3];
+      if (tid == 0) {
+        float t = 0.f;
+        for (int w = 0; w < FT / 32; ++w) t += red[w];
+        p.dht_dot[bh] = t;
+      }
     }
   }
   cta_sync();
@@ -555,17 +534,19 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 // (or <dht, ht> for the last one).  Keeping the sum inside the chunk avoids
 // accumulating the rounding of thousands of terms.
 
+constexpr int BT = 512;                  // backward threads (as the forward)
 constexpr int kB_KQ = 0;                 // [Kh0 | Qh0 | Kh1 | Qh1]
 constexpr int kB_ZO = 32768;             // [dZh0 | dOh0 | dZh1 | dOh1]
 constexpr int kB_GI = 65536;             // G_in tile (K-major [c][d])
 constexpr int kB_DG = 98304;             // dG tile (K-major [c][d])
-constexpr int kB_T = 131072;             // T [r][j]
-constexpr int kB_P = kB_T + 8192;        // P [r][j]
-constexpr int kB_DP = kB_P + 8192;       // dP o Gam [r][j]
-constexpr int kB_M = kB_DP + 8192;       // M = beta dA o Gam [r][j]
-constexpr int kB_X = kB_M + 8192;        // three 16 KB slots, reused by phase
-constexpr int kB_GATE = kB_X + 3 * 16384;  // gam, e, f, beta, db1, db2, dlc [64] each + red [4][64]
-constexpr int kB_BAR = kB_GATE + 7 * 256 + 1024 + 64;
+constexpr int kB_V = 131072;             // [Vh0 | Vh1]
+constexpr int kB_T = kB_V + 16384;       // T [r][j]; after the dZ product: M = beta dA o Gam
+constexpr int kB_P = kB_T + 8192;        // P [r][j]; after dO^T P: dP o Gam
+constexpr int kB_X = kB_P + 8192;        // three 16 KB slots, reused by phase
+constexpr int kB_GATE = kB_X + 3 * 16384;  // gam, e, f, beta, db1, db2, dlc [64] each
+constexpr int kB_RED = kB_GATE + 7 * 256;  // reduction scratch [16][64] floats
+constexpr int kB_EC = kB_RED + 4096;
+constexpr int kB_BAR = kB_EC + 64;
 constexpr int kBwdSmemBytes = kB_BAR + 128 + 1024;
 static_assert(kSolveBytes <= 3 * 16384, "solve scratch fits the X slots");
 static_assert(kBwdSmemBytes <= 227 * 1024, "shared memory budget");
@@ -578,7 +559,6 @@ constexpr uint32_t kBtKQ = 0, kBtR = 64, kBtX1 = 128, kBtX2 = 192, kBtU = 256, k
 struct BwdParams {
   const float* g;
   const float* beta;
-  const __nv_bfloat16* v;
   const float* dht;
   const float* dht_dot;          // <dht, ht> per sequence (workspace)
   const unsigned char* states;   // [B*H][N][32 KB]
@@ -599,17 +579,18 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// Sums v[0..63] over the 128 threads of the CTA; out[r] (r < 64) gets the sum.
-// Within a warp: five halving exchange steps (lane l ends with the sums of
-// indices 2l, 2l+1); across warps: red[4][64] in shared memory.
-__device__ __forceinline__ void cta_sum64(float (&v)[64], float* red, float* out) {
-  const int l = threadIdx.x & 31, w = threadIdx.x >> 5;
+// Each thread holds v[i] for tile column (16 cg + i) of its row; returns in
+// out[r] (r < 64) the sum over all 128 rows.  Within a warp: four halving
+// exchanges and one pairwise add (lane l ends with column 16 cg + l/2); across
+// the four warps of a column group: red[16][16] in shared memory.
+__device__ __forceinline__ void cta_sum_rows16(float (&v)[16], float* red, float* out) {
+  const int l = threadIdx.x & 31, w = threadIdx.x >> 5, quad = w & 3, cg = w >> 2;
 #pragma unroll
-  for (int step = 0; step < 5; ++step) {
-    const int off = 16 >> step, half = 32 >> step;
+  for (int step = 0; step < 4; ++step) {
+    const int off = 16 >> step, half = 8 >> step;
     const bool up = (l & off) != 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < 8; ++i) {
       if (i < half) {
         const float send = up ? v[i] : v[i + half];
         const float keep = up ? v[i + half] : v[i];
@@ -617,32 +598,33 @@ __device__ __forceinline__ void cta_sum64(float (&v)[64], float* red, float* out
       }
     }
   }
-  red[w * 64 + 2 * l] = v[0];
-  red[w * 64 + 2 * l + 1] = v[1];
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+  if ((l & 1) == 0) red[(cg * 4 + quad) * 16 + (l >> 1)] = v[0];
   __syncthreads();
-  if (threadIdx.x < 64)
-    out[threadIdx.x] = red[threadIdx.x] + red[64 + threadIdx.x] + red[128 + threadIdx.x] +
-                       red[192 + threadIdx.x];
+  if (threadIdx.x < 64) {
+    const int c = threadIdx.x >> 4, i = threadIdx.x & 15;
+    out[threadIdx.x] = red[(c * 4 + 0) * 16 + i] + red[(c * 4 + 1) * 16 + i] +
+                       red[(c * 4 + 2) * 16 + i] + red[(c * 4 + 3) * 16 + i];
+  }
   __syncthreads();
 }
 
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
-  float a[32];
-  tmem_ld32(taddr, a);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = a[i];
-  tmem_ld32(taddr + 32, a);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[32 + i] = a[i];
+// bf16 element (row, col) of a swizzled 64-wide K-major tile
+__device__ __forceinline__ float tile_elem(const unsigned char* tile, int row, int col) {
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+      tile + sw_row_off(row, col >> 3) + (col & 7) * 2));
 }
 
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(BT, 1)
 gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_do, BwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  BwdParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int tid = threadIdx.x, warp = tid / 32;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
+  const int quad = warp & 3, cg = warp >> 2;
+  const int row = quad * 32 + lane;
   const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
 
   float* gam = reinterpret_cast<float*>(sm + kB_GATE);
@@ -652,18 +634,18 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   float* db1 = bt + 64;
   float* db2 = db1 + 64;
   float* dlc = db2 + 64;
-  float* red = dlc + 64;  // [4][64]
-  float* eC = red + 256;
+  float* red = reinterpret_cast<float*>(sm + kB_RED);
+  float* eC = reinterpret_cast<float*>(sm + kB_EC);
   uint64_t* bar_load = reinterpret_cast<uint64_t*>(sm + kB_BAR);
   uint64_t* bar_mma = bar_load + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma + 1);
   float* Am = reinterpret_cast<float*>(sm + kB_X);
-  float* Tm = Am + 64 * kLdA;
-  float* Sm = Tm + 64 * kLdA;
+  float* Tm = Am + 64 * kLdF;
+  float* Sm = Tm + 64 * kLdF;
   const uint32_t sKQ = smem_u32(sm + kB_KQ), sZO = smem_u32(sm + kB_ZO);
   const uint32_t sGI = smem_u32(sm + kB_GI), sDG = smem_u32(sm + kB_DG);
   const uint32_t sT = smem_u32(sm + kB_T), sP = smem_u32(sm + kB_P);
-  const uint32_t sDP = smem_u32(sm + kB_DP), sM = smem_u32(sm + kB_M);
+  const uint32_t sDP = sP, sM = sT;
   const uint32_t sX0 = smem_u32(sm + kB_X), sX1 = sX0 + 16384, sX2 = sX0 + 32768;
 
   if (tid == 0) {
@@ -672,6 +654,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     fence_barrier_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
   }
   if (warp == 0) {
@@ -680,14 +663,40 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
   cta_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lb = (uint32_t)(warp * 32) << 16;
+  const uint32_t lb = (uint32_t)(quad * 32) << 16;
 
-  float dG[D];
+  // this thread's 32 state-gradient columns: d in [32 cg, 32 cg + 32)
+  const int g_region = cg >> 1, g_chunk0 = (cg & 1) * 4;
+  float dG[32];
 #pragma unroll
-  for (int d = 0; d < D; ++d) dG[d] = p.dht ? p.dht[((size_t)bh * D + d) * D + tid] : 0.f;
-  store_g_tile(sm + kB_DG, dG, tid, nullptr);
+  for (int i = 0; i < 32; ++i) dG[i] = p.dht ? p.dht[((size_t)bh * D + cg * 32 + i) * D + row] : 0.f;
+  auto write_dg = [&]() {
+    unsigned char* tile = sm + kB_DG + g_region * 16384;
+    for (int k = 0; k < 4; ++k) {
+      uint4 pk;
+      uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(dG[k * 8 + 2 * i], dG[k * 8 + 2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+      *reinterpret_cast<uint4*>(tile + sw_row_off(row, g_chunk0 + k)) = pk;
+    }
+  };
+  write_dg();
   // <dH_out, H_out> of the chunk being processed (the last chunk: <dht, ht>)
   float carry = p.dht_dot ? p.dht_dot[bh] : 0.f;
+
+  float pg0 = 0.f, pg1 = 0.f, pb0 = 0.f, pb1 = 0.f;
+  auto load_gates = [&](int ci) {
+    const int t0 = ci * C, n = min(C, p.T - t0);
+    const size_t base = ((size_t)b * p.T + t0) * p.H + h;
+    pg0 = lane < n ? p.g[base + (size_t)lane * p.H] : 0.f;
+    pg1 = lane + 32 < n ? p.g[base + (size_t)(lane + 32) * p.H] : 0.f;
+    pb0 = lane < n ? p.beta[base + (size_t)lane * p.H] : 0.f;
+    pb1 = lane + 32 < n ? p.beta[base + (size_t)(lane + 32) * p.H] : 0.f;
+  };
+  if (warp == 0) load_gates(p.N - 1);
 
   uint32_t mma_phase = 0, load_phase = 0;
   bool ok = true;
@@ -702,38 +711,37 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     fence_async_shared();
     cta_sync();
     if (tid == 0) {
-      mbar_arrive_expect_tx(bar_load, 6 * 8192 + 32768);
+      mbar_arrive_expect_tx(bar_load, 8 * 8192 + 32768);
       tma_load_4d(sm + kB_KQ + 0, &tm_k, bar_load, 0, h, t0, b);
       tma_load_4d(sm + kB_KQ + 8192, &tm_q, bar_load, 0, h, t0, b);
       tma_load_4d(sm + kB_KQ + 16384, &tm_k, bar_load, 64, h, t0, b);
       tma_load_4d(sm + kB_KQ + 24576, &tm_q, bar_load, 64, h, t0, b);
       tma_load_4d(sm + kB_ZO + 8192, &tm_do, bar_load, 0, h, t0, b);
       tma_load_4d(sm + kB_ZO + 24576, &tm_do, bar_load, 64, h, t0, b);
+      tma_load_4d(sm + kB_V, &tm_v, bar_load, 0, h, t0, b);
+      tma_load_4d(sm + kB_V + 8192, &tm_v, bar_load, 64, h, t0, b);
       bulk_load(sm + kB_GI, p.states + ((size_t)bh * p.N + ci) * 32768, 32768, bar_load);
     }
-    // gates
     if (warp == 0) {
-      const int l = tid;
-      const size_t base = ((size_t)b * p.T + t0) * p.H + h;
-      float g0 = l < n ? p.g[base + (size_t)l * p.H] : 0.f;
-      float g1 = l + 32 < n ? p.g[base + (size_t)(l + 32) * p.H] : 0.f;
-      bt[l] = l < n ? p.beta[base + (size_t)l * p.H] : 0.f;
-      bt[l + 32] = l + 32 < n ? p.beta[base + (size_t)(l + 32) * p.H] : 0.f;
+      float g0 = pg0, g1 = pg1;
+      bt[lane] = pb0;
+      bt[lane + 32] = pb1;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         float a0 = __shfl_up_sync(0xffffffffu, g0, off);
         float a1 = __shfl_up_sync(0xffffffffu, g1, off);
-        if (l >= off) g0 += a0, g1 += a1;
+        if (lane >= off) g0 += a0, g1 += a1;
       }
       g1 += __shfl_sync(0xffffffffu, g0, 31);
       const float gl = __shfl_sync(0xffffffffu, g1, 31);
-      gam[l] = g0;
-      gam[l + 32] = g1;
-      ee[l] = expf(g0);
-      ee[l + 32] = expf(g1);
-      ff[l] = expf(gl - g0);
-      ff[l + 32] = expf(gl - g1);
-      if (l == 0) *eC = expf(gl);
+      gam[lane] = g0;
+      gam[lane + 32] = g1;
+      ee[lane] = __expf(g0);
+      ee[lane + 32] = __expf(g1);
+      ff[lane] = __expf(gl - g0);
+      ff[lane + 32] = __expf(gl - g1);
+      if (lane == 0) *eC = __expf(gl);
+      if (ci > 0) load_gates(ci - 1);
     }
     ok = __syncthreads_and(mbar_wait(bar_load, load_phase));
     load_phase ^= 1;
@@ -751,42 +759,41 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     mma_wait();
     if (!ok) break;
     {
-      float kk[64];
-      tmem_ld64(tmem + lb + kBtKQ, kk);
-      if (tid < 64) {
-        const int r = tid;
+      float v[16];
+      tmem_ld16(tmem + lb + kBtKQ + cg * 16, v);
+      if (row < 64) {
+        const int r = row;
         const float gr = gam[r], br = bt[r];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) Am[r * kLdA + j] = (j < r) ? br * kk[j] * expf(gr - gam[j]) : 0.f;
+        for (int i = 0; i < 16; ++i) {
+          const int j = cg * 16 + i;
+          v[i] = (j < r) ? br * v[i] * __expf(gr - gam[j]) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          *reinterpret_cast<float4*>(Am + r * kLdF + cg * 16 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
       } else {
-        const int r = tid - 64;
+        const int r = row - 64;
         const float gr = gam[r];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) kk[j] = (j <= r) ? kk[j] * expf(gr - gam[j]) : 0.f;
-        store_row64(sm + kB_P, r, kk);
+        for (int i = 0; i < 16; ++i) {
+          const int j = cg * 16 + i;
+          v[i] = (j <= r) ? v[i] * __expf(gr - gam[j]) : 0.f;
+        }
+        store_chunks(sm + kB_P, r, cg * 2, v, 2);
       }
     }
     cta_sync();
-    solve_unit_lower(Am, Tm, Sm);
+    solve_unit_lower_f(Am, Tm, Sm);
     {
-      const int r = tid >> 1, hf = tid & 1;
-      float v[32];
+      const int r = tid >> 3, c8 = tid & 7;
+      float v[8];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int j = hf * 32 + i;
-        v[i] = (j <= r) ? Tm[r * kLdA + j] : 0.f;
+      for (int i = 0; i < 8; ++i) {
+        const int j = c8 * 8 + i;
+        v[i] = (j <= r) ? Tm[r * kLdF + j] : 0.f;
       }
-#pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        uint4 pk;
-        uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          __nv_bfloat162 a = __floats2bfloat162_rn(v[c8 * 8 + 2 * i], v[c8 * 8 + 2 * i + 1]);
-          w[i] = *reinterpret_cast<uint32_t*>(&a);
-        }
-        *reinterpret_cast<uint4*>(sm + kB_T + sw_row_off(r, hf * 4 + c8)) = pk;
-      }
+      store_chunks(sm + kB_T, r, c8, v, 1);
     }
     fence_async_shared();
     cta_sync();
@@ -809,21 +816,21 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     mma_wait();
     if (!ok) break;
-    // ---- E3: beta R^T -> X0, dU^T -> X1
+    // ---- E3: beta R^T -> X0, dU^T -> X1  (this thread: row c, columns 16 cg + i)
     {
-      float a[64], x[64];
-      tmem_ld64(tmem + lb + kBtR, a);
+      float a[16], x[16];
+      tmem_ld16(tmem + lb + kBtR + cg * 16, a);
 #pragma unroll
-      for (int r = 0; r < 64; ++r) {
-        const float vr = r < n ? __bfloat162float(p.v[(((size_t)b * p.T + t0 + r) * p.H + h) * D + tid]) : 0.f;
-        a[r] = bt[r] * (vr + ee[r] * a[r]);
+      for (int i = 0; i < 16; ++i) {
+        const int r = cg * 16 + i;
+        a[i] = bt[r] * (tile_elem(sm + kB_V + (row >> 6) * 8192, r, row & 63) + ee[r] * a[i]);
       }
-      store_row64(sm + kB_X, tid, a);
-      tmem_ld64(tmem + lb + kBtX1, a);
-      tmem_ld64(tmem + lb + kBtX2, x);
+      store_chunks(sm + kB_X, row, cg * 2, a, 2);
+      tmem_ld16(tmem + lb + kBtX1 + cg * 16, a);
+      tmem_ld16(tmem + lb + kBtX2 + cg * 16, x);
 #pragma unroll
-      for (int j = 0; j < 64; ++j) a[j] = ff[j] * a[j] + x[j];
-      store_row64(sm + kB_X + 16384, tid, a);
+      for (int i = 0; i < 16; ++i) a[i] = ff[cg * 16 + i] * a[i] + x[i];
+      store_chunks(sm + kB_X + 16384, row, cg * 2, a, 2);
     }
     fence_async_shared();
     cta_sync();
@@ -842,33 +849,32 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     mma_wait();
     if (!ok) break;
     // ---- E4: U^T -> X0, (U diag f)^T -> X2, e dR^T -> X1, dZ rows -> ZO, dv, dbeta part 1
-    float acc[64];  // per-lane terms of the log-gate gradient (summed over lanes later)
+    float acc[16];  // this thread's terms of the log-gate gradient, columns 16 cg + i
     {
-      float u[64];
-      tmem_ld64(tmem + lb + kBtU, u);
-      store_row64(sm + kB_X, tid, u);
+      float u[16];
+      tmem_ld16(tmem + lb + kBtU + cg * 16, u);
+      store_chunks(sm + kB_X, row, cg * 2, u, 2);
 #pragma unroll
-      for (int j = 0; j < 64; ++j) u[j] *= ff[j];
-      store_row64(sm + kB_X + 32768, tid, u);
-      float z[64], rr[64];
-      tmem_ld64(tmem + lb + kBtZ, z);
-      tmem_ld64(tmem + lb + kBtR, rr);
+      for (int i = 0; i < 16; ++i) u[i] *= ff[cg * 16 + i];
+      store_chunks(sm + kB_X + 32768, row, cg * 2, u, 2);
+      float z[16], rr[16];
+      tmem_ld16(tmem + lb + kBtZ + cg * 16, z);
+      tmem_ld16(tmem + lb + kBtR + cg * 16, rr);
+      const int half = row >> 6, cc = row & 63;
 #pragma unroll
-      for (int r = 0; r < 64; ++r) {
-        const size_t off = (((size_t)b * p.T + t0 + r) * p.H + h) * D + tid;
-        const float vr = r < n ? __bfloat162float(p.v[off]) : 0.f;
-        const float dr = bt[r] * z[r];
-        if (r < n) p.dv[off] = __float2bfloat16_rn(dr);
-        acc[r] = -vr * dr;                       // -v . dv
-        rr[r] = z[r] * (vr + ee[r] * rr[r]);     // dZ_rc R_rc
-        // dZ row r, column c = tid, into the dZ half of the [dZ; dO] operand
-        const int half = tid >> 6, cc = tid & 63;
+      for (int i = 0; i < 16; ++i) {
+        const int r = cg * 16 + i;
+        const float vr = tile_elem(sm + kB_V + half * 8192, r, cc);
+        const float dr = bt[r] * z[i];
+        if (r < n) p.dv[(((size_t)b * p.T + t0 + r) * p.H + h) * D + row] = __float2bfloat16_rn(dr);
+        acc[i] = -vr * dr;                        // -v . dv
+        rr[i] = z[i] * (vr + ee[r] * rr[i]);      // dZ_rc R_rc
         *reinterpret_cast<__nv_bfloat16*>(sm + kB_ZO + half * 16384 + sw_row_off(r, cc >> 3) +
-                                          (cc & 7) * 2) = __float2bfloat16_rn(z[r]);
-        z[r] = ee[r] * dr;
+                                          (cc & 7) * 2) = __float2bfloat16_rn(z[i]);
+        z[i] = ee[r] * dr;
       }
-      store_row64(sm + kB_X + 16384, tid, z);
-      cta_sum64(rr, red, db1);
+      store_chunks(sm + kB_X + 16384, row, cg * 2, z, 2);
+      cta_sum_rows16(rr, red, db1);
     }
     fence_async_shared();
     cta_sync();
@@ -883,36 +889,38 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     mma_wait();
     if (!ok) break;
     {
-      float x[64];
-      tmem_ld64(tmem + lb + kBtX1, x);
-      if (tid < 64) {
+      float x[16];
+      tmem_ld16(tmem + lb + kBtX1 + cg * 16, x);
+      if (row < 64) {
         // dA = -strict_lower(dZ U^T); dbeta part 2; M = beta dA o Gam
-        const int r = tid;
-        float kk[64];
-        tmem_ld64(tmem + lb + kBtKQ, kk);
+        const int r = row;
+        float kk[16];
+        tmem_ld16(tmem + lb + kBtKQ + cg * 16, kk);
         const float gr = gam[r], br = bt[r];
         float s2 = 0.f;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const float w = (j < r) ? expf(gr - gam[j]) : 0.f;
-          const float da = -x[j];
-          s2 += da * kk[j] * w;
-          x[j] = br * da * w;
+        for (int i = 0; i < 16; ++i) {
+          const int j = cg * 16 + i;
+          const float w = (j < r) ? __expf(gr - gam[j]) : 0.f;
+          const float da = -x[i];
+          s2 += da * kk[i] * w;
+          x[i] = br * da * w;
         }
-        db2[r] = s2;
-        store_row64(sm + kB_M, r, x);
+        red[cg * 64 + r] = s2;
+        store_chunks(sm + kB_T, r, cg * 2, x, 2);
       } else {
-        const int r = tid - 64;
-        float kk[64];
-        tmem_ld64(tmem + lb + kBtKQ, kk);  // keep the warp-collective load uniform
+        const int r = row - 64;
         const float gr = gam[r];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) x[j] = (j <= r) ? x[j] * expf(gr - gam[j]) : 0.f;
-        store_row64(sm + kB_DP, r, x);
+        for (int i = 0; i < 16; ++i) {
+          const int j = cg * 16 + i;
+          x[i] = (j <= r) ? x[i] * __expf(gr - gam[j]) : 0.f;
+        }
+        store_chunks(sm + kB_P, r, cg * 2, x, 2);
       }
     }
     // scale dO rows by e in place (dO is done as an operand of dO^T P and G4)
-    for (int i = tid; i < 2 * 64 * 8; i += NT) {
+    for (int i = tid; i < 2 * 64 * 8; i += BT) {
       const int half = i / 512, r = (i / 8) % 64, c8 = i % 8;
       uint4* ptr = reinterpret_cast<uint4*>(sm + kB_ZO + half * 16384 + 8192 + r * 128 + c8 * 16);
       uint4 val = *ptr;
@@ -927,6 +935,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     fence_async_shared();
     cta_sync();
+    if (tid < 64) db2[tid] = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
     // ---- dG_in part, dQ^T, dK^T
     if (tid == 0) {
       // G3 = (e dO)^T Q - (e dR)^T K   [c x d]
@@ -972,77 +981,75 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     {
       const float ec = *eC;
       float v32[32];
+      tmem_ld32(tmem + lb + kBtG3 + cg * 32, v32);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        tmem_ld32(tmem + lb + kBtG3 + q4 * 32, v32);
+      for (int i = 0; i < 32; ++i) dG[i] = fmaf(ec, dG[i], v32[i]);
+      float x[16];
+      tmem_ld16(tmem + lb + kBtX2 + cg * 16, x);  // dQ^T row d = row, columns r = 16 cg + i
+      const int half = row >> 6, cc = row & 63;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) dG[q4 * 32 + i] = fmaf(ec, dG[q4 * 32 + i], v32[i]);
+      for (int i = 0; i < 16; ++i) {
+        const int r = cg * 16 + i;
+        acc[i] += tile_elem(sm + kB_KQ + half * 16384 + 8192, r, cc) * x[i];
+        if (r < n) p.dq[(((size_t)b * p.T + t0 + r) * p.H + h) * D + row] = __float2bfloat16_rn(x[i]);
       }
-      float x[64];
-      tmem_ld64(tmem + lb + kBtX2, x);  // dQ^T row d = tid
+      tmem_ld16(tmem + lb + kBtU + cg * 16, x);  // dK^T row d, columns j
 #pragma unroll
-      for (int r = 0; r < 64; ++r) {
-        const size_t off = (((size_t)b * p.T + t0 + r) * p.H + h) * D + tid;
-        // q from the K|Q tile: row r, column d = tid
-        const int half = tid >> 6, cc = tid & 63;
-        const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-            sm + kB_KQ + half * 16384 + 8192 + sw_row_off(r, cc >> 3) + (cc & 7) * 2));
-        acc[r] += qv * x[r];
-        if (r < n) p.dq[off] = __float2bfloat16_rn(x[r]);
+      for (int i = 0; i < 16; ++i) {
+        const int j = cg * 16 + i;
+        if (j < n) p.dk[(((size_t)b * p.T + t0 + j) * p.H + h) * D + row] = __float2bfloat16_rn(x[i]);
       }
-      tmem_ld64(tmem + lb + kBtU, x);  // dK^T row d = tid
-#pragma unroll
-      for (int j = 0; j < 64; ++j)
-        if (j < n) p.dk[(((size_t)b * p.T + t0 + j) * p.H + h) * D + tid] = __float2bfloat16_rn(x[j]);
     }
-    cta_sum64(acc, red, dlc);
+    cta_sum_rows16(acc, red, dlc);
     if (tid < 64) {
       const int r = tid;
       if (r < n) p.dbeta[((size_t)b * p.T + t0 + r) * p.H + h] = db1[r] + db2[r];
     }
     // <dH_in, H_in> of this chunk = <dH_out, H_out> of the chunk before it
     float dot = 0.f;
+    {
+      const unsigned char* tile = sm + kB_GI + g_region * 16384;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        const uint4 pk = *reinterpret_cast<const uint4*>(sm + kB_GI + half * 16384 + sw_row_off(tid, c8));
+      for (int k = 0; k < 4; ++k) {
+        const uint4 pk = *reinterpret_cast<const uint4*>(tile + sw_row_off(row, g_chunk0 + k));
         const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&pk);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float2 f2 = __bfloat1622float2(h2[i]);
-          dot = fmaf(dG[half * 64 + c8 * 8 + 2 * i], f2.x, dot);
-          dot = fmaf(dG[half * 64 + c8 * 8 + 2 * i + 1], f2.y, dot);
+          dot = fmaf(dG[k * 8 + 2 * i], f2.x, dot);
+          dot = fmaf(dG[k * 8 + 2 * i + 1], f2.y, dot);
         }
       }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-    if ((tid & 31) == 0) red[warp] = dot;
+    if (lane == 0) red[256 + warp] = dot;
     __syncthreads();
     if (warp == 0) {
       // dg_t = sum_{s >= t, s in chunk} (q_s.dq_s - v_s.dv_s) + <dH_out, H_out>
-      float a0 = dlc[tid], a1 = dlc[tid + 32];
+      float a0 = dlc[lane], a1 = dlc[lane + 32];
       float s1 = a1;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const float y = __shfl_down_sync(0xffffffffu, s1, off);
-        if (tid + off < 32) s1 += y;
+        if (lane + off < 32) s1 += y;
       }
       const float tot1 = __shfl_sync(0xffffffffu, s1, 0);
       float s0 = a0;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const float y = __shfl_down_sync(0xffffffffu, s0, off);
-        if (tid + off < 32) s0 += y;
+        if (lane + off < 32) s0 += y;
       }
       s0 += tot1;
       const size_t base = ((size_t)b * p.T + t0) * p.H + h;
-      if (tid < n) p.dg[base + (size_t)tid * p.H] = carry + s0;
-      if (tid + 32 < n) p.dg[base + (size_t)(tid + 32) * p.H] = carry + s1;
+      if (lane < n) p.dg[base + (size_t)lane * p.H] = carry + s0;
+      if (lane + 32 < n) p.dg[base + (size_t)(lane + 32) * p.H] = carry + s1;
     }
-    carry = red[0] + red[1] + red[2] + red[3];
-    store_g_tile(sm + kB_DG, dG, tid, nullptr);
+    carry = 0.f;
+#pragma unroll
+    for (int w = 0; w < BT / 32; ++w) carry += red[256 + w];
+    write_dg();
   }
 
   if (!ok) {
@@ -1050,7 +1057,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     mbar_wait(bar_load, load_phase, 1u << 20);
   } else if (p.dh0) {
 #pragma unroll
-    for (int d = 0; d < D; ++d) p.dh0[((size_t)bh * D + d) * D + tid] = dG[d];
+    for (int i = 0; i < 32; ++i) p.dh0[((size_t)bh * D + cg * 32 + i) * D + row] = dG[i];
   }
   cta_sync();
   if (warp == 0) tmem_dealloc(tmem, kTmCols);
@@ -1099,7 +1106,7 @@ cudaError_t launch_fwd(const Problem& p, cudaStream_t s, bool want_out, __nv_bfl
   e = cudaFuncSetAttribute(gdn_tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   prof_before(s);
-  gdn_tc_fwd_kernel<<<p.B * p.H, NT, kSmemBytes, s>>>(mq, mk, mv, fp);
+  gdn_tc_fwd_kernel<<<p.B * p.H, FT, kSmemBytes, s>>>(mq, mk, mv, fp);
   prof_after(s, want_out ? kTcFwd : kTcStates);
   return cudaGetLastError();
 }
@@ -1126,11 +1133,12 @@ cudaError_t tc_bwd(const Problem& p, cudaStream_t s) {
   float* dht_dot = reinterpret_cast<float*>(ws + align_up((size_t)p.B * p.H * p.N * 32768, 256));
   cudaError_t e = launch_fwd(p, s, false, states, dht_dot);
   if (e != cudaSuccess) return e;
-  CUtensorMap mq, mk, mdo;
+  CUtensorMap mq, mk, mv, mdo;
   if ((e = make_token_map(&mq, p.q, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mk, p.k, p)) != cudaSuccess) return e;
+  if ((e = make_token_map(&mv, p.v, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mdo, p.do_, p)) != cudaSuccess) return e;
-  BwdParams bp{p.g, p.beta, static_cast<const __nv_bfloat16*>(p.v), p.dht, dht_dot,
+  BwdParams bp{p.g, p.beta, p.dht, dht_dot,
                reinterpret_cast<const unsigned char*>(states), static_cast<__nv_bfloat16*>(p.dq),
                static_cast<__nv_bfloat16*>(p.dk_), static_cast<__nv_bfloat16*>(p.dv_), p.dg, p.dbeta,
                p.dh0, p.B, p.T, p.H, p.N};
@@ -1138,7 +1146,7 @@ cudaError_t tc_bwd(const Problem& p, cudaStream_t s) {
                            kBwdSmemBytes);
   if (e != cudaSuccess) return e;
   prof_before(s);
-  gdn_tc_bwd_kernel<<<p.B * p.H, NT, kBwdSmemBytes, s>>>(mq, mk, mdo, bp);
+  gdn_tc_bwd_kernel<<<p.B * p.H, BT, kBwdSmemBytes, s>>>(mq, mk, mv, mdo, bp);
   prof_after(s, kTcBwd);
   return cudaGetLastError();
 }
