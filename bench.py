@@ -240,6 +240,12 @@ def barrier(ws):
         dist.barrier()
 
 
+def aggregate_tokens_per_s(tokens_per_step, steps, world, slowest_rank_s):
+    """Whole-job throughput: every rank processes its own batch (weak scaling),
+    timed by the slowest rank."""
+    return tokens_per_step * steps * world / slowest_rank_s
+
+
 def max_over_ranks(x, ws, device):
     if ws == 1:
         return x
@@ -329,7 +335,7 @@ def run_ours(args):
     roof_step_s = max(step_bytes / (peaks["hbm_gbs"] * 1e9), step_flops / (peaks["bf16_tflops"] * 1e12))
 
     tokens_step = w.B * w.T
-    value = tokens_step * K * ws / dev_s_max
+    value = aggregate_tokens_per_s(tokens_step, K, ws, dev_s_max)
     ms_step = dev_s_max * 1e3 / K
 
     e2e = None
