@@ -15,7 +15,7 @@
 //         T' = T diag(beta e),  T'' = T diag(beta)
 //   MMA2  W^T  = K^T T'^T                       (W = T diag(beta e) K)
 //   MMA3  U^T  = V^T T''^T - G W^T              (U = T diag(beta)(V - eK H))
-//   MMA4  O^T  = G (eQ)^T + U^T P^T             (O = diag(e) Q H + P U)
+//   MMA4  O    = (eQ) G^T + P U                 (M = 64: rows are tokens)
 //   MMA5  dG   = (U diag(f))^T K                (G' = eC G + dG)
 //
 // Every product has M = 128.  The TMA tiles of K and V serve both as K-major
@@ -54,32 +54,31 @@ using namespace tc;
 constexpr int C = 64;     // chunk
 constexpr int D = 128;    // dk = dv
 
-// ---------------------------------------------------------------- shared memory map
-// Offsets in bytes from a 1024-aligned base.  Stage s (double buffer) holds
-// [K d0-63 | Q d0-63 | K d64-127 | Q d64-127] (8 KB each) then [V d0-63 | V d64-127].
-constexpr int kStageKQ = 0;
-constexpr int kStageV = 32768;
-constexpr int kStageBytes = 49152;
-constexpr int kOffStage0 = 0;
-constexpr int kOffG = 2 * kStageBytes;          // G bf16, K-major [c][d], 2 x 16 KB
-constexpr int kOffT1 = kOffG + 32768;           // T' [r][j] K-major          (8 KB)
-constexpr int kOffT2 = kOffT1 + 8192;           // T'' [r][j]                  (8 KB)
-constexpr int kOffP = kOffT2 + 8192;            // P [r][j]                    (8 KB)
-constexpr int kOffW = kOffP + 8192;             // W, MN-major rows d, 64 r   (16 KB)
-constexpr int kOffU = kOffW + 16384;            // U^T [c][j] K-major          (16 KB)
-constexpr int kOffUf = kOffU + 16384;           // (U diag f)^T [c][j]         (16 KB)
-// The fp32 solve scratch (A, T [64][65] and S [3][16][16]) aliases W / U / Uf:
-// those are written only after the solve and its T', T'' outputs are done.
-constexpr int kOffSolve = kOffW;
-constexpr int kSolveBytes = (2 * 64 * 68 + 3 * 256) * 4;   // A, T [64][68] fp32 + S
-static_assert(kSolveBytes <= 3 * 16384, "solve scratch must fit in W/U/Uf");
-constexpr int kOffGate = kOffUf + 16384;         // gam, e, f, beta [64] each, eC
-constexpr int kOffBar = kOffGate + 4 * 64 * 4 + 64;
-constexpr int kSmemBytes = kOffBar + 128 + 1024;  // + alignment slack
+// ---------------------------------------------------------------- forward shared memory
+// Offsets in bytes from a 1024-aligned base.  Two K|Q stages hold
+// [K d0-63 | Q d0-63 | K d64-127 | Q d64-127] (8 KB each) so that [K;Q] is one
+// 128-row operand; V is single-buffered (only the preparation reads it).
+constexpr int kLdF = 68;                   // fp32 row stride of the solve scratch (16-byte rows)
+constexpr int kF_KQ = 0;                   // 2 x 32 KB
+constexpr int kF_V = 65536;                // 16 KB
+constexpr int kF_G = 81920;                // G bf16, K-major [c][d], 2 x 16 KB
+constexpr int kF_W = 114688;               // W, MN-major rows d, 64 r   (16 KB)
+constexpr int kF_P = 131072;               // 2 x P [r][j]                (8 KB each)
+constexpr int kF_T1 = 147456;              // T' = T diag(beta e) [r][j]  (8 KB)
+constexpr int kF_T0 = 155648;              // T'' = T diag(beta) [r][j]   (8 KB)
+constexpr int kF_U = 163840;               // U^T [c][j] K-major          (16 KB)
+constexpr int kF_SOLVE = 180224;           // A, T fp32 [64][kLdF] + S [3][16][16]
+constexpr int kSolveBytes = (2 * 64 * kLdF + 3 * 256) * 4;
+constexpr int kF_GATE = kF_SOLVE + kSolveBytes;
+constexpr int kGateBlock = 1600;           // gamma, e, f, beta, er, ie [64] each, eC, fast; two blocks
+constexpr int kF_BAR = kF_GATE + 2 * kGateBlock;
+constexpr int kSmemBytes = kF_BAR + 128 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
-// TMEM columns
-constexpr uint32_t kTmKQ = 0, kTmW = 64, kTmU = 128, kTmO = 192, kTmG = 256, kTmCols = 512;
+// TMEM columns of the forward kernel: K K^T | Q K^T, W^T, two U^T buffers,
+// O (M = 64 rows: token r in lane 32 (r / 16) + r % 16, 128 columns) and the
+// fp32 state G (128 columns).
+constexpr uint32_t kTmKQ = 0, kTmW = 64, kTmU0 = 128, kTmO = 256, kTmG = 384, kTmCols = 512;
 
 struct FwdParams {
   const float* g;
@@ -110,18 +109,25 @@ __device__ __forceinline__ void report_timeout() { atomicExch(&g_device_status, 
 
 // ---------------------------------------------------------------- forward kernel
 //
-// 512 threads: warp w reads TMEM lane quadrant q = w % 4 (lanes 32q..32q+31)
-// and handles column group cg = w / 4 of every tile, so each epilogue is split
-// four ways and every scheduler has four warps.  Thread (row, cg) owns
-// columns [32 cg, 32 cg + 32) of state row `row`.
+// Warp-specialised, 512 threads.  Warps 0-7 (the chain group) run the
+// state-dependent part of chunk c: MMA3b/MMA4a, U^T, MMA4b/MMA5, the output
+// and the next state tile.  Warps 8-15 (the preparation group) meanwhile run
+// the state-independent part of chunk c+1: MMA1, A and P, the triangular
+// solve, T' and T'', the row scalings (eQ, fK), MMA2/MMA3a and W.
+// Warp w reads TMEM lane quadrant w % 4 and handles column half (w / 4) % 2
+// of every tile.  Hand-offs use mbarriers; each group synchronises internally
+// with its own named barrier.  The fp32 state lives in TMEM: before MMA5 the
+// chain scales it by eC and MMA5 accumulates (U diag f)^T K onto it.
 
-constexpr int FT = 512;              // forward threads
-constexpr int kLdF = 68;             // fp32 row stride of the solve scratch (16-byte rows)
+constexpr int FT = 512;
+constexpr int kGroup = 256;
+constexpr int kBarChain = 1, kBarPrep = 2;
 
-// 64-element row chunk helpers: write n16 groups of 8 bf16 (16 B) of a
-// swizzled 128-byte row, starting at 16-byte chunk c0.
+// 64-element row chunk helper: writes nchunks groups of 8 bf16 (16 B) of a
+// swizzled 128-byte row, starting at 16-byte chunk c0 (and the same bytes to
+// dst if given).
 __device__ __forceinline__ void store_chunks(unsigned char* tile, int row, int c0, const float* v,
-                                             int nchunks) {
+                                             int nchunks, unsigned char* dst = nullptr) {
   for (int k = 0; k < nchunks; ++k) {
     uint4 pk;
     uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
@@ -130,56 +136,196 @@ __device__ __forceinline__ void store_chunks(unsigned char* tile, int row, int c
       __nv_bfloat162 b2 = __floats2bfloat162_rn(v[k * 8 + 2 * i], v[k * 8 + 2 * i + 1]);
       w[i] = *reinterpret_cast<uint32_t*>(&b2);
     }
-    *reinterpret_cast<uint4*>(tile + sw_row_off(row, c0 + k)) = pk;
+    const int off = sw_row_off(row, c0 + k);
+    *reinterpret_cast<uint4*>(tile + off) = pk;
+    if (dst) *reinterpret_cast<uint4*>(dst + off) = pk;
   }
 }
 
+// Scales each 128-byte bf16 row r of `rows` consecutive rows by s[r]
+// (16-byte chunks spread over nth threads; t = this thread's index).
+__device__ __forceinline__ void scale_rows(unsigned char* base, int rows, const float* s, int t,
+                                           int nth) {
+  for (int i = t; i < rows * 8; i += nth) {
+    const int r = i >> 3;
+    uint4* ptr = reinterpret_cast<uint4*>(base + i * 16);
+    uint4 val = *ptr;
+    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&val);
+    const float e = s[r];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float2 f2 = __bfloat1622float2(h2[k]);
+      h2[k] = __floats2bfloat162_rn(f2.x * e, f2.y * e);
+    }
+    *ptr = val;
+  }
+}
+
+// One level of the blocked inverse: for the nb = 4 - L blocks (ib, jb = ib - L),
+// S = sum_{kb=jb}^{ib-1} A[ib][kb] T[kb][jb], then T[ib][jb] = -T[ib][ib] S.
+// Work item = (block, row, 4 columns); k loops are fully unrolled with float4
+// loads so that the shared-memory latency overlaps.
+template <int L, class Sync>
+__device__ __forceinline__ void solve_level(const float* A, float* T, float* S, int t, int nth,
+                                            Sync sync) {
+  constexpr int kItems = (4 - L) * 64;
+  for (int it = t; it < kItems; it += nth) {
+    const int b = it >> 6, r = (it >> 2) & 15, c4 = (it & 3) * 4;
+    const int ib = b + L, jb = b;
+    const float* arow = A + (ib * 16 + r) * kLdF + jb * 16;
+    const float* tcol = T + (jb * 16) * kLdF + jb * 16 + c4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 16 * L; ++k) {
+      const float a = arow[k];
+      const float4 tv = *reinterpret_cast<const float4*>(tcol + k * kLdF);
+      acc.x = fmaf(a, tv.x, acc.x);
+      acc.y = fmaf(a, tv.y, acc.y);
+      acc.z = fmaf(a, tv.z, acc.z);
+      acc.w = fmaf(a, tv.w, acc.w);
+    }
+    *reinterpret_cast<float4*>(S + b * 256 + r * 16 + c4) = acc;
+  }
+  sync();
+  for (int it = t; it < kItems; it += nth) {
+    const int b = it >> 6, r = (it >> 2) & 15, c4 = (it & 3) * 4;
+    const int ib = b + L, jb = b;
+    const float* trow = T + (ib * 16 + r) * kLdF + ib * 16;  // zero above the diagonal
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float a = trow[k];
+      const float4 sv = *reinterpret_cast<const float4*>(S + b * 256 + k * 16 + c4);
+      acc.x = fmaf(a, sv.x, acc.x);
+      acc.y = fmaf(a, sv.y, acc.y);
+      acc.z = fmaf(a, sv.z, acc.z);
+      acc.w = fmaf(a, sv.w, acc.w);
+    }
+    *reinterpret_cast<float4*>(T + (ib * 16 + r) * kLdF + jb * 16 + c4) =
+        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  }
+  sync();
+}
+
 // T = (I + A)^-1 for a 64 x 64 strictly lower A (fp32, row stride kLdF), by
-// 16 x 16 blocks; all FT threads take part.
-__device__ void solve_unit_lower_f(const float* A, float* T, float* S) {
-  const int tid = threadIdx.x;
-  if (tid < 64) {
-    const int ib = tid / 16, jj = tid % 16, o = ib * 16;
+// 16 x 16 blocks: the diagonal blocks by forward substitution (one thread per
+// column), then three levels of block products.  nth threads take part
+// (t = this thread's index); sync() is their barrier.
+template <class Sync>
+__device__ void solve_unit_lower(const float* A, float* T, float* S, int t, int nth, Sync sync) {
+  if (t < 64) {
+    // column jj of the inverse of diagonal block ib: x_r = -sum_{i<r} A[r][i] x_i,
+    // x_jj = 1, x_r = 0 above jj (so the sum may run over every i < r and all
+    // 16 lanes of a block execute the same instructions)
+    const int ib = t / 16, jj = t % 16, o = ib * 16;
     float x[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-      float s = (r == jj) ? 1.f : 0.f;
-      if (r > jj) {
+      float a[16];
 #pragma unroll
-        for (int i = 0; i < r; ++i)
-          if (i >= jj) s -= A[(o + r) * kLdF + o + i] * x[i];
+      for (int q = 0; q < 4; ++q) {
+        const float4 v4 = *reinterpret_cast<const float4*>(A + (o + r) * kLdF + o + 4 * q);
+        a[4 * q] = v4.x, a[4 * q + 1] = v4.y, a[4 * q + 2] = v4.z, a[4 * q + 3] = v4.w;
       }
-      x[r] = (r >= jj) ? s : 0.f;
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+      for (int i = 0; i < r; ++i) {
+        if ((i & 3) == 0) s0 = fmaf(a[i], x[i], s0);
+        if ((i & 3) == 1) s1 = fmaf(a[i], x[i], s1);
+        if ((i & 3) == 2) s2 = fmaf(a[i], x[i], s2);
+        if ((i & 3) == 3) s3 = fmaf(a[i], x[i], s3);
+      }
+      const float s = -((s0 + s1) + (s2 + s3));
+      x[r] = (r == jj) ? 1.f : ((r > jj) ? s : 0.f);
     }
 #pragma unroll
     for (int r = 0; r < 16; ++r) T[(o + r) * kLdF + o + jj] = x[r];
   } else {
-    // zero the strictly upper blocks (never read as T, but keep T well defined)
-    for (int i = tid - 64; i < 64 * 64; i += FT - 64) {
+    for (int i = t - 64; i < 64 * 64; i += nth - 64) {
       const int r = i / 64, c = i % 64;
       if ((c / 16) > (r / 16)) T[r * kLdF + c] = 0.f;
     }
   }
-  __syncthreads();
-  for (int L = 1; L < 4; ++L) {
-    const int nb = 4 - L;
-    for (int i = tid; i < nb * 256; i += FT) {
-      const int b = i / 256, r = (i / 16) % 16, c = i % 16;
-      const int ib = b + L, jb = b;
-      float s = 0.f;
-      for (int k = jb * 16; k < ib * 16; ++k) s += A[(ib * 16 + r) * kLdF + k] * T[k * kLdF + jb * 16 + c];
-      S[b * 256 + r * 16 + c] = s;
-    }
-    __syncthreads();
-    for (int i = tid; i < nb * 256; i += FT) {
-      const int b = i / 256, r = (i / 16) % 16, c = i % 16;
-      const int ib = b + L, jb = b;
-      float s = 0.f;
-      for (int k = 0; k <= r; ++k) s += T[(ib * 16 + r) * kLdF + ib * 16 + k] * S[b * 256 + k * 16 + c];
-      T[(ib * 16 + r) * kLdF + jb * 16 + c] = -s;
-    }
-    __syncthreads();
+  sync();
+  solve_level<1>(A, T, S, t, nth, sync);
+  solve_level<2>(A, T, S, t, nth, sync);
+  solve_level<3>(A, T, S, t, nth, sync);
+}
+
+
+// Gates of one chunk, computed by one warp from the lane's two log gates
+// (rows lane and lane + 32) and betas: gamma = inclusive cumsum of g,
+// e = exp(gamma), f = exp(gamma_last - gamma), eC = exp(gamma_last).  For the
+// decay factors Gam[r][j] = exp(gamma_r - gamma_j) it also writes
+// er = exp(gamma - gref) and ie = exp(gref - gamma) with gref the middle of
+// the chunk's gamma range; when that range is below 80 the product er_r ie_j
+// equals Gam[r][j] without overflow and *fast is set, otherwise the exact
+// per-element exponential is used.
+struct GateView {
+  float *gam, *ee, *ff, *bt, *er, *ie, *eC, *fast;
+};
+
+__device__ __forceinline__ void chunk_gates(const GateView& G, float g0, float g1, float b0,
+                                            float b1, int lane) {
+  G.bt[lane] = b0;
+  G.bt[lane + 32] = b1;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float a0 = __shfl_up_sync(0xffffffffu, g0, off);
+    const float a1 = __shfl_up_sync(0xffffffffu, g1, off);
+    if (lane >= off) g0 += a0, g1 += a1;
   }
+  g1 += __shfl_sync(0xffffffffu, g0, 31);
+  const float gl = __shfl_sync(0xffffffffu, g1, 31);
+  float mx = fmaxf(g0, g1), mn = fminf(g0, g1);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+  }
+  const float gref = 0.5f * (mx + mn);
+  G.gam[lane] = g0;
+  G.gam[lane + 32] = g1;
+  G.ee[lane] = __expf(g0);
+  G.ee[lane + 32] = __expf(g1);
+  G.ff[lane] = __expf(gl - g0);
+  G.ff[lane + 32] = __expf(gl - g1);
+  G.er[lane] = __expf(g0 - gref);
+  G.er[lane + 32] = __expf(g1 - gref);
+  G.ie[lane] = __expf(gref - g0);
+  G.ie[lane + 32] = __expf(gref - g1);
+  if (lane == 0) {
+    *G.eC = __expf(gl);
+    *G.fast = (mx - mn < 80.f) ? 1.f : 0.f;
+  }
+}
+
+// Decayed row: v[i] <- v[i] * Gam[r][j0 + i] for j0 + i <= r (or < r when
+// strict), 0 above; n columns.
+template <int n>
+__device__ __forceinline__ void decay_row(float (&v)[n], const GateView& G, int r, int j0,
+                                          bool strict, float scale) {
+  if (*G.fast != 0.f) {
+    const float a = G.er[r] * scale;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+      const int j = j0 + i;
+      v[i] = (strict ? j < r : j <= r) ? v[i] * a * G.ie[j] : 0.f;
+    }
+  } else {
+    const float gr = G.gam[r];
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+      const int j = j0 + i;
+      v[i] = (strict ? j < r : j <= r) ? scale * v[i] * __expf(gr - G.gam[j]) : 0.f;
+    }
+  }
+}
+
+__device__ __forceinline__ void group_sync_tc(int id) {
+  tc_fence_before();
+  group_sync(id, kGroup);
+  tc_fence_after();
 }
 
 __global__ void __launch_bounds__(FT, 1)
@@ -189,26 +335,27 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
-  const int quad = warp & 3, cg = warp >> 2;
+  const int quad = warp & 3, half = (warp >> 2) & 1, grp = warp >> 3;
   const int row = quad * 32 + lane;    // TMEM lane / tile row owned by this thread
   const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
 
-  float* gam = reinterpret_cast<float*>(sm + kOffGate);
-  float* ee = gam + 64;
-  float* ff = ee + 64;
-  float* bt = ff + 64;
-  float* eC = bt + 64;
-  uint64_t* bar_load = reinterpret_cast<uint64_t*>(sm + kOffBar);  // [2]
-  uint64_t* bar_mma = bar_load + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma + 1);
-  float* Am = reinterpret_cast<float*>(sm + kOffSolve);
+  uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + kF_BAR);  // [2] K|Q stage loaded
+  uint64_t* bar_v = bar_kq + 2;                                  // V loaded
+  uint64_t* bar_p = bar_kq + 3;                                  // preparation MMAs done
+  uint64_t* bar_s = bar_kq + 4;                                  // chain MMAs done
+  uint64_t* bar_pd = bar_kq + 5;                                 // preparation of a chunk done
+  uint64_t* bar_wf = bar_kq + 6;                                 // W tile free again
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_kq + 7);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* cnt = reinterpret_cast<int*>(tmem_slot + 2);  // [0..1] kq issued, [2..3] kq waited, [4] v issued, [5] v waited
+  float* Am = reinterpret_cast<float*>(sm + kF_SOLVE);
   float* Tm = Am + 64 * kLdF;
   float* Sm = Tm + 64 * kLdF;
 
   if (tid == 0) {
-    mbar_init(&bar_load[0], 1);
-    mbar_init(&bar_load[1], 1);
-    mbar_init(bar_mma, 1);
+    for (int i = 0; i < 7; ++i) mbar_init(&bar_kq[i], 1);
+    *abort_flag = 0;
+    for (int i = 0; i < 6; ++i) cnt[i] = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -222,17 +369,23 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const uint32_t tmem = *tmem_slot;
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
 
-  auto issue_load = [&](int ci) {
-    unsigned char* st = sm + kOffStage0 + (ci & 1) * kStageBytes;
-    uint64_t* bar = &bar_load[ci & 1];
-    mbar_arrive_expect_tx(bar, 6 * 8192);
+  auto load_kq = [&](int ci) {
+    const int st = ci & 1;
+    unsigned char* dst = sm + kF_KQ + st * 32768;
+    mbar_arrive_expect_tx(&bar_kq[st], 32768);
     const int t0 = ci * C;
-    tma_load_4d(st + kStageKQ + 0, &tm_k, bar, 0, h, t0, b);
-    tma_load_4d(st + kStageKQ + 8192, &tm_q, bar, 0, h, t0, b);
-    tma_load_4d(st + kStageKQ + 16384, &tm_k, bar, 64, h, t0, b);
-    tma_load_4d(st + kStageKQ + 24576, &tm_q, bar, 64, h, t0, b);
-    tma_load_4d(st + kStageV + 0, &tm_v, bar, 0, h, t0, b);
-    tma_load_4d(st + kStageV + 8192, &tm_v, bar, 64, h, t0, b);
+    tma_load_4d(dst + 0, &tm_k, &bar_kq[st], 0, h, t0, b);
+    tma_load_4d(dst + 8192, &tm_q, &bar_kq[st], 0, h, t0, b);
+    tma_load_4d(dst + 16384, &tm_k, &bar_kq[st], 64, h, t0, b);
+    tma_load_4d(dst + 24576, &tm_q, &bar_kq[st], 64, h, t0, b);
+    cnt[st] += 1;
+  };
+  auto load_v = [&](int ci) {
+    mbar_arrive_expect_tx(bar_v, 16384);
+    const int t0 = ci * C;
+    tma_load_4d(sm + kF_V, &tm_v, bar_v, 0, h, t0, b);
+    tma_load_4d(sm + kF_V + 8192, &tm_v, bar_v, 64, h, t0, b);
+    cnt[4] += 1;
   };
   auto state_dst = [&](int ci) -> unsigned char* {
     return p.states ? reinterpret_cast<unsigned char*>(p.states) +
@@ -240,269 +393,312 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     : nullptr;
   };
   const bool want_o = p.o != nullptr;
-  // this thread's 32 state columns: d in [32 cg, 32 cg + 32) = tile region cg/2, chunks 4(cg%2)..
-  const int g_region = cg >> 1, g_chunk0 = (cg & 1) * 4;
-  auto write_g = [&](const float* Gv, unsigned char* dst) {
-    unsigned char* tile = sm + kOffG + g_region * 16384;
-    for (int k = 0; k < 4; ++k) {
-      uint4 pk;
-      uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(Gv[k * 8 + 2 * i], Gv[k * 8 + 2 * i + 1]);
-        w[i] = *reinterpret_cast<uint32_t*>(&b2);
-      }
-      const int off = sw_row_off(row, g_chunk0 + k);
-      *reinterpret_cast<uint4*>(tile + off) = pk;
-      if (dst) *reinterpret_cast<uint4*>(dst + g_region * 16384 + off) = pk;
-    }
-  };
 
-  float G[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i)
-    G[i] = p.h0 ? p.h0[((size_t)bh * D + cg * 32 + i) * D + row] : 0.f;
-  write_g(G, state_dst(0));
-
-  // gate prefetch (warp 0): registers for the next chunk
-  float pg0 = 0.f, pg1 = 0.f, pb0 = 0.f, pb1 = 0.f;
-  auto load_gates = [&](int ci) {
-    const int t0 = ci * C, n = min(C, p.T - t0);
-    const size_t base = ((size_t)b * p.T + t0) * p.H + h;
-    pg0 = lane < n ? p.g[base + (size_t)lane * p.H] : 0.f;
-    pg1 = lane + 32 < n ? p.g[base + (size_t)(lane + 32) * p.H] : 0.f;
-    pb0 = lane < n ? p.beta[base + (size_t)lane * p.H] : 0.f;
-    pb1 = lane + 32 < n ? p.beta[base + (size_t)(lane + 32) * p.H] : 0.f;
-  };
-  if (warp == 0) load_gates(0);
-  fence_async_shared();
-  if (tid == 0) issue_load(0);
-  cta_sync();
-
-  uint32_t mma_phase = 0;
-  uint32_t load_phase[2] = {0, 0};
+  if (tid == 0) {
+    load_kq(0);
+    if (p.N > 1) load_kq(1);
+    load_v(0);
+  }
   bool ok = true;
-  auto mma_wait = [&]() {
-    ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
-    mma_phase ^= 1;
-    tc_fence_after();
-  };
 
-  for (int ci = 0; ci < p.N && ok; ++ci) {
-    const int s = ci & 1, t0 = ci * C, n = min(C, p.T - t0);
-    unsigned char* st = sm + kOffStage0 + s * kStageBytes;
-    const uint32_t st_kq = smem_u32(st + kStageKQ), st_v = smem_u32(st + kStageV);
-
-    if (warp == 0) {
-      float g0 = pg0, g1 = pg1;
-      bt[lane] = pb0;
-      bt[lane + 32] = pb1;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        float a0 = __shfl_up_sync(0xffffffffu, g0, off);
-        float a1 = __shfl_up_sync(0xffffffffu, g1, off);
-        if (lane >= off) g0 += a0, g1 += a1;
-      }
-      g1 += __shfl_sync(0xffffffffu, g0, 31);
-      const float gl = __shfl_sync(0xffffffffu, g1, 31);
-      gam[lane] = g0;
-      gam[lane + 32] = g1;
-      ee[lane] = __expf(g0);
-      ee[lane + 32] = __expf(g1);
-      ff[lane] = __expf(gl - g0);
-      ff[lane + 32] = __expf(gl - g1);
-      if (lane == 0) *eC = __expf(gl);
-      if (ci + 1 < p.N) load_gates(ci + 1);
-    }
-    ok = __syncthreads_and(mbar_wait(&bar_load[s], load_phase[s]));
-    load_phase[s] ^= 1;
-    if (!ok) break;
-    if (tid == 0) {
-      // MMA1: [K;Q] K^T, M=128 N=64 K=128
-      const uint32_t idesc = idesc_bf16(128, 64, false, false);
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
-        mma_bf16(tmem + kTmKQ, sw128_desc(st_kq + off, 16, 1024), sw128_desc(st_kq + off, 16, 1024),
-                 idesc, ks > 0);
-      }
-      mma_commit(bar_mma);
-      if (ci + 1 < p.N) issue_load(ci + 1);
-    }
-    mma_wait();
-    if (!ok) break;
-
-    // E1: rows 0-63: A (fp32); rows 64-127: P (bf16); this thread: 16 columns
+  if (grp == 0) {
+    // ============================== chain group ==============================
+    const int gt = tid;
+    // initial state: fp32 in TMEM and the bf16 tile; this thread: d in [64 half, 64 half + 64)
     {
-      float v[16];
-      tmem_ld16(tmem + lane_base + kTmKQ + cg * 16, v);
-      if (row < 64) {
-        const int r = row;
-        const float gr = gam[r], br = bt[r];
+      float v[32];
+#pragma unroll
+      for (int q32 = 0; q32 < 2; ++q32) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          v[i] = p.h0 ? p.h0[((size_t)bh * D + half * 64 + q32 * 32 + i) * D + row] : 0.f;
+        tmem_st32(tmem + lane_base + kTmG + half * 64 + q32 * 32, v);
+        unsigned char* dst0 = state_dst(0);
+        store_chunks(sm + kF_G + half * 16384, row, q32 * 4, v, 4,
+                     dst0 ? dst0 + half * 16384 : nullptr);
+      }
+    }
+    fence_async_shared();
+    group_sync_tc(kBarChain);
+    uint32_t s_phase = 0;
+    for (int ci = 0; ci < p.N; ++ci) {
+      const int s = ci & 1, t0 = ci * C, n = min(C, p.T - t0);
+      const float* gates = reinterpret_cast<const float*>(sm + kF_GATE + s * kGateBlock);  // eC at [384]
+      ok = group_and(kBarChain, kGroup, mbar_wait(bar_pd, ci & 1) && !*abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      {
+        // G <- eC G  (MMA5 accumulates onto it)
+        const float ec = gates[384];
+        float v[32];
+#pragma unroll
+        for (int q32 = 0; q32 < 2; ++q32) {
+          const uint32_t ta = tmem + lane_base + kTmG + half * 64 + q32 * 32;
+          tmem_ld32(ta, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= ec;
+          tmem_st32(ta, v);
+        }
+      }
+      group_sync_tc(kBarChain);
+      const uint32_t st_kq = smem_u32(sm + kF_KQ + s * 32768);
+      const uint32_t tmU = kTmU0 + 64 * s;
+      if (gt == 0) {
+        // MMA3b: U^T += -G W^T (A: G K-major M=c K=d; B: W MN-major N=r K=d)
+        const uint32_t id3 = idesc_bf16(128, 64, false, true, true);
+        for (int ks = 0; ks < 8; ++ks)
+          mma_bf16(tmem + tmU, sw128_desc(smem_u32(sm + kF_G) + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024),
+                   sw128_desc(smem_u32(sm + kF_W) + ks * 2048, 16384, 1024), id3, 1);
+        // MMA4a: O = (eQ) G^T  (M=64: A = eQ rows r, K=d; B = G tile rows c, K=d)
+        const uint32_t id4 = idesc_bf16(64, 128, false, false);
+        for (int ks = 0; ks < (want_o ? 8 : 0); ++ks) {
+          const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
+          mma_bf16(tmem + kTmO, sw128_desc(st_kq + 8192 + off, 16, 1024),
+                   sw128_desc(smem_u32(sm + kF_G) + off, 16, 1024), id4, ks > 0);
+        }
+        mma_commit(bar_s);
+      }
+      ok = group_and(kBarChain, kGroup, mbar_wait(bar_s, s_phase));
+      s_phase ^= 1;
+      tc_fence_after();
+      if (!ok) break;
+      if (gt == 0) mbar_arrive(bar_wf);  // W may be overwritten by the next preparation
+      {
+        float u[32];
+        tmem_ld32(tmem + lane_base + tmU + half * 32, u);
+        store_chunks(sm + kF_U, row, half * 4, u, 4);
+      }
+      fence_async_shared();
+      group_sync_tc(kBarChain);
+      if (gt == 0) {
+        // MMA4b: O += P U  (A = P rows r, K=j; B = U^T tile rows c, K=j)
+        const uint32_t id4 = idesc_bf16(64, 128, false, false);
+        for (int ks = 0; ks < (want_o ? 4 : 0); ++ks)
+          mma_bf16(tmem + kTmO, sw128_desc(smem_u32(sm + kF_P + s * 8192) + ks * 32, 16, 1024),
+                   sw128_desc(smem_u32(sm + kF_U) + ks * 32, 16, 1024), id4, 1);
+        // MMA5: G += U^T (f K)  (B: K tile, rows scaled by f, MN-major N=d, K=j)
+        const uint32_t id5 = idesc_bf16(128, 128, false, true);
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem + kTmG, sw128_desc(smem_u32(sm + kF_U) + ks * 32, 16, 1024),
+                   sw128_desc(st_kq + ks * 2048, 16384, 1024), id5, 1);
+        mma_commit(bar_s);
+      }
+      ok = group_and(kBarChain, kGroup, mbar_wait(bar_s, s_phase));
+      s_phase ^= 1;
+      tc_fence_after();
+      if (!ok) break;
+      if (gt == 0 && ci + 2 < p.N) load_kq(ci + 2);  // this stage is no longer read
+      if (want_o) {
+        // O row r = 16 quad + lane (lanes 0-15 of each quadrant), columns 64 half + [0, 64)
+        const int r = quad * 16 + lane;
+        __nv_bfloat16* orow = p.o + (((size_t)b * p.T + t0 + r) * p.H + h) * D + half * 64;
+#pragma unroll
+        for (int q32 = 0; q32 < 2; ++q32) {
+          float v[32];
+          tmem_ld32(tmem + lane_base + kTmO + half * 64 + q32 * 32, v);
+          if (lane < 16 && r < n) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint4 pk;
+              uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(v[k * 8 + 2 * i], v[k * 8 + 2 * i + 1]);
+                w[i] = *reinterpret_cast<uint32_t*>(&b2);
+              }
+              *reinterpret_cast<uint4*>(orow + q32 * 32 + k * 8) = pk;
+            }
+          }
+        }
+      }
+      {
+        unsigned char* dst = ci + 1 < p.N ? state_dst(ci + 1) : nullptr;
+        float v[32];
+#pragma unroll
+        for (int q32 = 0; q32 < 2; ++q32) {
+          tmem_ld32(tmem + lane_base + kTmG + half * 64 + q32 * 32, v);
+          store_chunks(sm + kF_G + half * 16384, row, q32 * 4, v, 4, dst ? dst + half * 16384 : nullptr);
+        }
+      }
+      fence_async_shared();
+      group_sync_tc(kBarChain);
+    }
+    if (!ok) *abort_flag = 1;
+    if (ok) {
+      float v[32];
+      float acc = 0.f;
+#pragma unroll
+      for (int q32 = 0; q32 < 2; ++q32) {
+        tmem_ld32(tmem + lane_base + kTmG + half * 64 + q32 * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const size_t off = ((size_t)bh * D + half * 64 + q32 * 32 + i) * D + row;
+          if (p.ht) p.ht[off] = v[i];
+          if (p.dht) acc += p.dht[off] * v[i];
+        }
+      }
+      if (p.dht_dot) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        float* red = Sm;  // the solve scratch is idle once the preparation group is done
+        group_sync(kBarChain, kGroup);
+        if (lane == 0) red[warp] = acc;
+        group_sync(kBarChain, kGroup);
+        if (gt == 0) {
+          float t = 0.f;
+          for (int w = 0; w < 8; ++w) t += red[w];
+          p.dht_dot[bh] = t;
+        }
+      }
+    }
+  } else {
+    // =========================== preparation group ===========================
+    const int pt = tid - kGroup;
+    auto psync = [&]() { group_sync(kBarPrep, kGroup); };
+    float pg0 = 0.f, pg1 = 0.f, pb0 = 0.f, pb1 = 0.f;
+    auto load_gates = [&](int ci) {
+      const int t0 = ci * C, n = min(C, p.T - t0);
+      const size_t base = ((size_t)b * p.T + t0) * p.H + h;
+      pg0 = lane < n ? p.g[base + (size_t)lane * p.H] : 0.f;
+      pg1 = lane + 32 < n ? p.g[base + (size_t)(lane + 32) * p.H] : 0.f;
+      pb0 = lane < n ? p.beta[base + (size_t)lane * p.H] : 0.f;
+      pb1 = lane + 32 < n ? p.beta[base + (size_t)(lane + 32) * p.H] : 0.f;
+    };
+    if (warp == 8) load_gates(0);
+    uint32_t p_phase = 0;
+    for (int ci = 0; ci < p.N; ++ci) {
+      const int s = ci & 1;
+      float* gates = reinterpret_cast<float*>(sm + kF_GATE + s * kGateBlock);
+      const GateView GV{gates, gates + 64, gates + 128, gates + 192, gates + 256, gates + 320,
+                        gates + 384, gates + 385};
+      float* ee = GV.ee;
+      float* ff = GV.ff;
+      float* bt = GV.bt;
+      unsigned char* st = sm + kF_KQ + s * 32768;
+      const uint32_t st_kq = smem_u32(st);
+      ok = group_and(kBarPrep, kGroup, mbar_wait(&bar_kq[s], (ci >> 1) & 1) && !*abort_flag);
+      if (!ok) break;
+      if (pt == 0) cnt[2 + s] += 1;
+      if (pt == 0) {
+        // MMA1: [K;Q] K^T, M=128 N=64 K=128
+        const uint32_t idesc = idesc_bf16(128, 64, false, false);
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
+          mma_bf16(tmem + kTmKQ, sw128_desc(st_kq + off, 16, 1024), sw128_desc(st_kq + off, 16, 1024),
+                   idesc, ks > 0);
+        }
+        mma_commit(bar_p);
+      }
+      if (warp == 8) {
+        // gates of this chunk (the previous user of this block finished with it
+        // before this stage's tiles were requested)
+        chunk_gates(GV, pg0, pg1, pb0, pb1, lane);
+        if (ci + 1 < p.N) load_gates(ci + 1);
+      }
+      ok = group_and(kBarPrep, kGroup, mbar_wait(bar_p, p_phase));
+      p_phase ^= 1;
+      tc_fence_after();
+      if (!ok) break;
+      // A (rows 0-63, fp32) and P (rows 64-127, bf16): 32 columns per thread.
+      // Quadrants 0 and 2 hold rows 0-31 of A / P: their columns 32-63 are zero.
+      {
+        float v[32];
+        const bool upper_zero = (quad == 0 || quad == 2) && half == 1;
+        if (!upper_zero && (row < 64 || want_o)) tmem_ld32(tmem + lane_base + kTmKQ + half * 32, v);
+        if (row < 64) {
+          const int r = row;
+          if (upper_zero) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          } else {
+            decay_row(v, GV, r, half * 32, true, bt[r]);
+          }
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(Am + r * kLdF + half * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else if (want_o) {  // P is read only by the output product
+          const int r = row - 64;
+          if (upper_zero) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          } else {
+            decay_row(v, GV, r, half * 32, false, 1.f);
+          }
+          store_chunks(sm + kF_P + s * 8192, r, half * 4, v, 4);
+        }
+      }
+      tc_fence_before();
+      psync();
+      solve_unit_lower(Am, Tm, Sm, pt, kGroup, psync);
+      // T' = T diag(beta e) and T'' = T diag(beta): 16 values per thread (row r, two chunks)
+      {
+        const int r = pt >> 2, c0 = (pt & 3) * 2;
+        float v1[16], v0[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int j = cg * 16 + i;
-          v[i] = (j < r) ? br * v[i] * __expf(gr - gam[j]) : 0.f;
+          const int j = c0 * 8 + i;
+          const float t = (j <= r) ? Tm[r * kLdF + j] * bt[j] : 0.f;
+          v0[i] = t;
+          v1[i] = t * ee[j];
         }
-#pragma unroll
-        for (int i = 0; i < 16; i += 4)
-          *reinterpret_cast<float4*>(Am + r * kLdF + cg * 16 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-      } else {
-        const int r = row - 64;
-        const float gr = gam[r];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int j = cg * 16 + i;
-          v[i] = (j <= r) ? v[i] * __expf(gr - gam[j]) : 0.f;
-        }
-        store_chunks(sm + kOffP, r, cg * 2, v, 2);
+        store_chunks(sm + kF_T1, r, c0, v1, 2);
+        store_chunks(sm + kF_T0, r, c0, v0, 2);
       }
-    }
-    cta_sync();
-    solve_unit_lower_f(Am, Tm, Sm);
-    // T' = T diag(beta e), T'' = T diag(beta): one 16-byte chunk per thread
-    {
-      const int r = tid >> 3, c8 = tid & 7;
-      float v1[8], v2[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int j = c8 * 8 + i;
-        const float t = (j <= r) ? Tm[r * kLdF + j] : 0.f;
-        v2[i] = t * bt[j];
-        v1[i] = v2[i] * ee[j];
+      // e Q rows (read by the chain's MMA4a); MMA1 is done with Q
+      scale_rows(st + 8192, 64, ee, pt, kGroup);
+      scale_rows(st + 24576, 64, ee, pt, kGroup);
+      ok = group_and(kBarPrep, kGroup, mbar_wait(bar_v, ci & 1));
+      if (!ok) break;
+      if (pt == 0) cnt[5] += 1;
+      fence_async_shared();
+      tc_fence_before();
+      psync();
+      tc_fence_after();
+      if (pt == 0) {
+        // MMA2: W^T = K^T T'^T  (A: K tile MN-major, M=d; B: T' K-major, N=r)
+        const uint32_t id2 = idesc_bf16(128, 64, true, false);
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem + kTmW, sw128_desc(st_kq + ks * 2048, 16384, 1024),
+                   sw128_desc(smem_u32(sm + kF_T1) + ks * 32, 16, 1024), id2, ks > 0);
+        // MMA3a: U^T = V^T T''^T  (A: V tile MN-major, M=c; B: T'' K-major, N=r)
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem + kTmU0 + 64 * s, sw128_desc(smem_u32(sm + kF_V) + ks * 2048, 8192, 1024),
+                   sw128_desc(smem_u32(sm + kF_T0) + ks * 32, 16, 1024), id2, ks > 0);
+        mma_commit(bar_p);
       }
-      store_chunks(sm + kOffT1, r, c8, v1, 1);
-      store_chunks(sm + kOffT2, r, c8, v2, 1);
-    }
-    // scale Q rows in place by e_r (Q is done as an MMA1 operand): 2 chunks per thread
-    for (int i = tid; i < 2 * 64 * 8; i += FT) {
-      const int half = i / 512, r = (i / 8) % 64, c8 = i % 8;
-      uint4* ptr = reinterpret_cast<uint4*>(st + kStageKQ + half * 16384 + 8192 + r * 128 + c8 * 16);
-      uint4 val = *ptr;
-      __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&val);
-      const float e = ee[r];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float2 f2 = __bfloat1622float2(h2[k]);
-        h2[k] = __floats2bfloat162_rn(f2.x * e, f2.y * e);
+      ok = group_and(kBarPrep, kGroup, mbar_wait(bar_p, p_phase));
+      p_phase ^= 1;
+      tc_fence_after();
+      if (!ok) break;
+      if (pt == 0 && ci + 1 < p.N) load_v(ci + 1);
+      if (ci > 0) {
+        ok = group_and(kBarPrep, kGroup, mbar_wait(bar_wf, (ci - 1) & 1));
+        if (!ok) break;
       }
-      *ptr = val;
-    }
-    fence_async_shared();
-    cta_sync();
-    if (tid == 0) {
-      // MMA2: W^T = K^T T'^T  (A: K tile MN-major, M=d; B: T' K-major, N=r)
-      const uint32_t id2 = idesc_bf16(128, 64, true, false);
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + kTmW, sw128_desc(st_kq + ks * 2048, 16384, 1024),
-                 sw128_desc(smem_u32(sm + kOffT1) + ks * 32, 16, 1024), id2, ks > 0);
-      // MMA3a: U^T = V^T T''^T  (A: V tile MN-major, M=c)
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + kTmU, sw128_desc(st_v + ks * 2048, 8192, 1024),
-                 sw128_desc(smem_u32(sm + kOffT2) + ks * 32, 16, 1024), id2, ks > 0);
-      mma_commit(bar_mma);
-    }
-    mma_wait();
-    if (!ok) break;
-    // E2: W^T row d -> W tile (MN-major: row d holds 64 r)
-    {
-      float w[16];
-      tmem_ld16(tmem + lane_base + kTmW + cg * 16, w);
-      store_chunks(sm + kOffW, row, cg * 2, w, 2);
-    }
-    fence_async_shared();
-    cta_sync();
-    if (tid == 0) {
-      // MMA3b: U^T += -G W^T (A: G K-major M=c K=d; B: W MN-major N=r K=d)
-      const uint32_t id3 = idesc_bf16(128, 64, false, true, true);
-      for (int ks = 0; ks < 8; ++ks)
-        mma_bf16(tmem + kTmU, sw128_desc(smem_u32(sm + kOffG) + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024),
-                 sw128_desc(smem_u32(sm + kOffW) + ks * 2048, 16384, 1024), id3, 1);
-      // MMA4a: O^T = G (eQ)^T (B: Q tile K-major N=r K=d)
-      const uint32_t id4 = idesc_bf16(128, 64, false, false);
-      for (int ks = 0; ks < (want_o ? 8 : 0); ++ks) {
-        const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
-        mma_bf16(tmem + kTmO, sw128_desc(smem_u32(sm + kOffG) + off, 16, 1024),
-                 sw128_desc(st_kq + 8192 + off, 16, 1024), id4, ks > 0);
+      {
+        float w[32];
+        tmem_ld32(tmem + lane_base + kTmW + half * 32, w);
+        store_chunks(sm + kF_W, row, half * 4, w, 4);
       }
-      mma_commit(bar_mma);
+      // f K rows (read by the chain's MMA5); MMA1 and MMA2 are done with K
+      scale_rows(st, 64, ff, pt, kGroup);
+      scale_rows(st + 16384, 64, ff, pt, kGroup);
+      fence_async_shared();
+      tc_fence_before();
+      psync();
+      if (pt == 0) mbar_arrive(bar_pd);
     }
-    mma_wait();
-    if (!ok) break;
-    // E3: U^T row c -> U^T tile and (U diag f)^T tile
-    {
-      float u[16];
-      tmem_ld16(tmem + lane_base + kTmU + cg * 16, u);
-      store_chunks(sm + kOffU, row, cg * 2, u, 2);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) u[i] *= ff[cg * 16 + i];
-      store_chunks(sm + kOffUf, row, cg * 2, u, 2);
-    }
-    fence_async_shared();
-    cta_sync();
-    if (tid == 0) {
-      // MMA4b: O^T += U^T P^T (A: U^T K-major M=c K=j; B: P K-major N=r K=j)
-      const uint32_t id4 = idesc_bf16(128, 64, false, false);
-      for (int ks = 0; ks < (want_o ? 4 : 0); ++ks)
-        mma_bf16(tmem + kTmO, sw128_desc(smem_u32(sm + kOffU) + ks * 32, 16, 1024),
-                 sw128_desc(smem_u32(sm + kOffP) + ks * 32, 16, 1024), id4, 1);
-      // MMA5: dG = (U diag f)^T K (B: K tile MN-major, N=d (2 atoms), K=j)
-      const uint32_t id5 = idesc_bf16(128, 128, false, true);
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + kTmG, sw128_desc(smem_u32(sm + kOffUf) + ks * 32, 16, 1024),
-                 sw128_desc(st_kq + ks * 2048, 16384, 1024), id5, ks > 0);
-      mma_commit(bar_mma);
-    }
-    mma_wait();
-    if (!ok) break;
-    // E4: O^T row c, columns r in [16 cg, 16 cg + 16) -> o[b, t0 + r, h, c]
-    if (want_o) {
-      float v[16];
-      tmem_ld16(tmem + lane_base + kTmO + cg * 16, v);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int r = cg * 16 + i;
-        if (r < n) p.o[(((size_t)b * p.T + t0 + r) * p.H + h) * D + row] = __float2bfloat16_rn(v[i]);
-      }
-    }
-    // E5: G = eC G + dG on this thread's 32 columns; bf16 copy for the next chunk
-    {
-      const float ec = *eC;
-      float v32[32];
-      tmem_ld32(tmem + lane_base + kTmG + cg * 32, v32);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) G[i] = fmaf(ec, G[i], v32[i]);
-      write_g(G, ci + 1 < p.N ? state_dst(ci + 1) : nullptr);
-    }
-    fence_async_shared();
-    cta_sync();
+    if (!ok) *abort_flag = 1;
   }
 
-  if (!ok) {
-    if (tid == 0) report_timeout();
-    // let any tile load still in flight land before the CTA exits (bounded)
-    for (int s2 = 0; s2 < 2; ++s2) mbar_wait(&bar_load[s2], load_phase[s2], 1u << 20);
-  } else {
-    if (p.ht) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) p.ht[((size_t)bh * D + cg * 32 + i) * D + row] = G[i];
-    }
-    if (p.dht_dot) {
-      float acc = 0.f;
-      if (p.dht) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc += p.dht[((size_t)bh * D + cg * 32 + i) * D + row] * G[i];
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      float* red = reinterpret_cast<float*>(sm + kOffGate);  // gates are no longer needed
-      __syncthreads();
-      if (lane == 0) red[warp] = acc;
-      __syncthreads();
-      if (tid == 0) {
-        float t = 0.f;
-        for (int w = 0; w < FT / 32; ++w) t += red[w];
-        p.dht_dot[bh] = t;
-      }
+  __syncthreads();
+  if (*abort_flag) {
+    if (tid == 0) {
+      report_timeout();
+      // let tile loads still in flight land before the CTA exits (bounded)
+      for (int st = 0; st < 2; ++st)
+        for (int k = cnt[2 + st]; k < cnt[st]; ++k) mbar_wait(&bar_kq[st], k & 1, 10000);
+      for (int k = cnt[5]; k < cnt[4]; ++k) mbar_wait(bar_v, k & 1, 10000);
     }
   }
   cta_sync();
@@ -543,8 +739,8 @@ constexpr int kB_V = 131072;             // [Vh0 | Vh1]
 constexpr int kB_T = kB_V + 16384;       // T [r][j]; after the dZ product: M = beta dA o Gam
 constexpr int kB_P = kB_T + 8192;        // P [r][j]; after dO^T P: dP o Gam
 constexpr int kB_X = kB_P + 8192;        // three 16 KB slots, reused by phase
-constexpr int kB_GATE = kB_X + 3 * 16384;  // gam, e, f, beta, db1, db2, dlc [64] each
-constexpr int kB_RED = kB_GATE + 7 * 256;  // reduction scratch [16][64] floats
+constexpr int kB_GATE = kB_X + 3 * 16384;  // gam, e, f, beta, er, ie, db1, db2, dlc [64] each, eC, fast
+constexpr int kB_RED = kB_GATE + 9 * 256 + 16;  // reduction scratch [16][64] floats
 constexpr int kB_EC = kB_RED + 4096;
 constexpr int kB_BAR = kB_EC + 64;
 constexpr int kBwdSmemBytes = kB_BAR + 128 + 1024;
@@ -631,11 +827,12 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   float* ee = gam + 64;
   float* ff = ee + 64;
   float* bt = ff + 64;
-  float* db1 = bt + 64;
+  float* db1 = gam + 384;
   float* db2 = db1 + 64;
   float* dlc = db2 + 64;
   float* red = reinterpret_cast<float*>(sm + kB_RED);
   float* eC = reinterpret_cast<float*>(sm + kB_EC);
+  const GateView GV{gam, ee, ff, bt, gam + 256, gam + 320, eC, gam + 576};
   uint64_t* bar_load = reinterpret_cast<uint64_t*>(sm + kB_BAR);
   uint64_t* bar_mma = bar_load + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma + 1);
@@ -721,26 +918,22 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       tma_load_4d(sm + kB_V, &tm_v, bar_load, 0, h, t0, b);
       tma_load_4d(sm + kB_V + 8192, &tm_v, bar_load, 64, h, t0, b);
       bulk_load(sm + kB_GI, p.states + ((size_t)bh * p.N + ci) * 32768, 32768, bar_load);
+      if (ci > 0) {
+        // the next chunk in the reverse scan: start pulling its tiles into L2
+        const int tp = t0 - C;
+        tma_prefetch_l2_4d(&tm_k, 0, h, tp, b);
+        tma_prefetch_l2_4d(&tm_k, 64, h, tp, b);
+        tma_prefetch_l2_4d(&tm_q, 0, h, tp, b);
+        tma_prefetch_l2_4d(&tm_q, 64, h, tp, b);
+        tma_prefetch_l2_4d(&tm_do, 0, h, tp, b);
+        tma_prefetch_l2_4d(&tm_do, 64, h, tp, b);
+        tma_prefetch_l2_4d(&tm_v, 0, h, tp, b);
+        tma_prefetch_l2_4d(&tm_v, 64, h, tp, b);
+        bulk_prefetch_l2(p.states + ((size_t)bh * p.N + ci - 1) * 32768, 32768);
+      }
     }
     if (warp == 0) {
-      float g0 = pg0, g1 = pg1;
-      bt[lane] = pb0;
-      bt[lane + 32] = pb1;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        float a0 = __shfl_up_sync(0xffffffffu, g0, off);
-        float a1 = __shfl_up_sync(0xffffffffu, g1, off);
-        if (lane >= off) g0 += a0, g1 += a1;
-      }
-      g1 += __shfl_sync(0xffffffffu, g0, 31);
-      const float gl = __shfl_sync(0xffffffffu, g1, 31);
-      gam[lane] = g0;
-      gam[lane + 32] = g1;
-      ee[lane] = __expf(g0);
-      ee[lane + 32] = __expf(g1);
-      ff[lane] = __expf(gl - g0);
-      ff[lane + 32] = __expf(gl - g1);
-      if (lane == 0) *eC = __expf(gl);
+      chunk_gates(GV, pg0, pg1, pb0, pb1, lane);
       if (ci > 0) load_gates(ci - 1);
     }
     ok = __syncthreads_and(mbar_wait(bar_load, load_phase));
@@ -763,28 +956,18 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       tmem_ld16(tmem + lb + kBtKQ + cg * 16, v);
       if (row < 64) {
         const int r = row;
-        const float gr = gam[r], br = bt[r];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int j = cg * 16 + i;
-          v[i] = (j < r) ? br * v[i] * __expf(gr - gam[j]) : 0.f;
-        }
+        decay_row(v, GV, r, cg * 16, true, bt[r]);
 #pragma unroll
         for (int i = 0; i < 16; i += 4)
           *reinterpret_cast<float4*>(Am + r * kLdF + cg * 16 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
       } else {
         const int r = row - 64;
-        const float gr = gam[r];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int j = cg * 16 + i;
-          v[i] = (j <= r) ? v[i] * __expf(gr - gam[j]) : 0.f;
-        }
+        decay_row(v, GV, r, cg * 16, false, 1.f);
         store_chunks(sm + kB_P, r, cg * 2, v, 2);
       }
     }
     cta_sync();
-    solve_unit_lower_f(Am, Tm, Sm);
+    solve_unit_lower(Am, Tm, Sm, tid, BT, [] { __syncthreads(); });
     {
       const int r = tid >> 3, c8 = tid & 7;
       float v[8];
@@ -892,30 +1075,26 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       float x[16];
       tmem_ld16(tmem + lb + kBtX1 + cg * 16, x);
       if (row < 64) {
-        // dA = -strict_lower(dZ U^T); dbeta part 2; M = beta dA o Gam
+        // dA = -strict_lower(dZ U^T); dbeta part 2: sum_j dA_rj (K K^T o Gam)_rj;
+        // M = beta dA o Gam
         const int r = row;
         float kk[16];
         tmem_ld16(tmem + lb + kBtKQ + cg * 16, kk);
-        const float gr = gam[r], br = bt[r];
+        const float br = bt[r];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = -x[i];
+        decay_row(x, GV, r, cg * 16, true, 1.f);   // x = dA o Gam
         float s2 = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int j = cg * 16 + i;
-          const float w = (j < r) ? __expf(gr - gam[j]) : 0.f;
-          const float da = -x[i];
-          s2 += da * kk[i] * w;
-          x[i] = br * da * w;
+          s2 += x[i] * kk[i];
+          x[i] *= br;
         }
         red[cg * 64 + r] = s2;
         store_chunks(sm + kB_T, r, cg * 2, x, 2);
       } else {
         const int r = row - 64;
-        const float gr = gam[r];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int j = cg * 16 + i;
-          x[i] = (j <= r) ? x[i] * __expf(gr - gam[j]) : 0.f;
-        }
+        decay_row(x, GV, r, cg * 16, false, 1.f);
         store_chunks(sm + kB_P, r, cg * 2, x, 2);
       }
     }
@@ -1054,7 +1233,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   if (!ok) {
     if (tid == 0) report_timeout();
-    mbar_wait(bar_load, load_phase, 1u << 20);
+    mbar_wait(bar_load, load_phase, 10000);
   } else if (p.dh0) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) p.dh0[((size_t)bh * D + cg * 32 + i) * D + row] = dG[i];
