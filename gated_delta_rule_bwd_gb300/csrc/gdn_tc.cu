@@ -67,8 +67,9 @@ constexpr int kF_P = 131072;               // 2 x P [r][j]                (8 KB 
 constexpr int kF_T1 = 147456;              // T' = T diag(beta e) [r][j]  (8 KB)
 constexpr int kF_T0 = 155648;              // T'' = T diag(beta) [r][j]   (8 KB)
 constexpr int kF_U = 163840;               // U^T [c][j] K-major          (16 KB)
-constexpr int kF_SOLVE = 180224;           // A, T fp32 [64][kLdF] + S [3][16][16]
-constexpr int kSolveBytes = (2 * 64 * kLdF + 3 * 256) * 4;
+constexpr int kF_SOLVE = 180224;           // A, T fp32 [64][kLdF] + kSolveScratch floats
+constexpr int kSolveScratch = 32 * 36;     // largest scratch use: the 32 x 32 product, row stride 36
+constexpr int kSolveBytes = (2 * 64 * kLdF + kSolveScratch) * 4;   // A, T [64][kLdF] + scratch
 constexpr int kF_GATE = kF_SOLVE + kSolveBytes;
 constexpr int kGateBlock = 1600;           // gamma, e, f, beta, er, ie [64] each, eC, fast; two blocks
 constexpr int kF_BAR = kF_GATE + 2 * kGateBlock;
@@ -161,97 +162,156 @@ __device__ __forceinline__ void scale_rows(unsigned char* base, int rows, const 
   }
 }
 
-// One level of the blocked inverse: for the nb = 4 - L blocks (ib, jb = ib - L),
-// S = sum_{kb=jb}^{ib-1} A[ib][kb] T[kb][jb], then T[ib][jb] = -T[ib][ib] S.
-// Work item = (block, row, 4 columns); k loops are fully unrolled with float4
-// loads so that the shared-memory latency overlaps.
-template <int L, class Sync>
-__device__ __forceinline__ void solve_level(const float* A, float* T, float* S, int t, int nth,
-                                            Sync sync) {
-  constexpr int kItems = (4 - L) * 64;
-  for (int it = t; it < kItems; it += nth) {
-    const int b = it >> 6, r = (it >> 2) & 15, c4 = (it & 3) * 4;
-    const int ib = b + L, jb = b;
-    const float* arow = A + (ib * 16 + r) * kLdF + jb * 16;
-    const float* tcol = T + (jb * 16) * kLdF + jb * 16 + c4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int k = 0; k < 16 * L; ++k) {
-      const float a = arow[k];
-      const float4 tv = *reinterpret_cast<const float4*>(tcol + k * kLdF);
-      acc.x = fmaf(a, tv.x, acc.x);
-      acc.y = fmaf(a, tv.y, acc.y);
-      acc.z = fmaf(a, tv.z, acc.z);
-      acc.w = fmaf(a, tv.w, acc.w);
-    }
-    *reinterpret_cast<float4*>(S + b * 256 + r * 16 + c4) = acc;
-  }
-  sync();
-  for (int it = t; it < kItems; it += nth) {
-    const int b = it >> 6, r = (it >> 2) & 15, c4 = (it & 3) * 4;
-    const int ib = b + L, jb = b;
-    const float* trow = T + (ib * 16 + r) * kLdF + ib * 16;  // zero above the diagonal
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float a = trow[k];
-      const float4 sv = *reinterpret_cast<const float4*>(S + b * 256 + k * 16 + c4);
-      acc.x = fmaf(a, sv.x, acc.x);
-      acc.y = fmaf(a, sv.y, acc.y);
-      acc.z = fmaf(a, sv.z, acc.z);
-      acc.w = fmaf(a, sv.w, acc.w);
-    }
-    *reinterpret_cast<float4*>(T + (ib * 16 + r) * kLdF + jb * 16 + c4) =
-        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-  }
-  sync();
+// ---- small fp32 products on the warp-level tensor path (TF32, fp32 accumulate)
+// used by the 64 x 64 triangular solve.  Fragment layout of mma.m16n8k8:
+// g = lane / 4, q = lane % 4; A (16 x 8, row-major) a0 = A[g][q], a1 = A[g+8][q],
+// a2 = A[g][q+4], a3 = A[g+8][q+4]; B (8 x 8) b0 = B[q][g], b1 = B[q+4][g];
+// C (16 x 8) c0 = C[g][2q], c1 = C[g][2q+1], c2 = C[g+8][2q], c3 = C[g+8][2q+1].
+// Row strides of 68, 36 or 24 floats make these loads conflict-free.
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
 }
 
-// T = (I + A)^-1 for a 64 x 64 strictly lower A (fp32, row stride kLdF), by
-// 16 x 16 blocks: the diagonal blocks by forward substitution (one thread per
-// column), then three levels of block products.  nth threads take part
-// (t = this thread's index); sync() is their barrier.
+// d += A[m0:m0+16][ka:ka+8] * B[kb:kb+8][n0:n0+8]
+__device__ __forceinline__ void tf32_mma_step(float (&d)[4], const float* A, int lda, int m0, int ka,
+                                              const float* B, int ldb, int kb, int n0) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const uint32_t a0 = to_tf32(A[(m0 + g) * lda + ka + q]);
+  const uint32_t a1 = to_tf32(A[(m0 + g + 8) * lda + ka + q]);
+  const uint32_t a2 = to_tf32(A[(m0 + g) * lda + ka + q + 4]);
+  const uint32_t a3 = to_tf32(A[(m0 + g + 8) * lda + ka + q + 4]);
+  const uint32_t b0 = to_tf32(B[(kb + q) * ldb + n0 + g]);
+  const uint32_t b1 = to_tf32(B[(kb + q + 4) * ldb + n0 + g]);
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void store_c_tile(const float (&d)[4], float* C, int ldc, int m0, int n0) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  *reinterpret_cast<float2*>(C + (m0 + g) * ldc + n0 + 2 * q) = make_float2(d[0], d[1]);
+  *reinterpret_cast<float2*>(C + (m0 + g + 8) * ldc + n0 + 2 * q) = make_float2(d[2], d[3]);
+}
+
+// T = (I + A)^-1 for a 64 x 64 strictly lower A (fp32, row stride kLdF); T is
+// written with zeros above the diagonal.  Three steps:
+//  1. each 16 x 16 diagonal block by one warp: its two 8 x 8 diagonal blocks
+//     by forward substitution (one lane per column), then the 8 x 8 coupling
+//     T21 = -T22 (A21 T11);
+//  2. inside each 32 x 32 half, T[1][0] = -T[1][1] (A[1][0] T[0][0]) over the
+//     16 x 16 blocks (and the same for blocks 3, 2);
+//  3. T_BA = -T_B (A_BA T_A) for the 32 x 32 halves.
+// Steps 2 and 3 run on the warp-level tensor path in TF32 with fp32
+// accumulation (its rounding is below that of the bf16 copies of T made next).
+// nth threads take part (t = this thread's index, nth >= 256); sync() is
+// their barrier.  S holds kSolveScratch floats (step 1 uses S[0, 256), step 2
+// S[256, 1024), step 3 S[0, 32 * 36)).
 template <class Sync>
 __device__ void solve_unit_lower(const float* A, float* T, float* S, int t, int nth, Sync sync) {
-  if (t < 64) {
-    // column jj of the inverse of diagonal block ib: x_r = -sum_{i<r} A[r][i] x_i,
-    // x_jj = 1, x_r = 0 above jj (so the sum may run over every i < r and all
-    // 16 lanes of a block execute the same instructions)
-    const int ib = t / 16, jj = t % 16, o = ib * 16;
-    float x[16];
+  const int w = t >> 5, l = t & 31;
+  if (w < 4) {
+    const int o = w * 16;
+    if (l < 16) {
+      const int so = o + (l >> 3) * 8, jj = l & 7;
+      float x[8];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float a[16];
+      for (int r = 0; r < 8; ++r) {
+        const float4 a0 = *reinterpret_cast<const float4*>(A + (so + r) * kLdF + so);
+        const float4 a1 = *reinterpret_cast<const float4*>(A + (so + r) * kLdF + so + 4);
+        const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v4 = *reinterpret_cast<const float4*>(A + (o + r) * kLdF + o + 4 * q);
-        a[4 * q] = v4.x, a[4 * q + 1] = v4.y, a[4 * q + 2] = v4.z, a[4 * q + 3] = v4.w;
+        for (int i = 0; i < r; ++i) {
+          if (i & 1) s1 = fmaf(a[i], x[i], s1);
+          else s0 = fmaf(a[i], x[i], s0);
+        }
+        x[r] = (r == jj) ? 1.f : ((r > jj) ? -(s0 + s1) : 0.f);
       }
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-      for (int i = 0; i < r; ++i) {
-        if ((i & 3) == 0) s0 = fmaf(a[i], x[i], s0);
-        if ((i & 3) == 1) s1 = fmaf(a[i], x[i], s1);
-        if ((i & 3) == 2) s2 = fmaf(a[i], x[i], s2);
-        if ((i & 3) == 3) s3 = fmaf(a[i], x[i], s3);
-      }
-      const float s = -((s0 + s1) + (s2 + s3));
-      x[r] = (r == jj) ? 1.f : ((r > jj) ? s : 0.f);
+      for (int r = 0; r < 8; ++r) T[(so + r) * kLdF + so + jj] = x[r];
+    } else {
+      // zero the 8 x 8 block above the diagonal of this 16 x 16 block
+      for (int i = l - 16; i < 64; i += 16) T[(o + (i >> 3)) * kLdF + o + 8 + (i & 7)] = 0.f;
     }
+    __syncwarp();
+    float* S8 = S + w * 64;
+    const int r = l >> 2, c = (l & 3) * 2;
+    {
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int r = 0; r < 16; ++r) T[(o + r) * kLdF + o + jj] = x[r];
+      for (int k = 0; k < 8; ++k) {
+        const float a = A[(o + 8 + r) * kLdF + o + k];
+        s0 = fmaf(a, T[(o + k) * kLdF + o + c], s0);
+        s1 = fmaf(a, T[(o + k) * kLdF + o + c + 1], s1);
+      }
+      S8[r * 8 + c] = s0;
+      S8[r * 8 + c + 1] = s1;
+    }
+    __syncwarp();
+    {
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float a = T[(o + 8 + r) * kLdF + o + 8 + k];  // zero for k > r
+        s0 = fmaf(a, S8[k * 8 + c], s0);
+        s1 = fmaf(a, S8[k * 8 + c + 1], s1);
+      }
+      T[(o + 8 + r) * kLdF + o + c] = -s0;
+      T[(o + 8 + r) * kLdF + o + c + 1] = -s1;
+    }
   } else {
-    for (int i = t - 64; i < 64 * 64; i += nth - 64) {
-      const int r = i / 64, c = i % 64;
-      if ((c / 16) > (r / 16)) T[r * kLdF + c] = 0.f;
+    // zero the 16 x 16 blocks above the block diagonal
+    for (int i = t - 128; i < 64 * 64; i += nth - 128) {
+      const int rr = i >> 6, cc = i & 63;
+      if ((cc >> 4) > (rr >> 4)) T[rr * kLdF + cc] = 0.f;
     }
   }
   sync();
-  solve_level<1>(A, T, S, t, nth, sync);
-  solve_level<2>(A, T, S, t, nth, sync);
-  solve_level<3>(A, T, S, t, nth, sync);
+  // step 2: per 32 x 32 half b, S = A[2b+1][2b] T[2b][2b], T[2b+1][2b] = -T[2b+1][2b+1] S
+  // (16 x 16 blocks); warp w < 4 takes half w / 2 and output columns 8 (w % 2) + [0, 8)
+  if (w < 4) {
+    const int hb = w >> 1, n0 = (w & 1) * 8;
+    const int r0 = 32 * hb + 16, c0 = 32 * hb;
+    float* Sb = S + 256 + hb * 16 * 24;  // 16 x 16, row stride 24
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k0 = 0; k0 < 16; k0 += 8) tf32_mma_step(d, A, kLdF, r0, c0 + k0, T, kLdF, c0 + k0, c0 + n0);
+    store_c_tile(d, Sb, 24, 0, n0);
+    __syncwarp();  // this warp's columns of S are all it reads next
+    float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k0 = 0; k0 < 16; k0 += 8) tf32_mma_step(e, T, kLdF, r0, r0 + k0, Sb, 24, k0, n0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) e[i] = -e[i];
+    store_c_tile(e, T, kLdF, r0, c0 + n0);
+  }
+  sync();
+  // step 3: S32 = A[32:64][0:32] T[0:32][0:32], T[32:64][0:32] = -T[32:64][32:64] S32;
+  // 8 output tiles of 16 x 8 (warp w < 8 takes tile w)
+  if (w < 8) {
+    const int m0 = (w >> 2) * 16, n0 = (w & 3) * 8;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k0 = 0; k0 < 32; k0 += 8) tf32_mma_step(d, A, kLdF, 32 + m0, k0, T, kLdF, k0, n0);
+    store_c_tile(d, S, 36, m0, n0);
+  }
+  sync();
+  if (w < 8) {
+    const int m0 = (w >> 2) * 16, n0 = (w & 3) * 8;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k0 = 0; k0 < 32; k0 += 8) tf32_mma_step(d, T, kLdF, 32 + m0, 32 + k0, S, 36, k0, n0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = -d[i];
+    store_c_tile(d, T, kLdF, 32 + m0, n0);
+  }
+  sync();
 }
-
 
 // Gates of one chunk, computed by one warp from the lane's two log gates
 // (rows lane and lane + 32) and betas: gamma = inclusive cumsum of g,
@@ -345,17 +405,18 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   uint64_t* bar_s = bar_kq + 4;                                  // chain MMAs done
   uint64_t* bar_pd = bar_kq + 5;                                 // preparation of a chunk done
   uint64_t* bar_wf = bar_kq + 6;                                 // W tile free again
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_kq + 7);
+  uint64_t* bar_p1 = bar_kq + 7;                                 // preparation MMA1 done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_kq + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* cnt = reinterpret_cast<int*>(tmem_slot + 2);  // [0..1] kq issued, [2..3] kq waited, [4] v issued, [5] v waited
+  int* cnt = reinterpret_cast<int*>(tmem_slot + 2);  // [0..1] kq issued, [2..3] kq waited, [4] v issued, [5] v waited, [6] early MMA1
   float* Am = reinterpret_cast<float*>(sm + kF_SOLVE);
   float* Tm = Am + 64 * kLdF;
   float* Sm = Tm + 64 * kLdF;
 
   if (tid == 0) {
-    for (int i = 0; i < 7; ++i) mbar_init(&bar_kq[i], 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&bar_kq[i], 1);
     *abort_flag = 0;
-    for (int i = 0; i < 6; ++i) cnt[i] = 0;
+    for (int i = 0; i < 7; ++i) cnt[i] = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -565,6 +626,19 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       pb1 = lane + 32 < n ? p.beta[base + (size_t)(lane + 32) * p.H] : 0.f;
     };
     if (warp == 8) load_gates(0);
+    volatile int* early_mma1 = cnt + 6;
+    if (pt == 0) *early_mma1 = 0;
+    auto issue_mma1 = [&](int cn) {
+      // MMA1: [K;Q] K^T, M=128 N=64 K=128 on the stage of chunk cn
+      const uint32_t kq = smem_u32(sm + kF_KQ + (cn & 1) * 32768);
+      const uint32_t idesc = idesc_bf16(128, 64, false, false);
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
+        mma_bf16(tmem + kTmKQ, sw128_desc(kq + off, 16, 1024), sw128_desc(kq + off, 16, 1024), idesc,
+                 ks > 0);
+      }
+      mma_commit(bar_p1);
+    };
     uint32_t p_phase = 0;
     for (int ci = 0; ci < p.N; ++ci) {
       const int s = ci & 1;
@@ -579,24 +653,14 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ok = group_and(kBarPrep, kGroup, mbar_wait(&bar_kq[s], (ci >> 1) & 1) && !*abort_flag);
       if (!ok) break;
       if (pt == 0) cnt[2 + s] += 1;
-      if (pt == 0) {
-        // MMA1: [K;Q] K^T, M=128 N=64 K=128
-        const uint32_t idesc = idesc_bf16(128, 64, false, false);
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
-          mma_bf16(tmem + kTmKQ, sw128_desc(st_kq + off, 16, 1024), sw128_desc(st_kq + off, 16, 1024),
-                   idesc, ks > 0);
-        }
-        mma_commit(bar_p);
-      }
+      if (pt == 0 && !*early_mma1) issue_mma1(ci);
       if (warp == 8) {
         // gates of this chunk (the previous user of this block finished with it
         // before this stage's tiles were requested)
         chunk_gates(GV, pg0, pg1, pb0, pb1, lane);
         if (ci + 1 < p.N) load_gates(ci + 1);
       }
-      ok = group_and(kBarPrep, kGroup, mbar_wait(bar_p, p_phase));
-      p_phase ^= 1;
+      ok = group_and(kBarPrep, kGroup, mbar_wait(bar_p1, ci & 1));
       tc_fence_after();
       if (!ok) break;
       // A (rows 0-63, fp32) and P (rows 64-127, bf16): 32 columns per thread.
@@ -671,6 +735,13 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       tc_fence_after();
       if (!ok) break;
       if (pt == 0 && ci + 1 < p.N) load_v(ci + 1);
+      if (pt == 0) {
+        // K K^T | Q K^T is free again: start the next chunk's MMA1 now if its
+        // tiles have landed (otherwise it is issued at the top of that chunk)
+        const int cn = ci + 1;
+        *early_mma1 = (cn < p.N && mbar_try_wait(&bar_kq[cn & 1], (cn >> 1) & 1)) ? 1 : 0;
+        if (*early_mma1) issue_mma1(cn);
+      }
       if (ci > 0) {
         ok = group_and(kBarPrep, kGroup, mbar_wait(bar_wf, (ci - 1) & 1));
         if (!ok) break;
