@@ -110,11 +110,11 @@ __device__ __forceinline__ void report_timeout() { atomicExch(&g_device_status, 
 
 // ---------------------------------------------------------------- forward kernel
 //
-// Warp-specialised, 512 threads.  Warps 0-7 (the chain group) run the
-// state-dependent part of chunk c: MMA3b/MMA4a, U^T, MMA4b/MMA5, the output
-// and the next state tile.  Warps 8-15 (the preparation group) meanwhile run
-// the state-independent part of chunk c+1: MMA1, A and P, the triangular
-// solve, T' and T'', the row scalings (eQ, fK), MMA2/MMA3a and W.
+// Warp-specialised, 512 threads.  Warps 8-15 (the preparation group) run the
+// state-independent part of chunk c+1: MMA1, A and P, the triangular solve,
+// T' and T'', MMA2/MMA3a.  Warps 0-7 (the chain group) meanwhile run chunk c:
+// the W tile from W^T, the row scalings eQ and fK, MMA3b/MMA4a, U^T,
+// MMA4b/MMA5, the output and the next state tile.
 // Warp w reads TMEM lane quadrant w % 4 and handles column half (w / 4) % 2
 // of every tile.  Hand-offs use mbarriers; each group synchronises internally
 // with its own named barrier.  The fp32 state lives in TMEM: before MMA5 the
@@ -404,7 +404,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   uint64_t* bar_p = bar_kq + 3;                                  // preparation MMAs done
   uint64_t* bar_s = bar_kq + 4;                                  // chain MMAs done
   uint64_t* bar_pd = bar_kq + 5;                                 // preparation of a chunk done
-  uint64_t* bar_wf = bar_kq + 6;                                 // W tile free again
+  uint64_t* bar_wf = bar_kq + 6;                                 // W^T TMEM read by the chain
   uint64_t* bar_p1 = bar_kq + 7;                                 // preparation MMA1 done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_kq + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -489,6 +489,25 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (!ok) break;
       tc_fence_after();
       {
+        // W^T (TMEM) -> W tile, MN-major: row d holds W[0..63][d]
+        float w[32];
+        tmem_ld32(tmem + lane_base + kTmW + half * 32, w);
+        store_chunks(sm + kF_W, row, half * 4, w, 4);
+      }
+      {
+        // rows of this chunk's stage: Q by e (for MMA4a), K by f (for MMA5);
+        // the preparation's MMA1 and MMA2 are done with both
+        unsigned char* stc = sm + kF_KQ + s * 32768;
+        const float* ge = gates + 64;
+        const float* gf = gates + 128;
+        if (want_o) {
+          scale_rows(stc + 8192, 64, ge, gt, kGroup);
+          scale_rows(stc + 24576, 64, ge, gt, kGroup);
+        }
+        scale_rows(stc, 64, gf, gt, kGroup);
+        scale_rows(stc + 16384, 64, gf, gt, kGroup);
+      }
+      {
         // G <- eC G  (MMA5 accumulates onto it)
         const float ec = gates[384];
         float v[32];
@@ -501,7 +520,9 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           tmem_st32(ta, v);
         }
       }
+      fence_async_shared();
       group_sync_tc(kBarChain);
+      if (gt == 0) mbar_arrive(bar_wf);  // W^T has been copied: the next MMA2 may run
       const uint32_t st_kq = smem_u32(sm + kF_KQ + s * 32768);
       const uint32_t tmU = kTmU0 + 64 * s;
       if (gt == 0) {
@@ -523,7 +544,6 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       s_phase ^= 1;
       tc_fence_after();
       if (!ok) break;
-      if (gt == 0) mbar_arrive(bar_wf);  // W may be overwritten by the next preparation
       {
         float u[32];
         tmem_ld32(tmem + lane_base + tmU + half * 32, u);
@@ -708,12 +728,14 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         store_chunks(sm + kF_T1, r, c0, v1, 2);
         store_chunks(sm + kF_T0, r, c0, v0, 2);
       }
-      // e Q rows (read by the chain's MMA4a); MMA1 is done with Q
-      scale_rows(st + 8192, 64, ee, pt, kGroup);
-      scale_rows(st + 24576, 64, ee, pt, kGroup);
       ok = group_and(kBarPrep, kGroup, mbar_wait(bar_v, ci & 1));
       if (!ok) break;
       if (pt == 0) cnt[5] += 1;
+      if (ci > 0) {
+        // the chain has copied the previous chunk's W^T out of TMEM
+        ok = group_and(kBarPrep, kGroup, mbar_wait(bar_wf, (ci - 1) & 1));
+        if (!ok) break;
+      }
       fence_async_shared();
       tc_fence_before();
       psync();
@@ -742,19 +764,6 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         *early_mma1 = (cn < p.N && mbar_try_wait(&bar_kq[cn & 1], (cn >> 1) & 1)) ? 1 : 0;
         if (*early_mma1) issue_mma1(cn);
       }
-      if (ci > 0) {
-        ok = group_and(kBarPrep, kGroup, mbar_wait(bar_wf, (ci - 1) & 1));
-        if (!ok) break;
-      }
-      {
-        float w[32];
-        tmem_ld32(tmem + lane_base + kTmW + half * 32, w);
-        store_chunks(sm + kF_W, row, half * 4, w, 4);
-      }
-      // f K rows (read by the chain's MMA5); MMA1 and MMA2 are done with K
-      scale_rows(st, 64, ff, pt, kGroup);
-      scale_rows(st + 16384, 64, ff, pt, kGroup);
-      fence_async_shared();
       tc_fence_before();
       psync();
       if (pt == 0) mbar_arrive(bar_pd);
