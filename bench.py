@@ -269,13 +269,15 @@ def run_ours(args):
     bwd = gdn.kda_bwd if w.kda else gdn.gdn_bwd
 
     x = w.make(device=dev, seed=rank)
-    wsb = torch.empty(max(16, gdn.bwd_workspace_bytes(x.q, x.v, w.chunk, w.kda)),
+    # one workspace serves both passes (the forward needs a prefix of the backward's)
+    wsb = torch.empty(max(16, gdn.bwd_workspace_bytes(x.q, x.v, w.chunk, w.kda),
+                          gdn.fwd_workspace_bytes(x.q, x.v, w.chunk, w.kda)),
                       dtype=torch.uint8, device=dev)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        o, ht = fwd(x.q, x.k, x.v, x.g, x.beta, x.h0, chunk=w.chunk)
+        o, ht = fwd(x.q, x.k, x.v, x.g, x.beta, x.h0, chunk=w.chunk, workspace=wsb)
         gr = bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do, None, chunk=w.chunk, workspace=wsb)
         return o, ht, gr
 
@@ -385,7 +387,8 @@ def run_e2e(gdn, w, x, wsb, dev, stream, K, warmup, ws):
         for n in names:
             dev_in[n].copy_(host_in[n], non_blocking=True)
         d = dev_in
-        o, ht = fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0"), chunk=w.chunk)
+        o, ht = fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0"), chunk=w.chunk,
+                    workspace=wsb)
         gr = bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0"), d["do"], None,
                  chunk=w.chunk, workspace=wsb)
         outs = {"o": o, "ht": ht, **{k: v for k, v in gr.items() if v is not None}}

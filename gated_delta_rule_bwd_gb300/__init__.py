@@ -39,7 +39,8 @@ class GdnError(RuntimeError):
 
 _lock = threading.Lock()
 _lib = None
-EXPORTS = ("gdn_fwd", "gdn_bwd", "kda_fwd", "kda_bwd", "gdn_bwd_workspace", "kda_bwd_workspace",
+EXPORTS = ("gdn_fwd", "gdn_bwd", "kda_fwd", "kda_bwd", "gdn_fwd_workspace", "kda_fwd_workspace",
+           "gdn_bwd_workspace", "kda_bwd_workspace",
            "gdn_status_str", "gdn_last_cuda_error", "gdn_device_status", "gdn_uses_tensor_cores",
            "gdn_profile_begin", "gdn_profile_end", "gdn_profile_read", "gdn_kernel_name")
 
@@ -55,7 +56,8 @@ def lib():
             L = ctypes.CDLL(LIB_PATH)
             vp, sz, fp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p
             sp = ctypes.POINTER(GdnShape)
-            for name in ("gdn_bwd_workspace", "kda_bwd_workspace"):
+            for name in ("gdn_fwd_workspace", "kda_fwd_workspace", "gdn_bwd_workspace",
+                         "kda_bwd_workspace"):
                 getattr(L, name).argtypes = [sp]
                 getattr(L, name).restype = sz
             for name in ("gdn_fwd", "kda_fwd"):
@@ -128,10 +130,22 @@ def _stream(dev):
     return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
 
 
+def fwd_workspace_bytes(q, v, chunk=64, kda=False) -> int:
+    L = lib()
+    s = make_shape(q, v, chunk)
+    return int((L.kda_fwd_workspace if kda else L.gdn_fwd_workspace)(ctypes.byref(s)))
+
+
 def bwd_workspace_bytes(q, v, chunk=64, kda=False) -> int:
     L = lib()
     s = make_shape(q, v, chunk)
     return int((L.kda_bwd_workspace if kda else L.gdn_bwd_workspace)(ctypes.byref(s)))
+
+
+def _workspace(need, given, device):
+    if given is not None and given.numel() >= need:
+        return given
+    return torch.empty(max(need, 16), dtype=torch.uint8, device=device)
 
 
 def uses_tensor_cores(q, v, chunk=64) -> bool:
@@ -139,17 +153,19 @@ def uses_tensor_cores(q, v, chunk=64) -> bool:
     return bool(lib().gdn_uses_tensor_cores(ctypes.byref(s)))
 
 
-def _fwd(kda, q, k, v, g, beta, h0=None, chunk=64, output_final_state=True, out=None):
+def _fwd(kda, q, k, v, g, beta, h0=None, chunk=64, output_final_state=True, out=None,
+         workspace=None):
     B, T, H, dk = q.shape
     dv = v.shape[3]
     _validate(q, k, v, g, beta, kda, [("h0", (h0, (B, H, dk, dv), torch.float32))])
     o = out if out is not None else torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     ht = (torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
           if output_final_state else None)
+    ws = _workspace(fwd_workspace_bytes(q, v, chunk, kda), workspace, q.device)
     s = make_shape(q, v, chunk)
     fn = lib().kda_fwd if kda else lib().gdn_fwd
     _check(fn(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
-              _ptr(ht), None, 0, _stream(q.device)))
+              _ptr(ht), _ptr(ws), ws.numel(), _stream(q.device)))
     return o, ht
 
 
@@ -162,10 +178,7 @@ def _bwd(kda, q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, works
     e = lambda x: torch.empty_like(x)
     dq, dk_, dv_, dg, dbeta = e(q), e(k), e(v), e(g), e(beta)
     dh0 = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device) if want_dh0 else None
-    need = bwd_workspace_bytes(q, v, chunk, kda)
-    ws = workspace
-    if ws is None or ws.numel() < need:
-        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws = _workspace(bwd_workspace_bytes(q, v, chunk, kda), workspace, q.device)
     s = make_shape(q, v, chunk)
     fn = lib().kda_bwd if kda else lib().gdn_bwd
     _check(fn(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(do),
@@ -174,14 +187,16 @@ def _bwd(kda, q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, works
     return {"dq": dq, "dk": dk_, "dv": dv_, "dg": dg, "dbeta": dbeta, "dh0": dh0}
 
 
-def gdn_fwd(q, k, v, g, beta, h0=None, chunk=64, output_final_state=True):
-    """GDN forward.  Returns ``(o, ht)`` (``ht`` None if not requested)."""
-    return _fwd(False, q, k, v, g, beta, h0, chunk, output_final_state)
+def gdn_fwd(q, k, v, g, beta, h0=None, chunk=64, output_final_state=True, workspace=None):
+    """GDN forward.  Returns ``(o, ht)`` (``ht`` None if not requested).  ``workspace``
+    (uint8 CUDA tensor) is used when it holds ``fwd_workspace_bytes`` bytes, else one
+    is allocated."""
+    return _fwd(False, q, k, v, g, beta, h0, chunk, output_final_state, workspace=workspace)
 
 
-def kda_fwd(q, k, v, g, beta, h0=None, chunk=64, output_final_state=True):
+def kda_fwd(q, k, v, g, beta, h0=None, chunk=64, output_final_state=True, workspace=None):
     """KDA forward (``g`` is ``[B,T,H,dk]``).  Returns ``(o, ht)``."""
-    return _fwd(True, q, k, v, g, beta, h0, chunk, output_final_state)
+    return _fwd(True, q, k, v, g, beta, h0, chunk, output_final_state, workspace=workspace)
 
 
 def gdn_bwd(q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, workspace=None):

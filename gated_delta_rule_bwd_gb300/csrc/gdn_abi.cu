@@ -47,6 +47,11 @@ int check_shape(const gdn_shape* s, bool kda, gdn::Problem* p) {
 
 bool empty(const gdn::Problem& p) { return p.B == 0 || p.H == 0; }
 
+size_t fwd_ws(const gdn::Problem& p) {
+  if (empty(p) || p.T == 0) return 0;
+  return gdn::tc_supported(p) ? gdn::tc_fwd_workspace(p) : 0;
+}
+
 size_t bwd_ws(const gdn::Problem& p) {
   if (empty(p) || p.T == 0) return 0;
   return gdn::tc_supported(p) ? gdn::tc_bwd_workspace(p) : gdn::simt_bwd_workspace(p);
@@ -71,7 +76,7 @@ int run_fwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
   if (empty(p)) return GDN_OK;
   // token tensors of an empty sequence hold no data and may be NULL
   if (p.T > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_ARG;
-  const void* ptrs[] = {q, k, v, g, beta, h0, o, ht};
+  const void* ptrs[] = {q, k, v, g, beta, h0, o, ht, ws};
   for (const void* x : ptrs)
     if (x && !aligned16(x)) return GDN_ERR_ALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -79,6 +84,8 @@ int run_fwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
     cudaError_t e = copy_state_or_zero(ht, h0, p, st);
     return e == cudaSuccess ? GDN_OK : fail_cuda(e);
   }
+  const size_t need = fwd_ws(p);
+  if (need > 0 && (!ws || ws_bytes < need)) return GDN_ERR_WORKSPACE;
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.o = o; p.ht = ht;
   p.ws = ws; p.ws_bytes = ws_bytes;
   cudaError_t e = gdn::tc_supported(p) ? gdn::tc_fwd(p, st) : gdn::simt_fwd(p, st);
@@ -112,10 +119,10 @@ int run_bwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
   return e == cudaSuccess ? GDN_OK : fail_cuda(e);
 }
 
-size_t query_ws(const gdn_shape* shape, bool kda) {
+size_t query_ws(const gdn_shape* shape, bool kda, bool bwd) {
   gdn::Problem p;
   if (check_shape(shape, kda, &p) != GDN_OK) return 0;
-  return bwd_ws(p);
+  return bwd ? bwd_ws(p) : fwd_ws(p);
 }
 
 }  // namespace
@@ -125,7 +132,7 @@ namespace gdn {
 const char* kernel_name(int id) {
   static const char* names[kNumKernelIds] = {
       "simt_fwd", "simt_states", "simt_bwd", "simt_bwd_reduce",
-      "tc_fwd", "tc_states", "tc_bwd", "tc_bwd_reduce"};
+      "tc_fwd", "tc_states", "tc_bwd", "tc_solve"};
   return (id >= 0 && id < kNumKernelIds) ? names[id] : "unknown";
 }
 
@@ -185,8 +192,10 @@ int gdn_profile_read(int* kernel_ids, float* ms, int max) {
 
 const char* gdn_kernel_name(int kernel_id) { return gdn::kernel_name(kernel_id); }
 
-size_t gdn_bwd_workspace(const gdn_shape* shape) { return query_ws(shape, false); }
-size_t kda_bwd_workspace(const gdn_shape* shape) { return query_ws(shape, true); }
+size_t gdn_fwd_workspace(const gdn_shape* shape) { return query_ws(shape, false, false); }
+size_t kda_fwd_workspace(const gdn_shape* shape) { return query_ws(shape, true, false); }
+size_t gdn_bwd_workspace(const gdn_shape* shape) { return query_ws(shape, false, true); }
+size_t kda_bwd_workspace(const gdn_shape* shape) { return query_ws(shape, true, true); }
 
 int gdn_fwd(const gdn_shape* shape, const void* q, const void* k, const void* v, const float* g,
             const float* beta, const float* h0, void* o, float* ht, void* ws, size_t ws_bytes,

@@ -30,6 +30,7 @@ cudaError_t simt_bwd(const Problem& p, cudaStream_t s);
 
 // Tensor-core kernels (bf16, dk = dv = 128, chunk = 64).
 bool tc_supported(const Problem& p);
+size_t tc_fwd_workspace(const Problem& p);
 size_t tc_bwd_workspace(const Problem& p);
 cudaError_t tc_fwd(const Problem& p, cudaStream_t s);
 cudaError_t tc_bwd(const Problem& p, cudaStream_t s);
@@ -43,7 +44,7 @@ enum KernelId {
   kTcFwd = 4,
   kTcStates = 5,
   kTcBwd = 6,
-  kTcBwdReduce = 7,
+  kTcSolve = 7,
   kNumKernelIds = 8
 };
 const char* kernel_name(int id);

@@ -1,28 +1,33 @@
 // Tensor-core (tcgen05 / TMEM / TMA) kernels for the GDN mixer: bf16 inputs,
 // dk = dv = 128, chunk C = 64, fp32 state and accumulation.
 //
-// One CTA (128 threads = the 128 TMEM lanes) owns one (batch, head) sequence
-// and walks its chunks in order.  The state is held transposed, G = H^T
-// (dv x dk, row c = value dimension), as fp32 in registers (thread c owns
-// row c) with a bf16 copy in shared memory as the MMA operand.  Per chunk
-// (Q, K, V tiles of 64 x 128 loaded by TMA with 128-byte swizzle; gamma =
-// within-chunk cumulative log gate, e = exp(gamma), f = exp(gamma_last -
-// gamma), eC = exp(gamma_last)):
+// Notation (gamma = within-chunk cumulative log gate, e = exp(gamma),
+// f = exp(gamma_last - gamma), eC = exp(gamma_last), Gam[r][j] =
+// exp(gamma_r - gamma_j)):
+//   A = strict_lower(beta_r K K^T o Gam),  T = (I + A)^-1,
+//   P = lower(Q K^T o Gam),  W = T diag(beta e) K,  U = T diag(beta)(V - eK H).
 //
-//   MMA1  [K;Q] K^T          -> K K^T (lanes 0-63), Q K^T (lanes 64-127)
-//         A = strict_lower(beta_r K K^T o Gam),  P = lower(Q K^T o Gam)
-//         T = (I + A)^-1 on CUDA cores (blocked 16 x 16 solve)
-//         T' = T diag(beta e),  T'' = T diag(beta)
-//   MMA2  W^T  = K^T T'^T                       (W = T diag(beta e) K)
-//   MMA3  U^T  = V^T T''^T - G W^T              (U = T diag(beta)(V - eK H))
-//   MMA4  O    = (eQ) G^T + P U                 (M = 64: rows are tokens)
-//   MMA5  dG   = (U diag(f))^T K                (G' = eC G + dG)
+// Three kernels:
+//   solve     one CTA per chunk, all chunks at once: MMA1 K K^T, A, and the
+//             blocked triangular solve; writes T as a bf16 64 x 64 tile in
+//             MMA-operand layout (8 KB per chunk) to the workspace.
+//   forward   one CTA per (batch, head) walking its chunks in order.  The
+//             state is held transposed, G = H^T (dv x dk), fp32 in TMEM with
+//             a bf16 copy in shared memory as the MMA operand.  Per chunk:
+//               MMA   Q K^T -> P
+//               MMA2  W^T = K^T T'^T, T' = T diag(beta e)
+//               MMA3  U^T = V^T T''^T - G W^T, T'' = T diag(beta)
+//               MMA4  O = (eQ) G^T + P U          (M = 64: rows are tokens)
+//               MMA5  G <- eC G + (U diag(f))^T K
+//             In states mode (for the backward pass) it skips P and O and
+//             dumps every chunk's entry state.
+//   backward  the reverse chunk scan (described at its kernel).
 //
-// Every product has M = 128.  The TMA tiles of K and V serve both as K-major
-// operands (rows = tokens) and, through MN-major descriptors, as their own
-// transposes, so nothing is transposed in software.  MMAs are issued by one
-// thread and complete on an mbarrier; every wait is bounded and a timeout is
-// reported through the device status word instead of hanging.
+// The TMA tiles of K and V serve both as K-major operands (rows = tokens) and,
+// through MN-major descriptors, as their own transposes, so nothing is
+// transposed in software.  MMAs are issued by one thread and complete on an
+// mbarrier; every wait is bounded and a timeout is reported through the device
+// status word instead of hanging.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -57,8 +62,10 @@ constexpr int D = 128;    // dk = dv
 // ---------------------------------------------------------------- forward shared memory
 // Offsets in bytes from a 1024-aligned base.  Two K|Q stages hold
 // [K d0-63 | Q d0-63 | K d64-127 | Q d64-127] (8 KB each) so that [K;Q] is one
-// 128-row operand; V is single-buffered (only the preparation reads it).
-constexpr int kLdF = 68;                   // fp32 row stride of the solve scratch (16-byte rows)
+// 128-row operand, each with the chunk's T tile; V is single-buffered (only
+// the preparation reads it).
+constexpr int kLdF = 68;                   // fp32 row stride of A and T in the solve (16-byte rows)
+constexpr int kSolveScratch = 32 * 36;     // largest solve scratch use: the 32 x 32 product, row stride 36
 constexpr int kF_KQ = 0;                   // 2 x 32 KB
 constexpr int kF_V = 65536;                // 16 KB
 constexpr int kF_G = 81920;                // G bf16, K-major [c][d], 2 x 16 KB
@@ -67,12 +74,11 @@ constexpr int kF_P = 131072;               // 2 x P [r][j]                (8 KB 
 constexpr int kF_T1 = 147456;              // T' = T diag(beta e) [r][j]  (8 KB)
 constexpr int kF_T0 = 155648;              // T'' = T diag(beta) [r][j]   (8 KB)
 constexpr int kF_U = 163840;               // U^T [c][j] K-major          (16 KB)
-constexpr int kF_SOLVE = 180224;           // A, T fp32 [64][kLdF] + kSolveScratch floats
-constexpr int kSolveScratch = 32 * 36;     // largest scratch use: the 32 x 32 product, row stride 36
-constexpr int kSolveBytes = (2 * 64 * kLdF + kSolveScratch) * 4;   // A, T [64][kLdF] + scratch
-constexpr int kF_GATE = kF_SOLVE + kSolveBytes;
+constexpr int kF_TR = 180224;              // 2 x T [r][j] as written by the solve kernel (8 KB each)
+constexpr int kF_GATE = kF_TR + 2 * 8192;
 constexpr int kGateBlock = 1600;           // gamma, e, f, beta, er, ie [64] each, eC, fast; two blocks
-constexpr int kF_BAR = kF_GATE + 2 * kGateBlock;
+constexpr int kF_GRAW = kF_GATE + 2 * kGateBlock;  // 2 x 128 raw g, beta (prefetch)
+constexpr int kF_BAR = kF_GRAW + 2 * 512;
 constexpr int kSmemBytes = kF_BAR + 128 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
@@ -91,6 +97,7 @@ struct FwdParams {
                           // ([B*H][N][32 KB], shared-memory layout)
   const float* dht;       // with states: d(final state), for dht_dot
   float* dht_dot;         // with states: <dht, ht> per sequence
+  const unsigned char* tiles;  // T of every chunk ([B*H][N][8 KB], from the solve kernel)
   int B, T, H, N;
 };
 
@@ -106,13 +113,23 @@ __device__ __forceinline__ void cta_sync() {
   tc_fence_after();
 }
 
+// 1-D bulk copy global -> shared completing on an mbarrier (16-byte aligned
+// addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void report_timeout() { atomicExch(&g_device_status, GDN_ERR_DEVICE_TIMEOUT); }
 
 // ---------------------------------------------------------------- forward kernel
 //
 // Warp-specialised, 512 threads.  Warps 8-15 (the preparation group) run the
-// state-independent part of chunk c+1: MMA1, A and P, the triangular solve,
-// T' and T'', MMA2/MMA3a.  Warps 0-7 (the chain group) meanwhile run chunk c:
+// state-independent part of chunk c+1: the gates, T' and T'' from the loaded
+// T tile, Q K^T and P, MMA2/MMA3a.  Warps 0-7 (the chain group) meanwhile run chunk c:
 // the W tile from W^T, the row scalings eQ and fK, MMA3b/MMA4a, U^T,
 // MMA4b/MMA5, the output and the next state tile.
 // Warp w reads TMEM lane quadrant w % 4 and handles column half (w / 4) % 2
@@ -360,6 +377,29 @@ __device__ __forceinline__ void chunk_gates(const GateView& G, float g0, float g
   }
 }
 
+// The gates of the next chunk are prefetched by one warp with asynchronous
+// 4-byte copies into a raw block [g rows 0-31 | g rows 32-63 | beta rows 0-31 |
+// beta rows 32-63] (128 floats; rows past the sequence end read as zero), so
+// that their global-memory latency stays off the chunk's critical path.
+__device__ __forceinline__ void prefetch_gates(float* raw, const float* g, const float* beta, int b,
+                                               int T, int H, int h, int ci, int lane) {
+  const int t0 = ci * C, n = min(C, T - t0);
+  const size_t base = ((size_t)b * T + t0) * H + h;
+  const size_t o0 = lane < n ? base + (size_t)lane * H : base;
+  const size_t o1 = lane + 32 < n ? base + (size_t)(lane + 32) * H : base;
+  cp_async4(raw + lane, g + o0, lane < n);
+  cp_async4(raw + 32 + lane, g + o1, lane + 32 < n);
+  cp_async4(raw + 64 + lane, beta + o0, lane < n);
+  cp_async4(raw + 96 + lane, beta + o1, lane + 32 < n);
+  cp_async_commit();
+}
+
+// chunk_gates from a prefetched raw block (each lane reads only what it copied)
+__device__ __forceinline__ void chunk_gates_raw(const GateView& G, const float* raw, int lane) {
+  cp_async_wait_all();
+  chunk_gates(G, raw[lane], raw[32 + lane], raw[64 + lane], raw[96 + lane], lane);
+}
+
 // Decayed row: v[i] <- v[i] * Gam[r][j0 + i] for j0 + i <= r (or < r when
 // strict), 0 above; n columns.
 template <int n>
@@ -409,9 +449,6 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_kq + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* cnt = reinterpret_cast<int*>(tmem_slot + 2);  // [0..1] kq issued, [2..3] kq waited, [4] v issued, [5] v waited, [6] early MMA1
-  float* Am = reinterpret_cast<float*>(sm + kF_SOLVE);
-  float* Tm = Am + 64 * kLdF;
-  float* Sm = Tm + 64 * kLdF;
 
   if (tid == 0) {
     for (int i = 0; i < 8; ++i) mbar_init(&bar_kq[i], 1);
@@ -433,12 +470,13 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   auto load_kq = [&](int ci) {
     const int st = ci & 1;
     unsigned char* dst = sm + kF_KQ + st * 32768;
-    mbar_arrive_expect_tx(&bar_kq[st], 32768);
+    mbar_arrive_expect_tx(&bar_kq[st], 32768 + 8192);
     const int t0 = ci * C;
     tma_load_4d(dst + 0, &tm_k, &bar_kq[st], 0, h, t0, b);
     tma_load_4d(dst + 8192, &tm_q, &bar_kq[st], 0, h, t0, b);
     tma_load_4d(dst + 16384, &tm_k, &bar_kq[st], 64, h, t0, b);
     tma_load_4d(dst + 24576, &tm_q, &bar_kq[st], 64, h, t0, b);
+    bulk_load(sm + kF_TR + st * 8192, p.tiles + ((size_t)bh * p.N + ci) * 8192, 8192, &bar_kq[st]);
     cnt[st] += 1;
   };
   auto load_v = [&](int ci) {
@@ -621,7 +659,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (p.dht_dot) {
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        float* red = Sm;  // the solve scratch is idle once the preparation group is done
+        float* red = reinterpret_cast<float*>(sm + kF_TR);  // idle once every chunk is done
         group_sync(kBarChain, kGroup);
         if (lane == 0) red[warp] = acc;
         group_sync(kBarChain, kGroup);
@@ -636,16 +674,22 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // =========================== preparation group ===========================
     const int pt = tid - kGroup;
     auto psync = [&]() { group_sync(kBarPrep, kGroup); };
-    float pg0 = 0.f, pg1 = 0.f, pb0 = 0.f, pb1 = 0.f;
+    float* graw = reinterpret_cast<float*>(sm + kF_GRAW);
     auto load_gates = [&](int ci) {
-      const int t0 = ci * C, n = min(C, p.T - t0);
-      const size_t base = ((size_t)b * p.T + t0) * p.H + h;
-      pg0 = lane < n ? p.g[base + (size_t)lane * p.H] : 0.f;
-      pg1 = lane + 32 < n ? p.g[base + (size_t)(lane + 32) * p.H] : 0.f;
-      pb0 = lane < n ? p.beta[base + (size_t)lane * p.H] : 0.f;
-      pb1 = lane + 32 < n ? p.beta[base + (size_t)(lane + 32) * p.H] : 0.f;
+      prefetch_gates(graw + (ci & 1) * 128, p.g, p.beta, b, p.T, p.H, h, ci, lane);
     };
-    if (warp == 8) load_gates(0);
+    // Warp 9 (which issues nothing) computes each chunk's gates one chunk
+    // ahead, at the end of the previous chunk's preparation, from raw values
+    // prefetched one more chunk ahead; chunk 0's here.
+    auto gate_view = [&](int ci) {
+      float* gb = reinterpret_cast<float*>(sm + kF_GATE + (ci & 1) * kGateBlock);
+      return GateView{gb, gb + 64, gb + 128, gb + 192, gb + 256, gb + 320, gb + 384, gb + 385};
+    };
+    if (warp == 9) {
+      load_gates(0);
+      chunk_gates_raw(gate_view(0), graw, lane);
+      if (p.N > 1) load_gates(1);
+    }
     volatile int* early_mma1 = cnt + 6;
     if (pt == 0) *early_mma1 = 0;
     auto issue_mma1 = [&](int cn) {
@@ -666,67 +710,70 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const GateView GV{gates, gates + 64, gates + 128, gates + 192, gates + 256, gates + 320,
                         gates + 384, gates + 385};
       float* ee = GV.ee;
-      float* ff = GV.ff;
       float* bt = GV.bt;
       unsigned char* st = sm + kF_KQ + s * 32768;
       const uint32_t st_kq = smem_u32(st);
       ok = group_and(kBarPrep, kGroup, mbar_wait(&bar_kq[s], (ci >> 1) & 1) && !*abort_flag);
       if (!ok) break;
       if (pt == 0) cnt[2 + s] += 1;
-      if (pt == 0 && !*early_mma1) issue_mma1(ci);
-      if (warp == 8) {
-        // gates of this chunk (the previous user of this block finished with it
-        // before this stage's tiles were requested)
-        chunk_gates(GV, pg0, pg1, pb0, pb1, lane);
-        if (ci + 1 < p.N) load_gates(ci + 1);
-      }
-      ok = group_and(kBarPrep, kGroup, mbar_wait(bar_p1, ci & 1));
-      tc_fence_after();
-      if (!ok) break;
-      // A (rows 0-63, fp32) and P (rows 64-127, bf16): 32 columns per thread.
-      // Quadrants 0 and 2 hold rows 0-31 of A / P: their columns 32-63 are zero.
+      if (want_o && pt == 0 && !*early_mma1) issue_mma1(ci);
       {
-        float v[32];
-        const bool upper_zero = (quad == 0 || quad == 2) && half == 1;
-        if (!upper_zero && (row < 64 || want_o)) tmem_ld32(tmem + lane_base + kTmKQ + half * 32, v);
-        if (row < 64) {
-          const int r = row;
-          if (upper_zero) {
+        // T' = T diag(beta e) and T'' = T diag(beta): columns of the loaded T
+        // tile (same swizzled layout in and out).  This thread: 16-byte column
+        // chunk c8 of rows r and r + 32.
+        const int c8 = pt & 7, r0 = pt >> 3;
+        float sb[8], sbe[8];
+        {
+          const float4 b0 = *reinterpret_cast<const float4*>(bt + c8 * 8);
+          const float4 b1 = *reinterpret_cast<const float4*>(bt + c8 * 8 + 4);
+          const float4 e0 = *reinterpret_cast<const float4*>(ee + c8 * 8);
+          const float4 e1 = *reinterpret_cast<const float4*>(ee + c8 * 8 + 4);
+          const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+          const float e8[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
-          } else {
-            decay_row(v, GV, r, half * 32, true, bt[r]);
+          for (int k = 0; k < 8; ++k) {
+            sb[k] = bb[k];
+            sbe[k] = bb[k] * e8[k];
           }
+        }
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(Am + r * kLdF + half * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-        } else if (want_o) {  // P is read only by the output product
+        for (int rr = 0; rr < 2; ++rr) {
+          const int off = sw_row_off(r0 + 32 * rr, c8);
+          const uint4 raw = *reinterpret_cast<const uint4*>(sm + kF_TR + s * 8192 + off);
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+          uint4 o1, o0;
+          uint32_t* w1 = reinterpret_cast<uint32_t*>(&o1);
+          uint32_t* w0 = reinterpret_cast<uint32_t*>(&o0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 t = __bfloat1622float2(h2[k]);
+            __nv_bfloat162 x0 = __floats2bfloat162_rn(t.x * sb[2 * k], t.y * sb[2 * k + 1]);
+            __nv_bfloat162 x1 = __floats2bfloat162_rn(t.x * sbe[2 * k], t.y * sbe[2 * k + 1]);
+            w0[k] = *reinterpret_cast<uint32_t*>(&x0);
+            w1[k] = *reinterpret_cast<uint32_t*>(&x1);
+          }
+          *reinterpret_cast<uint4*>(sm + kF_T1 + off) = o1;
+          *reinterpret_cast<uint4*>(sm + kF_T0 + off) = o0;
+        }
+      }
+      if (want_o) {
+        ok = group_and(kBarPrep, kGroup, mbar_wait(bar_p1, ci & 1));
+        tc_fence_after();
+        if (!ok) break;
+        // P (TMEM lanes 64-127): 32 columns per thread; quadrant 2 holds rows
+        // 0-31, whose columns 32-63 are zero
+        if (row >= 64) {
           const int r = row - 64;
-          if (upper_zero) {
+          float v[32];
+          if (quad == 2 && half == 1) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
           } else {
+            tmem_ld32(tmem + lane_base + kTmKQ + half * 32, v);
             decay_row(v, GV, r, half * 32, false, 1.f);
           }
           store_chunks(sm + kF_P + s * 8192, r, half * 4, v, 4);
         }
-      }
-      tc_fence_before();
-      psync();
-      solve_unit_lower(Am, Tm, Sm, pt, kGroup, psync);
-      // T' = T diag(beta e) and T'' = T diag(beta): 16 values per thread (row r, two chunks)
-      {
-        const int r = pt >> 2, c0 = (pt & 3) * 2;
-        float v1[16], v0[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int j = c0 * 8 + i;
-          const float t = (j <= r) ? Tm[r * kLdF + j] * bt[j] : 0.f;
-          v0[i] = t;
-          v1[i] = t * ee[j];
-        }
-        store_chunks(sm + kF_T1, r, c0, v1, 2);
-        store_chunks(sm + kF_T0, r, c0, v0, 2);
       }
       ok = group_and(kBarPrep, kGroup, mbar_wait(bar_v, ci & 1));
       if (!ok) break;
@@ -752,14 +799,20 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                    sw128_desc(smem_u32(sm + kF_T0) + ks * 32, 16, 1024), id2, ks > 0);
         mma_commit(bar_p);
       }
+      if (warp == 9 && ci + 1 < p.N) {
+        // gates of the next chunk: its block was last read by the chain for
+        // chunk ci - 1, which has released it (the w_free wait above)
+        chunk_gates_raw(gate_view(ci + 1), graw + ((ci + 1) & 1) * 128, lane);
+        if (ci + 2 < p.N) load_gates(ci + 2);
+      }
       ok = group_and(kBarPrep, kGroup, mbar_wait(bar_p, p_phase));
       p_phase ^= 1;
       tc_fence_after();
       if (!ok) break;
       if (pt == 0 && ci + 1 < p.N) load_v(ci + 1);
-      if (pt == 0) {
-        // K K^T | Q K^T is free again: start the next chunk's MMA1 now if its
-        // tiles have landed (otherwise it is issued at the top of that chunk)
+      if (want_o && pt == 0) {
+        // the Q K^T columns are free again: start the next chunk's MMA1 now if
+        // its tiles have landed (otherwise it is issued at the top of that chunk)
         const int cn = ci + 1;
         *early_mma1 = (cn < p.N && mbar_try_wait(&bar_kq[cn & 1], (cn >> 1) & 1)) ? 1 : 0;
         if (*early_mma1) issue_mma1(cn);
@@ -781,8 +834,137 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int k = cnt[5]; k < cnt[4]; ++k) mbar_wait(bar_v, k & 1, 10000);
     }
   }
+  cp_async_wait_all();  // no gate prefetch may still be writing shared memory at exit
   cta_sync();
   if (warp == 0) tmem_dealloc(tmem, kTmCols);
+}
+
+// ---------------------------------------------------------------- solve kernel
+//
+// One CTA of 256 threads per chunk, every chunk of every sequence at once (the
+// solve does not depend on the state):
+//   MMA1  K K^T (M = 64: row r in TMEM lane 32 (r / 16) + r % 16)
+//         A = strict_lower(beta_r K K^T o Gam)            (fp32, shared memory)
+//         T = (I + A)^-1                                   (solve_unit_lower)
+// T is written as a bf16 64 x 64 tile, zero above the diagonal, in the
+// K-major 128-byte-swizzled layout of an MMA operand, so that the scans copy
+// it into shared memory unchanged (8 KB per chunk, [B*H][N] order).
+// About 53 KB of shared memory and 64 TMEM columns: four CTAs per SM.
+
+constexpr int ST = 256;
+constexpr int kS_K = 0;                            // [K d0-63 | K d64-127]; solve scratch after MMA1
+constexpr int kS_A = 16384;                        // A fp32 [64][kLdF]
+constexpr int kS_T = kS_A + 64 * kLdF * 4;         // T fp32 [64][kLdF]
+constexpr int kS_GATE = kS_T + 64 * kLdF * 4;      // one gate block
+constexpr int kS_BAR = kS_GATE + kGateBlock;
+constexpr int kSolveSmemBytes = kS_BAR + 64 + 1024;  // + alignment slack
+static_assert(kSolveScratch * 4 <= 16384, "solve scratch fits the K tile");
+static_assert(4 * (kSolveSmemBytes + 1024) <= 228 * 1024, "four solve CTAs per SM");
+
+struct SolveParams {
+  const float* g;
+  const float* beta;
+  unsigned char* tiles;  // [B*H][N][8 KB]
+  int B, T, H, N;
+};
+
+__global__ void __launch_bounds__(ST)
+gdn_tc_solve_kernel(const __grid_constant__ CUtensorMap tm_k, SolveParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
+  const int quad = warp & 3, half = warp >> 2;
+  const int bh = blockIdx.x / p.N, ci = blockIdx.x % p.N, b = bh / p.H, h = bh % p.H;
+  const int t0 = ci * C, n = min(C, p.T - t0);
+  float* gates = reinterpret_cast<float*>(sm + kS_GATE);
+  const GateView GV{gates, gates + 64, gates + 128, gates + 192, gates + 256, gates + 320,
+                    gates + 384, gates + 385};
+  float* Am = reinterpret_cast<float*>(sm + kS_A);
+  float* Tm = reinterpret_cast<float*>(sm + kS_T);
+  float* Sm = reinterpret_cast<float*>(sm + kS_K);
+  uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + kS_BAR);
+  uint64_t* bar_mma = bar_ld + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma + 1);
+
+  if (tid == 0) {
+    mbar_init(bar_ld, 1);
+    mbar_init(bar_mma, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(bar_ld, 16384);
+    tma_load_4d(sm + kS_K, &tm_k, bar_ld, 0, h, t0, b);
+    tma_load_4d(sm + kS_K + 8192, &tm_k, bar_ld, 64, h, t0, b);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 64);
+    tmem_relinquish();
+  }
+  if (warp == 1) {
+    const size_t base = ((size_t)b * p.T + t0) * p.H + h;
+    const float g0 = lane < n ? p.g[base + (size_t)lane * p.H] : 0.f;
+    const float g1 = lane + 32 < n ? p.g[base + (size_t)(lane + 32) * p.H] : 0.f;
+    const float b0 = lane < n ? p.beta[base + (size_t)lane * p.H] : 0.f;
+    const float b1 = lane + 32 < n ? p.beta[base + (size_t)(lane + 32) * p.H] : 0.f;
+    chunk_gates(GV, g0, g1, b0, b1, lane);
+  }
+  cta_sync();
+  const uint32_t tmem = *tmem_slot;
+  bool loaded = __syncthreads_and(mbar_wait(bar_ld, 0));
+  bool ok = loaded;
+  if (ok) {
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t sk = smem_u32(sm + kS_K);
+      const uint32_t id = idesc_bf16(64, 64, false, false);
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t off = (ks / 4) * 8192 + (ks % 4) * 32;
+        mma_bf16(tmem, sw128_desc(sk + off, 16, 1024), sw128_desc(sk + off, 16, 1024), id, ks > 0);
+      }
+      mma_commit(bar_mma);
+    }
+    ok = __syncthreads_and(mbar_wait(bar_mma, 0));
+    tc_fence_after();
+  }
+  if (ok) {
+    // A rows 16 quad + lane (lanes 0-15), columns 32 half + [0, 32)
+    float v[32];
+    tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + half * 32, v);
+    if (lane < 16) {
+      const int r = quad * 16 + lane;
+      decay_row(v, GV, r, half * 32, true, GV.bt[r]);
+#pragma unroll
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(Am + r * kLdF + half * 32 + i) =
+            make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    }
+    __syncthreads();
+    solve_unit_lower(Am, Tm, Sm, tid, ST, [] { __syncthreads(); });
+    // row r = tid / 4, 16-byte chunks 2 (tid % 4) + {0, 1}
+    const int r = tid >> 2;
+    unsigned char* dst = p.tiles + ((size_t)bh * p.N + ci) * 8192;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int c8 = (tid & 3) * 2 + k;
+      uint4 pk;
+      uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = c8 * 8 + 2 * i;
+        const float x0 = j <= r ? Tm[r * kLdF + j] : 0.f;
+        const float x1 = j + 1 <= r ? Tm[r * kLdF + j + 1] : 0.f;
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(x0, x1);
+        w[i] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+      *reinterpret_cast<uint4*>(dst + sw_row_off(r, c8)) = pk;
+    }
+  } else if (tid == 0) {
+    report_timeout();
+    // nothing may still be writing this CTA's shared memory or TMEM at exit (bounded)
+    if (!loaded) mbar_wait(bar_ld, 0, 10000);
+    else mbar_wait(bar_mma, 0, 10000);
+  }
+  cta_sync();
+  if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
 // ---------------------------------------------------------------- backward kernel
@@ -790,12 +972,14 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 // Reverse chunk scan, one CTA per sequence.  The running state gradient is
 // held transposed, dG = dH^T (dv x dk), fp32 in registers (thread c owns row
 // c) with a bf16 copy in shared memory.  Each chunk's entry state G_in comes
-// from the workspace (written by the forward kernel in states mode).  With
-// R = V - diag(e) K H_in, U = T diag(beta) R, T = (I + A)^-1:
+// from the workspace (written by the forward kernel in states mode), and so
+// does its T tile (written by the solve kernel).  With R = V - diag(e) K H_in,
+// U = T diag(beta) R, T = (I + A)^-1:
 //
-//   MMA1  [K;Q] K^T                -> K K^T (kept in TMEM), Q K^T -> P
-//   MMA   -G_in K^T                -> R^T = V^T + (-G_in K^T) diag(e)
-//   MMA   dG K^T, dO^T P           -> dU^T = (dG K^T) diag(f) + dO^T P
+//   MMA1  [K;Q] K^T, -G_in K^T, dG K^T  (one batch)
+//                                  -> K K^T (kept in TMEM), Q K^T -> P,
+//                                     R^T = V^T + (-G_in K^T) diag(e)
+//   MMA   dO^T P                   -> dU^T = (dG K^T) diag(f) + dO^T P
 //   MMA   U^T = (R^T diag beta) T^T,  dZ^T = dU^T T     (dZ = (I+A)^-T dU)
 //   MMA   [dZ; dO] U^T             -> dA = -strict_lower(dZ U^T), dP = dO U^T
 //   MMA   dG_in = eC dG + (e dO)^T Q - (e dR)^T K       (dR = diag(beta) dZ)
@@ -822,9 +1006,9 @@ constexpr int kB_X = kB_P + 8192;        // three 16 KB slots, reused by phase
 constexpr int kB_GATE = kB_X + 3 * 16384;  // gam, e, f, beta, er, ie, db1, db2, dlc [64] each, eC, fast
 constexpr int kB_RED = kB_GATE + 9 * 256 + 16;  // reduction scratch [16][64] floats
 constexpr int kB_EC = kB_RED + 4096;
-constexpr int kB_BAR = kB_EC + 64;
+constexpr int kB_GRAW = kB_EC + 64;     // 2 x 128 raw g, beta (prefetch)
+constexpr int kB_BAR = kB_GRAW + 2 * 512;
 constexpr int kBwdSmemBytes = kB_BAR + 128 + 1024;
-static_assert(kSolveBytes <= 3 * 16384, "solve scratch fits the X slots");
 static_assert(kBwdSmemBytes <= 227 * 1024, "shared memory budget");
 
 // TMEM columns of the backward kernel
@@ -844,16 +1028,9 @@ struct BwdParams {
   float* dg;
   float* dbeta;
   float* dh0;
+  const unsigned char* tiles;    // T of every chunk ([B*H][N][8 KB], from the solve kernel)
   int B, T, H, N;
 };
-
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
 
 // Each thread holds v[i] for tile column (16 cg + i) of its row; returns in
 // out[r] (r < 64) the sum over all 128 rows.  Within a warp: four halving
@@ -916,9 +1093,6 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   uint64_t* bar_load = reinterpret_cast<uint64_t*>(sm + kB_BAR);
   uint64_t* bar_mma = bar_load + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma + 1);
-  float* Am = reinterpret_cast<float*>(sm + kB_X);
-  float* Tm = Am + 64 * kLdF;
-  float* Sm = Tm + 64 * kLdF;
   const uint32_t sKQ = smem_u32(sm + kB_KQ), sZO = smem_u32(sm + kB_ZO);
   const uint32_t sGI = smem_u32(sm + kB_GI), sDG = smem_u32(sm + kB_DG);
   const uint32_t sT = smem_u32(sm + kB_T), sP = smem_u32(sm + kB_P);
@@ -964,14 +1138,9 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // <dH_out, H_out> of the chunk being processed (the last chunk: <dht, ht>)
   float carry = p.dht_dot ? p.dht_dot[bh] : 0.f;
 
-  float pg0 = 0.f, pg1 = 0.f, pb0 = 0.f, pb1 = 0.f;
+  float* graw = reinterpret_cast<float*>(sm + kB_GRAW);
   auto load_gates = [&](int ci) {
-    const int t0 = ci * C, n = min(C, p.T - t0);
-    const size_t base = ((size_t)b * p.T + t0) * p.H + h;
-    pg0 = lane < n ? p.g[base + (size_t)lane * p.H] : 0.f;
-    pg1 = lane + 32 < n ? p.g[base + (size_t)(lane + 32) * p.H] : 0.f;
-    pb0 = lane < n ? p.beta[base + (size_t)lane * p.H] : 0.f;
-    pb1 = lane + 32 < n ? p.beta[base + (size_t)(lane + 32) * p.H] : 0.f;
+    prefetch_gates(graw + (ci & 1) * 128, p.g, p.beta, b, p.T, p.H, h, ci, lane);
   };
   if (warp == 0) load_gates(p.N - 1);
 
@@ -988,7 +1157,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     fence_async_shared();
     cta_sync();
     if (tid == 0) {
-      mbar_arrive_expect_tx(bar_load, 8 * 8192 + 32768);
+      mbar_arrive_expect_tx(bar_load, 8 * 8192 + 32768 + 8192);
       tma_load_4d(sm + kB_KQ + 0, &tm_k, bar_load, 0, h, t0, b);
       tma_load_4d(sm + kB_KQ + 8192, &tm_q, bar_load, 0, h, t0, b);
       tma_load_4d(sm + kB_KQ + 16384, &tm_k, bar_load, 64, h, t0, b);
@@ -998,6 +1167,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       tma_load_4d(sm + kB_V, &tm_v, bar_load, 0, h, t0, b);
       tma_load_4d(sm + kB_V + 8192, &tm_v, bar_load, 64, h, t0, b);
       bulk_load(sm + kB_GI, p.states + ((size_t)bh * p.N + ci) * 32768, 32768, bar_load);
+      bulk_load(sm + kB_T, p.tiles + ((size_t)bh * p.N + ci) * 8192, 8192, bar_load);
       if (ci > 0) {
         // the next chunk in the reverse scan: start pulling its tiles into L2
         const int tp = t0 - C;
@@ -1010,67 +1180,45 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tma_prefetch_l2_4d(&tm_v, 0, h, tp, b);
         tma_prefetch_l2_4d(&tm_v, 64, h, tp, b);
         bulk_prefetch_l2(p.states + ((size_t)bh * p.N + ci - 1) * 32768, 32768);
+        bulk_prefetch_l2(p.tiles + ((size_t)bh * p.N + ci - 1) * 8192, 8192);
       }
     }
     if (warp == 0) {
-      chunk_gates(GV, pg0, pg1, pb0, pb1, lane);
+      chunk_gates_raw(GV, graw + (ci & 1) * 128, lane);
       if (ci > 0) load_gates(ci - 1);
     }
     ok = __syncthreads_and(mbar_wait(bar_load, load_phase));
     load_phase ^= 1;
     if (!ok) break;
-    // ---- MMA1: [K;Q] K^T
+    // ---- MMA1: [K;Q] K^T;  -G_in K^T;  dG K^T
     if (tid == 0) {
       const uint32_t id = idesc_bf16(128, 64, false, false);
+      const uint32_t idn = idesc_bf16(128, 64, false, false, true);
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
         mma_bf16(tmem + kBtKQ, sw128_desc(sKQ + off, 16, 1024), sw128_desc(sKQ + off, 16, 1024), id,
+                 ks > 0);
+        mma_bf16(tmem + kBtR, sw128_desc(sGI + off, 16, 1024), sw128_desc(sKQ + off, 16, 1024), idn,
+                 ks > 0);
+        mma_bf16(tmem + kBtX1, sw128_desc(sDG + off, 16, 1024), sw128_desc(sKQ + off, 16, 1024), id,
                  ks > 0);
       }
       mma_commit(bar_mma);
     }
     mma_wait();
     if (!ok) break;
-    {
+    // P = lower(Q K^T o Gam) from TMEM lanes 64-127
+    if (row >= 64) {
+      const int r = row - 64;
       float v[16];
       tmem_ld16(tmem + lb + kBtKQ + cg * 16, v);
-      if (row < 64) {
-        const int r = row;
-        decay_row(v, GV, r, cg * 16, true, bt[r]);
-#pragma unroll
-        for (int i = 0; i < 16; i += 4)
-          *reinterpret_cast<float4*>(Am + r * kLdF + cg * 16 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-      } else {
-        const int r = row - 64;
-        decay_row(v, GV, r, cg * 16, false, 1.f);
-        store_chunks(sm + kB_P, r, cg * 2, v, 2);
-      }
-    }
-    cta_sync();
-    solve_unit_lower(Am, Tm, Sm, tid, BT, [] { __syncthreads(); });
-    {
-      const int r = tid >> 3, c8 = tid & 7;
-      float v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int j = c8 * 8 + i;
-        v[i] = (j <= r) ? Tm[r * kLdF + j] : 0.f;
-      }
-      store_chunks(sm + kB_T, r, c8, v, 1);
+      decay_row(v, GV, r, cg * 16, false, 1.f);
+      store_chunks(sm + kB_P, r, cg * 2, v, 2);
     }
     fence_async_shared();
     cta_sync();
-    // ---- -G_in K^T, dG K^T, dO^T P
+    // ---- dO^T P
     if (tid == 0) {
-      const uint32_t idn = idesc_bf16(128, 64, false, false, true);
-      const uint32_t id = idesc_bf16(128, 64, false, false);
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
-        mma_bf16(tmem + kBtR, sw128_desc(sGI + off, 16, 1024), sw128_desc(sKQ + off, 16, 1024), idn,
-                 ks > 0);
-        mma_bf16(tmem + kBtX1, sw128_desc(sDG + off, 16, 1024), sw128_desc(sKQ + off, 16, 1024), id,
-                 ks > 0);
-      }
       const uint32_t idmm = idesc_bf16(128, 64, true, true);
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16(tmem + kBtX2, sw128_desc(sZO + 8192 + ks * 2048, 16384, 1024),
@@ -1318,6 +1466,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
     for (int i = 0; i < 32; ++i) p.dh0[((size_t)bh * D + cg * 32 + i) * D + row] = dG[i];
   }
+  cp_async_wait_all();  // no gate prefetch may still be writing shared memory at exit
   cta_sync();
   if (warp == 0) tmem_dealloc(tmem, kTmCols);
 }
@@ -1352,8 +1501,23 @@ cudaError_t make_token_map(CUtensorMap* m, const void* ptr, const Problem& p) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// T tiles of every chunk into `tiles` ([B*H][N][8 KB])
+cudaError_t launch_solve(const Problem& p, cudaStream_t s, unsigned char* tiles) {
+  CUtensorMap mk;
+  cudaError_t e;
+  if ((e = make_token_map(&mk, p.k, p)) != cudaSuccess) return e;
+  SolveParams sp{p.g, p.beta, tiles, p.B, p.T, p.H, p.N};
+  e = cudaFuncSetAttribute(gdn_tc_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSolveSmemBytes);
+  if (e != cudaSuccess) return e;
+  prof_before(s);
+  gdn_tc_solve_kernel<<<(unsigned)((size_t)p.B * p.H * p.N), ST, kSolveSmemBytes, s>>>(mk, sp);
+  prof_after(s, kTcSolve);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fwd(const Problem& p, cudaStream_t s, bool want_out, __nv_bfloat16* states,
-                       float* dht_dot) {
+                       float* dht_dot, const unsigned char* tiles) {
   CUtensorMap mq, mk, mv;
   cudaError_t e;
   if ((e = make_token_map(&mq, p.q, p)) != cudaSuccess) return e;
@@ -1361,7 +1525,7 @@ cudaError_t launch_fwd(const Problem& p, cudaStream_t s, bool want_out, __nv_bfl
   if ((e = make_token_map(&mv, p.v, p)) != cudaSuccess) return e;
   FwdParams fp{p.g, p.beta, p.h0, want_out ? static_cast<__nv_bfloat16*>(p.o) : nullptr,
                want_out ? p.ht : nullptr, states, want_out ? nullptr : p.dht,
-               dht_dot, p.B, p.T, p.H, p.N};
+               dht_dot, tiles, p.B, p.T, p.H, p.N};
   e = cudaFuncSetAttribute(gdn_tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   prof_before(s);
@@ -1376,21 +1540,34 @@ bool tc_supported(const Problem& p) {
   return p.bf16 && !p.kda && p.dk == D && p.dv == D && p.C == C;
 }
 
+size_t tiles_bytes(const Problem& p) { return align_up((size_t)p.B * p.H * p.N * 8192, 256); }
+size_t states_bytes(const Problem& p) { return align_up((size_t)p.B * p.H * p.N * 32768, 256); }
+
+// Workspace of the tensor-core forward pass: the T tile of every chunk.
+size_t tc_fwd_workspace(const Problem& p) { return tiles_bytes(p); }
+
 // Workspace of the tensor-core backward pass: the bf16 entry state of every
-// chunk in MMA-operand layout (32 KB each), then <dht, ht> per sequence.
+// chunk in MMA-operand layout (32 KB each), the T tile of every chunk, then
+// <dht, ht> per sequence.
 size_t tc_bwd_workspace(const Problem& p) {
-  return align_up((size_t)p.B * p.H * p.N * 32768, 256) + align_up((size_t)p.B * p.H * 4, 256);
+  return states_bytes(p) + tiles_bytes(p) + align_up((size_t)p.B * p.H * 4, 256);
 }
 
 cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
-  return launch_fwd(p, s, true, nullptr, nullptr);
+  unsigned char* tiles = static_cast<unsigned char*>(p.ws);
+  cudaError_t e = launch_solve(p, s, tiles);
+  if (e != cudaSuccess) return e;
+  return launch_fwd(p, s, true, nullptr, nullptr, tiles);
 }
 
 cudaError_t tc_bwd(const Problem& p, cudaStream_t s) {
   unsigned char* ws = static_cast<unsigned char*>(p.ws);
   __nv_bfloat16* states = reinterpret_cast<__nv_bfloat16*>(ws);
-  float* dht_dot = reinterpret_cast<float*>(ws + align_up((size_t)p.B * p.H * p.N * 32768, 256));
-  cudaError_t e = launch_fwd(p, s, false, states, dht_dot);
+  unsigned char* tiles = ws + states_bytes(p);
+  float* dht_dot = reinterpret_cast<float*>(tiles + tiles_bytes(p));
+  cudaError_t e = launch_solve(p, s, tiles);
+  if (e != cudaSuccess) return e;
+  e = launch_fwd(p, s, false, states, dht_dot, tiles);
   if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv, mdo;
   if ((e = make_token_map(&mq, p.q, p)) != cudaSuccess) return e;
@@ -1400,7 +1577,7 @@ cudaError_t tc_bwd(const Problem& p, cudaStream_t s) {
   BwdParams bp{p.g, p.beta, p.dht, dht_dot,
                reinterpret_cast<const unsigned char*>(states), static_cast<__nv_bfloat16*>(p.dq),
                static_cast<__nv_bfloat16*>(p.dk_), static_cast<__nv_bfloat16*>(p.dv_), p.dg, p.dbeta,
-               p.dh0, p.B, p.T, p.H, p.N};
+               p.dh0, tiles, p.B, p.T, p.H, p.N};
   e = cudaFuncSetAttribute(gdn_tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kBwdSmemBytes);
   if (e != cudaSuccess) return e;

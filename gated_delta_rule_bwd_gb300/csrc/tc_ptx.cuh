@@ -74,6 +74,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return false;
 }
 
+// ------------------------------------------------------------------ small asynchronous copies
+
+// 4-byte global -> shared copy that completes in the background (cp.async);
+// with valid = false nothing is read and the destination is zero-filled.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 4u : 0u)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Waits until every cp.async of the calling thread has landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ------------------------------------------------------------------ proxies / fences
 
 // Generic-proxy shared-memory writes -> visible to the async proxy (MMA, TMA).

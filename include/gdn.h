@@ -32,9 +32,12 @@
  * respect to the tensors passed.
  *
  * Memory and streams.  Every pointer is a device pointer owned by the
- * caller and must be 16-byte aligned.  The library allocates nothing: the
- * backward pass needs a caller-provided device workspace of at least
- * *_bwd_workspace() bytes (the forward pass needs none; pass NULL/0).  All
+ * caller and must be 16-byte aligned.  The library allocates nothing: each
+ * pass needs a caller-provided device workspace of at least
+ * *_fwd_workspace() / *_bwd_workspace() bytes (0 for some shapes, where
+ * NULL/0 may be passed).  The workspace holds per-chunk intermediates of one
+ * call; its contents need no initialisation and are not meaningful
+ * afterwards, and two calls in flight at once need separate workspaces.  All
  * work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  * stream); the calls do not synchronise.  Outputs are overwritten, never
  * accumulated.  Results are deterministic (no atomics).
@@ -90,13 +93,20 @@ typedef struct {
 /* With T = 0 the token pointers may be NULL: the forward pass copies h0 to ht
  * (or zeroes ht), the backward pass copies dht to dh0 (or zeroes dh0).
  *
- * Workspace bytes the backward entry points need for this shape (0 if the
- * shape is invalid).  The forward entry points need none. */
+ * Workspace bytes each entry point needs for this shape (0 if the shape is
+ * invalid or needs none).  The tensor-core path of the forward pass keeps the
+ * chunkwise form's triangular-solve result T = (I + A)^-1 of every 64-token
+ * chunk (8 KB each, bf16); the backward pass keeps those plus the bf16 state
+ * entering every chunk (32 KB each), both recomputed from the inputs inside
+ * the call.  The CUDA-core fp32 path needs workspace for the backward pass
+ * only. */
+GDN_API size_t gdn_fwd_workspace(const gdn_shape* shape);
+GDN_API size_t kda_fwd_workspace(const gdn_shape* shape);
 GDN_API size_t gdn_bwd_workspace(const gdn_shape* shape);
 GDN_API size_t kda_bwd_workspace(const gdn_shape* shape);
 
 /* GDN forward: o (and ht if non-NULL) from q, k, v, g [B,T,H], beta and h0
- * (NULL = zero initial state).  ws/ws_bytes are unused (may be NULL/0). */
+ * (NULL = zero initial state).  ws must hold gdn_fwd_workspace() bytes. */
 GDN_API int gdn_fwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
             const float* g, const float* beta, const float* h0, void* o, float* ht,
             void* ws, size_t ws_bytes, void* stream);

@@ -104,6 +104,25 @@ def test_workspace_query_and_check(L):
     assert L.kda_bwd_workspace(ctypes.byref(big)) >= 2 * 4 * 32 * 128 * 128 * 4
     f32 = shape(B=2, T=2048, H=4, dk=128, dv=128, chunk=64, dtype=0)
     assert L.gdn_bwd_workspace(ctypes.byref(f32)) >= 2 * 4 * 32 * 128 * 128 * 4
+    # the tensor-core path also keeps T = (I + A)^-1 of every chunk (bf16 64 x 64)
+    assert L.gdn_bwd_workspace(ctypes.byref(big)) >= 2 * 4 * 32 * (128 * 128 + 64 * 64) * 2
+
+
+def test_forward_workspace_query_and_check(L):
+    big = shape(B=2, T=2048, H=4, dk=128, dv=128, chunk=64, dtype=1)
+    need = L.gdn_fwd_workspace(ctypes.byref(big))
+    assert need >= 2 * 4 * 32 * 64 * 64 * 2      # T of every chunk, bf16
+    assert need <= L.gdn_bwd_workspace(ctypes.byref(big))
+    assert call_fwd(L, big) == GDN_ERR_WORKSPACE
+    fn = L.gdn_fwd
+    args = (ctypes.byref(big), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None)
+    assert fn(*args, FAKE, need - 1, None) == GDN_ERR_WORKSPACE
+    assert fn(*args, ctypes.c_void_p(0x10008), need, None) == GDN_ERR_ALIGN
+    # the CUDA-core paths (fp32, KDA) need none
+    f32 = shape(B=2, T=2048, H=4, dk=128, dv=128, chunk=64, dtype=0)
+    assert L.gdn_fwd_workspace(ctypes.byref(f32)) == 0
+    assert L.kda_fwd_workspace(ctypes.byref(big)) == 0
+    assert L.gdn_fwd_workspace(ctypes.byref(shape(chunk=3))) == 0
 
 
 def test_empty_batch_is_a_no_op(L):
