@@ -215,8 +215,9 @@ __device__ __forceinline__ void store_c_tile(const float (&d)[4], float* C, int 
   *reinterpret_cast<float2*>(C + (m0 + g + 8) * ldc + n0 + 2 * q) = make_float2(d[2], d[3]);
 }
 
-// T = (I + A)^-1 for a 64 x 64 strictly lower A (fp32, row stride kLdF); T is
-// written with zeros above the diagonal.  Three steps:
+// T = (I + A)^-1 for a 64 x 64 strictly lower A (fp32, row stride kLdF).  T
+// is valid on and below the diagonal; above it only the entries that the
+// steps read are zeroed, so callers mask columns j > r.  Three steps:
 //  1. each 16 x 16 diagonal block by one warp: its two 8 x 8 diagonal blocks
 //     by forward substitution (one lane per column), then the 8 x 8 coupling
 //     T21 = -T22 (A21 T11);
@@ -281,12 +282,12 @@ __device__ void solve_unit_lower(const float* A, float* T, float* S, int t, int 
       T[(o + 8 + r) * kLdF + o + c] = -s0;
       T[(o + 8 + r) * kLdF + o + c + 1] = -s1;
     }
-  } else {
-    // zero the 16 x 16 blocks above the block diagonal
-    for (int i = t - 128; i < 64 * 64; i += nth - 128) {
-      const int rr = i >> 6, cc = i & 63;
-      if ((cc >> 4) > (rr >> 4)) T[rr * kLdF + cc] = 0.f;
-    }
+  } else if (t < 256) {
+    // zero the two 16 x 16 blocks above the block diagonal that steps 2 and 3
+    // read as operands: rows 0-15 x columns 16-31 and rows 32-47 x columns 48-63
+    const int i = t - 128, blk = i >> 6, rr = (i >> 2) & 15, c4 = (i & 3) * 4;
+    *reinterpret_cast<float4*>(T + (32 * blk + rr) * kLdF + 32 * blk + 16 + c4) =
+        make_float4(0.f, 0.f, 0.f, 0.f);
   }
   sync();
   // step 2: per 32 x 32 half b, S = A[2b+1][2b] T[2b][2b], T[2b+1][2b] = -T[2b+1][2b+1] S
