@@ -1063,6 +1063,14 @@ __device__ __forceinline__ void cta_sum_rows16(float (&v)[16], float* red, float
   __syncthreads();
 }
 
+// Writes x as the bf16 element (token r, feature d) of a [64 x 128] staging tile
+// made of two K-major 128-byte-swizzled halves (features 0-63, 64-127; 8 KB
+// each) -- the layout a TMA store of two 64 x 64 boxes reads.
+__device__ __forceinline__ void stage_bf16(unsigned char* tile2, int r, int d, float x) {
+  *reinterpret_cast<__nv_bfloat16*>(tile2 + (d >> 6) * 8192 + sw_row_off(r, (d & 63) >> 3) +
+                                    (d & 7) * 2) = __float2bfloat16_rn(x);
+}
+
 // bf16 element (row, col) of a swizzled 64-wide K-major tile
 __device__ __forceinline__ float tile_elem(const unsigned char* tile, int row, int col) {
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
@@ -1072,7 +1080,8 @@ __device__ __forceinline__ float tile_elem(const unsigned char* tile, int row, i
 __global__ void __launch_bounds__(BT, 1)
 gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  BwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                  const __grid_constant__ CUtensorMap tm_dv, BwdParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1155,6 +1164,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   for (int ci = p.N - 1; ci >= 0 && ok; --ci) {
     const int t0 = ci * C, n = min(C, p.T - t0);
+    if (tid == 0) bulk_wait_read_all();  // X0 / X1 staging of the previous chunk has been read
     fence_async_shared();
     cta_sync();
     if (tid == 0) {
@@ -1278,7 +1288,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int r = cg * 16 + i;
         const float vr = tile_elem(sm + kB_V + half * 8192, r, cc);
         const float dr = bt[r] * z[i];
-        if (r < n) p.dv[(((size_t)b * p.T + t0 + r) * p.H + h) * D + row] = __float2bfloat16_rn(dr);
+        stage_bf16(sm + kB_T, r, row, dr);  // dv; T and P have been read for the last time
         acc[i] = -vr * dr;                        // -v . dv
         rr[i] = z[i] * (vr + ee[r] * rr[i]);      // dZ_rc R_rc
         *reinterpret_cast<__nv_bfloat16*>(sm + kB_ZO + half * 16384 + sw_row_off(r, cc >> 3) +
@@ -1292,11 +1302,16 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     cta_sync();
     // ---- G4: [dZ; dO] U^T  (lanes 0-63: dZ U^T, lanes 64-127: dO U^T)
     if (tid == 0) {
+      // dv: TMA store of the staged tile (rows past T are not written)
+      tma_store_4d(&tm_dv, sm + kB_T, 0, h, t0, b);
+      tma_store_4d(&tm_dv, sm + kB_T + 8192, 64, h, t0, b);
+      bulk_commit_group();
       const uint32_t id = idesc_bf16(128, 64, false, true);
       for (int ks = 0; ks < 8; ++ks)
         mma_bf16(tmem + kBtX1, sw128_desc(sZO + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024),
                  sw128_desc(sX0 + ks * 2048, 16384, 1024), id, ks > 0);
       mma_commit(bar_mma);
+      bulk_wait_read_all();  // the staged dv is read before M and dP o Gam overwrite it
     }
     mma_wait();
     if (!ok) break;
@@ -1399,16 +1414,24 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int i = 0; i < 16; ++i) {
         const int r = cg * 16 + i;
         acc[i] += tile_elem(sm + kB_KQ + half * 16384 + 8192, r, cc) * x[i];
-        if (r < n) p.dq[(((size_t)b * p.T + t0 + r) * p.H + h) * D + row] = __float2bfloat16_rn(x[i]);
+        stage_bf16(sm + kB_X, r, row, x[i]);  // dq (X0 is free once the products are done)
       }
       tmem_ld16(tmem + lb + kBtU + cg * 16, x);  // dK^T row d, columns j
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int j = cg * 16 + i;
-        if (j < n) p.dk[(((size_t)b * p.T + t0 + j) * p.H + h) * D + row] = __float2bfloat16_rn(x[i]);
+        stage_bf16(sm + kB_X + 16384, j, row, x[i]);  // dk (X1)
       }
     }
-    cta_sum_rows16(acc, red, dlc);
+    fence_async_shared();
+    cta_sum_rows16(acc, red, dlc);  // (its barriers also publish the staged dq, dk)
+    if (tid == 0) {
+      tma_store_4d(&tm_dq, sm + kB_X, 0, h, t0, b);
+      tma_store_4d(&tm_dq, sm + kB_X + 8192, 64, h, t0, b);
+      tma_store_4d(&tm_dk, sm + kB_X + 16384, 0, h, t0, b);
+      tma_store_4d(&tm_dk, sm + kB_X + 24576, 64, h, t0, b);
+      bulk_commit_group();
+    }
     if (tid < 64) {
       const int r = tid;
       if (r < n) p.dbeta[((size_t)b * p.T + t0 + r) * p.H + h] = db1[r] + db2[r];
@@ -1467,6 +1490,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
     for (int i = 0; i < 32; ++i) p.dh0[((size_t)bh * D + cg * 32 + i) * D + row] = dG[i];
   }
+  if (tid == 0) bulk_wait_all();  // the TMA stores of dq, dk, dv are complete
   cp_async_wait_all();  // no gate prefetch may still be writing shared memory at exit
   cta_sync();
   if (warp == 0) tmem_dealloc(tmem, kTmCols);
@@ -1570,11 +1594,14 @@ cudaError_t tc_bwd(const Problem& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   e = launch_fwd(p, s, false, states, dht_dot, tiles);
   if (e != cudaSuccess) return e;
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
   if ((e = make_token_map(&mq, p.q, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mk, p.k, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mv, p.v, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mdo, p.do_, p)) != cudaSuccess) return e;
+  if ((e = make_token_map(&mdq, p.dq, p)) != cudaSuccess) return e;
+  if ((e = make_token_map(&mdk, p.dk_, p)) != cudaSuccess) return e;
+  if ((e = make_token_map(&mdv, p.dv_, p)) != cudaSuccess) return e;
   BwdParams bp{p.g, p.beta, p.dht, dht_dot,
                reinterpret_cast<const unsigned char*>(states), static_cast<__nv_bfloat16*>(p.dq),
                static_cast<__nv_bfloat16*>(p.dk_), static_cast<__nv_bfloat16*>(p.dv_), p.dg, p.dbeta,
@@ -1583,7 +1610,7 @@ cudaError_t tc_bwd(const Problem& p, cudaStream_t s) {
                            kBwdSmemBytes);
   if (e != cudaSuccess) return e;
   prof_before(s);
-  gdn_tc_bwd_kernel<<<p.B * p.H, BT, kBwdSmemBytes, s>>>(mq, mk, mv, mdo, bp);
+  gdn_tc_bwd_kernel<<<p.B * p.H, BT, kBwdSmemBytes, s>>>(mq, mk, mv, mdo, mdq, mdk, mdv, bp);
   prof_after(s, kTcBwd);
   return cudaGetLastError();
 }
