@@ -95,8 +95,6 @@ struct FwdParams {
   float* ht;
   __nv_bfloat16* states;  // optional: bf16 G tile of every chunk's entry state
                           // ([B*H][N][32 KB], shared-memory layout)
-  const float* dht;       // with states: d(final state), for dht_dot
-  float* dht_dot;         // with states: <dht, ht> per sequence
   const unsigned char* tiles;  // T of every chunk ([B*H][N][8 KB], from the solve kernel)
   int B, T, H, N;
 };
@@ -644,31 +642,14 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       group_sync_tc(kBarChain);
     }
     if (!ok) *abort_flag = 1;
-    if (ok) {
+    if (ok && p.ht) {
       float v[32];
-      float acc = 0.f;
 #pragma unroll
       for (int q32 = 0; q32 < 2; ++q32) {
         tmem_ld32(tmem + lane_base + kTmG + half * 64 + q32 * 32, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const size_t off = ((size_t)bh * D + half * 64 + q32 * 32 + i) * D + row;
-          if (p.ht) p.ht[off] = v[i];
-          if (p.dht) acc += p.dht[off] * v[i];
-        }
-      }
-      if (p.dht_dot) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        float* red = reinterpret_cast<float*>(sm + kF_TR);  // idle once every chunk is done
-        group_sync(kBarChain, kGroup);
-        if (lane == 0) red[warp] = acc;
-        group_sync(kBarChain, kGroup);
-        if (gt == 0) {
-          float t = 0.f;
-          for (int w = 0; w < 8; ++w) t += red[w];
-          p.dht_dot[bh] = t;
-        }
+        for (int i = 0; i < 32; ++i)
+          p.ht[((size_t)bh * D + half * 64 + q32 * 32 + i) * D + row] = v[i];
       }
     }
   } else {
@@ -1021,7 +1002,6 @@ struct BwdParams {
   const float* g;
   const float* beta;
   const float* dht;
-  const float* dht_dot;          // <dht, ht> per sequence (workspace)
   const unsigned char* states;   // [B*H][N][32 KB]
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
@@ -1126,33 +1106,46 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const uint32_t tmem = *tmem_slot;
   const uint32_t lb = (uint32_t)(quad * 32) << 16;
 
-  // this thread's 32 state-gradient columns: d in [32 cg, 32 cg + 32)
+  // The running state gradient dG (fp32) lives in TMEM columns kBtG3..+127
+  // (row c = lane, column d); the dG_in product accumulates onto it.  This
+  // thread's 32 columns: d in [32 cg, 32 cg + 32).
   const int g_region = cg >> 1, g_chunk0 = (cg & 1) * 4;
-  float dG[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) dG[i] = p.dht ? p.dht[((size_t)bh * D + cg * 32 + i) * D + row] : 0.f;
-  auto write_dg = [&]() {
+  const uint32_t t_dg = tmem + lb + kBtG3 + cg * 32;
+  // bf16 copy of dG (the MMA operand)
+  auto write_dg = [&](const float (&g)[32]) {
     unsigned char* tile = sm + kB_DG + g_region * 16384;
+#pragma unroll
     for (int k = 0; k < 4; ++k) {
       uint4 pk;
       uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(dG[k * 8 + 2 * i], dG[k * 8 + 2 * i + 1]);
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(g[k * 8 + 2 * i], g[k * 8 + 2 * i + 1]);
         w[i] = *reinterpret_cast<uint32_t*>(&b2);
       }
       *reinterpret_cast<uint4*>(tile + sw_row_off(row, g_chunk0 + k)) = pk;
     }
   };
-  write_dg();
-  // <dH_out, H_out> of the chunk being processed (the last chunk: <dht, ht>)
-  float carry = p.dht_dot ? p.dht_dot[bh] : 0.f;
+  {
+    float g[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) g[i] = p.dht ? p.dht[((size_t)bh * D + cg * 32 + i) * D + row] : 0.f;
+    tmem_st32(t_dg, g);
+    write_dg(g);
+  }
 
   float* graw = reinterpret_cast<float*>(sm + kB_GRAW);
   auto load_gates = [&](int ci) {
     prefetch_gates(graw + (ci & 1) * 128, p.g, p.beta, b, p.T, p.H, h, ci, lane);
   };
-  if (warp == 0) load_gates(p.N - 1);
+  // The gates of each chunk are computed by warp 1 near the end of the chunk
+  // before it in the reverse scan, from g and beta prefetched one more chunk
+  // ahead; the last chunk's here.
+  if (warp == 0 && p.N > 0) {
+    load_gates(p.N - 1);
+    chunk_gates_raw(GV, graw + ((p.N - 1) & 1) * 128, lane);
+    if (p.N > 1) load_gates(p.N - 2);
+  }
 
   uint32_t mma_phase = 0, load_phase = 0;
   bool ok = true;
@@ -1162,45 +1155,67 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tc_fence_after();
   };
 
+  // Tiles of chunk ci land on bar_load.  The loads for the next chunk of the
+  // reverse scan are issued inside the current one as soon as each slot has
+  // been read for the last time: V after the dv/dZ epilogue, K, dO, G_in and
+  // T once the last products are done, Q after the q . dq sums.  The whole
+  // chunk's byte count is announced with the first of them.
+  constexpr uint32_t kChunkBytes = 8 * 8192 + 32768 + 8192;
+  int inflight = -1;   // thread 0: chunk whose tiles are requested but not yet waited for
+  int parts = 0;       // thread 0: how many of its three load groups are issued
+  auto issue_v = [&](int cn) {
+    const int tn = cn * C;
+    inflight = cn;
+    parts = 1;
+    mbar_arrive_expect_tx(bar_load, kChunkBytes);
+    tma_load_4d(sm + kB_V, &tm_v, bar_load, 0, h, tn, b);
+    tma_load_4d(sm + kB_V + 8192, &tm_v, bar_load, 64, h, tn, b);
+  };
+  auto issue_rest = [&](int cn) {
+    const int tn = cn * C;
+    parts = 2;
+    tma_load_4d(sm + kB_KQ + 0, &tm_k, bar_load, 0, h, tn, b);
+    tma_load_4d(sm + kB_KQ + 16384, &tm_k, bar_load, 64, h, tn, b);
+    tma_load_4d(sm + kB_ZO + 8192, &tm_do, bar_load, 0, h, tn, b);
+    tma_load_4d(sm + kB_ZO + 24576, &tm_do, bar_load, 64, h, tn, b);
+    bulk_load(sm + kB_GI, p.states + ((size_t)bh * p.N + cn) * 32768, 32768, bar_load);
+    bulk_load(sm + kB_T, p.tiles + ((size_t)bh * p.N + cn) * 8192, 8192, bar_load);
+  };
+  auto issue_q = [&](int cn) {
+    const int tn = cn * C;
+    parts = 3;
+    tma_load_4d(sm + kB_KQ + 8192, &tm_q, bar_load, 0, h, tn, b);
+    tma_load_4d(sm + kB_KQ + 24576, &tm_q, bar_load, 64, h, tn, b);
+  };
+  if (tid == 0 && p.N > 0) {
+    issue_v(p.N - 1);
+    issue_rest(p.N - 1);
+    issue_q(p.N - 1);
+  }
+
   for (int ci = p.N - 1; ci >= 0 && ok; --ci) {
     const int t0 = ci * C, n = min(C, p.T - t0);
     if (tid == 0) bulk_wait_read_all();  // X0 / X1 staging of the previous chunk has been read
     fence_async_shared();
     cta_sync();
-    if (tid == 0) {
-      mbar_arrive_expect_tx(bar_load, 8 * 8192 + 32768 + 8192);
-      tma_load_4d(sm + kB_KQ + 0, &tm_k, bar_load, 0, h, t0, b);
-      tma_load_4d(sm + kB_KQ + 8192, &tm_q, bar_load, 0, h, t0, b);
-      tma_load_4d(sm + kB_KQ + 16384, &tm_k, bar_load, 64, h, t0, b);
-      tma_load_4d(sm + kB_KQ + 24576, &tm_q, bar_load, 64, h, t0, b);
-      tma_load_4d(sm + kB_ZO + 8192, &tm_do, bar_load, 0, h, t0, b);
-      tma_load_4d(sm + kB_ZO + 24576, &tm_do, bar_load, 64, h, t0, b);
-      tma_load_4d(sm + kB_V, &tm_v, bar_load, 0, h, t0, b);
-      tma_load_4d(sm + kB_V + 8192, &tm_v, bar_load, 64, h, t0, b);
-      bulk_load(sm + kB_GI, p.states + ((size_t)bh * p.N + ci) * 32768, 32768, bar_load);
-      bulk_load(sm + kB_T, p.tiles + ((size_t)bh * p.N + ci) * 8192, 8192, bar_load);
-      if (ci > 0) {
-        // the next chunk in the reverse scan: start pulling its tiles into L2
-        const int tp = t0 - C;
-        tma_prefetch_l2_4d(&tm_k, 0, h, tp, b);
-        tma_prefetch_l2_4d(&tm_k, 64, h, tp, b);
-        tma_prefetch_l2_4d(&tm_q, 0, h, tp, b);
-        tma_prefetch_l2_4d(&tm_q, 64, h, tp, b);
-        tma_prefetch_l2_4d(&tm_do, 0, h, tp, b);
-        tma_prefetch_l2_4d(&tm_do, 64, h, tp, b);
-        tma_prefetch_l2_4d(&tm_v, 0, h, tp, b);
-        tma_prefetch_l2_4d(&tm_v, 64, h, tp, b);
-        bulk_prefetch_l2(p.states + ((size_t)bh * p.N + ci - 1) * 32768, 32768);
-        bulk_prefetch_l2(p.tiles + ((size_t)bh * p.N + ci - 1) * 8192, 8192);
-      }
-    }
-    if (warp == 0) {
-      chunk_gates_raw(GV, graw + (ci & 1) * 128, lane);
-      if (ci > 0) load_gates(ci - 1);
+    if (tid == 0 && ci > 0) {
+      // the next chunk in the reverse scan: start pulling its tiles into L2
+      const int tp = t0 - C;
+      tma_prefetch_l2_4d(&tm_k, 0, h, tp, b);
+      tma_prefetch_l2_4d(&tm_k, 64, h, tp, b);
+      tma_prefetch_l2_4d(&tm_q, 0, h, tp, b);
+      tma_prefetch_l2_4d(&tm_q, 64, h, tp, b);
+      tma_prefetch_l2_4d(&tm_do, 0, h, tp, b);
+      tma_prefetch_l2_4d(&tm_do, 64, h, tp, b);
+      tma_prefetch_l2_4d(&tm_v, 0, h, tp, b);
+      tma_prefetch_l2_4d(&tm_v, 64, h, tp, b);
+      bulk_prefetch_l2(p.states + ((size_t)bh * p.N + ci - 1) * 32768, 32768);
+      bulk_prefetch_l2(p.tiles + ((size_t)bh * p.N + ci - 1) * 8192, 8192);
     }
     ok = __syncthreads_and(mbar_wait(bar_load, load_phase));
-    load_phase ^= 1;
     if (!ok) break;
+    load_phase ^= 1;
+    inflight = -1;
     // ---- MMA1: [K;Q] K^T;  -G_in K^T;  dG K^T
     if (tid == 0) {
       const uint32_t id = idesc_bf16(128, 64, false, false);
@@ -1273,12 +1288,46 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // ---- E4: U^T -> X0, (U diag f)^T -> X2, e dR^T -> X1, dZ rows -> ZO, dv, dbeta part 1
     float acc[16];  // this thread's terms of the log-gate gradient, columns 16 cg + i
     {
+      // <dH_out, H_out> of this chunk, with H_out = eC H_in + K^T diag(f) U its
+      // state update: eC <dG, G_in> + sum_{c,j} (U diag f)^T_cj (dG K^T)_cj
+      float cdot = 0.f;
+      {
+        float g[32];
+        tmem_ld32(t_dg, g);  // dG_out
+        const unsigned char* tile = sm + kB_GI + g_region * 16384;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 pk = *reinterpret_cast<const uint4*>(tile + sw_row_off(row, g_chunk0 + k));
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&pk);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f2 = __bfloat1622float2(h2[i]);
+            cdot = fmaf(g[k * 8 + 2 * i], f2.x, cdot);
+            cdot = fmaf(g[k * 8 + 2 * i + 1], f2.y, cdot);
+          }
+        }
+        const float ec = *eC;
+        cdot *= ec;
+        // dG <- eC dG; the dG_in product of this chunk accumulates onto it
+#pragma unroll
+        for (int i = 0; i < 32; ++i) g[i] *= ec;
+        tmem_st32(t_dg, g);
+      }
       float u[16];
       tmem_ld16(tmem + lb + kBtU + cg * 16, u);
       store_chunks(sm + kB_X, row, cg * 2, u, 2);
 #pragma unroll
       for (int i = 0; i < 16; ++i) u[i] *= ff[cg * 16 + i];
       store_chunks(sm + kB_X + 32768, row, cg * 2, u, 2);
+      {
+        float x1[16];
+        tmem_ld16(tmem + lb + kBtX1 + cg * 16, x1);  // dG K^T, row c, columns j
+#pragma unroll
+        for (int i = 0; i < 16; ++i) cdot = fmaf(u[i], x1[i], cdot);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) cdot += __shfl_xor_sync(0xffffffffu, cdot, off);
+      if (lane == 0) red[256 + warp] = cdot;  // summed by warp 0 for dg
       float z[16], rr[16];
       tmem_ld16(tmem + lb + kBtZ + cg * 16, z);
       tmem_ld16(tmem + lb + kBtR + cg * 16, rr);
@@ -1306,6 +1355,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       tma_store_4d(&tm_dv, sm + kB_T, 0, h, t0, b);
       tma_store_4d(&tm_dv, sm + kB_T + 8192, 64, h, t0, b);
       bulk_commit_group();
+      if (ci > 0) issue_v(ci - 1);  // V has been read for the last time
       const uint32_t id = idesc_bf16(128, 64, false, true);
       for (int ks = 0; ks < 8; ++ks)
         mma_bf16(tmem + kBtX1, sw128_desc(sZO + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024),
@@ -1365,7 +1415,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const uint32_t idg = idesc_bf16(128, 128, true, true);
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16(tmem + kBtG3, sw128_desc(sZO + 8192 + ks * 2048, 16384, 1024),
-                 sw128_desc(sKQ + 8192 + ks * 2048, 16384, 1024), idg, ks > 0);
+                 sw128_desc(sKQ + 8192 + ks * 2048, 16384, 1024), idg, 1);
       const uint32_t idgn = idesc_bf16(128, 128, false, true, true);
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16(tmem + kBtG3, sw128_desc(sX1 + ks * 32, 16, 1024), sw128_desc(sKQ + ks * 2048, 16384, 1024),
@@ -1401,12 +1451,14 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     mma_wait();
     if (!ok) break;
     // ---- E6: dG update, dq (+ q.dq), dk, dbeta, dg
+    // K, dO, G_in and T have been read for the last time
+    if (tid == 0 && ci > 0) issue_rest(ci - 1);
     {
-      const float ec = *eC;
-      float v32[32];
-      tmem_ld32(tmem + lb + kBtG3 + cg * 32, v32);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) dG[i] = fmaf(ec, dG[i], v32[i]);
+      {
+        float g[32];
+        tmem_ld32(t_dg, g);  // dG_in = eC dG_out + (e dO)^T Q - (e dR)^T K
+        write_dg(g);         // the products that read the old copy are done
+      }
       float x[16];
       tmem_ld16(tmem + lb + kBtX2 + cg * 16, x);  // dQ^T row d = row, columns r = 16 cg + i
       const int half = row >> 6, cc = row & 63;
@@ -1431,33 +1483,22 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       tma_store_4d(&tm_dk, sm + kB_X + 16384, 0, h, t0, b);
       tma_store_4d(&tm_dk, sm + kB_X + 24576, 64, h, t0, b);
       bulk_commit_group();
+      if (ci > 0) issue_q(ci - 1);  // Q has been read for the last time
+    }
+    if (warp == 1 && ci > 0) {
+      // gates of the next chunk of the reverse scan (this chunk's are no longer read)
+      chunk_gates_raw(GV, graw + ((ci - 1) & 1) * 128, lane);
+      if (ci > 1) load_gates(ci - 2);
     }
     if (tid < 64) {
       const int r = tid;
       if (r < n) p.dbeta[((size_t)b * p.T + t0 + r) * p.H + h] = db1[r] + db2[r];
     }
-    // <dH_in, H_in> of this chunk = <dH_out, H_out> of the chunk before it
-    float dot = 0.f;
-    {
-      const unsigned char* tile = sm + kB_GI + g_region * 16384;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint4 pk = *reinterpret_cast<const uint4*>(tile + sw_row_off(row, g_chunk0 + k));
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&pk);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f2 = __bfloat1622float2(h2[i]);
-          dot = fmaf(dG[k * 8 + 2 * i], f2.x, dot);
-          dot = fmaf(dG[k * 8 + 2 * i + 1], f2.y, dot);
-        }
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-    if (lane == 0) red[256 + warp] = dot;
-    __syncthreads();
     if (warp == 0) {
       // dg_t = sum_{s >= t, s in chunk} (q_s.dq_s - v_s.dv_s) + <dH_out, H_out>
+      float carry = 0.f;
+#pragma unroll
+      for (int w = 0; w < BT / 32; ++w) carry += red[256 + w];
       float a0 = dlc[lane], a1 = dlc[lane + 32];
       float s1 = a1;
 #pragma unroll
@@ -1477,18 +1518,23 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (lane < n) p.dg[base + (size_t)lane * p.H] = carry + s0;
       if (lane + 32 < n) p.dg[base + (size_t)(lane + 32) * p.H] = carry + s1;
     }
-    carry = 0.f;
-#pragma unroll
-    for (int w = 0; w < BT / 32; ++w) carry += red[256 + w];
-    write_dg();
   }
 
   if (!ok) {
-    if (tid == 0) report_timeout();
-    mbar_wait(bar_load, load_phase, 10000);
+    if (tid == 0) {
+      report_timeout();
+      // let the tile loads still in flight land before the CTA exits (bounded)
+      if (inflight >= 0) {
+        if (parts < 2) issue_rest(inflight);
+        if (parts < 3) issue_q(inflight);
+        mbar_wait(bar_load, load_phase, 10000);
+      }
+    }
   } else if (p.dh0) {
+    float g[32];
+    tmem_ld32(t_dg, g);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) p.dh0[((size_t)bh * D + cg * 32 + i) * D + row] = dG[i];
+    for (int i = 0; i < 32; ++i) p.dh0[((size_t)bh * D + cg * 32 + i) * D + row] = g[i];
   }
   if (tid == 0) bulk_wait_all();  // the TMA stores of dq, dk, dv are complete
   cp_async_wait_all();  // no gate prefetch may still be writing shared memory at exit
@@ -1542,15 +1588,14 @@ cudaError_t launch_solve(const Problem& p, cudaStream_t s, unsigned char* tiles)
 }
 
 cudaError_t launch_fwd(const Problem& p, cudaStream_t s, bool want_out, __nv_bfloat16* states,
-                       float* dht_dot, const unsigned char* tiles) {
+                       const unsigned char* tiles) {
   CUtensorMap mq, mk, mv;
   cudaError_t e;
   if ((e = make_token_map(&mq, p.q, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mk, p.k, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mv, p.v, p)) != cudaSuccess) return e;
   FwdParams fp{p.g, p.beta, p.h0, want_out ? static_cast<__nv_bfloat16*>(p.o) : nullptr,
-               want_out ? p.ht : nullptr, states, want_out ? nullptr : p.dht,
-               dht_dot, tiles, p.B, p.T, p.H, p.N};
+               want_out ? p.ht : nullptr, states, tiles, p.B, p.T, p.H, p.N};
   e = cudaFuncSetAttribute(gdn_tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   prof_before(s);
@@ -1572,27 +1617,23 @@ size_t states_bytes(const Problem& p) { return align_up((size_t)p.B * p.H * p.N 
 size_t tc_fwd_workspace(const Problem& p) { return tiles_bytes(p); }
 
 // Workspace of the tensor-core backward pass: the bf16 entry state of every
-// chunk in MMA-operand layout (32 KB each), the T tile of every chunk, then
-// <dht, ht> per sequence.
-size_t tc_bwd_workspace(const Problem& p) {
-  return states_bytes(p) + tiles_bytes(p) + align_up((size_t)p.B * p.H * 4, 256);
-}
+// chunk in MMA-operand layout (32 KB each), then the T tile of every chunk.
+size_t tc_bwd_workspace(const Problem& p) { return states_bytes(p) + tiles_bytes(p); }
 
 cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
   unsigned char* tiles = static_cast<unsigned char*>(p.ws);
   cudaError_t e = launch_solve(p, s, tiles);
   if (e != cudaSuccess) return e;
-  return launch_fwd(p, s, true, nullptr, nullptr, tiles);
+  return launch_fwd(p, s, true, nullptr, tiles);
 }
 
 cudaError_t tc_bwd(const Problem& p, cudaStream_t s) {
   unsigned char* ws = static_cast<unsigned char*>(p.ws);
   __nv_bfloat16* states = reinterpret_cast<__nv_bfloat16*>(ws);
   unsigned char* tiles = ws + states_bytes(p);
-  float* dht_dot = reinterpret_cast<float*>(tiles + tiles_bytes(p));
   cudaError_t e = launch_solve(p, s, tiles);
   if (e != cudaSuccess) return e;
-  e = launch_fwd(p, s, false, states, dht_dot, tiles);
+  e = launch_fwd(p, s, false, states, tiles);
   if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
   if ((e = make_token_map(&mq, p.q, p)) != cudaSuccess) return e;
@@ -1602,7 +1643,7 @@ cudaError_t tc_bwd(const Problem& p, cudaStream_t s) {
   if ((e = make_token_map(&mdq, p.dq, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mdk, p.dk_, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mdv, p.dv_, p)) != cudaSuccess) return e;
-  BwdParams bp{p.g, p.beta, p.dht, dht_dot,
+  BwdParams bp{p.g, p.beta, p.dht,
                reinterpret_cast<const unsigned char*>(states), static_cast<__nv_bfloat16*>(p.dq),
                static_cast<__nv_bfloat16*>(p.dk_), static_cast<__nv_bfloat16*>(p.dv_), p.dg, p.dbeta,
                p.dh0, tiles, p.B, p.T, p.H, p.N};
