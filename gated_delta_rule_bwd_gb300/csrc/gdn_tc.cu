@@ -544,8 +544,9 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         scale_rows(stc, 64, gf, gt, kGroup);
         scale_rows(stc + 16384, 64, gf, gt, kGroup);
       }
-      {
-        // G <- eC G  (MMA5 accumulates onto it)
+      if (ci == 0) {
+        // G <- eC G  (MMA5 accumulates onto it; for later chunks the previous
+        // chunk's last epilogue does this)
         const float ec = gates[384];
         float v[32];
 #pragma unroll
@@ -630,12 +631,23 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
       }
       {
-        unsigned char* dst = ci + 1 < p.N ? state_dst(ci + 1) : nullptr;
+        // bf16 copy of the next chunk's entry state; then G <- eC G with the
+        // next chunk's eC (its gates are ready: they precede its hand-over)
+        const bool more = ci + 1 < p.N;
+        unsigned char* dst = more ? state_dst(ci + 1) : nullptr;
+        const float ecn =
+            more ? reinterpret_cast<const float*>(sm + kF_GATE + ((ci + 1) & 1) * kGateBlock)[384] : 1.f;
         float v[32];
 #pragma unroll
         for (int q32 = 0; q32 < 2; ++q32) {
-          tmem_ld32(tmem + lane_base + kTmG + half * 64 + q32 * 32, v);
+          const uint32_t ta = tmem + lane_base + kTmG + half * 64 + q32 * 32;
+          tmem_ld32(ta, v);
           store_chunks(sm + kF_G + half * 16384, row, q32 * 4, v, 4, dst ? dst + half * 16384 : nullptr);
+          if (more) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= ecn;
+            tmem_st32(ta, v);
+          }
         }
       }
       fence_async_shared();
@@ -796,7 +808,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // the Q K^T columns are free again: start the next chunk's MMA1 now if
         // its tiles have landed (otherwise it is issued at the top of that chunk)
         const int cn = ci + 1;
-        *early_mma1 = (cn < p.N && mbar_try_wait(&bar_kq[cn & 1], (cn >> 1) & 1)) ? 1 : 0;
+        *early_mma1 = (cn < p.N && mbar_test_wait(&bar_kq[cn & 1], (cn >> 1) & 1)) ? 1 : 0;
         if (*early_mma1) issue_mma1(cn);
       }
       tc_fence_before();
