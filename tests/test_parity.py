@@ -188,6 +188,25 @@ def test_results_are_deterministic(kda):
         assert torch.equal(r1[2][n], r2[2][n]), n
 
 
+def test_shared_workspace_across_calls():
+    """One caller-provided workspace reused by the forward and the backward
+    call, twice in a row (as a training loop does): every result bit-equal to
+    calls that each allocate their own workspace."""
+    x = make_inputs(2, 200, 2, 128, 128, dtype="bf16", h0_std=0.1, with_dht=True, seed=11)
+    d = x.to("cuda")
+    need = max(gdn.fwd_workspace_bytes(d.q, d.v), gdn.bwd_workspace_bytes(d.q, d.v))
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ref_o, ref_ht = gdn.gdn_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0)
+    ref_g = gdn.gdn_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, d.dht)
+    for _ in range(2):
+        o, ht = gdn.gdn_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, workspace=ws)
+        gr = gdn.gdn_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, d.dht, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(o, ref_o) and torch.equal(ht, ref_ht)
+        for n in ref_g:
+            assert torch.equal(gr[n], ref_g[n]), n
+
+
 def test_beta_zero_gives_pure_decay_on_gpu():
     x = make_inputs(1, 96, 2, 128, 128, dtype="bf16", h0_std=0.5, seed=6)
     x.beta.zero_()
