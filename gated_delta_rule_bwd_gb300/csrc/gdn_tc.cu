@@ -121,6 +121,13 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// 1-D bulk copy shared -> global (bulk-group completion; same alignment rules)
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void report_timeout() { atomicExch(&g_device_status, GDN_ERR_DEVICE_TIMEOUT); }
 
 // ---------------------------------------------------------------- forward kernel
@@ -511,13 +518,16 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int i = 0; i < 32; ++i)
           v[i] = p.h0 ? p.h0[((size_t)bh * D + half * 64 + q32 * 32 + i) * D + row] : 0.f;
         tmem_st32(tmem + lane_base + kTmG + half * 64 + q32 * 32, v);
-        unsigned char* dst0 = state_dst(0);
-        store_chunks(sm + kF_G + half * 16384, row, q32 * 4, v, 4,
-                     dst0 ? dst0 + half * 16384 : nullptr);
+        store_chunks(sm + kF_G + half * 16384, row, q32 * 4, v, 4);
       }
     }
     fence_async_shared();
     group_sync_tc(kBarChain);
+    if (gt == 0 && p.states) {
+      // states mode: the tile is also chunk 0's entry state in the workspace
+      bulk_store(state_dst(0), sm + kF_G, 32768);
+      bulk_commit_group();
+    }
     uint32_t s_phase = 0;
     for (int ci = 0; ci < p.N; ++ci) {
       const int s = ci & 1, t0 = ci * C, n = min(C, p.T - t0);
@@ -601,6 +611,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           mma_bf16(tmem + kTmG, sw128_desc(smem_u32(sm + kF_U) + ks * 32, 16, 1024),
                    sw128_desc(st_kq + ks * 2048, 16384, 1024), id5, 1);
         mma_commit(bar_s);
+        bulk_wait_read_all();  // the last entry-state copy has read the tile E5 rewrites next
       }
       ok = group_and(kBarChain, kGroup, mbar_wait(bar_s, s_phase));
       s_phase ^= 1;
@@ -642,17 +653,22 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int q32 = 0; q32 < 2; ++q32) {
           const uint32_t ta = tmem + lane_base + kTmG + half * 64 + q32 * 32;
           tmem_ld32(ta, v);
-          store_chunks(sm + kF_G + half * 16384, row, q32 * 4, v, 4, dst ? dst + half * 16384 : nullptr);
+          store_chunks(sm + kF_G + half * 16384, row, q32 * 4, v, 4);
           if (more) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] *= ecn;
             tmem_st32(ta, v);
           }
         }
+        fence_async_shared();
+        group_sync_tc(kBarChain);
+        if (gt == 0 && dst) {
+          bulk_store(dst, sm + kF_G, 32768);  // the next chunk's entry state to the workspace
+          bulk_commit_group();
+        }
       }
-      fence_async_shared();
-      group_sync_tc(kBarChain);
     }
+    if (gt == 0) bulk_wait_all();  // entry-state copies complete (and their tile reads)
     if (!ok) *abort_flag = 1;
     if (ok && p.ht) {
       float v[32];
