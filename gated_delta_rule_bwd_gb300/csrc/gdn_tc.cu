@@ -436,7 +436,8 @@ __device__ __forceinline__ void group_sync_tc(int id) {
 
 __global__ void __launch_bounds__(FT, 1)
 gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  FwdParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -587,6 +588,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                    sw128_desc(smem_u32(sm + kF_G) + off, 16, 1024), id4, ks > 0);
         }
         mma_commit(bar_s);
+        bulk_wait_read_all();  // the last output rows staged in the U^T slot have been read
       }
       ok = group_and(kBarChain, kGroup, mbar_wait(bar_s, s_phase));
       s_phase ^= 1;
@@ -619,26 +621,14 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (!ok) break;
       if (gt == 0 && ci + 2 < p.N) load_kq(ci + 2);  // this stage is no longer read
       if (want_o) {
-        // O row r = 16 quad + lane (lanes 0-15 of each quadrant), columns 64 half + [0, 64)
+        // O row r = 16 quad + lane (lanes 0-15 of each quadrant), columns 64 half + [0, 64),
+        // staged in the U^T tile's slot (its products are done) for a TMA store
         const int r = quad * 16 + lane;
-        __nv_bfloat16* orow = p.o + (((size_t)b * p.T + t0 + r) * p.H + h) * D + half * 64;
 #pragma unroll
         for (int q32 = 0; q32 < 2; ++q32) {
           float v[32];
           tmem_ld32(tmem + lane_base + kTmO + half * 64 + q32 * 32, v);
-          if (lane < 16 && r < n) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint4 pk;
-              uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(v[k * 8 + 2 * i], v[k * 8 + 2 * i + 1]);
-                w[i] = *reinterpret_cast<uint32_t*>(&b2);
-              }
-              *reinterpret_cast<uint4*>(orow + q32 * 32 + k * 8) = pk;
-            }
-          }
+          if (lane < 16) store_chunks(sm + kF_U + half * 8192, r, q32 * 4, v, 4);
         }
       }
       {
@@ -662,8 +652,13 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         fence_async_shared();
         group_sync_tc(kBarChain);
-        if (gt == 0 && dst) {
-          bulk_store(dst, sm + kF_G, 32768);  // the next chunk's entry state to the workspace
+        if (gt == 0 && (dst || want_o)) {
+          if (dst) bulk_store(dst, sm + kF_G, 32768);  // the next chunk's entry state to the workspace
+          if (want_o) {
+            // the output rows (rows past T are not written)
+            tma_store_4d(&tm_o, sm + kF_U, 0, h, t0, b);
+            tma_store_4d(&tm_o, sm + kF_U + 8192, 64, h, t0, b);
+          }
           bulk_commit_group();
         }
       }
@@ -1617,17 +1612,18 @@ cudaError_t launch_solve(const Problem& p, cudaStream_t s, unsigned char* tiles)
 
 cudaError_t launch_fwd(const Problem& p, cudaStream_t s, bool want_out, __nv_bfloat16* states,
                        const unsigned char* tiles) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   cudaError_t e;
   if ((e = make_token_map(&mq, p.q, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mk, p.k, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mv, p.v, p)) != cudaSuccess) return e;
+  if ((e = make_token_map(&mo, want_out ? p.o : p.q, p)) != cudaSuccess) return e;  // unused without output
   FwdParams fp{p.g, p.beta, p.h0, want_out ? static_cast<__nv_bfloat16*>(p.o) : nullptr,
                want_out ? p.ht : nullptr, states, tiles, p.B, p.T, p.H, p.N};
   e = cudaFuncSetAttribute(gdn_tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   prof_before(s);
-  gdn_tc_fwd_kernel<<<p.B * p.H, FT, kSmemBytes, s>>>(mq, mk, mv, fp);
+  gdn_tc_fwd_kernel<<<p.B * p.H, FT, kSmemBytes, s>>>(mq, mk, mv, mo, fp);
   prof_after(s, want_out ? kTcFwd : kTcStates);
   return cudaGetLastError();
 }
