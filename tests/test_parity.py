@@ -89,6 +89,8 @@ SMALL = [
     (1, 300, 2, 128, 128, 64, "f32", False, True, True),   # full head dims on CUDA cores
     (1, 300, 2, 128, 128, 64, "f32", True, True, True),
     (2, 192, 2, 128, 128, 32, "bf16", False, True, False),
+    (2, 200, 2, 128, 128, 64, "bf16", False, True, True),  # tensor-core path, 8-token tail
+    (1, 37, 3, 128, 128, 64, "bf16", False, True, True),   # tensor-core path, T < chunk
 ]
 
 
