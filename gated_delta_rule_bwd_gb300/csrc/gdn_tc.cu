@@ -19,8 +19,9 @@
 //               MMA3  U^T = V^T T''^T - G W^T, T'' = T diag(beta)
 //               MMA4  O = (eQ) G^T + P U          (M = 64: rows are tokens)
 //               MMA5  G <- eC G + (U diag(f))^T K
-//             In states mode (for the backward pass) it skips P and O and
-//             dumps every chunk's entry state.
+//             The output rows and (in states mode, for the backward pass,
+//             which skips P and O) every chunk's bf16 entry state leave the
+//             CTA by TMA / bulk copies of their shared-memory tiles.
 //   backward  the reverse chunk scan (described at its kernel).
 //
 // The TMA tiles of K and V serve both as K-major operands (rows = tokens) and,
@@ -975,10 +976,12 @@ gdn_tc_solve_kernel(const __grid_constant__ CUtensorMap tm_k, SolveParams p) {
 // ---------------------------------------------------------------- backward kernel
 //
 // Reverse chunk scan, one CTA per sequence.  The running state gradient is
-// held transposed, dG = dH^T (dv x dk), fp32 in registers (thread c owns row
-// c) with a bf16 copy in shared memory.  Each chunk's entry state G_in comes
-// from the workspace (written by the forward kernel in states mode), and so
-// does its T tile (written by the solve kernel).  With R = V - diag(e) K H_in,
+// held transposed, dG = dH^T (dv x dk), fp32 in TMEM (128 columns; the dG_in
+// product accumulates onto it) with a bf16 copy in shared memory as the MMA
+// operand.  Each chunk's entry state G_in comes from the workspace (written
+// by the forward kernel in states mode), and so does its T tile (written by
+// the solve kernel); the next chunk's tiles are requested as soon as each
+// slot has been read for the last time.  With R = V - diag(e) K H_in,
 // U = T diag(beta) R, T = (I + A)^-1:
 //
 //   MMA1  [K;Q] K^T, -G_in K^T, dG K^T  (one batch)
@@ -989,14 +992,16 @@ gdn_tc_solve_kernel(const __grid_constant__ CUtensorMap tm_k, SolveParams p) {
 //   MMA   [dZ; dO] U^T             -> dA = -strict_lower(dZ U^T), dP = dO U^T
 //   MMA   dG_in = eC dG + (e dO)^T Q - (e dR)^T K       (dR = diag(beta) dZ)
 //   MMA   dQ^T = G_in^T (e dO)^T + K^T (dP o Gam)^T
-//   MMA   dK^T = dG^T (U diag f)^T - G_in^T (e dR)^T... + Q^T (dP o Gam)
+//   MMA   dK^T = dG^T (U diag f)^T - G_in^T (e dR)^T + Q^T (dP o Gam)
 //               + K^T (M + M^T),  M = diag(beta) dA o Gam
 //
-// dv = dR; dbeta_r = sum_c dZ_rc R_rc + sum_j dA_rj (K K^T o Gam)_rj.  The
+// dv = dR; dbeta_r = sum_c dZ_rc R_rc + sum_j dA_rj (K K^T o Gam)_rj.  dq, dk
+// and dv are staged in shared memory and leave by TMA tensor stores.  The
 // log-gate gradient uses the scaling identity of the scalar gate inside each
 // chunk: dg_t = sum_{s >= t in the chunk} (q_s . dq_s - v_s . dv_s) +
-// <dH_out, H_out>, where <dH_out, H_out> is <dH_in, H_in> of the next chunk
-// (or <dht, ht> for the last one).  Keeping the sum inside the chunk avoids
+// <dH_out, H_out>, with <dH_out, H_out> taken from the chunk's own state
+// update H_out = eC H_in + K^T diag(f) U as eC <dH_out, H_in> +
+// sum (U diag f)^T o (dG K^T).  Keeping the sum inside the chunk avoids
 // accumulating the rounding of thousands of terms.
 
 constexpr int BT = 512;                  // backward threads (as the forward)
