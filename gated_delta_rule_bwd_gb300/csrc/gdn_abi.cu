@@ -132,7 +132,7 @@ namespace gdn {
 const char* kernel_name(int id) {
   static const char* names[kNumKernelIds] = {
       "simt_fwd", "simt_states", "simt_bwd", "simt_bwd_reduce",
-      "tc_fwd", "tc_states", "tc_bwd", "tc_solve"};
+      "tc_fwd", "tc_states", "tc_bwd", "tc_solve", "tc_fwd_segment", "tc_combine"};
   return (id >= 0 && id < kNumKernelIds) ? names[id] : "unknown";
 }
 

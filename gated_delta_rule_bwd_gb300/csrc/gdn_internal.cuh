@@ -45,7 +45,9 @@ enum KernelId {
   kTcStates = 5,
   kTcBwd = 6,
   kTcSolve = 7,
-  kNumKernelIds = 8
+  kTcSegment = 8,
+  kTcCombine = 9,
+  kNumKernelIds = 10
 };
 const char* kernel_name(int id);
 

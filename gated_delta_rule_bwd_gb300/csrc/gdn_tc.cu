@@ -30,6 +30,8 @@
 // mbarrier; every wait is bounded and a timeout is reported through the device
 // status word instead of hanging.
 
+#include <algorithm>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -98,6 +100,12 @@ struct FwdParams {
                           // ([B*H][N][32 KB], shared-memory layout)
   const unsigned char* tiles;  // T of every chunk ([B*H][N][8 KB], from the solve kernel)
   int B, T, H, N;
+  // Segments (long sequences): with seg_chunks > 0 each CTA runs seg_chunks
+  // chunks of one sequence (CTA = sequence * nseg + segment); h0 and ht are
+  // then per segment ([B*H*nseg][dk][dv]).
+  int seg_chunks;
+  int v_zero;       // treat V as zero (the segment's transition map)
+  int h0_identity;  // start from H = I instead of h0 (dk = dv)
 };
 
 // byte offset of element (row, col) in a K-major SW128 tile whose rows are
@@ -445,7 +453,13 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
   const int quad = warp & 3, half = (warp >> 2) & 1, grp = warp >> 3;
   const int row = quad * 32 + lane;    // TMEM lane / tile row owned by this thread
-  const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
+  // this CTA's sequence and chunks [c0, c0 + NL) (the whole sequence unless segmented)
+  const int nseg = p.seg_chunks ? (p.N + p.seg_chunks - 1) / p.seg_chunks : 1;
+  const int seg = blockIdx.x % nseg, bh = blockIdx.x / nseg, b = bh / p.H, h = bh % p.H;
+  const int c0 = seg * p.seg_chunks;
+  const int NL = p.seg_chunks ? min(p.seg_chunks, p.N - c0) : p.N;
+  const size_t st_idx = (size_t)bh * nseg + seg;  // index of h0 / ht
+  const bool has_v = !p.v_zero;
 
   uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + kF_BAR);  // [2] K|Q stage loaded
   uint64_t* bar_v = bar_kq + 2;                                  // V loaded
@@ -479,32 +493,32 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int st = ci & 1;
     unsigned char* dst = sm + kF_KQ + st * 32768;
     mbar_arrive_expect_tx(&bar_kq[st], 32768 + 8192);
-    const int t0 = ci * C;
+    const int t0 = (c0 + ci) * C;
     tma_load_4d(dst + 0, &tm_k, &bar_kq[st], 0, h, t0, b);
     tma_load_4d(dst + 8192, &tm_q, &bar_kq[st], 0, h, t0, b);
     tma_load_4d(dst + 16384, &tm_k, &bar_kq[st], 64, h, t0, b);
     tma_load_4d(dst + 24576, &tm_q, &bar_kq[st], 64, h, t0, b);
-    bulk_load(sm + kF_TR + st * 8192, p.tiles + ((size_t)bh * p.N + ci) * 8192, 8192, &bar_kq[st]);
+    bulk_load(sm + kF_TR + st * 8192, p.tiles + ((size_t)bh * p.N + c0 + ci) * 8192, 8192, &bar_kq[st]);
     cnt[st] += 1;
   };
   auto load_v = [&](int ci) {
     mbar_arrive_expect_tx(bar_v, 16384);
-    const int t0 = ci * C;
+    const int t0 = (c0 + ci) * C;
     tma_load_4d(sm + kF_V, &tm_v, bar_v, 0, h, t0, b);
     tma_load_4d(sm + kF_V + 8192, &tm_v, bar_v, 64, h, t0, b);
     cnt[4] += 1;
   };
   auto state_dst = [&](int ci) -> unsigned char* {
     return p.states ? reinterpret_cast<unsigned char*>(p.states) +
-                          ((size_t)bh * p.N + ci) * (size_t)(2 * 16384)
+                          ((size_t)bh * p.N + c0 + ci) * (size_t)(2 * 16384)
                     : nullptr;
   };
   const bool want_o = p.o != nullptr;
 
   if (tid == 0) {
     load_kq(0);
-    if (p.N > 1) load_kq(1);
-    load_v(0);
+    if (NL > 1) load_kq(1);
+    if (has_v) load_v(0);
   }
   bool ok = true;
 
@@ -517,8 +531,11 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
       for (int q32 = 0; q32 < 2; ++q32) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          v[i] = p.h0 ? p.h0[((size_t)bh * D + half * 64 + q32 * 32 + i) * D + row] : 0.f;
+        for (int i = 0; i < 32; ++i) {
+          const int d = half * 64 + q32 * 32 + i;
+          v[i] = p.h0_identity ? (d == row ? 1.f : 0.f)
+                               : (p.h0 ? p.h0[(st_idx * D + d) * D + row] : 0.f);
+        }
         tmem_st32(tmem + lane_base + kTmG + half * 64 + q32 * 32, v);
         store_chunks(sm + kF_G + half * 16384, row, q32 * 4, v, 4);
       }
@@ -531,8 +548,8 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       bulk_commit_group();
     }
     uint32_t s_phase = 0;
-    for (int ci = 0; ci < p.N; ++ci) {
-      const int s = ci & 1, t0 = ci * C, n = min(C, p.T - t0);
+    for (int ci = 0; ci < NL; ++ci) {
+      const int s = ci & 1, t0 = (c0 + ci) * C;
       const float* gates = reinterpret_cast<const float*>(sm + kF_GATE + s * kGateBlock);  // eC at [384]
       ok = group_and(kBarChain, kGroup, mbar_wait(bar_pd, ci & 1) && !*abort_flag);
       if (!ok) break;
@@ -580,7 +597,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const uint32_t id3 = idesc_bf16(128, 64, false, true, true);
         for (int ks = 0; ks < 8; ++ks)
           mma_bf16(tmem + tmU, sw128_desc(smem_u32(sm + kF_G) + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024),
-                   sw128_desc(smem_u32(sm + kF_W) + ks * 2048, 16384, 1024), id3, 1);
+                   sw128_desc(smem_u32(sm + kF_W) + ks * 2048, 16384, 1024), id3, has_v || ks > 0);
         // MMA4a: O = (eQ) G^T  (M=64: A = eQ rows r, K=d; B = G tile rows c, K=d)
         const uint32_t id4 = idesc_bf16(64, 128, false, false);
         for (int ks = 0; ks < (want_o ? 8 : 0); ++ks) {
@@ -620,7 +637,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       s_phase ^= 1;
       tc_fence_after();
       if (!ok) break;
-      if (gt == 0 && ci + 2 < p.N) load_kq(ci + 2);  // this stage is no longer read
+      if (gt == 0 && ci + 2 < NL) load_kq(ci + 2);  // this stage is no longer read
       if (want_o) {
         // O row r = 16 quad + lane (lanes 0-15 of each quadrant), columns 64 half + [0, 64),
         // staged in the U^T tile's slot (its products are done) for a TMA store
@@ -635,7 +652,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       {
         // bf16 copy of the next chunk's entry state; then G <- eC G with the
         // next chunk's eC (its gates are ready: they precede its hand-over)
-        const bool more = ci + 1 < p.N;
+        const bool more = ci + 1 < NL;
         unsigned char* dst = more ? state_dst(ci + 1) : nullptr;
         const float ecn =
             more ? reinterpret_cast<const float*>(sm + kF_GATE + ((ci + 1) & 1) * kGateBlock)[384] : 1.f;
@@ -673,7 +690,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tmem_ld32(tmem + lane_base + kTmG + half * 64 + q32 * 32, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          p.ht[((size_t)bh * D + half * 64 + q32 * 32 + i) * D + row] = v[i];
+          p.ht[(st_idx * D + half * 64 + q32 * 32 + i) * D + row] = v[i];
       }
     }
   } else {
@@ -682,7 +699,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     auto psync = [&]() { group_sync(kBarPrep, kGroup); };
     float* graw = reinterpret_cast<float*>(sm + kF_GRAW);
     auto load_gates = [&](int ci) {
-      prefetch_gates(graw + (ci & 1) * 128, p.g, p.beta, b, p.T, p.H, h, ci, lane);
+      prefetch_gates(graw + (ci & 1) * 128, p.g, p.beta, b, p.T, p.H, h, c0 + ci, lane);
     };
     // Warp 9 (which issues nothing) computes each chunk's gates one chunk
     // ahead, at the end of the previous chunk's preparation, from raw values
@@ -694,7 +711,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (warp == 9) {
       load_gates(0);
       chunk_gates_raw(gate_view(0), graw, lane);
-      if (p.N > 1) load_gates(1);
+      if (NL > 1) load_gates(1);
     }
     volatile int* early_mma1 = cnt + 6;
     if (pt == 0) *early_mma1 = 0;
@@ -710,7 +727,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mma_commit(bar_p1);
     };
     uint32_t p_phase = 0;
-    for (int ci = 0; ci < p.N; ++ci) {
+    for (int ci = 0; ci < NL; ++ci) {
       const int s = ci & 1;
       float* gates = reinterpret_cast<float*>(sm + kF_GATE + s * kGateBlock);
       const GateView GV{gates, gates + 64, gates + 128, gates + 192, gates + 256, gates + 320,
@@ -781,9 +798,11 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           store_chunks(sm + kF_P + s * 8192, r, half * 4, v, 4);
         }
       }
-      ok = group_and(kBarPrep, kGroup, mbar_wait(bar_v, ci & 1));
-      if (!ok) break;
-      if (pt == 0) cnt[5] += 1;
+      if (has_v) {
+        ok = group_and(kBarPrep, kGroup, mbar_wait(bar_v, ci & 1));
+        if (!ok) break;
+        if (pt == 0) cnt[5] += 1;
+      }
       if (ci > 0) {
         // the chain has copied the previous chunk's W^T out of TMEM
         ok = group_and(kBarPrep, kGroup, mbar_wait(bar_wf, (ci - 1) & 1));
@@ -800,27 +819,27 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           mma_bf16(tmem + kTmW, sw128_desc(st_kq + ks * 2048, 16384, 1024),
                    sw128_desc(smem_u32(sm + kF_T1) + ks * 32, 16, 1024), id2, ks > 0);
         // MMA3a: U^T = V^T T''^T  (A: V tile MN-major, M=c; B: T'' K-major, N=r)
-        for (int ks = 0; ks < 4; ++ks)
+        for (int ks = 0; ks < (has_v ? 4 : 0); ++ks)
           mma_bf16(tmem + kTmU0 + 64 * s, sw128_desc(smem_u32(sm + kF_V) + ks * 2048, 8192, 1024),
                    sw128_desc(smem_u32(sm + kF_T0) + ks * 32, 16, 1024), id2, ks > 0);
         mma_commit(bar_p);
       }
-      if (warp == 9 && ci + 1 < p.N) {
+      if (warp == 9 && ci + 1 < NL) {
         // gates of the next chunk: its block was last read by the chain for
         // chunk ci - 1, which has released it (the w_free wait above)
         chunk_gates_raw(gate_view(ci + 1), graw + ((ci + 1) & 1) * 128, lane);
-        if (ci + 2 < p.N) load_gates(ci + 2);
+        if (ci + 2 < NL) load_gates(ci + 2);
       }
       ok = group_and(kBarPrep, kGroup, mbar_wait(bar_p, p_phase));
       p_phase ^= 1;
       tc_fence_after();
       if (!ok) break;
-      if (pt == 0 && ci + 1 < p.N) load_v(ci + 1);
+      if (has_v && pt == 0 && ci + 1 < NL) load_v(ci + 1);
       if (want_o && pt == 0) {
         // the Q K^T columns are free again: start the next chunk's MMA1 now if
         // its tiles have landed (otherwise it is issued at the top of that chunk)
         const int cn = ci + 1;
-        *early_mma1 = (cn < p.N && mbar_test_wait(&bar_kq[cn & 1], (cn >> 1) & 1)) ? 1 : 0;
+        *early_mma1 = (cn < NL && mbar_test_wait(&bar_kq[cn & 1], (cn >> 1) & 1)) ? 1 : 0;
         if (*early_mma1) issue_mma1(cn);
       }
       tc_fence_before();
@@ -1615,22 +1634,118 @@ cudaError_t launch_solve(const Problem& p, cudaStream_t s, unsigned char* tiles)
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(const Problem& p, cudaStream_t s, bool want_out, __nv_bfloat16* states,
-                       const unsigned char* tiles) {
+// One launch of the forward kernel.  Without segments: the whole forward
+// (want_out) or the states pass (states != nullptr).  With seg_chunks > 0:
+// one pass of the segmented forward (h0 / ht per segment).
+struct FwdLaunch {
+  bool want_out = false;
+  __nv_bfloat16* states = nullptr;
+  const float* h0 = nullptr;
+  float* ht = nullptr;
+  int seg_chunks = 0, v_zero = 0, h0_identity = 0;
+  int kernel_id = kTcFwd;
+};
+
+cudaError_t launch_fwd(const Problem& p, cudaStream_t s, const unsigned char* tiles,
+                       const FwdLaunch& f) {
   CUtensorMap mq, mk, mv, mo;
   cudaError_t e;
   if ((e = make_token_map(&mq, p.q, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mk, p.k, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mv, p.v, p)) != cudaSuccess) return e;
-  if ((e = make_token_map(&mo, want_out ? p.o : p.q, p)) != cudaSuccess) return e;  // unused without output
-  FwdParams fp{p.g, p.beta, p.h0, want_out ? static_cast<__nv_bfloat16*>(p.o) : nullptr,
-               want_out ? p.ht : nullptr, states, tiles, p.B, p.T, p.H, p.N};
+  if ((e = make_token_map(&mo, f.want_out ? p.o : p.q, p)) != cudaSuccess) return e;  // unused without output
+  FwdParams fp{p.g, p.beta, f.h0, f.want_out ? static_cast<__nv_bfloat16*>(p.o) : nullptr,
+               f.ht, f.states, tiles, p.B, p.T, p.H, p.N, f.seg_chunks, f.v_zero, f.h0_identity};
   e = cudaFuncSetAttribute(gdn_tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
+  const int nseg = f.seg_chunks ? (p.N + f.seg_chunks - 1) / f.seg_chunks : 1;
   prof_before(s);
-  gdn_tc_fwd_kernel<<<p.B * p.H, FT, kSmemBytes, s>>>(mq, mk, mv, mo, fp);
-  prof_after(s, want_out ? kTcFwd : kTcStates);
+  gdn_tc_fwd_kernel<<<(unsigned)((size_t)p.B * p.H * nseg), FT, kSmemBytes, s>>>(mq, mk, mv, mo, fp);
+  prof_after(s, f.kernel_id);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- segmented forward
+//
+// A sequence's state map over a run of chunks is affine, H_out = M H_in + N:
+// M is the run with V = 0 started from H = I, N the run started from H = 0.
+// With few sequences and many chunks (a long context), the forward splits
+// each sequence into segments so that every SM has work: pass 1 computes M
+// and N of every segment in parallel, the combine kernel chains
+// H_in(s+1) = M_s H_in(s) + N_s in fp32 per sequence, and pass 2 reruns every
+// segment from its entry state to produce the output.  About three times the
+// arithmetic of the plain forward, spread over B*H*nseg CTAs instead of B*H.
+
+constexpr int kCombineThreads = 256;
+constexpr int kCombineSmem = 2 * D * D * 4;  // H and M, fp32
+
+__global__ void __launch_bounds__(kCombineThreads)
+gdn_tc_combine_kernel(const float* M, const float* Nl, const float* h0, float* Hin, float* ht,
+                      int nseg) {
+  extern __shared__ float csm[];
+  float* Hs = csm;           // [dk][dv]
+  float* Ms = csm + D * D;   // [dk][dk]
+  const int t = threadIdx.x, bh = blockIdx.x;
+  const int d0 = (t / 16) * 8, e0 = (t % 16) * 8;  // this thread's 8 x 8 block of H
+  for (int i = t; i < D * D; i += kCombineThreads) Hs[i] = h0 ? h0[(size_t)bh * D * D + i] : 0.f;
+  __syncthreads();
+  for (int sgi = 0; sgi < nseg; ++sgi) {
+    const size_t base = ((size_t)bh * nseg + sgi) * D * D;
+    for (int i = t; i < D * D; i += kCombineThreads) {
+      Hin[base + i] = Hs[i];
+      Ms[i] = M[base + i];
+    }
+    __syncthreads();
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = Nl[base + (size_t)(d0 + i) * D + e0 + j];
+    for (int k = 0; k < D; ++k) {
+      const float4 h_lo = *reinterpret_cast<const float4*>(Hs + k * D + e0);
+      const float4 h_hi = *reinterpret_cast<const float4*>(Hs + k * D + e0 + 4);
+      const float hv[8] = {h_lo.x, h_lo.y, h_lo.z, h_lo.w, h_hi.x, h_hi.y, h_hi.z, h_hi.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float m = Ms[(d0 + i) * D + k];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(m, hv[j], acc[i][j]);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) Hs[(d0 + i) * D + e0 + j] = acc[i][j];
+    __syncthreads();
+  }
+  if (ht)
+    for (int i = t; i < D * D; i += kCombineThreads) ht[(size_t)bh * D * D + i] = Hs[i];
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 152;
+  return n;
+}
+
+// Chunks per segment of the forward pass, or 0 for no segments: only when the
+// sequences fill at most half of the SMs and are at least 64 chunks long;
+// segments are at least 32 chunks.
+int fwd_seg_chunks(const Problem& p) {
+  const long seqs = (long)p.B * p.H;
+  const int sms = sm_count();
+  if (seqs <= 0 || seqs * 2 > sms || p.N < 64) return 0;
+  const long want = std::min<long>(sms / seqs, p.N / 32);
+  if (want < 2) return 0;
+  return (int)((p.N + want - 1) / want);
+}
+
+size_t seg_state_bytes(const Problem& p, int seg_chunks) {
+  const int nseg = (p.N + seg_chunks - 1) / seg_chunks;
+  return align_up((size_t)p.B * p.H * nseg * D * D * 4, 256);
 }
 
 }  // namespace
@@ -1642,8 +1757,12 @@ bool tc_supported(const Problem& p) {
 size_t tiles_bytes(const Problem& p) { return align_up((size_t)p.B * p.H * p.N * 8192, 256); }
 size_t states_bytes(const Problem& p) { return align_up((size_t)p.B * p.H * p.N * 32768, 256); }
 
-// Workspace of the tensor-core forward pass: the T tile of every chunk.
-size_t tc_fwd_workspace(const Problem& p) { return tiles_bytes(p); }
+// Workspace of the tensor-core forward pass: the T tile of every chunk; with
+// segments also M, N and the entry state of every segment (fp32, dk x dv).
+size_t tc_fwd_workspace(const Problem& p) {
+  const int sc = fwd_seg_chunks(p);
+  return tiles_bytes(p) + (sc ? 3 * seg_state_bytes(p, sc) : 0);
+}
 
 // Workspace of the tensor-core backward pass: the bf16 entry state of every
 // chunk in MMA-operand layout (32 KB each), then the T tile of every chunk.
@@ -1653,7 +1772,44 @@ cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
   unsigned char* tiles = static_cast<unsigned char*>(p.ws);
   cudaError_t e = launch_solve(p, s, tiles);
   if (e != cudaSuccess) return e;
-  return launch_fwd(p, s, true, nullptr, tiles);
+  const int sc = fwd_seg_chunks(p);
+  if (!sc) {
+    FwdLaunch f;
+    f.want_out = true;
+    f.h0 = p.h0;
+    f.ht = p.ht;
+    return launch_fwd(p, s, tiles, f);
+  }
+  const int nseg = (p.N + sc - 1) / sc;
+  const size_t sb = seg_state_bytes(p, sc);
+  float* Mt = reinterpret_cast<float*>(tiles + tiles_bytes(p));
+  float* Nl = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(Mt) + sb);
+  float* Hin = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(Nl) + sb);
+  FwdLaunch m;  // transitions: V = 0 from H = I
+  m.ht = Mt;
+  m.seg_chunks = sc;
+  m.v_zero = 1;
+  m.h0_identity = 1;
+  m.kernel_id = kTcSegment;
+  if ((e = launch_fwd(p, s, tiles, m)) != cudaSuccess) return e;
+  FwdLaunch n;  // local states from H = 0
+  n.ht = Nl;
+  n.seg_chunks = sc;
+  n.kernel_id = kTcSegment;
+  if ((e = launch_fwd(p, s, tiles, n)) != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(gdn_tc_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kCombineSmem);
+  if (e != cudaSuccess) return e;
+  prof_before(s);
+  gdn_tc_combine_kernel<<<p.B * p.H, kCombineThreads, kCombineSmem, s>>>(Mt, Nl, p.h0, Hin, p.ht,
+                                                                          nseg);
+  prof_after(s, kTcCombine);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  FwdLaunch o;  // outputs from every segment's entry state
+  o.want_out = true;
+  o.h0 = Hin;
+  o.seg_chunks = sc;
+  return launch_fwd(p, s, tiles, o);
 }
 
 cudaError_t tc_bwd(const Problem& p, cudaStream_t s) {
@@ -1662,7 +1818,11 @@ cudaError_t tc_bwd(const Problem& p, cudaStream_t s) {
   unsigned char* tiles = ws + states_bytes(p);
   cudaError_t e = launch_solve(p, s, tiles);
   if (e != cudaSuccess) return e;
-  e = launch_fwd(p, s, false, states, tiles);
+  FwdLaunch st;
+  st.states = states;
+  st.h0 = p.h0;
+  st.kernel_id = kTcStates;
+  e = launch_fwd(p, s, tiles, st);
   if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
   if ((e = make_token_map(&mq, p.q, p)) != cudaSuccess) return e;

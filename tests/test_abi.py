@@ -118,6 +118,10 @@ def test_forward_workspace_query_and_check(L):
     args = (ctypes.byref(big), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None)
     assert fn(*args, FAKE, need - 1, None) == GDN_ERR_WORKSPACE
     assert fn(*args, ctypes.c_void_p(0x10008), need, None) == GDN_ERR_ALIGN
+    # few sequences with many chunks: the forward runs in segments and also
+    # keeps three fp32 dk x dv states per segment
+    long = shape(B=1, T=64 * 1024, H=2, dk=128, dv=128, chunk=64, dtype=1)
+    assert L.gdn_fwd_workspace(ctypes.byref(long)) > 2 * 1024 * 64 * 64 * 2 + 3 * 2 * 128 * 128 * 4
     # the CUDA-core paths (fp32, KDA) need none
     f32 = shape(B=2, T=2048, H=4, dk=128, dv=128, chunk=64, dtype=0)
     assert L.gdn_fwd_workspace(ctypes.byref(f32)) == 0

@@ -138,6 +138,21 @@ def test_long_context_forward_sampled():
     check("o", got_o, o_ref, fp32=False)
 
 
+def test_segmented_forward_matches_oracle():
+    """Few sequences, many chunks: the forward splits each sequence into
+    segments (transition and local-state passes, an fp32 combine, then the
+    output pass).  Output and final state against the oracle, with an initial
+    state and a ragged tail; the combine kernel must have run."""
+    x = make_inputs(1, 64 * 96 + 17, 2, 128, 128, dtype="bf16", h0_std=0.3, seed=12)
+    d = x.to("cuda")
+    with gdn.KernelTimer() as t:
+        o, ht = gdn.gdn_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0)
+        torch.cuda.synchronize()
+    names = [n for n, _ in t.records()]
+    assert "tc_combine" in names and names.count("tc_fwd_segment") == 2, names
+    compare(x, o, ht, None, fp32=False)
+
+
 # ----------------------------------------------------------- invariants on the GPU
 
 def test_kda_with_broadcast_gate_equals_gdn():
