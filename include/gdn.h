@@ -96,10 +96,12 @@ typedef struct {
  * Workspace bytes each entry point needs for this shape (0 if the shape is
  * invalid or needs none).  The tensor-core path of the forward pass keeps the
  * chunkwise form's triangular-solve result T = (I + A)^-1 of every 64-token
- * chunk (8 KB each, bf16); the backward pass keeps those plus the bf16 state
- * entering every chunk (32 KB each), both recomputed from the inputs inside
- * the call.  The CUDA-core fp32 path needs workspace for the backward pass
- * only. */
+ * chunk (8 KB each, bf16), and, when few long sequences make it run each
+ * sequence in segments, three fp32 dk x dv states per segment; the backward
+ * pass keeps the T tiles plus the bf16 state entering every chunk (32 KB
+ * each).  Everything is recomputed from the inputs inside the call.  The
+ * CUDA-core fp32 path needs workspace for the backward pass only.  The
+ * forward's size depends on the current device's SM count. */
 GDN_API size_t gdn_fwd_workspace(const gdn_shape* shape);
 GDN_API size_t kda_fwd_workspace(const gdn_shape* shape);
 GDN_API size_t gdn_bwd_workspace(const gdn_shape* shape);
