@@ -4,7 +4,10 @@
 One step = one forward and one backward pass of the mixer over one batch of
 synthetic inputs (every step of the chunkwise method: gate prep, decayed
 K K^T, the triangular solve, WY factors, outputs, the inter-chunk state
-recurrence, the recomputed reverse chunk scan and the gate gradients).
+recurrence, the reverse chunk scan and the gate gradients).  The forward
+keeps each chunk's entry state and solve result in a saved context that the
+backward reads (gdn_fwd_save / gdn_bwd_saved); the step with the backward
+recomputing them is timed beside it and reported as "recompute_variant".
 
 Default workload: GDN, B=16, T=2048, H=8, dk=dv=128, chunk 64, bf16 inputs
 with fp32 state (the 300M-model pre-training shape).  Prints one JSON line.
@@ -265,20 +268,27 @@ def run_ours(args):
     dist_init(ws, "nccl")
     dev = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
+    fwd_s = gdn.kda_fwd_save if w.kda else gdn.gdn_fwd_save
+    bwd_s = gdn.kda_bwd_saved if w.kda else gdn.gdn_bwd_saved
     fwd = gdn.kda_fwd if w.kda else gdn.gdn_fwd
     bwd = gdn.kda_bwd if w.kda else gdn.gdn_bwd
 
     x = w.make(device=dev, seed=rank)
-    # one workspace serves both passes (the forward needs a prefix of the backward's)
-    wsb = torch.empty(max(16, gdn.bwd_workspace_bytes(x.q, x.v, w.chunk, w.kda),
-                          gdn.fwd_workspace_bytes(x.q, x.v, w.chunk, w.kda)),
-                      dtype=torch.uint8, device=dev)
+    # the training step: the forward keeps the per-chunk entry states and
+    # solve results in the saved context, the backward reads them
+    ctx = gdn.new_ctx(x.q, x.v, w.chunk, w.kda)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        o, ht = fwd(x.q, x.k, x.v, x.g, x.beta, x.h0, chunk=w.chunk, workspace=wsb)
-        gr = bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do, None, chunk=w.chunk, workspace=wsb)
+        o, ht, _ = fwd_s(x.q, x.k, x.v, x.g, x.beta, x.h0, chunk=w.chunk, ctx=ctx)
+        gr = bwd_s(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do, ctx, None, chunk=w.chunk)
+        return o, ht, gr
+
+    def step_recompute():
+        # the same step with the backward recomputing the context (ctx as workspace)
+        o, ht = fwd(x.q, x.k, x.v, x.g, x.beta, x.h0, chunk=w.chunk, workspace=ctx)
+        gr = bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do, None, chunk=w.chunk, workspace=ctx)
         return o, ht, gr
 
     for _ in range(args.warmup):
@@ -304,6 +314,18 @@ def run_ours(args):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     dev_s = sum(step_ms) / 1e3
     dev_s_max = max_over_ranks(dev_s, ws, dev)
+
+    # the recomputing variant of the step, timed the same way (reported beside)
+    for _ in range(args.warmup):
+        step_recompute()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step_recompute()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    rc_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    rc_s_max = max_over_ranks(sum(rc_ms) / 1e3, ws, dev)
 
     # per-kernel live timing (events recorded on the launch stream)
     per = {}
@@ -342,7 +364,7 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(gdn, w, x, wsb, dev, stream, K, args.warmup, ws)
+        e2e = run_e2e(gdn, w, x, ctx, dev, stream, K, args.warmup, ws)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -361,6 +383,11 @@ def run_ours(args):
                        "roofline_step_us": roof_step_s * 1e6,
                        "step_frac_of_roofline": roof_step_s / (ms_step * 1e-3),
                        "wall_s": wall},
+            "saved_context": {"bytes": ctx.numel(), "what": "forward keeps each chunk's entry "
+                              "state and solve result for the backward"},
+            "recompute_variant": {"ms_per_step": rc_s_max * 1e3 / K,
+                                  "value": aggregate_tokens_per_s(tokens_step, K, ws, rc_s_max),
+                                  "what": "backward recomputes the context (*_fwd + *_bwd)"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": timer.launches * ws, "clocks": clocks.summary(),
         }
@@ -370,15 +397,15 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(gdn, w, x, wsb, dev, stream, K, warmup, ws):
+def run_e2e(gdn, w, x, ctx, dev, stream, K, warmup, ws):
     """Same step through the public API with pinned host buffers: every step's
     host-to-device copy of its inputs and device-to-host copy of every result
     are inside the timed region.  The loop is pipelined the way a training
     input pipeline is: step i+1's inputs are copied in on one stream and step
     i-1's results copied out on another while step i computes (two sets of
     device input buffers; each result's memory is held until its copy ends)."""
-    fwd = gdn.kda_fwd if w.kda else gdn.gdn_fwd
-    bwd = gdn.kda_bwd if w.kda else gdn.gdn_bwd
+    fwd_s = gdn.kda_fwd_save if w.kda else gdn.gdn_fwd_save
+    bwd_s = gdn.kda_bwd_saved if w.kda else gdn.gdn_bwd_saved
     names = ["q", "k", "v", "g", "beta", "do"] + (["h0"] if x.h0 is not None else [])
     host_in = {n: getattr(x, n).cpu().pin_memory() for n in names}
     dev_in = [{n: torch.empty_like(getattr(x, n)) for n in names} for _ in range(2)]
@@ -413,10 +440,10 @@ def run_e2e(gdn, w, x, wsb, dev, stream, K, warmup, ws):
             for ev in ready[bi]:
                 stream.wait_event(ev)
             d = dev_in[bi]
-            o, ht = fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0"), chunk=w.chunk,
-                        workspace=wsb)
-            gr = bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0"), d["do"], None,
-                     chunk=w.chunk, workspace=wsb)
+            o, ht, _ = fwd_s(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0"),
+                             chunk=w.chunk, ctx=ctx)
+            gr = bwd_s(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0"), d["do"], ctx,
+                       None, chunk=w.chunk)
             done[bi].record(stream)
             outs = {"o": o, "ht": ht, **{k: v for k, v in gr.items() if v is not None}}
             for j, st in enumerate(s_out):

@@ -40,7 +40,8 @@ class GdnError(RuntimeError):
 _lock = threading.Lock()
 _lib = None
 EXPORTS = ("gdn_fwd", "gdn_bwd", "kda_fwd", "kda_bwd", "gdn_fwd_workspace", "kda_fwd_workspace",
-           "gdn_bwd_workspace", "kda_bwd_workspace",
+           "gdn_bwd_workspace", "kda_bwd_workspace", "gdn_ctx_bytes", "kda_ctx_bytes",
+           "gdn_fwd_save", "kda_fwd_save", "gdn_bwd_saved", "kda_bwd_saved",
            "gdn_status_str", "gdn_last_cuda_error", "gdn_device_status", "gdn_uses_tensor_cores",
            "gdn_profile_begin", "gdn_profile_end", "gdn_profile_read", "gdn_kernel_name")
 
@@ -57,13 +58,13 @@ def lib():
             vp, sz, fp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p
             sp = ctypes.POINTER(GdnShape)
             for name in ("gdn_fwd_workspace", "kda_fwd_workspace", "gdn_bwd_workspace",
-                         "kda_bwd_workspace"):
+                         "kda_bwd_workspace", "gdn_ctx_bytes", "kda_ctx_bytes"):
                 getattr(L, name).argtypes = [sp]
                 getattr(L, name).restype = sz
-            for name in ("gdn_fwd", "kda_fwd"):
+            for name in ("gdn_fwd", "kda_fwd", "gdn_fwd_save", "kda_fwd_save"):
                 getattr(L, name).argtypes = [sp] + [vp] * 8 + [vp, sz, vp]
                 getattr(L, name).restype = ctypes.c_int
-            for name in ("gdn_bwd", "kda_bwd"):
+            for name in ("gdn_bwd", "kda_bwd", "gdn_bwd_saved", "kda_bwd_saved"):
                 getattr(L, name).argtypes = [sp] + [vp] * 14 + [vp, sz, vp]
                 getattr(L, name).restype = ctypes.c_int
             L.gdn_status_str.argtypes = [ctypes.c_int]
@@ -142,6 +143,13 @@ def bwd_workspace_bytes(q, v, chunk=64, kda=False) -> int:
     return int((L.kda_bwd_workspace if kda else L.gdn_bwd_workspace)(ctypes.byref(s)))
 
 
+def ctx_bytes(q, v, chunk=64, kda=False) -> int:
+    """Bytes of the saved context of ``*_fwd_save`` / ``*_bwd_saved``."""
+    L = lib()
+    s = make_shape(q, v, chunk)
+    return int((L.kda_ctx_bytes if kda else L.gdn_ctx_bytes)(ctypes.byref(s)))
+
+
 def _workspace(need, given, device):
     if given is not None and given.numel() >= need:
         return given
@@ -154,22 +162,35 @@ def uses_tensor_cores(q, v, chunk=64) -> bool:
 
 
 def _fwd(kda, q, k, v, g, beta, h0=None, chunk=64, output_final_state=True, out=None,
-         workspace=None):
+         workspace=None, ctx=None):
     B, T, H, dk = q.shape
     dv = v.shape[3]
     _validate(q, k, v, g, beta, kda, [("h0", (h0, (B, H, dk, dv), torch.float32))])
     o = out if out is not None else torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     ht = (torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
           if output_final_state else None)
-    ws = _workspace(fwd_workspace_bytes(q, v, chunk, kda), workspace, q.device)
+    if ctx is not None:
+        _check_ctx(ctx, ctx_bytes(q, v, chunk, kda), q.device)
+        ws = ctx
+        fn = lib().kda_fwd_save if kda else lib().gdn_fwd_save
+    else:
+        ws = _workspace(fwd_workspace_bytes(q, v, chunk, kda), workspace, q.device)
+        fn = lib().kda_fwd if kda else lib().gdn_fwd
     s = make_shape(q, v, chunk)
-    fn = lib().kda_fwd if kda else lib().gdn_fwd
     _check(fn(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
               _ptr(ht), _ptr(ws), ws.numel(), _stream(q.device)))
     return o, ht
 
 
-def _bwd(kda, q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, workspace=None):
+def _check_ctx(ctx, need, device):
+    if (not isinstance(ctx, torch.Tensor) or ctx.dtype != torch.uint8 or ctx.device != device
+            or not ctx.is_contiguous() or ctx.numel() < need):
+        raise GdnError(f"ctx must be a contiguous uint8 tensor of at least {need} bytes "
+                       f"on {device} (see new_ctx)")
+
+
+def _bwd(kda, q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, workspace=None,
+         ctx=None):
     B, T, H, dk = q.shape
     dv = v.shape[3]
     _validate(q, k, v, g, beta, kda, [("h0", (h0, (B, H, dk, dv), torch.float32)),
@@ -178,9 +199,14 @@ def _bwd(kda, q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, works
     e = lambda x: torch.empty_like(x)
     dq, dk_, dv_, dg, dbeta = e(q), e(k), e(v), e(g), e(beta)
     dh0 = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device) if want_dh0 else None
-    ws = _workspace(bwd_workspace_bytes(q, v, chunk, kda), workspace, q.device)
+    if ctx is not None:
+        _check_ctx(ctx, ctx_bytes(q, v, chunk, kda), q.device)
+        ws = ctx
+        fn = lib().kda_bwd_saved if kda else lib().gdn_bwd_saved
+    else:
+        ws = _workspace(bwd_workspace_bytes(q, v, chunk, kda), workspace, q.device)
+        fn = lib().kda_bwd if kda else lib().gdn_bwd
     s = make_shape(q, v, chunk)
-    fn = lib().kda_bwd if kda else lib().gdn_bwd
     _check(fn(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(do),
               _ptr(dht), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(dbeta), _ptr(dh0),
               _ptr(ws), ws.numel(), _stream(q.device)))
@@ -207,6 +233,37 @@ def gdn_bwd(q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, workspa
 def kda_bwd(q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, workspace=None):
     """KDA backward.  Returns a dict ``dq, dk, dv, dg, dbeta, dh0``."""
     return _bwd(True, q, k, v, g, beta, h0, do, dht, chunk, want_dh0, workspace)
+
+
+def new_ctx(q, v, chunk=64, kda=False):
+    """An uninitialised saved-context buffer for ``q``/``v``'s shape."""
+    return torch.empty(max(16, ctx_bytes(q, v, chunk, kda)), dtype=torch.uint8, device=q.device)
+
+
+def gdn_fwd_save(q, k, v, g, beta, h0=None, chunk=64, output_final_state=True, ctx=None):
+    """GDN forward that also leaves the saved context for ``gdn_bwd_saved``.
+    Returns ``(o, ht, ctx)``; ``ctx`` (from ``new_ctx``) is allocated if not given."""
+    ctx = new_ctx(q, v, chunk) if ctx is None else ctx
+    o, ht = _fwd(False, q, k, v, g, beta, h0, chunk, output_final_state, ctx=ctx)
+    return o, ht, ctx
+
+
+def kda_fwd_save(q, k, v, g, beta, h0=None, chunk=64, output_final_state=True, ctx=None):
+    """KDA forward that also leaves the saved context for ``kda_bwd_saved``."""
+    ctx = new_ctx(q, v, chunk, True) if ctx is None else ctx
+    o, ht = _fwd(True, q, k, v, g, beta, h0, chunk, output_final_state, ctx=ctx)
+    return o, ht, ctx
+
+
+def gdn_bwd_saved(q, k, v, g, beta, h0, do, ctx, dht=None, chunk=64, want_dh0=True):
+    """GDN backward reading the context ``gdn_fwd_save`` left in ``ctx`` (the same
+    q, k, v, g, beta, h0 must be passed).  Returns the dict of ``gdn_bwd``."""
+    return _bwd(False, q, k, v, g, beta, h0, do, dht, chunk, want_dh0, ctx=ctx)
+
+
+def kda_bwd_saved(q, k, v, g, beta, h0, do, ctx, dht=None, chunk=64, want_dh0=True):
+    """KDA backward reading the context ``kda_fwd_save`` left in ``ctx``."""
+    return _bwd(True, q, k, v, g, beta, h0, do, dht, chunk, want_dh0, ctx=ctx)
 
 
 def device_status() -> int:
@@ -243,24 +300,32 @@ class KernelTimer:
 
 
 class GatedDeltaRule(torch.autograd.Function):
-    """Autograd wrapper: forward via ``gdn_fwd``/``kda_fwd``, backward via
-    ``gdn_bwd``/``kda_bwd`` (inputs are saved; the library recomputes)."""
+    """Autograd wrapper: forward via ``*_fwd`` (``*_fwd_save`` with
+    ``save_context``), backward via ``*_bwd`` (``*_bwd_saved``).  The inputs
+    are saved; with ``save_context`` the forward also keeps the per-chunk
+    entry states and solve results (``ctx_bytes``) instead of the backward
+    recomputing them."""
 
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, h0, chunk, kda):
-        o, ht = _fwd(kda, q, k, v, g, beta, h0, chunk, True)
+    def forward(ctx, q, k, v, g, beta, h0, chunk, kda, save_context):
+        saved = new_ctx(q, v, chunk, kda) if save_context else None
+        o, ht = _fwd(kda, q, k, v, g, beta, h0, chunk, True, ctx=saved)
         ctx.save_for_backward(q, k, v, g, beta, h0)
-        ctx.chunk, ctx.kda = chunk, kda
+        ctx.chunk, ctx.kda, ctx.saved = chunk, kda, saved
         return o, ht
 
     @staticmethod
     def backward(ctx, do, dht):
         q, k, v, g, beta, h0 = ctx.saved_tensors
         gr = _bwd(ctx.kda, q, k, v, g, beta, h0, do.contiguous(),
-                  None if dht is None else dht.contiguous(), ctx.chunk, h0 is not None)
-        return gr["dq"], gr["dk"], gr["dv"], gr["dg"], gr["dbeta"], gr["dh0"], None, None
+                  None if dht is None else dht.contiguous(), ctx.chunk, h0 is not None,
+                  ctx=ctx.saved)
+        ctx.saved = None
+        return (gr["dq"], gr["dk"], gr["dv"], gr["dg"], gr["dbeta"], gr["dh0"], None, None,
+                None)
 
 
-def gated_delta_rule(q, k, v, g, beta, h0=None, chunk=64, kda=False):
-    """Differentiable mixer: returns ``(o, final_state)``."""
-    return GatedDeltaRule.apply(q, k, v, g, beta, h0, chunk, kda)
+def gated_delta_rule(q, k, v, g, beta, h0=None, chunk=64, kda=False, save_context=True):
+    """Differentiable mixer: returns ``(o, final_state)``.  ``save_context``
+    trades ``ctx_bytes`` of device memory per call for a faster backward."""
+    return GatedDeltaRule.apply(q, k, v, g, beta, h0, chunk, kda, save_context)

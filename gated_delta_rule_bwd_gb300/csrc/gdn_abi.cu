@@ -57,6 +57,13 @@ size_t bwd_ws(const gdn::Problem& p) {
   return gdn::tc_supported(p) ? gdn::tc_bwd_workspace(p) : gdn::simt_bwd_workspace(p);
 }
 
+// The CUDA-core path keeps nothing between the passes: its context is the
+// backward pass's workspace.
+size_t ctx_bytes(const gdn::Problem& p) {
+  if (empty(p) || p.T == 0) return 0;
+  return gdn::tc_supported(p) ? gdn::tc_ctx_bytes(p) : gdn::simt_bwd_workspace(p);
+}
+
 // Zero-length sequences: the final state is the initial one and every
 // gradient of the (empty) token tensors is empty.
 cudaError_t copy_state_or_zero(float* dst, const float* src, const gdn::Problem& p,
@@ -69,7 +76,7 @@ cudaError_t copy_state_or_zero(float* dst, const float* src, const gdn::Problem&
 
 int run_fwd(const gdn_shape* shape, bool kda, const void* q, const void* k, const void* v,
             const float* g, const float* beta, const float* h0, void* o, float* ht, void* ws,
-            size_t ws_bytes, void* stream) {
+            size_t ws_bytes, void* stream, bool save = false) {
   gdn::Problem p;
   int rc = check_shape(shape, kda, &p);
   if (rc != GDN_OK) return rc;
@@ -84,18 +91,18 @@ int run_fwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
     cudaError_t e = copy_state_or_zero(ht, h0, p, st);
     return e == cudaSuccess ? GDN_OK : fail_cuda(e);
   }
-  const size_t need = fwd_ws(p);
+  const size_t need = save ? ctx_bytes(p) : fwd_ws(p);
   if (need > 0 && (!ws || ws_bytes < need)) return GDN_ERR_WORKSPACE;
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.o = o; p.ht = ht;
   p.ws = ws; p.ws_bytes = ws_bytes;
-  cudaError_t e = gdn::tc_supported(p) ? gdn::tc_fwd(p, st) : gdn::simt_fwd(p, st);
+  cudaError_t e = gdn::tc_supported(p) ? gdn::tc_fwd(p, st, save) : gdn::simt_fwd(p, st);
   return e == cudaSuccess ? GDN_OK : fail_cuda(e);
 }
 
 int run_bwd(const gdn_shape* shape, bool kda, const void* q, const void* k, const void* v,
             const float* g, const float* beta, const float* h0, const void* do_,
             const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
-            float* dh0, void* ws, size_t ws_bytes, void* stream) {
+            float* dh0, void* ws, size_t ws_bytes, void* stream, bool saved = false) {
   gdn::Problem p;
   int rc = check_shape(shape, kda, &p);
   if (rc != GDN_OK) return rc;
@@ -110,12 +117,12 @@ int run_bwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
     cudaError_t e = copy_state_or_zero(dh0, dht, p, st);
     return e == cudaSuccess ? GDN_OK : fail_cuda(e);
   }
-  const size_t need = bwd_ws(p);
+  const size_t need = saved ? ctx_bytes(p) : bwd_ws(p);
   if (need > 0 && (!ws || ws_bytes < need)) return GDN_ERR_WORKSPACE;
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.do_ = do_; p.dht = dht;
   p.dq = dq; p.dk_ = dk; p.dv_ = dv; p.dg = dg; p.dbeta = dbeta; p.dh0 = dh0;
   p.ws = ws; p.ws_bytes = ws_bytes;
-  cudaError_t e = gdn::tc_supported(p) ? gdn::tc_bwd(p, st) : gdn::simt_bwd(p, st);
+  cudaError_t e = gdn::tc_supported(p) ? gdn::tc_bwd(p, st, saved) : gdn::simt_bwd(p, st);
   return e == cudaSuccess ? GDN_OK : fail_cuda(e);
 }
 
@@ -123,6 +130,12 @@ size_t query_ws(const gdn_shape* shape, bool kda, bool bwd) {
   gdn::Problem p;
   if (check_shape(shape, kda, &p) != GDN_OK) return 0;
   return bwd ? bwd_ws(p) : fwd_ws(p);
+}
+
+size_t query_ctx(const gdn_shape* shape, bool kda) {
+  gdn::Problem p;
+  if (check_shape(shape, kda, &p) != GDN_OK) return 0;
+  return ctx_bytes(p);
 }
 
 }  // namespace
@@ -223,6 +236,37 @@ int kda_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
             void* stream) {
   return run_bwd(shape, true, q, k, v, g, beta, h0, do_, dht, dq, dk, dv, dg, dbeta, dh0, ws,
                  ws_bytes, stream);
+}
+
+size_t gdn_ctx_bytes(const gdn_shape* shape) { return query_ctx(shape, false); }
+size_t kda_ctx_bytes(const gdn_shape* shape) { return query_ctx(shape, true); }
+
+int gdn_fwd_save(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                 const float* g, const float* beta, const float* h0, void* o, float* ht,
+                 void* ctx, size_t ctx_bytes, void* stream) {
+  return run_fwd(shape, false, q, k, v, g, beta, h0, o, ht, ctx, ctx_bytes, stream, true);
+}
+
+int kda_fwd_save(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                 const float* g, const float* beta, const float* h0, void* o, float* ht,
+                 void* ctx, size_t ctx_bytes, void* stream) {
+  return run_fwd(shape, true, q, k, v, g, beta, h0, o, ht, ctx, ctx_bytes, stream, true);
+}
+
+int gdn_bwd_saved(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                  const float* g, const float* beta, const float* h0, const void* do_,
+                  const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                  float* dh0, void* ctx, size_t ctx_bytes, void* stream) {
+  return run_bwd(shape, false, q, k, v, g, beta, h0, do_, dht, dq, dk, dv, dg, dbeta, dh0, ctx,
+                 ctx_bytes, stream, true);
+}
+
+int kda_bwd_saved(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                  const float* g, const float* beta, const float* h0, const void* do_,
+                  const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                  float* dh0, void* ctx, size_t ctx_bytes, void* stream) {
+  return run_bwd(shape, true, q, k, v, g, beta, h0, do_, dht, dq, dk, dv, dg, dbeta, dh0, ctx,
+                 ctx_bytes, stream, true);
 }
 
 const char* gdn_status_str(int status) {

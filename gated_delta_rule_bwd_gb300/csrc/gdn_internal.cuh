@@ -32,8 +32,11 @@ cudaError_t simt_bwd(const Problem& p, cudaStream_t s);
 bool tc_supported(const Problem& p);
 size_t tc_fwd_workspace(const Problem& p);
 size_t tc_bwd_workspace(const Problem& p);
-cudaError_t tc_fwd(const Problem& p, cudaStream_t s);
-cudaError_t tc_bwd(const Problem& p, cudaStream_t s);
+size_t tc_ctx_bytes(const Problem& p);
+// save / saved: the workspace is a saved context (tc_ctx_bytes) that the
+// forward fills and the backward of the same inputs reads.
+cudaError_t tc_fwd(const Problem& p, cudaStream_t s, bool save);
+cudaError_t tc_bwd(const Problem& p, cudaStream_t s, bool saved);
 
 // Kernel ids reported by the timing hook (gdn_profile_*).
 enum KernelId {

@@ -1731,15 +1731,16 @@ int sm_count() {
   return n;
 }
 
-// Chunks per segment of the forward pass, or 0 for no segments: only when the
-// sequences fill at most half of the SMs and are at least 64 chunks long;
-// segments are at least 32 chunks.
+// Chunks per segment of the forward pass, or 0 for no segments.  Segments
+// cost about three times the arithmetic, so they are used only when they
+// multiply the number of busy SMs by at least four; segments are at least 32
+// chunks long.
 int fwd_seg_chunks(const Problem& p) {
   const long seqs = (long)p.B * p.H;
   const int sms = sm_count();
-  if (seqs <= 0 || seqs * 2 > sms || p.N < 64) return 0;
+  if (seqs <= 0 || p.N < 128) return 0;
   const long want = std::min<long>(sms / seqs, p.N / 32);
-  if (want < 2) return 0;
+  if (want < 4) return 0;
   return (int)((p.N + want - 1) / want);
 }
 
@@ -1757,25 +1758,37 @@ bool tc_supported(const Problem& p) {
 size_t tiles_bytes(const Problem& p) { return align_up((size_t)p.B * p.H * p.N * 8192, 256); }
 size_t states_bytes(const Problem& p) { return align_up((size_t)p.B * p.H * p.N * 32768, 256); }
 
+size_t seg_scratch_bytes(const Problem& p) {
+  const int sc = fwd_seg_chunks(p);
+  return sc ? 3 * seg_state_bytes(p, sc) : 0;
+}
+
 // Workspace of the tensor-core forward pass: the T tile of every chunk; with
 // segments also M, N and the entry state of every segment (fp32, dk x dv).
-size_t tc_fwd_workspace(const Problem& p) {
-  const int sc = fwd_seg_chunks(p);
-  return tiles_bytes(p) + (sc ? 3 * seg_state_bytes(p, sc) : 0);
-}
+size_t tc_fwd_workspace(const Problem& p) { return tiles_bytes(p) + seg_scratch_bytes(p); }
 
 // Workspace of the tensor-core backward pass: the bf16 entry state of every
 // chunk in MMA-operand layout (32 KB each), then the T tile of every chunk.
 size_t tc_bwd_workspace(const Problem& p) { return states_bytes(p) + tiles_bytes(p); }
 
-cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
-  unsigned char* tiles = static_cast<unsigned char*>(p.ws);
+// Saved context: the backward pass's workspace as the forward pass leaves it
+// (entry states, then T tiles), then the forward's segment scratch.
+size_t tc_ctx_bytes(const Problem& p) { return tc_bwd_workspace(p) + seg_scratch_bytes(p); }
+
+// With save, the workspace is a saved context: the output pass also writes
+// every chunk's bf16 entry state in front of the T tiles, where the backward
+// pass of the same inputs finds both.
+cudaError_t tc_fwd(const Problem& p, cudaStream_t s, bool save) {
+  unsigned char* ws = static_cast<unsigned char*>(p.ws);
+  __nv_bfloat16* states = save ? reinterpret_cast<__nv_bfloat16*>(ws) : nullptr;
+  unsigned char* tiles = save ? ws + states_bytes(p) : ws;
   cudaError_t e = launch_solve(p, s, tiles);
   if (e != cudaSuccess) return e;
   const int sc = fwd_seg_chunks(p);
   if (!sc) {
     FwdLaunch f;
     f.want_out = true;
+    f.states = states;
     f.h0 = p.h0;
     f.ht = p.ht;
     return launch_fwd(p, s, tiles, f);
@@ -1807,23 +1820,27 @@ cudaError_t tc_fwd(const Problem& p, cudaStream_t s) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   FwdLaunch o;  // outputs from every segment's entry state
   o.want_out = true;
+  o.states = states;
   o.h0 = Hin;
   o.seg_chunks = sc;
   return launch_fwd(p, s, tiles, o);
 }
 
-cudaError_t tc_bwd(const Problem& p, cudaStream_t s) {
+// With saved, the workspace is a context filled by tc_fwd(save) on the same
+// inputs: the solve and the states pass are not run again.
+cudaError_t tc_bwd(const Problem& p, cudaStream_t s, bool saved) {
   unsigned char* ws = static_cast<unsigned char*>(p.ws);
   __nv_bfloat16* states = reinterpret_cast<__nv_bfloat16*>(ws);
   unsigned char* tiles = ws + states_bytes(p);
-  cudaError_t e = launch_solve(p, s, tiles);
-  if (e != cudaSuccess) return e;
-  FwdLaunch st;
-  st.states = states;
-  st.h0 = p.h0;
-  st.kernel_id = kTcStates;
-  e = launch_fwd(p, s, tiles, st);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
+  if (!saved) {
+    if ((e = launch_solve(p, s, tiles)) != cudaSuccess) return e;
+    FwdLaunch st;
+    st.states = states;
+    st.h0 = p.h0;
+    st.kernel_id = kTcStates;
+    if ((e = launch_fwd(p, s, tiles, st)) != cudaSuccess) return e;
+  }
   CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
   if ((e = make_token_map(&mq, p.q, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mk, p.k, p)) != cudaSuccess) return e;

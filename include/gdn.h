@@ -19,7 +19,10 @@
  * The backward entry points return the gradients of a scalar loss with
  * respect to q, k, v, g, beta and the initial state, given dL/do and
  * (optionally) dL/d(final state).  They take the forward inputs again and
- * recompute what they need; no context is saved between calls.
+ * recompute what they need; no context is saved between calls.  The
+ * *_fwd_save / *_bwd_saved pair below is the same computation with the
+ * forward pass keeping, in a caller-owned buffer, what the backward pass
+ * would otherwise recompute.
  *
  * Layout (all row-major, innermost dimension contiguous):
  *   q, k, dq, dk          [B, T, H, dk]   dtype per gdn_shape.dtype
@@ -129,6 +132,51 @@ GDN_API int kda_bwd(const gdn_shape* shape, const void* q, const void* k, const 
             const float* g, const float* beta, const float* h0, const void* do_,
             const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
             float* dh0, void* ws, size_t ws_bytes, void* stream);
+
+/* Training step with a saved context.  The backward pass needs the state
+ * entering every chunk and the triangular-solve result of every chunk (the
+ * chunkwise form of the recurrence above); gdn_bwd recomputes both.  The
+ * pair below lets the forward pass keep them instead, in a caller-owned
+ * device buffer `ctx` of at least *_ctx_bytes() bytes:
+ *
+ *   *_fwd_save   is *_fwd (same arguments, same results) using ctx as its
+ *                workspace and leaving the context in it;
+ *   *_bwd_saved  is *_bwd (same arguments, same results up to rounding) using
+ *                ctx as its workspace and reading the context from it instead
+ *                of recomputing it.
+ *
+ * The caller must pass *_bwd_saved the same shape and the same q, k, v, g,
+ * beta and h0 contents as the *_fwd_save that filled ctx, with ctx not
+ * written in between (nor used by another call in flight); the library
+ * cannot check this, and other inputs give meaningless gradients.  On the
+ * tensor-core path the context holds the bf16 entry state of every chunk
+ * (32 KB) and its bf16 T = (I + A)^-1 tile (8 KB), plus the forward's
+ * segment scratch; the result equals *_bwd's bit for bit when the forward
+ * ran without segments.  On the CUDA-core path nothing is kept and
+ * *_bwd_saved recomputes.  ctx needs no initialisation.  Errors as for
+ * *_fwd / *_bwd, with GDN_ERR_WORKSPACE when ctx is NULL or smaller than
+ * *_ctx_bytes(); *_ctx_bytes() is 0 for an invalid shape or one with no
+ * work, and depends on the current device's SM count. */
+GDN_API size_t gdn_ctx_bytes(const gdn_shape* shape);
+GDN_API size_t kda_ctx_bytes(const gdn_shape* shape);
+
+GDN_API int gdn_fwd_save(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, const float* h0, void* o, float* ht,
+                         void* ctx, size_t ctx_bytes, void* stream);
+
+GDN_API int gdn_bwd_saved(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                          const float* g, const float* beta, const float* h0, const void* do_,
+                          const float* dht, void* dq, void* dk, void* dv, float* dg,
+                          float* dbeta, float* dh0, void* ctx, size_t ctx_bytes, void* stream);
+
+GDN_API int kda_fwd_save(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, const float* h0, void* o, float* ht,
+                         void* ctx, size_t ctx_bytes, void* stream);
+
+GDN_API int kda_bwd_saved(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                          const float* g, const float* beta, const float* h0, const void* do_,
+                          const float* dht, void* dq, void* dk, void* dv, float* dg,
+                          float* dbeta, float* dh0, void* ctx, size_t ctx_bytes, void* stream);
 
 /* Human-readable name of a gdn_status value. */
 GDN_API const char* gdn_status_str(int status);

@@ -129,6 +129,32 @@ def test_forward_workspace_query_and_check(L):
     assert L.gdn_fwd_workspace(ctypes.byref(shape(chunk=3))) == 0
 
 
+def test_saved_context_size_and_check(L):
+    big = shape(B=2, T=2048, H=4, dk=128, dv=128, chunk=64, dtype=1)
+    need = L.gdn_ctx_bytes(ctypes.byref(big))
+    # the backward's workspace (entry states + T tiles) as the forward leaves it
+    assert need >= L.gdn_bwd_workspace(ctypes.byref(big))
+    assert need >= L.gdn_fwd_workspace(ctypes.byref(big))
+    long = shape(B=1, T=64 * 1024, H=2, dk=128, dv=128, chunk=64, dtype=1)
+    assert L.gdn_ctx_bytes(ctypes.byref(long)) >= max(L.gdn_fwd_workspace(ctypes.byref(long)),
+                                                      L.gdn_bwd_workspace(ctypes.byref(long)))
+    # CUDA-core path: the context is the backward's workspace
+    f32 = shape(B=2, T=2048, H=4, dk=128, dv=128, chunk=64, dtype=0)
+    assert L.gdn_ctx_bytes(ctypes.byref(f32)) == L.gdn_bwd_workspace(ctypes.byref(f32))
+    assert L.kda_ctx_bytes(ctypes.byref(big)) == L.kda_bwd_workspace(ctypes.byref(big))
+    assert L.gdn_ctx_bytes(ctypes.byref(shape(B=0))) == 0
+    assert L.gdn_ctx_bytes(ctypes.byref(shape(chunk=3))) == 0
+    fwd_args = (ctypes.byref(big), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None)
+    bwd_args = (ctypes.byref(big),) + (FAKE,) * 5 + (None, FAKE, None) + (FAKE,) * 5 + (None,)
+    for fn, args in ((L.gdn_fwd_save, fwd_args), (L.gdn_bwd_saved, bwd_args)):
+        assert fn(*args, None, 0, None) == GDN_ERR_WORKSPACE
+        # a buffer big enough for the plain pass is still too small for the context
+        assert fn(*args, FAKE, need - 1, None) == GDN_ERR_WORKSPACE
+        assert fn(*args, ctypes.c_void_p(0x10008), need, None) == GDN_ERR_ALIGN
+    assert L.gdn_fwd_save(ctypes.byref(shape(B=0)), *fwd_args[1:], None, 0, None) == GDN_OK
+    assert L.kda_bwd_saved(ctypes.byref(shape(H=0)), *bwd_args[1:], None, 0, None) == GDN_OK
+
+
 def test_empty_batch_is_a_no_op(L):
     assert call_fwd(L, shape(B=0)) == GDN_OK
     assert call_fwd(L, shape(H=0), q=None) == GDN_OK

@@ -140,10 +140,10 @@ def test_long_context_forward_sampled():
 
 def test_segmented_forward_matches_oracle():
     """Few sequences, many chunks: the forward splits each sequence into
-    segments (transition and local-state passes, an fp32 combine, then the
-    output pass).  Output and final state against the oracle, with an initial
+    segments (here five; transition and local-state passes, an fp32 combine,
+    then the output pass).  Output and final state against the oracle, with an initial
     state and a ragged tail; the combine kernel must have run."""
-    x = make_inputs(1, 64 * 96 + 17, 2, 128, 128, dtype="bf16", h0_std=0.3, seed=12)
+    x = make_inputs(1, 64 * 160 + 17, 2, 128, 128, dtype="bf16", h0_std=0.3, seed=12)
     d = x.to("cuda")
     with gdn.KernelTimer() as t:
         o, ht = gdn.gdn_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0)
@@ -151,6 +151,78 @@ def test_segmented_forward_matches_oracle():
     names = [n for n, _ in t.records()]
     assert "tc_combine" in names and names.count("tc_fwd_segment") == 2, names
     compare(x, o, ht, None, fp32=False)
+
+
+# ----------------------------------------------------------- saved context
+
+SAVED = [
+    # B, T, H, dk, dv, chunk, dtype, kda
+    (2, 200, 2, 128, 128, 64, "bf16", False),   # tensor-core path, 8-token tail
+    (1, 37, 3, 128, 128, 64, "bf16", False),    # tensor-core path, T < chunk
+    (2, 100, 3, 32, 48, 32, "f32", False),      # CUDA-core path: the context is a workspace
+    (2, 200, 2, 64, 64, 64, "bf16", True),      # KDA
+]
+
+
+@pytest.mark.parametrize("case", SAVED, ids=lambda c: "x".join(map(str, c)))
+def test_saved_context_matches_oracle_and_recompute(case):
+    """*_fwd_save then *_bwd_saved against the oracle, and bit-equal to the
+    recomputing *_fwd / *_bwd.  The context buffer starts out as garbage, so
+    every byte the backward reads must have been written by the forward; on
+    the tensor-core path the backward launches neither the solve nor the
+    states pass."""
+    B, T, H, dk, dv, chunk, dtype, kda = case
+    x = make_inputs(B, T, H, dk, dv, kda=kda, dtype=dtype, h0_std=0.3, with_dht=True, seed=13)
+    d = x.to("cuda")
+    fwd_s = gdn.kda_fwd_save if kda else gdn.gdn_fwd_save
+    bwd_s = gdn.kda_bwd_saved if kda else gdn.gdn_bwd_saved
+    ctx = gdn.new_ctx(d.q, d.v, chunk, kda).fill_(0xAB)
+    o, ht, ctx = fwd_s(d.q, d.k, d.v, d.g, d.beta, d.h0, chunk=chunk, ctx=ctx)
+    with gdn.KernelTimer() as t:
+        gr = bwd_s(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, ctx, d.dht, chunk=chunk)
+        torch.cuda.synchronize()
+    names = [n for n, _ in t.records()]
+    if gdn.uses_tensor_cores(d.q, d.v, chunk):
+        assert names == ["tc_bwd"], names
+    compare(x, o, ht, gr, fp32=dtype == "f32")
+    ro, rht, rgr = run_gpu(x, chunk)
+    assert torch.equal(o, ro) and torch.equal(ht, rht)
+    for n in rgr:
+        assert torch.equal(gr[n], rgr[n]), n
+
+
+def test_saved_context_from_segmented_forward():
+    """The context left by a segmented forward (five segments; entry states
+    of later segments come from the fp32 combine).  dO is zero from token tau
+    on and there is no final-state gradient, so the gradients of the first
+    tau tokens are those of the prefix problem alone (which the oracle
+    solves) and the rest are zero.  Over the whole sequence the result
+    matches the recomputing backward up to the rounding of the segment entry
+    states."""
+    T, tau = 64 * 160 + 17, 4000
+    x = make_inputs(1, T, 2, 128, 128, dtype="bf16", h0_std=0.3, seed=14)
+    x.do[:, tau:] = 0
+    d = x.to("cuda")
+    ctx = gdn.new_ctx(d.q, d.v).fill_(0xAB)
+    with gdn.KernelTimer() as t:
+        o, ht, ctx = gdn.gdn_fwd_save(d.q, d.k, d.v, d.g, d.beta, d.h0, ctx=ctx)
+        gr = gdn.gdn_bwd_saved(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, ctx)
+        torch.cuda.synchronize()
+    names = [n for n, _ in t.records()]
+    assert "tc_combine" in names and names.count("tc_solve") == 1, names
+    assert "tc_states" not in names, names
+    po, pht = gdn.gdn_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0)
+    assert torch.equal(o, po) and torch.equal(ht, pht)
+    pre = lambda t: t[:, :tau].contiguous()
+    ref = oracle.bwd(pre(x.q), pre(x.k), pre(x.v), pre(x.g), pre(x.beta), x.h0, pre(x.do), None)
+    for n in ("dq", "dk", "dv", "dg", "dbeta"):
+        full = np.zeros(gr[n].shape)
+        full[:, :tau] = ref[n]
+        check(n, gr[n].cpu(), full, fp32=False)
+    check("dh0", gr["dh0"].cpu(), ref["dh0"], fp32=False)
+    rg = gdn.gdn_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do)
+    for n in rg:
+        assert rel_l2(gr[n].float().cpu(), rg[n].float().cpu()) < 5e-3, n
 
 
 # ----------------------------------------------------------- invariants on the GPU
@@ -244,10 +316,11 @@ def test_empty_sequence_copies_state():
     assert torch.equal(ht, d.h0) and torch.equal(gr["dh0"], d.dht)
 
 
-def test_autograd_wrapper_matches_direct_calls():
+@pytest.mark.parametrize("save_context", [True, False])
+def test_autograd_wrapper_matches_direct_calls(save_context):
     x = make_inputs(1, 128, 2, 128, 128, dtype="bf16", h0_std=0.1, seed=8).to("cuda")
     q, k, v = (t.clone().requires_grad_() for t in (x.q, x.k, x.v))
-    o, ht = gdn.gated_delta_rule(q, k, v, x.g, x.beta, x.h0)
+    o, ht = gdn.gated_delta_rule(q, k, v, x.g, x.beta, x.h0, save_context=save_context)
     (o.float() * x.do.float()).sum().backward()
     ref = gdn.gdn_bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do)
     assert torch.equal(q.grad, ref["dq"]) and torch.equal(v.grad, ref["dv"])
