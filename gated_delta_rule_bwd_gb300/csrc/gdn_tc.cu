@@ -19,9 +19,10 @@
 //               MMA3  U^T = V^T T''^T - G W^T, T'' = T diag(beta)
 //               MMA4  O = (eQ) G^T + P U          (M = 64: rows are tokens)
 //               MMA5  G <- eC G + (U diag(f))^T K
-//             The output rows and (in states mode, for the backward pass,
-//             which skips P and O) every chunk's bf16 entry state leave the
-//             CTA by TMA / bulk copies of their shared-memory tiles.
+//             The output rows and, when asked, every chunk's bf16 entry state
+//             (for the backward pass: in states mode, which skips P and O, or
+//             alongside the output for a saved context) leave the CTA by
+//             TMA / bulk copies of their shared-memory tiles.
 //   backward  the reverse chunk scan (described at its kernel).
 //
 // The TMA tiles of K and V serve both as K-major operands (rows = tokens) and,
@@ -31,6 +32,7 @@
 // status word instead of hanging.
 
 #include <algorithm>
+#include <utility>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -488,6 +490,8 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   cta_sync();
   const uint32_t tmem = *tmem_slot;
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+  grid_dep_wait();  // the previous kernel's results (and its reads of what this one writes)
+  grid_dep_launch();
 
   auto load_kq = [&](int ci) {
     const int st = ci & 1;
@@ -912,6 +916,8 @@ gdn_tc_solve_kernel(const __grid_constant__ CUtensorMap tm_k, SolveParams p) {
   uint64_t* bar_mma = bar_ld + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma + 1);
 
+  grid_dep_wait();  // the previous kernel's results (and its reads of what this one writes)
+  grid_dep_launch();
   if (tid == 0) {
     mbar_init(bar_ld, 1);
     mbar_init(bar_mma, 1);
@@ -998,8 +1004,8 @@ gdn_tc_solve_kernel(const __grid_constant__ CUtensorMap tm_k, SolveParams p) {
 // held transposed, dG = dH^T (dv x dk), fp32 in TMEM (128 columns; the dG_in
 // product accumulates onto it) with a bf16 copy in shared memory as the MMA
 // operand.  Each chunk's entry state G_in comes from the workspace (written
-// by the forward kernel in states mode), and so does its T tile (written by
-// the solve kernel); the next chunk's tiles are requested as soon as each
+// by the forward kernel, in states mode or by the forward pass that filled a
+// saved context), and so does its T tile (written by the solve kernel); the next chunk's tiles are requested as soon as each
 // slot has been read for the last time.  With R = V - diag(e) K H_in,
 // U = T diag(beta) R, T = (I + A)^-1:
 //
@@ -1152,6 +1158,8 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   cta_sync();
   const uint32_t tmem = *tmem_slot;
   const uint32_t lb = (uint32_t)(quad * 32) << 16;
+  grid_dep_wait();  // the previous kernel's results (and its reads of what this one writes)
+  grid_dep_launch();
 
   // The running state gradient dG (fp32) lives in TMEM columns kBtG3..+127
   // (row c = lane, column d); the dG_in product accumulates onto it.  This
@@ -1619,6 +1627,26 @@ cudaError_t make_token_map(CUtensorMap* m, const void* ptr, const Problem& p) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Launches a kernel that may start while the previous kernel in the stream
+// finishes (programmatic stream serialization): the kernels of this file wait
+// for it with grid_dep_wait() after their prologue (barrier set-up, TMEM
+// allocation) and before any global-memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), unsigned grid, unsigned block,
+                              size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // T tiles of every chunk into `tiles` ([B*H][N][8 KB])
 cudaError_t launch_solve(const Problem& p, cudaStream_t s, unsigned char* tiles) {
   CUtensorMap mk;
@@ -1629,9 +1657,10 @@ cudaError_t launch_solve(const Problem& p, cudaStream_t s, unsigned char* tiles)
                            kSolveSmemBytes);
   if (e != cudaSuccess) return e;
   prof_before(s);
-  gdn_tc_solve_kernel<<<(unsigned)((size_t)p.B * p.H * p.N), ST, kSolveSmemBytes, s>>>(mk, sp);
+  e = launch_overlapped(gdn_tc_solve_kernel, (unsigned)((size_t)p.B * p.H * p.N), ST,
+                        kSolveSmemBytes, s, mk, sp);
   prof_after(s, kTcSolve);
-  return cudaGetLastError();
+  return e;
 }
 
 // One launch of the forward kernel.  Without segments: the whole forward
@@ -1660,9 +1689,10 @@ cudaError_t launch_fwd(const Problem& p, cudaStream_t s, const unsigned char* ti
   if (e != cudaSuccess) return e;
   const int nseg = f.seg_chunks ? (p.N + f.seg_chunks - 1) / f.seg_chunks : 1;
   prof_before(s);
-  gdn_tc_fwd_kernel<<<(unsigned)((size_t)p.B * p.H * nseg), FT, kSmemBytes, s>>>(mq, mk, mv, mo, fp);
+  e = launch_overlapped(gdn_tc_fwd_kernel, (unsigned)((size_t)p.B * p.H * nseg), FT, kSmemBytes,
+                        s, mq, mk, mv, mo, fp);
   prof_after(s, f.kernel_id);
-  return cudaGetLastError();
+  return e;
 }
 
 // ---------------------------------------------------------------- segmented forward
@@ -1857,9 +1887,10 @@ cudaError_t tc_bwd(const Problem& p, cudaStream_t s, bool saved) {
                            kBwdSmemBytes);
   if (e != cudaSuccess) return e;
   prof_before(s);
-  gdn_tc_bwd_kernel<<<p.B * p.H, BT, kBwdSmemBytes, s>>>(mq, mk, mv, mdo, mdq, mdk, mdv, bp);
+  e = launch_overlapped(gdn_tc_bwd_kernel, (unsigned)(p.B * p.H), BT, kBwdSmemBytes, s, mq, mk, mv,
+                        mdo, mdq, mdk, mdv, bp);
   prof_after(s, kTcBwd);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace gdn

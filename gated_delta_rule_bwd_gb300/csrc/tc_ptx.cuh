@@ -23,6 +23,21 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------------------------------ launch order
+//
+// Kernels launched with programmatic stream serialization may start while the
+// kernel before them in the stream is still running.  grid_dep_wait() blocks
+// until that kernel has completed and its memory is visible: it must precede
+// every global-memory access.  grid_dep_launch() lets the next such kernel
+// start its own prologue (it still waits for this one to complete).  Both are
+// no-ops for a kernel launched the ordinary way.
+
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
