@@ -225,6 +225,41 @@ def test_saved_context_from_segmented_forward():
         assert rel_l2(gr[n].float().cpu(), rg[n].float().cpu()) < 5e-3, n
 
 
+def test_saved_context_step_replays_in_a_cuda_graph():
+    """The training step (forward with saved context, then backward) captured
+    in a CUDA graph, whose kernels keep their overlapped-launch edges: each
+    replay reads the inputs' current contents and gives the bits of eager
+    calls on them."""
+    x = make_inputs(2, 200, 2, 128, 128, dtype="bf16", h0_std=0.1, with_dht=True, seed=15)
+    y = make_inputs(2, 200, 2, 128, 128, dtype="bf16", h0_std=0.1, with_dht=True, seed=16)
+    d = x.to("cuda")
+    ctx = gdn.new_ctx(d.q, d.v)
+
+    def step():
+        o, ht, _ = gdn.gdn_fwd_save(d.q, d.k, d.v, d.g, d.beta, d.h0, ctx=ctx)
+        gr = gdn.gdn_bwd_saved(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, ctx, d.dht)
+        return [o, ht] + [gr[n] for n in sorted(gr)]
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()  # warm-up off the capture stream
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        out = step()
+    for src in (x, y, x):
+        for n in ("q", "k", "v", "g", "beta", "h0", "do", "dht"):
+            getattr(d, n).copy_(getattr(src, n))
+        ref = [t.clone() for t in step()]
+        for t in out:
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(out, ref):
+            assert torch.equal(a, b)
+
+
 # ----------------------------------------------------------- invariants on the GPU
 
 def test_kda_with_broadcast_gate_equals_gdn():
