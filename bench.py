@@ -13,6 +13,8 @@ Default workload: GDN, B=16, T=2048, H=8, dk=dv=128, chunk 64, bf16 inputs
 with fp32 state (the 300M-model pre-training shape).  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  (default K: 1000 GDN steps, about 0.6 s timed, so that the clock samples
+  fall inside the timed region; 5 KDA steps; 20 for the reference arm)
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
 
 With N > 1 (launched by torch.distributed.run) every rank runs its own batch
@@ -133,7 +135,7 @@ def load_peaks():
 
 # ------------------------------------------------------------------ clocks
 
-CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -150,7 +152,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={CLOCK_FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -166,13 +168,20 @@ class ClockSampler:
                 self.proc.kill()
         return False
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Clock record of the samples taken between wall-clock times t0 and t1
+        (the timed region); all samples if none fall inside."""
+        import datetime
         rows = []
         try:
             for line in open(self.path):
                 f = [x.strip() for x in line.split(",")]
-                if len(f) >= 9 and f[1].replace(".", "").isdigit():
-                    rows.append(f)
+                if len(f) >= 10 and f[2].replace(".", "").isdigit():
+                    try:
+                        ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    except ValueError:
+                        ts = None
+                    rows.append([ts] + f[1:])
         except Exception:
             pass
         finally:
@@ -182,11 +191,15 @@ class ClockSampler:
                 pass
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        inside = [r for r in rows if t0 is not None and r[0] is not None and t0 <= r[0] <= t1]
+        in_region = bool(inside)
+        rows = inside or rows
+        rows = [r[1:] for r in rows]
         sm = [float(r[1]) for r in rows]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = [n for i, n in enumerate(names) if any(r[5 + i].lower() == "active" for r in rows)]
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
-                "reasons": reasons, "samples": len(rows),
+                "reasons": reasons, "samples": len(rows), "samples_in_timed_region": in_region,
                 "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
                 if any(r[3].replace(".", "").isdigit() for r in rows) else None}
 
@@ -299,30 +312,31 @@ def run_ours(args):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
 
-    def timed_steps(fn, cap):
+    def timed_steps(fn, cap, n=K):
         # cap = 0: the library only counts its launches (no events between its
         # kernels, which may then overlap one another's start and end)
         with gdn.KernelTimer(cap=cap) as t:
-            for i in range(K):
+            for i in range(n):
                 flush.fill_(i & 0xFF)  # evict L2 between timed steps (outside the events)
                 starts[i].record(stream)
                 fn()
                 ends[i].record(stream)
         torch.cuda.synchronize(dev)
-        return ([s.elapsed_time(e) for s, e in zip(starts, ends)], t.launches,
+        return ([s.elapsed_time(e) for s, e in zip(starts[:n], ends[:n])], t.launches,
                 t.records() if cap else [])
 
     with ClockSampler(torch.cuda.current_device()) as clocks:
         barrier(ws)
         torch.cuda.synchronize(dev)
-        wall0 = time.perf_counter()
+        wall0, epoch0 = time.perf_counter(), time.time()
         step_ms, launches, _ = timed_steps(step, 0)
-        wall = time.perf_counter() - wall0
+        wall, epoch1 = time.perf_counter() - wall0, time.time()
         barrier(ws)
     dev_s = sum(step_ms) / 1e3
     dev_s_max = max_over_ranks(dev_s, ws, dev)
-    # the same steps again with every library kernel bracketed by events
-    _, _, records = timed_steps(step, 64 * K)
+    # the same steps again (at most 100 of them) with every library kernel
+    # bracketed by events
+    _, _, records = timed_steps(step, 64 * min(K, 100), min(K, 100))
 
     # the recomputing variant of the step, timed the same way (reported beside)
     for _ in range(args.warmup):
@@ -394,7 +408,7 @@ def run_ours(args):
                                   "value": aggregate_tokens_per_s(tokens_step, K, ws, rc_s_max),
                                   "what": "backward recomputes the context (*_fwd + *_bwd)"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches * ws, "clocks": clocks.summary(),
+            "gpu_launches": launches * ws, "clocks": clocks.summary(epoch0, epoch1),
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -522,8 +536,11 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    # defaults: 1000 timed steps (about 0.6 s at the 300M shape, long enough for
+    # clock samples inside the timed region) for this library, 20 for the CPU
+    # oracle (about 0.3 s a step)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gdn_300m")
     ap.add_argument("--no-e2e", action="store_true")
@@ -532,6 +549,11 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()
+    if args.steps is None:
+        ours = 5 if WORKLOADS[args.workload].kda else 1000  # KDA: about 0.17 s a step
+        args.steps = 20 if args.impl == "reference" else ours
+    if args.warmup is None:
+        args.warmup = 3 if args.impl == "reference" or args.steps < 100 else 20
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
