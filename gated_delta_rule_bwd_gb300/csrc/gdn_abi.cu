@@ -57,8 +57,8 @@ size_t bwd_ws(const gdn::Problem& p) {
   return gdn::tc_supported(p) ? gdn::tc_bwd_workspace(p) : gdn::simt_bwd_workspace(p);
 }
 
-// The CUDA-core path keeps nothing between the passes: its context is the
-// backward pass's workspace.
+// The CUDA-core path's context is the backward pass's workspace, whose first
+// part (the fp32 entry state of every chunk) the forward pass fills.
 size_t ctx_bytes(const gdn::Problem& p) {
   if (empty(p) || p.T == 0) return 0;
   return gdn::tc_supported(p) ? gdn::tc_ctx_bytes(p) : gdn::simt_bwd_workspace(p);
@@ -95,7 +95,7 @@ int run_fwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
   if (need > 0 && (!ws || ws_bytes < need)) return GDN_ERR_WORKSPACE;
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.o = o; p.ht = ht;
   p.ws = ws; p.ws_bytes = ws_bytes;
-  cudaError_t e = gdn::tc_supported(p) ? gdn::tc_fwd(p, st, save) : gdn::simt_fwd(p, st);
+  cudaError_t e = gdn::tc_supported(p) ? gdn::tc_fwd(p, st, save) : gdn::simt_fwd(p, st, save);
   return e == cudaSuccess ? GDN_OK : fail_cuda(e);
 }
 
@@ -122,7 +122,8 @@ int run_bwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.do_ = do_; p.dht = dht;
   p.dq = dq; p.dk_ = dk; p.dv_ = dv; p.dg = dg; p.dbeta = dbeta; p.dh0 = dh0;
   p.ws = ws; p.ws_bytes = ws_bytes;
-  cudaError_t e = gdn::tc_supported(p) ? gdn::tc_bwd(p, st, saved) : gdn::simt_bwd(p, st);
+  cudaError_t e =
+      gdn::tc_supported(p) ? gdn::tc_bwd(p, st, saved) : gdn::simt_bwd(p, st, saved);
   return e == cudaSuccess ? GDN_OK : fail_cuda(e);
 }
 

@@ -25,8 +25,11 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // CUDA-core fp32 kernels (any dk, dv <= 128; chunk 16/32/64).
 size_t simt_bwd_workspace(const Problem& p);
-cudaError_t simt_fwd(const Problem& p, cudaStream_t s);
-cudaError_t simt_bwd(const Problem& p, cudaStream_t s);
+// save / saved: the workspace is a saved context (simt_bwd_workspace bytes);
+// the forward writes every chunk's fp32 entry state into it and the backward
+// reads them instead of running the states pass.
+cudaError_t simt_fwd(const Problem& p, cudaStream_t s, bool save);
+cudaError_t simt_bwd(const Problem& p, cudaStream_t s, bool saved);
 
 // Tensor-core kernels (bf16, dk = dv = 128, chunk = 64).
 bool tc_supported(const Problem& p);

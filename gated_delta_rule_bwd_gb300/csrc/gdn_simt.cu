@@ -621,11 +621,13 @@ cudaError_t launch_fwd(const Problem& p, cudaStream_t s, float* states, bool wan
   return cudaGetLastError();
 }
 
+// With saved, the workspace holds the entry states that launch_fwd wrote
+// alongside the output (a saved context), and the states pass is skipped.
 template <typename TIn, bool KDA>
-cudaError_t launch_bwd(const Problem& p, cudaStream_t s) {
+cudaError_t launch_bwd(const Problem& p, cudaStream_t s, bool saved) {
   float* states = static_cast<float*>(p.ws);
-  cudaError_t e = launch_fwd<TIn, KDA>(p, s, states, false);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
+  if (!saved && (e = launch_fwd<TIn, KDA>(p, s, states, false)) != cudaSuccess) return e;
   SimtArgs a{};
   a.p = p;
   a.dvs = pick_dvs_bwd(p);
@@ -655,16 +657,18 @@ size_t simt_bwd_workspace(const Problem& p) {
   return states_bytes(p) + align_up(part_layout(p, nsplit).total * sizeof(float), 256);
 }
 
-cudaError_t simt_fwd(const Problem& p, cudaStream_t s) {
-  if (p.bf16) return p.kda ? launch_fwd<__nv_bfloat16, true>(p, s, nullptr, true)
-                           : launch_fwd<__nv_bfloat16, false>(p, s, nullptr, true);
-  return p.kda ? launch_fwd<float, true>(p, s, nullptr, true)
-               : launch_fwd<float, false>(p, s, nullptr, true);
+cudaError_t simt_fwd(const Problem& p, cudaStream_t s, bool save) {
+  float* st = save ? static_cast<float*>(p.ws) : nullptr;
+  if (p.bf16) return p.kda ? launch_fwd<__nv_bfloat16, true>(p, s, st, true)
+                           : launch_fwd<__nv_bfloat16, false>(p, s, st, true);
+  return p.kda ? launch_fwd<float, true>(p, s, st, true) : launch_fwd<float, false>(p, s, st, true);
 }
 
-cudaError_t simt_bwd(const Problem& p, cudaStream_t s) {
-  if (p.bf16) return p.kda ? launch_bwd<__nv_bfloat16, true>(p, s) : launch_bwd<__nv_bfloat16, false>(p, s);
-  return p.kda ? launch_bwd<float, true>(p, s) : launch_bwd<float, false>(p, s);
+cudaError_t simt_bwd(const Problem& p, cudaStream_t s, bool saved) {
+  if (p.bf16)
+    return p.kda ? launch_bwd<__nv_bfloat16, true>(p, s, saved)
+                 : launch_bwd<__nv_bfloat16, false>(p, s, saved);
+  return p.kda ? launch_bwd<float, true>(p, s, saved) : launch_bwd<float, false>(p, s, saved);
 }
 
 }  // namespace gdn

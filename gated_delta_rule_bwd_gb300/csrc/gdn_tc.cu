@@ -1250,7 +1250,6 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   for (int ci = p.N - 1; ci >= 0 && ok; --ci) {
     const int t0 = ci * C, n = min(C, p.T - t0);
-    if (tid == 0) bulk_wait_read_all();  // X0 / X1 staging of the previous chunk has been read
     fence_async_shared();
     cta_sync();
     if (tid == 0 && ci > 0) {
@@ -1305,6 +1304,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         mma_bf16(tmem + kBtX2, sw128_desc(sZO + 8192 + ks * 2048, 16384, 1024),
                  sw128_desc(sP + ks * 2048, 16384, 1024), idmm, ks > 0);
       mma_commit(bar_mma);
+      bulk_wait_read_all();  // the previous chunk's dq / dk staging (X0, X1) has been read
     }
     mma_wait();
     if (!ok) break;
@@ -1503,11 +1503,27 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                  idmm, 1);
       mma_commit(bar_mma);
     }
+    // this thread's Q values for the q . dq sums (bf16 pairs), read while the
+    // products run so that Q can be reloaded as soon as they are done
+    __nv_bfloat162 qv[8];
+    {
+      const unsigned char* qt = sm + kB_KQ + (row >> 6) * 16384 + 8192;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = cg * 16 + 2 * i, cc = row & 63;
+        qv[i].x = *reinterpret_cast<const __nv_bfloat16*>(qt + sw_row_off(r, cc >> 3) + (cc & 7) * 2);
+        qv[i].y = *reinterpret_cast<const __nv_bfloat16*>(qt + sw_row_off(r + 1, cc >> 3) + (cc & 7) * 2);
+      }
+    }
+    fence_async_shared();  // these reads come before the TMA that overwrites Q
     mma_wait();
     if (!ok) break;
     // ---- E6: dG update, dq (+ q.dq), dk, dbeta, dg
-    // K, dO, G_in and T have been read for the last time
-    if (tid == 0 && ci > 0) issue_rest(ci - 1);
+    // K, Q, dO, G_in and T have been read for the last time
+    if (tid == 0 && ci > 0) {
+      issue_rest(ci - 1);
+      issue_q(ci - 1);
+    }
     {
       {
         float g[32];
@@ -1516,11 +1532,11 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       float x[16];
       tmem_ld16(tmem + lb + kBtX2 + cg * 16, x);  // dQ^T row d = row, columns r = 16 cg + i
-      const int half = row >> 6, cc = row & 63;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int r = cg * 16 + i;
-        acc[i] += tile_elem(sm + kB_KQ + half * 16384 + 8192, r, cc) * x[i];
+        const float2 q2 = __bfloat1622float2(qv[i / 2]);
+        acc[i] += ((i & 1) ? q2.y : q2.x) * x[i];
         stage_bf16(sm + kB_X, r, row, x[i]);  // dq (X0 is free once the products are done)
       }
       tmem_ld16(tmem + lb + kBtU + cg * 16, x);  // dK^T row d, columns j
@@ -1538,7 +1554,6 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       tma_store_4d(&tm_dk, sm + kB_X + 16384, 0, h, t0, b);
       tma_store_4d(&tm_dk, sm + kB_X + 24576, 64, h, t0, b);
       bulk_commit_group();
-      if (ci > 0) issue_q(ci - 1);  // Q has been read for the last time
     }
     if (warp == 1 && ci > 0) {
       // gates of the next chunk of the reverse scan (this chunk's are no longer read)

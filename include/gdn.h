@@ -151,9 +151,10 @@ GDN_API int kda_bwd(const gdn_shape* shape, const void* q, const void* k, const 
  * cannot check this, and other inputs give meaningless gradients.  On the
  * tensor-core path the context holds the bf16 entry state of every chunk
  * (32 KB) and its bf16 T = (I + A)^-1 tile (8 KB), plus the forward's
- * segment scratch; the result equals *_bwd's bit for bit when the forward
- * ran without segments.  On the CUDA-core path nothing is kept and
- * *_bwd_saved recomputes.  ctx needs no initialisation.  Errors as for
+ * segment scratch; on the CUDA-core path the fp32 entry state of every chunk
+ * plus the backward's scratch.  The result equals *_bwd's bit for bit except
+ * after a segmented tensor-core forward (few long sequences), whose later
+ * segments' entry states differ by rounding.  ctx needs no initialisation.  Errors as for
  * *_fwd / *_bwd, with GDN_ERR_WORKSPACE when ctx is NULL or smaller than
  * *_ctx_bytes(); *_ctx_bytes() is 0 for an invalid shape or one with no
  * work, and depends on the current device's SM count. */

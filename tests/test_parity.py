@@ -159,7 +159,7 @@ SAVED = [
     # B, T, H, dk, dv, chunk, dtype, kda
     (2, 200, 2, 128, 128, 64, "bf16", False),   # tensor-core path, 8-token tail
     (1, 37, 3, 128, 128, 64, "bf16", False),    # tensor-core path, T < chunk
-    (2, 100, 3, 32, 48, 32, "f32", False),      # CUDA-core path: the context is a workspace
+    (2, 100, 3, 32, 48, 32, "f32", False),      # CUDA-core path: fp32 entry states
     (2, 200, 2, 64, 64, 64, "bf16", True),      # KDA
 ]
 
@@ -168,9 +168,8 @@ SAVED = [
 def test_saved_context_matches_oracle_and_recompute(case):
     """*_fwd_save then *_bwd_saved against the oracle, and bit-equal to the
     recomputing *_fwd / *_bwd.  The context buffer starts out as garbage, so
-    every byte the backward reads must have been written by the forward; on
-    the tensor-core path the backward launches neither the solve nor the
-    states pass."""
+    every byte the backward reads must have been written by the forward; the
+    backward launches neither the solve nor the states pass."""
     B, T, H, dk, dv, chunk, dtype, kda = case
     x = make_inputs(B, T, H, dk, dv, kda=kda, dtype=dtype, h0_std=0.3, with_dht=True, seed=13)
     d = x.to("cuda")
@@ -182,8 +181,10 @@ def test_saved_context_matches_oracle_and_recompute(case):
         gr = bwd_s(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, ctx, d.dht, chunk=chunk)
         torch.cuda.synchronize()
     names = [n for n, _ in t.records()]
-    if gdn.uses_tensor_cores(d.q, d.v, chunk):
+    if gdn.uses_tensor_cores(d.q, d.v, chunk) and not kda:
         assert names == ["tc_bwd"], names
+    else:
+        assert names == ["simt_bwd", "simt_bwd_reduce"], names
     compare(x, o, ht, gr, fp32=dtype == "f32")
     ro, rht, rgr = run_gpu(x, chunk)
     assert torch.equal(o, ro) and torch.equal(ht, rht)
