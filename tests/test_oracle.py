@@ -339,3 +339,43 @@ def test_gdn_gate_gradient_scaling_identity():
     dlogc[:, -1] += (dht * ht).sum((-1, -2))
     want = np.cumsum(dlogc[:, ::-1], axis=1)[:, ::-1]
     np.testing.assert_allclose(gr["dg"], want, rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------- worked examples
+
+def _golden_cases():
+    """Parses tests/golden/worked_examples.txt (hand-derived values)."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                        "worked_examples.txt")
+    cases, cur = {}, None
+    for line in open(path):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        if line.startswith("["):
+            cur = cases.setdefault(line.strip("[]"), {})
+            continue
+        key, val = (x.strip() for x in line.split("=", 1))
+
+        def num(tok):
+            if tok.startswith("ln(") and tok.endswith(")"):
+                return float(np.log(float(Fraction(tok[3:-1]))))
+            return float(Fraction(tok))
+        cur[key] = [[num(t) for t in part.split()] for part in val.split("|")]
+    return cases
+
+
+@pytest.mark.parametrize("name", ["gdn", "kda"])
+def test_hand_worked_examples(name):
+    c = _golden_cases()[name]
+    T = int(c["T"][0][0])
+    kda = name == "kda"
+    tok = lambda key: np.array(c[key], dtype=np.float64).reshape(1, T, 1, -1)
+    g = np.array(c["g"], dtype=np.float64).reshape(1, T, 1, -1)
+    g = g if kda else g.reshape(1, T, 1)
+    beta = np.array(c["beta"], dtype=np.float64).reshape(1, T, 1)
+    h0 = np.array(c["h0"], dtype=np.float64).reshape(1, 1, 2, 2)
+    o, ht = oracle.fwd(tok("q"), tok("k"), tok("v"), g, beta, h0, kda=kda)
+    np.testing.assert_allclose(o.reshape(T, 2), np.array(c["o"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ht.reshape(2, 2), np.array(c["ht"]), rtol=0, atol=1e-12)
+
