@@ -1250,8 +1250,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   for (int ci = p.N - 1; ci >= 0 && ok; --ci) {
     const int t0 = ci * C, n = min(C, p.T - t0);
-    fence_async_shared();
-    cta_sync();
+    fence_async_shared();  // the dG tile written last chunk, for MMA1 (after the barrier below)
     if (tid == 0 && ci > 0) {
       // the next chunk in the reverse scan: start pulling its tiles into L2
       const int tp = t0 - C;
