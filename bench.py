@@ -14,7 +14,9 @@ with fp32 state (the 300M-model pre-training shape).  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   (default K: 1000 GDN steps, about 0.6 s timed, so that the clock samples
-  fall inside the timed region; 5 KDA steps; 20 for the reference arm)
+  fall inside the timed region; 5 KDA steps; 5000 decode steps; 20 for the
+  reference arm)
+  python bench.py --workload gdn_decode   # single-token decode step
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
 
 With N > 1 (launched by torch.distributed.run) every rank runs its own batch
@@ -43,7 +45,9 @@ METRIC = "GDN/KDA mixer fwd+bwd tokens/s on 1 GB300; fraction of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
 WORKLOADS = {"gdn_300m": W.GDN_300M_BF16, "kda_300m": W.KDA_300M_BF16, "gdn_1b": W.GDN_1B_BF16_H0,
-             "gdn_tiny": W.GDN_TINY_FP32}
+             "gdn_tiny": W.GDN_TINY_FP32, "gdn_decode": W.GDN_DECODE_BF16,
+             "kda_decode": W.KDA_DECODE_BF16}
+DECODE_METRIC = "GDN/KDA single-token decode step tokens/s on 1 GB300; fraction of roofline"
 
 
 # ------------------------------------------------------------------ algorithmic work
@@ -95,7 +99,7 @@ def kernel_work(w, kernel):
     return 0.0, 0.0
 
 
-KERNEL_SOURCES = {"tc": "gdn_tc.cu", "simt": "gdn_simt.cu"}
+KERNEL_SOURCES = {"tc": "gdn_tc.cu", "simt": "gdn_simt.cu", "decode": "gdn_decode.cu"}
 
 
 def recorded_traffic(kernel, workload_key):
@@ -498,6 +502,135 @@ def run_e2e(gdn, w, x, ctx, dev, stream, K, warmup, ws):
             "overlap step i (one copy stream per direction)"}
 
 
+# ------------------------------------------------------------------ decode
+
+def decode_bytes(w):
+    """Algorithmic bytes of one decode call per (b, h): the fp32 state read and
+    written once, each token's q, k, v, o and its gate and beta."""
+    e = 2 if w.dtype == "bf16" else 4
+    sg = 4 * w.dk if w.kda else 4
+    return 2 * 4 * w.dk * w.dv + w.T * (e * (2 * w.dk + 2 * w.dv) + sg + 4)
+
+
+def run_decode(args):
+    """One step = one decode call (T tokens for each of B sequences x H heads),
+    the states resident and updated in place.  The states exceed the L2, so no
+    flush is needed between steps."""
+    import gated_delta_rule_bwd_gb300 as gdn
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init(ws, "nccl")
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    dec = gdn.kda_decode if w.kda else gdn.gdn_decode
+    x = w.make(device=dev, seed=rank)
+    state = x.h0.clone()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return dec(x.q, x.k, x.v, x.g, x.beta, state)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        epoch0 = time.time()
+        with gdn.KernelTimer(cap=0) as counter:
+            t0.record(stream)
+            for _ in range(K):
+                step()
+            t1.record(stream)
+        torch.cuda.synchronize(dev)
+        epoch1 = time.time()
+        barrier(ws)
+    dev_s_max = max_over_ranks(t0.elapsed_time(t1) / 1e3, ws, dev)
+    n_ev = min(K, 200)
+    with gdn.KernelTimer(cap=2 * n_ev) as timer:
+        for _ in range(n_ev):
+            step()
+    torch.cuda.synchronize(dev)
+    per = [ms for name, ms in timer.records() if name == "decode"]
+    kern_ms = statistics.mean(per)
+    peaks, peak_src = load_peaks()
+    nbytes = decode_bytes(w) * w.B * w.H
+    roof = {"bound": "hbm", "achieved": nbytes / (kern_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "kernel": "decode", "kernel_ms": kern_ms, "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": nbytes,
+            "kernel_timing": f"CUDA events around each of {n_ev} launches on the launch stream"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    wkey = next((k for k, v in WORKLOADS.items() if v is w), w.name)
+    roof["traffic"] = args.traffic if args.traffic is not None else recorded_traffic("decode", wkey)
+
+    e2e = None
+    if not args.no_e2e:
+        # per step: this step's q, k, v, g, beta in from pinned host memory and
+        # its o out (the states stay on the device, as in serving)
+        names = ["q", "k", "v", "g", "beta"]
+        host = {n: getattr(x, n).cpu().pin_memory() for n in names}
+        o_host = torch.empty((w.B, w.T, w.H, w.dv), dtype=x.q.dtype, pin_memory=True)
+        dbuf = {n: torch.empty_like(getattr(x, n)) for n in names}
+
+        def e2e_step():
+            for n in names:
+                dbuf[n].copy_(host[n], non_blocking=True)
+            o, _ = dec(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], state)
+            o_host.copy_(o, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        es = max_over_ranks(e0.elapsed_time(e1) / 1e3, ws, dev)
+        e2e = {"value": w.B * w.T * K * ws / es, "unit": "tokens/s",
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
+               "d2h_bytes_per_step": o_host.numel() * o_host.element_size()}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        rows = max(1, (os.cpu_count() or 1) // w.H)
+        xs = w.make(device="cpu", seed=0, B=rows)
+        oracle.fwd(xs.q, xs.k, xs.v, xs.g, xs.beta, xs.h0, kda=w.kda)  # warm
+        c0, n = time.perf_counter(), 0
+        while time.perf_counter() - c0 < args.cpu_seconds:
+            oracle.fwd(xs.q, xs.k, xs.v, xs.g, xs.beta, xs.h0, kda=w.kda)
+            n += 1
+        dt = time.perf_counter() - c0
+        cpu = {"value": rows * w.T * n / dt, "unit": "tokens/s", "cores": os.cpu_count() or 1,
+               "kind": "oracle", "sample": f"{n} x ({rows} sequences x {w.H} heads x {w.T} token) "
+               f"of {w.name}, fp64 token recurrence, {dt:.1f} s"}
+
+    if rank == 0:
+        ms_step = dev_s_max * 1e3 / K
+        line = {
+            "metric": DECODE_METRIC, "value": w.B * w.T * K * ws / dev_s_max, "unit": "tokens/s",
+            "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic",
+            "config": {"workload": w.name, "op": ("kda" if w.kda else "gdn") + " decode",
+                       "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                       "tokens_per_step": w.B * w.T, "parallelism": f"replicas x{ws}",
+                       "l2": "not flushed: the states (fp32) exceed the L2",
+                       "state_bytes": w.B * w.H * w.dk * w.dv * 4},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": counter.launches * ws, "clocks": clocks.summary(epoch0, epoch1),
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args):
@@ -549,14 +682,22 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()
+    wl = WORKLOADS[args.workload]
+    decode = wl.T == 1 and wl.fwd_only
     if args.steps is None:
-        ours = 5 if WORKLOADS[args.workload].kda else 1000  # KDA: about 0.17 s a step
+        ours = 5000 if decode else 5 if wl.kda else 1000  # KDA: about 0.17 s a step
         args.steps = 20 if args.impl == "reference" else ours
     if args.warmup is None:
         args.warmup = 3 if args.impl == "reference" or args.steps < 100 else 20
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":
+        if decode:
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the "
+                              "training step; decode has its CPU oracle timing in cpu_baseline"}))
+            return
         run_reference(args)
+    elif decode:
+        run_decode(args)
     else:
         run_ours(args)
 

@@ -42,6 +42,7 @@ _lib = None
 EXPORTS = ("gdn_fwd", "gdn_bwd", "kda_fwd", "kda_bwd", "gdn_fwd_workspace", "kda_fwd_workspace",
            "gdn_bwd_workspace", "kda_bwd_workspace", "gdn_ctx_bytes", "kda_ctx_bytes",
            "gdn_fwd_save", "kda_fwd_save", "gdn_bwd_saved", "kda_bwd_saved",
+           "gdn_decode", "kda_decode",
            "gdn_status_str", "gdn_last_cuda_error", "gdn_device_status", "gdn_uses_tensor_cores",
            "gdn_profile_begin", "gdn_profile_end", "gdn_profile_read", "gdn_kernel_name")
 
@@ -66,6 +67,9 @@ def lib():
                 getattr(L, name).restype = ctypes.c_int
             for name in ("gdn_bwd", "kda_bwd", "gdn_bwd_saved", "kda_bwd_saved"):
                 getattr(L, name).argtypes = [sp] + [vp] * 14 + [vp, sz, vp]
+                getattr(L, name).restype = ctypes.c_int
+            for name in ("gdn_decode", "kda_decode"):
+                getattr(L, name).argtypes = [sp] + [vp] * 8 + [vp]
                 getattr(L, name).restype = ctypes.c_int
             L.gdn_status_str.argtypes = [ctypes.c_int]
             L.gdn_status_str.restype = ctypes.c_char_p
@@ -264,6 +268,32 @@ def gdn_bwd_saved(q, k, v, g, beta, h0, do, ctx, dht=None, chunk=64, want_dh0=Tr
 def kda_bwd_saved(q, k, v, g, beta, h0, do, ctx, dht=None, chunk=64, want_dh0=True):
     """KDA backward reading the context ``kda_fwd_save`` left in ``ctx``."""
     return _bwd(True, q, k, v, g, beta, h0, do, dht, chunk, want_dh0, ctx=ctx)
+
+
+def _decode(kda, q, k, v, g, beta, state=None, inplace=True, chunk=64):
+    B, T, H, dk = q.shape
+    dv = v.shape[3]
+    _validate(q, k, v, g, beta, kda, [("state", (state, (B, H, dk, dv), torch.float32))])
+    o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    ht = state if (inplace and state is not None) else torch.empty(
+        (B, H, dk, dv), dtype=torch.float32, device=q.device)
+    s = make_shape(q, v, chunk)
+    fn = lib().kda_decode if kda else lib().gdn_decode
+    _check(fn(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+              _ptr(o), _ptr(ht), _stream(q.device)))
+    return o, ht
+
+
+def gdn_decode(q, k, v, g, beta, state=None, inplace=True):
+    """GDN forward run token by token (decode; a few tokens per sequence).
+    Returns ``(o, ht)``; with ``inplace`` (and a ``state``) the state tensor is
+    updated in place and returned as ``ht``.  ``state`` None is the zero state."""
+    return _decode(False, q, k, v, g, beta, state, inplace)
+
+
+def kda_decode(q, k, v, g, beta, state=None, inplace=True):
+    """KDA forward run token by token (``g`` is ``[B,T,H,dk]``); see ``gdn_decode``."""
+    return _decode(True, q, k, v, g, beta, state, inplace)
 
 
 def device_status() -> int:

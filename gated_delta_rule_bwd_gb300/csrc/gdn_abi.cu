@@ -127,6 +127,28 @@ int run_bwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
   return e == cudaSuccess ? GDN_OK : fail_cuda(e);
 }
 
+int run_decode(const gdn_shape* shape, bool kda, const void* q, const void* k, const void* v,
+               const float* g, const float* beta, const float* h0, void* o, float* ht,
+               void* stream) {
+  gdn::Problem p;
+  int rc = check_shape(shape, kda, &p);
+  if (rc != GDN_OK) return rc;
+  if (empty(p)) return GDN_OK;
+  if (p.T > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_ARG;
+  const void* ptrs[] = {q, k, v, g, beta, h0, o, ht};
+  for (const void* x : ptrs)
+    if (x && !aligned16(x)) return GDN_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p.T == 0) {
+    if (ht == h0 && ht) return GDN_OK;  // in place: nothing changes
+    cudaError_t e = copy_state_or_zero(ht, h0, p, st);
+    return e == cudaSuccess ? GDN_OK : fail_cuda(e);
+  }
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.o = o; p.ht = ht;
+  cudaError_t e = gdn::decode(p, st);
+  return e == cudaSuccess ? GDN_OK : fail_cuda(e);
+}
+
 size_t query_ws(const gdn_shape* shape, bool kda, bool bwd) {
   gdn::Problem p;
   if (check_shape(shape, kda, &p) != GDN_OK) return 0;
@@ -146,7 +168,7 @@ namespace gdn {
 const char* kernel_name(int id) {
   static const char* names[kNumKernelIds] = {
       "simt_fwd", "simt_states", "simt_bwd", "simt_bwd_reduce",
-      "tc_fwd", "tc_states", "tc_bwd", "tc_solve", "tc_fwd_segment", "tc_combine"};
+      "tc_fwd", "tc_states", "tc_bwd", "tc_solve", "tc_fwd_segment", "tc_combine", "decode"};
   return (id >= 0 && id < kNumKernelIds) ? names[id] : "unknown";
 }
 
@@ -268,6 +290,18 @@ int kda_bwd_saved(const gdn_shape* shape, const void* q, const void* k, const vo
                   float* dh0, void* ctx, size_t ctx_bytes, void* stream) {
   return run_bwd(shape, true, q, k, v, g, beta, h0, do_, dht, dq, dk, dv, dg, dbeta, dh0, ctx,
                  ctx_bytes, stream, true);
+}
+
+int gdn_decode(const gdn_shape* shape, const void* q, const void* k, const void* v,
+               const float* g, const float* beta, const float* h0, void* o, float* ht,
+               void* stream) {
+  return run_decode(shape, false, q, k, v, g, beta, h0, o, ht, stream);
+}
+
+int kda_decode(const gdn_shape* shape, const void* q, const void* k, const void* v,
+               const float* g, const float* beta, const float* h0, void* o, float* ht,
+               void* stream) {
+  return run_decode(shape, true, q, k, v, g, beta, h0, o, ht, stream);
 }
 
 const char* gdn_status_str(int status) {

@@ -41,6 +41,9 @@ size_t tc_ctx_bytes(const Problem& p);
 cudaError_t tc_fwd(const Problem& p, cudaStream_t s, bool save);
 cudaError_t tc_bwd(const Problem& p, cudaStream_t s, bool saved);
 
+// Token-recurrent forward for a few tokens per sequence (any dk, dv <= 128).
+cudaError_t decode(const Problem& p, cudaStream_t s);
+
 // Kernel ids reported by the timing hook (gdn_profile_*).
 enum KernelId {
   kSimtFwd = 0,
@@ -53,7 +56,8 @@ enum KernelId {
   kTcSolve = 7,
   kTcSegment = 8,
   kTcCombine = 9,
-  kNumKernelIds = 10
+  kDecode = 10,
+  kNumKernelIds = 11
 };
 const char* kernel_name(int id);
 

@@ -49,5 +49,14 @@ GDN_1B_BF16_H0 = Workload("gdn_1b_bf16_h0_B8_T2048_H16_d128_C64", 8, 2048, 16, 1
 GDN_1M_FWD_BF16 = Workload("gdn_1m_fwd_bf16_B1_T1048576_H16_d128_C64", 1, 1 << 20, 16, 128,
                            128, 64, g_mean=4.0, fwd_only=True)
 
-ALL = [GDN_TINY_FP32, GDN_300M_BF16, KDA_300M_BF16, GDN_1B_BF16_H0, GDN_1M_FWD_BF16]
+# Single-token decode on the same state layout: a serving batch of 256
+# sequences x 16 heads (the SFT guide's model has 16 heads), one token each;
+# the states (268 MB fp32) exceed the L2.
+GDN_DECODE_BF16 = Workload("gdn_decode_bf16_B256_T1_H16_d128", 256, 1, 16, 128, 128, 64,
+                           h0_std=0.02, fwd_only=True)
+KDA_DECODE_BF16 = Workload("kda_decode_bf16_B256_T1_H16_d128", 256, 1, 16, 128, 128, 64,
+                           kda=True, h0_std=0.02, fwd_only=True)
+
+ALL = [GDN_TINY_FP32, GDN_300M_BF16, KDA_300M_BF16, GDN_1B_BF16_H0, GDN_1M_FWD_BF16,
+       GDN_DECODE_BF16, KDA_DECODE_BF16]
 BY_NAME = {w.name: w for w in ALL}

@@ -179,6 +179,23 @@ GDN_API int kda_bwd_saved(const gdn_shape* shape, const void* q, const void* k, 
                           const float* dht, void* dq, void* dk, void* dv, float* dg,
                           float* dbeta, float* dh0, void* ctx, size_t ctx_bytes, void* stream);
 
+/* Decode: the forward recurrence run token by token, for a few tokens per
+ * sequence (T = 1 in single-token generation).  Same arguments, layout and
+ * results as *_fwd (o and the final state), with no workspace: each (b, h)
+ * state is read once from h0 and written once to ht, and kept in registers
+ * in between.  ht may equal h0 (the state is updated in place); h0 NULL is the
+ * zero state; ht NULL skips the final state.  shape->chunk is not used but
+ * must be a valid value.  Any dk, dv <= 128 and either dtype.  Its cost is
+ * the state traffic, 2 x 4 dk dv bytes per (b, h) per call, plus the tokens'
+ * own bytes; for long sequences *_fwd is the right call.  Errors as for
+ * *_fwd (there is no GDN_ERR_WORKSPACE). */
+GDN_API int gdn_decode(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, const float* h0, void* o, float* ht,
+                       void* stream);
+GDN_API int kda_decode(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, const float* h0, void* o, float* ht,
+                       void* stream);
+
 /* Human-readable name of a gdn_status value. */
 GDN_API const char* gdn_status_str(int status);
 

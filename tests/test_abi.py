@@ -155,6 +155,26 @@ def test_saved_context_size_and_check(L):
     assert L.kda_bwd_saved(ctypes.byref(shape(H=0)), *bwd_args[1:], None, 0, None) == GDN_OK
 
 
+def test_decode_validation(L):
+    def dec(s, kda=False, **over):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, h0=None, o=FAKE, ht=None)
+        a.update(over)
+        fn = L.kda_decode if kda else L.gdn_decode
+        return fn(ctypes.byref(s), a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], a["o"],
+                  a["ht"], None)
+    assert dec(shape(chunk=17)) == GDN_ERR_SHAPE
+    assert dec(shape(dk=129)) == GDN_ERR_SHAPE
+    assert dec(shape(dtype=5)) == GDN_ERR_DTYPE
+    assert dec(shape(), q=None) == GDN_ERR_ARG
+    assert dec(shape(), kda=True, beta=None) == GDN_ERR_ARG
+    assert dec(shape(), o=ctypes.c_void_p(0x10004)) == GDN_ERR_ALIGN
+    assert dec(shape(), ht=ctypes.c_void_p(0x10008)) == GDN_ERR_ALIGN
+    assert dec(shape(B=0)) == GDN_OK
+    # no tokens, state updated in place: nothing to do (nothing is launched)
+    assert dec(shape(T=0), q=None, k=None, v=None, g=None, beta=None, o=None, h0=FAKE,
+               ht=FAKE) == GDN_OK
+
+
 def test_empty_batch_is_a_no_op(L):
     assert call_fwd(L, shape(B=0)) == GDN_OK
     assert call_fwd(L, shape(H=0), q=None) == GDN_OK

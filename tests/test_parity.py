@@ -261,6 +261,54 @@ def test_saved_context_step_replays_in_a_cuda_graph():
             assert torch.equal(a, b)
 
 
+# ----------------------------------------------------------- decode
+
+DECODE = [
+    # B, T, H, dk, dv, dtype, kda
+    (3, 1, 2, 128, 128, "bf16", False),   # single-token step, full head dims
+    (3, 1, 2, 128, 128, "bf16", True),
+    (2, 3, 3, 40, 24, "f32", False),      # a few tokens, odd sizes (a partial column slice)
+    (2, 3, 3, 40, 24, "f32", True),
+    (1, 5, 2, 128, 96, "f32", False),
+]
+
+
+@pytest.mark.parametrize("case", DECODE, ids=lambda c: "x".join(map(str, c)))
+def test_decode_matches_oracle(case):
+    """Token-by-token decode against the oracle's forward (outputs and final
+    state), updating the state in place and into a new tensor."""
+    B, T, H, dk, dv, dtype, kda = case
+    x = make_inputs(B, T, H, dk, dv, kda=kda, dtype=dtype, h0_std=0.3, seed=17)
+    d = x.to("cuda")
+    dec = gdn.kda_decode if kda else gdn.gdn_decode
+    o1, ht1 = dec(d.q, d.k, d.v, d.g, d.beta, d.h0, inplace=False)
+    st = d.h0.clone()
+    o2, ht2 = dec(d.q, d.k, d.v, d.g, d.beta, st, inplace=True)
+    torch.cuda.synchronize()
+    assert ht2.data_ptr() == st.data_ptr()
+    assert torch.equal(o1, o2) and torch.equal(ht1, ht2)
+    compare(x, o1, ht1, None, fp32=dtype == "f32")
+
+
+def test_decode_steps_chain_like_one_call():
+    """Three single-token calls on an in-place state equal one three-token
+    call, and both match the chunkwise tensor-core forward."""
+    x = make_inputs(2, 3, 4, 128, 128, dtype="bf16", h0_std=0.2, seed=18)
+    d = x.to("cuda")
+    st = d.h0.clone()
+    outs = []
+    for t in range(3):
+        sl = lambda u: u[:, t:t + 1].contiguous()
+        o, _ = gdn.gdn_decode(sl(d.q), sl(d.k), sl(d.v), sl(d.g), sl(d.beta), st)
+        outs.append(o)
+    o3, h3 = gdn.gdn_decode(d.q, d.k, d.v, d.g, d.beta, d.h0, inplace=False)
+    of, hf = gdn.gdn_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(outs, 1), o3) and torch.equal(st, h3)
+    assert rel_l2(o3.float().cpu(), of.float().cpu()) < BF16_REL
+    assert rel_l2(h3.cpu(), hf.cpu()) < BF16_REL
+
+
 # ----------------------------------------------------------- invariants on the GPU
 
 def test_kda_with_broadcast_gate_equals_gdn():
