@@ -40,7 +40,9 @@
  * *_fwd_workspace() / *_bwd_workspace() bytes (0 for some shapes, where
  * NULL/0 may be passed).  The workspace holds per-chunk intermediates of one
  * call; its contents need no initialisation and are not meaningful
- * afterwards, and two calls in flight at once need separate workspaces.  All
+ * afterwards, and two calls in flight at once need separate workspaces (the
+ * saved-context pair below passes its buffer from the forward call to the
+ * backward one instead; decode needs no workspace).  All
  * work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  * stream); the calls do not synchronise.  Outputs are overwritten, never
  * accumulated.  Results are deterministic (no atomics).
