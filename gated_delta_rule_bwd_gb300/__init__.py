@@ -7,7 +7,10 @@ pointers and the current CUDA stream to the library.  Every step of the
 computation runs in the library's CUDA kernels; there is no other path.  If
 the library has not been built, every call raises.
 
-Names follow the ABI: ``gdn_fwd``, ``gdn_bwd``, ``kda_fwd``, ``kda_bwd``.
+Names follow the ABI: ``gdn_fwd``, ``gdn_bwd``, ``kda_fwd``, ``kda_bwd``; the
+training pair with a saved context ``gdn_fwd_save`` / ``gdn_bwd_saved`` (and
+the KDA pair), whose forward keeps what the backward would recompute; and the
+token-recurrent ``gdn_decode`` / ``kda_decode`` for a few tokens per sequence.
 Token tensors are ``[B, T, H, D]`` (fp32 or bf16, all the same dtype), ``g``
 is ``[B, T, H]`` (GDN) or ``[B, T, H, dk]`` (KDA) fp32, ``beta`` ``[B, T, H]``
 fp32, states ``[B, H, dk, dv]`` fp32.
