@@ -165,3 +165,78 @@ def backward(q, k, v, g, beta, h0, do, dht, chunk, kda=False):
                 out["dbeta"][b, sl, h] = db
             out["dh0"][b, h] = dS
     return out
+
+
+# ---------------------------------------------------------------- factored operands
+#
+# The same chunk forward written the way a tensor-core kernel forms it: every
+# decay folded into element-scaled operand tiles, so that each intra-chunk
+# product is one plain matrix product.  Around a per-key-dimension reference
+# lam_d (the midpoint of the chunk's gamma range in that dimension),
+#     exp(gamma_rd - gamma_jd) = exp(gamma_rd - lam_d) * exp(lam_d - gamma_jd),
+# each factor at most exp(half the range); the form is usable while that stays
+# below the fp32 / bf16 exponent range (FACTOR_LIMIT).
+
+FACTOR_LIMIT = 80.0
+
+
+def bf16_round(x):
+    """Round to the nearest bfloat16 (ties to even), returned as float64."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    u = a.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def chunk_forward_factored(Q, K, V, g, beta, H_in, kda, operand=None):
+    """One chunk's forward from element-scaled operands; returns (O, H_out, ok).
+
+    ``operand`` (e.g. ``bf16_round``) is applied to every matrix that enters a
+    product as an operand -- the scaled K and Q tiles, T, the bf16 copy of the
+    state and U -- while sums stay fp64, as tensor cores accumulate in fp32.
+    ``ok`` is False when a dimension's gamma range exceeds 2 * FACTOR_LIMIT
+    (the kernel then needs its exact per-element path)."""
+    rnd = operand if operand is not None else (lambda x: x)
+    dk = K.shape[1]
+    n = K.shape[0]
+    gam = np.cumsum(g, axis=0)
+    if not kda:
+        gam = np.repeat(gam[:, None], dk, axis=1)
+    lam = 0.5 * (gam.max(axis=0) + gam.min(axis=0))
+    ok = bool(np.all(gam.max(axis=0) - gam.min(axis=0) <= 2 * FACTOR_LIMIT))
+    Kp = rnd(K * np.exp(gam - lam))
+    Km = rnd(K * np.exp(lam - gam))
+    Qp = rnd(Q * np.exp(gam - lam))
+    KE = rnd(K * np.exp(gam))
+    QE = rnd(Q * np.exp(gam))
+    KF = rnd(K * np.exp(gam[-1][None, :] - gam))
+    A = np.tril(beta[:, None] * (Kp @ Km.T), -1)
+    P = np.tril(Qp @ Km.T)
+    T = rnd(np.linalg.inv(np.eye(n) + A))
+    G = rnd(H_in)                                   # the state as an operand
+    U = T @ (beta[:, None] * (rnd(V) - KE @ G))
+    Ur = rnd(U)
+    O = QE @ G + rnd(P) @ Ur
+    H_out = np.exp(gam[-1])[:, None] * H_in + KF.T @ Ur
+    return O, H_out, ok
+
+
+def forward_factored(q, k, v, g, beta, h0, chunk, kda=False, operand=None):
+    """Chunked forward through ``chunk_forward_factored``; returns (o, ht, ok)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[3]
+    o = np.zeros((B, T, H, dv))
+    ht = np.zeros((B, H, dk, dv))
+    ok = True
+    for b in range(B):
+        for h in range(H):
+            S = np.zeros((dk, dv)) if h0 is None else h0[b, h].astype(np.float64)
+            for c0 in range(0, T, chunk):
+                c1 = min(T, c0 + chunk)
+                o[b, c0:c1, h], S, fine = chunk_forward_factored(
+                    q[b, c0:c1, h], k[b, c0:c1, h], v[b, c0:c1, h], g[b, c0:c1, h],
+                    beta[b, c0:c1, h], S, kda, operand)
+                ok = ok and fine
+            ht[b, h] = S
+    return o, ht, ok
+
