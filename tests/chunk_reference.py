@@ -240,3 +240,112 @@ def forward_factored(q, k, v, g, beta, h0, chunk, kda=False, operand=None):
             ht[b, h] = S
     return o, ht, ok
 
+
+def chunk_backward_factored(Q, K, V, g, beta, H_in, dO, dH_out, kda, operand=None,
+                            scaled_operand=None):
+    """``chunk_backward`` from element-scaled operands; returns
+    (dQ, dK, dV, dg, dbeta, dH_in).  Each decayed sum over a row or column of
+    a chunk matrix is one product with a scaled tile and a row scaling:
+        sum_j M[r,j] K[j,d] Gam[r,j,d] = exp(gamma_rd - lam_d) (M Km)[r,d]
+        sum_r M[r,j] X[r,d] Gam[r,j,d] = exp(lam_d - gamma_jd) (M^T Xp)[j,d]
+    with Km = K exp(lam - gamma), Xp = X exp(gamma - lam).  ``operand`` rounds
+    every product operand, as in ``chunk_forward_factored``; ``scaled_operand``,
+    if given, rounds the three scaled tiles Kp, Km, Qp instead."""
+    rnd = operand if operand is not None else (lambda x: x)
+    srnd = scaled_operand if scaled_operand is not None else rnd
+    dk = K.shape[1]
+    n = K.shape[0]
+    gam = np.cumsum(g, axis=0)
+    if not kda:
+        gam = np.repeat(gam[:, None], dk, axis=1)
+    lam = 0.5 * (gam.max(axis=0) + gam.min(axis=0))
+    Ep, Em = np.exp(gam - lam), np.exp(lam - gam)
+    E, eC, F = np.exp(gam), np.exp(gam[-1]), np.exp(gam[-1][None, :] - gam)
+    mask = np.tril(np.ones((n, n), dtype=bool))
+    Kp, Km, Qp = srnd(K * Ep), srnd(K * Em), srnd(Q * Ep)
+    KE, QE, KF = rnd(K * E), rnd(Q * E), rnd(K * F)
+    KKs = np.tril(Kp @ Km.T, -1)                    # strictly lower decayed K K^T
+    L = np.eye(n) + beta[:, None] * KKs
+    T = rnd(np.linalg.inv(L))
+    G = rnd(H_in)
+    R = V - KE @ G
+    U = T @ (beta[:, None] * rnd(R))
+    Ur = rnd(U)
+    P = np.tril(Qp @ Km.T)
+    dOr, dHr = rnd(dO), rnd(dH_out)
+
+    dgam = np.zeros((n, dk))
+    dH_in = eC[:, None] * dH_out
+    dgam[-1] += eC * np.sum(dH_out * H_in, axis=1)
+    UdH = U @ dH_out.T
+    dK = F * UdH
+    dF = K * UdH
+    dgam[-1] += np.sum(dF * F, axis=0)
+    dgam -= dF * F
+    dU = KF @ dHr + rnd(P).T @ dOr
+    dQE = dOr @ G.T
+    dQ = E * dQE
+    dgam += Q * E * dQE
+    dH_in += QE.T @ dOr
+    dP = rnd((dOr @ Ur.T) * mask)
+    dQP = Ep * (dP @ Km)
+    dKP = Em * (dP.T @ Qp)
+    dQ += dQP
+    dK += dKP
+    dgam += Q * dQP - K * dKP
+    dZ = T.T @ dU
+    dA = np.tril(-rnd(dZ) @ Ur.T, -1)
+    dbeta = np.sum(dZ * R, axis=1) + np.sum(dA * KKs, axis=1)
+    dR = beta[:, None] * dZ
+    dRr = rnd(dR)
+    dV = dR
+    dKE = -dRr @ G.T
+    dK += E * dKE
+    dgam += K * E * dKE
+    dH_in -= KE.T @ dRr
+    dAt = rnd(dA * beta[:, None])
+    X = Ep * (dAt @ Km)
+    Y = Em * (dAt.T @ Kp)
+    dK += X + Y
+    dgam += K * X - K * Y
+    dg = np.cumsum(dgam[::-1], axis=0)[::-1]
+    if not kda:
+        dg = dg.sum(axis=1)
+    return dQ, dK, dV, dg, dbeta, dH_in
+
+
+def backward_factored(q, k, v, g, beta, h0, do, dht, chunk, kda=False, operand=None,
+                      scaled_operand=None):
+    """``backward`` through the factored chunk forms (entry states from the
+    factored forward at the same operand precision)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[3]
+    out = {n: np.zeros(x.shape) for n, x in (("dq", q), ("dk", k), ("dv", v), ("dg", g),
+                                               ("dbeta", beta))}
+    out["dh0"] = np.zeros((B, H, dk, dv))
+    for b in range(B):
+        for h in range(H):
+            S = np.zeros((dk, dv)) if h0 is None else h0[b, h].astype(np.float64)
+            starts = list(range(0, T, chunk))
+            states = []
+            for c0 in starts:
+                c1 = min(T, c0 + chunk)
+                states.append(S)
+                _, S, _ = chunk_forward_factored(q[b, c0:c1, h], k[b, c0:c1, h], v[b, c0:c1, h],
+                                                 g[b, c0:c1, h], beta[b, c0:c1, h], S, kda,
+                                                 operand)
+            dS = np.zeros((dk, dv)) if dht is None else dht[b, h].astype(np.float64)
+            for ci in reversed(range(len(starts))):
+                c0 = starts[ci]
+                sl = slice(c0, min(T, c0 + chunk))
+                dQ, dK, dV, dg, db, dS = chunk_backward_factored(
+                    q[b, sl, h], k[b, sl, h], v[b, sl, h], g[b, sl, h], beta[b, sl, h],
+                    states[ci], do[b, sl, h], dS, kda, operand, scaled_operand)
+                out["dq"][b, sl, h] = dQ
+                out["dk"][b, sl, h] = dK
+                out["dv"][b, sl, h] = dV
+                out["dg"][b, sl, h] = dg
+                out["dbeta"][b, sl, h] = db
+            out["dh0"][b, h] = dS
+    return out
+
