@@ -17,6 +17,7 @@ with fp32 state (the 300M-model pre-training shape).  Prints one JSON line.
   fall inside the timed region; 5 KDA steps; 5000 decode steps; 20 for the
   reference arm)
   python bench.py --workload gdn_decode   # single-token decode step
+  python bench.py --workload gdn_1m       # 1M-token forward
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
 
 With N > 1 (launched by torch.distributed.run) every rank runs its own batch
@@ -46,7 +47,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129 * 1024 * 1024
 WORKLOADS = {"gdn_300m": W.GDN_300M_BF16, "kda_300m": W.KDA_300M_BF16, "gdn_1b": W.GDN_1B_BF16_H0,
              "gdn_tiny": W.GDN_TINY_FP32, "gdn_decode": W.GDN_DECODE_BF16,
-             "kda_decode": W.KDA_DECODE_BF16}
+             "kda_decode": W.KDA_DECODE_BF16, "gdn_1m": W.GDN_1M_FWD_BF16}
+FWD_METRIC = "GDN long-context forward tokens/s on 1 GB300; fraction of roofline"
 DECODE_METRIC = "GDN/KDA single-token decode step tokens/s on 1 GB300; fraction of roofline"
 
 
@@ -631,6 +633,104 @@ def run_decode(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ forward only
+
+def run_forward(args):
+    """One step = one forward call over the whole workload (the 1M-token
+    context: the tensor-core forward runs each sequence in segments).  The
+    inputs (12 GB of bf16 q, k, v) exceed the L2, so no flush is needed."""
+    import gated_delta_rule_bwd_gb300 as gdn
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init(ws, "nccl")
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    fwd = gdn.kda_fwd if w.kda else gdn.gdn_fwd
+    x = w.make(device=dev, seed=rank)
+    wsb = torch.empty(max(16, gdn.fwd_workspace_bytes(x.q, x.v, w.chunk, w.kda)),
+                      dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return fwd(x.q, x.k, x.v, x.g, x.beta, x.h0, chunk=w.chunk, workspace=wsb)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        epoch0 = time.time()
+        with gdn.KernelTimer(cap=0) as counter:
+            t0.record(stream)
+            for _ in range(K):
+                step()
+            t1.record(stream)
+        torch.cuda.synchronize(dev)
+        epoch1 = time.time()
+        barrier(ws)
+    dev_s_max = max_over_ranks(t0.elapsed_time(t1) / 1e3, ws, dev)
+    n_ev = min(K, 5)
+    with gdn.KernelTimer(cap=16 * n_ev) as timer:
+        for _ in range(n_ev):
+            step()
+    torch.cuda.synchronize(dev)
+    per = {}
+    for name, ms in timer.records():
+        per.setdefault(name, []).append(ms)
+    totals = {k: sum(v) for k, v in per.items()}
+    dom = max(totals, key=totals.get)
+    peaks, peak_src = load_peaks()
+    a = algorithmic(w)
+    th = w.B * w.T * w.H
+    nbytes = a["fwd_bytes"] * th + state_bytes(w, "tc_fwd") * w.B * w.H
+    ms_step = dev_s_max * 1e3 / K
+    # the op's algorithmic bytes against the whole call (solve, segment passes,
+    # combine and output pass together)
+    roof = {"bound": "hbm", "achieved": nbytes / (ms_step * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "kernel": "whole forward call", "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": nbytes, "traffic": None,
+            "per_kernel_ms_per_call": {k: v / n_ev for k, v in totals.items()},
+            "dominant_kernel": dom,
+            "kernel_timing": f"CUDA events around each library kernel over {n_ev} calls"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        Ts = 1 << 14  # a bounded sample: every head, the first 16384 tokens
+        xs = w.make(device="cpu", seed=0, T=Ts)
+        c0, n = time.perf_counter(), 0
+        while n == 0 or time.perf_counter() - c0 < args.cpu_seconds:
+            oracle.fwd(xs.q, xs.k, xs.v, xs.g, xs.beta, xs.h0, kda=w.kda)
+            n += 1
+        dt = time.perf_counter() - c0
+        cpu = {"value": w.B * Ts * n / dt, "unit": "tokens/s", "cores": os.cpu_count() or 1,
+               "kind": "oracle", "sample": f"{n} x ({w.B} x {Ts} tokens x {w.H} heads) of "
+               f"{w.name}, fp64 token recurrence, forward, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": FWD_METRIC, "value": w.B * w.T * K * ws / dev_s_max, "unit": "tokens/s",
+            "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic",
+            "config": {"workload": w.name, "op": ("kda" if w.kda else "gdn") + " fwd",
+                       "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
+                       "tokens_per_step": w.B * w.T, "parallelism": f"replicas x{ws}",
+                       "l2": "not flushed: the inputs exceed the L2"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": None,
+            "gpu_launches": counter.launches * ws, "clocks": clocks.summary(epoch0, epoch1),
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args):
@@ -684,20 +784,25 @@ def main():
     args = ap.parse_args()
     wl = WORKLOADS[args.workload]
     decode = wl.T == 1 and wl.fwd_only
+    fwd_only = wl.fwd_only and not decode
     if args.steps is None:
-        ours = 5000 if decode else 5 if wl.kda else 1000  # KDA: about 0.17 s a step
+        # KDA: about 0.17 s a step; the 1M-token forward about 18 ms
+        ours = 5000 if decode else 40 if fwd_only else 5 if wl.kda else 1000
         args.steps = 20 if args.impl == "reference" else ours
     if args.warmup is None:
         args.warmup = 3 if args.impl == "reference" or args.steps < 100 else 20
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":
-        if decode:
+        if decode or fwd_only:
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the "
-                              "training step; decode has its CPU oracle timing in cpu_baseline"}))
+                              "training step; this workload has its CPU oracle timing in "
+                              "cpu_baseline"}))
             return
         run_reference(args)
     elif decode:
         run_decode(args)
+    elif fwd_only:
+        run_forward(args)
     else:
         run_ours(args)
 

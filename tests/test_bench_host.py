@@ -96,7 +96,9 @@ def test_default_step_counts(monkeypatch):
     monkeypatch.setattr(bench, "run_ours", lambda a: seen.setdefault("ours", (a.steps, a.warmup)))
     monkeypatch.setattr(bench, "run_decode", lambda a: seen.setdefault("dec", (a.steps, a.warmup)))
     monkeypatch.setattr(bench, "run_reference", lambda a: seen.setdefault("ref", (a.steps, a.warmup)))
+    monkeypatch.setattr(bench, "run_forward", lambda a: seen.setdefault("fwd", (a.steps, a.warmup)))
     for argv in (["bench.py"], ["bench.py", "--workload", "gdn_decode"],
+                 ["bench.py", "--workload", "gdn_1m"],
                  ["bench.py", "--impl", "reference"], ["bench.py", "--steps", "7", "--warmup", "1"]):
         monkeypatch.setattr("sys.argv", argv)
         seen.clear()
@@ -106,6 +108,8 @@ def test_default_step_counts(monkeypatch):
             assert key == "ours" and steps == 1000 and warmup >= 3
         elif "gdn_decode" in argv:
             assert key == "dec" and steps == 5000
+        elif "gdn_1m" in argv:
+            assert key == "fwd" and steps == 40 and warmup == 3
         elif "reference" in argv:
             assert key == "ref" and steps == 20
         else:
