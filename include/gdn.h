@@ -119,7 +119,12 @@ GDN_API int gdn_fwd(const gdn_shape* shape, const void* q, const void* k, const 
             void* ws, size_t ws_bytes, void* stream);
 
 /* GDN backward: gradients with respect to every forward input.  dht may be
- * NULL (zero gradient of the final state); dh0 may be NULL (not wanted). */
+ * NULL (zero gradient of the final state); dh0 may be NULL (not wanted).
+ * Precision of dg on the tensor-core path (bf16): measured rel-L2 against an
+ * fp64 reference is within 2e-2 for gates g = logsigmoid(N(2, 1)) (about
+ * -0.13 a token), but grows when the gates decay fast: 2.6e-2, 6.3e-2 and
+ * 0.37 for logsigmoid(N(mu, 1)) with mu = 0, -1, -3.  The other gradients and
+ * the CUDA-core path are not affected. */
 GDN_API int gdn_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
             const float* g, const float* beta, const float* h0, const void* do_,
             const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
