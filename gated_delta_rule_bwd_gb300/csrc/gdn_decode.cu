@@ -13,9 +13,9 @@
 // per call, and each token adds only its q, k, v, o, g and beta.  The token's
 // k, its decay a = exp(g) per key row and the products a k, a q go through a
 // per-warp shared-memory slice that every lane reads by broadcast:
-// P^T k = H^T (a k), P^T q = H^T (a q), and H <- diag(a) H + k u^T.  This path is bound by the state traffic
-// (2 x 4 dk dv bytes per (b, h) per call); long sequences belong to the
-// chunkwise kernels.
+// P^T k = H^T (a k), P^T q = H^T (a q), and H <- diag(a) H + k u^T.  This
+// path is bound by the state traffic (2 x 4 dk dv bytes per (b, h) per call);
+// long sequences belong to the chunkwise kernels.
 
 #include "gdn_internal.cuh"
 
