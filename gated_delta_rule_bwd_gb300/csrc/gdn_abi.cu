@@ -165,6 +165,8 @@ size_t query_ctx(const gdn_shape* shape, bool kda) {
 
 namespace gdn {
 
+int record_cuda_error(cudaError_t e) { return fail_cuda(e); }
+
 const char* kernel_name(int id) {
   static const char* names[kNumKernelIds] = {
       "simt_fwd", "simt_states", "simt_bwd", "simt_bwd_reduce",

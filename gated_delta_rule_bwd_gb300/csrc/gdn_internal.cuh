@@ -69,4 +69,8 @@ void prof_after(cudaStream_t s, int kernel_id);
 // Per-device status word written by bounded device-side waits.
 cudaError_t read_and_clear_device_status(int* status);
 
+// Records e as the calling thread's last CUDA error (what gdn_last_cuda_error
+// returns) and returns GDN_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
+
 }  // namespace gdn

@@ -20,12 +20,15 @@
 // it, so nothing needs clearing between calls.
 //
 // Set-up: the first call on each device looks up the array's device address
-// with cudaGetSymbolAddress (which can load the module on that device).  Make
-// that first call before capturing any stream into a CUDA graph.
+// with cudaGetSymbolAddress (which can load the module on that device) and
+// keeps it for the life of the process.  Make that first call before
+// capturing any stream into a CUDA graph.  A cudaDeviceReset after it would
+// leave the kept address stale, so it is not supported.
 
 #include <mutex>
 
 #include "gdn.h"
+#include "gdn_internal.cuh"
 
 namespace {
 
@@ -69,7 +72,8 @@ extern "C" GDN_API int gdn_bwd_noalloc(const gdn_shape* shape, const void* q, co
   const size_t need = gdn_bwd_workspace(shape);
   if (need > kScratchBytes) return GDN_ERR_WORKSPACE;
   void* scratch = nullptr;
-  if (scratch_address(&scratch) != cudaSuccess) return GDN_ERR_CUDA;  // set-up failed
+  const cudaError_t e = scratch_address(&scratch);
+  if (e != cudaSuccess) return gdn::record_cuda_error(e);  // set-up failed
   return gdn_bwd(shape, q, k, v, g, beta, h0, do_, dht, dq, dk, dv, dg, dbeta, dh0, scratch,
                  kScratchBytes, stream);
 }

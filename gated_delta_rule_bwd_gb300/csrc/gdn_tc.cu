@@ -1016,18 +1016,28 @@ gdn_tc_solve_kernel(const __grid_constant__ CUtensorMap tm_k, SolveParams p) {
 //   MMA   U^T = (R^T diag beta) T^T,  dZ^T = dU^T T     (dZ = (I+A)^-T dU)
 //   MMA   [dZ; dO] U^T             -> dA = -strict_lower(dZ U^T), dP = dO U^T
 //   MMA   dG_in = eC dG + (e dO)^T Q - (e dR)^T K       (dR = diag(beta) dZ)
-//   MMA   dQ^T = G_in^T (e dO)^T + K^T (dP o Gam)^T
+//   MMA   dQ^T = G_in^T (e dO)^T + K^T (dP o Gam)^T      (two accumulators)
 //   MMA   dK^T = dG^T (U diag f)^T - G_in^T (e dR)^T + Q^T (dP o Gam)
 //               + K^T (M + M^T),  M = diag(beta) dA o Gam
 //
 // dv = dR; dbeta_r = sum_c dZ_rc R_rc + sum_j dA_rj (K K^T o Gam)_rj.  dq, dk
-// and dv are staged in shared memory and leave by TMA tensor stores.  The
-// log-gate gradient uses the scaling identity of the scalar gate inside each
-// chunk: dg_t = sum_{s >= t in the chunk} (q_s . dq_s - v_s . dv_s) +
-// <dH_out, H_out>, with <dH_out, H_out> taken from the chunk's own state
-// update H_out = eC H_in + K^T diag(f) U as eC <dH_out, H_in> +
-// sum (U diag f)^T o (dG K^T).  Keeping the sum inside the chunk avoids
-// accumulating the rounding of thousands of terms.
+// and dv are staged in shared memory and leave by TMA tensor stores.
+//
+// Log-gate gradient.  dgamma_r (the gradient of the chunk's cumulative log
+// gate at row r) is the sum of the gate's appearances in the chunk, each
+// taken from a full-precision chunk matrix the scan already holds:
+//   e_r dO_r . (Q H_in)_r         q_r . (first accumulator of dQ)_r
+//   + rowsum - colsum of Z = dP o P and of dA o A (A = beta K K^T o Gam)
+//   - e_r dR_r . (K H_in)_r       K H_in from the -G_in K^T product
+//   - s_r,  s_j = f_j u_j . (dG K^T)_j,
+// and dg_t = sum_{s >= t in the chunk} dgamma_s + <dH_out, H_out>, the last
+// term (from the chunk's own state update H_out = eC H_in + K^T diag(f) U) being
+// eC <dH_out, H_in> + sum_j s_j.  The scalar gate's rescaling identity
+// dgamma = q . dq - v . dv gives the same value but as a difference of two
+// large, nearly equal sums once gates decay fast, where the bf16 rounding of
+// dq and dv no longer cancels; the terms above carry no such cancellation.
+// Keeping the sum inside the chunk avoids accumulating the rounding of
+// thousands of terms.
 
 constexpr int BT = 512;                  // backward threads (as the forward)
 constexpr int kB_KQ = 0;                 // [Kh0 | Qh0 | Kh1 | Qh1]
@@ -1039,7 +1049,9 @@ constexpr int kB_T = kB_V + 16384;       // T [r][j]; after the dZ product: M = 
 constexpr int kB_P = kB_T + 8192;        // P [r][j]; after dO^T P: dP o Gam
 constexpr int kB_X = kB_P + 8192;        // three 16 KB slots, reused by phase
 constexpr int kB_GATE = kB_X + 3 * 16384;  // gam, e, f, beta, er, ie, db1, db2, dlc [64] each, eC, fast
-constexpr int kB_RED = kB_GATE + 9 * 256 + 16;  // reduction scratch [16][64] floats
+constexpr int kB_RED = kB_GATE + 9 * 256 + 16;  // reduction scratch, 1024 floats:
+constexpr int kRedZ = 512;    //   [512, 768): rowsum(Z) partials [cg][r]
+constexpr int kRedRow = 768;  //   [768, 832): the chunk's row-sum terms of dgamma
 constexpr int kB_EC = kB_RED + 4096;
 constexpr int kB_GRAW = kB_EC + 64;     // 2 x 128 raw g, beta (prefetch)
 constexpr int kB_BAR = kB_GRAW + 2 * 512;
@@ -1374,10 +1386,16 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int i = 0; i < 16; ++i) u[i] *= ff[cg * 16 + i];
       store_chunks(sm + kB_X + 32768, row, cg * 2, u, 2);
       {
+        // s_j = f_j u_j . (dG K^T)_j enters dgamma_j with a minus sign and the
+        // chunk-end carry with a plus sign
         float x1[16];
         tmem_ld16(tmem + lb + kBtX1 + cg * 16, x1);  // dG K^T, row c, columns j
 #pragma unroll
-        for (int i = 0; i < 16; ++i) cdot = fmaf(u[i], x1[i], cdot);
+        for (int i = 0; i < 16; ++i) {
+          const float sj = u[i] * x1[i];
+          cdot += sj;
+          acc[i] = -sj;
+        }
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) cdot += __shfl_xor_sync(0xffffffffu, cdot, off);
@@ -1392,7 +1410,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const float vr = tile_elem(sm + kB_V + half * 8192, r, cc);
         const float dr = bt[r] * z[i];
         stage_bf16(sm + kB_T, r, row, dr);  // dv; T and P have been read for the last time
-        acc[i] = -vr * dr;                        // -v . dv
+        acc[i] = fmaf(ee[r] * dr, rr[i], acc[i]);  // -e_r dR_rc (K H_in)_rc  (rr = -(K H_in)^T)
         rr[i] = z[i] * (vr + ee[r] * rr[i]);      // dZ_rc R_rc
         *reinterpret_cast<__nv_bfloat16*>(sm + kB_ZO + half * 16384 + sw_row_off(r, cc >> 3) +
                                           (cc & 7) * 2) = __float2bfloat16_rn(z[i]);
@@ -1435,14 +1453,27 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         float s2 = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          s2 += x[i] * kk[i];
+          const float t = x[i] * kk[i];
+          s2 += t;
+          acc[i] = fmaf(-br, t, acc[i]);  // -colsum(dA o A)
           x[i] *= br;
         }
-        red[cg * 64 + r] = s2;
+        red[cg * 64 + r] = s2;             // rowsum(dA o A) = beta_r * (sum over cg)
         store_chunks(sm + kB_T, r, cg * 2, x, 2);
       } else {
+        // Z = dP o P with P = Q K^T o Gam (Q K^T still in these TMEM lanes)
         const int r = row - 64;
-        decay_row(x, GV, r, cg * 16, false, 1.f);
+        float qk[16];
+        tmem_ld16(tmem + lb + kBtKQ + cg * 16, qk);
+        decay_row(x, GV, r, cg * 16, false, 1.f);  // x = dP o Gam
+        float sz = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float t = x[i] * qk[i];
+          sz += t;
+          acc[i] -= t;                     // -colsum(Z)
+        }
+        red[kRedZ + cg * 64 + r] = sz;     // rowsum(Z) partial
         store_chunks(sm + kB_P, r, cg * 2, x, 2);
       }
     }
@@ -1462,7 +1493,13 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     fence_async_shared();
     cta_sync();
-    if (tid < 64) db2[tid] = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
+    if (tid < 64) {
+      const float s2 = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
+      db2[tid] = s2;
+      // rowsum(dA o A) + rowsum(Z) of this chunk's log-gate gradient
+      red[kRedRow + tid] = bt[tid] * s2 + red[kRedZ + tid] + red[kRedZ + 64 + tid] +
+                           red[kRedZ + 128 + tid] + red[kRedZ + 192 + tid];
+    }
     // ---- dG_in part, dQ^T, dK^T
     if (tid == 0) {
       // G3 = (e dO)^T Q - (e dR)^T K   [c x d]
@@ -1474,14 +1511,16 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16(tmem + kBtG3, sw128_desc(sX1 + ks * 32, 16, 1024), sw128_desc(sKQ + ks * 2048, 16384, 1024),
                  idgn, 1);
-      // dQ^T = G_in^T (e dO)^T + K^T (dP o Gam)^T   [d x r]  -> X2 columns
+      // dQ^T = G_in^T (e dO)^T + K^T (dP o Gam)^T   [d x r], the two terms in
+      // separate accumulators (R columns, X2 columns): q . (first term) is the
+      // state's part of the log-gate gradient
       const uint32_t idq = idesc_bf16(128, 64, true, false);
       for (int ks = 0; ks < 8; ++ks)
-        mma_bf16(tmem + kBtX2, sw128_desc(sGI + ks * 2048, 16384, 1024),
+        mma_bf16(tmem + kBtR, sw128_desc(sGI + ks * 2048, 16384, 1024),
                  sw128_desc(sZO + 8192 + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024), idq, ks > 0);
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16(tmem + kBtX2, sw128_desc(sKQ + ks * 2048, 16384, 1024), sw128_desc(sDP + ks * 32, 16, 1024),
-                 idq, 1);
+                 idq, ks > 0);
       // dK^T  [d x j] -> U columns
       const uint32_t idmm = idesc_bf16(128, 64, true, true);
       const uint32_t idmmn = idesc_bf16(128, 64, true, true, true);
@@ -1530,13 +1569,18 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         write_dg(g);         // the products that read the old copy are done
       }
       float x[16];
-      tmem_ld16(tmem + lb + kBtX2 + cg * 16, x);  // dQ^T row d = row, columns r = 16 cg + i
+      tmem_ld16(tmem + lb + kBtR + cg * 16, x);  // dQ^T state term, row d = row, columns r = 16 cg + i
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const int r = cg * 16 + i;
         const float2 q2 = __bfloat1622float2(qv[i / 2]);
-        acc[i] += ((i & 1) ? q2.y : q2.x) * x[i];
-        stage_bf16(sm + kB_X, r, row, x[i]);  // dq (X0 is free once the products are done)
+        acc[i] = fmaf((i & 1) ? q2.y : q2.x, x[i], acc[i]);  // e_r dO_r . (Q H_in)_r
+      }
+      {
+        float y[16];
+        tmem_ld16(tmem + lb + kBtX2 + cg * 16, y);  // dQ^T intra-chunk term
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          stage_bf16(sm + kB_X, cg * 16 + i, row, x[i] + y[i]);  // dq (X0 is free once the products are done)
       }
       tmem_ld16(tmem + lb + kBtU + cg * 16, x);  // dK^T row d, columns j
 #pragma unroll
@@ -1564,11 +1608,11 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (r < n) p.dbeta[((size_t)b * p.T + t0 + r) * p.H + h] = db1[r] + db2[r];
     }
     if (warp == 0) {
-      // dg_t = sum_{s >= t, s in chunk} (q_s.dq_s - v_s.dv_s) + <dH_out, H_out>
+      // dg_t = sum_{s >= t, s in chunk} dgamma_s + <dH_out, H_out>
       float carry = 0.f;
 #pragma unroll
       for (int w = 0; w < BT / 32; ++w) carry += red[256 + w];
-      float a0 = dlc[lane], a1 = dlc[lane + 32];
+      float a0 = dlc[lane] + red[kRedRow + lane], a1 = dlc[lane + 32] + red[kRedRow + lane + 32];
       float s1 = a1;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {

@@ -119,12 +119,7 @@ GDN_API int gdn_fwd(const gdn_shape* shape, const void* q, const void* k, const 
             void* ws, size_t ws_bytes, void* stream);
 
 /* GDN backward: gradients with respect to every forward input.  dht may be
- * NULL (zero gradient of the final state); dh0 may be NULL (not wanted).
- * Precision of dg on the tensor-core path (bf16): measured rel-L2 against an
- * fp64 reference is within 2e-2 for gates g = logsigmoid(N(2, 1)) (about
- * -0.13 a token), but grows when the gates decay fast: 2.6e-2, 6.3e-2 and
- * 0.37 for logsigmoid(N(mu, 1)) with mu = 0, -1, -3.  The other gradients and
- * the CUDA-core path are not affected. */
+ * NULL (zero gradient of the final state); dh0 may be NULL (not wanted). */
 GDN_API int gdn_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
             const float* g, const float* beta, const float* h0, const void* do_,
             const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
@@ -228,8 +223,10 @@ GDN_API int gdn_uses_tensor_cores(const gdn_shape* shape);
  * and launch nothing.  All calls share the array: calls whose GPU work
  * overlaps (other streams, unordered host threads) race and give wrong
  * results.  The first call on each device looks up the array's address
- * (cudaGetSymbolAddress); make it before any stream capture.  A failure of
- * that set-up returns GDN_ERR_CUDA. */
+ * (cudaGetSymbolAddress) and keeps it until the process exits; make that call
+ * before any stream capture, and do not call cudaDeviceReset after it (the
+ * kept address would be stale).  A failure of that set-up returns
+ * GDN_ERR_CUDA, with the CUDA error in gdn_last_cuda_error(). */
 GDN_API int gdn_bwd_noalloc(const gdn_shape* shape, const void* q, const void* k, const void* v,
                             const float* g, const float* beta, const float* h0,
                             const void* do_, const float* dht, void* dq, void* dk, void* dv,

@@ -94,22 +94,20 @@ def tf32_round(x):
 @pytest.mark.parametrize("kda", [False, True])
 @pytest.mark.parametrize("g_mean", [2.0, -1.0])
 def test_factored_backward_with_bf16_operands(kda, g_mean):
-    """Every gradient meets the bf16 bar with all operands in bf16 for the
-    workloads' gates.  With gates that decay ten times faster, dg does not
-    (about 1.4e-2 for GDN and 2.3e-2 for KDA): it is a difference of two
-    nearly equal decayed sums, and the bf16 rounding of the scaled tiles
-    K exp(+-(gamma - lam)), Q exp(gamma - lam) no longer cancels.  Holding
-    just those three tiles at TF32 precision brings it back to ~3e-3."""
+    """With the three scaled tiles K exp(+-(gamma - lam)) and Q exp(gamma - lam)
+    at TF32 precision and every other operand in bf16, every gradient meets
+    the bf16 bar, for the workloads' gates and for gates that decay ten times
+    faster.  (With those tiles in bf16 as well, dg at the faster gates is a
+    difference of nearly equal decayed sums whose rounding no longer cancels;
+    the other gradients are unaffected, which is checked too.)"""
     x, do, dht = grads_inputs(192, 1, 128, 128, kda, g_mean, seed=5)
     ref = oracle.bwd(*x, do, dht, kda=kda)
-    got = cr.backward_factored(*x, do, dht, 64, kda, operand=cr.bf16_round)
-    for n in ref:
-        if n == "dg" and g_mean < 0:
-            assert 5e-3 < rel(got[n], ref[n]) < 5e-2, rel(got[n], ref[n])
-        else:
-            assert rel(got[n], ref[n]) < 2e-2, (n, rel(got[n], ref[n]))
     mixed = cr.backward_factored(*x, do, dht, 64, kda, operand=cr.bf16_round,
                                  scaled_operand=tf32_round)
     for n in ref:
         assert rel(mixed[n], ref[n]) < 1e-2, (n, rel(mixed[n], ref[n]))
+    got = cr.backward_factored(*x, do, dht, 64, kda, operand=cr.bf16_round)
+    for n in ref:
+        if n != "dg":
+            assert rel(got[n], ref[n]) < 2e-2, (n, rel(got[n], ref[n]))
 

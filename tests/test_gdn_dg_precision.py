@@ -3,19 +3,21 @@
 A numpy model of one reverse-scan chunk of the tensor-core backward, with
 bf16 rounding at the places the kernel rounds (every MMA operand tile: the T
 tile, the entry state, P, beta R, dU, U and U f, dZ, e dR, M, dP o Gam, e dO;
-sums and TMEM values in full precision), computes dg two ways:
+sums and TMEM values in full precision), computes dg the way the kernel does:
+from the term decomposition of the chunk's cumulative-log-gate gradient,
+whose terms are all full-precision chunk matrices --
+  q . (the state term of dQ, a separate accumulator) = e dO . (Q H_in),
+  + rowsum - colsum of Z = dP o P and of dA o A,
+  - e dR . (K H_in), - s_j with s_j = f_j u_j . (dH^T k_j),
+plus the chunk-end state terms, reverse-summed inside the chunk.
 
-* the scalar gate's per-chunk identity the kernel uses,
-  dg_t = sum_{s >= t} (q_s . dq_s - v_s . dv_s) + <dH_out, H_out>;
-* the term decomposition, whose terms are all full-precision chunk matrices:
-  +rowsum - colsum of Z = dP o P and of dA o A, rowsum(dO o e Q H_in),
-  -rowsum(dR o e K H_in), and the chunk-end state terms.
-
-On the inputs of the GPU test of fast-decaying gates (logsigmoid(N(mu, 1))
-gates, mu = 0, -1, -3), the model's identity gives dg errors of 1.3e-2, 3.8e-2
-and 0.24 -- the same trend as the kernel's measured 2.6e-2, 6.3e-2 and 0.37
-(the kernel rounds in a few more places than modelled) -- while the term
-decomposition stays near 8e-4 in all three: the fix for the kernel's dg.
+The pin: on the inputs of the GPU test of fast-decaying gates
+(logsigmoid(N(mu, 1)) gates, mu from the workloads' 2 down to -5, 64-token
+gate ranges up to about 320) this form stays within 5e-3 of the oracle's dg.
+The scalar gate's rescaling identity dg = revcumsum(q . dq - v . dv) + carry,
+which an earlier kernel used, is a difference of two large, nearly equal
+sums there; the test also checks that the model reproduces that failure
+(so that it does model the rounding that matters).
 """
 import os
 import sys
@@ -34,14 +36,15 @@ rnd = cr.bf16_round
 def chunk_bwd_model(Q, K, V, g, beta, H, dO, dH):
     """One chunk (n = 64 rows) of the tensor-core backward at its rounding
     points; H is the bf16 entry state (dk x dv), dH the fp32 gradient of the
-    exit state.  Returns (dq, dk, dv, dbeta, dH_in, dg_identity, dg_terms)."""
+    exit state.  Returns (dH_in, dg_kernel, dg_identity)."""
     n = Q.shape[0]
     gam = np.cumsum(g)
     e, eC, f = np.exp(gam), np.exp(gam[-1]), np.exp(gam[-1] - gam)
     low = np.tril(np.ones((n, n)))
+    strict = np.tril(np.ones((n, n)), -1)
     Gam = np.exp(np.where(low > 0, gam[:, None] - gam[None, :], 0.0)) * low
     KK, QK = K @ K.T, Q @ K.T
-    A = beta[:, None] * KK * Gam * np.tril(np.ones((n, n)), -1)
+    A = beta[:, None] * KK * Gam * strict
     T = rnd(np.linalg.inv(np.eye(n) + A))            # the solve kernel's bf16 tile
     P = QK * Gam
     KH = K @ H
@@ -49,32 +52,27 @@ def chunk_bwd_model(Q, K, V, g, beta, H, dO, dH):
     dHb = rnd(dH)                                     # bf16 copy of dG
     dU = f[:, None] * (K @ dHb) + rnd(P).T @ dO
     U = T @ rnd(beta[:, None] * R)
-    Ub, Ufb = rnd(U), rnd(U * f[:, None])
+    Ub = rnd(U)
     dZ = T.T @ rnd(dU)
     dR = beta[:, None] * dZ
     edRb = rnd(e[:, None] * dR)
-    dA = -(rnd(dZ) @ Ub.T) * np.tril(np.ones((n, n)), -1)
+    dA = -(rnd(dZ) @ Ub.T) * strict
     dP = (dO @ Ub.T) * low
-    M = rnd(beta[:, None] * dA * Gam)
     dPG = rnd(dP * Gam)
     edO = rnd(e[:, None] * dO)
     dH_in = eC * dH + Q.T @ edO - K.T @ edRb
-    dq = edO @ H.T + dPG @ K
-    dk = Ufb @ dHb.T - edRb @ H.T + dPG.T @ Q + (M + M.T) @ K
-    dbeta = np.sum(dZ * R, axis=1) + np.sum(dA * Gam * KK, axis=1)
-    # the chunk's <dH_out, H_out> from its own state update
-    s = f * np.sum(U * (K @ dH), axis=1)              # s_j = f_j u_j . (dH^T k_j)
+    dq1 = edO @ H.T                                   # state term of dQ (own accumulator)
+    dq = dq1 + dPG @ K
+    s = f * np.sum(U * (K @ dHb), axis=1)             # s_j = f_j u_j . (dG K^T)_j
     carry = eC * np.sum(dH * H) + s.sum()
-    # identity
-    dlc = np.sum(Q * dq, axis=1) - np.sum(V * dR, axis=1)
-    dg_id = np.cumsum(dlc[::-1])[::-1] + carry
-    # term decomposition (every term from full-precision chunk matrices)
     Z = dP * P
     Ga = dA * A
-    dgam = (e * np.sum(dO * (Q @ H), axis=1) + Z.sum(1) - Z.sum(0) + Ga.sum(1) - Ga.sum(0)
+    dgam = (np.sum(Q * dq1, axis=1) + Z.sum(1) - Z.sum(0) + Ga.sum(1) - Ga.sum(0)
             - e * np.sum(dR * KH, axis=1) - s)
-    dg_terms = np.cumsum(dgam[::-1])[::-1] + carry
-    return dq, dk, dR, dbeta, dH_in, dg_id, dg_terms
+    dg_kernel = np.cumsum(dgam[::-1])[::-1] + carry
+    dlc = np.sum(Q * dq, axis=1) - np.sum(V * dR, axis=1)
+    dg_identity = np.cumsum(dlc[::-1])[::-1] + carry
+    return dH_in, dg_kernel, dg_identity
 
 
 def model_backward(q, k, v, g, beta, h0, do, dht):
@@ -88,13 +86,13 @@ def model_backward(q, k, v, g, beta, h0, do, dht):
         _, S = cr.chunk_forward(q[c0:c0 + 64], k[c0:c0 + 64], v[c0:c0 + 64], g[c0:c0 + 64],
                                 beta[c0:c0 + 64], S, False)
     dH = dht.astype(np.float64)
-    dg_id, dg_terms = np.zeros(T), np.zeros(T)
+    dg_k, dg_id = np.zeros(T), np.zeros(T)
     for ci in reversed(range(T // 64)):
         sl = slice(64 * ci, 64 * ci + 64)
-        _, _, _, _, dH, a, b = chunk_bwd_model(q[sl], k[sl], v[sl], g[sl], beta[sl],
-                                               rnd(states[ci]), do[sl], dH)
-        dg_id[sl], dg_terms[sl] = a, b
-    return dg_id, dg_terms
+        dH, a, b = chunk_bwd_model(q[sl], k[sl], v[sl], g[sl], beta[sl], rnd(states[ci]),
+                                   do[sl], dH)
+        dg_k[sl], dg_id[sl] = a, b
+    return dg_k, dg_id
 
 
 def case(mu, h):
@@ -112,19 +110,19 @@ def rel(x, ref):
     return np.linalg.norm(x - ref) / np.linalg.norm(ref)
 
 
-@pytest.mark.parametrize("mu", [2.0, 0.0, -1.0, -3.0])
-def test_term_decomposition_keeps_dg_accurate(mu):
-    ids, terms, refs = [], [], []
+@pytest.mark.parametrize("mu", [2.0, 0.0, -1.0, -3.0, -5.0])
+def test_kernel_dg_form_stays_accurate(mu):
+    kern, ident, refs = [], [], []
     for h in range(2):
         x, *args = case(mu, h)
         if h == 0:
             ref = oracle.bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do, x.dht)
         a, b = model_backward(*args)
-        ids.append(a)
-        terms.append(b)
+        kern.append(a)
+        ident.append(b)
         refs.append(ref["dg"][0, :, h])
-    ids, terms, refs = map(np.concatenate, (ids, terms, refs))
-    r_id, r_terms = rel(ids, refs), rel(terms, refs)
-    assert r_terms < 5e-3, (r_id, r_terms)
-    if mu < 1:  # the identity's error grows as the gates forget faster
-        assert r_id > 5 * r_terms, (r_id, r_terms)
+    kern, ident, refs = map(np.concatenate, (kern, ident, refs))
+    r_kern, r_id = rel(kern, refs), rel(ident, refs)
+    assert r_kern < 5e-3, (r_kern, r_id)
+    if mu <= -3:  # the rounding this models does break the rescaling identity here
+        assert r_id > 2e-2, (r_kern, r_id)

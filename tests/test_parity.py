@@ -156,14 +156,15 @@ def test_segmented_forward_matches_oracle():
 # ----------------------------------------------------------- fast-decaying gates
 
 # The workloads' gates are logsigmoid(N(2, 1)), about -0.13 a token.  These
-# decay 5-20 times faster: 64-token ranges of about 48, 86 and 191, the last
-# two past the tensor-core kernels' factor limit, so their decays take the
-# exact per-element path.
-FAST = [0.0, -1.0, -3.0]
+# decay 5-40 times faster: 64-token ranges of about 48, 86, 191 and 320, the
+# last three past the tensor-core kernels' factor limit, so their decays take
+# the exact per-element path.  dg is the output this stresses: its terms are
+# large and nearly cancel when the state forgets quickly.
+FAST = [0.0, -1.0, -3.0, -5.0]
 
 
 @pytest.mark.parametrize("g_mean", FAST)
-def test_fast_decaying_gates_match_oracle_except_dg(g_mean):
+def test_fast_decaying_gates_match_oracle(g_mean):
     x = make_inputs(1, 256, 2, 128, 128, dtype="bf16", g_mean=g_mean, h0_std=0.3,
                     with_dht=True, seed=21)
     o, ht, gr = run_gpu(x, 64)
@@ -171,20 +172,8 @@ def test_fast_decaying_gates_match_oracle_except_dg(g_mean):
     o_ref, ht_ref = oracle.fwd(x.q, x.k, x.v, x.g, x.beta, x.h0)
     check("o", o.cpu(), o_ref, fp32=False)
     check("ht", ht.cpu(), ht_ref, fp32=False)
-    for n in ("dq", "dk", "dv", "dbeta", "dh0"):
+    for n in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
         check(n, gr[n].cpu(), ref[n], fp32=False)
-
-
-@pytest.mark.xfail(strict=True, reason="known limitation: the tensor-core backward takes dg from "
-                   "the scalar gate's per-chunk identity, a difference of nearly equal sums when "
-                   "gates decay fast (rel-L2 2.6e-2, 6.3e-2, 0.37 for these three)")
-@pytest.mark.parametrize("g_mean", FAST)
-def test_fast_decaying_gates_dg(g_mean):
-    x = make_inputs(1, 256, 2, 128, 128, dtype="bf16", g_mean=g_mean, h0_std=0.3,
-                    with_dht=True, seed=21)
-    _, _, gr = run_gpu(x, 64)
-    ref = oracle.bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do, x.dht)
-    check("dg", gr["dg"].cpu(), ref["dg"], fp32=False)
 
 
 # ----------------------------------------------------------- saved context

@@ -7,10 +7,12 @@ could not provide, so the library offers gdn_bwd_noalloc, which takes its
 scratch from a fixed device array built into the library.
 
 This file checks, through the C ABI, that it returns the same gradients as
-gdn_bwd (within the bf16 tolerance the parity tests use) on two calls in a
-row -- the second call finds the scratch array as the first one left it --
-and that shapes needing more scratch than the array holds are refused before
-anything runs.  It is named to be collected last.
+gdn_bwd, bit for bit (both run the same deterministic kernels on the same
+inputs), on two calls in a row -- the second call finds the scratch array as
+the first one left it -- for a tensor-core shape and a CUDA-core fp32 shape
+(whose workspace is laid out differently inside the array), and that shapes
+needing more scratch than the array holds are refused before anything runs.
+It is named to be collected last.
 """
 import ctypes
 
@@ -60,16 +62,23 @@ def _rel_l2(a, b):
     return np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
 
 
-def test_noalloc_matches_gdn_bwd_on_two_calls_in_a_row():
+# B, T, H, dk, dv, chunk, dtype: the tensor-core path, then the CUDA-core fp32 path
+SHAPES = [(2, 200, 2, 128, 128, 64, "bf16"), (2, 100, 3, 32, 48, 32, "f32")]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda c: "x".join(map(str, c)))
+def test_noalloc_matches_gdn_bwd_on_two_calls_in_a_row(shape):
+    B, T, H, dk, dv, chunk, dtype = shape
     for seed in (11, 12):
-        x = make_inputs(2, 200, 2, 128, 128, dtype="bf16", h0_std=0.1, with_dht=True,
+        x = make_inputs(B, T, H, dk, dv, dtype=dtype, h0_std=0.1, with_dht=True,
                         seed=seed).to("cuda")
-        got = _call_noalloc(x)
-        ref = gdn.gdn_bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do, x.dht)
+        got = _call_noalloc(x, chunk)
+        ref = gdn.gdn_bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do, x.dht, chunk=chunk)
         torch.cuda.synchronize()
         for name, r in ref.items():
             assert torch.isfinite(got[name].float()).all(), name
             assert _rel_l2(got[name], r) <= BF16_REL, (seed, name)
+            assert torch.equal(got[name], r), (seed, name)
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch():
