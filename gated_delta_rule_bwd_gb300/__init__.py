@@ -47,6 +47,7 @@ EXPORTS = ("gdn_fwd", "gdn_bwd", "kda_fwd", "kda_bwd", "gdn_fwd_workspace", "kda
            "gdn_fwd_save", "kda_fwd_save", "gdn_bwd_saved", "kda_bwd_saved",
            "gdn_decode", "kda_decode",
            "gdn_status_str", "gdn_last_cuda_error", "gdn_device_status", "gdn_uses_tensor_cores",
+           "gdn_wait_selftest", "kda_uses_tensor_cores",
            "gdn_profile_begin", "gdn_profile_end", "gdn_profile_read", "gdn_kernel_name")
 
 
@@ -80,8 +81,11 @@ def lib():
             L.gdn_last_cuda_error.restype = ctypes.c_int
             L.gdn_device_status.argtypes = []
             L.gdn_device_status.restype = ctypes.c_int
-            L.gdn_uses_tensor_cores.argtypes = [sp]
-            L.gdn_uses_tensor_cores.restype = ctypes.c_int
+            L.gdn_wait_selftest.argtypes = [ctypes.c_int, vp]
+            L.gdn_wait_selftest.restype = ctypes.c_int
+            for name in ("gdn_uses_tensor_cores", "kda_uses_tensor_cores"):
+                getattr(L, name).argtypes = [sp]
+                getattr(L, name).restype = ctypes.c_int
             L.gdn_profile_begin.argtypes = [ctypes.c_int]
             L.gdn_profile_begin.restype = ctypes.c_int
             L.gdn_profile_end.argtypes = []
@@ -163,9 +167,10 @@ def _workspace(need, given, device):
     return torch.empty(max(need, 16), dtype=torch.uint8, device=device)
 
 
-def uses_tensor_cores(q, v, chunk=64) -> bool:
+def uses_tensor_cores(q, v, chunk=64, kda=False) -> bool:
     s = make_shape(q, v, chunk)
-    return bool(lib().gdn_uses_tensor_cores(ctypes.byref(s)))
+    fn = lib().kda_uses_tensor_cores if kda else lib().gdn_uses_tensor_cores
+    return bool(fn(ctypes.byref(s)))
 
 
 def _fwd(kda, q, k, v, g, beta, h0=None, chunk=64, output_final_state=True, out=None,
@@ -297,6 +302,11 @@ def gdn_decode(q, k, v, g, beta, state=None, inplace=True):
 def kda_decode(q, k, v, g, beta, state=None, inplace=True):
     """KDA forward run token by token (``g`` is ``[B,T,H,dk]``); see ``gdn_decode``."""
     return _decode(True, q, k, v, g, beta, state, inplace)
+
+
+def wait_selftest(max_tries=5):
+    """Runs the device-side timeout path once (see gdn_wait_selftest in gdn.h)."""
+    _check(lib().gdn_wait_selftest(max_tries, _stream(torch.device("cuda", torch.cuda.current_device()))))
 
 
 def device_status() -> int:

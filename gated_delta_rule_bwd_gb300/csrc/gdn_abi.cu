@@ -49,18 +49,22 @@ bool empty(const gdn::Problem& p) { return p.B == 0 || p.H == 0; }
 
 size_t fwd_ws(const gdn::Problem& p) {
   if (empty(p) || p.T == 0) return 0;
+  if (gdn::kda_tc_supported(p)) return gdn::kda_tc_fwd_workspace(p);
   return gdn::tc_supported(p) ? gdn::tc_fwd_workspace(p) : 0;
 }
 
 size_t bwd_ws(const gdn::Problem& p) {
   if (empty(p) || p.T == 0) return 0;
+  if (gdn::kda_tc_supported(p)) return gdn::kda_tc_bwd_workspace(p);
   return gdn::tc_supported(p) ? gdn::tc_bwd_workspace(p) : gdn::simt_bwd_workspace(p);
 }
 
 // The CUDA-core path's context is the backward pass's workspace, whose first
-// part (the fp32 entry state of every chunk) the forward pass fills.
+// part (the fp32 entry state of every chunk) the forward pass fills; the KDA
+// tensor-core path's is its backward workspace as well.
 size_t ctx_bytes(const gdn::Problem& p) {
   if (empty(p) || p.T == 0) return 0;
+  if (gdn::kda_tc_supported(p)) return gdn::kda_tc_bwd_workspace(p);
   return gdn::tc_supported(p) ? gdn::tc_ctx_bytes(p) : gdn::simt_bwd_workspace(p);
 }
 
@@ -95,7 +99,9 @@ int run_fwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
   if (need > 0 && (!ws || ws_bytes < need)) return GDN_ERR_WORKSPACE;
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.o = o; p.ht = ht;
   p.ws = ws; p.ws_bytes = ws_bytes;
-  cudaError_t e = gdn::tc_supported(p) ? gdn::tc_fwd(p, st, save) : gdn::simt_fwd(p, st, save);
+  cudaError_t e = gdn::kda_tc_supported(p) ? gdn::kda_tc_fwd(p, st, save)
+                  : gdn::tc_supported(p)     ? gdn::tc_fwd(p, st, save)
+                                             : gdn::simt_fwd(p, st, save);
   return e == cudaSuccess ? GDN_OK : fail_cuda(e);
 }
 
@@ -122,8 +128,9 @@ int run_bwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.do_ = do_; p.dht = dht;
   p.dq = dq; p.dk_ = dk; p.dv_ = dv; p.dg = dg; p.dbeta = dbeta; p.dh0 = dh0;
   p.ws = ws; p.ws_bytes = ws_bytes;
-  cudaError_t e =
-      gdn::tc_supported(p) ? gdn::tc_bwd(p, st, saved) : gdn::simt_bwd(p, st, saved);
+  cudaError_t e = gdn::kda_tc_supported(p) ? gdn::kda_tc_bwd(p, st, saved)
+                  : gdn::tc_supported(p)     ? gdn::tc_bwd(p, st, saved)
+                                             : gdn::simt_bwd(p, st, saved);
   return e == cudaSuccess ? GDN_OK : fail_cuda(e);
 }
 
@@ -170,7 +177,8 @@ int record_cuda_error(cudaError_t e) { return fail_cuda(e); }
 const char* kernel_name(int id) {
   static const char* names[kNumKernelIds] = {
       "simt_fwd", "simt_states", "simt_bwd", "simt_bwd_reduce",
-      "tc_fwd", "tc_states", "tc_bwd", "tc_solve", "tc_fwd_segment", "tc_combine", "decode"};
+      "tc_fwd", "tc_states", "tc_bwd", "tc_solve", "tc_fwd_segment", "tc_combine", "decode",
+      "kda_tc_prep", "kda_tc_fwd", "kda_tc_states", "kda_tc_bwd"};
   return (id >= 0 && id < kNumKernelIds) ? names[id] : "unknown";
 }
 
@@ -329,10 +337,22 @@ int gdn_device_status(void) {
   return status;
 }
 
+int gdn_wait_selftest(int max_tries, void* stream) {
+  if (max_tries < 1 || max_tries > 1000) return GDN_ERR_ARG;
+  cudaError_t e = gdn::wait_selftest(max_tries, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GDN_OK : fail_cuda(e);
+}
+
 int gdn_uses_tensor_cores(const gdn_shape* shape) {
   gdn::Problem p;
   if (check_shape(shape, false, &p) != GDN_OK) return 0;
   return gdn::tc_supported(p) ? 1 : 0;
+}
+
+int kda_uses_tensor_cores(const gdn_shape* shape) {
+  gdn::Problem p;
+  if (check_shape(shape, true, &p) != GDN_OK) return 0;
+  return gdn::kda_tc_supported(p) ? 1 : 0;
 }
 
 }  // extern "C"

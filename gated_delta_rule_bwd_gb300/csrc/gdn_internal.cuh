@@ -28,8 +28,10 @@ size_t simt_bwd_workspace(const Problem& p);
 // save / saved: the workspace is a saved context (simt_bwd_workspace bytes);
 // the forward writes every chunk's fp32 entry state into it and the backward
 // reads them instead of running the states pass.
-cudaError_t simt_fwd(const Problem& p, cudaStream_t s, bool save);
-cudaError_t simt_bwd(const Problem& p, cudaStream_t s, bool saved);
+// only: if non-NULL, a per-sequence flag array [B*H]; the kernels then run
+// only the sequences whose flag is set (the others' outputs are untouched).
+cudaError_t simt_fwd(const Problem& p, cudaStream_t s, bool save, const int* only = nullptr);
+cudaError_t simt_bwd(const Problem& p, cudaStream_t s, bool saved, const int* only = nullptr);
 
 // Tensor-core kernels (bf16, dk = dv = 128, chunk = 64).
 bool tc_supported(const Problem& p);
@@ -40,6 +42,16 @@ size_t tc_ctx_bytes(const Problem& p);
 // forward fills and the backward of the same inputs reads.
 cudaError_t tc_fwd(const Problem& p, cudaStream_t s, bool save);
 cudaError_t tc_bwd(const Problem& p, cudaStream_t s, bool saved);
+
+// KDA tensor-core kernels (bf16, dk = dv = 128, chunk = 64).  Sequences
+// with a chunk whose per-dimension gate range is too wide for them are
+// flagged and computed by the CUDA-core kernels inside the same calls.
+bool kda_tc_supported(const Problem& p);
+size_t kda_tc_fwd_workspace(const Problem& p);
+size_t kda_tc_bwd_workspace(const Problem& p);  // also the saved context
+cudaError_t kda_tc_fwd(const Problem& p, cudaStream_t s, bool save);
+cudaError_t kda_tc_bwd(const Problem& p, cudaStream_t s, bool saved);
+cudaError_t kda_read_and_clear_status(int* status);
 
 // Token-recurrent forward for a few tokens per sequence (any dk, dv <= 128).
 cudaError_t decode(const Problem& p, cudaStream_t s);
@@ -57,7 +69,11 @@ enum KernelId {
   kTcSegment = 8,
   kTcCombine = 9,
   kDecode = 10,
-  kNumKernelIds = 11
+  kKdaPrep = 11,
+  kKdaFwd = 12,
+  kKdaStates = 13,
+  kKdaBwd = 14,
+  kNumKernelIds = 15
 };
 const char* kernel_name(int id);
 
@@ -68,6 +84,9 @@ void prof_after(cudaStream_t s, int kernel_id);
 
 // Per-device status word written by bounded device-side waits.
 cudaError_t read_and_clear_device_status(int* status);
+
+// One CTA whose bounded wait runs out on purpose (see gdn_wait_selftest).
+cudaError_t wait_selftest(int max_tries, cudaStream_t s);
 
 // Records e as the calling thread's last CUDA error (what gdn_last_cuda_error
 // returns) and returns GDN_ERR_CUDA.

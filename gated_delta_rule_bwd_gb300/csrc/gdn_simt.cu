@@ -50,6 +50,7 @@ struct SimtArgs {
   int nsplit;     // CTAs per sequence along dv
   float* states;  // [B*H][N][dk][dv] chunk-entry states (bwd) or nullptr
   float* part;    // partial sums of the backward pass
+  const int* only;  // if set, the kernels run only the sequences bh with only[bh] != 0
 };
 
 __device__ __forceinline__ size_t tok(const Problem& p, int b, int t, int h, int D) {
@@ -228,6 +229,7 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(SimtArgs a) {
   extern __shared__ float sm[];
   const Problem& p = a.p;
   const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
+  if (a.only && !a.only[bh]) return;
   const int dk = p.dk, C = p.C, dvs = a.dvs, lk = dk + 1, lc = C + 1;
   const int v0 = blockIdx.y * dvs, nv = min(dvs, p.dv - v0);
   const FwdSmem L = fwd_smem(dk, dvs, C, KDA);
@@ -344,6 +346,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(SimtArgs a) {
   extern __shared__ float sm[];
   const Problem& p = a.p;
   const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H, split = blockIdx.y;
+  if (a.only && !a.only[bh]) return;
   const int dk = p.dk, C = p.C, dvs = a.dvs, lk = dk + 1, lc = C + 1;
   const int v0 = split * dvs, nv = min(dvs, p.dv - v0);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -547,6 +550,7 @@ template <typename TIn, bool KDA>
 __global__ void __launch_bounds__(kThreads) simt_bwd_reduce_kernel(SimtArgs a) {
   const Problem& p = a.p;
   const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H, ci = blockIdx.y;
+  if (a.only && !a.only[bh]) return;
   const int dk = p.dk, t0 = ci * p.C, n = min(p.C, p.T - t0);
   const PartLayout PL = part_layout(p, a.nsplit);
   const size_t tokh = (size_t)p.B * p.T * p.H;
@@ -603,10 +607,12 @@ size_t states_bytes(const Problem& p) {
 }
 
 template <typename TIn, bool KDA>
-cudaError_t launch_fwd(const Problem& p, cudaStream_t s, float* states, bool want_out) {
+cudaError_t launch_fwd(const Problem& p, cudaStream_t s, float* states, bool want_out,
+                       const int* only) {
   const int kid = want_out ? kSimtFwd : kSimtStates;
   SimtArgs a{};
   a.p = p;
+  a.only = only;
   if (!want_out) a.p.o = nullptr, a.p.ht = nullptr;
   a.dvs = pick_dvs_fwd(p);
   a.nsplit = (p.dv + a.dvs - 1) / a.dvs;
@@ -624,12 +630,13 @@ cudaError_t launch_fwd(const Problem& p, cudaStream_t s, float* states, bool wan
 // With saved, the workspace holds the entry states that launch_fwd wrote
 // alongside the output (a saved context), and the states pass is skipped.
 template <typename TIn, bool KDA>
-cudaError_t launch_bwd(const Problem& p, cudaStream_t s, bool saved) {
+cudaError_t launch_bwd(const Problem& p, cudaStream_t s, bool saved, const int* only) {
   float* states = static_cast<float*>(p.ws);
   cudaError_t e;
-  if (!saved && (e = launch_fwd<TIn, KDA>(p, s, states, false)) != cudaSuccess) return e;
+  if (!saved && (e = launch_fwd<TIn, KDA>(p, s, states, false, only)) != cudaSuccess) return e;
   SimtArgs a{};
   a.p = p;
+  a.only = only;
   a.dvs = pick_dvs_bwd(p);
   a.nsplit = (p.dv + a.dvs - 1) / a.dvs;
   a.states = states;
@@ -657,18 +664,20 @@ size_t simt_bwd_workspace(const Problem& p) {
   return states_bytes(p) + align_up(part_layout(p, nsplit).total * sizeof(float), 256);
 }
 
-cudaError_t simt_fwd(const Problem& p, cudaStream_t s, bool save) {
+cudaError_t simt_fwd(const Problem& p, cudaStream_t s, bool save, const int* only) {
   float* st = save ? static_cast<float*>(p.ws) : nullptr;
-  if (p.bf16) return p.kda ? launch_fwd<__nv_bfloat16, true>(p, s, st, true)
-                           : launch_fwd<__nv_bfloat16, false>(p, s, st, true);
-  return p.kda ? launch_fwd<float, true>(p, s, st, true) : launch_fwd<float, false>(p, s, st, true);
+  if (p.bf16) return p.kda ? launch_fwd<__nv_bfloat16, true>(p, s, st, true, only)
+                           : launch_fwd<__nv_bfloat16, false>(p, s, st, true, only);
+  return p.kda ? launch_fwd<float, true>(p, s, st, true, only)
+               : launch_fwd<float, false>(p, s, st, true, only);
 }
 
-cudaError_t simt_bwd(const Problem& p, cudaStream_t s, bool saved) {
+cudaError_t simt_bwd(const Problem& p, cudaStream_t s, bool saved, const int* only) {
   if (p.bf16)
-    return p.kda ? launch_bwd<__nv_bfloat16, true>(p, s, saved)
-                 : launch_bwd<__nv_bfloat16, false>(p, s, saved);
-  return p.kda ? launch_bwd<float, true>(p, s, saved) : launch_bwd<float, false>(p, s, saved);
+    return p.kda ? launch_bwd<__nv_bfloat16, true>(p, s, saved, only)
+                 : launch_bwd<__nv_bfloat16, false>(p, s, saved, only);
+  return p.kda ? launch_bwd<float, true>(p, s, saved, only)
+               : launch_bwd<float, false>(p, s, saved, only);
 }
 
 }  // namespace gdn

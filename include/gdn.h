@@ -57,7 +57,12 @@
  * Kernel selection.  dtype BF16 with dk = dv = 128 and chunk = 64 runs the
  * tensor-core (tcgen05/TMEM, TMA-fed) kernels; every other valid shape runs
  * the CUDA-core fp32 kernels (chunk in {16, 32, 64}, 1 <= dk, dv <= 128).
- * T need not be a multiple of chunk.
+ * T need not be a multiple of chunk.  KDA on the tensor cores factors each
+ * chunk's per-dimension decays into scaled bf16 operand tiles; a sequence
+ * with a 64-token chunk whose cumulative log gate spans more than 80 in some
+ * key dimension (an average decay faster than exp(-1.25) per token there) is
+ * computed by the CUDA-core kernels inside the same call, so results meet the
+ * same bounds for any gates.
  */
 #ifndef GDN_H_
 #define GDN_H_
@@ -209,8 +214,24 @@ GDN_API int gdn_last_cuda_error(void);
  * GDN_ERR_CUDA if the read itself fails. */
 GDN_API int gdn_device_status(void);
 
-/* 1 if the tensor-core kernels would run for this shape, else 0. */
+/* Exercises the device-side timeout path.  Launches one CTA on `stream` that
+ * sets up an mbarrier and tensor memory as the scan kernels do, then waits on
+ * the barrier for at most max_tries bounded polls (each suspends the waiting
+ * threads for at most about 20 us) while nothing can complete it: no thread
+ * arrives and no copy or tensor-core operation is in flight.  The wait runs
+ * out, and the CTA takes the scan kernels' timeout branch: it records
+ * GDN_ERR_DEVICE_TIMEOUT in the device status word, frees its tensor memory
+ * and returns.  A following gdn_device_status() returns
+ * GDN_ERR_DEVICE_TIMEOUT (and clears it); the context stays usable.
+ * max_tries must be in [1, 1000] (GDN_ERR_ARG otherwise). */
+GDN_API int gdn_wait_selftest(int max_tries, void* stream);
+
+/* 1 if the tensor-core kernels would run for this shape, else 0 (GDN / KDA).
+ * For KDA this is the kernel family of the shape; a sequence whose gates
+ * decay too fast for it inside some chunk is still computed by the CUDA-core
+ * kernels (see "Kernel selection" above). */
 GDN_API int gdn_uses_tensor_cores(const gdn_shape* shape);
+GDN_API int kda_uses_tensor_cores(const gdn_shape* shape);
 
 /* GDN backward for callers that cannot allocate device memory (an allocator
  * callback that must not re-enter the allocator, a framework thread that only

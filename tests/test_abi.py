@@ -122,11 +122,18 @@ def test_forward_workspace_query_and_check(L):
     # keeps three fp32 dk x dv states per segment
     long = shape(B=1, T=64 * 1024, H=2, dk=128, dv=128, chunk=64, dtype=1)
     assert L.gdn_fwd_workspace(ctypes.byref(long)) > 2 * 1024 * 64 * 64 * 2 + 3 * 2 * 128 * 128 * 4
-    # the CUDA-core paths (fp32, KDA) need none
+    # the CUDA-core paths (fp32) need none
     f32 = shape(B=2, T=2048, H=4, dk=128, dv=128, chunk=64, dtype=0)
     assert L.gdn_fwd_workspace(ctypes.byref(f32)) == 0
-    assert L.kda_fwd_workspace(ctypes.byref(big)) == 0
+    assert L.kda_fwd_workspace(ctypes.byref(f32)) == 0
     assert L.gdn_fwd_workspace(ctypes.byref(shape(chunk=3))) == 0
+    # the KDA tensor-core forward keeps each chunk's scaled Kp|Qp, Km and T
+    # tiles (56 KB) and its factor vectors, plus a flag per sequence
+    kda_need = L.kda_fwd_workspace(ctypes.byref(big))
+    assert kda_need >= 2 * 4 * 32 * (32768 + 16384 + 8192)
+    assert kda_need <= L.kda_bwd_workspace(ctypes.byref(big))
+    fn = L.kda_fwd
+    assert fn(*args, FAKE, kda_need - 1, None) == GDN_ERR_WORKSPACE
 
 
 def test_saved_context_size_and_check(L):
@@ -193,6 +200,9 @@ def test_tensor_core_selection_rule(L):
               shape(dtype=1, dk=128, dv=128, chunk=32)):
         assert L.gdn_uses_tensor_cores(ctypes.byref(s)) == 0
     assert L.gdn_uses_tensor_cores(ctypes.byref(shape(dtype=1, dk=128, dv=128, chunk=64))) == 1
+    for s in (shape(dtype=0, dk=128, dv=128, chunk=64), shape(dtype=1, dk=128, dv=64, chunk=64)):
+        assert L.kda_uses_tensor_cores(ctypes.byref(s)) == 0
+    assert L.kda_uses_tensor_cores(ctypes.byref(shape(dtype=1, dk=128, dv=128, chunk=64))) == 1
 
 
 def test_binding_refuses_cpu_tensors(L):
@@ -200,3 +210,8 @@ def test_binding_refuses_cpu_tensors(L):
     x = torch.zeros(1, 4, 1, 16)
     with pytest.raises(gdn.GdnError):
         gdn.gdn_fwd(x, x, x, torch.zeros(1, 4, 1), torch.zeros(1, 4, 1), chunk=16)
+
+
+def test_wait_selftest_validates_its_argument(L):
+    assert L.gdn_wait_selftest(0, None) == GDN_ERR_ARG
+    assert L.gdn_wait_selftest(1001, None) == GDN_ERR_ARG

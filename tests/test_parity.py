@@ -91,6 +91,9 @@ SMALL = [
     (2, 192, 2, 128, 128, 32, "bf16", False, True, False),
     (2, 200, 2, 128, 128, 64, "bf16", False, True, True),  # tensor-core path, 8-token tail
     (1, 37, 3, 128, 128, 64, "bf16", False, True, True),   # tensor-core path, T < chunk
+    (2, 200, 2, 128, 128, 64, "bf16", True, True, True),   # KDA tensor-core path, 8-token tail
+    (1, 37, 3, 128, 128, 64, "bf16", True, True, True),    # KDA tensor-core path, T < chunk
+    (1, 64, 2, 128, 128, 64, "bf16", True, False, True),   # KDA tensor-core path, one full chunk
 ]
 
 
@@ -176,6 +179,41 @@ def test_fast_decaying_gates_match_oracle(g_mean):
         check(n, gr[n].cpu(), ref[n], fp32=False)
 
 
+# KDA: per-key-dimension gates logsigmoid(N(mu, 1)).  The tensor-core kernels
+# take a sequence while every 64-token chunk's cumulative log gate spans at
+# most 80 in each dimension (mu = 0: largest span about 65); wider spans send
+# the sequence to the CUDA-core kernels inside the same call (mu = -1, -3).
+KDA_FAST = [0.0, -1.0, -3.0]
+
+
+@pytest.mark.parametrize("g_mean", KDA_FAST)
+def test_kda_fast_decaying_gates_match_oracle(g_mean):
+    x = make_inputs(1, 256, 2, 128, 128, kda=True, dtype="bf16", g_mean=g_mean, h0_std=0.3,
+                    with_dht=True, seed=21)
+    o, ht, gr = run_gpu(x, 64)
+    compare(x, o, ht, gr, fp32=False)
+
+
+def test_kda_mixed_paths_in_one_call():
+    """One call whose sequences split between the paths: batch row 0 has the
+    workloads' slowly decaying gates (tensor cores), row 1 gates so fast that
+    its chunks exceed the factor range (CUDA cores); both match the oracle,
+    with the saved context and without."""
+    x = make_inputs(2, 200, 2, 128, 128, kda=True, dtype="bf16", h0_std=0.3, with_dht=True, seed=22)
+    fast = make_inputs(2, 200, 2, 128, 128, kda=True, dtype="bf16", g_mean=-3.0, h0_std=0.3,
+                       with_dht=True, seed=22)
+    x.g[1] = fast.g[1]
+    o, ht, gr = run_gpu(x, 64)
+    compare(x, o, ht, gr, fp32=False)
+    d = x.to("cuda")
+    o2, ht2, ctx = gdn.kda_fwd_save(d.q, d.k, d.v, d.g, d.beta, d.h0)
+    gr2 = gdn.kda_bwd_saved(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, ctx, d.dht)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, o) and torch.equal(ht2, ht)
+    for n in gr:
+        assert torch.equal(gr2[n], gr[n]), n
+
+
 # ----------------------------------------------------------- saved context
 
 SAVED = [
@@ -183,7 +221,8 @@ SAVED = [
     (2, 200, 2, 128, 128, 64, "bf16", False),   # tensor-core path, 8-token tail
     (1, 37, 3, 128, 128, 64, "bf16", False),    # tensor-core path, T < chunk
     (2, 100, 3, 32, 48, 32, "f32", False),      # CUDA-core path: fp32 entry states
-    (2, 200, 2, 64, 64, 64, "bf16", True),      # KDA
+    (2, 200, 2, 64, 64, 64, "bf16", True),      # KDA, CUDA-core path
+    (2, 200, 2, 128, 128, 64, "bf16", True),    # KDA tensor-core path
 ]
 
 
@@ -204,8 +243,9 @@ def test_saved_context_matches_oracle_and_recompute(case):
         gr = bwd_s(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, ctx, d.dht, chunk=chunk)
         torch.cuda.synchronize()
     names = [n for n, _ in t.records()]
-    if gdn.uses_tensor_cores(d.q, d.v, chunk) and not kda:
-        assert names == ["tc_bwd"], names
+    if gdn.uses_tensor_cores(d.q, d.v, chunk, kda):
+        # KDA: the CUDA-core kernels run too, for the sequences flagged (none here)
+        assert names == (["kda_tc_bwd", "simt_bwd", "simt_bwd_reduce"] if kda else ["tc_bwd"]), names
     else:
         assert names == ["simt_bwd", "simt_bwd_reduce"], names
     compare(x, o, ht, gr, fp32=dtype == "f32")
@@ -335,9 +375,9 @@ def test_decode_steps_chain_like_one_call():
 # ----------------------------------------------------------- invariants on the GPU
 
 def test_kda_with_broadcast_gate_equals_gdn():
-    """KDA (CUDA-core kernels) with one gate value repeated over the key
-    dimension against GDN (tensor-core kernels): equal within the bf16
-    tolerance; dg of GDN is the sum of KDA's over the key dimension."""
+    """KDA with one gate value repeated over the key dimension against GDN
+    (both on their tensor-core kernels): equal within the bf16 tolerance; dg
+    of GDN is the sum of KDA's over the key dimension."""
     x = make_inputs(2, 130, 2, 128, 128, dtype="bf16", h0_std=0.1, with_dht=True, seed=3)
     d = x.to("cuda")
     gk = d.g[..., None].expand(*d.g.shape, 128).contiguous()
@@ -431,3 +471,21 @@ def test_autograd_wrapper_matches_direct_calls(save_context):
     (o.float() * x.do.float()).sum().backward()
     ref = gdn.gdn_bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do)
     assert torch.equal(q.grad, ref["dq"]) and torch.equal(v.grad, ref["dv"])
+
+
+# ----------------------------------------------------------- bounded waits
+
+def test_bounded_wait_timeout_is_reported_and_context_survives():
+    """A device-side wait that nothing completes (no copy or tensor-core
+    operation in flight) runs out after its bounded polls; the kernel records
+    GDN_ERR_DEVICE_TIMEOUT, frees its tensor memory and returns.  The status
+    word reports it once, and the next library calls run normally."""
+    assert gdn.device_status() == 0
+    gdn.wait_selftest(5)
+    torch.cuda.synchronize()
+    assert gdn.device_status() == -7
+    assert gdn.device_status() == 0  # read and cleared
+    x = make_inputs(1, 130, 2, 128, 128, dtype="bf16", h0_std=0.1, with_dht=True, seed=19)
+    o, ht, gr = run_gpu(x, 64)
+    compare(x, o, ht, gr, fp32=False)
+    assert gdn.device_status() == 0
