@@ -13,7 +13,9 @@ wraps it with ctypes.  Every function takes arrays in the library's layout
 arrays.
 
 Parity status of each function is recorded next to its pins in
-``tests/test_oracle.py``: ``fwd`` and ``bwd`` are pinned for GDN and KDA.
+``tests/test_oracle.py``: ``fwd`` and ``bwd`` are pinned for GDN and KDA, and
+for the Mamba2 mixer (``delta=False``: the scalar-gated state without the
+delta rule).
 """
 from __future__ import annotations
 
@@ -83,20 +85,28 @@ def _dims(q, v, g, kda):
     return B, T, H, dk, dv
 
 
-def fwd(q, k, v, g, beta, h0=None, kda=False, nthreads=0, _lib_override=None):
-    """Token-recurrence forward.  Returns ``(o, ht)`` as fp64 arrays."""
+def _mode(kda, delta):
+    return int(bool(kda)) | (0 if delta else 2)
+
+
+def fwd(q, k, v, g, beta, h0=None, kda=False, nthreads=0, _lib_override=None, delta=True):
+    """Token-recurrence forward.  Returns ``(o, ht)`` as fp64 arrays.
+
+    ``delta=False`` drops the delta rule (the state only accumulates
+    ``beta k v^T``): the Mamba2 mixer of the same mixer list."""
     q, k, v, g, beta, h0 = map(_as64, (q, k, v, g, beta, h0))
     B, T, H, dk, dv = _dims(q, v, g, kda)
     o = np.zeros((B, T, H, dv))
     ht = np.zeros((B, H, dk, dv))
-    rc = (_lib_override or _load()).oracle_fwd(int(kda), B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+    rc = (_lib_override or _load()).oracle_fwd(_mode(kda, delta), B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                             _ptr(beta), _ptr(h0), _ptr(o), _ptr(ht), int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_fwd failed ({rc})")
     return o, ht
 
 
-def bwd(q, k, v, g, beta, h0, do, dht=None, kda=False, nthreads=0, _lib_override=None):
+def bwd(q, k, v, g, beta, h0, do, dht=None, kda=False, nthreads=0, _lib_override=None,
+        delta=True):
     """Reverse-mode backward.  Returns a dict of fp64 gradients.
 
     Keys: ``dq, dk, dv, dg, dbeta, dh0`` (``dh0`` is the gradient with respect
@@ -112,7 +122,7 @@ def bwd(q, k, v, g, beta, h0, do, dht=None, kda=False, nthreads=0, _lib_override
         "dbeta": np.zeros((B, T, H)),
         "dh0": np.zeros((B, H, dk, dv)),
     }
-    rc = (_lib_override or _load()).oracle_bwd(int(kda), B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+    rc = (_lib_override or _load()).oracle_bwd(_mode(kda, delta), B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                             _ptr(beta), _ptr(h0), _ptr(do), _ptr(dht), _ptr(out["dq"]),
                             _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
                             _ptr(out["dbeta"]), _ptr(out["dh0"]), int(nthreads))

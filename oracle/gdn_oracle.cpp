@@ -23,7 +23,12 @@
 //
 // which is S_t = a_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T with
 // S = H^T and o_t = S_t q_t; for KDA the decay is applied before the erase
-// term.  The backward pass is plain reverse-mode differentiation of this loop
+// term.  The same blog describes Mamba2, on the same mixer list, as the
+// scalar-gated state that GDN extends with the delta rule: its state only
+// accumulates.  That mixer is this loop without the delta rule's prediction,
+// vpred = 0, so that H = a_t H + beta_t k_t v_t^T (beta_t the write strength,
+// k/v/q the state-space input, input projection and read-out); the "no delta"
+// flag selects it, with either gate form.  The backward pass is plain reverse-mode differentiation of this loop
 // (every H_t is kept, so nothing is recomputed).  All arithmetic is fp64 and
 // follows the loop token by token: no chunking, no blocking, no reordering.
 //
@@ -43,7 +48,7 @@
 namespace {
 
 struct Dims {
-  int B, T, H, dk, dv, kda;
+  int B, T, H, dk, dv, kda, no_delta;
   size_t tok(int b, int t, int h, int D) const {
     return (((size_t)b * T + t) * H + h) * (size_t)D;
   }
@@ -89,8 +94,9 @@ void token_step(const Dims& d, const double* Hprev, const double* kt,
     for (int j = 0; j < dv; ++j) Pbuf[(size_t)i * dv + j] = a * Hprev[(size_t)i * dv + j];
   }
   for (int j = 0; j < dv; ++j) vp[j] = 0.0;
-  for (int i = 0; i < dk; ++i)
-    for (int j = 0; j < dv; ++j) vp[j] += Pbuf[(size_t)i * dv + j] * kt[i];
+  if (!d.no_delta)
+    for (int i = 0; i < dk; ++i)
+      for (int j = 0; j < dv; ++j) vp[j] += Pbuf[(size_t)i * dv + j] * kt[i];
   for (int i = 0; i < dk; ++i)
     for (int j = 0; j < dv; ++j) {
       const double u = bt * (vt[j] - vp[j]);
@@ -102,15 +108,17 @@ void token_step(const Dims& d, const double* Hprev, const double* kt,
 
 extern "C" {
 
+// mode: bit 0 = one gate per key dimension (KDA), bit 1 = no delta rule.
+//
 // Forward.  h0 may be NULL (zero initial state); ht may be NULL.
 // Returns 0 on success, -1 on bad arguments.
-int oracle_fwd(int kda, int B, int T, int H, int dk, int dv, const double* q,
+int oracle_fwd(int mode, int B, int T, int H, int dk, int dv, const double* q,
                const double* k, const double* v, const double* g,
                const double* beta, const double* h0, double* o, double* ht,
                int nthreads) {
   if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0) return -1;
   if (B == 0 || H == 0) return 0;
-  const Dims d{B, T, H, dk, dv, kda ? 1 : 0};
+  const Dims d{B, T, H, dk, dv, mode & 1, (mode >> 1) & 1};
   for_each_sequence(d, nthreads, [&](int b, int h) {
     std::vector<double> Hs((size_t)dk * dv, 0.0), Hn((size_t)dk * dv), P((size_t)dk * dv);
     std::vector<double> vp(dv);
@@ -135,7 +143,7 @@ int oracle_fwd(int kda, int B, int T, int H, int dk, int dv, const double* q,
 // Backward (reverse mode of oracle_fwd).  h0 and dht may be NULL (zero);
 // dh0 may be NULL (not wanted).  Keeps every H_t of one sequence in memory:
 // T*dk*dv doubles per worker thread; refuses (-2) above 2^26 doubles.
-int oracle_bwd(int kda, int B, int T, int H, int dk, int dv, const double* q,
+int oracle_bwd(int mode, int B, int T, int H, int dk, int dv, const double* q,
                const double* k, const double* v, const double* g,
                const double* beta, const double* h0, const double* dout,
                const double* dht, double* dq, double* dk_, double* dv_,
@@ -143,7 +151,7 @@ int oracle_bwd(int kda, int B, int T, int H, int dk, int dv, const double* q,
   if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0) return -1;
   if ((double)(T + 1) * dk * dv > (double)(1u << 26)) return -2;
   if (B == 0 || H == 0) return 0;
-  const Dims d{B, T, H, dk, dv, kda ? 1 : 0};
+  const Dims d{B, T, H, dk, dv, mode & 1, (mode >> 1) & 1};
   const size_t S = (size_t)dk * dv;
   for_each_sequence(d, nthreads, [&](int b, int h) {
     // Hall[t] = state after token t-1 (Hall[0] = h0); Hall[T] = final.
@@ -175,8 +183,9 @@ int oracle_bwd(int kda, int B, int T, int H, int dk, int dv, const double* q,
         for (int j = 0; j < dv; ++j) P[(size_t)i * dv + j] = a * Hprev[(size_t)i * dv + j];
       }
       for (int j = 0; j < dv; ++j) vp[j] = 0.0;
-      for (int i = 0; i < dk; ++i)
-        for (int j = 0; j < dv; ++j) vp[j] += P[(size_t)i * dv + j] * kt[i];
+      if (!d.no_delta)
+        for (int i = 0; i < dk; ++i)
+          for (int j = 0; j < dv; ++j) vp[j] += P[(size_t)i * dv + j] * kt[i];
       // o_t = H_t^T q_t
       for (int i = 0; i < dk; ++i) {
         double s = 0.0;
@@ -202,7 +211,7 @@ int oracle_bwd(int kda, int B, int T, int H, int dk, int dv, const double* q,
       for (int j = 0; j < dv; ++j) {
         dvt[j] = bt * du[j];
         db += du[j] * (vt[j] - vp[j]);
-        dvp[j] = -bt * du[j];
+        dvp[j] = d.no_delta ? 0.0 : -bt * du[j];  // without the delta rule vpred is not formed
       }
       dbeta[((size_t)b * T + t) * H + h] = db;
       // vpred = P^T k ;  dP = dH + k dvp^T

@@ -37,16 +37,18 @@ def _chunk_gates(g_chunk, dk, kda):
     return gam, Gam, mask
 
 
-def chunk_forward(Q, K, V, g, beta, H_in, kda):
+def chunk_forward(Q, K, V, g, beta, H_in, kda, delta=True):
+    """One chunk's output and exit state.  ``delta=False`` drops the delta
+    rule (the Mamba2 mixer): A = 0 and R = V, so U = diag(beta) V."""
     dk = K.shape[1]
     n = K.shape[0]
     gam, Gam, mask = _chunk_gates(g, dk, kda)
     E = np.exp(gam)
     F = np.exp(gam[-1][None, :] - gam)
     KKg = np.einsum("rd,jd,rjd->rj", K, K, Gam)
-    A = np.tril(beta[:, None] * KKg, -1)
+    A = np.tril(beta[:, None] * KKg, -1) if delta else np.zeros((n, n))
     L = np.eye(n) + A
-    R = V - (K * E) @ H_in
+    R = V - (K * E) @ H_in if delta else V
     U = np.linalg.solve(L, beta[:, None] * R)
     P = np.einsum("rd,jd,rjd->rj", Q, K, Gam) * mask
     O = (Q * E) @ H_in + P @ U
@@ -54,7 +56,7 @@ def chunk_forward(Q, K, V, g, beta, H_in, kda):
     return O, H_out
 
 
-def forward(q, k, v, g, beta, h0, chunk, kda=False):
+def forward(q, k, v, g, beta, h0, chunk, kda=False, delta=True):
     """Chunked forward over [B,T,H,*] inputs; returns (o, ht)."""
     B, T, H, dk = q.shape
     dv = v.shape[3]
@@ -66,12 +68,12 @@ def forward(q, k, v, g, beta, h0, chunk, kda=False):
             for c0 in range(0, T, chunk):
                 c1 = min(T, c0 + chunk)
                 o[b, c0:c1, h], S = chunk_forward(q[b, c0:c1, h], k[b, c0:c1, h], v[b, c0:c1, h],
-                                                  g[b, c0:c1, h], beta[b, c0:c1, h], S, kda)
+                                                  g[b, c0:c1, h], beta[b, c0:c1, h], S, kda, delta)
             ht[b, h] = S
     return o, ht
 
 
-def chunk_backward(Q, K, V, g, beta, H_in, dO, dH_out, kda):
+def chunk_backward(Q, K, V, g, beta, H_in, dO, dH_out, kda, delta=True):
     """Gradients of one chunk; returns (dQ, dK, dV, dg, dbeta, dH_in)."""
     dk = K.shape[1]
     n = K.shape[0]
@@ -80,9 +82,9 @@ def chunk_backward(Q, K, V, g, beta, H_in, dO, dH_out, kda):
     eC = np.exp(gam[-1])
     F = np.exp(gam[-1][None, :] - gam)
     KKg = np.einsum("rd,jd,rjd->rj", K, K, Gam)
-    A = np.tril(beta[:, None] * KKg, -1)
+    A = np.tril(beta[:, None] * KKg, -1) if delta else np.zeros((n, n))
     L = np.eye(n) + A
-    R = V - (K * E) @ H_in
+    R = V - (K * E) @ H_in if delta else V
     U = np.linalg.solve(L, beta[:, None] * R)
     P = np.einsum("rd,jd,rjd->rj", Q, K, Gam) * mask
 
@@ -111,15 +113,16 @@ def chunk_backward(Q, K, V, g, beta, H_in, dO, dH_out, kda):
     dgam += Q * dQP - K * dKP
     # U = L^-1 diag(beta) R
     dZ = np.linalg.solve(L.T, dU)
-    dA = np.tril(-dZ @ U.T, -1)
+    dA = np.tril(-dZ @ U.T, -1) if delta else np.zeros((n, n))
     dbeta = np.sum(dZ * R, axis=1) + np.sum(dA * KKg, axis=1)
     dR = beta[:, None] * dZ
     # R = V - (K*E) H_in
     dV = dR
-    dKE = -dR @ H_in.T
-    dK += E * dKE
-    dgam += K * E * dKE
-    dH_in -= (K * E).T @ dR
+    if delta:
+        dKE = -dR @ H_in.T
+        dK += E * dKE
+        dgam += K * E * dKE
+        dH_in -= (K * E).T @ dR
     # A[r,j] = beta_r sum_d k_rd k_jd Gam[r,j,d]   (j < r)
     dAt = dA * beta[:, None]
     X = np.einsum("rj,jd,rjd->rd", dAt, K, Gam)
@@ -133,7 +136,7 @@ def chunk_backward(Q, K, V, g, beta, H_in, dO, dH_out, kda):
     return dQ, dK, dV, dg, dbeta, dH_in
 
 
-def backward(q, k, v, g, beta, h0, do, dht, chunk, kda=False):
+def backward(q, k, v, g, beta, h0, do, dht, chunk, kda=False, delta=True):
     """Chunked backward (state recompute, then reverse chunk scan)."""
     B, T, H, dk = q.shape
     dv = v.shape[3]
@@ -149,7 +152,7 @@ def backward(q, k, v, g, beta, h0, do, dht, chunk, kda=False):
                 c1 = min(T, c0 + chunk)
                 states.append(S)
                 _, S = chunk_forward(q[b, c0:c1, h], k[b, c0:c1, h], v[b, c0:c1, h],
-                                     g[b, c0:c1, h], beta[b, c0:c1, h], S, kda)
+                                     g[b, c0:c1, h], beta[b, c0:c1, h], S, kda, delta)
             dS = np.zeros((dk, dv)) if dht is None else dht[b, h].astype(np.float64)
             for ci in reversed(range(len(starts))):
                 c0 = starts[ci]
@@ -157,7 +160,7 @@ def backward(q, k, v, g, beta, h0, do, dht, chunk, kda=False):
                 sl = slice(c0, c1)
                 dQ, dK, dV, dg, db, dS = chunk_backward(q[b, sl, h], k[b, sl, h], v[b, sl, h],
                                                         g[b, sl, h], beta[b, sl, h], states[ci],
-                                                        do[b, sl, h], dS, kda)
+                                                        do[b, sl, h], dS, kda, delta)
                 out["dq"][b, sl, h] = dQ
                 out["dk"][b, sl, h] = dK
                 out["dv"][b, sl, h] = dV

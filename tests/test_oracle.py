@@ -379,3 +379,89 @@ def test_hand_worked_examples(name):
     np.testing.assert_allclose(o.reshape(T, 2), np.array(c["o"]), rtol=0, atol=1e-12)
     np.testing.assert_allclose(ht.reshape(2, 2), np.array(c["ht"]), rtol=0, atol=1e-12)
 
+
+
+# ------------------------------------------------- the Mamba2 mixer (no delta rule)
+#
+# The same mixer list describes Mamba2 as the scalar-gated state that GDN
+# extends with the delta rule; without it the state only accumulates,
+# H_t = a_t H_{t-1} + beta_t k_t v_t^T, which unrolls into gated linear
+# attention for any keys (not only orthogonal ones).
+
+def _decayed_h0_term(q, g, h0, kda):
+    """exp(gamma_t) applied to h0, read out by q_t (per sequence, per token)."""
+    gam = np.cumsum(g, axis=1)
+    B, T, H, dk = q.shape
+    out = np.zeros((B, T, H, h0.shape[-1]))
+    for b in range(B):
+        for h in range(H):
+            for t in range(T):
+                a = np.exp(gam[b, t, h]) if kda else np.full(dk, np.exp(gam[b, t, h]))
+                out[b, t, h] = (a * q[b, t, h]) @ h0[b, h]
+    return out
+
+
+@pytest.mark.parametrize("kda", [False, True])
+def test_no_delta_is_gated_linear_attention(kda):
+    q, k, v, g, beta, h0 = rand_inputs(2, 9, 2, 5, 3, kda=kda, rng=np.random.default_rng(31))
+    o, ht = oracle.fwd(q, k, v, g, beta, h0, kda=kda, delta=False)
+    ref = gla_quadratic(q, k, v, g, beta, kda) + _decayed_h0_term(q, g, h0, kda)
+    np.testing.assert_allclose(o, ref, rtol=1e-12, atol=1e-12)
+    # final state in closed form: sum_j exp(gam_T - gam_j) beta_j k_j v_j^T + exp(gam_T) h0
+    gam = np.cumsum(g, axis=1)
+    for b in range(2):
+        for h in range(2):
+            last = gam[b, -1, h]
+            want = (np.exp(last) if kda else np.exp(last) * np.ones(5))[:, None] * h0[b, h]
+            for j in range(9):
+                dec = np.exp(last - gam[b, j, h]) if kda else np.exp(last - gam[b, j, h]) * np.ones(5)
+                want = want + np.outer(dec * k[b, j, h], beta[b, j, h] * v[b, j, h])
+            np.testing.assert_allclose(ht[b, h], want, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("kda", [False, True])
+def test_no_delta_gradients_match_finite_differences(kda):
+    B, T, H, dk, dv = 1, 6, 1, 3, 2
+    rng = np.random.default_rng(41 + kda)
+    q, k, v, g, beta, h0 = rand_inputs(B, T, H, dk, dv, kda=kda, rng=rng)
+    do = rng.standard_normal((B, T, H, dv))
+    dht = rng.standard_normal((B, H, dk, dv))
+    args = dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0)
+
+    def loss(a):
+        o, ht = oracle.fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], kda=kda, delta=False)
+        return float(np.sum(o * do) + np.sum(ht * dht))
+
+    grads = oracle.bwd(q, k, v, g, beta, h0, do, dht, kda=kda, delta=False)
+    names = {"q": "dq", "k": "dk", "v": "dv", "g": "dg", "beta": "dbeta", "h0": "dh0"}
+    eps = 1e-6
+    for name, gname in names.items():
+        x = args[name]
+        fd = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = x[idx]
+            x[idx] = old + eps
+            lp = loss(args)
+            x[idx] = old - eps
+            lm = loss(args)
+            x[idx] = old
+            fd[idx] = (lp - lm) / (2 * eps)
+        scale = max(1.0, np.max(np.abs(fd)))
+        assert np.max(np.abs(grads[gname] - fd)) / scale < 1e-6, name
+
+
+@pytest.mark.parametrize("chunk,T", [(4, 13), (16, 40)])
+def test_no_delta_chunked_form_equals_token_form(chunk, T):
+    q, k, v, g, beta, h0 = rand_inputs(2, T, 2, 6, 5, rng=np.random.default_rng(51))
+    do = np.random.default_rng(52).standard_normal(v.shape)
+    dht = np.random.default_rng(53).standard_normal(h0.shape)
+    o, ht = oracle.fwd(q, k, v, g, beta, h0, delta=False)
+    oc, htc = chunk_reference.forward(q, k, v, g, beta, h0, chunk, delta=False)
+    np.testing.assert_allclose(oc, o, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(htc, ht, rtol=1e-11, atol=1e-12)
+    ref = oracle.bwd(q, k, v, g, beta, h0, do, dht, delta=False)
+    got = chunk_reference.backward(q, k, v, g, beta, h0, do, dht, chunk, delta=False)
+    for n in ref:
+        np.testing.assert_allclose(got[n], ref[n], rtol=1e-10, atol=1e-11, err_msg=n)

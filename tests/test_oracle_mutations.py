@@ -42,6 +42,12 @@ MUTANTS = [
     ("state_grad_not_decayed",
      "dH[e] = a * dP[e];",
      "dH[e] = dP[e];"),
+    ("no_delta_still_predicts",
+     "  if (!d.no_delta)\n    for (int i = 0; i < dk; ++i)\n      for (int j = 0; j < dv; ++j) vp[j] += Pbuf",
+     "  if (true)\n    for (int i = 0; i < dk; ++i)\n      for (int j = 0; j < dv; ++j) vp[j] += Pbuf"),
+    ("no_delta_backward_keeps_prediction_grad",
+     "dvp[j] = d.no_delta ? 0.0 : -bt * du[j];",
+     "dvp[j] = -bt * du[j];"),
     ("kda_state_grad_drops_gate",
      "dH[(size_t)i * dv + j] = a * dP[(size_t)i * dv + j];",
      "dH[(size_t)i * dv + j] = dP[(size_t)i * dv + j];"),
