@@ -46,6 +46,7 @@ METRIC = "GDN/KDA mixer fwd+bwd tokens/s on 1 GB300; fraction of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
 WORKLOADS = {"gdn_300m": W.GDN_300M_BF16, "kda_300m": W.KDA_300M_BF16, "gdn_1b": W.GDN_1B_BF16_H0,
+             "mamba2_300m": W.MAMBA2_300M_BF16,
              "gdn_tiny": W.GDN_TINY_FP32, "gdn_decode": W.GDN_DECODE_BF16,
              "kda_decode": W.KDA_DECODE_BF16, "gdn_1m": W.GDN_1M_FWD_BF16}
 FWD_METRIC = "GDN long-context forward tokens/s on 1 GB300; fraction of roofline"
@@ -68,6 +69,11 @@ def algorithmic(w):
     sb = 4
     fwd_flops = 2 * C * (3 * dk + 2 * dv) + 6 * dk * dv + C * C / 3
     bwd_flops = 2 * C * (7 * dk + 5 * dv) + 14 * dk * dv + C * C / 3
+    if not getattr(w, "delta", True):
+        # without the delta rule: Q K^T, P U, Q H, the state update (forward);
+        # their recompute and the gradient products (backward); no solve
+        fwd_flops = 2 * C * (dk + dv) + 4 * dk * dv
+        bwd_flops = 2 * C * (2 * dk + 3 * dv) + 8 * dk * dv
     fwd_bytes = e * (2 * dk + 2 * dv) + sg + sb
     bwd_bytes = e * (2 * dk + 2 * dv) + sg + sb + e * (2 * dk + dv) + sg + sb
     return {"fwd_flops": fwd_flops, "bwd_flops": bwd_flops, "fwd_bytes": fwd_bytes,
@@ -101,7 +107,7 @@ def kernel_work(w, kernel):
     return 0.0, 0.0
 
 
-KERNEL_SOURCES = {"tc": "gdn_tc.cu", "simt": "gdn_simt.cu", "decode": "gdn_decode.cu"}
+KERNEL_SOURCES = {"tc": "gdn_tc.cu", "simt": "gdn_simt.cu", "decode": "gdn_decode.cu", "kda": "kda_tc.cu"}
 
 
 def recorded_traffic(kernel, workload_key):
@@ -218,9 +224,10 @@ def cpu_oracle_run(w, rows, seed=0):
     x = w.make(device="cpu", seed=seed, B=rows)
     nthreads = os.cpu_count() or 1
     t0 = time.perf_counter()
-    oracle.fwd(x.q, x.k, x.v, x.g, x.beta, x.h0, kda=w.kda, nthreads=nthreads)
+    oracle.fwd(x.q, x.k, x.v, x.g, x.beta, x.h0, kda=w.kda, nthreads=nthreads, delta=w.delta)
     if not w.fwd_only:
-        oracle.bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do, None, kda=w.kda, nthreads=nthreads)
+        oracle.bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do, None, kda=w.kda, nthreads=nthreads,
+                   delta=w.delta)
     return time.perf_counter() - t0, nthreads
 
 
@@ -287,15 +294,15 @@ def run_ours(args):
     dist_init(ws, "nccl")
     dev = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
-    fwd_s = gdn.kda_fwd_save if w.kda else gdn.gdn_fwd_save
-    bwd_s = gdn.kda_bwd_saved if w.kda else gdn.gdn_bwd_saved
-    fwd = gdn.kda_fwd if w.kda else gdn.gdn_fwd
-    bwd = gdn.kda_bwd if w.kda else gdn.gdn_bwd
+    fwd_s = getattr(gdn, f"{w.mixer}_fwd_save")
+    bwd_s = getattr(gdn, f"{w.mixer}_bwd_saved")
+    fwd = getattr(gdn, f"{w.mixer}_fwd")
+    bwd = getattr(gdn, f"{w.mixer}_bwd")
 
     x = w.make(device=dev, seed=rank)
     # the training step: the forward keeps the per-chunk entry states and
     # solve results in the saved context, the backward reads them
-    ctx = gdn.new_ctx(x.q, x.v, w.chunk, w.kda)
+    ctx = gdn.new_ctx(x.q, x.v, w.chunk, w.kda, w.delta)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -400,7 +407,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": {"workload": w.name, "op": ("kda" if w.kda else "gdn") + " fwd+bwd",
+            "config": {"workload": w.name, "op": w.mixer + " fwd+bwd",
                        "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
                        "tokens_per_step": tokens_step, "global_batch": w.B * ws,
                        "parallelism": f"replicas x{ws} (independent sequences)",
@@ -429,8 +436,8 @@ def run_e2e(gdn, w, x, ctx, dev, stream, K, warmup, ws):
     input pipeline is: step i+1's inputs are copied in on one stream and step
     i-1's results copied out on another while step i computes (two sets of
     device input buffers; each result's memory is held until its copy ends)."""
-    fwd_s = gdn.kda_fwd_save if w.kda else gdn.gdn_fwd_save
-    bwd_s = gdn.kda_bwd_saved if w.kda else gdn.gdn_bwd_saved
+    fwd_s = getattr(gdn, f"{w.mixer}_fwd_save")
+    bwd_s = getattr(gdn, f"{w.mixer}_bwd_saved")
     names = ["q", "k", "v", "g", "beta", "do"] + (["h0"] if x.h0 is not None else [])
     host_in = {n: getattr(x, n).cpu().pin_memory() for n in names}
     dev_in = [{n: torch.empty_like(getattr(x, n)) for n in names} for _ in range(2)]
@@ -757,7 +764,7 @@ def run_reference(args):
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": total * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "op": ("kda" if w.kda else "gdn") + " fwd+bwd",
+            "config": {"workload": w.name, "op": w.mixer + " fwd+bwd",
                        "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nthreads,
                              "kind": "oracle", "sample": sample},
@@ -786,8 +793,8 @@ def main():
     decode = wl.T == 1 and wl.fwd_only
     fwd_only = wl.fwd_only and not decode
     if args.steps is None:
-        # KDA: about 0.17 s a step; the 1M-token forward about 18 ms
-        ours = 5000 if decode else 40 if fwd_only else 5 if wl.kda else 1000
+        # the 1M-token forward takes about 18 ms a step
+        ours = 5000 if decode else 40 if fwd_only else 1000
         args.steps = 20 if args.impl == "reference" else ours
     if args.warmup is None:
         args.warmup = 3 if args.impl == "reference" or args.steps < 100 else 20

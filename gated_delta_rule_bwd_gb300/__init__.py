@@ -7,10 +7,12 @@ pointers and the current CUDA stream to the library.  Every step of the
 computation runs in the library's CUDA kernels; there is no other path.  If
 the library has not been built, every call raises.
 
-Names follow the ABI: ``gdn_fwd``, ``gdn_bwd``, ``kda_fwd``, ``kda_bwd``; the
-training pair with a saved context ``gdn_fwd_save`` / ``gdn_bwd_saved`` (and
-the KDA pair), whose forward keeps what the backward would recompute; and the
-token-recurrent ``gdn_decode`` / ``kda_decode`` for a few tokens per sequence.
+Names follow the ABI: ``gdn_fwd``, ``gdn_bwd``, ``kda_fwd``, ``kda_bwd`` and
+``mamba2_fwd``, ``mamba2_bwd`` (the scalar-gated state without the delta rule);
+the training pair with a saved context ``gdn_fwd_save`` / ``gdn_bwd_saved``
+(and the KDA and Mamba2 pairs), whose forward keeps what the backward would
+recompute; and the token-recurrent ``gdn_decode`` / ``kda_decode`` for a few
+tokens per sequence.
 Token tensors are ``[B, T, H, D]`` (fp32 or bf16, all the same dtype), ``g``
 is ``[B, T, H]`` (GDN) or ``[B, T, H, dk]`` (KDA) fp32, ``beta`` ``[B, T, H]``
 fp32, states ``[B, H, dk, dv]`` fp32.
@@ -45,6 +47,8 @@ _lib = None
 EXPORTS = ("gdn_fwd", "gdn_bwd", "kda_fwd", "kda_bwd", "gdn_fwd_workspace", "kda_fwd_workspace",
            "gdn_bwd_workspace", "kda_bwd_workspace", "gdn_ctx_bytes", "kda_ctx_bytes",
            "gdn_fwd_save", "kda_fwd_save", "gdn_bwd_saved", "kda_bwd_saved",
+           "mamba2_fwd", "mamba2_bwd", "mamba2_fwd_save", "mamba2_bwd_saved",
+           "mamba2_fwd_workspace", "mamba2_bwd_workspace", "mamba2_ctx_bytes",
            "gdn_decode", "kda_decode",
            "gdn_status_str", "gdn_last_cuda_error", "gdn_device_status", "gdn_uses_tensor_cores",
            "gdn_wait_selftest", "kda_uses_tensor_cores",
@@ -63,13 +67,16 @@ def lib():
             vp, sz, fp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p
             sp = ctypes.POINTER(GdnShape)
             for name in ("gdn_fwd_workspace", "kda_fwd_workspace", "gdn_bwd_workspace",
-                         "kda_bwd_workspace", "gdn_ctx_bytes", "kda_ctx_bytes"):
+                         "kda_bwd_workspace", "gdn_ctx_bytes", "kda_ctx_bytes",
+                         "mamba2_fwd_workspace", "mamba2_bwd_workspace", "mamba2_ctx_bytes"):
                 getattr(L, name).argtypes = [sp]
                 getattr(L, name).restype = sz
-            for name in ("gdn_fwd", "kda_fwd", "gdn_fwd_save", "kda_fwd_save"):
+            for name in ("gdn_fwd", "kda_fwd", "gdn_fwd_save", "kda_fwd_save", "mamba2_fwd",
+                         "mamba2_fwd_save"):
                 getattr(L, name).argtypes = [sp] + [vp] * 8 + [vp, sz, vp]
                 getattr(L, name).restype = ctypes.c_int
-            for name in ("gdn_bwd", "kda_bwd", "gdn_bwd_saved", "kda_bwd_saved"):
+            for name in ("gdn_bwd", "kda_bwd", "gdn_bwd_saved", "kda_bwd_saved", "mamba2_bwd",
+                         "mamba2_bwd_saved"):
                 getattr(L, name).argtypes = [sp] + [vp] * 14 + [vp, sz, vp]
                 getattr(L, name).restype = ctypes.c_int
             for name in ("gdn_decode", "kda_decode"):
@@ -142,23 +149,31 @@ def _stream(dev):
     return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
 
 
-def fwd_workspace_bytes(q, v, chunk=64, kda=False) -> int:
-    L = lib()
+def _mixer(kda, delta):
+    if kda and not delta:
+        raise GdnError("the per-key-dimension gate is only offered with the delta rule (KDA)")
+    return "kda" if kda else ("gdn" if delta else "mamba2")
+
+
+def _entry(kda, delta, name):
+    """The ABI function ``<mixer>_<name>``."""
+    return getattr(lib(), f"{_mixer(kda, delta)}_{name}")
+
+
+def fwd_workspace_bytes(q, v, chunk=64, kda=False, delta=True) -> int:
     s = make_shape(q, v, chunk)
-    return int((L.kda_fwd_workspace if kda else L.gdn_fwd_workspace)(ctypes.byref(s)))
+    return int(_entry(kda, delta, "fwd_workspace")(ctypes.byref(s)))
 
 
-def bwd_workspace_bytes(q, v, chunk=64, kda=False) -> int:
-    L = lib()
+def bwd_workspace_bytes(q, v, chunk=64, kda=False, delta=True) -> int:
     s = make_shape(q, v, chunk)
-    return int((L.kda_bwd_workspace if kda else L.gdn_bwd_workspace)(ctypes.byref(s)))
+    return int(_entry(kda, delta, "bwd_workspace")(ctypes.byref(s)))
 
 
-def ctx_bytes(q, v, chunk=64, kda=False) -> int:
+def ctx_bytes(q, v, chunk=64, kda=False, delta=True) -> int:
     """Bytes of the saved context of ``*_fwd_save`` / ``*_bwd_saved``."""
-    L = lib()
     s = make_shape(q, v, chunk)
-    return int((L.kda_ctx_bytes if kda else L.gdn_ctx_bytes)(ctypes.byref(s)))
+    return int(_entry(kda, delta, "ctx_bytes")(ctypes.byref(s)))
 
 
 def _workspace(need, given, device):
@@ -174,7 +189,7 @@ def uses_tensor_cores(q, v, chunk=64, kda=False) -> bool:
 
 
 def _fwd(kda, q, k, v, g, beta, h0=None, chunk=64, output_final_state=True, out=None,
-         workspace=None, ctx=None):
+         workspace=None, ctx=None, delta=True):
     B, T, H, dk = q.shape
     dv = v.shape[3]
     _validate(q, k, v, g, beta, kda, [("h0", (h0, (B, H, dk, dv), torch.float32))])
@@ -182,12 +197,12 @@ def _fwd(kda, q, k, v, g, beta, h0=None, chunk=64, output_final_state=True, out=
     ht = (torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
           if output_final_state else None)
     if ctx is not None:
-        _check_ctx(ctx, ctx_bytes(q, v, chunk, kda), q.device)
+        _check_ctx(ctx, ctx_bytes(q, v, chunk, kda, delta), q.device)
         ws = ctx
-        fn = lib().kda_fwd_save if kda else lib().gdn_fwd_save
+        fn = _entry(kda, delta, "fwd_save")
     else:
-        ws = _workspace(fwd_workspace_bytes(q, v, chunk, kda), workspace, q.device)
-        fn = lib().kda_fwd if kda else lib().gdn_fwd
+        ws = _workspace(fwd_workspace_bytes(q, v, chunk, kda, delta), workspace, q.device)
+        fn = _entry(kda, delta, "fwd")
     s = make_shape(q, v, chunk)
     _check(fn(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
               _ptr(ht), _ptr(ws), ws.numel(), _stream(q.device)))
@@ -202,7 +217,7 @@ def _check_ctx(ctx, need, device):
 
 
 def _bwd(kda, q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, workspace=None,
-         ctx=None):
+         ctx=None, delta=True):
     B, T, H, dk = q.shape
     dv = v.shape[3]
     _validate(q, k, v, g, beta, kda, [("h0", (h0, (B, H, dk, dv), torch.float32)),
@@ -212,12 +227,12 @@ def _bwd(kda, q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, works
     dq, dk_, dv_, dg, dbeta = e(q), e(k), e(v), e(g), e(beta)
     dh0 = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device) if want_dh0 else None
     if ctx is not None:
-        _check_ctx(ctx, ctx_bytes(q, v, chunk, kda), q.device)
+        _check_ctx(ctx, ctx_bytes(q, v, chunk, kda, delta), q.device)
         ws = ctx
-        fn = lib().kda_bwd_saved if kda else lib().gdn_bwd_saved
+        fn = _entry(kda, delta, "bwd_saved")
     else:
-        ws = _workspace(bwd_workspace_bytes(q, v, chunk, kda), workspace, q.device)
-        fn = lib().kda_bwd if kda else lib().gdn_bwd
+        ws = _workspace(bwd_workspace_bytes(q, v, chunk, kda, delta), workspace, q.device)
+        fn = _entry(kda, delta, "bwd")
     s = make_shape(q, v, chunk)
     _check(fn(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(do),
               _ptr(dht), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(dbeta), _ptr(dh0),
@@ -247,9 +262,10 @@ def kda_bwd(q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, workspa
     return _bwd(True, q, k, v, g, beta, h0, do, dht, chunk, want_dh0, workspace)
 
 
-def new_ctx(q, v, chunk=64, kda=False):
+def new_ctx(q, v, chunk=64, kda=False, delta=True):
     """An uninitialised saved-context buffer for ``q``/``v``'s shape."""
-    return torch.empty(max(16, ctx_bytes(q, v, chunk, kda)), dtype=torch.uint8, device=q.device)
+    return torch.empty(max(16, ctx_bytes(q, v, chunk, kda, delta)), dtype=torch.uint8,
+                       device=q.device)
 
 
 def gdn_fwd_save(q, k, v, g, beta, h0=None, chunk=64, output_final_state=True, ctx=None):
@@ -276,6 +292,30 @@ def gdn_bwd_saved(q, k, v, g, beta, h0, do, ctx, dht=None, chunk=64, want_dh0=Tr
 def kda_bwd_saved(q, k, v, g, beta, h0, do, ctx, dht=None, chunk=64, want_dh0=True):
     """KDA backward reading the context ``kda_fwd_save`` left in ``ctx``."""
     return _bwd(True, q, k, v, g, beta, h0, do, dht, chunk, want_dh0, ctx=ctx)
+
+
+def mamba2_fwd(q, k, v, g, beta, h0=None, chunk=64, output_final_state=True, workspace=None):
+    """Mamba2 forward (``g`` is ``[B,T,H]``): the scalar-gated state without the
+    delta rule, ``H_t = exp(g_t) H_{t-1} + beta_t k_t v_t^T``.  Returns ``(o, ht)``."""
+    return _fwd(False, q, k, v, g, beta, h0, chunk, output_final_state, workspace=workspace,
+                delta=False)
+
+
+def mamba2_bwd(q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, workspace=None):
+    """Mamba2 backward.  Returns a dict ``dq, dk, dv, dg, dbeta, dh0``."""
+    return _bwd(False, q, k, v, g, beta, h0, do, dht, chunk, want_dh0, workspace, delta=False)
+
+
+def mamba2_fwd_save(q, k, v, g, beta, h0=None, chunk=64, output_final_state=True, ctx=None):
+    """Mamba2 forward that also leaves the saved context for ``mamba2_bwd_saved``."""
+    ctx = new_ctx(q, v, chunk, delta=False) if ctx is None else ctx
+    o, ht = _fwd(False, q, k, v, g, beta, h0, chunk, output_final_state, ctx=ctx, delta=False)
+    return o, ht, ctx
+
+
+def mamba2_bwd_saved(q, k, v, g, beta, h0, do, ctx, dht=None, chunk=64, want_dh0=True):
+    """Mamba2 backward reading the context ``mamba2_fwd_save`` left in ``ctx``."""
+    return _bwd(False, q, k, v, g, beta, h0, do, dht, chunk, want_dh0, ctx=ctx, delta=False)
 
 
 def _decode(kda, q, k, v, g, beta, state=None, inplace=True, chunk=64):
@@ -350,11 +390,11 @@ class GatedDeltaRule(torch.autograd.Function):
     recomputing them."""
 
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, h0, chunk, kda, save_context):
-        saved = new_ctx(q, v, chunk, kda) if save_context else None
-        o, ht = _fwd(kda, q, k, v, g, beta, h0, chunk, True, ctx=saved)
+    def forward(ctx, q, k, v, g, beta, h0, chunk, kda, save_context, delta=True):
+        saved = new_ctx(q, v, chunk, kda, delta) if save_context else None
+        o, ht = _fwd(kda, q, k, v, g, beta, h0, chunk, True, ctx=saved, delta=delta)
         ctx.save_for_backward(q, k, v, g, beta, h0)
-        ctx.chunk, ctx.kda, ctx.saved = chunk, kda, saved
+        ctx.chunk, ctx.kda, ctx.saved, ctx.delta = chunk, kda, saved, delta
         return o, ht
 
     @staticmethod
@@ -362,13 +402,16 @@ class GatedDeltaRule(torch.autograd.Function):
         q, k, v, g, beta, h0 = ctx.saved_tensors
         gr = _bwd(ctx.kda, q, k, v, g, beta, h0, do.contiguous(),
                   None if dht is None else dht.contiguous(), ctx.chunk, h0 is not None,
-                  ctx=ctx.saved)
+                  ctx=ctx.saved, delta=ctx.delta)
         ctx.saved = None
         return (gr["dq"], gr["dk"], gr["dv"], gr["dg"], gr["dbeta"], gr["dh0"], None, None,
-                None)
+                None, None)
 
 
-def gated_delta_rule(q, k, v, g, beta, h0=None, chunk=64, kda=False, save_context=True):
+def gated_delta_rule(q, k, v, g, beta, h0=None, chunk=64, kda=False, save_context=True,
+                     delta=True):
     """Differentiable mixer: returns ``(o, final_state)``.  ``save_context``
-    trades ``ctx_bytes`` of device memory per call for a faster backward."""
-    return GatedDeltaRule.apply(q, k, v, g, beta, h0, chunk, kda, save_context)
+    trades ``ctx_bytes`` of device memory per call for a faster backward;
+    ``delta=False`` selects the Mamba2 mixer (no delta rule, scalar gate)."""
+    _mixer(kda, delta)
+    return GatedDeltaRule.apply(q, k, v, g, beta, h0, chunk, kda, save_context, delta)

@@ -26,7 +26,7 @@ int fail_cuda(cudaError_t e) {
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Validates the shape; fills the size fields of a Problem.
-int check_shape(const gdn_shape* s, bool kda, gdn::Problem* p) {
+int check_shape(const gdn_shape* s, bool kda, gdn::Problem* p, bool no_delta = false) {
   if (!s) return GDN_ERR_ARG;
   if (s->dtype != GDN_F32 && s->dtype != GDN_BF16) return GDN_ERR_DTYPE;
   if (s->B < 0 || s->T < 0 || s->H < 0) return GDN_ERR_SHAPE;
@@ -41,6 +41,7 @@ int check_shape(const gdn_shape* s, bool kda, gdn::Problem* p) {
   p->C = s->chunk;
   p->N = (s->T + s->chunk - 1) / s->chunk;
   p->kda = kda;
+  p->no_delta = no_delta;
   p->bf16 = s->dtype == GDN_BF16;
   return GDN_OK;
 }
@@ -80,9 +81,9 @@ cudaError_t copy_state_or_zero(float* dst, const float* src, const gdn::Problem&
 
 int run_fwd(const gdn_shape* shape, bool kda, const void* q, const void* k, const void* v,
             const float* g, const float* beta, const float* h0, void* o, float* ht, void* ws,
-            size_t ws_bytes, void* stream, bool save = false) {
+            size_t ws_bytes, void* stream, bool save = false, bool no_delta = false) {
   gdn::Problem p;
-  int rc = check_shape(shape, kda, &p);
+  int rc = check_shape(shape, kda, &p, no_delta);
   if (rc != GDN_OK) return rc;
   if (empty(p)) return GDN_OK;
   // token tensors of an empty sequence hold no data and may be NULL
@@ -108,9 +109,10 @@ int run_fwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
 int run_bwd(const gdn_shape* shape, bool kda, const void* q, const void* k, const void* v,
             const float* g, const float* beta, const float* h0, const void* do_,
             const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
-            float* dh0, void* ws, size_t ws_bytes, void* stream, bool saved = false) {
+            float* dh0, void* ws, size_t ws_bytes, void* stream, bool saved = false,
+            bool no_delta = false) {
   gdn::Problem p;
-  int rc = check_shape(shape, kda, &p);
+  int rc = check_shape(shape, kda, &p, no_delta);
   if (rc != GDN_OK) return rc;
   if (empty(p)) return GDN_OK;
   if (p.T > 0 && (!q || !k || !v || !g || !beta || !do_ || !dq || !dk || !dv || !dg || !dbeta))
@@ -156,15 +158,15 @@ int run_decode(const gdn_shape* shape, bool kda, const void* q, const void* k, c
   return e == cudaSuccess ? GDN_OK : fail_cuda(e);
 }
 
-size_t query_ws(const gdn_shape* shape, bool kda, bool bwd) {
+size_t query_ws(const gdn_shape* shape, bool kda, bool bwd, bool no_delta = false) {
   gdn::Problem p;
-  if (check_shape(shape, kda, &p) != GDN_OK) return 0;
+  if (check_shape(shape, kda, &p, no_delta) != GDN_OK) return 0;
   return bwd ? bwd_ws(p) : fwd_ws(p);
 }
 
-size_t query_ctx(const gdn_shape* shape, bool kda) {
+size_t query_ctx(const gdn_shape* shape, bool kda, bool no_delta = false) {
   gdn::Problem p;
-  if (check_shape(shape, kda, &p) != GDN_OK) return 0;
+  if (check_shape(shape, kda, &p, no_delta) != GDN_OK) return 0;
   return ctx_bytes(p);
 }
 
@@ -312,6 +314,38 @@ int kda_decode(const gdn_shape* shape, const void* q, const void* k, const void*
                const float* g, const float* beta, const float* h0, void* o, float* ht,
                void* stream) {
   return run_decode(shape, true, q, k, v, g, beta, h0, o, ht, stream);
+}
+
+size_t mamba2_fwd_workspace(const gdn_shape* shape) { return query_ws(shape, false, false, true); }
+size_t mamba2_bwd_workspace(const gdn_shape* shape) { return query_ws(shape, false, true, true); }
+size_t mamba2_ctx_bytes(const gdn_shape* shape) { return query_ctx(shape, false, true); }
+
+int mamba2_fwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
+               const float* g, const float* beta, const float* h0, void* o, float* ht, void* ws,
+               size_t ws_bytes, void* stream) {
+  return run_fwd(shape, false, q, k, v, g, beta, h0, o, ht, ws, ws_bytes, stream, false, true);
+}
+
+int mamba2_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
+               const float* g, const float* beta, const float* h0, const void* do_,
+               const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+               float* dh0, void* ws, size_t ws_bytes, void* stream) {
+  return run_bwd(shape, false, q, k, v, g, beta, h0, do_, dht, dq, dk, dv, dg, dbeta, dh0, ws,
+                 ws_bytes, stream, false, true);
+}
+
+int mamba2_fwd_save(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                    const float* g, const float* beta, const float* h0, void* o, float* ht,
+                    void* ctx, size_t ctx_bytes, void* stream) {
+  return run_fwd(shape, false, q, k, v, g, beta, h0, o, ht, ctx, ctx_bytes, stream, true, true);
+}
+
+int mamba2_bwd_saved(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                     const float* g, const float* beta, const float* h0, const void* do_,
+                     const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                     float* dh0, void* ctx, size_t ctx_bytes, void* stream) {
+  return run_bwd(shape, false, q, k, v, g, beta, h0, do_, dht, dq, dk, dv, dg, dbeta, dh0, ctx,
+                 ctx_bytes, stream, true, true);
 }
 
 const char* gdn_status_str(int status) {

@@ -13,6 +13,7 @@ namespace gdn {
 struct Problem {
   int B, T, H, dk, dv, C, N;  // N = ceil(T / C) chunks per sequence
   bool kda, bf16;
+  bool no_delta;  // the Mamba2 mixer: the state only accumulates beta k v^T (no delta rule)
   const void *q, *k, *v, *do_;
   const float *g, *beta, *h0, *dht;
   void *o, *dq, *dk_, *dv_;

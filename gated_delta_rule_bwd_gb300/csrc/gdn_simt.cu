@@ -258,19 +258,20 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(SimtArgs a) {
       Rs[i] = (r < n && c < nv) ? ldf(v + tok(p, b, t0 + r, h, p.dv) + v0 + c) : 0.f;
     }
     load_chunk_keys<TIn, KDA>(p, b, h, t0, n, Ks, Qs, gm, bt, E, F);
-    // decayed K K^T (strict lower, beta applied in the solve) and masked Q K^T
+    // decayed K K^T (strict lower, beta applied in the solve; zero without the
+    // delta rule) and masked Q K^T
     for (int i = threadIdx.x; i < C * C; i += kThreads) {
       const int r = i / C, j = i % C;
       float av = 0.f, pv = 0.f;
       if (j <= r) {
-        if (j < r) av = decayed_dot<KDA>(Ks, Ks, gm, r, j, dk);
+        if (j < r && !p.no_delta) av = decayed_dot<KDA>(Ks, Ks, gm, r, j, dk);
         pv = decayed_dot<KDA>(Qs, Ks, gm, r, j, dk);
       }
       As[r * lc + j] = av;
       Ps[r * lc + j] = pv;
     }
-    // R = V - (K o E) H_in
-    for (int i = threadIdx.x; i < C * dvs; i += kThreads) {
+    // R = V - (K o E) H_in  (R = V without the delta rule)
+    for (int i = threadIdx.x; i < C * dvs && !p.no_delta; i += kThreads) {
       const int r = i / dvs, c = i % dvs;
       float s = 0.f;
       if (KDA) {
@@ -392,13 +393,13 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(SimtArgs a) {
       const int r = i / C, j = i % C;
       float mv = 0.f, pv = 0.f;
       if (j <= r) {
-        if (j < r) mv = decayed_dot<KDA>(Ks, Ks, gm, r, j, dk);
+        if (j < r && !p.no_delta) mv = decayed_dot<KDA>(Ks, Ks, gm, r, j, dk);
         pv = decayed_dot<KDA>(Qs, Ks, gm, r, j, dk);
       }
       Ms[r * lc + j] = mv;
       Ps[r * lc + j] = pv;
     }
-    for (int i = threadIdx.x; i < C * dvs; i += kThreads) {
+    for (int i = threadIdx.x; i < C * dvs && !p.no_delta; i += kThreads) {
       const int r = i / dvs, c = i % dvs;
       float s = 0.f;
       if (KDA) {
@@ -436,7 +437,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(SimtArgs a) {
       float dp = 0.f, da = 0.f;
       if (j <= r) {
         for (int c = 0; c < nv; ++c) dp += Os[r * dvs + c] * Us[j * dvs + c];
-        if (j < r) {
+        if (j < r && !p.no_delta) {
           for (int c = 0; c < nv; ++c) da -= Zs[r * dvs + c] * Us[j * dvs + c];
         }
       }
@@ -481,6 +482,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(SimtArgs a) {
           udh += Us[r * dvs + c] * dHs[d * dvs + c];
           drh += Zs[r * dvs + c] * hdc;
         }
+        if (p.no_delta) drh = 0.f;  // R holds no state term
         float dqp = 0.f, dkp = 0.f, x = 0.f, y = 0.f;
         const float gr = KDA ? gm[r * lk + d] : gm[r];
         for (int j = 0; j <= r; ++j) {
@@ -520,16 +522,19 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(SimtArgs a) {
     }
     __syncthreads();
     // dH_in = diag(exp(gamma_last)) dH_out + (Q o E)^T dO - (K o E)^T dR
+    // (without the delta rule R holds no state term: no dR part)
+    const float kr = p.no_delta ? 0.f : 1.f;
     for (int i = threadIdx.x; i < dk * nv; i += kThreads) {
       const int d = i / nv, c = i % nv;
       float s = 0.f, ec;
       if (KDA) {
         for (int r = 0; r < C; ++r)
-          s += expf(gm[r * lk + d]) * (Qs[r * lk + d] * Os[r * dvs + c] - Ks[r * lk + d] * Zs[r * dvs + c]);
+          s += expf(gm[r * lk + d]) *
+               (Qs[r * lk + d] * Os[r * dvs + c] - kr * Ks[r * lk + d] * Zs[r * dvs + c]);
         ec = expf(gm[(C - 1) * lk + d]);
       } else {
         for (int r = 0; r < C; ++r)
-          s += E[r] * (Qs[r * lk + d] * Os[r * dvs + c] - Ks[r * lk + d] * Zs[r * dvs + c]);
+          s += E[r] * (Qs[r * lk + d] * Os[r * dvs + c] - kr * Ks[r * lk + d] * Zs[r * dvs + c]);
         ec = E[C - 1];
       }
       dHs[d * dvs + c] = ec * dHs[d * dvs + c] + s;

@@ -208,6 +208,7 @@ __device__ __forceinline__ void decay_row(float (&v)[n], const GateView& G, int 
   }
 }
 
+template <bool NoDelta>
 __global__ void __launch_bounds__(FT, 1)
 gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -259,13 +260,14 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   auto load_kq = [&](int ci) {
     const int st = ci & 1;
     unsigned char* dst = sm + kF_KQ + st * 32768;
-    mbar_arrive_expect_tx(&bar_kq[st], 32768 + 8192);
+    mbar_arrive_expect_tx(&bar_kq[st], 32768 + (NoDelta ? 0 : 8192));
     const int t0 = (c0 + ci) * C;
     tma_load_4d(dst + 0, &tm_k, &bar_kq[st], 0, h, t0, b);
     tma_load_4d(dst + 8192, &tm_q, &bar_kq[st], 0, h, t0, b);
     tma_load_4d(dst + 16384, &tm_k, &bar_kq[st], 64, h, t0, b);
     tma_load_4d(dst + 24576, &tm_q, &bar_kq[st], 64, h, t0, b);
-    bulk_load(sm + kF_TR + st * 8192, p.tiles + ((size_t)bh * p.N + c0 + ci) * 8192, 8192, &bar_kq[st]);
+    if (!NoDelta)
+      bulk_load(sm + kF_TR + st * 8192, p.tiles + ((size_t)bh * p.N + c0 + ci) * 8192, 8192, &bar_kq[st]);
     cnt[st] += 1;
   };
   auto load_v = [&](int ci) {
@@ -321,7 +323,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ok = group_and(kBarChain, kGroup, mbar_wait(bar_pd, ci & 1) && !*abort_flag);
       if (!ok) break;
       tc_fence_after();
-      {
+      if (!NoDelta) {
         // W^T (TMEM) -> W tile, MN-major: row d holds W[0..63][d]
         float w[32];
         tmem_ld32(tmem + lane_base + kTmW + half * 32, w);
@@ -360,9 +362,10 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const uint32_t st_kq = smem_u32(sm + kF_KQ + s * 32768);
       const uint32_t tmU = kTmU0 + 64 * s;
       if (gt == 0) {
-        // MMA3b: U^T += -G W^T (A: G K-major M=c K=d; B: W MN-major N=r K=d)
+        // MMA3b: U^T += -G W^T (A: G K-major M=c K=d; B: W MN-major N=r K=d);
+        // without the delta rule U = diag(beta) V holds no state term
         const uint32_t id3 = idesc_bf16(128, 64, false, true, true);
-        for (int ks = 0; ks < 8; ++ks)
+        for (int ks = 0; ks < (NoDelta ? 0 : 8); ++ks)
           mma_bf16(tmem + tmU, sw128_desc(smem_u32(sm + kF_G) + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024),
                    sw128_desc(smem_u32(sm + kF_W) + ks * 2048, 16384, 1024), id3, has_v || ks > 0);
         // MMA4a: O = (eQ) G^T  (M=64: A = eQ rows r, K=d; B = G tile rows c, K=d)
@@ -529,7 +532,17 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
           const int off = sw_row_off(r0 + 32 * rr, c8);
-          const uint4 raw = *reinterpret_cast<const uint4*>(sm + kF_TR + s * 8192 + off);
+          uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+          if (NoDelta) {
+            // T = I: the row's diagonal element, if it falls in this column chunk
+            const int rw = r0 + 32 * rr;
+            if ((rw >> 3) == c8) {
+              __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&raw);
+              e[rw & 7] = __float2bfloat16_rn(1.f);
+            }
+          } else {
+            raw = *reinterpret_cast<const uint4*>(sm + kF_TR + s * 8192 + off);
+          }
           const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
           uint4 o1, o0;
           uint32_t* w1 = reinterpret_cast<uint32_t*>(&o1);
@@ -582,7 +595,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (pt == 0) {
         // MMA2: W^T = K^T T'^T  (A: K tile MN-major, M=d; B: T' K-major, N=r)
         const uint32_t id2 = idesc_bf16(128, 64, true, false);
-        for (int ks = 0; ks < 4; ++ks)
+        for (int ks = 0; ks < (NoDelta ? 0 : 4); ++ks)
           mma_bf16(tmem + kTmW, sw128_desc(st_kq + ks * 2048, 16384, 1024),
                    sw128_desc(smem_u32(sm + kF_T1) + ks * 32, 16, 1024), id2, ks > 0);
         // MMA3a: U^T = V^T T''^T  (A: V tile MN-major, M=c; B: T'' K-major, N=r)
@@ -841,6 +854,7 @@ struct BwdParams {
   int B, T, H, N;
 };
 
+template <bool NoDelta>
 __global__ void __launch_bounds__(BT, 1)
 gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -946,7 +960,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // been read for the last time: V after the dv/dZ epilogue, K, dO, G_in and
   // T once the last products are done, Q after the q . dq sums.  The whole
   // chunk's byte count is announced with the first of them.
-  constexpr uint32_t kChunkBytes = 8 * 8192 + 32768 + 8192;
+  constexpr uint32_t kChunkBytes = 8 * 8192 + 32768 + (NoDelta ? 0 : 8192);
   int inflight = -1;   // thread 0: chunk whose tiles are requested but not yet waited for
   int parts = 0;       // thread 0: how many of its three load groups are issued
   auto issue_v = [&](int cn) {
@@ -965,7 +979,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tma_load_4d(sm + kB_ZO + 8192, &tm_do, bar_load, 0, h, tn, b);
     tma_load_4d(sm + kB_ZO + 24576, &tm_do, bar_load, 64, h, tn, b);
     bulk_load(sm + kB_GI, p.states + ((size_t)bh * p.N + cn) * 32768, 32768, bar_load);
-    bulk_load(sm + kB_T, p.tiles + ((size_t)bh * p.N + cn) * 8192, 8192, bar_load);
+    if (!NoDelta) bulk_load(sm + kB_T, p.tiles + ((size_t)bh * p.N + cn) * 8192, 8192, bar_load);
   };
   auto issue_q = [&](int cn) {
     const int tn = cn * C;
@@ -994,13 +1008,21 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       tma_prefetch_l2_4d(&tm_v, 0, h, tp, b);
       tma_prefetch_l2_4d(&tm_v, 64, h, tp, b);
       bulk_prefetch_l2(p.states + ((size_t)bh * p.N + ci - 1) * 32768, 32768);
-      bulk_prefetch_l2(p.tiles + ((size_t)bh * p.N + ci - 1) * 8192, 8192);
+      if (!NoDelta) bulk_prefetch_l2(p.tiles + ((size_t)bh * p.N + ci - 1) * 8192, 8192);
     }
     ok = __syncthreads_and(mbar_wait(bar_load, load_phase));
     if (!ok) break;
     load_phase ^= 1;
     inflight = -1;
-    // ---- MMA1: [K;Q] K^T;  -G_in K^T;  dG K^T
+    if (NoDelta) {
+      // T = I (the tile slot is rewritten later in the chunk): thread tid writes
+      // the 16-byte chunk tid % 8 of row tid / 8
+      const int r = tid >> 3, c8 = tid & 7;
+      uint4 pk = make_uint4(0u, 0u, 0u, 0u);
+      if ((r >> 3) == c8) reinterpret_cast<__nv_bfloat16*>(&pk)[r & 7] = __float2bfloat16_rn(1.f);
+      *reinterpret_cast<uint4*>(sm + kB_T + sw_row_off(r, c8)) = pk;
+    }
+    // ---- MMA1: [K;Q] K^T;  -G_in K^T (not formed without the delta rule);  dG K^T
     if (tid == 0) {
       const uint32_t id = idesc_bf16(128, 64, false, false);
       const uint32_t idn = idesc_bf16(128, 64, false, false, true);
@@ -1008,8 +1030,9 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
         mma_bf16(tmem + kBtKQ, sw128_desc(sKQ + off, 16, 1024), sw128_desc(sKQ + off, 16, 1024), id,
                  ks > 0);
-        mma_bf16(tmem + kBtR, sw128_desc(sGI + off, 16, 1024), sw128_desc(sKQ + off, 16, 1024), idn,
-                 ks > 0);
+        if (!NoDelta)
+          mma_bf16(tmem + kBtR, sw128_desc(sGI + off, 16, 1024), sw128_desc(sKQ + off, 16, 1024), idn,
+                   ks > 0);
         mma_bf16(tmem + kBtX1, sw128_desc(sDG + off, 16, 1024), sw128_desc(sKQ + off, 16, 1024), id,
                  ks > 0);
       }
@@ -1045,7 +1068,8 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int r = cg * 16 + i;
-        a[i] = bt[r] * (tile_elem(sm + kB_V + (row >> 6) * 8192, r, row & 63) + ee[r] * a[i]);
+        const float kh = NoDelta ? 0.f : ee[r] * a[i];
+        a[i] = bt[r] * (tile_elem(sm + kB_V + (row >> 6) * 8192, r, row & 63) + kh);
       }
       store_chunks(sm + kB_X, row, cg * 2, a, 2);
       tmem_ld16(tmem + lb + kBtX1 + cg * 16, a);
@@ -1122,6 +1146,10 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       float z[16], rr[16];
       tmem_ld16(tmem + lb + kBtZ + cg * 16, z);
       tmem_ld16(tmem + lb + kBtR + cg * 16, rr);
+      if (NoDelta) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) rr[i] = 0.f;  // R = V
+      }
       const int half = row >> 6, cc = row & 63;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -1167,7 +1195,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tmem_ld16(tmem + lb + kBtKQ + cg * 16, kk);
         const float br = bt[r];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = -x[i];
+        for (int i = 0; i < 16; ++i) x[i] = NoDelta ? 0.f : -x[i];  // no A without the delta rule
         decay_row(x, GV, r, cg * 16, true, 1.f);   // x = dA o Gam
         float s2 = 0.f;
 #pragma unroll
@@ -1227,7 +1255,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         mma_bf16(tmem + kBtG3, sw128_desc(sZO + 8192 + ks * 2048, 16384, 1024),
                  sw128_desc(sKQ + 8192 + ks * 2048, 16384, 1024), idg, 1);
       const uint32_t idgn = idesc_bf16(128, 128, false, true, true);
-      for (int ks = 0; ks < 4; ++ks)
+      for (int ks = 0; ks < (NoDelta ? 0 : 4); ++ks)
         mma_bf16(tmem + kBtG3, sw128_desc(sX1 + ks * 32, 16, 1024), sw128_desc(sKQ + ks * 2048, 16384, 1024),
                  idgn, 1);
       // dQ^T = G_in^T (e dO)^T + K^T (dP o Gam)^T   [d x r], the two terms in
@@ -1246,16 +1274,17 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int ks = 0; ks < 8; ++ks)
         mma_bf16(tmem + kBtU, sw128_desc(sDG + ks * 2048, 16384, 1024), sw128_desc(sX2 + ks * 2048, 16384, 1024),
                  idmm, ks > 0);
-      for (int ks = 0; ks < 8; ++ks)
+      const int nd = NoDelta ? 0 : 1;  // the R- and A-terms vanish without the delta rule
+      for (int ks = 0; ks < 8 * nd; ++ks)
         mma_bf16(tmem + kBtU, sw128_desc(sGI + ks * 2048, 16384, 1024), sw128_desc(sX1 + ks * 2048, 16384, 1024),
                  idmmn, 1);
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16(tmem + kBtU, sw128_desc(sKQ + 8192 + ks * 2048, 16384, 1024),
                  sw128_desc(sDP + ks * 2048, 16384, 1024), idmm, 1);
-      for (int ks = 0; ks < 4; ++ks)
+      for (int ks = 0; ks < 4 * nd; ++ks)
         mma_bf16(tmem + kBtU, sw128_desc(sKQ + ks * 2048, 16384, 1024), sw128_desc(sM + ks * 32, 16, 1024),
                  idq, 1);
-      for (int ks = 0; ks < 4; ++ks)
+      for (int ks = 0; ks < 4 * nd; ++ks)
         mma_bf16(tmem + kBtU, sw128_desc(sKQ + ks * 2048, 16384, 1024), sw128_desc(sM + ks * 2048, 16384, 1024),
                  idmm, 1);
       mma_commit(bar_mma);
@@ -1443,12 +1472,14 @@ cudaError_t launch_fwd(const Problem& p, cudaStream_t s, const unsigned char* ti
   if ((e = make_token_map(&mo, f.want_out ? p.o : p.q, p)) != cudaSuccess) return e;  // unused without output
   FwdParams fp{p.g, p.beta, f.h0, f.want_out ? static_cast<__nv_bfloat16*>(p.o) : nullptr,
                f.ht, f.states, tiles, p.B, p.T, p.H, p.N, f.seg_chunks, f.v_zero, f.h0_identity};
-  e = cudaFuncSetAttribute(gdn_tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  // the Mamba2 mixer (no delta rule) is a separate instance: T = I, no W products
+  auto kern = p.no_delta ? gdn_tc_fwd_kernel<true> : gdn_tc_fwd_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int nseg = f.seg_chunks ? (p.N + f.seg_chunks - 1) / f.seg_chunks : 1;
   prof_before(s);
-  e = launch_overlapped(gdn_tc_fwd_kernel, (unsigned)((size_t)p.B * p.H * nseg), FT, kSmemBytes,
-                        s, mq, mk, mv, mo, fp);
+  e = launch_overlapped(kern, (unsigned)((size_t)p.B * p.H * nseg), FT, kSmemBytes, s, mq, mk, mv,
+                        mo, fp);
   prof_after(s, f.kernel_id);
   return e;
 }
@@ -1516,6 +1547,7 @@ gdn_tc_combine_kernel(const float* M, const float* Nl, const float* h0, float* H
 // multiply the number of busy SMs by at least four; segments are at least 32
 // chunks long.
 int fwd_seg_chunks(const Problem& p) {
+  if (p.no_delta) return 0;  // not segmented without the delta rule
   const long seqs = (long)p.B * p.H;
   const int sms = sm_count();
   if (seqs <= 0 || p.N < 128) return 0;
@@ -1567,7 +1599,7 @@ cudaError_t tc_fwd(const Problem& p, cudaStream_t s, bool save) {
   unsigned char* ws = static_cast<unsigned char*>(p.ws);
   __nv_bfloat16* states = save ? reinterpret_cast<__nv_bfloat16*>(ws) : nullptr;
   unsigned char* tiles = save ? ws + states_bytes(p) : ws;
-  cudaError_t e = launch_solve(p, s, tiles);
+  cudaError_t e = p.no_delta ? cudaSuccess : launch_solve(p, s, tiles);  // T = I without the delta rule
   if (e != cudaSuccess) return e;
   const int sc = fwd_seg_chunks(p);
   if (!sc) {
@@ -1619,7 +1651,7 @@ cudaError_t tc_bwd(const Problem& p, cudaStream_t s, bool saved) {
   unsigned char* tiles = ws + states_bytes(p);
   cudaError_t e;
   if (!saved) {
-    if ((e = launch_solve(p, s, tiles)) != cudaSuccess) return e;
+    if (!p.no_delta && (e = launch_solve(p, s, tiles)) != cudaSuccess) return e;
     FwdLaunch st;
     st.states = states;
     st.h0 = p.h0;
@@ -1638,12 +1670,12 @@ cudaError_t tc_bwd(const Problem& p, cudaStream_t s, bool saved) {
                reinterpret_cast<const unsigned char*>(states), static_cast<__nv_bfloat16*>(p.dq),
                static_cast<__nv_bfloat16*>(p.dk_), static_cast<__nv_bfloat16*>(p.dv_), p.dg, p.dbeta,
                p.dh0, tiles, p.B, p.T, p.H, p.N};
-  e = cudaFuncSetAttribute(gdn_tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kBwdSmemBytes);
+  auto kern = p.no_delta ? gdn_tc_bwd_kernel<true> : gdn_tc_bwd_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemBytes);
   if (e != cudaSuccess) return e;
   prof_before(s);
-  e = launch_overlapped(gdn_tc_bwd_kernel, (unsigned)(p.B * p.H), BT, kBwdSmemBytes, s, mq, mk, mv,
-                        mdo, mdq, mdk, mdv, bp);
+  e = launch_overlapped(kern, (unsigned)(p.B * p.H), BT, kBwdSmemBytes, s, mq, mk, mv, mdo, mdq, mdk,
+                        mdv, bp);
   prof_after(s, kTcBwd);
   return e;
 }

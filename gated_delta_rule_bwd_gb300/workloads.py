@@ -26,6 +26,11 @@ class Workload:
     g_mean: float = 2.0
     h0_std: float | None = None
     fwd_only: bool = False
+    delta: bool = True  # False: the Mamba2 mixer (scalar gate, no delta rule)
+
+    @property
+    def mixer(self) -> str:
+        return "kda" if self.kda else ("gdn" if self.delta else "mamba2")
 
     @property
     def tokens(self) -> int:
@@ -44,6 +49,10 @@ GDN_TINY_FP32 = Workload("gdn_tiny_fp32_B1_T64_H2_d16_C16", 1, 64, 2, 16, 16, 16
 GDN_300M_BF16 = Workload("gdn_300m_bf16_B16_T2048_H8_d128_C64", 16, 2048, 8, 128, 128, 64)
 KDA_300M_BF16 = Workload("kda_300m_bf16_B16_T2048_H8_d128_C64", 16, 2048, 8, 128, 128, 64,
                          kda=True)
+# The Mamba2 mixer of the same model list (the scalar-gated state GDN extends
+# with the delta rule) at the 300M pre-training shape.
+MAMBA2_300M_BF16 = Workload("mamba2_300m_bf16_B16_T2048_H8_d128_C64", 16, 2048, 8, 128, 128, 64,
+                            delta=False)
 GDN_1B_BF16_H0 = Workload("gdn_1b_bf16_h0_B8_T2048_H16_d128_C64", 8, 2048, 16, 128, 128, 64,
                           h0_std=0.02)
 GDN_1M_FWD_BF16 = Workload("gdn_1m_fwd_bf16_B1_T1048576_H16_d128_C64", 1, 1 << 20, 16, 128,
@@ -57,6 +66,6 @@ GDN_DECODE_BF16 = Workload("gdn_decode_bf16_B256_T1_H16_d128", 256, 1, 16, 128, 
 KDA_DECODE_BF16 = Workload("kda_decode_bf16_B256_T1_H16_d128", 256, 1, 16, 128, 128, 64,
                            kda=True, h0_std=0.02, fwd_only=True)
 
-ALL = [GDN_TINY_FP32, GDN_300M_BF16, KDA_300M_BF16, GDN_1B_BF16_H0, GDN_1M_FWD_BF16,
-       GDN_DECODE_BF16, KDA_DECODE_BF16]
+ALL = [GDN_TINY_FP32, GDN_300M_BF16, KDA_300M_BF16, MAMBA2_300M_BF16, GDN_1B_BF16_H0,
+       GDN_1M_FWD_BF16, GDN_DECODE_BF16, KDA_DECODE_BF16]
 BY_NAME = {w.name: w for w in ALL}

@@ -186,6 +186,38 @@ GDN_API int kda_bwd_saved(const gdn_shape* shape, const void* q, const void* k, 
                           const float* dht, void* dq, void* dk, void* dv, float* dg,
                           float* dbeta, float* dh0, void* ctx, size_t ctx_bytes, void* stream);
 
+/* Mamba2: the mixer that GDN extends with the delta rule.  The Primus blog's
+ * section "How hybrid models are defined in Primus" lists it beside GDN and
+ * KDA as a selective state-space model with one scalar forget gate per head,
+ * and describes GDN as that model plus the delta rule; without the delta
+ * rule the state only accumulates:
+ *
+ *   H_t = exp(g_t) H_{t-1} + beta_t k_t v_t^T,    o_t = H_t^T q_t,
+ *
+ * with k, v and q in the roles of the state-space model's input projection,
+ * input and read-out, and beta_t the per-token write strength (its step
+ * size).  Arguments, layouts (g is [B,T,H]), workspace rules, saved context,
+ * errors and kernel selection are those of the gdn_* calls of the same name;
+ * the chunkwise form needs no triangular solve (T = I). */
+GDN_API size_t mamba2_fwd_workspace(const gdn_shape* shape);
+GDN_API size_t mamba2_bwd_workspace(const gdn_shape* shape);
+GDN_API size_t mamba2_ctx_bytes(const gdn_shape* shape);
+GDN_API int mamba2_fwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, const float* h0, void* o, float* ht,
+                       void* ws, size_t ws_bytes, void* stream);
+GDN_API int mamba2_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, const float* h0, const void* do_,
+                       const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                       float* dh0, void* ws, size_t ws_bytes, void* stream);
+GDN_API int mamba2_fwd_save(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                            const float* g, const float* beta, const float* h0, void* o,
+                            float* ht, void* ctx, size_t ctx_bytes, void* stream);
+GDN_API int mamba2_bwd_saved(const gdn_shape* shape, const void* q, const void* k,
+                             const void* v, const float* g, const float* beta, const float* h0,
+                             const void* do_, const float* dht, void* dq, void* dk, void* dv,
+                             float* dg, float* dbeta, float* dh0, void* ctx, size_t ctx_bytes,
+                             void* stream);
+
 /* Decode: the forward recurrence run token by token, for a few tokens per
  * sequence (T = 1 in single-token generation).  Same arguments, layout and
  * results as *_fwd (o and the final state), with no workspace: each (b, h)

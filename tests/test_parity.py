@@ -42,10 +42,10 @@ def check(name, got, ref, fp32):
     return r
 
 
-def run_gpu(x, chunk, fwd_only=False):
+def run_gpu(x, chunk, fwd_only=False, delta=True):
     d = x.to("cuda")
-    fwd = gdn.kda_fwd if x.kda else gdn.gdn_fwd
-    bwd = gdn.kda_bwd if x.kda else gdn.gdn_bwd
+    fwd = gdn.kda_fwd if x.kda else (gdn.gdn_fwd if delta else gdn.mamba2_fwd)
+    bwd = gdn.kda_bwd if x.kda else (gdn.gdn_bwd if delta else gdn.mamba2_bwd)
     o, ht = fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, chunk=chunk)
     gr = None
     if not fwd_only:
@@ -54,7 +54,7 @@ def run_gpu(x, chunk, fwd_only=False):
     return o, ht, gr
 
 
-def compare(x, o, ht, gr, fp32, pairs=None):
+def compare(x, o, ht, gr, fp32, pairs=None, delta=True):
     """Compare GPU results for the sequences in ``pairs`` (default: all)."""
     if pairs is not None:
         sub = x.select(pairs)
@@ -63,11 +63,12 @@ def compare(x, o, ht, gr, fp32, pairs=None):
     else:
         sub = x
         pick_tok = pick_st = lambda t: t
-    o_ref, ht_ref = oracle.fwd(sub.q, sub.k, sub.v, sub.g, sub.beta, sub.h0, kda=x.kda)
+    o_ref, ht_ref = oracle.fwd(sub.q, sub.k, sub.v, sub.g, sub.beta, sub.h0, kda=x.kda, delta=delta)
     errs = {"o": check("o", pick_tok(o.cpu()), o_ref, fp32),
             "ht": check("ht", pick_st(ht.cpu()), ht_ref, fp32)}
     if gr is not None:
-        ref = oracle.bwd(sub.q, sub.k, sub.v, sub.g, sub.beta, sub.h0, sub.do, sub.dht, kda=x.kda)
+        ref = oracle.bwd(sub.q, sub.k, sub.v, sub.g, sub.beta, sub.h0, sub.do, sub.dht, kda=x.kda,
+                         delta=delta)
         for n in ("dq", "dk", "dv", "dg", "dbeta"):
             errs[n] = check(n, pick_tok(gr[n].cpu()), ref[n], fp32)
         errs["dh0"] = check("dh0", pick_st(gr["dh0"].cpu()), ref["dh0"], fp32)
@@ -212,6 +213,65 @@ def test_kda_mixed_paths_in_one_call():
     assert torch.equal(o2, o) and torch.equal(ht2, ht)
     for n in gr:
         assert torch.equal(gr2[n], gr[n]), n
+
+
+# ----------------------------------------------------------- Mamba2 (no delta rule)
+
+MAMBA2 = [
+    # B, T, H, dk, dv, chunk, dtype
+    (1, 64, 2, 16, 16, 16, "f32"),        # CUDA-core path
+    (2, 100, 3, 32, 48, 32, "f32"),       # ragged tail, dk != dv
+    (2, 200, 2, 128, 128, 64, "bf16"),    # tensor-core path, 8-token tail
+    (1, 37, 3, 128, 128, 64, "bf16"),     # tensor-core path, T < chunk
+]
+
+
+@pytest.mark.parametrize("case", MAMBA2, ids=lambda c: "x".join(map(str, c)))
+def test_mamba2_matches_oracle(case):
+    B, T, H, dk, dv, chunk, dtype = case
+    x = make_inputs(B, T, H, dk, dv, dtype=dtype, h0_std=0.3, with_dht=True, seed=23)
+    o, ht, gr = run_gpu(x, chunk, delta=False)
+    compare(x, o, ht, gr, fp32=dtype == "f32", delta=False)
+
+
+@pytest.mark.parametrize("g_mean", [2.0, -1.0, -3.0])
+def test_mamba2_training_shape_and_fast_gates(g_mean):
+    """The 300M training shape (sampled sequences) at the workloads' gates, and
+    a short case at fast-decaying gates; the saved-context pair gives the same
+    bits as the recomputing one."""
+    if g_mean == 2.0:
+        x = make_inputs(16, 2048, 8, 128, 128, dtype="bf16", seed=24)
+        pairs = [(0, 0), (15, 7), (5, 3)]
+    else:
+        x = make_inputs(1, 256, 2, 128, 128, dtype="bf16", g_mean=g_mean, h0_std=0.3,
+                        with_dht=True, seed=25)
+        pairs = None
+    o, ht, gr = run_gpu(x, 64, delta=False)
+    compare(x, o, ht, gr, fp32=False, pairs=pairs, delta=False)
+    d = x.to("cuda")
+    o2, ht2, ctx = gdn.mamba2_fwd_save(d.q, d.k, d.v, d.g, d.beta, d.h0)
+    gr2 = gdn.mamba2_bwd_saved(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, ctx, d.dht)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, o) and torch.equal(ht2, ht)
+    for n in gr:
+        assert torch.equal(gr2[n], gr[n]), n
+
+
+def test_mamba2_autograd_and_no_solve():
+    """The differentiable wrapper with delta=False, and the tensor-core
+    Mamba2 step launches no triangular solve."""
+    x = make_inputs(1, 128, 2, 128, 128, dtype="bf16", h0_std=0.1, seed=26).to("cuda")
+    with gdn.KernelTimer() as t:
+        gdn.mamba2_fwd(x.q, x.k, x.v, x.g, x.beta, x.h0)
+        gdn.mamba2_bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do)
+        torch.cuda.synchronize()
+    names = [n for n, _ in t.records()]
+    assert names == ["tc_fwd", "tc_states", "tc_bwd"], names
+    q, k, v = (t.clone().requires_grad_() for t in (x.q, x.k, x.v))
+    o, ht = gdn.gated_delta_rule(q, k, v, x.g, x.beta, x.h0, delta=False)
+    (o.float() * x.do.float()).sum().backward()
+    ref = gdn.mamba2_bwd(x.q, x.k, x.v, x.g, x.beta, x.h0, x.do)
+    assert torch.equal(q.grad, ref["dq"]) and torch.equal(v.grad, ref["dv"])
 
 
 # ----------------------------------------------------------- saved context
