@@ -52,6 +52,9 @@ EXPORTS = ("gdn_fwd", "gdn_bwd", "kda_fwd", "kda_bwd", "gdn_fwd_workspace", "kda
            "gdn_decode", "kda_decode",
            "gdn_status_str", "gdn_last_cuda_error", "gdn_device_status", "gdn_uses_tensor_cores",
            "gdn_wait_selftest", "kda_uses_tensor_cores",
+           "gdn_varlen_workspace", "kda_varlen_workspace", "mamba2_varlen_workspace",
+           "gdn_fwd_varlen", "gdn_bwd_varlen", "kda_fwd_varlen", "kda_bwd_varlen",
+           "mamba2_fwd_varlen", "mamba2_bwd_varlen",
            "gdn_profile_begin", "gdn_profile_end", "gdn_profile_read", "gdn_kernel_name")
 
 
@@ -88,6 +91,15 @@ def lib():
             L.gdn_last_cuda_error.restype = ctypes.c_int
             L.gdn_device_status.argtypes = []
             L.gdn_device_status.restype = ctypes.c_int
+            for name in ("gdn_varlen_workspace", "kda_varlen_workspace", "mamba2_varlen_workspace"):
+                getattr(L, name).argtypes = [sp, ctypes.c_int, ctypes.c_int]
+                getattr(L, name).restype = sz
+            for name in ("gdn_fwd_varlen", "kda_fwd_varlen", "mamba2_fwd_varlen"):
+                getattr(L, name).argtypes = [sp, vp, ctypes.c_int] + [vp] * 8 + [vp, sz, vp]
+                getattr(L, name).restype = ctypes.c_int
+            for name in ("gdn_bwd_varlen", "kda_bwd_varlen", "mamba2_bwd_varlen"):
+                getattr(L, name).argtypes = [sp, vp, ctypes.c_int] + [vp] * 14 + [vp, sz, vp]
+                getattr(L, name).restype = ctypes.c_int
             L.gdn_wait_selftest.argtypes = [ctypes.c_int, vp]
             L.gdn_wait_selftest.restype = ctypes.c_int
             for name in ("gdn_uses_tensor_cores", "kda_uses_tensor_cores"):
@@ -316,6 +328,90 @@ def mamba2_fwd_save(q, k, v, g, beta, h0=None, chunk=64, output_final_state=True
 def mamba2_bwd_saved(q, k, v, g, beta, h0, do, ctx, dht=None, chunk=64, want_dh0=True):
     """Mamba2 backward reading the context ``mamba2_fwd_save`` left in ``ctx``."""
     return _bwd(False, q, k, v, g, beta, h0, do, dht, chunk, want_dh0, ctx=ctx, delta=False)
+
+
+# ------------------------------------------------------------------ packed sequences
+
+def varlen_workspace_bytes(q, v, nseq, chunk=64, kda=False, delta=True, backward=False) -> int:
+    """Workspace bytes of a packed-sequence call (``*_varlen_workspace``)."""
+    s = make_shape(q, v, chunk)
+    return int(_entry(kda, delta, "varlen_workspace")(ctypes.byref(s), int(nseq), int(backward)))
+
+
+def _check_cu(cu_seqlens, q):
+    if (not isinstance(cu_seqlens, torch.Tensor) or cu_seqlens.dtype != torch.int32
+            or cu_seqlens.device != q.device or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1
+            or not cu_seqlens.is_contiguous()):
+        raise GdnError("cu_seqlens must be a contiguous 1-D int32 tensor on the inputs' device")
+    if q.shape[0] != 1:
+        raise GdnError("packed sequences: the token tensors must be [1, T, H, D]")
+    return cu_seqlens.numel() - 1
+
+
+def _fwd_varlen(kda, delta, q, k, v, g, beta, cu_seqlens, h0, chunk, workspace):
+    nseq = _check_cu(cu_seqlens, q)
+    _, T, H, dk = q.shape
+    dv = v.shape[3]
+    _validate(q, k, v, g, beta, kda, [("h0", (h0, (nseq, H, dk, dv), torch.float32))])
+    o = torch.empty((1, T, H, dv), dtype=q.dtype, device=q.device)
+    ht = torch.empty((nseq, H, dk, dv), dtype=torch.float32, device=q.device)
+    ws = _workspace(varlen_workspace_bytes(q, v, nseq, chunk, kda, delta), workspace, q.device)
+    s = make_shape(q, v, chunk)
+    _check(_entry(kda, delta, "fwd_varlen")(ctypes.byref(s), _ptr(cu_seqlens), nseq, _ptr(q), _ptr(k),
+                                            _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(ht),
+                                            _ptr(ws), ws.numel(), _stream(q.device)))
+    return o, ht
+
+
+def _bwd_varlen(kda, delta, q, k, v, g, beta, cu_seqlens, h0, do, dht, chunk, workspace):
+    nseq = _check_cu(cu_seqlens, q)
+    _, T, H, dk = q.shape
+    dv = v.shape[3]
+    _validate(q, k, v, g, beta, kda, [("h0", (h0, (nseq, H, dk, dv), torch.float32)),
+                                      ("do", (do, (1, T, H, dv), q.dtype)),
+                                      ("dht", (dht, (nseq, H, dk, dv), torch.float32))])
+    e = lambda x: torch.empty_like(x)
+    dq, dk_, dv_, dg, dbeta = e(q), e(k), e(v), e(g), e(beta)
+    dh0 = torch.empty((nseq, H, dk, dv), dtype=torch.float32, device=q.device)
+    ws = _workspace(varlen_workspace_bytes(q, v, nseq, chunk, kda, delta, True), workspace, q.device)
+    s = make_shape(q, v, chunk)
+    _check(_entry(kda, delta, "bwd_varlen")(ctypes.byref(s), _ptr(cu_seqlens), nseq, _ptr(q), _ptr(k),
+                                            _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(do), _ptr(dht),
+                                            _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(dbeta),
+                                            _ptr(dh0), _ptr(ws), ws.numel(), _stream(q.device)))
+    return {"dq": dq, "dk": dk_, "dv": dv_, "dg": dg, "dbeta": dbeta, "dh0": dh0}
+
+
+def gdn_fwd_varlen(q, k, v, g, beta, cu_seqlens, h0=None, chunk=64, workspace=None):
+    """GDN forward over packed sequences: token tensors ``[1, T, H, D]``,
+    ``cu_seqlens`` an int32 device tensor of ``nseq + 1`` offsets, ``h0`` and the
+    returned ``ht`` ``[nseq, H, dk, dv]``.  Returns ``(o, ht)``."""
+    return _fwd_varlen(False, True, q, k, v, g, beta, cu_seqlens, h0, chunk, workspace)
+
+
+def gdn_bwd_varlen(q, k, v, g, beta, cu_seqlens, h0, do, dht=None, chunk=64, workspace=None):
+    """GDN backward over packed sequences; returns the dict of ``gdn_bwd``."""
+    return _bwd_varlen(False, True, q, k, v, g, beta, cu_seqlens, h0, do, dht, chunk, workspace)
+
+
+def kda_fwd_varlen(q, k, v, g, beta, cu_seqlens, h0=None, chunk=64, workspace=None):
+    """KDA forward over packed sequences (``g`` is ``[1, T, H, dk]``)."""
+    return _fwd_varlen(True, True, q, k, v, g, beta, cu_seqlens, h0, chunk, workspace)
+
+
+def kda_bwd_varlen(q, k, v, g, beta, cu_seqlens, h0, do, dht=None, chunk=64, workspace=None):
+    """KDA backward over packed sequences."""
+    return _bwd_varlen(True, True, q, k, v, g, beta, cu_seqlens, h0, do, dht, chunk, workspace)
+
+
+def mamba2_fwd_varlen(q, k, v, g, beta, cu_seqlens, h0=None, chunk=64, workspace=None):
+    """Mamba2 forward over packed sequences."""
+    return _fwd_varlen(False, False, q, k, v, g, beta, cu_seqlens, h0, chunk, workspace)
+
+
+def mamba2_bwd_varlen(q, k, v, g, beta, cu_seqlens, h0, do, dht=None, chunk=64, workspace=None):
+    """Mamba2 backward over packed sequences."""
+    return _bwd_varlen(False, False, q, k, v, g, beta, cu_seqlens, h0, do, dht, chunk, workspace)
 
 
 def _decode(kda, q, k, v, g, beta, state=None, inplace=True, chunk=64):

@@ -46,7 +46,24 @@ int check_shape(const gdn_shape* s, bool kda, gdn::Problem* p, bool no_delta = f
   return GDN_OK;
 }
 
-bool empty(const gdn::Problem& p) { return p.B == 0 || p.H == 0; }
+bool empty(const gdn::Problem& p) { return gdn::num_seqs(p) == 0 || p.H == 0; }
+
+// Packed sequences: the chunk offsets sit in front of the mixer's workspace.
+size_t seq_prefix(const gdn::Problem& p) {
+  return p.cu_seqlens ? gdn::align_up((size_t)(p.nseq + 1) * sizeof(int), 256) : 0;
+}
+
+// Marks a problem as packed (B must be 1); the pointer is the caller's
+// device array of nseq + 1 token offsets.
+int set_packed(gdn::Problem* p, const int* cu_seqlens, int nseq) {
+  if (nseq < 0) return GDN_ERR_SHAPE;
+  if (p->B != 1) return GDN_ERR_SHAPE;
+  if (!cu_seqlens) return GDN_ERR_ARG;
+  if (((uintptr_t)cu_seqlens & 3u) != 0) return GDN_ERR_ALIGN;
+  p->cu_seqlens = cu_seqlens;
+  p->nseq = nseq;
+  return GDN_OK;
+}
 
 size_t fwd_ws(const gdn::Problem& p) {
   if (empty(p) || p.T == 0) return 0;
@@ -73,7 +90,7 @@ size_t ctx_bytes(const gdn::Problem& p) {
 // gradient of the (empty) token tensors is empty.
 cudaError_t copy_state_or_zero(float* dst, const float* src, const gdn::Problem& p,
                                cudaStream_t st) {
-  const size_t bytes = (size_t)p.B * p.H * p.dk * p.dv * sizeof(float);
+  const size_t bytes = (size_t)gdn::num_seqs(p) * p.H * p.dk * p.dv * sizeof(float);
   if (!dst) return cudaSuccess;
   if (src) return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st);
   return cudaMemsetAsync(dst, 0, bytes, st);
@@ -81,10 +98,12 @@ cudaError_t copy_state_or_zero(float* dst, const float* src, const gdn::Problem&
 
 int run_fwd(const gdn_shape* shape, bool kda, const void* q, const void* k, const void* v,
             const float* g, const float* beta, const float* h0, void* o, float* ht, void* ws,
-            size_t ws_bytes, void* stream, bool save = false, bool no_delta = false) {
+            size_t ws_bytes, void* stream, bool save = false, bool no_delta = false,
+            const int* cu_seqlens = nullptr, int nseq = -1) {
   gdn::Problem p;
   int rc = check_shape(shape, kda, &p, no_delta);
   if (rc != GDN_OK) return rc;
+  if (nseq >= 0 && (rc = set_packed(&p, cu_seqlens, nseq)) != GDN_OK) return rc;
   if (empty(p)) return GDN_OK;
   // token tensors of an empty sequence hold no data and may be NULL
   if (p.T > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_ARG;
@@ -96,10 +115,17 @@ int run_fwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
     cudaError_t e = copy_state_or_zero(ht, h0, p, st);
     return e == cudaSuccess ? GDN_OK : fail_cuda(e);
   }
-  const size_t need = save ? ctx_bytes(p) : fwd_ws(p);
+  const size_t pre = seq_prefix(p);
+  const size_t need = pre + (save ? ctx_bytes(p) : fwd_ws(p));
   if (need > 0 && (!ws || ws_bytes < need)) return GDN_ERR_WORKSPACE;
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.o = o; p.ht = ht;
-  p.ws = ws; p.ws_bytes = ws_bytes;
+  p.ws = static_cast<unsigned char*>(ws) + pre;
+  p.ws_bytes = ws_bytes - pre;
+  if (p.cu_seqlens) {
+    p.chunk_off = static_cast<int*>(ws);
+    cudaError_t e = gdn::setup_seqlens(p, static_cast<int*>(ws), st);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
   cudaError_t e = gdn::kda_tc_supported(p) ? gdn::kda_tc_fwd(p, st, save)
                   : gdn::tc_supported(p)     ? gdn::tc_fwd(p, st, save)
                                              : gdn::simt_fwd(p, st, save);
@@ -110,10 +136,11 @@ int run_bwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
             const float* g, const float* beta, const float* h0, const void* do_,
             const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
             float* dh0, void* ws, size_t ws_bytes, void* stream, bool saved = false,
-            bool no_delta = false) {
+            bool no_delta = false, const int* cu_seqlens = nullptr, int nseq = -1) {
   gdn::Problem p;
   int rc = check_shape(shape, kda, &p, no_delta);
   if (rc != GDN_OK) return rc;
+  if (nseq >= 0 && (rc = set_packed(&p, cu_seqlens, nseq)) != GDN_OK) return rc;
   if (empty(p)) return GDN_OK;
   if (p.T > 0 && (!q || !k || !v || !g || !beta || !do_ || !dq || !dk || !dv || !dg || !dbeta))
     return GDN_ERR_ARG;
@@ -125,11 +152,18 @@ int run_bwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
     cudaError_t e = copy_state_or_zero(dh0, dht, p, st);
     return e == cudaSuccess ? GDN_OK : fail_cuda(e);
   }
-  const size_t need = saved ? ctx_bytes(p) : bwd_ws(p);
+  const size_t pre = seq_prefix(p);
+  const size_t need = pre + (saved ? ctx_bytes(p) : bwd_ws(p));
   if (need > 0 && (!ws || ws_bytes < need)) return GDN_ERR_WORKSPACE;
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.do_ = do_; p.dht = dht;
   p.dq = dq; p.dk_ = dk; p.dv_ = dv; p.dg = dg; p.dbeta = dbeta; p.dh0 = dh0;
-  p.ws = ws; p.ws_bytes = ws_bytes;
+  p.ws = static_cast<unsigned char*>(ws) + pre;
+  p.ws_bytes = ws_bytes - pre;
+  if (p.cu_seqlens) {
+    p.chunk_off = static_cast<int*>(ws);
+    cudaError_t e = gdn::setup_seqlens(p, static_cast<int*>(ws), st);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
   cudaError_t e = gdn::kda_tc_supported(p) ? gdn::kda_tc_bwd(p, st, saved)
                   : gdn::tc_supported(p)     ? gdn::tc_bwd(p, st, saved)
                                              : gdn::simt_bwd(p, st, saved);
@@ -158,10 +192,13 @@ int run_decode(const gdn_shape* shape, bool kda, const void* q, const void* k, c
   return e == cudaSuccess ? GDN_OK : fail_cuda(e);
 }
 
-size_t query_ws(const gdn_shape* shape, bool kda, bool bwd, bool no_delta = false) {
+size_t query_ws(const gdn_shape* shape, bool kda, bool bwd, bool no_delta = false, int nseq = -1) {
   gdn::Problem p;
   if (check_shape(shape, kda, &p, no_delta) != GDN_OK) return 0;
-  return bwd ? bwd_ws(p) : fwd_ws(p);
+  static const int kAnyOffsets[1] = {0};  // only the size matters here
+  if (nseq >= 0 && set_packed(&p, kAnyOffsets, nseq) != GDN_OK) return 0;
+  if (empty(p) || p.T == 0) return 0;
+  return seq_prefix(p) + (bwd ? bwd_ws(p) : fwd_ws(p));
 }
 
 size_t query_ctx(const gdn_shape* shape, bool kda, bool no_delta = false) {
@@ -180,7 +217,7 @@ const char* kernel_name(int id) {
   static const char* names[kNumKernelIds] = {
       "simt_fwd", "simt_states", "simt_bwd", "simt_bwd_reduce",
       "tc_fwd", "tc_states", "tc_bwd", "tc_solve", "tc_fwd_segment", "tc_combine", "decode",
-      "kda_tc_prep", "kda_tc_fwd", "kda_tc_states", "kda_tc_bwd"};
+      "kda_tc_prep", "kda_tc_fwd", "kda_tc_states", "kda_tc_bwd", "seqlens_setup"};
   return (id >= 0 && id < kNumKernelIds) ? names[id] : "unknown";
 }
 
@@ -348,6 +385,39 @@ int mamba2_bwd_saved(const gdn_shape* shape, const void* q, const void* k, const
                  ctx_bytes, stream, true, true);
 }
 
+size_t gdn_varlen_workspace(const gdn_shape* shape, int nseq, int backward) {
+  return query_ws(shape, false, backward != 0, false, nseq);
+}
+size_t kda_varlen_workspace(const gdn_shape* shape, int nseq, int backward) {
+  return query_ws(shape, true, backward != 0, false, nseq);
+}
+size_t mamba2_varlen_workspace(const gdn_shape* shape, int nseq, int backward) {
+  return query_ws(shape, false, backward != 0, true, nseq);
+}
+
+#define GDN_VARLEN_PAIR(name, kda, nodelta)                                                        \
+  int name##_fwd_varlen(const gdn_shape* shape, const int* cu_seqlens, int nseq, const void* q,  \
+                        const void* k, const void* v, const float* g, const float* beta,         \
+                        const float* h0, void* o, float* ht, void* ws, size_t ws_bytes,          \
+                        void* stream) {                                                          \
+    if (nseq < 0) return GDN_ERR_SHAPE;                                                          \
+    return run_fwd(shape, kda, q, k, v, g, beta, h0, o, ht, ws, ws_bytes, stream, false,         \
+                   nodelta, cu_seqlens, nseq);                                                    \
+  }                                                                                              \
+  int name##_bwd_varlen(const gdn_shape* shape, const int* cu_seqlens, int nseq, const void* q,  \
+                        const void* k, const void* v, const float* g, const float* beta,         \
+                        const float* h0, const void* do_, const float* dht, void* dq, void* dk,  \
+                        void* dv, float* dg, float* dbeta, float* dh0, void* ws,                 \
+                        size_t ws_bytes, void* stream) {                                         \
+    if (nseq < 0) return GDN_ERR_SHAPE;                                                          \
+    return run_bwd(shape, kda, q, k, v, g, beta, h0, do_, dht, dq, dk, dv, dg, dbeta, dh0, ws,   \
+                   ws_bytes, stream, false, nodelta, cu_seqlens, nseq);                           \
+  }
+GDN_VARLEN_PAIR(gdn, false, false)
+GDN_VARLEN_PAIR(kda, true, false)
+GDN_VARLEN_PAIR(mamba2, false, true)
+#undef GDN_VARLEN_PAIR
+
 const char* gdn_status_str(int status) {
   switch (status) {
     case GDN_OK: return "GDN_OK";
@@ -358,6 +428,8 @@ const char* gdn_status_str(int status) {
     case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing or too small";
     case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA call failed (see gdn_last_cuda_error)";
     case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT: a device-side wait ran out";
+    case GDN_ERR_SEQLENS:
+      return "GDN_ERR_SEQLENS: cu_seqlens does not rise from 0 to T (packed sequences)";
     default: return "unknown gdn_status";
   }
 }

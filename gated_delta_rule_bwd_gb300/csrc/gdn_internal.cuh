@@ -20,9 +20,101 @@ struct Problem {
   float *ht, *dg, *dbeta, *dh0;
   void* ws;
   size_t ws_bytes;
+  // Packed variable-length sequences (B = 1, T = all tokens): sequence s is
+  // tokens [cu_seqlens[s], cu_seqlens[s+1]); nullptr for a batch of B rows of
+  // T tokens.  chunk_off (device, in the workspace) holds the first global
+  // chunk of each sequence, written by the set-up kernel.
+  const int* cu_seqlens;
+  int nseq;
+  const int* chunk_off;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Number of sequences (batch rows, or packed sequences).
+inline int num_seqs(const Problem& p) { return p.cu_seqlens ? p.nseq : p.B; }
+
+// Chunks of all sequences: exact for a batch, an upper bound for packed
+// sequences (sum of ceil(len / C) <= ceil(T / C) + nseq).
+inline long max_chunks(const Problem& p) {
+  return p.cu_seqlens ? (long)p.N + p.nseq : (long)p.B * p.N;
+}
+
+// Device view of the sequences of a call, shared by every kernel.  Tokens
+// live in [B, T, H, D] tensors; a sequence is addressed by its batch row b
+// and first token t0 within it, its length and chunk count, and the global
+// index of per-chunk records (T tiles, entry states), laid out
+// [chunk][head] for packed sequences and [sequence * H + head][chunk] for a
+// batch.
+struct Seqs {
+  const int* cu;     // packed: [nseq + 1] token offsets; nullptr: a batch
+  const int* choff;  // packed: [nseq + 1] chunk offsets
+  int T, N, H, C;    // batch: tokens and chunks per row; heads; chunk size
+
+  __host__ __device__ static Seqs of(const Problem& p) {
+    return Seqs{p.cu_seqlens, p.chunk_off, p.T, p.N, p.H, p.C};
+  }
+  // batch row, first token within it, length and chunks of sequence s
+  __device__ __forceinline__ void get(int s, int& b, int& t0, int& len, int& nch) const {
+    if (!cu) {
+      b = s, t0 = 0, len = T, nch = N;
+    } else {  // chunk counts from the offsets: all zero when cu_seqlens was invalid
+      b = 0, t0 = cu[s], len = cu[s + 1] - cu[s], nch = choff[s + 1] - choff[s];
+    }
+  }
+  // index of the per-chunk record of chunk ci of (sequence s, head h)
+  __device__ __forceinline__ size_t rec(int s, int h, int ci) const {
+    return cu ? (size_t)(choff[s] + ci) * H + h : ((size_t)s * H + h) * N + ci;
+  }
+  // the same with the mode fixed at compile time (kernels instantiated per mode)
+  template <bool Packed>
+  __device__ __forceinline__ void get_t(int s, int& b, int& t0, int& len, int& nch) const {
+    if constexpr (Packed) {
+      b = 0, t0 = cu[s], len = cu[s + 1] - cu[s], nch = choff[s + 1] - choff[s];
+    } else {
+      b = s, t0 = 0, len = T, nch = N;
+    }
+  }
+  template <bool Packed>
+  __device__ __forceinline__ size_t rec_t(int s, int h, int ci) const {
+    if constexpr (Packed) return (size_t)(choff[s] + ci) * H + h;
+    else return (size_t)(s * H + h) * N + ci;
+  }
+  // chunk-parallel kernels: the (sequence, head, chunk) of block x of a grid
+  // of max_chunks * H blocks; false for blocks past the last chunk
+  __device__ __forceinline__ bool chunk_of(long x, int nseq, int& s, int& h, int& ci) const {
+    if (!cu) {
+      const long bh = x / N;
+      ci = (int)(x % N), s = (int)(bh / H), h = (int)(bh % H);
+      return true;
+    }
+    const long gc = x / H;
+    h = (int)(x % H);
+    if (gc >= choff[nseq]) return false;
+    int lo = 0, hi = nseq - 1;  // the last s with choff[s] <= gc
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) / 2;
+      if (choff[mid] <= gc) lo = mid;
+      else hi = mid - 1;
+    }
+    s = lo, ci = (int)(gc - choff[lo]);
+    return true;
+  }
+};
+
+// Record index of chunk ci for a kernel whose block is bh = s * H + h (for a
+// batch simply bh * N + ci, N the chunks per sequence).
+template <bool Packed>
+__device__ __forceinline__ size_t rec_bh(const Seqs& q, int N, int bh, int s, int h, int ci) {
+  if constexpr (Packed) return q.template rec_t<true>(s, h, ci);
+  else return (size_t)bh * N + ci;
+}
+
+// Packed sequences: checks cu_seqlens (non-decreasing from 0 to T) and writes
+// the chunk offsets; an invalid offset array is recorded as
+// GDN_ERR_SEQLENS in the device status word and leaves every chunk count at
+// zero, so that the kernels that follow do nothing.
+cudaError_t setup_seqlens(const Problem& p, int* chunk_off, cudaStream_t s);
 
 // CUDA-core fp32 kernels (any dk, dv <= 128; chunk 16/32/64).
 size_t simt_bwd_workspace(const Problem& p);
@@ -74,7 +166,8 @@ enum KernelId {
   kKdaFwd = 12,
   kKdaStates = 13,
   kKdaBwd = 14,
-  kNumKernelIds = 15
+  kSeqSetup = 15,
+  kNumKernelIds = 16
 };
 const char* kernel_name(int id);
 

@@ -228,8 +228,11 @@ template <typename TIn, bool KDA>
 __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(SimtArgs a) {
   extern __shared__ float sm[];
   const Problem& p = a.p;
-  const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
+  const int bh = blockIdx.x, sq = bh / p.H, h = bh % p.H;
   if (a.only && !a.only[bh]) return;
+  const Seqs seqs = Seqs::of(p);
+  int b, tb, len, nch;
+  seqs.get(sq, b, tb, len, nch);
   const int dk = p.dk, C = p.C, dvs = a.dvs, lk = dk + 1, lc = C + 1;
   const int v0 = blockIdx.y * dvs, nv = min(dvs, p.dv - v0);
   const FwdSmem L = fwd_smem(dk, dvs, C, KDA);
@@ -243,11 +246,11 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(SimtArgs a) {
     const int d = i / dvs, c = i % dvs;
     Hs[i] = (p.h0 && c < nv) ? p.h0[((size_t)bh * dk + d) * p.dv + v0 + c] : 0.f;
   }
-  for (int ci = 0; ci < p.N; ++ci) {
-    const int t0 = ci * C, n = min(C, p.T - t0);
+  for (int ci = 0; ci < nch; ++ci) {
+    const int t0 = tb + ci * C, n = min(C, len - ci * C);  // t0: token within batch row b
     __syncthreads();
     if (a.states) {
-      float* st = a.states + ((size_t)bh * p.N + ci) * dk * p.dv;
+      float* st = a.states + seqs.rec(sq, h, ci) * dk * p.dv;
       for (int i = threadIdx.x; i < dk * nv; i += kThreads) {
         const int d = i / nv, c = i % nv;
         st[(size_t)d * p.dv + v0 + c] = Hs[d * dvs + c];
@@ -346,8 +349,11 @@ template <typename TIn, bool KDA>
 __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(SimtArgs a) {
   extern __shared__ float sm[];
   const Problem& p = a.p;
-  const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H, split = blockIdx.y;
+  const int bh = blockIdx.x, sq = bh / p.H, h = bh % p.H, split = blockIdx.y;
   if (a.only && !a.only[bh]) return;
+  const Seqs seqs = Seqs::of(p);
+  int b, tb, len, nch;
+  seqs.get(sq, b, tb, len, nch);
   const int dk = p.dk, C = p.C, dvs = a.dvs, lk = dk + 1, lc = C + 1;
   const int v0 = split * dvs, nv = min(dvs, p.dv - v0);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -371,11 +377,11 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(SimtArgs a) {
     const int d = i / dvs, c = i % dvs;
     dHs[i] = (p.dht && c < nv) ? p.dht[((size_t)bh * dk + d) * p.dv + v0 + c] : 0.f;
   }
-  for (int ci = p.N - 1; ci >= 0; --ci) {
-    const int t0 = ci * C, n = min(C, p.T - t0);
+  for (int ci = nch - 1; ci >= 0; --ci) {
+    const int t0 = tb + ci * C, n = min(C, len - ci * C);  // t0: token within batch row b
     __syncthreads();
     {
-      const float* st = a.states + ((size_t)bh * p.N + ci) * dk * p.dv;
+      const float* st = a.states + seqs.rec(sq, h, ci) * dk * p.dv;
       for (int i = threadIdx.x; i < dk * dvs; i += kThreads) {
         const int d = i / dvs, c = i % dvs;
         Hs[i] = c < nv ? st[(size_t)d * p.dv + v0 + c] : 0.f;
@@ -554,9 +560,13 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(SimtArgs a) {
 template <typename TIn, bool KDA>
 __global__ void __launch_bounds__(kThreads) simt_bwd_reduce_kernel(SimtArgs a) {
   const Problem& p = a.p;
-  const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H, ci = blockIdx.y;
-  if (a.only && !a.only[bh]) return;
-  const int dk = p.dk, t0 = ci * p.C, n = min(p.C, p.T - t0);
+  const Seqs seqs = Seqs::of(p);
+  int sq, h, ci, b, tb, len, nch;
+  if (!seqs.chunk_of(blockIdx.x, p.nseq, sq, h, ci)) return;  // past the last packed chunk
+  if (a.only && !a.only[sq * p.H + h]) return;
+  seqs.get(sq, b, tb, len, nch);
+  if (ci >= nch) return;
+  const int dk = p.dk, t0 = tb + ci * p.C, n = min(p.C, len - ci * p.C);
   const PartLayout PL = part_layout(p, a.nsplit);
   const size_t tokh = (size_t)p.B * p.T * p.H;
   const int GD = KDA ? dk : 1;
@@ -608,7 +618,7 @@ int pick_dvs_bwd(const Problem& p) {
 }
 
 size_t states_bytes(const Problem& p) {
-  return align_up((size_t)p.B * p.H * p.N * p.dk * p.dv * sizeof(float), 256);
+  return align_up((size_t)max_chunks(p) * p.H * p.dk * p.dv * sizeof(float), 256);
 }
 
 template <typename TIn, bool KDA>
@@ -627,7 +637,7 @@ cudaError_t launch_fwd(const Problem& p, cudaStream_t s, float* states, bool wan
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   prof_before(s);
-  kern<<<dim3(p.B * p.H, a.nsplit), kThreads, smem, s>>>(a);
+  kern<<<dim3(num_seqs(p) * p.H, a.nsplit), kThreads, smem, s>>>(a);
   prof_after(s, kid);
   return cudaGetLastError();
 }
@@ -651,12 +661,12 @@ cudaError_t launch_bwd(const Problem& p, cudaStream_t s, bool saved, const int* 
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   prof_before(s);
-  kern<<<dim3(p.B * p.H, a.nsplit), kThreads, smem, s>>>(a);
+  kern<<<dim3(num_seqs(p) * p.H, a.nsplit), kThreads, smem, s>>>(a);
   prof_after(s, kSimtBwd);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_before(s);
-  simt_bwd_reduce_kernel<TIn, KDA><<<dim3(p.B * p.H, p.N), kThreads, 0, s>>>(a);
+  simt_bwd_reduce_kernel<TIn, KDA><<<(unsigned)(max_chunks(p) * p.H), kThreads, 0, s>>>(a);
   prof_after(s, kSimtBwdReduce);
   return cudaGetLastError();
 }

@@ -95,6 +95,7 @@ struct FwdParams {
                           // ([B*H][N][32 KB], shared-memory layout)
   const unsigned char* tiles;  // T of every chunk ([B*H][N][8 KB], from the solve kernel)
   int B, T, H, N;
+  Seqs sq;  // the call's sequences (a batch, or packed sequences)
   // Segments (long sequences): with seg_chunks > 0 each CTA runs seg_chunks
   // chunks of one sequence (CTA = sequence * nseg + segment); h0 and ht are
   // then per segment ([B*H*nseg][dk][dv]).
@@ -167,10 +168,9 @@ __device__ __forceinline__ void chunk_gates(const GateView& G, float g0, float g
 // 4-byte copies into a raw block [g rows 0-31 | g rows 32-63 | beta rows 0-31 |
 // beta rows 32-63] (128 floats; rows past the sequence end read as zero), so
 // that their global-memory latency stays off the chunk's critical path.
-__device__ __forceinline__ void prefetch_gates(float* raw, const float* g, const float* beta, int b,
-                                               int T, int H, int h, int ci, int lane) {
-  const int t0 = ci * C, n = min(C, T - t0);
-  const size_t base = ((size_t)b * T + t0) * H + h;
+__device__ __forceinline__ void prefetch_gates(float* raw, const float* g, const float* beta,
+                                               size_t row0, int n, int H, int h, int lane) {
+  const size_t base = row0 * H + h;
   const size_t o0 = lane < n ? base + (size_t)lane * H : base;
   const size_t o1 = lane + 32 < n ? base + (size_t)(lane + 32) * H : base;
   cp_async4(raw + lane, g + o0, lane < n);
@@ -208,7 +208,7 @@ __device__ __forceinline__ void decay_row(float (&v)[n], const GateView& G, int 
   }
 }
 
-template <bool NoDelta>
+template <bool NoDelta, bool Packed>
 __global__ void __launch_bounds__(FT, 1)
 gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -219,11 +219,12 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
   const int quad = warp & 3, half = (warp >> 2) & 1, grp = warp >> 3;
   const int row = quad * 32 + lane;    // TMEM lane / tile row owned by this thread
-  // this CTA's sequence and chunks [c0, c0 + NL) (the whole sequence unless segmented)
+  // this CTA's sequence and chunks [c0, c0 + NL) (the whole sequence unless
+  // segmented; segments are used for batches only)
   const int nseg = p.seg_chunks ? (p.N + p.seg_chunks - 1) / p.seg_chunks : 1;
-  const int seg = blockIdx.x % nseg, bh = blockIdx.x / nseg, b = bh / p.H, h = bh % p.H;
+  const int seg = blockIdx.x % nseg, bh = blockIdx.x / nseg, sq_s = bh / p.H, h = bh % p.H;
   const int c0 = seg * p.seg_chunks;
-  const int NL = p.seg_chunks ? min(p.seg_chunks, p.N - c0) : p.N;
+  int b = 0, tb = 0, slen = 0, NL = 0;  // batch row, first token, length, chunks (after the wait)
   const size_t st_idx = (size_t)bh * nseg + seg;  // index of h0 / ht
   const bool has_v = !p.v_zero;
 
@@ -256,35 +257,39 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
   grid_dep_wait();  // the previous kernel's results (and its reads of what this one writes)
   grid_dep_launch();
+  {
+    int nch;
+    p.sq.get_t<Packed>(sq_s, b, tb, slen, nch);
+    NL = p.seg_chunks ? min(p.seg_chunks, nch - c0) : nch;
+  }
 
   auto load_kq = [&](int ci) {
     const int st = ci & 1;
     unsigned char* dst = sm + kF_KQ + st * 32768;
     mbar_arrive_expect_tx(&bar_kq[st], 32768 + (NoDelta ? 0 : 8192));
-    const int t0 = (c0 + ci) * C;
+    const int t0 = tb + (c0 + ci) * C;
     tma_load_4d(dst + 0, &tm_k, &bar_kq[st], 0, h, t0, b);
     tma_load_4d(dst + 8192, &tm_q, &bar_kq[st], 0, h, t0, b);
     tma_load_4d(dst + 16384, &tm_k, &bar_kq[st], 64, h, t0, b);
     tma_load_4d(dst + 24576, &tm_q, &bar_kq[st], 64, h, t0, b);
     if (!NoDelta)
-      bulk_load(sm + kF_TR + st * 8192, p.tiles + ((size_t)bh * p.N + c0 + ci) * 8192, 8192, &bar_kq[st]);
+      bulk_load(sm + kF_TR + st * 8192, p.tiles + rec_bh<Packed>(p.sq, p.N, bh, sq_s, h, c0 + ci) * 8192, 8192, &bar_kq[st]);
     cnt[st] += 1;
   };
   auto load_v = [&](int ci) {
     mbar_arrive_expect_tx(bar_v, 16384);
-    const int t0 = (c0 + ci) * C;
+    const int t0 = tb + (c0 + ci) * C;
     tma_load_4d(sm + kF_V, &tm_v, bar_v, 0, h, t0, b);
     tma_load_4d(sm + kF_V + 8192, &tm_v, bar_v, 64, h, t0, b);
     cnt[4] += 1;
   };
   auto state_dst = [&](int ci) -> unsigned char* {
-    return p.states ? reinterpret_cast<unsigned char*>(p.states) +
-                          ((size_t)bh * p.N + c0 + ci) * (size_t)(2 * 16384)
+    return p.states ? reinterpret_cast<unsigned char*>(p.states) + rec_bh<Packed>(p.sq, p.N, bh, sq_s, h, c0 + ci) * (size_t)32768
                     : nullptr;
   };
   const bool want_o = p.o != nullptr;
 
-  if (tid == 0) {
+  if (tid == 0 && NL > 0) {
     load_kq(0);
     if (NL > 1) load_kq(1);
     if (has_v) load_v(0);
@@ -311,14 +316,14 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     fence_async_shared();
     group_sync_tc(kBarChain);
-    if (gt == 0 && p.states) {
+    if (gt == 0 && p.states && NL > 0) {
       // states mode: the tile is also chunk 0's entry state in the workspace
       bulk_store(state_dst(0), sm + kF_G, 32768);
       bulk_commit_group();
     }
     uint32_t s_phase = 0;
     for (int ci = 0; ci < NL; ++ci) {
-      const int s = ci & 1, t0 = (c0 + ci) * C;
+      const int s = ci & 1, t0 = tb + (c0 + ci) * C, nrow = min(C, slen - (c0 + ci) * C);
       const float* gates = reinterpret_cast<const float*>(sm + kF_GATE + s * kGateBlock);  // eC at [384]
       ok = group_and(kBarChain, kGroup, mbar_wait(bar_pd, ci & 1) && !*abort_flag);
       if (!ok) break;
@@ -440,10 +445,15 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         fence_async_shared();
         group_sync_tc(kBarChain);
+        // the output rows: a tensor store (rows past T are not written), or row
+        // by row for a packed sequence's partial last chunk
+        const bool rowwise = Packed && want_o && nrow < C;
+        if (rowwise)
+          store_rows_bf16(sm + kF_U, p.o + (((size_t)b * p.T + t0) * p.H + h) * D, (size_t)p.H * D, nrow,
+                          gt, kGroup);
         if (gt == 0 && (dst || want_o)) {
           if (dst) bulk_store(dst, sm + kF_G, 32768);  // the next chunk's entry state to the workspace
-          if (want_o) {
-            // the output rows (rows past T are not written)
+          if (want_o && !rowwise) {
             tma_store_4d(&tm_o, sm + kF_U, 0, h, t0, b);
             tma_store_4d(&tm_o, sm + kF_U + 8192, 64, h, t0, b);
           }
@@ -469,7 +479,9 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     auto psync = [&]() { group_sync(kBarPrep, kGroup); };
     float* graw = reinterpret_cast<float*>(sm + kF_GRAW);
     auto load_gates = [&](int ci) {
-      prefetch_gates(graw + (ci & 1) * 128, p.g, p.beta, b, p.T, p.H, h, c0 + ci, lane);
+      const int t = (c0 + ci) * C;
+      prefetch_gates(graw + (ci & 1) * 128, p.g, p.beta, (size_t)b * p.T + tb + t, min(C, slen - t), p.H,
+                     h, lane);
     };
     // Warp 9 (which issues nothing) computes each chunk's gates one chunk
     // ahead, at the end of the previous chunk's preparation, from raw values
@@ -478,7 +490,7 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       float* gb = reinterpret_cast<float*>(sm + kF_GATE + (ci & 1) * kGateBlock);
       return GateView{gb, gb + 64, gb + 128, gb + 192, gb + 256, gb + 320, gb + 384, gb + 385};
     };
-    if (warp == 9) {
+    if (warp == 9 && NL > 0) {
       load_gates(0);
       chunk_gates_raw(gate_view(0), graw, lane);
       if (NL > 1) load_gates(1);
@@ -669,10 +681,13 @@ static_assert(4 * (kSolveSmemBytes + 1024) <= 228 * 1024, "four solve CTAs per S
 struct SolveParams {
   const float* g;
   const float* beta;
-  unsigned char* tiles;  // [B*H][N][8 KB]
+  unsigned char* tiles;  // 8 KB per chunk record
   int B, T, H, N;
+  Seqs sq;
+  int nseq;
 };
 
+template <bool Packed>
 __global__ void __launch_bounds__(ST)
 gdn_tc_solve_kernel(const __grid_constant__ CUtensorMap tm_k, SolveParams p) {
   extern __shared__ unsigned char smem_raw[];
@@ -680,8 +695,6 @@ gdn_tc_solve_kernel(const __grid_constant__ CUtensorMap tm_k, SolveParams p) {
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
   const int quad = warp & 3, half = warp >> 2;
-  const int bh = blockIdx.x / p.N, ci = blockIdx.x % p.N, b = bh / p.H, h = bh % p.H;
-  const int t0 = ci * C, n = min(C, p.T - t0);
   float* gates = reinterpret_cast<float*>(sm + kS_GATE);
   const GateView GV{gates, gates + 64, gates + 128, gates + 192, gates + 256, gates + 320,
                     gates + 384, gates + 385};
@@ -694,6 +707,10 @@ gdn_tc_solve_kernel(const __grid_constant__ CUtensorMap tm_k, SolveParams p) {
 
   grid_dep_wait();  // the previous kernel's results (and its reads of what this one writes)
   grid_dep_launch();
+  int sqi, h, ci, b, tb, len, nch;
+  if (!p.sq.chunk_of(blockIdx.x, p.nseq, sqi, h, ci)) return;  // past the last packed chunk
+  p.sq.get_t<Packed>(sqi, b, tb, len, nch);
+  const int t0 = tb + ci * C, n = min(C, len - ci * C);
   if (tid == 0) {
     mbar_init(bar_ld, 1);
     mbar_init(bar_mma, 1);
@@ -748,7 +765,7 @@ gdn_tc_solve_kernel(const __grid_constant__ CUtensorMap tm_k, SolveParams p) {
     solve_unit_lower(Am, Tm, Sm, tid, ST, [] { __syncthreads(); });
     // row r = tid / 4, 16-byte chunks 2 (tid % 4) + {0, 1}
     const int r = tid >> 2;
-    unsigned char* dst = p.tiles + ((size_t)bh * p.N + ci) * 8192;
+    unsigned char* dst = p.tiles + p.sq.template rec_t<Packed>(sqi, h, ci) * 8192;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const int c8 = (tid & 3) * 2 + k;
@@ -850,11 +867,12 @@ struct BwdParams {
   float* dg;
   float* dbeta;
   float* dh0;
-  const unsigned char* tiles;    // T of every chunk ([B*H][N][8 KB], from the solve kernel)
+  const unsigned char* tiles;    // T of every chunk (8 KB per chunk record, from the solve kernel)
   int B, T, H, N;
+  Seqs sq;
 };
 
-template <bool NoDelta>
+template <bool NoDelta, bool Packed>
 __global__ void __launch_bounds__(BT, 1)
 gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -866,7 +884,8 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
   const int quad = warp & 3, cg = warp >> 2;
   const int row = quad * 32 + lane;
-  const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
+  const int bh = blockIdx.x, sq_s = bh / p.H, h = bh % p.H;
+  int b = 0, tb = 0, slen = 0, NN = 0;  // batch row, first token, length, chunks (after the wait)
 
   float* gam = reinterpret_cast<float*>(sm + kB_GATE);
   float* ee = gam + 64;
@@ -905,6 +924,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const uint32_t lb = (uint32_t)(quad * 32) << 16;
   grid_dep_wait();  // the previous kernel's results (and its reads of what this one writes)
   grid_dep_launch();
+  p.sq.get_t<Packed>(sq_s, b, tb, slen, NN);
 
   // The running state gradient dG (fp32) lives in TMEM columns kBtG3..+127
   // (row c = lane, column d); the dG_in product accumulates onto it.  This
@@ -936,15 +956,16 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   float* graw = reinterpret_cast<float*>(sm + kB_GRAW);
   auto load_gates = [&](int ci) {
-    prefetch_gates(graw + (ci & 1) * 128, p.g, p.beta, b, p.T, p.H, h, ci, lane);
+    prefetch_gates(graw + (ci & 1) * 128, p.g, p.beta, (size_t)b * p.T + tb + ci * C,
+                   min(C, slen - ci * C), p.H, h, lane);
   };
   // The gates of each chunk are computed by warp 1 near the end of the chunk
   // before it in the reverse scan, from g and beta prefetched one more chunk
   // ahead; the last chunk's here.
-  if (warp == 0 && p.N > 0) {
-    load_gates(p.N - 1);
-    chunk_gates_raw(GV, graw + ((p.N - 1) & 1) * 128, lane);
-    if (p.N > 1) load_gates(p.N - 2);
+  if (warp == 0 && NN > 0) {
+    load_gates(NN - 1);
+    chunk_gates_raw(GV, graw + ((NN - 1) & 1) * 128, lane);
+    if (NN > 1) load_gates(NN - 2);
   }
 
   uint32_t mma_phase = 0, load_phase = 0;
@@ -964,7 +985,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   int inflight = -1;   // thread 0: chunk whose tiles are requested but not yet waited for
   int parts = 0;       // thread 0: how many of its three load groups are issued
   auto issue_v = [&](int cn) {
-    const int tn = cn * C;
+    const int tn = tb + cn * C;
     inflight = cn;
     parts = 1;
     mbar_arrive_expect_tx(bar_load, kChunkBytes);
@@ -972,29 +993,30 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tma_load_4d(sm + kB_V + 8192, &tm_v, bar_load, 64, h, tn, b);
   };
   auto issue_rest = [&](int cn) {
-    const int tn = cn * C;
+    const int tn = tb + cn * C;
     parts = 2;
     tma_load_4d(sm + kB_KQ + 0, &tm_k, bar_load, 0, h, tn, b);
     tma_load_4d(sm + kB_KQ + 16384, &tm_k, bar_load, 64, h, tn, b);
     tma_load_4d(sm + kB_ZO + 8192, &tm_do, bar_load, 0, h, tn, b);
     tma_load_4d(sm + kB_ZO + 24576, &tm_do, bar_load, 64, h, tn, b);
-    bulk_load(sm + kB_GI, p.states + ((size_t)bh * p.N + cn) * 32768, 32768, bar_load);
-    if (!NoDelta) bulk_load(sm + kB_T, p.tiles + ((size_t)bh * p.N + cn) * 8192, 8192, bar_load);
+    bulk_load(sm + kB_GI, p.states + rec_bh<Packed>(p.sq, p.N, bh, sq_s, h, cn) * 32768, 32768, bar_load);
+    if (!NoDelta) bulk_load(sm + kB_T, p.tiles + rec_bh<Packed>(p.sq, p.N, bh, sq_s, h, cn) * 8192, 8192, bar_load);
   };
   auto issue_q = [&](int cn) {
-    const int tn = cn * C;
+    const int tn = tb + cn * C;
     parts = 3;
     tma_load_4d(sm + kB_KQ + 8192, &tm_q, bar_load, 0, h, tn, b);
     tma_load_4d(sm + kB_KQ + 24576, &tm_q, bar_load, 64, h, tn, b);
   };
-  if (tid == 0 && p.N > 0) {
-    issue_v(p.N - 1);
-    issue_rest(p.N - 1);
-    issue_q(p.N - 1);
+  if (tid == 0 && NN > 0) {
+    issue_v(NN - 1);
+    issue_rest(NN - 1);
+    issue_q(NN - 1);
   }
 
-  for (int ci = p.N - 1; ci >= 0 && ok; --ci) {
-    const int t0 = ci * C, n = min(C, p.T - t0);
+  for (int ci = NN - 1; ci >= 0 && ok; --ci) {
+    const int t0 = tb + ci * C, n = min(C, slen - ci * C);
+    const bool rowwise = Packed && n < C;  // a packed sequence's partial last chunk
     fence_async_shared();  // the dG tile written last chunk, for MMA1 (after the barrier below)
     if (tid == 0 && ci > 0) {
       // the next chunk in the reverse scan: start pulling its tiles into L2
@@ -1007,13 +1029,23 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       tma_prefetch_l2_4d(&tm_do, 64, h, tp, b);
       tma_prefetch_l2_4d(&tm_v, 0, h, tp, b);
       tma_prefetch_l2_4d(&tm_v, 64, h, tp, b);
-      bulk_prefetch_l2(p.states + ((size_t)bh * p.N + ci - 1) * 32768, 32768);
-      if (!NoDelta) bulk_prefetch_l2(p.tiles + ((size_t)bh * p.N + ci - 1) * 8192, 8192);
+      bulk_prefetch_l2(p.states + rec_bh<Packed>(p.sq, p.N, bh, sq_s, h, ci - 1) * 32768, 32768);
+      if (!NoDelta) bulk_prefetch_l2(p.tiles + rec_bh<Packed>(p.sq, p.N, bh, sq_s, h, ci - 1) * 8192, 8192);
     }
     ok = __syncthreads_and(mbar_wait(bar_load, load_phase));
     if (!ok) break;
     load_phase ^= 1;
     inflight = -1;
+    if (rowwise) {
+      // rows past the sequence hold the next one's dO: zero them, so that no
+      // product carries them into this sequence's gradients (the gates of
+      // those rows are already masked to g = 0, beta = 0)
+      for (int i = tid; i < (C - n) * 16; i += BT) {
+        const int r = n + (i >> 4), hh = (i >> 3) & 1, c8 = i & 7;
+        *reinterpret_cast<uint4*>(sm + kB_ZO + hh * 16384 + 8192 + r * 128 + c8 * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     if (NoDelta) {
       // T = I (the tile slot is rewritten later in the chunk): thread tid writes
       // the 16-byte chunk tid % 8 of row tid / 8
@@ -1169,10 +1201,15 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     fence_async_shared();
     cta_sync();
     // ---- G4: [dZ; dO] U^T  (lanes 0-63: dZ U^T, lanes 64-127: dO U^T)
+    if (rowwise)
+      store_rows_bf16(sm + kB_T, p.dv + (((size_t)b * p.T + t0) * p.H + h) * D, (size_t)p.H * D, n, tid,
+                      BT);
     if (tid == 0) {
       // dv: TMA store of the staged tile (rows past T are not written)
-      tma_store_4d(&tm_dv, sm + kB_T, 0, h, t0, b);
-      tma_store_4d(&tm_dv, sm + kB_T + 8192, 64, h, t0, b);
+      if (!rowwise) {
+        tma_store_4d(&tm_dv, sm + kB_T, 0, h, t0, b);
+        tma_store_4d(&tm_dv, sm + kB_T + 8192, 64, h, t0, b);
+      }
       bulk_commit_group();
       if (ci > 0) issue_v(ci - 1);  // V has been read for the last time
       const uint32_t id = idesc_bf16(128, 64, false, true);
@@ -1339,7 +1376,11 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     fence_async_shared();
     cta_sum_rows16(acc, red, dlc);  // (its barriers also publish the staged dq, dk)
-    if (tid == 0) {
+    if (rowwise) {
+      const size_t o0 = (((size_t)b * p.T + t0) * p.H + h) * D;
+      store_rows_bf16(sm + kB_X, p.dq + o0, (size_t)p.H * D, n, tid, BT);
+      store_rows_bf16(sm + kB_X + 16384, p.dk + o0, (size_t)p.H * D, n, tid, BT);
+    } else if (tid == 0) {
       tma_store_4d(&tm_dq, sm + kB_X, 0, h, t0, b);
       tma_store_4d(&tm_dq, sm + kB_X + 8192, 64, h, t0, b);
       tma_store_4d(&tm_dk, sm + kB_X + 16384, 0, h, t0, b);
@@ -1432,6 +1473,61 @@ __global__ void __launch_bounds__(128, 1) gdn_wait_selftest_kernel(uint32_t max_
   if (warp == 0) tmem_dealloc(tmem, 32);
 }
 
+// ---------------------------------------------------------------- packed sequences
+//
+// One CTA: checks that cu_seqlens rises from 0 to T without decreasing, then
+// writes each sequence's first global chunk, chunk_off[s] = sum of
+// ceil(len / C) over the sequences before it (chunk_off[nseq] = all chunks).
+// Invalid offsets are recorded as GDN_ERR_SEQLENS and give zero chunks.
+
+constexpr int kSetupThreads = 1024;
+
+__global__ void __launch_bounds__(kSetupThreads)
+gdn_setup_seqlens_kernel(const int* cu, int nseq, int T, int Cc, int* chunk_off) {
+  __shared__ int bad, carry;
+  __shared__ int warp_sum[kSetupThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    bad = (cu[0] != 0 || cu[nseq] != T) ? 1 : 0;
+    carry = 0;
+  }
+  __syncthreads();
+  for (int s = tid; s < nseq; s += kSetupThreads)
+    if (cu[s + 1] < cu[s]) bad = 1;
+  __syncthreads();
+  for (int base = 0; base < nseq; base += kSetupThreads) {
+    const int s = base + tid;
+    const int c = (!bad && s < nseq) ? (cu[s + 1] - cu[s] + Cc - 1) / Cc : 0;
+    int x = c;  // inclusive scan within the warp
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) warp_sum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_sum[lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, off);
+        if (lane >= off) w += y;
+      }
+      warp_sum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int before = carry + (warp > 0 ? warp_sum[warp - 1] : 0) + x - c;
+    if (s < nseq) chunk_off[s] = before;
+    __syncthreads();
+    if (tid == kSetupThreads - 1) carry = before + c;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    chunk_off[nseq] = carry;
+    if (bad) atomicExch(&g_file_status, GDN_ERR_SEQLENS);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 // T tiles of every chunk into `tiles` ([B*H][N][8 KB])
@@ -1439,12 +1535,12 @@ cudaError_t launch_solve(const Problem& p, cudaStream_t s, unsigned char* tiles)
   CUtensorMap mk;
   cudaError_t e;
   if ((e = make_token_map(&mk, p.k, p)) != cudaSuccess) return e;
-  SolveParams sp{p.g, p.beta, tiles, p.B, p.T, p.H, p.N};
-  e = cudaFuncSetAttribute(gdn_tc_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSolveSmemBytes);
+  SolveParams sp{p.g, p.beta, tiles, p.B, p.T, p.H, p.N, Seqs::of(p), p.nseq};
+  auto kern = p.cu_seqlens ? gdn_tc_solve_kernel<true> : gdn_tc_solve_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSolveSmemBytes);
   if (e != cudaSuccess) return e;
   prof_before(s);
-  e = launch_overlapped(gdn_tc_solve_kernel, (unsigned)((size_t)p.B * p.H * p.N), ST,
+  e = launch_overlapped(kern, (unsigned)(max_chunks(p) * p.H), ST,
                         kSolveSmemBytes, s, mk, sp);
   prof_after(s, kTcSolve);
   return e;
@@ -1471,15 +1567,17 @@ cudaError_t launch_fwd(const Problem& p, cudaStream_t s, const unsigned char* ti
   if ((e = make_token_map(&mv, p.v, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mo, f.want_out ? p.o : p.q, p)) != cudaSuccess) return e;  // unused without output
   FwdParams fp{p.g, p.beta, f.h0, f.want_out ? static_cast<__nv_bfloat16*>(p.o) : nullptr,
-               f.ht, f.states, tiles, p.B, p.T, p.H, p.N, f.seg_chunks, f.v_zero, f.h0_identity};
+               f.ht, f.states, tiles, p.B, p.T, p.H, p.N, Seqs::of(p), f.seg_chunks, f.v_zero,
+               f.h0_identity};
   // the Mamba2 mixer (no delta rule) is a separate instance: T = I, no W products
-  auto kern = p.no_delta ? gdn_tc_fwd_kernel<true> : gdn_tc_fwd_kernel<false>;
+  auto kern = p.cu_seqlens ? (p.no_delta ? gdn_tc_fwd_kernel<true, true> : gdn_tc_fwd_kernel<false, true>)
+                           : (p.no_delta ? gdn_tc_fwd_kernel<true, false> : gdn_tc_fwd_kernel<false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int nseg = f.seg_chunks ? (p.N + f.seg_chunks - 1) / f.seg_chunks : 1;
   prof_before(s);
-  e = launch_overlapped(kern, (unsigned)((size_t)p.B * p.H * nseg), FT, kSmemBytes, s, mq, mk, mv,
-                        mo, fp);
+  e = launch_overlapped(kern, (unsigned)((size_t)num_seqs(p) * p.H * nseg), FT, kSmemBytes, s, mq, mk,
+                        mv, mo, fp);
   prof_after(s, f.kernel_id);
   return e;
 }
@@ -1547,7 +1645,7 @@ gdn_tc_combine_kernel(const float* M, const float* Nl, const float* h0, float* H
 // multiply the number of busy SMs by at least four; segments are at least 32
 // chunks long.
 int fwd_seg_chunks(const Problem& p) {
-  if (p.no_delta) return 0;  // not segmented without the delta rule
+  if (p.no_delta || p.cu_seqlens) return 0;  // segments: GDN batches only
   const long seqs = (long)p.B * p.H;
   const int sms = sm_count();
   if (seqs <= 0 || p.N < 128) return 0;
@@ -1563,6 +1661,13 @@ size_t seg_state_bytes(const Problem& p, int seg_chunks) {
 
 }  // namespace
 
+cudaError_t setup_seqlens(const Problem& p, int* chunk_off, cudaStream_t s) {
+  prof_before(s);
+  gdn_setup_seqlens_kernel<<<1, kSetupThreads, 0, s>>>(p.cu_seqlens, p.nseq, p.T, p.C, chunk_off);
+  prof_after(s, kSeqSetup);
+  return cudaGetLastError();
+}
+
 cudaError_t wait_selftest(int max_tries, cudaStream_t s) {
   gdn_wait_selftest_kernel<<<1, 128, 0, s>>>((uint32_t)max_tries);
   return cudaGetLastError();
@@ -1572,8 +1677,8 @@ bool tc_supported(const Problem& p) {
   return p.bf16 && !p.kda && p.dk == D && p.dv == D && p.C == C;
 }
 
-size_t tiles_bytes(const Problem& p) { return align_up((size_t)p.B * p.H * p.N * 8192, 256); }
-size_t states_bytes(const Problem& p) { return align_up((size_t)p.B * p.H * p.N * 32768, 256); }
+size_t tiles_bytes(const Problem& p) { return align_up((size_t)max_chunks(p) * p.H * 8192, 256); }
+size_t states_bytes(const Problem& p) { return align_up((size_t)max_chunks(p) * p.H * 32768, 256); }
 
 size_t seg_scratch_bytes(const Problem& p) {
   const int sc = fwd_seg_chunks(p);
@@ -1669,13 +1774,14 @@ cudaError_t tc_bwd(const Problem& p, cudaStream_t s, bool saved) {
   BwdParams bp{p.g, p.beta, p.dht,
                reinterpret_cast<const unsigned char*>(states), static_cast<__nv_bfloat16*>(p.dq),
                static_cast<__nv_bfloat16*>(p.dk_), static_cast<__nv_bfloat16*>(p.dv_), p.dg, p.dbeta,
-               p.dh0, tiles, p.B, p.T, p.H, p.N};
-  auto kern = p.no_delta ? gdn_tc_bwd_kernel<true> : gdn_tc_bwd_kernel<false>;
+               p.dh0, tiles, p.B, p.T, p.H, p.N, Seqs::of(p)};
+  auto kern = p.cu_seqlens ? (p.no_delta ? gdn_tc_bwd_kernel<true, true> : gdn_tc_bwd_kernel<false, true>)
+                           : (p.no_delta ? gdn_tc_bwd_kernel<true, false> : gdn_tc_bwd_kernel<false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemBytes);
   if (e != cudaSuccess) return e;
   prof_before(s);
-  e = launch_overlapped(kern, (unsigned)(p.B * p.H), BT, kBwdSmemBytes, s, mq, mk, mv, mdo, mdq, mdk,
-                        mdv, bp);
+  e = launch_overlapped(kern, (unsigned)(num_seqs(p) * p.H), BT, kBwdSmemBytes, s, mq, mk, mv, mdo, mdq,
+                        mdk, mdv, bp);
   prof_after(s, kTcBwd);
   return e;
 }

@@ -82,10 +82,13 @@ struct KdaPrepParams {
   const float* g;         // [B, T, H, dk]
   const float* beta;      // [B, T, H]
   unsigned char* ktiles;  // [B*H][N][kKTBytes]
-  int* skip;              // [B*H] sequence flags, zero before the launch
+  int* skip;              // [sequences * H] flags, zero before the launch
   int B, T, H, N;
+  Seqs sq;
+  int nseq;
 };
 
+template <bool Packed>
 __global__ void __launch_bounds__(PT)
 kda_tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                    KdaPrepParams p) {
@@ -94,8 +97,11 @@ kda_tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
   const int quad = warp & 3, half = warp >> 2;
-  const int bh = blockIdx.x / p.N, ci = blockIdx.x % p.N, b = bh / p.H, h = bh % p.H;
-  const int t0 = ci * C, n = min(C, p.T - t0);
+  int sqi, h, ci, b, tb, len, nch;
+  if (!p.sq.chunk_of(blockIdx.x, p.nseq, sqi, h, ci)) return;  // past the last packed chunk
+  p.sq.get_t<Packed>(sqi, b, tb, len, nch);
+  const int bh = sqi * p.H + h;
+  const int t0 = tb + ci * C, n = min(C, len - ci * C);
   float* vec = reinterpret_cast<float*>(sm + kP_VEC);
   float* Am = reinterpret_cast<float*>(sm + kP_A);
   float* Tm = reinterpret_cast<float*>(sm + kP_T);
@@ -188,7 +194,7 @@ kda_tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
   }
   fence_async_shared();
   ok = __syncthreads_and(ok);
-  unsigned char* dst = p.ktiles + ((size_t)bh * p.N + ci) * kKTBytes;
+  unsigned char* dst = p.ktiles + rec_bh<Packed>(p.sq, p.N, bh, sqi, h, ci) * kKTBytes;
   if (ok && tid == 0) {
     bulk_store(dst + kKT_KQ, sm + kP_KQ, 32768);
     bulk_store(dst + kKT_KM, sm + kP_KM, 16384);
@@ -292,8 +298,10 @@ struct KdaFwdParams {
   const unsigned char* ktiles;  // the prep kernel's per-chunk blocks
   const int* skip;              // sequences the CUDA-core kernels take
   int B, T, H, N;
+  Seqs sq;
 };
 
+template <bool Packed>
 __global__ void __launch_bounds__(FT, 1)
 kda_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   KdaFwdParams p) {
@@ -303,8 +311,8 @@ kda_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
   const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
   const int quad = warp & 3, half = (warp >> 2) & 1, grp = warp >> 3;
   const int row = quad * 32 + lane;
-  const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
-  const int NL = p.N;
+  const int bh = blockIdx.x, sqi = bh / p.H, h = bh % p.H;
+  int b = 0, tb = 0, slen = 0, NL = 0;  // batch row, first token, length, chunks (after the wait)
 
   uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + kF_BAR);  // [2] stage loaded
   uint64_t* bar_v = bar_kq + 2;
@@ -334,13 +342,16 @@ kda_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
   grid_dep_wait();
   grid_dep_launch();
-  if (p.skip[bh]) {  // this sequence is computed by the CUDA-core kernels
+  p.sq.get_t<Packed>(sqi, b, tb, slen, NL);
+  if (p.skip[bh] || (Packed && NL == 0)) {  // the CUDA-core kernels take it (or it is empty)
+    if (!p.skip[bh] && p.ht)      // an empty packed sequence keeps its initial state
+      for (int i = tid; i < D * D; i += FT) p.ht[(size_t)bh * D * D + i] = p.h0 ? p.h0[(size_t)bh * D * D + i] : 0.f;
     cta_sync();
     if (warp == 0) tmem_dealloc(tmem, kTmCols);
     return;
   }
 
-  auto blk = [&](int ci) { return p.ktiles + ((size_t)bh * p.N + ci) * kKTBytes; };
+  auto blk = [&](int ci) { return p.ktiles + rec_bh<Packed>(p.sq, p.N, bh, sqi, h, ci) * kKTBytes; };
   auto vec = [&](int ci) { return reinterpret_cast<const float*>(sm + kF_VEC + (ci & 1) * kVecBytes); };
   auto load_kq = [&](int ci) {
     const int st = ci & 1;
@@ -354,13 +365,13 @@ kda_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
   };
   auto load_v = [&](int ci) {
     mbar_arrive_expect_tx(bar_v, 16384);
-    const int t0 = ci * C;
+    const int t0 = tb + ci * C;
     tma_load_4d(sm + kF_V, &tm_v, bar_v, 0, h, t0, b);
     tma_load_4d(sm + kF_V + 8192, &tm_v, bar_v, 64, h, t0, b);
     cnt[4] += 1;
   };
   auto state_dst = [&](int ci) -> unsigned char* {
-    return p.states ? reinterpret_cast<unsigned char*>(p.states) + ((size_t)bh * p.N + ci) * (size_t)32768
+    return p.states ? reinterpret_cast<unsigned char*>(p.states) + rec_bh<Packed>(p.sq, p.N, bh, sqi, h, ci) * (size_t)32768
                     : nullptr;
   };
   const bool want_o = p.o != nullptr;
@@ -399,7 +410,7 @@ kda_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
     }
     uint32_t s_phase = 0;
     for (int ci = 0; ci < NL && ok; ++ci) {
-      const int s = ci & 1, t0 = ci * C;
+      const int s = ci & 1, t0 = tb + ci * C, nrow = min(C, slen - ci * C);
       ok = group_and(kBarChain, kGroup, mbar_wait(bar_pd, ci & 1) && !*abort_flag);
       if (!ok) break;
       tc_fence_after();
@@ -497,9 +508,15 @@ kda_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
         }
         fence_async_shared();
         group_sync_tc(kBarChain);
+        // the output rows: a tensor store, or row by row for a packed
+        // sequence's partial last chunk (the rows past it belong to the next)
+        const bool rowwise = Packed && want_o && nrow < C;
+        if (rowwise)
+          store_rows_bf16(sm + kF_U, p.o + (((size_t)b * p.T + t0) * p.H + h) * D, (size_t)p.H * D, nrow,
+                          gt, kGroup);
         if (gt == 0 && (dstate || want_o)) {
           if (dstate) bulk_store(dstate, sm + kF_G, 32768);
-          if (want_o) {
+          if (want_o && !rowwise) {
             tma_store_4d(&tm_o, sm + kF_U, 0, h, t0, b);
             tma_store_4d(&tm_o, sm + kF_U + 8192, 64, h, t0, b);
           }
@@ -701,7 +718,12 @@ struct KdaBwdParams {
   const int* skip;
   float* dbeta;
   float* dh0;
+  __nv_bfloat16* dq;   // the token gradients, for the row-by-row stores of a
+  __nv_bfloat16* dk;   // packed sequence's partial last chunk
+  __nv_bfloat16* dv;
+  float* dg;
   int B, T, H, N;
+  Seqs sq;
 };
 
 // Each thread holds v[i], i < 32, for tile column 32 cg + i of its TMEM lane;
@@ -732,6 +754,7 @@ __device__ __forceinline__ float* gate_elem(unsigned char* sm, int r, int d) {
   return reinterpret_cast<float*>(base + r * 128 + (d & 31) * 4);
 }
 
+template <bool Packed>
 __global__ void __launch_bounds__(BT, 1)
 kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_dq,
@@ -743,7 +766,8 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
   const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
   const int quad = warp & 3, cg = warp >> 2;
   const int row = quad * 32 + lane;
-  const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
+  const int bh = blockIdx.x, sqi = bh / p.H, h = bh % p.H;
+  int b = 0, tb = 0, slen = 0, NN = 0;  // batch row, first token, length, chunks (after the wait)
 
   float* red = reinterpret_cast<float*>(sm + kB_RED);
   float* db1 = reinterpret_cast<float*>(sm + kB_SM);
@@ -777,13 +801,22 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
   const uint32_t lb = (uint32_t)(quad * 32) << 16;
   grid_dep_wait();
   grid_dep_launch();
+  if constexpr (Packed) p.sq.get_t<true>(sqi, b, tb, slen, NN);
+  else b = sqi, slen = p.T, NN = p.N;
   if (p.skip[bh]) {  // this sequence is computed by the CUDA-core kernels
     cta_sync();
     if (warp == 0) tmem_dealloc(tmem, kTmCols);
     return;
   }
+  if (Packed && NN == 0) {  // an empty packed sequence: the state gradient passes through
+    if (p.dh0)
+      for (int i = tid; i < D * D; i += BT) p.dh0[(size_t)bh * D * D + i] = p.dht ? p.dht[(size_t)bh * D * D + i] : 0.f;
+    cta_sync();
+    if (warp == 0) tmem_dealloc(tmem, kTmCols);
+    return;
+  }
 
-  auto blk = [&](int ci) { return p.ktiles + ((size_t)bh * p.N + ci) * kKTBytes; };
+  auto blk = [&](int ci) { return p.ktiles + (Packed ? p.sq.template rec_t<true>(sqi, h, ci) : (size_t)bh * p.N + ci) * kKTBytes; };
   auto vec = [&](int ci) { return reinterpret_cast<const float*>(sm + kB_VEC + (ci & 1) * kVecBytes); };
   // loads (thread 0): the main tiles of chunk cn on bar_load, announced in full
   // with the first part (G~, T, dO) and completed by the second (Kp|Qp, Km)
@@ -793,10 +826,10 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
     inflight = cn;
     parts = 1;
     mbar_arrive_expect_tx(bar_load, kMainBytes);
-    bulk_load(sm + kB_GI, p.states + ((size_t)bh * p.N + cn) * 32768, 32768, bar_load);
+    bulk_load(sm + kB_GI, p.states + (Packed ? p.sq.template rec_t<true>(sqi, h, cn) : (size_t)bh * p.N + cn) * 32768, 32768, bar_load);
     bulk_load(sm + kB_T, blk(cn) + kKT_T, 8192, bar_load);
-    tma_load_4d(sm + kB_ZO + 8192, &tm_do, bar_load, 0, h, cn * C, b);
-    tma_load_4d(sm + kB_ZO + 24576, &tm_do, bar_load, 64, h, cn * C, b);
+    tma_load_4d(sm + kB_ZO + 8192, &tm_do, bar_load, 0, h, tb + cn * C, b);
+    tma_load_4d(sm + kB_ZO + 24576, &tm_do, bar_load, 64, h, tb + cn * C, b);
   };
   auto issue_main2 = [&](int cn) {
     parts = 2;
@@ -806,8 +839,8 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
   int v_issued = 0, v_waited = 0, vec_issued = 0, vec_waited = 0, g_issued = 0, g_waited = 0;
   auto issue_v = [&](int cn) {
     mbar_arrive_expect_tx(bar_v, 16384);
-    tma_load_4d(sm + kB_V, &tm_v, bar_v, 0, h, cn * C, b);
-    tma_load_4d(sm + kB_V + 8192, &tm_v, bar_v, 64, h, cn * C, b);
+    tma_load_4d(sm + kB_V, &tm_v, bar_v, 0, h, tb + cn * C, b);
+    tma_load_4d(sm + kB_V + 8192, &tm_v, bar_v, 64, h, tb + cn * C, b);
     ++v_issued;
   };
   auto issue_vec = [&](int cn) {
@@ -818,10 +851,10 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
 
   bool ok = true;
   if (tid == 0) {
-    issue_vec(p.N - 1);
-    issue_main1(p.N - 1);
-    issue_main2(p.N - 1);
-    issue_v(p.N - 1);
+    issue_vec(NN - 1);
+    issue_main1(NN - 1);
+    issue_main2(NN - 1);
+    issue_v(NN - 1);
   }
   // dG^ of the last chunk: dht diag(cf)  (fp32 in TMEM, bf16 tile)
   const int g_region = cg >> 1, g_chunk0 = (cg & 1) * 4;
@@ -843,7 +876,7 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
   ok = __syncthreads_and(mbar_wait(bar_vec, 0));
   vec_waited = 1;
   if (ok) {
-    const float* cfv = vec(p.N - 1) + kVecCf;
+    const float* cfv = vec(NN - 1) + kVecCf;
     float g[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
@@ -861,13 +894,14 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
     tc_fence_after();
   };
 
-  for (int ci = p.N - 1; ci >= 0 && ok; --ci) {
-    const int t0 = ci * C, n = min(C, p.T - t0);
+  for (int ci = NN - 1; ci >= 0 && ok; --ci) {
+    const int t0 = tb + ci * C, n = min(C, slen - ci * C);
+    const bool rowwise = Packed && n < C;  // a packed sequence's partial last chunk
     const float* vc = vec(ci);
     const float* bt = vc + kVecBeta;
     fence_async_shared();  // the dG^ tile written last chunk, for MMA1 (after the barrier below)
     if (tid == 0) {
-      if (ci < p.N - 1) {
+      if (ci < NN - 1) {
         bulk_wait_read_all();  // the last chunk's dg, dq, dk stores have read the V slot
         issue_v(ci);
       }
@@ -876,7 +910,7 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
         // the next chunk of the reverse scan: start pulling its tiles into L2
         const int tp = t0 - C;
         bulk_prefetch_l2(blk(ci - 1), kKTBytes);
-        bulk_prefetch_l2(p.states + ((size_t)bh * p.N + ci - 1) * 32768, 32768);
+        bulk_prefetch_l2(p.states + (Packed ? p.sq.template rec_t<true>(sqi, h, ci - 1) : (size_t)bh * p.N + ci - 1) * 32768, 32768);
         tma_prefetch_l2_4d(&tm_do, 0, h, tp, b);
         tma_prefetch_l2_4d(&tm_do, 64, h, tp, b);
         tma_prefetch_l2_4d(&tm_v, 0, h, tp, b);
@@ -888,6 +922,15 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
     if (!ok) break;
     load_phase ^= 1;
     inflight = -1;
+    if (rowwise) {
+      // rows past the sequence hold the next one's dO: zero them (their gates
+      // and beta are already masked)
+      for (int i = tid; i < (C - n) * 16; i += BT) {
+        const int r = n + (i >> 4), hh = (i >> 3) & 1, c8 = i & 7;
+        *reinterpret_cast<uint4*>(sm + kB_ZO + hh * 16384 + 8192 + r * 128 + c8 * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     // T - I: the products take the off-diagonal part, the identity is added in fp32
     if (tid < 64)
       *reinterpret_cast<__nv_bfloat16*>(sm + kB_T + sw_row_off(tid, tid >> 3) + (tid & 7) * 2) =
@@ -1018,9 +1061,14 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
     fence_async_shared();
     cta_sync();
     // ---- G4: [dZ; dO] U^T  (lanes 0-63: dZ U^T, lanes 64-127: dO U^T)
+    if (rowwise)
+      store_rows_bf16(sm + kB_T, p.dv + (((size_t)b * p.T + t0) * p.H + h) * D, (size_t)p.H * D, n, tid,
+                      BT);
     if (tid == 0) {
-      tma_store_4d(&tm_dv, sm + kB_T, 0, h, t0, b);
-      tma_store_4d(&tm_dv, sm + kB_T + 8192, 64, h, t0, b);
+      if (!rowwise) {
+        tma_store_4d(&tm_dv, sm + kB_T, 0, h, t0, b);
+        tma_store_4d(&tm_dv, sm + kB_T + 8192, 64, h, t0, b);
+      }
       bulk_commit_group();
       // the gate tile, d 0-63 into the V slot (V is read for the last time)
       mbar_arrive_expect_tx(bar_g, 32768);
@@ -1150,7 +1198,8 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
     const int d = row;
     float gam[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) gam[i] = *gate_elem(sm, cg * 16 + i, d);
+    for (int i = 0; i < 16; ++i)  // (a packed sequence's rows past its end hold the next one's gates)
+      gam[i] = (!Packed || cg * 16 + i < n) ? *gate_elem(sm, cg * 16 + i, d) : 0.f;
 #pragma unroll
     for (int i = 1; i < 16; ++i) gam[i] += gam[i - 1];
     red[kR_TOT + cg * 128 + d] = gam[15];
@@ -1227,7 +1276,16 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
     }
     fence_async_shared();
     cta_sync();
-    if (tid == 0) {
+    if (rowwise) {
+      const size_t o0 = (((size_t)b * p.T + t0) * p.H + h) * D;
+      store_rows_bf16(sm + kB_X, p.dq + o0, (size_t)p.H * D, n, tid, BT);
+      store_rows_bf16(sm + kB_X + 16384, p.dk + o0, (size_t)p.H * D, n, tid, BT);
+      for (int i = tid; i < n * 32; i += BT) {  // dg: 16-byte pieces of the fp32 rows
+        const int r = i >> 5, c = i & 31;
+        const float4 v = *reinterpret_cast<const float4*>(gate_elem(sm, r, c * 4));
+        *reinterpret_cast<float4*>(p.dg + o0 + (size_t)r * p.H * D + c * 4) = v;
+      }
+    } else if (tid == 0) {
       tma_store_4d(&tm_dq, sm + kB_X, 0, h, t0, b);
       tma_store_4d(&tm_dq, sm + kB_X + 8192, 64, h, t0, b);
       tma_store_4d(&tm_dk, sm + kB_X + 16384, 0, h, t0, b);
@@ -1266,9 +1324,9 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
 
 // ---------------------------------------------------------------- host side
 
-size_t skip_bytes(const Problem& p) { return align_up((size_t)p.B * p.H * sizeof(int), 256); }
-size_t ktiles_bytes(const Problem& p) { return align_up((size_t)p.B * p.H * p.N * kKTBytes, 256); }
-size_t kstates_bytes(const Problem& p) { return align_up((size_t)p.B * p.H * p.N * 32768, 256); }
+size_t skip_bytes(const Problem& p) { return align_up((size_t)num_seqs(p) * p.H * sizeof(int), 256); }
+size_t ktiles_bytes(const Problem& p) { return align_up((size_t)max_chunks(p) * p.H * kKTBytes, 256); }
+size_t kstates_bytes(const Problem& p) { return align_up((size_t)max_chunks(p) * p.H * 32768, 256); }
 
 struct KdaLayout {
   int* skip;
@@ -1306,17 +1364,18 @@ cudaError_t make_gate_map(CUtensorMap* m, const void* ptr, const Problem& p) {
 }
 
 cudaError_t launch_prep(const Problem& p, cudaStream_t s, const KdaLayout& L) {
-  cudaError_t e = cudaMemsetAsync(L.skip, 0, (size_t)p.B * p.H * sizeof(int), s);
+  cudaError_t e = cudaMemsetAsync(L.skip, 0, (size_t)num_seqs(p) * p.H * sizeof(int), s);
   if (e != cudaSuccess) return e;
   CUtensorMap mk, mq;
   if ((e = make_token_map(&mk, p.k, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mq, p.q, p)) != cudaSuccess) return e;
-  KdaPrepParams pp{p.g, p.beta, L.ktiles, L.skip, p.B, p.T, p.H, p.N};
-  e = cudaFuncSetAttribute(kda_tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmemBytes);
+  KdaPrepParams pp{p.g, p.beta, L.ktiles, L.skip, p.B, p.T, p.H, p.N, Seqs::of(p), p.nseq};
+  auto kern = p.cu_seqlens ? kda_tc_prep_kernel<true> : kda_tc_prep_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmemBytes);
   if (e != cudaSuccess) return e;
   // an ordinary launch: it must follow the flags' reset in full
   prof_before(s);
-  kda_tc_prep_kernel<<<(unsigned)((size_t)p.B * p.H * p.N), PT, kPrepSmemBytes, s>>>(mk, mq, pp);
+  kern<<<(unsigned)(max_chunks(p) * p.H), PT, kPrepSmemBytes, s>>>(mk, mq, pp);
   prof_after(s, kKdaPrep);
   return cudaGetLastError();
 }
@@ -1329,11 +1388,12 @@ cudaError_t launch_fwd(const Problem& p, cudaStream_t s, const KdaLayout& L, boo
   if ((e = make_token_map(&mv, p.v, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mo, want_out ? p.o : p.v, p)) != cudaSuccess) return e;
   KdaFwdParams fp{p.h0, want_out ? static_cast<__nv_bfloat16*>(p.o) : nullptr, want_out ? p.ht : nullptr,
-                  states, L.ktiles, L.skip, p.B, p.T, p.H, p.N};
-  e = cudaFuncSetAttribute(kda_tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmemBytes);
+                  states, L.ktiles, L.skip, p.B, p.T, p.H, p.N, Seqs::of(p)};
+  auto kern = p.cu_seqlens ? kda_tc_fwd_kernel<true> : kda_tc_fwd_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmemBytes);
   if (e != cudaSuccess) return e;
   prof_before(s);
-  e = launch_overlapped(kda_tc_fwd_kernel, (unsigned)(p.B * p.H), FT, kFwdSmemBytes, s, mv, mo, fp);
+  e = launch_overlapped(kern, (unsigned)(num_seqs(p) * p.H), FT, kFwdSmemBytes, s, mv, mo, fp);
   prof_after(s, kernel_id);
   return e;
 }
@@ -1382,12 +1442,14 @@ cudaError_t kda_tc_bwd(const Problem& p, cudaStream_t s, bool saved) {
   if ((e = make_token_map(&mdv, p.dv_, p)) != cudaSuccess) return e;
   if ((e = make_gate_map(&mdg, p.dg, p)) != cudaSuccess) return e;
   KdaBwdParams bp{p.dht, L.ktiles, reinterpret_cast<const unsigned char*>(L.states), L.skip,
-                  p.dbeta, p.dh0, p.B, p.T, p.H, p.N};
-  e = cudaFuncSetAttribute(kda_tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemBytes);
+                  p.dbeta, p.dh0, static_cast<__nv_bfloat16*>(p.dq), static_cast<__nv_bfloat16*>(p.dk_),
+                  static_cast<__nv_bfloat16*>(p.dv_), p.dg, p.B, p.T, p.H, p.N, Seqs::of(p)};
+  auto kern = p.cu_seqlens ? kda_tc_bwd_kernel<true> : kda_tc_bwd_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemBytes);
   if (e != cudaSuccess) return e;
   prof_before(s);
-  e = launch_overlapped(kda_tc_bwd_kernel, (unsigned)(p.B * p.H), BT, kBwdSmemBytes, s, mv, mdo, mg, mdq,
-                        mdk, mdv, mdg, bp);
+  e = launch_overlapped(kern, (unsigned)(num_seqs(p) * p.H), BT, kBwdSmemBytes, s, mv, mdo, mg, mdq, mdk,
+                        mdv, mdg, bp);
   prof_after(s, kKdaBwd);
   if (e != cudaSuccess) return e;
   // flagged sequences: the CUDA-core backward (with the entry states its

@@ -308,6 +308,21 @@ __device__ __forceinline__ void stage_bf16(unsigned char* tile2, int r, int d, f
                                     (d & 7) * 2) = __float2bfloat16_rn(x);
 }
 
+// Writes rows [0, n) of a [64 x 128] bf16 staging tile (two K-major
+// 128-byte-swizzled halves of 8 KB, features 0-63 and 64-127) to global rows
+// dst + r * row_stride (in elements), 16 bytes per store; t / nth: this
+// thread's index among nth writers.  Used for a packed sequence's last
+// chunk, whose rows past the sequence belong to the next one (a tensor store
+// would write all 64).
+__device__ __forceinline__ void store_rows_bf16(const unsigned char* tile2, __nv_bfloat16* dst,
+                                                size_t row_stride, int n, int t, int nth) {
+  for (int i = t; i < n * 16; i += nth) {
+    const int r = i >> 4, hh = (i >> 3) & 1, c8 = i & 7;
+    const uint4 v = *reinterpret_cast<const uint4*>(tile2 + hh * 8192 + sw_row_off(r, c8));
+    *reinterpret_cast<uint4*>(dst + r * row_stride + hh * 64 + c8 * 8) = v;
+  }
+}
+
 // bf16 element (row, col) of a swizzled 64-wide K-major tile
 __device__ __forceinline__ float tile_elem(const unsigned char* tile, int row, int col) {
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(

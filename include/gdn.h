@@ -87,7 +87,9 @@ typedef enum {
   GDN_ERR_ALIGN = -4,          /* a pointer is not 16-byte aligned             */
   GDN_ERR_WORKSPACE = -5,      /* workspace NULL or smaller than required      */
   GDN_ERR_CUDA = -6,           /* a CUDA call failed; see gdn_last_cuda_error  */
-  GDN_ERR_DEVICE_TIMEOUT = -7  /* a bounded device-side wait ran out           */
+  GDN_ERR_DEVICE_TIMEOUT = -7, /* a bounded device-side wait ran out           */
+  GDN_ERR_SEQLENS = -8         /* packed sequences: cu_seqlens not rising from
+                                  0 to T (found on the device; see *_varlen)   */
 } gdn_status;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
@@ -218,6 +220,53 @@ GDN_API int mamba2_bwd_saved(const gdn_shape* shape, const void* q, const void* 
                              float* dg, float* dbeta, float* dh0, void* ctx, size_t ctx_bytes,
                              void* stream);
 
+/* Packed variable-length sequences.  The *_varlen calls take nseq sequences
+ * of different lengths packed one after another along the token dimension,
+ * as the 1M-token SFT guide packs its samples (section 4.2): shape->B must
+ * be 1 and shape->T the total token count; cu_seqlens is a DEVICE array of
+ * nseq + 1 int32 token offsets (4-byte aligned), sequence s being tokens
+ * [cu_seqlens[s], cu_seqlens[s+1]).  Each sequence starts from its own
+ * initial state and ends in its own final state: h0, ht, dht and dh0 are
+ * [nseq, H, dk, dv]; every other tensor keeps its [1, T, H, ...] layout.  A
+ * sequence may be empty (its final state is its initial one).  Arguments,
+ * dtypes, kernel selection and errors are those of the fixed-length calls,
+ * except that the workspace is *_varlen_workspace(shape, nseq, backward)
+ * bytes (it also holds each sequence's chunk offsets, which the call
+ * derives from cu_seqlens on the device), the backward recomputes its
+ * context (there is no saved-context pair), and offsets that do not rise
+ * from 0 to T are found on the device: nothing is computed and
+ * gdn_device_status() then returns GDN_ERR_SEQLENS. */
+GDN_API size_t gdn_varlen_workspace(const gdn_shape* shape, int nseq, int backward);
+GDN_API size_t kda_varlen_workspace(const gdn_shape* shape, int nseq, int backward);
+GDN_API size_t mamba2_varlen_workspace(const gdn_shape* shape, int nseq, int backward);
+GDN_API int gdn_fwd_varlen(const gdn_shape* shape, const int* cu_seqlens, int nseq, const void* q,
+                           const void* k, const void* v, const float* g, const float* beta,
+                           const float* h0, void* o, float* ht, void* ws, size_t ws_bytes,
+                           void* stream);
+GDN_API int gdn_bwd_varlen(const gdn_shape* shape, const int* cu_seqlens, int nseq, const void* q,
+                           const void* k, const void* v, const float* g, const float* beta,
+                           const float* h0, const void* do_, const float* dht, void* dq,
+                           void* dk, void* dv, float* dg, float* dbeta, float* dh0, void* ws,
+                           size_t ws_bytes, void* stream);
+GDN_API int kda_fwd_varlen(const gdn_shape* shape, const int* cu_seqlens, int nseq, const void* q,
+                           const void* k, const void* v, const float* g, const float* beta,
+                           const float* h0, void* o, float* ht, void* ws, size_t ws_bytes,
+                           void* stream);
+GDN_API int kda_bwd_varlen(const gdn_shape* shape, const int* cu_seqlens, int nseq, const void* q,
+                           const void* k, const void* v, const float* g, const float* beta,
+                           const float* h0, const void* do_, const float* dht, void* dq,
+                           void* dk, void* dv, float* dg, float* dbeta, float* dh0, void* ws,
+                           size_t ws_bytes, void* stream);
+GDN_API int mamba2_fwd_varlen(const gdn_shape* shape, const int* cu_seqlens, int nseq,
+                              const void* q, const void* k, const void* v, const float* g,
+                              const float* beta, const float* h0, void* o, float* ht, void* ws,
+                              size_t ws_bytes, void* stream);
+GDN_API int mamba2_bwd_varlen(const gdn_shape* shape, const int* cu_seqlens, int nseq,
+                              const void* q, const void* k, const void* v, const float* g,
+                              const float* beta, const float* h0, const void* do_,
+                              const float* dht, void* dq, void* dk, void* dv, float* dg,
+                              float* dbeta, float* dh0, void* ws, size_t ws_bytes, void* stream);
+
 /* Decode: the forward recurrence run token by token, for a few tokens per
  * sequence (T = 1 in single-token generation).  Same arguments, layout and
  * results as *_fwd (o and the final state), with no workspace: each (b, h)
@@ -241,9 +290,9 @@ GDN_API const char* gdn_status_str(int status);
 /* cudaError_t of the most recent GDN_ERR_CUDA on the calling thread. */
 GDN_API int gdn_last_cuda_error(void);
 
-/* Reads and clears the device status word of the current device: GDN_OK or
- * GDN_ERR_DEVICE_TIMEOUT.  Synchronises the current device.  Returns
- * GDN_ERR_CUDA if the read itself fails. */
+/* Reads and clears the device status word of the current device: GDN_OK,
+ * GDN_ERR_DEVICE_TIMEOUT or GDN_ERR_SEQLENS.  Synchronises the current
+ * device.  Returns GDN_ERR_CUDA if the read itself fails. */
 GDN_API int gdn_device_status(void);
 
 /* Exercises the device-side timeout path.  Launches one CTA on `stream` that

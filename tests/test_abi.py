@@ -215,3 +215,23 @@ def test_binding_refuses_cpu_tensors(L):
 def test_wait_selftest_validates_its_argument(L):
     assert L.gdn_wait_selftest(0, None) == GDN_ERR_ARG
     assert L.gdn_wait_selftest(1001, None) == GDN_ERR_ARG
+
+
+def test_varlen_validation(L):
+    s1 = shape(B=1, T=100, H=2, dk=128, dv=128, chunk=64, dtype=1)
+    need = L.gdn_varlen_workspace(ctypes.byref(s1), 3, 0)
+    # the chunk offsets come first, then the forward's T tiles for up to
+    # ceil(T / 64) + nseq chunks per head
+    assert need >= 2 * (2 + 3) * 64 * 64 * 2
+    assert L.gdn_varlen_workspace(ctypes.byref(s1), 3, 1) > need
+    assert L.gdn_varlen_workspace(ctypes.byref(shape(B=2)), 3, 0) == 0   # B must be 1
+    cu = FAKE
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None)
+    fn = L.gdn_fwd_varlen
+    assert fn(ctypes.byref(shape(B=2, T=100)), cu, 3, *args, FAKE, 1 << 30, None) == GDN_ERR_SHAPE
+    assert fn(ctypes.byref(s1), None, 3, *args, FAKE, 1 << 30, None) == GDN_ERR_ARG
+    assert fn(ctypes.byref(s1), ctypes.c_void_p(0x10002), 3, *args, FAKE, 1 << 30, None) == GDN_ERR_ALIGN
+    assert fn(ctypes.byref(s1), cu, -1, *args, FAKE, 1 << 30, None) == GDN_ERR_SHAPE
+    assert fn(ctypes.byref(s1), cu, 3, *args, FAKE, need - 1, None) == GDN_ERR_WORKSPACE
+    assert fn(ctypes.byref(s1), cu, 0, *args, None, 0, None) == GDN_OK  # no sequences: nothing to do
+    assert L.gdn_status_str(-8).decode().startswith("GDN_ERR_SEQLENS")

@@ -549,3 +549,93 @@ def test_bounded_wait_timeout_is_reported_and_context_survives():
     o, ht, gr = run_gpu(x, 64)
     compare(x, o, ht, gr, fp32=False)
     assert gdn.device_status() == 0
+
+
+# ----------------------------------------------------------- packed variable-length sequences
+
+def _pack(seqs):
+    """Concatenate per-sequence MixerInputs (B = 1 each) along the tokens."""
+    cat = lambda n: torch.cat([getattr(x, n) for x in seqs], 1)
+    st = lambda n: None if getattr(seqs[0], n) is None else torch.cat([getattr(x, n) for x in seqs], 0)
+    lens = [x.q.shape[1] for x in seqs]
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    return {n: cat(n) for n in ("q", "k", "v", "g", "beta", "do")} | {"h0": st("h0"), "dht": st("dht")}, cu
+
+
+# lengths: a one-token sequence, chunk boundaries inside and at the end of a
+# 64-token chunk, an empty sequence, a sequence longer than two chunks
+VARLEN = [
+    # lengths, dk, dv, chunk, dtype, mixer
+    ([1, 64, 100, 37, 0, 130], 128, 128, 64, "bf16", "gdn"),
+    ([1, 64, 100, 37, 0, 130], 128, 128, 64, "bf16", "kda"),
+    ([1, 64, 100, 37, 0, 130], 128, 128, 64, "bf16", "mamba2"),
+    ([5, 16, 33, 0, 50], 32, 48, 16, "f32", "gdn"),
+    ([5, 16, 33, 0, 50], 32, 48, 32, "f32", "kda"),
+    ([5, 16, 33, 0, 50], 32, 48, 16, "f32", "mamba2"),
+]
+
+
+@pytest.mark.parametrize("case", VARLEN, ids=lambda c: f"{c[5]}-{c[4]}-d{c[1]}x{c[2]}-C{c[3]}")
+def test_varlen_matches_oracle_per_sequence(case):
+    """Packed sequences against the oracle run on each sequence alone (its own
+    initial state and final-state gradient), every output."""
+    lens, dk, dv, chunk, dtype, mixer = case
+    kda, delta = mixer == "kda", mixer != "mamba2"
+    seqs = [make_inputs(1, L, 2, dk, dv, kda=kda, dtype=dtype, h0_std=0.3, with_dht=True,
+                        seed=100 + i) for i, L in enumerate(lens)]
+    x, cu = _pack(seqs)
+    d = {n: (t.to("cuda") if t is not None else None) for n, t in x.items()}
+    cu_d = cu.to("cuda")
+    fwd = getattr(gdn, f"{mixer}_fwd_varlen")
+    bwd = getattr(gdn, f"{mixer}_bwd_varlen")
+    o, ht = fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_d, d["h0"], chunk=chunk)
+    gr = bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_d, d["h0"], d["do"], d["dht"], chunk=chunk)
+    torch.cuda.synchronize()
+    assert gdn.device_status() == 0
+    fp32 = dtype == "f32"
+    for i, sq in enumerate(seqs):
+        a, b = int(cu[i]), int(cu[i + 1])
+        o_ref, ht_ref = oracle.fwd(sq.q, sq.k, sq.v, sq.g, sq.beta, sq.h0, kda=kda, delta=delta)
+        check(f"ht[{i}]", ht[i:i + 1].cpu(), ht_ref, fp32)
+        if b == a:
+            assert torch.equal(gr["dh0"][i:i + 1].cpu(), sq.dht), "empty sequence: dh0 = dht"
+            continue
+        ref = oracle.bwd(sq.q, sq.k, sq.v, sq.g, sq.beta, sq.h0, sq.do, sq.dht, kda=kda, delta=delta)
+        check(f"o[{i}]", o[:, a:b].cpu(), o_ref, fp32)
+        for n in ("dq", "dk", "dv", "dg", "dbeta"):
+            check(f"{n}[{i}]", gr[n][:, a:b].cpu(), ref[n], fp32)
+        check(f"dh0[{i}]", gr["dh0"][i:i + 1].cpu(), ref["dh0"], fp32)
+
+
+def test_varlen_equal_lengths_match_the_batch_call():
+    """Packed sequences of equal length give the bits of the batched call on the
+    same data (the same kernels, addressed differently)."""
+    x = make_inputs(3, 200, 2, 128, 128, dtype="bf16", h0_std=0.3, with_dht=True, seed=27)
+    d = x.to("cuda")
+    flat = lambda t: t.reshape(1, -1, *t.shape[2:]).contiguous()
+    cu = torch.tensor([0, 200, 400, 600], dtype=torch.int32, device="cuda")
+    o, ht = gdn.gdn_fwd_varlen(flat(d.q), flat(d.k), flat(d.v), flat(d.g), flat(d.beta), cu, d.h0)
+    gr = gdn.gdn_bwd_varlen(flat(d.q), flat(d.k), flat(d.v), flat(d.g), flat(d.beta), cu, d.h0,
+                            flat(d.do), d.dht)
+    ro, rht = gdn.gdn_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0)
+    rg = gdn.gdn_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, d.dht)
+    torch.cuda.synchronize()
+    assert torch.equal(o, flat(ro)) and torch.equal(ht, rht)
+    for n in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert torch.equal(gr[n], flat(rg[n])), n
+    assert torch.equal(gr["dh0"], rg["dh0"])
+
+
+def test_varlen_invalid_offsets_are_reported():
+    """Offsets that decrease are found on the device: nothing is computed, the
+    status word says GDN_ERR_SEQLENS, and the next call runs normally."""
+    x = make_inputs(1, 100, 2, 128, 128, dtype="bf16", seed=28).to("cuda")
+    cu = torch.tensor([0, 60, 40, 100], dtype=torch.int32, device="cuda")
+    gdn.gdn_fwd_varlen(x.q, x.k, x.v, x.g, x.beta, cu)
+    torch.cuda.synchronize()
+    assert gdn.device_status() == -8
+    assert gdn.device_status() == 0
+    good = torch.tensor([0, 60, 100], dtype=torch.int32, device="cuda")
+    o, ht = gdn.gdn_fwd_varlen(x.q, x.k, x.v, x.g, x.beta, good)
+    torch.cuda.synchronize()
+    assert gdn.device_status() == 0 and torch.isfinite(o.float()).all()
