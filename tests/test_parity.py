@@ -126,13 +126,14 @@ def test_training_workloads_sampled(w):
 
 
 def test_long_context_forward_sampled():
-    """1M-token forward: final state and outputs of two heads vs the oracle."""
+    """1M-token forward: final state and outputs of four heads (the first, two
+    middle ones, the last) vs the oracle."""
     w = W.GDN_1M_FWD_BF16
     x = w.make(device="cuda")
     fwd = gdn.gdn_fwd
     o, ht = fwd(x.q, x.k, x.v, x.g, x.beta, x.h0, chunk=w.chunk)
     torch.cuda.synchronize()
-    heads = [0, w.H - 1]
+    heads = [0, w.H // 3, 2 * w.H // 3, w.H - 1]
     pairs = [(0, h) for h in heads]
     sub = x.select(pairs).to("cpu")
     o_ref, ht_ref = oracle.fwd(sub.q, sub.k, sub.v, sub.g, sub.beta, None)
