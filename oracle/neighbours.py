@@ -15,8 +15,9 @@ the definition, fp64):
   (zero before the sequence start), then SiLU:
       s[t, c] = sum_{i=0}^{W-1} w[c, i] x[t - (W - 1) + i, c],   y = s * sigmoid(s);
   for the query and key projections the head's D values of each token are
-  then L2-normalised and scaled (the mixer's q and k inputs):
-      z[t, h, :] = scale * y[t, h, :] / ||y[t, h, :]||_2;
+  then L2-normalised and scaled (the mixer's q and k inputs), with the
+  recipe's epsilon under the root so that an all-zero row stays finite:
+      z[t, h, :] = scale * y[t, h, :] / sqrt(||y[t, h, :]||^2 + eps);
 * gated norm: per token and head, an RMS norm of the mixer output o over its
   D values, with a learned per-dimension weight, gated by SiLU of a gate
   projection:
@@ -34,7 +35,7 @@ def _sig(x):
     return 1.0 / (1.0 + np.exp(-x))
 
 
-def short_conv_fwd(x, w, H, l2norm=False, scale=1.0):
+def short_conv_fwd(x, w, H, l2norm=False, scale=1.0, eps=1e-6):
     """x: [B, T, H*D], w: [H*D, W].  Returns (z, s): the output [B, T, H*D]
     and the pre-activation s (kept for the backward pass)."""
     x = np.asarray(x, np.float64)
@@ -57,11 +58,11 @@ def short_conv_fwd(x, w, H, l2norm=False, scale=1.0):
         for t in range(T):
             for h in range(H):
                 seg = y[b, t, h * D:(h + 1) * D]
-                z[b, t, h * D:(h + 1) * D] = scale * seg / np.sqrt(np.sum(seg * seg))
+                z[b, t, h * D:(h + 1) * D] = scale * seg / np.sqrt(np.sum(seg * seg) + eps)
     return z, s
 
 
-def short_conv_bwd(x, w, dz, H, l2norm=False, scale=1.0):
+def short_conv_bwd(x, w, dz, H, l2norm=False, scale=1.0, eps=1e-6):
     """Gradients (dx, dw) of sum(z * dz) with respect to x and w."""
     x = np.asarray(x, np.float64)
     w = np.asarray(w, np.float64)
@@ -78,10 +79,10 @@ def short_conv_bwd(x, w, dz, H, l2norm=False, scale=1.0):
             for t in range(T):
                 for h in range(H):
                     sl = slice(h * D, (h + 1) * D)
-                    nrm = np.sqrt(np.sum(y[b, t, sl] ** 2))
-                    u = y[b, t, sl] / nrm
+                    r = 1.0 / np.sqrt(np.sum(y[b, t, sl] ** 2) + eps)
                     g = dz[b, t, sl]
-                    dy[b, t, sl] = scale * (g - u * np.dot(u, g)) / nrm
+                    # z = scale y r:  dy = scale r (g - y r^2 <y, g>)
+                    dy[b, t, sl] = scale * r * (g - y[b, t, sl] * (r * r) * np.dot(y[b, t, sl], g))
     else:
         dy = dz
     ds = dy * (sg + s * sg * (1.0 - sg))     # d/ds of s sigmoid(s)

@@ -4,7 +4,7 @@ The short convolution and the gated norm are checked against what fixes them
 independently of the oracle's loops: numpy's convolution routine and torch's
 depthwise conv1d / rms_norm / SiLU in fp64 (with torch's own autograd for the
 gradients), central finite differences, causality, the unit norm of the
-normalised q/k rows, and a closed form of the gated norm's RMS.
+normalised q/k rows (up to the epsilon under the root), and a closed form of the gated norm's RMS.
 """
 import numpy as np
 import pytest
@@ -40,7 +40,7 @@ def test_conv_matches_torch_depthwise_conv_and_autograd(l2norm):
     y = F.silu(s).transpose(1, 2)
     if l2norm:
         y4 = y.reshape(B, T, H, D)
-        y = (scale * y4 / y4.norm(dim=-1, keepdim=True)).reshape(B, T, H * D)
+        y = (scale * y4 / torch.sqrt((y4 * y4).sum(-1, keepdim=True) + 1e-6)).reshape(B, T, H * D)
     (y * torch.tensor(dz)).sum().backward()
     z, _ = nb.short_conv_fwd(x, w, H, l2norm, scale)
     np.testing.assert_allclose(z, y.detach().numpy(), rtol=1e-12, atol=1e-12)
@@ -57,8 +57,14 @@ def test_conv_is_causal_and_normalised():
     z2, _ = nb.short_conv_fwd(x2, w, H=2, l2norm=True, scale=0.25)
     np.testing.assert_array_equal(z[0, :7], z2[0, :7])
     assert np.max(np.abs(z[0, 7] - z2[0, 7])) > 1e-3
+    _, s = nb.short_conv_fwd(x, w, H=2)
+    y = (s / (1 + np.exp(-s))).reshape(1, 12, 2, 5)
+    ss = np.sum(y * y, axis=-1)
     norms = np.linalg.norm(z.reshape(1, 12, 2, 5), axis=-1)
-    np.testing.assert_allclose(norms, 0.25, rtol=1e-13)
+    np.testing.assert_allclose(norms, 0.25 * np.sqrt(ss / (ss + 1e-6)), rtol=1e-13)
+    # an all-zero input row gives a zero (finite) output row
+    z0, _ = nb.short_conv_fwd(np.zeros((1, 3, 10)), w, H=2, l2norm=True)
+    assert np.all(z0 == 0)
 
 
 def _fd(f, x, eps=1e-6):
