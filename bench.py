@@ -46,11 +46,13 @@ METRIC = "GDN/KDA mixer fwd+bwd tokens/s on 1 GB300; fraction of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
 WORKLOADS = {"gdn_300m": W.GDN_300M_BF16, "kda_300m": W.KDA_300M_BF16, "gdn_1b": W.GDN_1B_BF16_H0,
-             "mamba2_300m": W.MAMBA2_300M_BF16,
+             "mamba2_300m": W.MAMBA2_300M_BF16, "gdn_block_300m": W.GDN_BLOCK_300M_BF16,
              "gdn_tiny": W.GDN_TINY_FP32, "gdn_decode": W.GDN_DECODE_BF16,
              "kda_decode": W.KDA_DECODE_BF16, "gdn_1m": W.GDN_1M_FWD_BF16}
 FWD_METRIC = "GDN long-context forward tokens/s on 1 GB300; fraction of roofline"
 DECODE_METRIC = "GDN/KDA single-token decode step tokens/s on 1 GB300; fraction of roofline"
+BLOCK_METRIC = ("GDN layer token-mixing path (short conv + mixer + gated norm) fwd+bwd tokens/s "
+                "on 1 GB300; fraction of roofline")
 
 
 # ------------------------------------------------------------------ algorithmic work
@@ -91,12 +93,30 @@ def state_bytes(w, kernel):
     return 0
 
 
+def neighbour_bytes(w, kernel):
+    """Algorithmic bytes of one launch of a neighbour kernel on workload ``w``:
+    each token tensor read once and written once (x -> z; x, dz -> dx; o, gate
+    -> out; o, gate, dout -> do, dgate) plus the fp32 weights and their
+    gradients; None for other kernels (the partial sums carry none)."""
+    e = 2 if w.dtype == "bf16" else 4
+    n = w.B * w.T * w.H * w.dk
+    taps = w.H * w.dk * w.conv_width * 4
+    return {"short_conv_fwd": 2 * e * n + taps, "short_conv_bwd": 3 * e * n + 2 * taps,
+            "gated_rmsnorm_fwd": 3 * e * n + 4 * w.dk,
+            "gated_rmsnorm_bwd": 5 * e * n + 8 * w.dk}.get(kernel)
+
+
 def kernel_work(w, kernel):
     """(algorithmic bytes, FLOPs) of one launch of ``kernel`` on workload ``w``.
 
     The forward kernel carries the forward op's work; the backward op's work
     is carried by its main reverse-scan kernel (the state recompute and the
     partial-sum reduction are implementation overhead and carry none)."""
+    nb = neighbour_bytes(w, kernel)
+    if nb is not None:
+        return float(nb), 0.0
+    if kernel == "sum_partials":
+        return 0.0, 0.0
     a = algorithmic(w)
     th = w.B * w.T * w.H
     seqs = w.B * w.H
@@ -430,17 +450,33 @@ def run_ours(args):
 
 
 def run_e2e(gdn, w, x, ctx, dev, stream, K, warmup, ws):
-    """Same step through the public API with pinned host buffers: every step's
+    """The mixer step through the public API with pinned host buffers (see
+    ``pipelined_e2e``)."""
+    fwd_s = getattr(gdn, f"{w.mixer}_fwd_save")
+    bwd_s = getattr(gdn, f"{w.mixer}_bwd_saved")
+    names = ["q", "k", "v", "g", "beta", "do"] + (["h0"] if x.h0 is not None else [])
+
+    def compute(d):
+        o, ht, _ = fwd_s(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0"), chunk=w.chunk,
+                         ctx=ctx)
+        gr = bwd_s(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0"), d["do"], ctx, None,
+                   chunk=w.chunk)
+        return {"o": o, "ht": ht, **{k: v for k, v in gr.items() if v is not None}}
+
+    return pipelined_e2e(names, x, compute, dev, stream, K, warmup, ws, w.B * w.T)
+
+
+def pipelined_e2e(names, src, compute, dev, stream, K, warmup, ws, tokens_per_step):
+    """A step through the public API with pinned host buffers: every step's
     host-to-device copy of its inputs and device-to-host copy of every result
     are inside the timed region.  The loop is pipelined the way a training
     input pipeline is: step i+1's inputs are copied in on one stream and step
     i-1's results copied out on another while step i computes (two sets of
-    device input buffers; each result's memory is held until its copy ends)."""
-    fwd_s = getattr(gdn, f"{w.mixer}_fwd_save")
-    bwd_s = getattr(gdn, f"{w.mixer}_bwd_saved")
-    names = ["q", "k", "v", "g", "beta", "do"] + (["h0"] if x.h0 is not None else [])
-    host_in = {n: getattr(x, n).cpu().pin_memory() for n in names}
-    dev_in = [{n: torch.empty_like(getattr(x, n)) for n in names} for _ in range(2)]
+    device input buffers; each result's memory is held until its copy ends).
+    ``compute(d)`` runs one step on the device inputs ``d`` (a dict by name)
+    and returns its results by name."""
+    host_in = {n: getattr(src, n).cpu().pin_memory() for n in names}
+    dev_in = [{n: torch.empty_like(getattr(src, n)) for n in names} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     n_copy = 1  # copy streams per direction (two measured no faster: the host link is the limit)
     s_in = [torch.cuda.Stream(dev) for _ in range(n_copy)]
@@ -471,13 +507,8 @@ def run_e2e(gdn, w, x, ctx, dev, stream, K, warmup, ws):
                 copy_in(i + 1)
             for ev in ready[bi]:
                 stream.wait_event(ev)
-            d = dev_in[bi]
-            o, ht, _ = fwd_s(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0"),
-                             chunk=w.chunk, ctx=ctx)
-            gr = bwd_s(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("h0"), d["do"], ctx,
-                       None, chunk=w.chunk)
+            outs = compute(dev_in[bi])
             done[bi].record(stream)
-            outs = {"o": o, "ht": ht, **{k: v for k, v in gr.items() if v is not None}}
             for j, st in enumerate(s_out):
                 with torch.cuda.stream(st):
                     st.wait_event(done[bi])
@@ -506,9 +537,176 @@ def run_e2e(gdn, w, x, ctx, dev, stream, K, warmup, ws):
     t1.record(stream)
     torch.cuda.synchronize(dev)
     s = max_over_ranks(t0.elapsed_time(t1) / 1e3, ws, dev)
-    return {"value": w.B * w.T * K * ws / s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    return {"value": tokens_per_step * K * ws / s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "pipelined": "copy-in of step i+1 and copy-out of step i-1 "
             "overlap step i (one copy stream per direction)"}
+
+
+# ------------------------------------------------------------------ mixer block
+
+def block_oracle_run(w, rows, seed=0):
+    """The oracle's composition of the block (short convolutions, mixer, gated
+    norm; forward and backward) over ``rows`` batch rows of workload ``w``."""
+    import numpy as np
+    import oracle
+    from oracle import neighbours as nb
+    x = w.make_block(device="cpu", seed=seed, B=rows)
+    f = lambda t: t.double().numpy()
+    H, D = w.H, w.dk
+    shp = (rows, w.T, H, D)
+    nthreads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    q = nb.short_conv_fwd(f(x.xq), f(x.wq), H, True, D ** -0.5)[0].reshape(shp)
+    k = nb.short_conv_fwd(f(x.xk), f(x.wk), H, True, 1.0)[0].reshape(shp)
+    v = nb.short_conv_fwd(f(x.xv), f(x.wv), H, False, 1.0)[0].reshape(shp)
+    o, _ = oracle.fwd(q, k, v, x.g, x.beta, None, kda=w.kda, nthreads=nthreads)
+    nb.gated_rmsnorm_fwd(o, f(x.gate), f(x.weight))
+    do, _, _ = nb.gated_rmsnorm_bwd(o, f(x.gate), f(x.weight), f(x.dout))
+    gr = oracle.bwd(q, k, v, x.g, x.beta, None, do, None, kda=w.kda, nthreads=nthreads)
+    flat = lambda a: np.ascontiguousarray(a).reshape(rows, w.T, H * D)
+    nb.short_conv_bwd(f(x.xq), f(x.wq), flat(gr["dq"]), H, True, D ** -0.5)
+    nb.short_conv_bwd(f(x.xk), f(x.wk), flat(gr["dk"]), H, True, 1.0)
+    nb.short_conv_bwd(f(x.xv), f(x.wv), flat(gr["dv"]), H, False, 1.0)
+    return time.perf_counter() - t0, nthreads
+
+
+def run_block(args):
+    """One step = the GDN layer's token-mixing path, forward and backward:
+    three short convolutions, the mixer (saved context), the gated norm, then
+    the norm's, the mixer's and the convolutions' backward passes."""
+    import gated_delta_rule_bwd_gb300 as gdn
+    from gated_delta_rule_bwd_gb300.block import block_bwd, block_fwd
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init(ws, "nccl")
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    x = w.make_block(device=dev, seed=rank)
+    shp = (w.B, w.T, w.H, w.dk)
+    ctx = gdn.new_ctx(x.xq.view(shp), x.xv.view(shp), w.chunk, w.kda)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def compute(d):
+        out, ht, saved = block_fwd(d["xq"], d["xk"], d["xv"], d["wq"], d["wk"], d["wv"], d["g"],
+                                   d["beta"], d["gate"], d["weight"], chunk=w.chunk, kda=w.kda,
+                                   ctx=ctx)
+        gr = block_bwd(saved, d["dout"])
+        return {"out": out, "ht": ht, **{k: v for k, v in gr.items() if v is not None}}
+
+    dx = {n: getattr(x, n) for n in ("xq", "xk", "xv", "wq", "wk", "wv", "g", "beta", "gate",
+                                     "weight", "dout")}
+
+    def step():
+        return compute(dx)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+
+    def timed_steps(cap, n=K):
+        with gdn.KernelTimer(cap=cap) as t:
+            for i in range(n):
+                flush.fill_(i & 0xFF)  # evict L2 between timed steps (outside the events)
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        return [s.elapsed_time(e) for s, e in zip(starts[:n], ends[:n])], t.launches, \
+            (t.records() if cap else [])
+
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        epoch0 = time.time()
+        step_ms, launches, _ = timed_steps(0)
+        epoch1 = time.time()
+        barrier(ws)
+    dev_s_max = max_over_ranks(sum(step_ms) / 1e3, ws, dev)
+    n_ev = min(K, 100)
+    _, _, records = timed_steps(64 * n_ev, n_ev)
+    per = {}
+    for name, ms in records:
+        per.setdefault(name, []).append(ms)
+    totals = {k: sum(v) for k, v in per.items()}
+    peaks, peak_src = load_peaks()
+    dom = max(totals, key=totals.get)
+    dom_ms = statistics.mean(per[dom])
+    nbytes, flops = kernel_work(w, dom)
+    roof = {"bound": "hbm", "achieved": nbytes / (dom_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "kernel": dom, "kernel_ms": dom_ms, "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
+            "kernel_share": totals[dom] / sum(totals.values()),
+            "kernel_timing": f"CUDA events around each library kernel on its launch stream, "
+                             f"over {n_ev} more steps",
+            "per_kernel_ms": {k: statistics.mean(v) for k, v in per.items()},
+            "launches_per_step": {k: len(v) / n_ev for k, v in per.items()}}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    wkey = next((k for k, v in WORKLOADS.items() if v is w), w.name)
+    roof["traffic"] = args.traffic if args.traffic is not None else recorded_traffic(dom, wkey)
+    # each neighbour kernel against its own bytes
+    nbr = {}
+    for k, v in per.items():
+        b = neighbour_bytes(w, k)
+        if b is not None:
+            m = statistics.mean(v)
+            nbr[k] = {"ms": m, "achieved_gbs": b / (m * 1e-3) / 1e9,
+                      "frac": b / (m * 1e-3) / 1e9 / peaks["hbm_gbs"], "bytes": b}
+    roof["neighbour_kernels"] = nbr
+    # whole-step roofline: the mixer's work plus every neighbour launch's bytes
+    a = algorithmic(w)
+    th = w.B * w.T * w.H
+    step_bytes = (a["fwd_bytes"] + a["bwd_bytes"]) * th + sum(
+        neighbour_bytes(w, k) * len(v) / n_ev for k, v in per.items()
+        if neighbour_bytes(w, k) is not None)
+    step_flops = (a["fwd_flops"] + a["bwd_flops"]) * th
+    roof_step_s = max(step_bytes / (peaks["hbm_gbs"] * 1e9),
+                      step_flops / (peaks["bf16_tflops"] * 1e12))
+    ms_step = dev_s_max * 1e3 / K
+    tokens_step = w.B * w.T
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = pipelined_e2e(list(dx), x, compute, dev, stream, K, args.warmup, ws, tokens_step)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        rows, elapsed, batches = 1, 0.0, 0
+        while elapsed < args.cpu_seconds:
+            dt, nthreads = block_oracle_run(w, rows, seed=batches)
+            elapsed += dt
+            batches += 1
+        cpu = {"value": rows * w.T * batches / elapsed, "unit": "tokens/s", "cores": nthreads,
+               "kind": "oracle", "sample": f"{batches} x ({rows} batch row x {w.H} heads x {w.T} "
+               f"tokens) of {w.name}: fp64 convolutions, token recurrence and norm, fwd+bwd, "
+               f"{elapsed:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": BLOCK_METRIC, "value": aggregate_tokens_per_s(tokens_step, K, ws, dev_s_max),
+            "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "op": w.mixer + " block fwd+bwd",
+                       "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
+                       "conv_width": w.conv_width, "tokens_per_step": tokens_step,
+                       "parallelism": f"replicas x{ws} (independent sequences)",
+                       "l2": "flushed between timed steps (2 x L2 buffer written outside the events)",
+                       "roofline_step_us": roof_step_s * 1e6,
+                       "step_frac_of_roofline": roof_step_s / (ms_step * 1e-3)},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches * ws, "clocks": clocks.summary(epoch0, epoch1),
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
 
 
 # ------------------------------------------------------------------ decode
@@ -749,22 +947,27 @@ def run_reference(args):
     oracle.build()
     cores = os.cpu_count() or 1
     rows = max(1, cores // w.H)
+    run = block_oracle_run if w.block else cpu_oracle_run
+    if w.block:
+        rows = 1
     for i in range(args.warmup):
-        cpu_oracle_run(w, rows, seed=1000 + i)
+        run(w, rows, seed=1000 + i)
     times = []
     nthreads = cores
     for i in range(args.steps):
-        dt, nthreads = cpu_oracle_run(w, rows, seed=i)
+        dt, nthreads = run(w, rows, seed=i)
         times.append(dt)
     total = sum(times)
     value = rows * w.T * args.steps / total
     sample = (f"each step: {rows} batch rows x {w.H} heads x {w.T} tokens of {w.name} "
-              f"(fp64 token recurrence fwd+bwd on {nthreads} threads)")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+              f"(fp64 token recurrence fwd+bwd on {nthreads} threads"
+              + ("; with the fp64 short convolutions and gated norm)" if w.block else ")"))
+    line = {"impl": "reference", "metric": BLOCK_METRIC if w.block else METRIC, "value": value,
+            "unit": "tokens/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": total * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "op": w.mixer + " fwd+bwd",
+            "config": {"workload": w.name, "op": w.mixer + (" block" if w.block else "") + " fwd+bwd",
                        "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nthreads,
                              "kind": "oracle", "sample": sample},
@@ -806,6 +1009,8 @@ def main():
                               "cpu_baseline"}))
             return
         run_reference(args)
+    elif wl.block:
+        run_block(args)
     elif decode:
         run_decode(args)
     elif fwd_only:

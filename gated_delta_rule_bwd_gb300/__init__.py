@@ -12,7 +12,9 @@ Names follow the ABI: ``gdn_fwd``, ``gdn_bwd``, ``kda_fwd``, ``kda_bwd`` and
 the training pair with a saved context ``gdn_fwd_save`` / ``gdn_bwd_saved``
 (and the KDA and Mamba2 pairs), whose forward keeps what the backward would
 recompute; and the token-recurrent ``gdn_decode`` / ``kda_decode`` for a few
-tokens per sequence.
+tokens per sequence.  The mixer's fused neighbours: ``short_conv_fwd`` /
+``short_conv_bwd`` (causal depthwise convolution + SiLU, with the per-head
+L2 norm for q and k) and ``gated_rmsnorm_fwd`` / ``gated_rmsnorm_bwd``.
 Token tensors are ``[B, T, H, D]`` (fp32 or bf16, all the same dtype), ``g``
 is ``[B, T, H]`` (GDN) or ``[B, T, H, dk]`` (KDA) fp32, ``beta`` ``[B, T, H]``
 fp32, states ``[B, H, dk, dv]`` fp32.
@@ -38,6 +40,15 @@ class GdnShape(ctypes.Structure):
                 ("dtype", ctypes.c_int)]
 
 
+class ConvShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
+                ("D", ctypes.c_int), ("W", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+class NormShape(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_longlong), ("D", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
 class GdnError(RuntimeError):
     pass
 
@@ -55,6 +66,8 @@ EXPORTS = ("gdn_fwd", "gdn_bwd", "kda_fwd", "kda_bwd", "gdn_fwd_workspace", "kda
            "gdn_varlen_workspace", "kda_varlen_workspace", "mamba2_varlen_workspace",
            "gdn_fwd_varlen", "gdn_bwd_varlen", "kda_fwd_varlen", "kda_bwd_varlen",
            "mamba2_fwd_varlen", "mamba2_bwd_varlen",
+           "gdn_short_conv_fwd", "gdn_short_conv_bwd", "gdn_short_conv_bwd_workspace",
+           "gdn_gated_rmsnorm_fwd", "gdn_gated_rmsnorm_bwd", "gdn_gated_rmsnorm_bwd_workspace",
            "gdn_profile_begin", "gdn_profile_end", "gdn_profile_read", "gdn_kernel_name")
 
 
@@ -105,6 +118,21 @@ def lib():
             for name in ("gdn_uses_tensor_cores", "kda_uses_tensor_cores"):
                 getattr(L, name).argtypes = [sp]
                 getattr(L, name).restype = ctypes.c_int
+            cs, ns, f32, i32 = (ctypes.POINTER(ConvShape), ctypes.POINTER(NormShape),
+                                ctypes.c_float, ctypes.c_int)
+            L.gdn_short_conv_fwd.argtypes = [cs, vp, vp, vp, i32, f32, f32, vp, i32, vp]
+            L.gdn_short_conv_fwd.restype = ctypes.c_int
+            L.gdn_short_conv_bwd_workspace.argtypes = [cs]
+            L.gdn_short_conv_bwd_workspace.restype = sz
+            L.gdn_short_conv_bwd.argtypes = [cs, vp, vp, vp, vp, vp, i32, f32, f32, vp, i32, vp, sz,
+                                             vp]
+            L.gdn_short_conv_bwd.restype = ctypes.c_int
+            L.gdn_gated_rmsnorm_fwd.argtypes = [ns, vp, vp, vp, vp, f32, vp]
+            L.gdn_gated_rmsnorm_fwd.restype = ctypes.c_int
+            L.gdn_gated_rmsnorm_bwd_workspace.argtypes = [ns]
+            L.gdn_gated_rmsnorm_bwd_workspace.restype = sz
+            L.gdn_gated_rmsnorm_bwd.argtypes = [ns, vp, vp, vp, vp, vp, vp, vp, f32, vp, sz, vp]
+            L.gdn_gated_rmsnorm_bwd.restype = ctypes.c_int
             L.gdn_profile_begin.argtypes = [ctypes.c_int]
             L.gdn_profile_begin.restype = ctypes.c_int
             L.gdn_profile_end.argtypes = []
@@ -412,6 +440,109 @@ def mamba2_fwd_varlen(q, k, v, g, beta, cu_seqlens, h0=None, chunk=64, workspace
 def mamba2_bwd_varlen(q, k, v, g, beta, cu_seqlens, h0, do, dht=None, chunk=64, workspace=None):
     """Mamba2 backward over packed sequences."""
     return _bwd_varlen(False, False, q, k, v, g, beta, cu_seqlens, h0, do, dht, chunk, workspace)
+
+
+# ---------------------------------------------------------------- neighbours
+NORM_EPS = 1e-6  # the recipe's normalisation epsilon
+
+
+def _nb_check(name, x, dtype=None, device=None, shape=None):
+    if not isinstance(x, torch.Tensor):
+        raise GdnError(f"{name} must be a tensor")
+    if x.device.type != "cuda":
+        raise GdnError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if dtype is not None and x.dtype != dtype:
+        raise GdnError(f"{name}: expected {dtype}, got {x.dtype}")
+    if device is not None and x.device != device:
+        raise GdnError(f"{name}: expected device {device}, got {x.device}")
+    if shape is not None and tuple(x.shape) != tuple(shape):
+        raise GdnError(f"{name}: expected shape {tuple(shape)}, got {tuple(x.shape)}")
+    if not x.is_contiguous():
+        raise GdnError(f"{name} must be contiguous")
+
+
+def _conv_args(x, w, H, cu_seqlens):
+    _nb_check("x", x)
+    if x.dtype not in _DTYPES or x.dim() != 3:
+        raise GdnError("x must be [B, T, H*D] fp32 or bf16")
+    B, T, CH = x.shape
+    if H <= 0 or CH % H:
+        raise GdnError(f"H={H} does not divide the {CH} channels of x")
+    _nb_check("w", w, torch.float32, x.device)
+    if w.dim() != 2 or w.shape[0] != CH:
+        raise GdnError(f"w must be [{CH}, W] fp32")
+    nseq = 0
+    if cu_seqlens is not None:
+        if (cu_seqlens.dtype != torch.int32 or cu_seqlens.device != x.device
+                or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1 or not cu_seqlens.is_contiguous()):
+            raise GdnError("cu_seqlens must be a contiguous 1-D int32 tensor on x's device")
+        nseq = cu_seqlens.numel() - 1
+    return ConvShape(B, T, H, CH // H, w.shape[1], _DTYPES[x.dtype]), nseq
+
+
+def short_conv_fwd(x, w, H, l2norm=False, scale=1.0, eps=NORM_EPS, cu_seqlens=None):
+    """Causal depthwise short convolution + SiLU over ``x [B, T, H*D]`` with
+    ``w [H*D, W]`` fp32; with ``l2norm`` each head's D outputs of a token are
+    scaled to ``scale * y / sqrt(|y|^2 + eps)`` (the q and k inputs of the
+    mixer).  ``cu_seqlens`` (int32, B = 1) restarts the convolution at every
+    packed sequence.  Returns ``z`` (layout and dtype of x)."""
+    s, nseq = _conv_args(x, w, H, cu_seqlens)
+    z = torch.empty_like(x)
+    _check(lib().gdn_short_conv_fwd(ctypes.byref(s), _ptr(x), _ptr(w), _ptr(z), int(bool(l2norm)),
+                                    float(scale), float(eps), _ptr(cu_seqlens), nseq,
+                                    _stream(x.device)))
+    return z
+
+
+def short_conv_bwd(x, w, dz, H, l2norm=False, scale=1.0, eps=NORM_EPS, cu_seqlens=None,
+                   workspace=None):
+    """Gradients of ``short_conv_fwd``: returns ``(dx, dw)`` (dw fp32, a
+    reproducible sum over the tokens)."""
+    s, nseq = _conv_args(x, w, H, cu_seqlens)
+    _nb_check("dz", dz, x.dtype, x.device, x.shape)
+    dx = torch.empty_like(x)
+    dw = torch.empty_like(w)
+    need = int(lib().gdn_short_conv_bwd_workspace(ctypes.byref(s)))
+    ws = _workspace(need, workspace, x.device)
+    _check(lib().gdn_short_conv_bwd(ctypes.byref(s), _ptr(x), _ptr(w), _ptr(dz), _ptr(dx), _ptr(dw),
+                                    int(bool(l2norm)), float(scale), float(eps), _ptr(cu_seqlens),
+                                    nseq, _ptr(ws), ws.numel(), _stream(x.device)))
+    return dx, dw
+
+
+def _norm_args(o, gate, weight):
+    _nb_check("o", o)
+    if o.dtype not in _DTYPES or o.dim() < 1:
+        raise GdnError("o must be [..., D] fp32 or bf16")
+    _nb_check("gate", gate, o.dtype, o.device, o.shape)
+    D = o.shape[-1]
+    _nb_check("weight", weight, torch.float32, o.device, (D,))
+    return NormShape(o.numel() // D if D else 0, D, _DTYPES[o.dtype])
+
+
+def gated_rmsnorm_fwd(o, gate, weight, eps=NORM_EPS):
+    """``o / sqrt(mean(o^2) + eps) * weight * SiLU(gate)`` over the last
+    dimension of ``o`` (e.g. the mixer output ``[B, T, H, dv]``); ``weight``
+    ``[D]`` fp32.  Returns ``out`` (layout and dtype of o)."""
+    s = _norm_args(o, gate, weight)
+    out = torch.empty_like(o)
+    _check(lib().gdn_gated_rmsnorm_fwd(ctypes.byref(s), _ptr(o), _ptr(gate), _ptr(weight), _ptr(out),
+                                       float(eps), _stream(o.device)))
+    return out
+
+
+def gated_rmsnorm_bwd(o, gate, weight, dout, eps=NORM_EPS, workspace=None):
+    """Gradients of ``gated_rmsnorm_fwd``: returns ``(do, dgate, dweight)``."""
+    s = _norm_args(o, gate, weight)
+    _nb_check("dout", dout, o.dtype, o.device, o.shape)
+    d_o, dgate = torch.empty_like(o), torch.empty_like(gate)
+    dweight = torch.empty_like(weight)
+    need = int(lib().gdn_gated_rmsnorm_bwd_workspace(ctypes.byref(s)))
+    ws = _workspace(need, workspace, o.device)
+    _check(lib().gdn_gated_rmsnorm_bwd(ctypes.byref(s), _ptr(o), _ptr(gate), _ptr(weight), _ptr(dout),
+                                       _ptr(d_o), _ptr(dgate), _ptr(dweight), float(eps), _ptr(ws),
+                                       ws.numel(), _stream(o.device)))
+    return d_o, dgate, dweight
 
 
 def _decode(kda, q, k, v, g, beta, state=None, inplace=True, chunk=64):

@@ -1,6 +1,7 @@
 // C ABI of the GDN / KDA mixer: argument checks, kernel selection, launch.
 // The operations, layouts and error rules are stated in include/gdn.h.
 
+#include <initializer_list>
 #include <vector>
 
 #include "gdn.h"
@@ -217,7 +218,8 @@ const char* kernel_name(int id) {
   static const char* names[kNumKernelIds] = {
       "simt_fwd", "simt_states", "simt_bwd", "simt_bwd_reduce",
       "tc_fwd", "tc_states", "tc_bwd", "tc_solve", "tc_fwd_segment", "tc_combine", "decode",
-      "kda_tc_prep", "kda_tc_fwd", "kda_tc_states", "kda_tc_bwd", "seqlens_setup"};
+      "kda_tc_prep", "kda_tc_fwd", "kda_tc_states", "kda_tc_bwd", "seqlens_setup",
+      "short_conv_fwd", "short_conv_bwd", "gated_rmsnorm_fwd", "gated_rmsnorm_bwd", "sum_partials"};
   return (id >= 0 && id < kNumKernelIds) ? names[id] : "unknown";
 }
 
@@ -417,6 +419,153 @@ GDN_VARLEN_PAIR(gdn, false, false)
 GDN_VARLEN_PAIR(kda, true, false)
 GDN_VARLEN_PAIR(mamba2, false, true)
 #undef GDN_VARLEN_PAIR
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- neighbours
+namespace {
+
+int conv_problem(const gdn_conv_shape* s, int l2norm, float scale, float eps,
+                 const int* cu_seqlens, int nseq, gdn::ConvProblem* p) {
+  if (!s) return GDN_ERR_ARG;
+  if (s->dtype != GDN_F32 && s->dtype != GDN_BF16) return GDN_ERR_DTYPE;
+  if (s->B < 0 || s->T < 0 || s->H < 0) return GDN_ERR_SHAPE;
+  if (s->D != 32 && s->D != 64 && s->D != 128) return GDN_ERR_SHAPE;
+  if (s->W < 1 || s->W > 4) return GDN_ERR_SHAPE;
+  if (!(eps >= 0.f)) return GDN_ERR_ARG;
+  if (s->H > 65535 || (long long)s->H * s->D > (1 << 24)) return GDN_ERR_SHAPE;
+  if ((long long)s->B * s->T > (1LL << 30)) return GDN_ERR_SHAPE;
+  *p = gdn::ConvProblem{};
+  p->B = s->B; p->T = s->T; p->H = s->H; p->D = s->D; p->W = s->W;
+  p->bf16 = s->dtype == GDN_BF16;
+  p->l2norm = l2norm != 0;
+  p->scale = scale;
+  p->eps = eps;
+  if (cu_seqlens) {
+    if (s->B != 1 || nseq < 0) return GDN_ERR_SHAPE;
+    if (((uintptr_t)cu_seqlens & 3u) != 0) return GDN_ERR_ALIGN;
+    p->cu_seqlens = cu_seqlens;
+    p->nseq = nseq;
+  }
+  return GDN_OK;
+}
+
+bool conv_empty(const gdn::ConvProblem& p) { return (long long)p.B * p.T == 0 || p.H == 0; }
+
+int norm_problem(const gdn_norm_shape* s, float eps, gdn::NormProblem* p) {
+  if (!s) return GDN_ERR_ARG;
+  if (s->dtype != GDN_F32 && s->dtype != GDN_BF16) return GDN_ERR_DTYPE;
+  if (s->rows < 0) return GDN_ERR_SHAPE;
+  if (s->D != 32 && s->D != 64 && s->D != 128) return GDN_ERR_SHAPE;
+  if (!(eps >= 0.f)) return GDN_ERR_ARG;
+  *p = gdn::NormProblem{};
+  p->rows = (long)s->rows;
+  p->D = s->D;
+  p->bf16 = s->dtype == GDN_BF16;
+  p->eps = eps;
+  return GDN_OK;
+}
+
+bool all_aligned(std::initializer_list<const void*> ptrs) {
+  for (const void* x : ptrs)
+    if (!x || !aligned16(x)) return false;
+  return true;
+}
+
+bool any_null(std::initializer_list<const void*> ptrs) {
+  for (const void* x : ptrs)
+    if (!x) return true;
+  return false;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_short_conv_fwd(const gdn_conv_shape* shape, const void* x, const float* w, void* z,
+                       int l2norm, float scale, float eps, const int* cu_seqlens, int nseq,
+                       void* stream) {
+  gdn::ConvProblem p;
+  int rc = conv_problem(shape, l2norm, scale, eps, cu_seqlens, nseq, &p);
+  if (rc != GDN_OK || conv_empty(p)) return rc;
+  if (any_null({x, w, z})) return GDN_ERR_ARG;
+  if (!all_aligned({x, z})) return GDN_ERR_ALIGN;
+  p.x = x; p.w = w; p.z = z;
+  cudaError_t e = gdn::short_conv_fwd(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GDN_OK : fail_cuda(e);
+}
+
+size_t gdn_short_conv_bwd_workspace(const gdn_conv_shape* shape) {
+  gdn::ConvProblem p;
+  if (conv_problem(shape, 0, 1.f, 0.f, nullptr, 0, &p) != GDN_OK) return 0;
+  return gdn::short_conv_bwd_workspace(p);
+}
+
+int gdn_short_conv_bwd(const gdn_conv_shape* shape, const void* x, const float* w,
+                       const void* dz, void* dx, float* dw, int l2norm, float scale, float eps,
+                       const int* cu_seqlens, int nseq, void* ws, size_t ws_bytes,
+                       void* stream) {
+  gdn::ConvProblem p;
+  int rc = conv_problem(shape, l2norm, scale, eps, cu_seqlens, nseq, &p);
+  if (rc != GDN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (conv_empty(p)) {
+    // no token: dw is the empty sum
+    if (!dw) return GDN_ERR_ARG;
+    const size_t n = (size_t)p.H * p.D * p.W;
+    cudaError_t e = n ? cudaMemsetAsync(dw, 0, n * sizeof(float), st) : cudaSuccess;
+    return e == cudaSuccess ? GDN_OK : fail_cuda(e);
+  }
+  if (any_null({x, w, dz, dx, dw})) return GDN_ERR_ARG;
+  if (!all_aligned({x, dz, dx})) return GDN_ERR_ALIGN;
+  const size_t need = gdn::short_conv_bwd_workspace(p);
+  if (!ws || ws_bytes < need) return GDN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return GDN_ERR_ALIGN;
+  p.x = x; p.w = w; p.dz = dz; p.dx = dx; p.dw = dw; p.ws = ws;
+  cudaError_t e = gdn::short_conv_bwd(p, st);
+  return e == cudaSuccess ? GDN_OK : fail_cuda(e);
+}
+
+int gdn_gated_rmsnorm_fwd(const gdn_norm_shape* shape, const void* o, const void* gate,
+                          const float* weight, void* out, float eps, void* stream) {
+  gdn::NormProblem p;
+  int rc = norm_problem(shape, eps, &p);
+  if (rc != GDN_OK || p.rows == 0) return rc;
+  if (any_null({o, gate, weight, out})) return GDN_ERR_ARG;
+  if (!all_aligned({o, gate, out})) return GDN_ERR_ALIGN;
+  p.o = o; p.gate = gate; p.weight = weight; p.out = out;
+  cudaError_t e = gdn::gated_rmsnorm_fwd(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GDN_OK : fail_cuda(e);
+}
+
+size_t gdn_gated_rmsnorm_bwd_workspace(const gdn_norm_shape* shape) {
+  gdn::NormProblem p;
+  if (norm_problem(shape, 0.f, &p) != GDN_OK) return 0;
+  return gdn::gated_rmsnorm_bwd_workspace(p);
+}
+
+int gdn_gated_rmsnorm_bwd(const gdn_norm_shape* shape, const void* o, const void* gate,
+                          const float* weight, const void* dout, void* do_, void* dgate,
+                          float* dweight, float eps, void* ws, size_t ws_bytes, void* stream) {
+  gdn::NormProblem p;
+  int rc = norm_problem(shape, eps, &p);
+  if (rc != GDN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p.rows == 0) {
+    if (!dweight) return GDN_ERR_ARG;
+    cudaError_t e = cudaMemsetAsync(dweight, 0, (size_t)p.D * sizeof(float), st);
+    return e == cudaSuccess ? GDN_OK : fail_cuda(e);
+  }
+  if (any_null({o, gate, weight, dout, do_, dgate, dweight})) return GDN_ERR_ARG;
+  if (!all_aligned({o, gate, dout, do_, dgate})) return GDN_ERR_ALIGN;
+  const size_t need = gdn::gated_rmsnorm_bwd_workspace(p);
+  if (!ws || ws_bytes < need) return GDN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return GDN_ERR_ALIGN;
+  p.o = o; p.gate = gate; p.weight = weight; p.dout = dout; p.dO = do_; p.dgate = dgate;
+  p.dweight = dweight; p.ws = ws;
+  cudaError_t e = gdn::gated_rmsnorm_bwd(p, st);
+  return e == cudaSuccess ? GDN_OK : fail_cuda(e);
+}
 
 const char* gdn_status_str(int status) {
   switch (status) {

@@ -149,6 +149,47 @@ cudaError_t kda_read_and_clear_status(int* status);
 // Token-recurrent forward for a few tokens per sequence (any dk, dv <= 128).
 cudaError_t decode(const Problem& p, cudaStream_t s);
 
+// The mixer's fused neighbours (neighbours.cu).  Short convolution over
+// x [B, T, H*D] (packed: B = 1 and cu_seqlens/nseq as for the mixer) with
+// weights w [H*D, W]; gated RMS norm over rows of D values.
+struct ConvProblem {
+  int B = 0, T = 0, H = 0, D = 0, W = 0;
+  bool bf16 = true, l2norm = false;
+  float scale = 1.f, eps = 1e-6f;
+  const int* cu_seqlens = nullptr;
+  int nseq = 0;
+  const void* x = nullptr;
+  const float* w = nullptr;
+  void* z = nullptr;
+  const void* dz = nullptr;
+  void* dx = nullptr;
+  float* dw = nullptr;
+  void* ws = nullptr;
+};
+size_t short_conv_bwd_workspace(const ConvProblem& p);
+cudaError_t short_conv_fwd(const ConvProblem& p, cudaStream_t s);
+cudaError_t short_conv_bwd(const ConvProblem& p, cudaStream_t s);
+
+struct NormProblem {
+  long rows = 0;
+  int D = 0;
+  bool bf16 = true;
+  float eps = 1e-6f;
+  const void* o = nullptr;
+  const void* gate = nullptr;
+  const float* weight = nullptr;
+  void* out = nullptr;
+  const void* dout = nullptr;
+  void* dO = nullptr;
+  void* dgate = nullptr;
+  float* dweight = nullptr;
+  void* ws = nullptr;
+};
+size_t gated_rmsnorm_bwd_workspace(const NormProblem& p);
+cudaError_t gated_rmsnorm_fwd(const NormProblem& p, cudaStream_t s);
+cudaError_t gated_rmsnorm_bwd(const NormProblem& p, cudaStream_t s);
+cudaError_t nb_read_and_clear_status(int* status);
+
 // Kernel ids reported by the timing hook (gdn_profile_*).
 enum KernelId {
   kSimtFwd = 0,
@@ -167,7 +208,12 @@ enum KernelId {
   kKdaStates = 13,
   kKdaBwd = 14,
   kSeqSetup = 15,
-  kNumKernelIds = 16
+  kConvFwd = 16,
+  kConvBwd = 17,
+  kNormFwd = 18,
+  kNormBwd = 19,
+  kSumPartials = 20,
+  kNumKernelIds = 21
 };
 const char* kernel_name(int id);
 

@@ -47,11 +47,12 @@ namespace gdn {
 // The status words of the bounded device-side waits: this file's and the KDA
 // kernels'; a timeout recorded in either is reported.
 cudaError_t read_and_clear_device_status(int* status) {
-  int a = GDN_OK, b = GDN_OK;
+  int a = GDN_OK, b = GDN_OK, c = GDN_OK;
   cudaError_t e = tc::read_and_clear_file_status(&a);
   if (e == cudaSuccess) e = kda_read_and_clear_status(&b);
+  if (e == cudaSuccess) e = nb_read_and_clear_status(&c);
   if (e != cudaSuccess) return e;
-  *status = a != GDN_OK ? a : b;
+  *status = a != GDN_OK ? a : (b != GDN_OK ? b : c);
   return cudaSuccess;
 }
 

@@ -113,3 +113,92 @@ def make_inputs(B: int, T: int, H: int, dk: int, dv: int, *, kda: bool = False,
     if with_dht:
         dht = torch.randn((B, H, dk, dv), generator=gen, device=device).float()
     return MixerInputs(q, k, v, g, beta, h0, do, dht, kda)
+
+
+@dataclasses.dataclass
+class NeighbourInputs:
+    """Inputs of the fused neighbours (short convolution and gated norm)."""
+    x: torch.Tensor       # [B, T, H*D]  projection output (conv input)
+    w: torch.Tensor       # [H*D, W]     fp32 conv taps
+    dz: torch.Tensor      # [B, T, H*D]  gradient of the conv output
+    o: torch.Tensor       # [B, T, H, D] mixer output (norm input)
+    gate: torch.Tensor    # [B, T, H, D] gate projection
+    weight: torch.Tensor  # [D]          fp32 norm weight
+    dout: torch.Tensor    # [B, T, H, D] gradient of the norm output
+
+    def to(self, device) -> "NeighbourInputs":
+        return NeighbourInputs(*(getattr(self, f.name).to(device).contiguous()
+                                 for f in dataclasses.fields(self)))
+
+
+def make_neighbour_inputs(B: int, T: int, H: int, D: int, W: int = 4, *, dtype: str = "bf16",
+                          seed: int = 0, device="cpu") -> NeighbourInputs:
+    """Seeded inputs of the short convolution and the gated norm.
+
+    Recipe (one ``torch.Generator`` seeded with ``seed``; draws in this order):
+    x ~ N(0,1) [B,T,H*D]; w ~ U(-1/sqrt(W), 1/sqrt(W)) [H*D,W] (the default
+    initialisation of a depthwise convolution); dz ~ N(0,1); o ~ N(0,1)
+    [B,T,H,D]; gate ~ N(0,1); weight = 1 + 0.1 N(0,1) [D]; dout ~ N(0,1).
+    x, dz, o, gate and dout are rounded to ``dtype``; w and weight stay fp32.
+    """
+    gen = torch.Generator().manual_seed(seed)
+    dt = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype]
+    n = lambda *s: torch.randn(*s, generator=gen, dtype=torch.float32)
+    x = n(B, T, H * D)
+    w = (torch.rand(H * D, W, generator=gen, dtype=torch.float32) * 2 - 1) / math.sqrt(W)
+    dz = n(B, T, H * D)
+    o = n(B, T, H, D)
+    gate = n(B, T, H, D)
+    weight = 1 + 0.1 * n(D)
+    dout = n(B, T, H, D)
+    r = lambda t: t.to(dt).contiguous()
+    out = NeighbourInputs(r(x), w.contiguous(), r(dz), r(o), r(gate), weight.contiguous(), r(dout))
+    return out.to(device) if str(device) != "cpu" else out
+
+
+@dataclasses.dataclass
+class BlockInputs:
+    """Inputs of the mixer with its neighbours: the q, k, v projections before
+    their short convolutions, the gate and the norm, and the gradient of the
+    block output."""
+    xq: torch.Tensor      # [B, T, H*D]
+    xk: torch.Tensor
+    xv: torch.Tensor
+    wq: torch.Tensor      # [H*D, W] fp32
+    wk: torch.Tensor
+    wv: torch.Tensor
+    g: torch.Tensor       # [B, T, H] (GDN) or [B, T, H, D] (KDA) fp32, log forget gate
+    beta: torch.Tensor    # [B, T, H] fp32
+    gate: torch.Tensor    # [B, T, H, D]
+    weight: torch.Tensor  # [D] fp32
+    dout: torch.Tensor    # [B, T, H, D]
+
+    def to(self, device) -> "BlockInputs":
+        return BlockInputs(*(getattr(self, f.name).to(device).contiguous()
+                             for f in dataclasses.fields(self)))
+
+
+def make_block_inputs(B: int, T: int, H: int, D: int, W: int = 4, *, kda: bool = False,
+                      dtype: str = "bf16", g_mean: float = 2.0, seed: int = 0,
+                      device="cpu") -> BlockInputs:
+    """Seeded inputs of the mixer block (one ``torch.Generator`` seeded with
+    ``seed``; draws in this order): xq, xk, xv ~ N(0,1) [B,T,H*D]; wq, wk, wv ~
+    U(-1/sqrt(W), 1/sqrt(W)) [H*D,W]; beta = sigmoid(N(0,1)) [B,T,H]; g =
+    logsigmoid(N(g_mean,1)) [B,T,H] or [B,T,H,D]; gate ~ N(0,1) [B,T,H,D];
+    weight = 1 + 0.1 N(0,1) [D]; dout ~ N(0,1).  Token tensors are rounded
+    to ``dtype``; weights, g and beta stay fp32.  Drawn on the CPU (the same
+    values on every device), then moved."""
+    gen = torch.Generator().manual_seed(seed)
+    dt = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype]
+    n = lambda *s: torch.randn(*s, generator=gen, dtype=torch.float32)
+    u = lambda: (torch.rand(H * D, W, generator=gen, dtype=torch.float32) * 2 - 1) / math.sqrt(W)
+    r = lambda t: t.to(dt).contiguous()
+    xq, xk, xv = r(n(B, T, H * D)), r(n(B, T, H * D)), r(n(B, T, H * D))
+    wq, wk, wv = u(), u(), u()
+    beta = torch.sigmoid(n(B, T, H))
+    g = F.logsigmoid(n(B, T, H, D) + g_mean if kda else n(B, T, H) + g_mean)
+    gate = r(n(B, T, H, D))
+    weight = 1 + 0.1 * n(D)
+    dout = r(n(B, T, H, D))
+    out = BlockInputs(xq, xk, xv, wq, wk, wv, g.contiguous(), beta.contiguous(), gate, weight, dout)
+    return out.to(device) if str(device) != "cpu" else out

@@ -27,6 +27,8 @@ class Workload:
     h0_std: float | None = None
     fwd_only: bool = False
     delta: bool = True  # False: the Mamba2 mixer (scalar gate, no delta rule)
+    block: bool = False  # the mixer with its fused neighbours (short conv, gated norm)
+    conv_width: int = 4
 
     @property
     def mixer(self) -> str:
@@ -35,6 +37,12 @@ class Workload:
     @property
     def tokens(self) -> int:
         return self.B * self.T
+
+    def make_block(self, device="cpu", seed: int = 0, B: int | None = None):
+        from .inputs import make_block_inputs
+        return make_block_inputs(self.B if B is None else B, self.T, self.H, self.dk,
+                                 self.conv_width, kda=self.kda, dtype=self.dtype,
+                                 g_mean=self.g_mean, seed=seed, device=device)
 
     def make(self, device="cpu", seed: int = 0, with_dht: bool = False, T: int | None = None,
              B: int | None = None):
@@ -53,6 +61,11 @@ KDA_300M_BF16 = Workload("kda_300m_bf16_B16_T2048_H8_d128_C64", 16, 2048, 8, 128
 # with the delta rule) at the 300M pre-training shape.
 MAMBA2_300M_BF16 = Workload("mamba2_300m_bf16_B16_T2048_H8_d128_C64", 16, 2048, 8, 128, 128, 64,
                             delta=False)
+# The GDN layer's token-mixing path at the 300M shape: short convolutions of
+# the q, k, v projections (width 4, q and k L2-normalised), the mixer, and the
+# gated RMS norm of its output, forward and backward.
+GDN_BLOCK_300M_BF16 = Workload("gdn_block_300m_bf16_B16_T2048_H8_d128_C64_W4", 16, 2048, 8, 128,
+                               128, 64, block=True)
 GDN_1B_BF16_H0 = Workload("gdn_1b_bf16_h0_B8_T2048_H16_d128_C64", 8, 2048, 16, 128, 128, 64,
                           h0_std=0.02)
 GDN_1M_FWD_BF16 = Workload("gdn_1m_fwd_bf16_B1_T1048576_H16_d128_C64", 1, 1 << 20, 16, 128,
@@ -66,6 +79,7 @@ GDN_DECODE_BF16 = Workload("gdn_decode_bf16_B256_T1_H16_d128", 256, 1, 16, 128, 
 KDA_DECODE_BF16 = Workload("kda_decode_bf16_B256_T1_H16_d128", 256, 1, 16, 128, 128, 64,
                            kda=True, h0_std=0.02, fwd_only=True)
 
-ALL = [GDN_TINY_FP32, GDN_300M_BF16, KDA_300M_BF16, MAMBA2_300M_BF16, GDN_1B_BF16_H0,
+ALL = [GDN_TINY_FP32, GDN_300M_BF16, KDA_300M_BF16, MAMBA2_300M_BF16, GDN_BLOCK_300M_BF16,
+       GDN_1B_BF16_H0,
        GDN_1M_FWD_BF16, GDN_DECODE_BF16, KDA_DECODE_BF16]
 BY_NAME = {w.name: w for w in ALL}

@@ -284,6 +284,75 @@ GDN_API int kda_decode(const gdn_shape* shape, const void* q, const void* k, con
                        const float* g, const float* beta, const float* h0, void* o, float* ht,
                        void* stream);
 
+/* The mixer's fused neighbours (Primus hybrid-LLM pretraining blog, section
+ * "Recipe", table 4: the "FLA fusions" row fuses the short convolution and
+ * the gated norm around each mixer; the same table's normalisation epsilon
+ * is 1e-6).  Both are elementwise along the tokens and bound by memory
+ * traffic; each reads its inputs once and writes its outputs once.
+ *
+ * Short convolution, per channel c of x [B, T, H*D] (row-major, channel
+ * fastest) with weights w [H*D, W] (fp32, row-major):
+ *   s[t, c] = sum_{i<W} w[c, i] * x[t - W + 1 + i, c]   (x = 0 before the
+ *             start of the token's sequence),
+ *   y = s * sigmoid(s) (SiLU), and with l2norm != 0 each token's D values of
+ *   a head are scaled:  z[t, h, :] = scale * y / sqrt(sum(y^2) + eps),
+ *   else z = y.  The q and k projections take l2norm = 1 (q and k of the
+ *   mixer), v takes l2norm = 0.
+ * The backward recomputes s from x (nothing is saved) and writes dx (same
+ * layout and dtype as x) and dw [H*D, W] (fp32, overwritten, summed over all
+ * tokens in a fixed order: bit-for-bit reproducible) from dz.  It needs
+ * gdn_short_conv_bwd_workspace(shape) bytes of device workspace.
+ *
+ * shape: D in {32, 64, 128}; W in [1, 4]; dtype GDN_F32 or GDN_BF16 (x, z,
+ * dz, dx); B, T, H >= 0 with B*T <= 2^30 and H <= 65535 (an empty problem
+ * launches nothing).  Packed
+ * sequences: cu_seqlens non-NULL, B = 1, T the total token count and
+ * cu_seqlens a DEVICE array of nseq + 1 int32 offsets as for the *_varlen
+ * mixer calls; the convolution restarts at every sequence start.  Offsets
+ * that do not rise from 0 to T give unspecified outputs (every access stays
+ * inside the arrays) and gdn_device_status() returns GDN_ERR_SEQLENS.  With
+ * cu_seqlens NULL, nseq is ignored and each of the B rows is one sequence.
+ * Every token tensor must be 16-byte aligned (GDN_ERR_ALIGN).  Errors:
+ * GDN_ERR_ARG (NULL pointer, eps < 0), GDN_ERR_SHAPE, GDN_ERR_DTYPE,
+ * GDN_ERR_ALIGN, GDN_ERR_WORKSPACE, GDN_ERR_CUDA.  All pointers are device
+ * pointers owned by the caller; the calls are asynchronous on `stream`. */
+typedef struct {
+  int B, T, H, D, W;
+  int dtype;
+} gdn_conv_shape;
+
+GDN_API int gdn_short_conv_fwd(const gdn_conv_shape* shape, const void* x, const float* w,
+                               void* z, int l2norm, float scale, float eps,
+                               const int* cu_seqlens, int nseq, void* stream);
+GDN_API size_t gdn_short_conv_bwd_workspace(const gdn_conv_shape* shape);
+GDN_API int gdn_short_conv_bwd(const gdn_conv_shape* shape, const void* x, const float* w,
+                               const void* dz, void* dx, float* dw, int l2norm, float scale,
+                               float eps, const int* cu_seqlens, int nseq, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/* Gated RMS norm of the mixer output, per row of D values (a row is one
+ * token of one head: o and gate [rows, D], e.g. [B, T, H, dv] with rows =
+ * B*T*H), with weight [D] (fp32) shared by all rows:
+ *   out = o / sqrt(mean(o^2) + eps) * weight * gate * sigmoid(gate).
+ * The backward writes do_ and dgate (layout and dtype of o) and dweight [D]
+ * (fp32, overwritten, reproducible sum) from dout; it needs
+ * gdn_gated_rmsnorm_bwd_workspace(shape) bytes of device workspace.  D in
+ * {32, 64, 128}; rows >= 0; dtype GDN_F32 or GDN_BF16; errors and alignment
+ * as for the short convolution. */
+typedef struct {
+  long long rows;
+  int D;
+  int dtype;
+} gdn_norm_shape;
+
+GDN_API int gdn_gated_rmsnorm_fwd(const gdn_norm_shape* shape, const void* o, const void* gate,
+                                  const float* weight, void* out, float eps, void* stream);
+GDN_API size_t gdn_gated_rmsnorm_bwd_workspace(const gdn_norm_shape* shape);
+GDN_API int gdn_gated_rmsnorm_bwd(const gdn_norm_shape* shape, const void* o, const void* gate,
+                                  const float* weight, const void* dout, void* do_, void* dgate,
+                                  float* dweight, float eps, void* ws, size_t ws_bytes,
+                                  void* stream);
+
 /* Human-readable name of a gdn_status value. */
 GDN_API const char* gdn_status_str(int status);
 

@@ -235,3 +235,80 @@ def test_varlen_validation(L):
     assert fn(ctypes.byref(s1), cu, 3, *args, FAKE, need - 1, None) == GDN_ERR_WORKSPACE
     assert fn(ctypes.byref(s1), cu, 0, *args, None, 0, None) == GDN_OK  # no sequences: nothing to do
     assert L.gdn_status_str(-8).decode().startswith("GDN_ERR_SEQLENS")
+
+
+def conv_shape(B=1, T=64, H=2, D=128, W=4, dtype=1):
+    return gdn.ConvShape(B, T, H, D, W, dtype)
+
+
+def call_conv_fwd(L, s, x=FAKE, w=FAKE, z=FAKE, eps=1e-6, cu=None, nseq=0):
+    return L.gdn_short_conv_fwd(ctypes.byref(s), x, w, z, 1, 1.0, eps, cu, nseq, None)
+
+
+def call_conv_bwd(L, s, ws=FAKE, ws_bytes=1 << 30, **over):
+    a = dict(x=FAKE, w=FAKE, dz=FAKE, dx=FAKE, dw=FAKE)
+    a.update(over)
+    return L.gdn_short_conv_bwd(ctypes.byref(s), a["x"], a["w"], a["dz"], a["dx"], a["dw"], 1, 1.0,
+                                1e-6, None, 0, ws, ws_bytes, None)
+
+
+def test_short_conv_validation(L):
+    for bad in (conv_shape(D=16), conv_shape(D=96), conv_shape(W=0), conv_shape(W=5),
+                conv_shape(T=-1), conv_shape(B=1 << 16, T=1 << 15)):
+        assert call_conv_fwd(L, bad) == GDN_ERR_SHAPE
+    assert call_conv_fwd(L, conv_shape(dtype=3)) == GDN_ERR_DTYPE
+    assert call_conv_fwd(L, conv_shape(), eps=-1.0) == GDN_ERR_ARG
+    assert call_conv_fwd(L, conv_shape(), eps=float("nan")) == GDN_ERR_ARG
+    assert call_conv_fwd(L, conv_shape(), x=None) == GDN_ERR_ARG
+    assert call_conv_fwd(L, conv_shape(), z=ctypes.c_void_p(0x10008)) == GDN_ERR_ALIGN
+    assert L.gdn_short_conv_fwd(None, FAKE, FAKE, FAKE, 0, 1.0, 1e-6, None, 0, None) == GDN_ERR_ARG
+    # packed: B must be 1, nseq >= 0, cu_seqlens 4-byte aligned
+    assert call_conv_fwd(L, conv_shape(B=2), cu=FAKE, nseq=2) == GDN_ERR_SHAPE
+    assert call_conv_fwd(L, conv_shape(), cu=FAKE, nseq=-1) == GDN_ERR_SHAPE
+    assert call_conv_fwd(L, conv_shape(), cu=ctypes.c_void_p(0x10002), nseq=2) == GDN_ERR_ALIGN
+    # no token: nothing to do
+    assert call_conv_fwd(L, conv_shape(B=0), x=None, z=None) == GDN_OK
+    assert call_conv_fwd(L, conv_shape(H=0), x=None, z=None) == GDN_OK
+
+
+def test_short_conv_workspace(L):
+    s = conv_shape(B=16, T=2048, H=8, D=128, W=4)
+    need = L.gdn_short_conv_bwd_workspace(ctypes.byref(s))
+    # one fp32 partial of dw [H*D, W] per CTA column, at most about 1024 CTAs in all
+    assert 8 * 128 * 4 * 4 <= need <= 1100 * 128 * 4 * 4
+    assert L.gdn_short_conv_bwd_workspace(ctypes.byref(conv_shape(D=48))) == 0
+    assert call_conv_bwd(L, conv_shape(), ws=None, ws_bytes=0) == GDN_ERR_WORKSPACE
+    small = L.gdn_short_conv_bwd_workspace(ctypes.byref(conv_shape()))
+    assert call_conv_bwd(L, conv_shape(), ws_bytes=small - 1) == GDN_ERR_WORKSPACE
+    assert call_conv_bwd(L, conv_shape(), dw=None) == GDN_ERR_ARG
+    assert call_conv_bwd(L, conv_shape(), dx=ctypes.c_void_p(0x10004)) == GDN_ERR_ALIGN
+
+
+def test_gated_rmsnorm_validation(L):
+    def fwd(s, **over):
+        a = dict(o=FAKE, gate=FAKE, weight=FAKE, out=FAKE, eps=1e-6)
+        a.update(over)
+        return L.gdn_gated_rmsnorm_fwd(ctypes.byref(s), a["o"], a["gate"], a["weight"], a["out"],
+                                       a["eps"], None)
+    ok = gdn.NormShape(1000, 128, 1)
+    assert fwd(gdn.NormShape(1000, 100, 1)) == GDN_ERR_SHAPE
+    assert fwd(gdn.NormShape(-1, 128, 1)) == GDN_ERR_SHAPE
+    assert fwd(gdn.NormShape(1000, 128, 2)) == GDN_ERR_DTYPE
+    assert fwd(ok, weight=None) == GDN_ERR_ARG
+    assert fwd(ok, eps=-1e-6) == GDN_ERR_ARG
+    assert fwd(ok, gate=ctypes.c_void_p(0x10002)) == GDN_ERR_ALIGN
+    assert fwd(gdn.NormShape(0, 128, 1), o=None, out=None) == GDN_OK
+    need = L.gdn_gated_rmsnorm_bwd_workspace(ctypes.byref(ok))
+    assert 128 * 4 <= need <= 600 * 128 * 4
+    r = L.gdn_gated_rmsnorm_bwd(ctypes.byref(ok), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1e-6,
+                                FAKE, need - 1, None)
+    assert r == GDN_ERR_WORKSPACE
+
+
+def test_neighbour_binding_refuses_cpu_tensors(L):
+    import torch
+    x = torch.zeros(1, 8, 256, dtype=torch.bfloat16)
+    with pytest.raises(gdn.GdnError):
+        gdn.short_conv_fwd(x, torch.zeros(256, 4), H=2)
+    with pytest.raises(gdn.GdnError):
+        gdn.gated_rmsnorm_fwd(x, x, torch.ones(256))
