@@ -14,41 +14,47 @@
 // warp owns one head's D channels of a token (D / 32 per lane), so the head's
 // norms are warp shuffles and a token row is one coalesced access.
 //
-// Short conv: a warp walks a run of kRun consecutive tokens and keeps the
-// previous W - 1 inputs of its channels in registers (the forward reads each
-// row once plus a 3-row halo per run, which the neighbouring warp has just
-// brought into L2).  The backward walks its run backwards, recomputing s from
-// x (no saved activations), with the last three ds values of its channels in
-// registers: dx_t = sum_i w_i ds_{t+W-1-i} needs ds of up to three later
-// tokens, which come from a 3-token halo after the run.  dw is summed per
-// warp in registers, per CTA in shared memory and over CTAs by a second
-// kernel in a fixed order, so the result is bit-for-bit reproducible.
-// Packed sequences split a run where a sequence ends; the windows restart
-// from zeros there.
+// Data movement: every warp streams its work through a private ring of
+// shared-memory stages filled by TMA copies that complete on one mbarrier per
+// stage (a 2-D tensor copy of a chunk's rows of one head for the short conv, a
+// 1-D bulk copy of a block of rows for the norm); the warp issues the copies of the
+// stage after next before it computes on the current one, so each SM keeps
+// 100-200 KB of loads in flight with no register cost and no block-wide
+// barrier.  Work items are numbered head-fastest, so the warps running at
+// any moment read whole token rows (every head of neighbouring tokens).
 //
-// Gated norm: a warp takes kNormRows rows at a time (all loads first, then
-// the arithmetic); dweight is reduced like dw.
+// Short conv: a warp's item is one head over a run of tokens, cut into
+// chunks of TC tokens; a chunk's stage holds its x rows and the three rows
+// before them, so every token reads x_{t-3..t} from shared memory (rows
+// before the token's sequence start count as zero).  The backward walks its
+// item downwards, recomputing s from x (no saved activations), with ds of
+// the next three tokens in registers: dx_t = sum_i w_i ds_{t+W-1-i}; an item
+// also computes ds for the three tokens after it (a halo that it does not
+// store).  dw is summed per warp in registers over its items (all of one
+// head), per CTA in shared memory, and over CTAs by a second kernel in a
+// fixed order, so the result is bit-for-bit reproducible.
+//
+// Gated norm: a warp's item is a block of consecutive rows (one bulk copy per
+// tensor); dweight is reduced like dw.
 
 #include <algorithm>
 #include <type_traits>
 
 #include "gdn.h"
 #include "gdn_internal.cuh"
+#include "tc_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace gdn {
 namespace {
 
 __device__ int g_nb_status = 0;
 
-constexpr int kNbWarps = 8;      // warps per CTA
-constexpr int kRun = 32;         // tokens per warp run (short conv)
-constexpr int kBatchFwd = 8;     // rows loaded ahead (short conv forward)
-constexpr int kBatchBwd = 4;     // token steps loaded ahead (short conv backward)
-constexpr int kNormRows = 4;     // rows per warp step (gated norm forward)
-constexpr int kNormRowsBwd = 2;  // rows per warp step (gated norm backward)
-constexpr int kMaxTaps = 4;      // widest convolution
-constexpr int kConvGroupsTarget = 1024;  // CTAs of the backward conv (before the head split)
-constexpr int kNormCtasMax = 512;
+constexpr int kMaxWarps = 16;       // warps per CTA (one CTA per SM)
+constexpr int kMaxTaps = 4;         // widest convolution
+constexpr int kRingBytes = 200 * 1024;  // shared memory of the staging rings per CTA
+constexpr int kStageTarget = 2048;  // bytes of one tensor's rows per stage (about)
+constexpr uint32_t kWaitTries = 100000;  // bounded mbarrier waits (about 2 s)
 
 // ---------------------------------------------------------------- vector access
 // One lane's EPL consecutive elements as one load: rows are prefetched in
@@ -148,6 +154,72 @@ __device__ __forceinline__ float warp_sum(float x) {
 // 1e-38).
 __device__ __forceinline__ float sigmoid(float s) { return __fdividef(1.f, 1.f + __expf(-s)); }
 
+// ---------------------------------------------------------------- staging
+using tc::fence_async_shared;
+using tc::fence_barrier_init;
+using tc::mbar_arrive_expect_tx;
+using tc::mbar_init;
+using tc::mbar_wait;
+using tc::smem_u32;
+
+// 1-D bulk copy global -> shared completing on `bar` (16-byte aligned
+// addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 2-D tensor copy of the box at (c0 = channel, c1 = row) into shared memory
+// (128-byte aligned), completing on `bar`; rows outside the tensor read as zero.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tmap, uint64_t* bar, int c0,
+                                            int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void report_timeout() { atomicExch(&g_nb_status, GDN_ERR_DEVICE_TIMEOUT); }
+
+// One warp's ring: nstg stages of `bytes` each and one mbarrier per stage.
+struct Ring {
+  unsigned char* buf;
+  uint64_t* full;
+  int bytes, nstg;
+  __device__ unsigned char* stage(int s) const { return buf + (size_t)s * bytes; }
+};
+
+// Carves warp wi's ring out of the dynamic shared memory and initialises its
+// barriers (lane 0); the warp syncs before use.
+__device__ __forceinline__ Ring make_ring(unsigned char* smem, int nw, int wi, int stage_bytes,
+                                          int nstg) {
+  Ring r;
+  smem += (128 - (smem_u32(smem) & 127)) & 127;  // TMA destinations: 128-byte aligned
+  r.buf = smem + (size_t)wi * nstg * stage_bytes;
+  r.full = reinterpret_cast<uint64_t*>(smem + (size_t)nw * nstg * stage_bytes) + wi * nstg;
+  r.bytes = stage_bytes;
+  r.nstg = nstg;
+  if ((threadIdx.x & 31) == 0) {
+    for (int s = 0; s < nstg; ++s) mbar_init(&r.full[s], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  return r;
+}
+
+// After a timed-out wait: wait (bounded) for the copies still in flight into
+// stages [k, k + inflight) so that none lands after the CTA has exited.
+__device__ __forceinline__ void drain(const Ring& r, int k, int inflight) {
+  for (int j = 0; j < inflight; ++j) {
+    const int kk = k + j;
+    mbar_wait(&r.full[kk % r.nstg], (kk / r.nstg) & 1, kWaitTries);
+  }
+}
+
 // ---------------------------------------------------------------- sequence bounds
 // The sequence [lo, hi) that holds flattened token t.  Fixed length: rows of
 // T tokens.  Packed: the largest j with cu[j] <= t.  Both ends are clamped
@@ -201,7 +273,7 @@ struct ConvArgs {
   void* z;
   const void* dz;
   void* dx;
-  float* part;  // backward: [gridDim.x][H*D*W] partial dw
+  float* part;  // backward: partial dw (see conv_partials)
   const int* cu;
   int nseq;
   int T;        // tokens per row (fixed length)
@@ -209,194 +281,365 @@ struct ConvArgs {
   int H, D, W;
   float scale, eps;
   int l2norm;
+  // work split (host): items are (head, part) pairs numbered head-fastest,
+  // part p covering tokens [p L, (p + 1) L); warp gw takes items gw, gw + Wt, ...
+  int L, nitems, Wt;
+  int TC;       // tokens per chunk
+  int nstg, stage_bytes;
+  int dz_off;   // backward: stage offset of the dz box (128-byte aligned)
+  int cta_heads;  // backward: heads per CTA row of the partials (H when H | warps per CTA)
 };
 
+// Items of one warp, cut into chunks of at most TC tokens.  Forward: chunks
+// in rising order over [t0, t1).  Backward: chunks in falling order over
+// [t0, te), te = min(t1 + 3, Ttot) (the own tokens and the ds halo).
+template <bool Bwd>
+struct ChunkIter {
+  int item, h, t0, t1, te, a, b;  // current chunk [a, b)
+  bool valid;
+  __device__ void setup(const ConvArgs& p) {
+    valid = false;
+    for (; item < p.nitems; item += p.Wt) {
+      h = item % p.H;
+      t0 = (item / p.H) * p.L;
+      t1 = min(t0 + p.L, p.Ttot);
+      if (t0 >= t1) continue;
+      te = min(t1 + kMaxTaps - 1, p.Ttot);
+      if (Bwd) {
+        b = te;
+        a = max(b - p.TC, t0);
+      } else {
+        a = t0;
+        b = min(a + p.TC, t1);
+      }
+      valid = true;
+      return;
+    }
+  }
+  __device__ void init(const ConvArgs& p, int gw) {
+    item = gw;
+    setup(p);
+  }
+  __device__ void next(const ConvArgs& p) {
+    if (Bwd) {
+      if (a > t0) {
+        b = a;
+        a = max(b - p.TC, t0);
+        return;
+      }
+    } else if (b < t1) {
+      a = b;
+      b = min(a + p.TC, t1);
+      return;
+    }
+    item += p.Wt;
+    setup(p);
+  }
+};
+
+// Issues one chunk's copies into stage s: the x box of rows [a - 3, a + TC)
+// (rows outside the tensor read as zero and are never used) and, backward,
+// the dz box of rows [a, a + TC) at dz_off.  Stage row r is global row
+// a - 3 + r; only rows below b are used.
+template <bool Bwd>
+__device__ __forceinline__ void issue_chunk(const ConvArgs& p, const Ring& ring, int s,
+                                            const ChunkIter<Bwd>& c, const CUtensorMap* tmx,
+                                            const CUtensorMap* tmdz, int rowb) {
+  if ((threadIdx.x & 31) == 0) {
+    const uint32_t bytes = (p.TC + kMaxTaps - 1 + (Bwd ? p.TC : 0)) * rowb;
+    mbar_arrive_expect_tx(&ring.full[s], bytes);
+    tma_load_2d(ring.stage(s), tmx, &ring.full[s], c.h * p.D, c.a - (kMaxTaps - 1));
+    if (Bwd) tma_load_2d(ring.stage(s) + p.dz_off, tmdz, &ring.full[s], c.h * p.D, c.a);
+  }
+  __syncwarp();
+}
+
 // ---------------------------------------------------------------- short conv forward
-template <typename T, int EPL, bool Packed>
-__global__ void __launch_bounds__(32 * kNbWarps, 2) short_conv_fwd_kernel(ConvArgs a) {
-  if (Packed && blockIdx.x == 0 && blockIdx.y == 0) check_offsets(a.cu, a.nseq, a.Ttot);
-  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
-  const int h = blockIdx.y;
+// x_{t-3..t} of the lane's channels from the chunk's stage (rows below lo,
+// the token's sequence start, read as zero unless Fast says none is).
+template <typename T, int EPL, bool Fast>
+__device__ __forceinline__ void load_window(const unsigned char* xs, int xb, int rowb, int t, int lo,
+                                            float (&xv)[kMaxTaps][EPL]) {
+#pragma unroll
+  for (int j = 0; j < kMaxTaps; ++j) {
+    const int row = t - (kMaxTaps - 1) + j;
+    if (Fast || row >= lo)
+      widen<T, EPL>(*reinterpret_cast<const typename Raw<T, EPL>::type*>(xs + (row - xb) * rowb),
+                    xv[j]);
+    else
+      zero(xv[j]);
+  }
+}
+
+// One token of the forward: z = SiLU(sum_j wp_j x_{t-3+j}), L2-normalised per head.
+template <typename T, int EPL, bool Norm, bool Fast>
+__device__ __forceinline__ void conv_fwd_token(const unsigned char* xs, int xb, int rowb, int t,
+                                               int lo, const float (&wp)[kMaxTaps][EPL],
+                                               float scale, float eps, T* __restrict__ zrow) {
+  float xv[kMaxTaps][EPL];
+  load_window<T, EPL, Fast>(xs, xb, rowb, t, lo, xv);
+  float y[EPL];
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    float sv = wp[kMaxTaps - 1][e] * xv[kMaxTaps - 1][e];
+#pragma unroll
+    for (int j = 0; j < kMaxTaps - 1; ++j) sv = fmaf(wp[j][e], xv[j][e], sv);
+    y[e] = sv * sigmoid(sv);
+    ss = fmaf(y[e], y[e], ss);
+  }
+  if (Norm) {
+    const float r = scale * rsqrtf(warp_sum(ss) + eps);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) y[e] *= r;
+  }
+  stv<T, EPL>(zrow, y);
+}
+
+template <typename T, int EPL, bool Packed, bool Norm>
+__global__ void __launch_bounds__(32 * kMaxWarps, 1)
+short_conv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, ConvArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  if (Packed && blockIdx.x == 0) check_offsets(a.cu, a.nseq, a.Ttot);
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const Ring ring = make_ring(smem, nw, wi, a.stage_bytes, a.nstg);
+  const int gw = blockIdx.x * nw + wi;
+  const int rowb = a.D * (int)sizeof(T);
   const long CH = (long)a.H * a.D;
-  const int c0 = h * a.D + lane * EPL;
-  const T* __restrict__ x = static_cast<const T*>(a.x) + c0;
-  T* __restrict__ z = static_cast<T*>(a.z) + c0;
+  ChunkIter<false> pc, cc;
+  pc.init(a, gw);
+  cc = pc;
+  int issued = 0;
+  for (; issued < a.nstg && pc.valid; ++issued, pc.next(a))
+    issue_chunk<false>(a, ring, issued, pc, &tmx, &tmx, rowb);
+  int h = -1;
   float wp[kMaxTaps][EPL];
-  load_taps<EPL>(a.w, a.W, c0, wp);
-  const int nruns = (a.Ttot + kRun - 1) / kRun;
-#pragma unroll 1
-  for (int r = blockIdx.x * kNbWarps + wi; r < nruns; r += gridDim.x * kNbWarps) {
-    const int r1 = min((r + 1) * kRun, a.Ttot);
-#pragma unroll 1
-    for (int t0 = r * kRun; t0 < r1;) {
-      int lo, hi;
-      seq_bounds<Packed>(t0, a.T, a.Ttot, a.cu, a.nseq, lo, hi);
-      const int t1 = min(r1, hi);
-      float win[kMaxTaps - 1][EPL];  // x_{t-3}, x_{t-2}, x_{t-1}
+  for (int k = 0; cc.valid; ++k, cc.next(a)) {
+    const int s = k % a.nstg;
+    if (!mbar_wait(&ring.full[s], (k / a.nstg) & 1, kWaitTries)) {
+      if (lane == 0) report_timeout();
+      drain(ring, k + 1, issued - k - 1);
+      return;
+    }
+    if (cc.h != h) {
+      h = cc.h;
+      load_taps<EPL>(a.w, a.W, h * a.D + lane * EPL, wp);
+    }
+    const unsigned char* xs = ring.stage(s) + lane * EPL * (int)sizeof(T);
+    const int xb = cc.a - (kMaxTaps - 1);  // global row of stage row 0
+    T* __restrict__ z = static_cast<T*>(a.z) + h * a.D + lane * EPL;
+    int lo, hi;
+    seq_bounds<Packed>(cc.a, a.T, a.Ttot, a.cu, a.nseq, lo, hi);
+    int t = cc.a;
+    if (lo <= xb && hi >= cc.b) {
+      // no sequence start among the chunk's rows: four independent tokens at a time
+      for (; t + 4 <= cc.b; t += 4) {
 #pragma unroll
-      for (int j = 0; j < kMaxTaps - 1; ++j) {
-        const int row = t0 - (kMaxTaps - 1) + j;
-        if (row >= lo) ldv<T, EPL>(x + (long)row * CH, win[j]); else zero(win[j]);
+        for (int q = 0; q < 4; ++q)
+          conv_fwd_token<T, EPL, Norm, true>(xs, xb, rowb, t + q, lo, wp, a.scale, a.eps,
+                                             z + (long)(t + q) * CH);
       }
-#pragma unroll 1
-      for (int t = t0; t < t1; t += kBatchFwd) {
-        typename Raw<T, EPL>::type xraw[kBatchFwd];
-#pragma unroll
-        for (int u = 0; u < kBatchFwd; ++u)
-          if (t + u < t1) xraw[u] = ldr<T, EPL>(x + (long)(t + u) * CH);
-#pragma unroll
-        for (int u = 0; u < kBatchFwd; ++u) {
-          if (t + u >= t1) break;
-          float xr[EPL], y[EPL];
-          widen<T, EPL>(xraw[u], xr);
-          float ss = 0.f;
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) {
-            float s = wp[kMaxTaps - 1][e] * xr[e];
-#pragma unroll
-            for (int j = 0; j < kMaxTaps - 1; ++j) s = fmaf(wp[j][e], win[j][e], s);
-            y[e] = s * sigmoid(s);
-            ss = fmaf(y[e], y[e], ss);
-          }
-          if (a.l2norm) {
-            const float r = a.scale * rsqrtf(warp_sum(ss) + a.eps);
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) y[e] *= r;
-          }
-          stv<T, EPL>(z + (long)(t + u) * CH, y);
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) {
-            win[0][e] = win[1][e];
-            win[1][e] = win[2][e];
-            win[2][e] = xr[e];
-          }
-        }
+      for (; t < cc.b; ++t)
+        conv_fwd_token<T, EPL, Norm, true>(xs, xb, rowb, t, lo, wp, a.scale, a.eps, z + (long)t * CH);
+    } else {
+      for (; t < cc.b; ++t) {
+        if (t >= hi) seq_bounds<Packed>(t, a.T, a.Ttot, a.cu, a.nseq, lo, hi);
+        conv_fwd_token<T, EPL, Norm, false>(xs, xb, rowb, t, lo, wp, a.scale, a.eps, z + (long)t * CH);
       }
-      t0 = t1;
+    }
+    __syncwarp();
+    fence_async_shared();
+    if (pc.valid) {
+      issue_chunk<false>(a, ring, s, pc, &tmx, &tmx, rowb);
+      pc.next(a);
+      ++issued;
     }
   }
 }
 
 // ---------------------------------------------------------------- short conv backward
-template <typename T, int EPL, bool Packed>
-__global__ void __launch_bounds__(32 * kNbWarps, 2) short_conv_bwd_kernel(ConvArgs a) {
-  __shared__ float red[kNbWarps][kMaxTaps][128];
-  if (Packed && blockIdx.x == 0 && blockIdx.y == 0) check_offsets(a.cu, a.nseq, a.Ttot);
-  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
-  const int h = blockIdx.y;
-  const long CH = (long)a.H * a.D;
-  const int c0 = h * a.D + lane * EPL;
-  const T* __restrict__ x = static_cast<const T*>(a.x) + c0;
-  const T* __restrict__ dz = static_cast<const T*>(a.dz) + c0;
-  T* __restrict__ dx = static_cast<T*>(a.dx) + c0;
-  float wp[kMaxTaps][EPL];
-  load_taps<EPL>(a.w, a.W, c0, wp);
-  float dwp[kMaxTaps][EPL];
+// ds_t of one token: the gradient at the pre-activation s_t from dz_t
+// (through the L2 norm and SiLU); dwp gains ds_t x_{t-3+j} for own tokens.
+template <typename T, int EPL, bool Norm, bool Fast>
+__device__ __forceinline__ void conv_bwd_ds(const unsigned char* xs, const unsigned char* dzs,
+                                            int xb, int a0, int rowb, int t, int lo, bool own,
+                                            const float (&wp)[kMaxTaps][EPL], float scale,
+                                            float eps, float (&ds)[EPL],
+                                            float (&dwp)[kMaxTaps][EPL]) {
+  float gr[EPL], xv[kMaxTaps][EPL];
+  load_window<T, EPL, Fast>(xs, xb, rowb, t, lo, xv);
+  widen<T, EPL>(*reinterpret_cast<const typename Raw<T, EPL>::type*>(dzs + (t - a0) * rowb), gr);
+  float sv[EPL], sg[EPL], y[EPL];
+  float ss = 0.f, yg = 0.f;
 #pragma unroll
-  for (int j = 0; j < kMaxTaps; ++j) zero(dwp[j]);
-  const int nruns = (a.Ttot + kRun - 1) / kRun;
-#pragma unroll 1
-  for (int r = blockIdx.x * kNbWarps + wi; r < nruns; r += gridDim.x * kNbWarps) {
-    const int r1 = min((r + 1) * kRun, a.Ttot);
-#pragma unroll 1
-    for (int t0 = r * kRun; t0 < r1;) {
-      int lo, hi;
-      seq_bounds<Packed>(t0, a.T, a.Ttot, a.cu, a.nseq, lo, hi);
-      const int t1 = min(r1, hi);             // own tokens [t0, t1)
-      const int te = min(t1 + kMaxTaps - 1, hi);  // plus the halo [t1, te)
-      typename Raw<T, EPL>::type xw[kMaxTaps];  // x_{t-3} .. x_t, as loaded
-#pragma unroll
-      for (int j = 0; j < kMaxTaps; ++j) {
-        const int row = te - kMaxTaps + j;
-        xw[j] = row >= lo ? ldr<T, EPL>(x + (long)row * CH) : raw_zero<T, EPL>();
-      }
-      float dsw[kMaxTaps - 1][EPL];  // ds_{t+1}, ds_{t+2}, ds_{t+3}
-#pragma unroll
-      for (int j = 0; j < kMaxTaps - 1; ++j) zero(dsw[j]);
-#pragma unroll 1
-      for (int t = te - 1; t >= t0; t -= kBatchBwd) {
-        typename Raw<T, EPL>::type graw[kBatchBwd], xnraw[kBatchBwd];
-#pragma unroll
-        for (int u = 0; u < kBatchBwd; ++u) {
-          const int tu = t - u;
-          if (tu >= t0) {
-            graw[u] = ldr<T, EPL>(dz + (long)tu * CH);
-            xnraw[u] = tu - kMaxTaps >= lo ? ldr<T, EPL>(x + (long)(tu - kMaxTaps) * CH) : raw_zero<T, EPL>();
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kBatchBwd; ++u) {
-          const int tu = t - u;
-          if (tu < t0) break;
-          float gr[EPL], xv[kMaxTaps][EPL];
-          widen<T, EPL>(graw[u], gr);
-#pragma unroll
-          for (int j = 0; j < kMaxTaps; ++j) widen<T, EPL>(xw[j], xv[j]);
-          float s[EPL], sg[EPL], y[EPL];
-          float ss = 0.f, yg = 0.f;
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) {
-            float v = 0.f;
-#pragma unroll
-            for (int j = 0; j < kMaxTaps; ++j) v = fmaf(wp[j][e], xv[j][e], v);
-            s[e] = v;
-            sg[e] = sigmoid(v);
-            y[e] = v * sg[e];
-            ss = fmaf(y[e], y[e], ss);
-            yg = fmaf(y[e], gr[e], yg);
-          }
-          float ds[EPL];
-          if (a.l2norm) {
-            const float r = rsqrtf(warp_sum(ss) + a.eps);
-            const float c = r * r * warp_sum(yg);
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) ds[e] = a.scale * r * (gr[e] - y[e] * c);
-          } else {
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) ds[e] = gr[e];
-          }
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) ds[e] *= sg[e] * (1.f + s[e] * (1.f - sg[e]));
-          if (tu < t1) {
-            float d[EPL];
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) {
-              d[e] = wp[kMaxTaps - 1][e] * ds[e];
-#pragma unroll
-              for (int j = 0; j < kMaxTaps - 1; ++j) d[e] = fmaf(wp[kMaxTaps - 2 - j][e], dsw[j][e], d[e]);
-#pragma unroll
-              for (int j = 0; j < kMaxTaps; ++j) dwp[j][e] = fmaf(ds[e], xv[j][e], dwp[j][e]);
-            }
-            stv<T, EPL>(dx + (long)tu * CH, d);
-          }
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) {
-            dsw[2][e] = dsw[1][e];
-            dsw[1][e] = dsw[0][e];
-            dsw[0][e] = ds[e];
-          }
-          xw[3] = xw[2];
-          xw[2] = xw[1];
-          xw[1] = xw[0];
-          xw[0] = xnraw[u];
-        }
-      }
-      t0 = t1;
-    }
-  }
-  // per-CTA partial dw, unpadded taps: part[blockIdx.x][c][i]
-#pragma unroll
-  for (int j = 0; j < kMaxTaps; ++j)
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) red[wi][j][lane * EPL + e] = dwp[j][e];
-  __syncthreads();
-  float* out = a.part + (long)blockIdx.x * CH * a.W + (long)h * a.D * a.W;
-  for (int k = threadIdx.x; k < a.D * a.W; k += blockDim.x) {
-    const int c = k / a.W, j = k % a.W + (kMaxTaps - a.W);
+  for (int e = 0; e < EPL; ++e) {
     float v = 0.f;
 #pragma unroll
-    for (int w = 0; w < kNbWarps; ++w) v += red[w][j][c];
-    out[k] = v;
+    for (int j = 0; j < kMaxTaps; ++j) v = fmaf(wp[j][e], xv[j][e], v);
+    sv[e] = v;
+    sg[e] = sigmoid(v);
+    y[e] = v * sg[e];
+    ss = fmaf(y[e], y[e], ss);
+    yg = fmaf(y[e], gr[e], yg);
+  }
+  if (Norm) {
+    const float r = rsqrtf(warp_sum(ss) + eps);
+    const float c = r * r * warp_sum(yg);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) ds[e] = scale * r * (gr[e] - y[e] * c);
+  } else {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) ds[e] = gr[e];
+  }
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) ds[e] *= sg[e] * (1.f + sv[e] * (1.f - sg[e]));
+  if (own)
+#pragma unroll
+    for (int j = 0; j < kMaxTaps; ++j)
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) dwp[j][e] = fmaf(ds[e], xv[j][e], dwp[j][e]);
+}
+
+// dx_t = sum_j wp_j ds_{t+3-j} from ds_t and the window of later ds (own
+// tokens only); then the window moves down one token.
+template <typename T, int EPL>
+__device__ __forceinline__ void conv_bwd_finish(bool own, const float (&wp)[kMaxTaps][EPL],
+                                                const float (&ds)[EPL],
+                                                float (&dsw)[kMaxTaps - 1][EPL],
+                                                T* __restrict__ dxrow) {
+  if (own) {
+    float d[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      d[e] = wp[kMaxTaps - 1][e] * ds[e];
+#pragma unroll
+      for (int j = 0; j < kMaxTaps - 1; ++j) d[e] = fmaf(wp[kMaxTaps - 2 - j][e], dsw[j][e], d[e]);
+    }
+    stv<T, EPL>(dxrow, d);
+  }
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    dsw[2][e] = dsw[1][e];
+    dsw[1][e] = dsw[0][e];
+    dsw[0][e] = ds[e];
+  }
+}
+
+template <typename T, int EPL, bool Packed, bool Norm>
+__global__ void __launch_bounds__(32 * kMaxWarps, 1)
+short_conv_bwd_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmdz,
+                      ConvArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  if (Packed && blockIdx.x == 0) check_offsets(a.cu, a.nseq, a.Ttot);
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const Ring ring = make_ring(smem, nw, wi, a.stage_bytes, a.nstg);
+  const int gw = blockIdx.x * nw + wi;
+  const int rowb = a.D * (int)sizeof(T);
+  const long CH = (long)a.H * a.D;
+  ChunkIter<true> pc, cc;
+  pc.init(a, gw);
+  cc = pc;
+  const int h = cc.valid ? cc.h : -1;  // every item of a warp has the same head (Wt % H == 0)
+  float wp[kMaxTaps][EPL], dwp[kMaxTaps][EPL];
+  if (h >= 0) load_taps<EPL>(a.w, a.W, h * a.D + lane * EPL, wp);
+#pragma unroll
+  for (int j = 0; j < kMaxTaps; ++j) zero(dwp[j]);
+  int issued = 0;
+  for (; issued < a.nstg && pc.valid; ++issued, pc.next(a))
+    issue_chunk<true>(a, ring, issued, pc, &tmx, &tmdz, rowb);
+  int item = -1, lo = 0, hi = 0;
+  float dsw[kMaxTaps - 1][EPL];  // ds of the next three tokens (same sequence), else 0
+  for (int k = 0; cc.valid; ++k, cc.next(a)) {
+    const int s = k % a.nstg;
+    if (!mbar_wait(&ring.full[s], (k / a.nstg) & 1, kWaitTries)) {
+      if (lane == 0) report_timeout();
+      drain(ring, k + 1, issued - k - 1);
+      break;
+    }
+    const unsigned char* xs = ring.stage(s) + lane * EPL * (int)sizeof(T);
+    const unsigned char* dzs = xs + a.dz_off;
+    const int xb = cc.a - (kMaxTaps - 1);
+    T* __restrict__ dx = static_cast<T*>(a.dx) + h * a.D + lane * EPL;
+    if (cc.item != item) {  // a new item starts at its top: no later ds
+      item = cc.item;
+#pragma unroll
+      for (int j = 0; j < kMaxTaps - 1; ++j) zero(dsw[j]);
+      seq_bounds<Packed>(cc.b - 1, a.T, a.Ttot, a.cu, a.nseq, lo, hi);
+    }
+    int t = cc.b - 1;
+    if (lo <= xb) {
+      // the chunk's tokens and rows all lie in one sequence: ds of four
+      // tokens at a time, then their dx from the top down
+      for (; t - 3 >= cc.a; t -= 4) {
+        float ds[4][EPL];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          conv_bwd_ds<T, EPL, Norm, true>(xs, dzs, xb, cc.a, rowb, t - q, lo, t - q < cc.t1, wp,
+                                          a.scale, a.eps, ds[q], dwp);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          conv_bwd_finish<T, EPL>(t - q < cc.t1, wp, ds[q], dsw, dx + (long)(t - q) * CH);
+      }
+      for (; t >= cc.a; --t) {
+        float ds[EPL];
+        conv_bwd_ds<T, EPL, Norm, true>(xs, dzs, xb, cc.a, rowb, t, lo, t < cc.t1, wp, a.scale,
+                                        a.eps, ds, dwp);
+        conv_bwd_finish<T, EPL>(t < cc.t1, wp, ds, dsw, dx + (long)t * CH);
+      }
+    } else {
+      for (; t >= cc.a; --t) {
+        if (t < lo) {  // crossed into the previous sequence
+          seq_bounds<Packed>(t, a.T, a.Ttot, a.cu, a.nseq, lo, hi);
+#pragma unroll
+          for (int j = 0; j < kMaxTaps - 1; ++j) zero(dsw[j]);
+        }
+        float ds[EPL];
+        conv_bwd_ds<T, EPL, Norm, false>(xs, dzs, xb, cc.a, rowb, t, lo, t < cc.t1, wp, a.scale,
+                                         a.eps, ds, dwp);
+        conv_bwd_finish<T, EPL>(t < cc.t1, wp, ds, dsw, dx + (long)t * CH);
+      }
+    }
+    __syncwarp();
+    fence_async_shared();
+    if (pc.valid) {
+      issue_chunk<true>(a, ring, s, pc, &tmx, &tmdz, rowb);
+      pc.next(a);
+      ++issued;
+    }
+  }
+  // partial dw: the CTA's warps sum their registers per head in shared memory
+  // (the rings are done), then one row per CTA (cta_heads heads) or per warp
+  __syncthreads();
+  float* red = reinterpret_cast<float*>(smem);  // [nw][D * W]
+  const int DW = a.D * a.W;
+  if (h >= 0) {
+#pragma unroll
+    for (int j = 0; j < kMaxTaps; ++j) {
+      const int i = j - (kMaxTaps - a.W);
+      if (i >= 0)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) red[wi * DW + (lane * EPL + e) * a.W + i] = dwp[j][e];
+    }
+  } else {
+    for (int k = lane; k < DW; k += 32) red[wi * DW + k] = 0.f;
+  }
+  __syncthreads();
+  if (a.cta_heads == a.H) {
+    // H divides the warps of a CTA: warp w has head w % H; one row per CTA
+    float* out = a.part + (long)blockIdx.x * a.H * DW;
+    for (int k = threadIdx.x; k < a.H * DW; k += blockDim.x) {
+      const int hh = k / DW, c = k % DW;
+      float v = 0.f;
+      for (int w = hh; w < nw; w += a.H) v += red[w * DW + c];
+      out[k] = v;
+    }
+  } else {
+    // one row per warp: warp gw = q H + h writes row q, head h
+    for (int k = threadIdx.x; k < nw * DW; k += blockDim.x) {
+      const int w = k / DW, c = k % DW;
+      const int g = blockIdx.x * nw + w;
+      a.part[(long)g * DW + c] = red[w * DW + c];
+    }
   }
 }
 
@@ -433,52 +676,136 @@ struct NormArgs {
   long rows;
   int D;
   float eps;
+  int RC;       // rows per chunk; warp gw takes chunks gw, gw + Wt, ...
+  long nchunks;
+  int Wt, nstg, stage_bytes;
 };
 
+// Issues chunk ch's rows of `ntens` tensors into stage s (one bulk copy each).
+__device__ __forceinline__ void issue_rows(const NormArgs& p, const Ring& ring, int s, long ch,
+                                           const void* const* src, int ntens, int rowb) {
+  if ((threadIdx.x & 31) != 0) return;
+  const long r0 = ch * p.RC;
+  const int n = (int)min((long)p.RC, p.rows - r0);
+  const uint32_t bytes = (uint32_t)(n * rowb);
+  mbar_arrive_expect_tx(&ring.full[s], bytes * ntens);
+  for (int i = 0; i < ntens; ++i)
+    bulk_copy(ring.stage(s) + i * p.RC * rowb,
+              static_cast<const unsigned char*>(src[i]) + r0 * rowb, bytes, &ring.full[s]);
+}
+
+// One row of the gated norm: out = o r weight SiLU(gate), r = 1 / sqrt(mean(o^2) + eps).
 template <typename T, int EPL>
-__global__ void __launch_bounds__(32 * kNbWarps, 2) gated_rmsnorm_fwd_kernel(NormArgs a) {
-  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
-  const int c0 = lane * EPL;
+__device__ __forceinline__ void norm_fwd_row(const unsigned char* os, const unsigned char* gs,
+                                             const float (&wt)[EPL], float invD, float eps,
+                                             T* __restrict__ out) {
+  float ov[EPL], gv[EPL];
+  widen<T, EPL>(*reinterpret_cast<const typename Raw<T, EPL>::type*>(os), ov);
+  widen<T, EPL>(*reinterpret_cast<const typename Raw<T, EPL>::type*>(gs), gv);
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) ss = fmaf(ov[e], ov[e], ss);
+  const float r = rsqrtf(warp_sum(ss) * invD + eps);
+  float y[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) y[e] = ov[e] * r * wt[e] * (gv[e] * sigmoid(gv[e]));
+  stv<T, EPL>(out, y);
+}
+
+// One row of the gated norm's backward: do, dgate, and the row's dweight terms.
+template <typename T, int EPL>
+__device__ __forceinline__ void norm_bwd_row(const unsigned char* os, const unsigned char* gs,
+                                             const unsigned char* ds, const float (&wt)[EPL],
+                                             float invD, float eps, float (&dwt)[EPL],
+                                             T* __restrict__ dO, T* __restrict__ dgate) {
+  float ov[EPL], gv[EPL], dv[EPL];
+  widen<T, EPL>(*reinterpret_cast<const typename Raw<T, EPL>::type*>(os), ov);
+  widen<T, EPL>(*reinterpret_cast<const typename Raw<T, EPL>::type*>(gs), gv);
+  widen<T, EPL>(*reinterpret_cast<const typename Raw<T, EPL>::type*>(ds), dv);
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) ss = fmaf(ov[e], ov[e], ss);
+  const float r = rsqrtf(warp_sum(ss) * invD + eps);
+  float nrm[EPL], sg[EPL], dn[EPL];
+  float dot = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    nrm[e] = ov[e] * r;
+    sg[e] = sigmoid(gv[e]);
+    const float act = gv[e] * sg[e];
+    dn[e] = dv[e] * wt[e] * act;
+    dot = fmaf(dn[e], nrm[e], dot);
+    dwt[e] = fmaf(dv[e] * nrm[e], act, dwt[e]);
+  }
+  const float c = warp_sum(dot) * invD;
+  float d_o[EPL], d_g[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    d_o[e] = r * (dn[e] - nrm[e] * c);
+    d_g[e] = dv[e] * nrm[e] * wt[e] * sg[e] * (1.f + gv[e] * (1.f - sg[e]));
+  }
+  stv<T, EPL>(dO, d_o);
+  stv<T, EPL>(dgate, d_g);
+}
+
+template <typename T, int EPL>
+__global__ void __launch_bounds__(32 * kMaxWarps, 1) gated_rmsnorm_fwd_kernel(NormArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const Ring ring = make_ring(smem, nw, wi, a.stage_bytes, a.nstg);
+  const long gw = (long)blockIdx.x * nw + wi;
+  const int rowb = a.D * (int)sizeof(T), c0 = lane * EPL;
+  const void* src[2] = {a.o, a.gate};
   float wt[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) wt[e] = a.weight[c0 + e];
   const float invD = 1.f / (float)a.D;
-  const T* __restrict__ o = static_cast<const T*>(a.o) + c0;
-  const T* __restrict__ gate = static_cast<const T*>(a.gate) + c0;
-  T* __restrict__ out = static_cast<T*>(a.out) + c0;
-  const long step = (long)gridDim.x * kNbWarps * kNormRows;
-#pragma unroll 1
-  for (long r0 = ((long)blockIdx.x * kNbWarps + wi) * kNormRows; r0 < a.rows; r0 += step) {
-    typename Raw<T, EPL>::type oraw[kNormRows], graw[kNormRows];
+  long pch = gw;
+  int issued = 0;
+  for (; issued < a.nstg && pch < a.nchunks; ++issued, pch += a.Wt)
+    issue_rows(a, ring, issued, pch, src, 2, rowb);
+  __syncwarp();
+  int k = 0;
+  for (long ch = gw; ch < a.nchunks; ch += a.Wt, ++k) {
+    const int s = k % a.nstg;
+    if (!mbar_wait(&ring.full[s], (k / a.nstg) & 1, kWaitTries)) {
+      if (lane == 0) report_timeout();
+      drain(ring, k + 1, issued - k - 1);
+      return;
+    }
+    const unsigned char* os = ring.stage(s) + c0 * (int)sizeof(T);
+    const unsigned char* gs = os + a.RC * rowb;
+    const long r0 = ch * a.RC;
+    const int n = (int)min((long)a.RC, a.rows - r0);
+    T* __restrict__ out = static_cast<T*>(a.out) + r0 * a.D + c0;
+    int u = 0;
+    for (; u + 4 <= n; u += 4) {
 #pragma unroll
-    for (int u = 0; u < kNormRows; ++u)
-      if (r0 + u < a.rows) {
-        oraw[u] = ldr<T, EPL>(o + r0 * a.D + u * a.D);
-        graw[u] = ldr<T, EPL>(gate + r0 * a.D + u * a.D);
-      }
-#pragma unroll
-    for (int u = 0; u < kNormRows; ++u) {
-      if (r0 + u >= a.rows) break;
-      float ov[EPL], gv[EPL];
-      widen<T, EPL>(oraw[u], ov);
-      widen<T, EPL>(graw[u], gv);
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) ss = fmaf(ov[e], ov[e], ss);
-      const float r = rsqrtf(warp_sum(ss) * invD + a.eps);
-      float y[EPL];
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) y[e] = ov[e] * r * wt[e] * (gv[e] * sigmoid(gv[e]));
-      stv<T, EPL>(out + r0 * a.D + u * a.D, y);
+      for (int q = 0; q < 4; ++q)
+        norm_fwd_row<T, EPL>(os + (u + q) * rowb, gs + (u + q) * rowb, wt, invD, a.eps,
+                             out + (long)(u + q) * a.D);
+    }
+    for (; u < n; ++u)
+      norm_fwd_row<T, EPL>(os + u * rowb, gs + u * rowb, wt, invD, a.eps, out + (long)u * a.D);
+    __syncwarp();
+    fence_async_shared();
+    if (pch < a.nchunks) {
+      issue_rows(a, ring, s, pch, src, 2, rowb);
+      __syncwarp();
+      pch += a.Wt;
+      ++issued;
     }
   }
 }
 
 template <typename T, int EPL>
-__global__ void __launch_bounds__(32 * kNbWarps, 2) gated_rmsnorm_bwd_kernel(NormArgs a) {
-  __shared__ float red[kNbWarps][128];
-  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
-  const int c0 = lane * EPL;
+__global__ void __launch_bounds__(32 * kMaxWarps, 1) gated_rmsnorm_bwd_kernel(NormArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const Ring ring = make_ring(smem, nw, wi, a.stage_bytes, a.nstg);
+  const long gw = (long)blockIdx.x * nw + wi;
+  const int rowb = a.D * (int)sizeof(T), c0 = lane * EPL;
+  const void* src[3] = {a.o, a.gate, a.dout};
   float wt[EPL], dwt[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) {
@@ -486,130 +813,121 @@ __global__ void __launch_bounds__(32 * kNbWarps, 2) gated_rmsnorm_bwd_kernel(Nor
     dwt[e] = 0.f;
   }
   const float invD = 1.f / (float)a.D;
-  const T* __restrict__ o = static_cast<const T*>(a.o) + c0;
-  const T* __restrict__ gate = static_cast<const T*>(a.gate) + c0;
-  const T* __restrict__ dout = static_cast<const T*>(a.dout) + c0;
-  T* __restrict__ dO = static_cast<T*>(a.dO) + c0;
-  T* __restrict__ dgate = static_cast<T*>(a.dgate) + c0;
-  const long step = (long)gridDim.x * kNbWarps * kNormRowsBwd;
-#pragma unroll 1
-  for (long r0 = ((long)blockIdx.x * kNbWarps + wi) * kNormRowsBwd; r0 < a.rows; r0 += step) {
-    typename Raw<T, EPL>::type oraw[kNormRowsBwd], graw[kNormRowsBwd], draw[kNormRowsBwd];
+  long pch = gw;
+  int issued = 0;
+  for (; issued < a.nstg && pch < a.nchunks; ++issued, pch += a.Wt)
+    issue_rows(a, ring, issued, pch, src, 3, rowb);
+  __syncwarp();
+  int k = 0;
+  for (long ch = gw; ch < a.nchunks; ch += a.Wt, ++k) {
+    const int s = k % a.nstg;
+    if (!mbar_wait(&ring.full[s], (k / a.nstg) & 1, kWaitTries)) {
+      if (lane == 0) report_timeout();
+      drain(ring, k + 1, issued - k - 1);
+      break;
+    }
+    const unsigned char* os = ring.stage(s) + c0 * (int)sizeof(T);
+    const unsigned char* gs = os + a.RC * rowb;
+    const unsigned char* dsm = gs + a.RC * rowb;
+    const long r0 = ch * a.RC;
+    const int n = (int)min((long)a.RC, a.rows - r0);
+    T* __restrict__ dO = static_cast<T*>(a.dO) + r0 * a.D + c0;
+    T* __restrict__ dgate = static_cast<T*>(a.dgate) + r0 * a.D + c0;
+    int u = 0;
+    for (; u + 4 <= n; u += 4) {
 #pragma unroll
-    for (int u = 0; u < kNormRowsBwd; ++u)
-      if (r0 + u < a.rows) {
-        const long off = r0 * a.D + u * a.D;
-        oraw[u] = ldr<T, EPL>(o + off);
-        graw[u] = ldr<T, EPL>(gate + off);
-        draw[u] = ldr<T, EPL>(dout + off);
-      }
-#pragma unroll
-    for (int u = 0; u < kNormRowsBwd; ++u) {
-      if (r0 + u >= a.rows) break;
-      float ov[EPL], gv[EPL], dv[EPL];
-      widen<T, EPL>(oraw[u], ov);
-      widen<T, EPL>(graw[u], gv);
-      widen<T, EPL>(draw[u], dv);
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) ss = fmaf(ov[e], ov[e], ss);
-      const float r = rsqrtf(warp_sum(ss) * invD + a.eps);
-      float n[EPL], sg[EPL], dn[EPL];
-      float dot = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        n[e] = ov[e] * r;
-        sg[e] = sigmoid(gv[e]);
-        const float act = gv[e] * sg[e];
-        dn[e] = dv[e] * wt[e] * act;
-        dot = fmaf(dn[e], n[e], dot);
-        dwt[e] = fmaf(dv[e] * n[e], act, dwt[e]);
-      }
-      const float c = warp_sum(dot) * invD;
-      float d_o[EPL], d_g[EPL];
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        d_o[e] = r * (dn[e] - n[e] * c);
-        d_g[e] = dv[e] * n[e] * wt[e] * sg[e] * (1.f + gv[e] * (1.f - sg[e]));
-      }
-      const long off = r0 * a.D + u * a.D;
-      stv<T, EPL>(dO + off, d_o);
-      stv<T, EPL>(dgate + off, d_g);
+      for (int q = 0; q < 4; ++q)
+        norm_bwd_row<T, EPL>(os + (u + q) * rowb, gs + (u + q) * rowb, dsm + (u + q) * rowb, wt,
+                             invD, a.eps, dwt, dO + (long)(u + q) * a.D, dgate + (long)(u + q) * a.D);
+    }
+    for (; u < n; ++u)
+      norm_bwd_row<T, EPL>(os + u * rowb, gs + u * rowb, dsm + u * rowb, wt, invD, a.eps, dwt,
+                           dO + (long)u * a.D, dgate + (long)u * a.D);
+    __syncwarp();
+    fence_async_shared();
+    if (pch < a.nchunks) {
+      issue_rows(a, ring, s, pch, src, 3, rowb);
+      __syncwarp();
+      pch += a.Wt;
+      ++issued;
     }
   }
+  __syncthreads();
+  float* red = reinterpret_cast<float*>(smem);  // [nw][D]
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) red[wi][c0 + e] = dwt[e];
+  for (int e = 0; e < EPL; ++e) red[wi * a.D + c0 + e] = dwt[e];
   __syncthreads();
   for (int c = threadIdx.x; c < a.D; c += blockDim.x) {
     float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < kNbWarps; ++w) v += red[w][c];
+    for (int w = 0; w < nw; ++w) v += red[w * a.D + c];
     a.part[(long)blockIdx.x * a.D + c] = v;
   }
 }
 
-// ---------------------------------------------------------------- dispatch
-// Grid of the short-conv kernels: x = CTAs per head, y = heads.  The
-// backward takes at most about kConvGroupsTarget CTAs in all, each looping
-// over an equal share of the run groups (its partial dw is one row of the
-// workspace).
-int conv_groups(const ConvProblem& p) {
-  const long ttot = (long)p.B * p.T;  // at most 2^30 (checked by the caller)
-  return (int)((ttot + (long)kRun * kNbWarps - 1) / ((long)kRun * kNbWarps));
-}
-
-int conv_bwd_grid_x(const ConvProblem& p) {
-  const int groups = conv_groups(p);
-  const int cap = std::max(1, kConvGroupsTarget / std::max(1, p.H));
-  const int per = (groups + cap - 1) / cap;
-  return std::max(1, (groups + per - 1) / per);
-}
-
-long norm_row_steps(const NormProblem& p, int rows_per_warp) {
-  return (p.rows + (long)kNbWarps * rows_per_warp - 1) / ((long)kNbWarps * rows_per_warp);
-}
-
-int norm_bwd_grid_x(const NormProblem& p) {
-  const long steps = norm_row_steps(p, kNormRowsBwd);
-  const long per = (steps + kNormCtasMax - 1) / kNormCtasMax;
-  return (int)std::max(1L, (steps + per - 1) / per);
-}
-
-template <typename T, int EPL>
-cudaError_t launch_conv(const ConvProblem& p, const ConvArgs& a, bool bwd, cudaStream_t s) {
-  const dim3 block(32 * kNbWarps);
-  if (!bwd) {
-    const dim3 grid(conv_groups(p), p.H);
-    prof_before(s);
-    if (p.cu_seqlens) short_conv_fwd_kernel<T, EPL, true><<<grid, block, 0, s>>>(a);
-    else short_conv_fwd_kernel<T, EPL, false><<<grid, block, 0, s>>>(a);
-    prof_after(s, kConvFwd);
-    return cudaGetLastError();
+// ---------------------------------------------------------------- launch geometry
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 152;
+    n = v;
   }
-  const dim3 grid(conv_bwd_grid_x(p), p.H);
-  prof_before(s);
-  if (p.cu_seqlens) short_conv_bwd_kernel<T, EPL, true><<<grid, block, 0, s>>>(a);
-  else short_conv_bwd_kernel<T, EPL, false><<<grid, block, 0, s>>>(a);
-  prof_after(s, kConvBwd);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int n = p.H * p.D * p.W;
-  prof_before(s);
-  sum_partials_kernel<<<(n + 31) / 32, dim3(32, 32), 0, s>>>(a.part, (int)grid.x, n, p.dw);
-  prof_after(s, kSumPartials);
-  return cudaGetLastError();
+  return n;
 }
 
-template <typename T>
-cudaError_t conv_dispatch(const ConvProblem& p, const ConvArgs& a, bool bwd, cudaStream_t s) {
-  switch (p.D) {
-    case 32: return launch_conv<T, 1>(p, a, bwd, s);
-    case 64: return launch_conv<T, 2>(p, a, bwd, s);
-    default: return launch_conv<T, 4>(p, a, bwd, s);
+int gcd(int x, int y) { return y == 0 ? x : gcd(y, x % y); }
+
+// Staging geometry shared by the kernels: warps per CTA, stages, stage bytes.
+struct Geometry {
+  int nw, nstg, stage_bytes, chunk;  // chunk: tokens (conv) or rows (norm) per stage
+  size_t smem() const { return 128 + (size_t)nw * nstg * stage_bytes + (size_t)nw * nstg * 8; }
+};
+
+int conv_dz_off(int D, int esize, int chunk) {
+  return ((chunk + kMaxTaps - 1) * D * esize + 127) / 128 * 128;
+}
+
+// conv: a stage holds chunk + 3 x rows (and, backward, chunk dz rows)
+Geometry conv_geometry(int D, int esize, bool bwd) {
+  const int rowb = D * esize;
+  Geometry g;
+  g.chunk = std::max(8, kStageTarget / rowb);
+  const int bytes = bwd ? conv_dz_off(D, esize, g.chunk) + g.chunk * rowb
+                        : (g.chunk + kMaxTaps - 1) * rowb;
+  g.stage_bytes = (bytes + 127) / 128 * 128;
+  g.nw = kMaxWarps;
+  g.nstg = 3;
+  while (g.nstg > 2 && g.smem() > (size_t)kRingBytes) --g.nstg;
+  while (g.nw > 4 && g.smem() > (size_t)kRingBytes) g.nw /= 2;
+  return g;
+}
+
+Geometry norm_geometry(int D, int esize, bool bwd) {
+  const int rowb = D * esize;
+  Geometry g;
+  g.chunk = std::max(1, kStageTarget / rowb);
+  g.stage_bytes = (bwd ? 3 : 2) * g.chunk * rowb;
+  g.nw = kMaxWarps;
+  g.nstg = 3;
+  while (g.nstg > 2 && g.smem() > (size_t)kRingBytes) --g.nstg;
+  while (g.nw > 4 && g.smem() > (size_t)kRingBytes) g.nw /= 2;
+  return g;
+}
+
+// Conv grid: one CTA per SM; the backward keeps the warp count a multiple of H
+// (every warp's items then have one head, so dw stays in its registers).
+int conv_grid(const ConvProblem& p, const Geometry& g, bool bwd) {
+  int grid = num_sms();
+  if (bwd) {
+    const int step = p.H / gcd(p.H, g.nw);  // CTAs per multiple of H warps
+    grid = std::max(1, grid / step) * step;
   }
+  return grid;
 }
 
-ConvArgs conv_args(const ConvProblem& p) {
+ConvArgs conv_args(const ConvProblem& p, const Geometry& g, int grid) {
   ConvArgs a{};
   a.x = p.x; a.w = p.w; a.z = p.z; a.dz = p.dz; a.dx = p.dx;
   a.part = static_cast<float*>(p.ws);
@@ -620,42 +938,102 @@ ConvArgs conv_args(const ConvProblem& p) {
   a.H = p.H; a.D = p.D; a.W = p.W;
   a.scale = p.scale; a.eps = p.eps;
   a.l2norm = p.l2norm ? 1 : 0;
+  a.Wt = grid * g.nw;
+  // about two items per warp: P parts of L tokens per head
+  const long P = std::max(1L, ((long)2 * a.Wt + p.H - 1) / p.H);
+  a.L = (int)std::max(1L, ((long)a.Ttot + P - 1) / P);
+  a.nitems = (int)(((long)a.Ttot + a.L - 1) / a.L) * p.H;
+  a.TC = g.chunk;
+  a.nstg = g.nstg;
+  a.stage_bytes = g.stage_bytes;
+  a.dz_off = conv_dz_off(p.D, p.bf16 ? 2 : 4, g.chunk);
+  a.cta_heads = (g.nw % p.H == 0) ? p.H : 0;
   return a;
 }
 
+// Rows of partial dw: one per CTA (H | warps per CTA) or one per H warps.
+int conv_partials(const ConvProblem& p, const Geometry& g, int grid) {
+  return (g.nw % p.H == 0) ? grid : grid * g.nw / p.H;
+}
+
+// 2-D map over a [Ttot, H*D] token tensor; box = D channels x rows tokens,
+// no swizzle; rows outside [0, Ttot) read as zero.
+template <typename T>
+cudaError_t make_rows_map(CUtensorMap* m, const void* ptr, const ConvProblem& p, int rows) {
+  auto enc = tc::get_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const CUtensorMapDataType dt =
+      std::is_same<T, float>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[2] = {(cuuint64_t)p.H * p.D, (cuuint64_t)p.B * p.T};
+  cuuint64_t strides[1] = {(cuuint64_t)p.H * p.D * sizeof(T)};
+  cuuint32_t box[2] = {(cuuint32_t)p.D, (cuuint32_t)rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <typename T, int EPL>
-cudaError_t launch_norm(const NormProblem& p, const NormArgs& a, bool bwd, cudaStream_t s) {
-  const dim3 block(32 * kNbWarps);
-  if (!bwd) {
-    const long steps = norm_row_steps(p, kNormRows);
-    const int grid = (int)std::min(steps, 65535L * 32);
-    prof_before(s);
-    gated_rmsnorm_fwd_kernel<T, EPL><<<grid, block, 0, s>>>(a);
-    prof_after(s, kNormFwd);
-    return cudaGetLastError();
-  }
-  const int grid = norm_bwd_grid_x(p);
-  prof_before(s);
-  gated_rmsnorm_bwd_kernel<T, EPL><<<grid, block, 0, s>>>(a);
-  prof_after(s, kNormBwd);
-  cudaError_t e = cudaGetLastError();
+cudaError_t launch_conv(const ConvProblem& p, bool bwd, cudaStream_t s) {
+  const Geometry g = conv_geometry(p.D, (int)sizeof(T), bwd);
+  const int grid = conv_grid(p, g, bwd);
+  const ConvArgs a = conv_args(p, g, grid);
+  const size_t smem = std::max(g.smem(), bwd ? (size_t)g.nw * p.D * p.W * 4 : (size_t)0);
+  CUtensorMap tmx, tmdz;
+  cudaError_t e = make_rows_map<T>(&tmx, p.x, p, g.chunk + kMaxTaps - 1);
+  if (e == cudaSuccess && bwd) e = make_rows_map<T>(&tmdz, p.dz, p, g.chunk);
   if (e != cudaSuccess) return e;
+  if (bwd) {
+    auto kf = p.cu_seqlens ? (p.l2norm ? short_conv_bwd_kernel<T, EPL, true, true>
+                                       : short_conv_bwd_kernel<T, EPL, true, false>)
+                           : (p.l2norm ? short_conv_bwd_kernel<T, EPL, false, true>
+                                       : short_conv_bwd_kernel<T, EPL, false, false>);
+    e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    prof_before(s);
+    kf<<<grid, 32 * g.nw, smem, s>>>(tmx, tmdz, a);
+    prof_after(s, kConvBwd);
+  } else {
+    auto kf = p.cu_seqlens ? (p.l2norm ? short_conv_fwd_kernel<T, EPL, true, true>
+                                       : short_conv_fwd_kernel<T, EPL, true, false>)
+                           : (p.l2norm ? short_conv_fwd_kernel<T, EPL, false, true>
+                                       : short_conv_fwd_kernel<T, EPL, false, false>);
+    e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    prof_before(s);
+    kf<<<grid, 32 * g.nw, smem, s>>>(tmx, a);
+    prof_after(s, kConvFwd);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !bwd) return e;
+  const int n = p.H * p.D * p.W;
   prof_before(s);
-  sum_partials_kernel<<<(p.D + 31) / 32, dim3(32, 32), 0, s>>>(a.part, grid, p.D, p.dweight);
+  sum_partials_kernel<<<(n + 31) / 32, dim3(32, 32), 0, s>>>(a.part, conv_partials(p, g, grid), n,
+                                                             p.dw);
   prof_after(s, kSumPartials);
   return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t norm_dispatch(const NormProblem& p, const NormArgs& a, bool bwd, cudaStream_t s) {
+cudaError_t conv_dispatch(const ConvProblem& p, bool bwd, cudaStream_t s) {
   switch (p.D) {
-    case 32: return launch_norm<T, 1>(p, a, bwd, s);
-    case 64: return launch_norm<T, 2>(p, a, bwd, s);
-    default: return launch_norm<T, 4>(p, a, bwd, s);
+    case 32: return launch_conv<T, 1>(p, bwd, s);
+    case 64: return launch_conv<T, 2>(p, bwd, s);
+    default: return launch_conv<T, 4>(p, bwd, s);
   }
 }
 
-NormArgs norm_args(const NormProblem& p) {
+int norm_grid(const NormProblem& p, const Geometry& g) {
+  const long chunks = (p.rows + g.chunk - 1) / g.chunk;
+  const long ctas = (chunks + g.nw - 1) / g.nw;
+  return (int)std::max(1L, std::min((long)num_sms(), ctas));
+}
+
+template <typename T, int EPL>
+cudaError_t launch_norm(const NormProblem& p, bool bwd, cudaStream_t s) {
+  const Geometry g = norm_geometry(p.D, (int)sizeof(T), bwd);
+  const int grid = norm_grid(p, g);
   NormArgs a{};
   a.o = p.o; a.gate = p.gate; a.weight = p.weight; a.out = p.out;
   a.dout = p.dout; a.dO = p.dO; a.dgate = p.dgate;
@@ -663,39 +1041,64 @@ NormArgs norm_args(const NormProblem& p) {
   a.rows = p.rows;
   a.D = p.D;
   a.eps = p.eps;
-  return a;
+  a.RC = g.chunk;
+  a.nchunks = (p.rows + g.chunk - 1) / g.chunk;
+  a.Wt = grid * g.nw;
+  a.nstg = g.nstg;
+  a.stage_bytes = g.stage_bytes;
+  const size_t smem = std::max(g.smem(), bwd ? (size_t)g.nw * p.D * 4 : (size_t)0);
+  auto kf = bwd ? gated_rmsnorm_bwd_kernel<T, EPL> : gated_rmsnorm_fwd_kernel<T, EPL>;
+  cudaError_t e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  prof_before(s);
+  kf<<<grid, 32 * g.nw, smem, s>>>(a);
+  prof_after(s, bwd ? kNormBwd : kNormFwd);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !bwd) return e;
+  prof_before(s);
+  sum_partials_kernel<<<(p.D + 31) / 32, dim3(32, 32), 0, s>>>(a.part, grid, p.D, p.dweight);
+  prof_after(s, kSumPartials);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t norm_dispatch(const NormProblem& p, bool bwd, cudaStream_t s) {
+  switch (p.D) {
+    case 32: return launch_norm<T, 1>(p, bwd, s);
+    case 64: return launch_norm<T, 2>(p, bwd, s);
+    default: return launch_norm<T, 4>(p, bwd, s);
+  }
 }
 
 }  // namespace
 
 size_t short_conv_bwd_workspace(const ConvProblem& p) {
   if ((long)p.B * p.T == 0 || p.H == 0) return 0;
-  return align_up((size_t)conv_bwd_grid_x(p) * p.H * p.D * p.W * sizeof(float), 256);
+  const Geometry g = conv_geometry(p.D, p.bf16 ? 2 : 4, true);
+  const int grid = conv_grid(p, g, true);
+  return align_up((size_t)conv_partials(p, g, grid) * p.H * p.D * p.W * sizeof(float), 256);
 }
 
 cudaError_t short_conv_fwd(const ConvProblem& p, cudaStream_t s) {
-  const ConvArgs a = conv_args(p);
-  return p.bf16 ? conv_dispatch<__nv_bfloat16>(p, a, false, s) : conv_dispatch<float>(p, a, false, s);
+  return p.bf16 ? conv_dispatch<__nv_bfloat16>(p, false, s) : conv_dispatch<float>(p, false, s);
 }
 
 cudaError_t short_conv_bwd(const ConvProblem& p, cudaStream_t s) {
-  const ConvArgs a = conv_args(p);
-  return p.bf16 ? conv_dispatch<__nv_bfloat16>(p, a, true, s) : conv_dispatch<float>(p, a, true, s);
+  return p.bf16 ? conv_dispatch<__nv_bfloat16>(p, true, s) : conv_dispatch<float>(p, true, s);
 }
 
 size_t gated_rmsnorm_bwd_workspace(const NormProblem& p) {
   if (p.rows == 0) return 0;
-  return align_up((size_t)norm_bwd_grid_x(p) * p.D * sizeof(float), 256);
+  const Geometry g = norm_geometry(p.D, p.bf16 ? 2 : 4, true);
+  return align_up((size_t)norm_grid(p, g) * p.D * sizeof(float), 256);
 }
 
 cudaError_t gated_rmsnorm_fwd(const NormProblem& p, cudaStream_t s) {
-  const NormArgs a = norm_args(p);
-  return p.bf16 ? norm_dispatch<__nv_bfloat16>(p, a, false, s) : norm_dispatch<float>(p, a, false, s);
+  return p.bf16 ? norm_dispatch<__nv_bfloat16>(p, false, s) : norm_dispatch<float>(p, false, s);
 }
 
 cudaError_t gated_rmsnorm_bwd(const NormProblem& p, cudaStream_t s) {
-  const NormArgs a = norm_args(p);
-  return p.bf16 ? norm_dispatch<__nv_bfloat16>(p, a, true, s) : norm_dispatch<float>(p, a, true, s);
+  return p.bf16 ? norm_dispatch<__nv_bfloat16>(p, true, s) : norm_dispatch<float>(p, true, s);
 }
 
 cudaError_t nb_read_and_clear_status(int* status) {
