@@ -149,10 +149,153 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// Fast-math sigmoid: the quotient's error (a few ulp) is far below the bf16
-// rounding of the outputs; for s < -87 it gives 0 (the exact value is below
-// 1e-38).
-__device__ __forceinline__ float sigmoid(float s) { return __fdividef(1.f, 1.f + __expf(-s)); }
+// ---------------------------------------------------------------- lane arithmetic
+// The kernels are instruction-bound, so element-wise arithmetic on a lane's
+// EPL values runs on packed fp32 pairs (FFMA2 / FMUL2 / FADD2: two results
+// per instruction, each rounded as the scalar operation would be), and the
+// sigmoid uses the hardware 2^x and reciprocal approximations directly:
+// sigmoid(x) = 1 / (1 + 2^(-x log2 e)), relative error a few 1e-7, with
+// 2^(...) = inf giving 0 and 0 giving 1 at the ends of the range.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rsqrt_approx(float x) {
+  float y;
+  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int N>
+__device__ __forceinline__ void vmul(float (&d)[N], const float (&a)[N], const float (&b)[N]) {
+  if constexpr (N % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+      const float2 r = __fmul2_rn(make_float2(a[i], a[i + 1]), make_float2(b[i], b[i + 1]));
+      d[i] = r.x;
+      d[i + 1] = r.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) d[i] = a[i] * b[i];
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void vscale(float (&d)[N], const float (&a)[N], float s) {
+  if constexpr (N % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+      const float2 r = __fmul2_rn(make_float2(a[i], a[i + 1]), make_float2(s, s));
+      d[i] = r.x;
+      d[i + 1] = r.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) d[i] = a[i] * s;
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void vfma(float (&d)[N], const float (&a)[N], const float (&b)[N],
+                                     const float (&c)[N]) {
+  if constexpr (N % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+      const float2 r = __ffma2_rn(make_float2(a[i], a[i + 1]), make_float2(b[i], b[i + 1]),
+                                  make_float2(c[i], c[i + 1]));
+      d[i] = r.x;
+      d[i + 1] = r.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) d[i] = fmaf(a[i], b[i], c[i]);
+  }
+}
+
+// d = a s + c (s broadcast)
+template <int N>
+__device__ __forceinline__ void vfma_s(float (&d)[N], const float (&a)[N], float s,
+                                       const float (&c)[N]) {
+  if constexpr (N % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+      const float2 r = __ffma2_rn(make_float2(a[i], a[i + 1]), make_float2(s, s),
+                                  make_float2(c[i], c[i + 1]));
+      d[i] = r.x;
+      d[i + 1] = r.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) d[i] = fmaf(a[i], s, c[i]);
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void vadd(float (&d)[N], const float (&a)[N], const float (&b)[N]) {
+  if constexpr (N % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+      const float2 r = __fadd2_rn(make_float2(a[i], a[i + 1]), make_float2(b[i], b[i + 1]));
+      d[i] = r.x;
+      d[i + 1] = r.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) d[i] = a[i] + b[i];
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void vadd_s(float (&d)[N], const float (&a)[N], float s) {
+  if constexpr (N % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+      const float2 r = __fadd2_rn(make_float2(a[i], a[i + 1]), make_float2(s, s));
+      d[i] = r.x;
+      d[i + 1] = r.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) d[i] = a[i] + s;
+  }
+}
+
+// sum_i a_i b_i over the lane's values
+template <int N>
+__device__ __forceinline__ float vdot(const float (&a)[N], const float (&b)[N]) {
+  if constexpr (N % 2 == 0) {
+    float2 acc = __fmul2_rn(make_float2(a[0], a[1]), make_float2(b[0], b[1]));
+#pragma unroll
+    for (int i = 2; i < N; i += 2)
+      acc = __ffma2_rn(make_float2(a[i], a[i + 1]), make_float2(b[i], b[i + 1]), acc);
+    return acc.x + acc.y;
+  } else {
+    float acc = a[0] * b[0];
+#pragma unroll
+    for (int i = 1; i < N; ++i) acc = fmaf(a[i], b[i], acc);
+    return acc;
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void vsigmoid(float (&sg)[N], const float (&x)[N]) {
+  float t[N];
+  vscale(t, x, -kLog2e);
+#pragma unroll
+  for (int i = 0; i < N; ++i) t[i] = ex2_approx(t[i]);
+  vadd_s(t, t, 1.f);
+#pragma unroll
+  for (int i = 0; i < N; ++i) sg[i] = rcp_approx(t[i]);
+}
 
 // ---------------------------------------------------------------- staging
 using tc::fence_async_shared;
@@ -371,29 +514,51 @@ __device__ __forceinline__ void load_window(const unsigned char* xs, int xb, int
   }
 }
 
-// One token of the forward: z = SiLU(sum_j wp_j x_{t-3+j}), L2-normalised per head.
-template <typename T, int EPL, bool Norm, bool Fast>
+// One token of the forward from its window x_{t-3..t}: z = SiLU(sum_j wp_j
+// x_{t-3+j}), L2-normalised per head and scaled.
+template <typename T, int EPL, bool Norm>
+__device__ __forceinline__ void conv_fwd_from(const float (&x0)[EPL], const float (&x1)[EPL],
+                                              const float (&x2)[EPL], const float (&x3)[EPL],
+                                              const float (&wp)[kMaxTaps][EPL], float scale,
+                                              float eps, T* __restrict__ zrow) {
+  float sv[EPL], sg[EPL], y[EPL];
+  vmul(sv, wp[3], x3);
+  vfma(sv, wp[2], x2, sv);
+  vfma(sv, wp[1], x1, sv);
+  vfma(sv, wp[0], x0, sv);
+  vsigmoid(sg, sv);
+  vmul(y, sv, sg);
+  if (Norm) vscale(y, y, scale * rsqrt_approx(warp_sum(vdot(y, y)) + eps));
+  stv<T, EPL>(zrow, y);
+}
+
+template <typename T, int EPL>
+__device__ __forceinline__ void smem_row(const unsigned char* xs, int rowb, int r, float (&v)[EPL]) {
+  widen<T, EPL>(*reinterpret_cast<const typename Raw<T, EPL>::type*>(xs + r * rowb), v);
+}
+
+// One token with sequence checks: rows before lo read as zero.
+template <typename T, int EPL, bool Norm>
 __device__ __forceinline__ void conv_fwd_token(const unsigned char* xs, int xb, int rowb, int t,
                                                int lo, const float (&wp)[kMaxTaps][EPL],
                                                float scale, float eps, T* __restrict__ zrow) {
   float xv[kMaxTaps][EPL];
-  load_window<T, EPL, Fast>(xs, xb, rowb, t, lo, xv);
-  float y[EPL];
-  float ss = 0.f;
+  load_window<T, EPL, false>(xs, xb, rowb, t, lo, xv);
+  conv_fwd_from<T, EPL, Norm>(xv[0], xv[1], xv[2], xv[3], wp, scale, eps, zrow);
+}
+
+// Four tokens t..t+3 of one sequence: their seven rows x_{t-3..t+3} are read once.
+template <typename T, int EPL, bool Norm>
+__device__ __forceinline__ void conv_fwd_group(const unsigned char* xs, int xb, int rowb, int t,
+                                               const float (&wp)[kMaxTaps][EPL], float scale,
+                                               float eps, T* __restrict__ z, long CH) {
+  float xr[7][EPL];
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) {
-    float sv = wp[kMaxTaps - 1][e] * xv[kMaxTaps - 1][e];
+  for (int r = 0; r < 7; ++r) smem_row<T, EPL>(xs, rowb, t - (kMaxTaps - 1) + r - xb, xr[r]);
 #pragma unroll
-    for (int j = 0; j < kMaxTaps - 1; ++j) sv = fmaf(wp[j][e], xv[j][e], sv);
-    y[e] = sv * sigmoid(sv);
-    ss = fmaf(y[e], y[e], ss);
-  }
-  if (Norm) {
-    const float r = scale * rsqrtf(warp_sum(ss) + eps);
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) y[e] *= r;
-  }
-  stv<T, EPL>(zrow, y);
+  for (int q = 0; q < 4; ++q)
+    conv_fwd_from<T, EPL, Norm>(xr[q], xr[q + 1], xr[q + 2], xr[q + 3], wp, scale, eps,
+                                z + (long)(t + q) * CH);
 }
 
 template <typename T, int EPL, bool Packed, bool Norm>
@@ -433,18 +598,13 @@ short_conv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, ConvArgs a) {
     int t = cc.a;
     if (lo <= xb && hi >= cc.b) {
       // no sequence start among the chunk's rows: four independent tokens at a time
-      for (; t + 4 <= cc.b; t += 4) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          conv_fwd_token<T, EPL, Norm, true>(xs, xb, rowb, t + q, lo, wp, a.scale, a.eps,
-                                             z + (long)(t + q) * CH);
-      }
+      for (; t + 4 <= cc.b; t += 4) conv_fwd_group<T, EPL, Norm>(xs, xb, rowb, t, wp, a.scale, a.eps, z, CH);
       for (; t < cc.b; ++t)
-        conv_fwd_token<T, EPL, Norm, true>(xs, xb, rowb, t, lo, wp, a.scale, a.eps, z + (long)t * CH);
+        conv_fwd_token<T, EPL, Norm>(xs, xb, rowb, t, lo, wp, a.scale, a.eps, z + (long)t * CH);
     } else {
       for (; t < cc.b; ++t) {
         if (t >= hi) seq_bounds<Packed>(t, a.T, a.Ttot, a.cu, a.nseq, lo, hi);
-        conv_fwd_token<T, EPL, Norm, false>(xs, xb, rowb, t, lo, wp, a.scale, a.eps, z + (long)t * CH);
+        conv_fwd_token<T, EPL, Norm>(xs, xb, rowb, t, lo, wp, a.scale, a.eps, z + (long)t * CH);
       }
     }
     __syncwarp();
@@ -458,46 +618,56 @@ short_conv_fwd_kernel(const __grid_constant__ CUtensorMap tmx, ConvArgs a) {
 }
 
 // ---------------------------------------------------------------- short conv backward
-// ds_t of one token: the gradient at the pre-activation s_t from dz_t
-// (through the L2 norm and SiLU); dwp gains ds_t x_{t-3+j} for own tokens.
-template <typename T, int EPL, bool Norm, bool Fast>
+// ds_t of one token from its window x_{t-3..t} and dz_t: the gradient at the
+// pre-activation s_t (through the L2 norm and SiLU); own tokens add
+// ds_t x_{t-3+j} to dw.
+template <typename T, int EPL, bool Norm>
+__device__ __forceinline__ void conv_bwd_from(const float (&x0)[EPL], const float (&x1)[EPL],
+                                              const float (&x2)[EPL], const float (&x3)[EPL],
+                                              const float (&gr)[EPL], bool own,
+                                              const float (&wp)[kMaxTaps][EPL], float scale,
+                                              float eps, float (&ds)[EPL],
+                                              float (&dwp)[kMaxTaps][EPL]) {
+  float sv[EPL], sg[EPL], y[EPL], dy[EPL];
+  vmul(sv, wp[3], x3);
+  vfma(sv, wp[2], x2, sv);
+  vfma(sv, wp[1], x1, sv);
+  vfma(sv, wp[0], x0, sv);
+  vsigmoid(sg, sv);
+  vmul(y, sv, sg);
+  if (Norm) {
+    const float r = rsqrt_approx(warp_sum(vdot(y, y)) + eps);
+    const float c = r * r * warp_sum(vdot(y, gr));
+    vfma_s(dy, y, -c, gr);     // g - c y
+    vscale(dy, dy, scale * r);
+  } else {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) dy[e] = gr[e];
+  }
+  // SiLU'(s) = sg (1 + s (1 - sg)) = (y + sg) - y sg
+  float ysg[EPL], d1[EPL];
+  vmul(ysg, y, sg);
+  vadd(d1, y, sg);
+  vfma_s(d1, ysg, -1.f, d1);
+  vmul(ds, dy, d1);
+  if (own) {
+    vfma(dwp[0], ds, x0, dwp[0]);
+    vfma(dwp[1], ds, x1, dwp[1]);
+    vfma(dwp[2], ds, x2, dwp[2]);
+    vfma(dwp[3], ds, x3, dwp[3]);
+  }
+}
+
+template <typename T, int EPL, bool Norm>
 __device__ __forceinline__ void conv_bwd_ds(const unsigned char* xs, const unsigned char* dzs,
                                             int xb, int a0, int rowb, int t, int lo, bool own,
                                             const float (&wp)[kMaxTaps][EPL], float scale,
                                             float eps, float (&ds)[EPL],
                                             float (&dwp)[kMaxTaps][EPL]) {
   float gr[EPL], xv[kMaxTaps][EPL];
-  load_window<T, EPL, Fast>(xs, xb, rowb, t, lo, xv);
-  widen<T, EPL>(*reinterpret_cast<const typename Raw<T, EPL>::type*>(dzs + (t - a0) * rowb), gr);
-  float sv[EPL], sg[EPL], y[EPL];
-  float ss = 0.f, yg = 0.f;
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) {
-    float v = 0.f;
-#pragma unroll
-    for (int j = 0; j < kMaxTaps; ++j) v = fmaf(wp[j][e], xv[j][e], v);
-    sv[e] = v;
-    sg[e] = sigmoid(v);
-    y[e] = v * sg[e];
-    ss = fmaf(y[e], y[e], ss);
-    yg = fmaf(y[e], gr[e], yg);
-  }
-  if (Norm) {
-    const float r = rsqrtf(warp_sum(ss) + eps);
-    const float c = r * r * warp_sum(yg);
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) ds[e] = scale * r * (gr[e] - y[e] * c);
-  } else {
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) ds[e] = gr[e];
-  }
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) ds[e] *= sg[e] * (1.f + sv[e] * (1.f - sg[e]));
-  if (own)
-#pragma unroll
-    for (int j = 0; j < kMaxTaps; ++j)
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) dwp[j][e] = fmaf(ds[e], xv[j][e], dwp[j][e]);
+  load_window<T, EPL, false>(xs, xb, rowb, t, lo, xv);
+  smem_row<T, EPL>(dzs, rowb, t - a0, gr);
+  conv_bwd_from<T, EPL, Norm>(xv[0], xv[1], xv[2], xv[3], gr, own, wp, scale, eps, ds, dwp);
 }
 
 // dx_t = sum_j wp_j ds_{t+3-j} from ds_t and the window of later ds (own
@@ -509,12 +679,10 @@ __device__ __forceinline__ void conv_bwd_finish(bool own, const float (&wp)[kMax
                                                 T* __restrict__ dxrow) {
   if (own) {
     float d[EPL];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      d[e] = wp[kMaxTaps - 1][e] * ds[e];
-#pragma unroll
-      for (int j = 0; j < kMaxTaps - 1; ++j) d[e] = fmaf(wp[kMaxTaps - 2 - j][e], dsw[j][e], d[e]);
-    }
+    vmul(d, wp[3], ds);
+    vfma(d, wp[2], dsw[0], d);
+    vfma(d, wp[1], dsw[1], d);
+    vfma(d, wp[0], dsw[2], d);
     stv<T, EPL>(dxrow, d);
   }
 #pragma unroll
@@ -571,19 +739,25 @@ short_conv_bwd_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_cons
       // the chunk's tokens and rows all lie in one sequence: ds of four
       // tokens at a time, then their dx from the top down
       for (; t - 3 >= cc.a; t -= 4) {
-        float ds[4][EPL];
+        // tokens t, t-1, t-2, t-3: x rows t-6..t read once
+        float ds[4][EPL], xr[7][EPL];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          conv_bwd_ds<T, EPL, Norm, true>(xs, dzs, xb, cc.a, rowb, t - q, lo, t - q < cc.t1, wp,
-                                          a.scale, a.eps, ds[q], dwp);
+        for (int r = 0; r < 7; ++r) smem_row<T, EPL>(xs, rowb, t - 6 + r - xb, xr[r]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float gr[EPL];
+          smem_row<T, EPL>(dzs, rowb, t - q - cc.a, gr);
+          conv_bwd_from<T, EPL, Norm>(xr[3 - q], xr[4 - q], xr[5 - q], xr[6 - q], gr,
+                                      t - q < cc.t1, wp, a.scale, a.eps, ds[q], dwp);
+        }
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           conv_bwd_finish<T, EPL>(t - q < cc.t1, wp, ds[q], dsw, dx + (long)(t - q) * CH);
       }
       for (; t >= cc.a; --t) {
         float ds[EPL];
-        conv_bwd_ds<T, EPL, Norm, true>(xs, dzs, xb, cc.a, rowb, t, lo, t < cc.t1, wp, a.scale,
-                                        a.eps, ds, dwp);
+        conv_bwd_ds<T, EPL, Norm>(xs, dzs, xb, cc.a, rowb, t, lo, t < cc.t1, wp, a.scale, a.eps,
+                                  ds, dwp);
         conv_bwd_finish<T, EPL>(t < cc.t1, wp, ds, dsw, dx + (long)t * CH);
       }
     } else {
@@ -594,8 +768,8 @@ short_conv_bwd_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_cons
           for (int j = 0; j < kMaxTaps - 1; ++j) zero(dsw[j]);
         }
         float ds[EPL];
-        conv_bwd_ds<T, EPL, Norm, false>(xs, dzs, xb, cc.a, rowb, t, lo, t < cc.t1, wp, a.scale,
-                                         a.eps, ds, dwp);
+        conv_bwd_ds<T, EPL, Norm>(xs, dzs, xb, cc.a, rowb, t, lo, t < cc.t1, wp, a.scale, a.eps,
+                                  ds, dwp);
         conv_bwd_finish<T, EPL>(t < cc.t1, wp, ds, dsw, dx + (long)t * CH);
       }
     }
@@ -702,13 +876,13 @@ __device__ __forceinline__ void norm_fwd_row(const unsigned char* os, const unsi
   float ov[EPL], gv[EPL];
   widen<T, EPL>(*reinterpret_cast<const typename Raw<T, EPL>::type*>(os), ov);
   widen<T, EPL>(*reinterpret_cast<const typename Raw<T, EPL>::type*>(gs), gv);
-  float ss = 0.f;
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) ss = fmaf(ov[e], ov[e], ss);
-  const float r = rsqrtf(warp_sum(ss) * invD + eps);
-  float y[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) y[e] = ov[e] * r * wt[e] * (gv[e] * sigmoid(gv[e]));
+  const float r = rsqrt_approx(warp_sum(vdot(ov, ov)) * invD + eps);
+  float sg[EPL], act[EPL], wr[EPL], y[EPL];
+  vsigmoid(sg, gv);
+  vmul(act, gv, sg);  // SiLU(gate)
+  vscale(wr, wt, r);
+  vmul(y, ov, wr);
+  vmul(y, y, act);
   stv<T, EPL>(out, y);
 }
 
@@ -722,28 +896,25 @@ __device__ __forceinline__ void norm_bwd_row(const unsigned char* os, const unsi
   widen<T, EPL>(*reinterpret_cast<const typename Raw<T, EPL>::type*>(os), ov);
   widen<T, EPL>(*reinterpret_cast<const typename Raw<T, EPL>::type*>(gs), gv);
   widen<T, EPL>(*reinterpret_cast<const typename Raw<T, EPL>::type*>(ds), dv);
-  float ss = 0.f;
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) ss = fmaf(ov[e], ov[e], ss);
-  const float r = rsqrtf(warp_sum(ss) * invD + eps);
-  float nrm[EPL], sg[EPL], dn[EPL];
-  float dot = 0.f;
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) {
-    nrm[e] = ov[e] * r;
-    sg[e] = sigmoid(gv[e]);
-    const float act = gv[e] * sg[e];
-    dn[e] = dv[e] * wt[e] * act;
-    dot = fmaf(dn[e], nrm[e], dot);
-    dwt[e] = fmaf(dv[e] * nrm[e], act, dwt[e]);
-  }
-  const float c = warp_sum(dot) * invD;
-  float d_o[EPL], d_g[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) {
-    d_o[e] = r * (dn[e] - nrm[e] * c);
-    d_g[e] = dv[e] * nrm[e] * wt[e] * sg[e] * (1.f + gv[e] * (1.f - sg[e]));
-  }
+  const float r = rsqrt_approx(warp_sum(vdot(ov, ov)) * invD + eps);
+  float nrm[EPL], sg[EPL], act[EPL], dn[EPL], dvn[EPL], t[EPL];
+  vscale(nrm, ov, r);
+  vsigmoid(sg, gv);
+  vmul(act, gv, sg);        // SiLU(gate)
+  vmul(t, dv, wt);
+  vmul(dn, t, act);         // d(out)/d(n) terms: dout weight SiLU(gate)
+  vmul(dvn, dv, nrm);
+  vfma(dwt, dvn, act, dwt); // dweight += dout n SiLU(gate)
+  const float c = warp_sum(vdot(dn, nrm)) * invD;
+  float d_o[EPL], d_g[EPL], d1[EPL], as[EPL];
+  vfma_s(t, nrm, -c, dn);
+  vscale(d_o, t, r);        // do = r (dn - n c)
+  // dgate = dout n weight SiLU'(gate), SiLU'(g) = (act + sg) - act sg
+  vmul(as, act, sg);
+  vadd(d1, act, sg);
+  vfma_s(d1, as, -1.f, d1);
+  vmul(t, dvn, wt);
+  vmul(d_g, t, d1);
   stv<T, EPL>(dO, d_o);
   stv<T, EPL>(dgate, d_g);
 }
