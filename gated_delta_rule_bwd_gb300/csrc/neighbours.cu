@@ -38,6 +38,8 @@
 // tensor); dweight is reduced like dw.
 
 #include <algorithm>
+#include <map>
+#include <mutex>
 #include <type_traits>
 
 #include "gdn.h"
@@ -1050,6 +1052,22 @@ int num_sms() {
 
 int gcd(int x, int y) { return y == 0 ? x : gcd(y, x % y); }
 
+// Raises a kernel's dynamic shared-memory limit once per device (the call
+// costs host time on every launch otherwise).
+cudaError_t set_smem(const void* kf, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& have = done[{dev, kf}];
+  if (have >= smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess) have = smem;
+  return e;
+}
+
 // Staging geometry shared by the kernels: warps per CTA, stages, stage bytes.
 struct Geometry {
   int nw, nstg, stage_bytes, chunk;  // chunk: tokens (conv) or rows (norm) per stage
@@ -1064,7 +1082,8 @@ int conv_dz_off(int D, int esize, int chunk) {
 Geometry conv_geometry(int D, int esize, bool bwd) {
   const int rowb = D * esize;
   Geometry g;
-  g.chunk = std::max(8, kStageTarget / rowb);
+  // the forward holds x only: twice the tokens per stage (fewer chunk overheads)
+  g.chunk = std::max(bwd ? 8 : 16, (bwd ? kStageTarget : 2 * kStageTarget) / rowb);
   const int bytes = bwd ? conv_dz_off(D, esize, g.chunk) + g.chunk * rowb
                         : (g.chunk + kMaxTaps - 1) * rowb;
   g.stage_bytes = (bytes + 127) / 128 * 128;
@@ -1160,7 +1179,7 @@ cudaError_t launch_conv(const ConvProblem& p, bool bwd, cudaStream_t s) {
                                        : short_conv_bwd_kernel<T, EPL, true, false>)
                            : (p.l2norm ? short_conv_bwd_kernel<T, EPL, false, true>
                                        : short_conv_bwd_kernel<T, EPL, false, false>);
-    e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = set_smem(reinterpret_cast<const void*>(kf), smem);
     if (e != cudaSuccess) return e;
     prof_before(s);
     kf<<<grid, 32 * g.nw, smem, s>>>(tmx, tmdz, a);
@@ -1170,7 +1189,7 @@ cudaError_t launch_conv(const ConvProblem& p, bool bwd, cudaStream_t s) {
                                        : short_conv_fwd_kernel<T, EPL, true, false>)
                            : (p.l2norm ? short_conv_fwd_kernel<T, EPL, false, true>
                                        : short_conv_fwd_kernel<T, EPL, false, false>);
-    e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = set_smem(reinterpret_cast<const void*>(kf), smem);
     if (e != cudaSuccess) return e;
     prof_before(s);
     kf<<<grid, 32 * g.nw, smem, s>>>(tmx, a);
@@ -1219,7 +1238,7 @@ cudaError_t launch_norm(const NormProblem& p, bool bwd, cudaStream_t s) {
   a.stage_bytes = g.stage_bytes;
   const size_t smem = std::max(g.smem(), bwd ? (size_t)g.nw * p.D * 4 : (size_t)0);
   auto kf = bwd ? gated_rmsnorm_bwd_kernel<T, EPL> : gated_rmsnorm_fwd_kernel<T, EPL>;
-  cudaError_t e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem(reinterpret_cast<const void*>(kf), smem);
   if (e != cudaSuccess) return e;
   prof_before(s);
   kf<<<grid, 32 * g.nw, smem, s>>>(a);
