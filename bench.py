@@ -46,6 +46,7 @@ METRIC = "GDN/KDA mixer fwd+bwd tokens/s on 1 GB300; fraction of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
 WORKLOADS = {"gdn_300m": W.GDN_300M_BF16, "kda_300m": W.KDA_300M_BF16, "gdn_1b": W.GDN_1B_BF16_H0,
+             "kda_300m_g16": W.KDA_300M_BF16_G16,
              "mamba2_300m": W.MAMBA2_300M_BF16, "gdn_block_300m": W.GDN_BLOCK_300M_BF16,
              "gdn_tiny": W.GDN_TINY_FP32, "gdn_decode": W.GDN_DECODE_BF16,
              "kda_decode": W.KDA_DECODE_BF16, "gdn_1m": W.GDN_1M_FWD_BF16}
@@ -67,7 +68,7 @@ def algorithmic(w):
     Bytes count each input read once and each output written once."""
     dk, dv, C = w.dk, w.dv, w.chunk
     e = 2 if w.dtype == "bf16" else 4
-    sg = 4 * dk if w.kda else 4
+    sg = (2 if getattr(w, "g_dtype", "f32") == "bf16" else 4) * dk if w.kda else 4
     sb = 4
     fwd_flops = 2 * C * (3 * dk + 2 * dv) + 6 * dk * dv + C * C / 3
     bwd_flops = 2 * C * (7 * dk + 5 * dv) + 14 * dk * dv + C * C / 3
@@ -429,6 +430,7 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "op": w.mixer + " fwd+bwd",
                        "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
+                       "gate_dtype": "bf16" if w.g_dtype == "bf16" else "f32",
                        "tokens_per_step": tokens_step, "global_batch": w.B * ws,
                        "parallelism": f"replicas x{ws} (independent sequences)",
                        "l2": "flushed between timed steps (2 x L2 buffer written outside the events)",

@@ -30,7 +30,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgdn.so")
 
-GDN_F32, GDN_BF16 = 0, 1
+GDN_F32, GDN_BF16, GDN_BF16_G16 = 0, 1, 2
 _DTYPES = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}
 
 
@@ -159,9 +159,13 @@ def _check(rc):
         raise GdnError(msg)
 
 
-def make_shape(q, v, chunk) -> GdnShape:
+def make_shape(q, v, chunk, g=None) -> GdnShape:
+    """The ABI shape of a call; a bf16 ``g`` (KDA) selects GDN_BF16_G16."""
     B, T, H, dk = q.shape
-    return GdnShape(B, T, H, dk, v.shape[3], chunk, _DTYPES[q.dtype])
+    dt = _DTYPES[q.dtype]
+    if g is not None and g.dtype == torch.bfloat16:
+        dt = GDN_BF16_G16
+    return GdnShape(B, T, H, dk, v.shape[3], chunk, dt)
 
 
 def _validate(q, k, v, g, beta, kda, extra=()):
@@ -173,7 +177,9 @@ def _validate(q, k, v, g, beta, kda, extra=()):
     B, T, H, dk = q.shape
     dv = v.shape[3]
     want = {"k": (k, (B, T, H, dk), q.dtype), "v": (v, (B, T, H, dv), q.dtype),
-            "g": (g, (B, T, H, dk) if kda else (B, T, H), torch.float32),
+            "g": (g, (B, T, H, dk) if kda else (B, T, H),
+                  torch.bfloat16 if (kda and g is not None and g.dtype == torch.bfloat16
+                                     and q.dtype == torch.bfloat16) else torch.float32),
             "beta": (beta, (B, T, H), torch.float32)}
     for name, (x, shape, dt) in list(want.items()) + list(extra):
         if x is None:
@@ -243,7 +249,7 @@ def _fwd(kda, q, k, v, g, beta, h0=None, chunk=64, output_final_state=True, out=
     else:
         ws = _workspace(fwd_workspace_bytes(q, v, chunk, kda, delta), workspace, q.device)
         fn = _entry(kda, delta, "fwd")
-    s = make_shape(q, v, chunk)
+    s = make_shape(q, v, chunk, g)
     _check(fn(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
               _ptr(ht), _ptr(ws), ws.numel(), _stream(q.device)))
     return o, ht
@@ -273,7 +279,7 @@ def _bwd(kda, q, k, v, g, beta, h0, do, dht=None, chunk=64, want_dh0=True, works
     else:
         ws = _workspace(bwd_workspace_bytes(q, v, chunk, kda, delta), workspace, q.device)
         fn = _entry(kda, delta, "bwd")
-    s = make_shape(q, v, chunk)
+    s = make_shape(q, v, chunk, g)
     _check(fn(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(do),
               _ptr(dht), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(dbeta), _ptr(dh0),
               _ptr(ws), ws.numel(), _stream(q.device)))
@@ -384,7 +390,7 @@ def _fwd_varlen(kda, delta, q, k, v, g, beta, cu_seqlens, h0, chunk, workspace):
     o = torch.empty((1, T, H, dv), dtype=q.dtype, device=q.device)
     ht = torch.empty((nseq, H, dk, dv), dtype=torch.float32, device=q.device)
     ws = _workspace(varlen_workspace_bytes(q, v, nseq, chunk, kda, delta), workspace, q.device)
-    s = make_shape(q, v, chunk)
+    s = make_shape(q, v, chunk, g)
     _check(_entry(kda, delta, "fwd_varlen")(ctypes.byref(s), _ptr(cu_seqlens), nseq, _ptr(q), _ptr(k),
                                             _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(ht),
                                             _ptr(ws), ws.numel(), _stream(q.device)))
@@ -402,7 +408,7 @@ def _bwd_varlen(kda, delta, q, k, v, g, beta, cu_seqlens, h0, do, dht, chunk, wo
     dq, dk_, dv_, dg, dbeta = e(q), e(k), e(v), e(g), e(beta)
     dh0 = torch.empty((nseq, H, dk, dv), dtype=torch.float32, device=q.device)
     ws = _workspace(varlen_workspace_bytes(q, v, nseq, chunk, kda, delta, True), workspace, q.device)
-    s = make_shape(q, v, chunk)
+    s = make_shape(q, v, chunk, g)
     _check(_entry(kda, delta, "bwd_varlen")(ctypes.byref(s), _ptr(cu_seqlens), nseq, _ptr(q), _ptr(k),
                                             _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(do), _ptr(dht),
                                             _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(dbeta),
@@ -552,7 +558,7 @@ def _decode(kda, q, k, v, g, beta, state=None, inplace=True, chunk=64):
     o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     ht = state if (inplace and state is not None) else torch.empty(
         (B, H, dk, dv), dtype=torch.float32, device=q.device)
-    s = make_shape(q, v, chunk)
+    s = make_shape(q, v, chunk, g)
     fn = lib().kda_decode if kda else lib().gdn_decode
     _check(fn(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
               _ptr(o), _ptr(ht), _stream(q.device)))

@@ -29,7 +29,8 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 // Validates the shape; fills the size fields of a Problem.
 int check_shape(const gdn_shape* s, bool kda, gdn::Problem* p, bool no_delta = false) {
   if (!s) return GDN_ERR_ARG;
-  if (s->dtype != GDN_F32 && s->dtype != GDN_BF16) return GDN_ERR_DTYPE;
+  if (s->dtype != GDN_F32 && s->dtype != GDN_BF16 && !(kda && s->dtype == GDN_BF16_G16))
+    return GDN_ERR_DTYPE;
   if (s->B < 0 || s->T < 0 || s->H < 0) return GDN_ERR_SHAPE;
   if (s->dk < 1 || s->dk > 128 || s->dv < 1 || s->dv > 128) return GDN_ERR_SHAPE;
   if (s->chunk != 16 && s->chunk != 32 && s->chunk != 64) return GDN_ERR_SHAPE;
@@ -43,7 +44,8 @@ int check_shape(const gdn_shape* s, bool kda, gdn::Problem* p, bool no_delta = f
   p->N = (s->T + s->chunk - 1) / s->chunk;
   p->kda = kda;
   p->no_delta = no_delta;
-  p->bf16 = s->dtype == GDN_BF16;
+  p->bf16 = s->dtype == GDN_BF16 || s->dtype == GDN_BF16_G16;
+  p->g16 = s->dtype == GDN_BF16_G16;
   return GDN_OK;
 }
 
@@ -98,7 +100,7 @@ cudaError_t copy_state_or_zero(float* dst, const float* src, const gdn::Problem&
 }
 
 int run_fwd(const gdn_shape* shape, bool kda, const void* q, const void* k, const void* v,
-            const float* g, const float* beta, const float* h0, void* o, float* ht, void* ws,
+            const void* g, const float* beta, const float* h0, void* o, float* ht, void* ws,
             size_t ws_bytes, void* stream, bool save = false, bool no_delta = false,
             const int* cu_seqlens = nullptr, int nseq = -1) {
   gdn::Problem p;
@@ -119,7 +121,7 @@ int run_fwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
   const size_t pre = seq_prefix(p);
   const size_t need = pre + (save ? ctx_bytes(p) : fwd_ws(p));
   if (need > 0 && (!ws || ws_bytes < need)) return GDN_ERR_WORKSPACE;
-  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.o = o; p.ht = ht;
+  p.q = q; p.k = k; p.v = v; p.g = static_cast<const float*>(g); p.beta = beta; p.h0 = h0; p.o = o; p.ht = ht;
   p.ws = static_cast<unsigned char*>(ws) + pre;
   p.ws_bytes = ws_bytes - pre;
   if (p.cu_seqlens) {
@@ -134,8 +136,8 @@ int run_fwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
 }
 
 int run_bwd(const gdn_shape* shape, bool kda, const void* q, const void* k, const void* v,
-            const float* g, const float* beta, const float* h0, const void* do_,
-            const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+            const void* g, const float* beta, const float* h0, const void* do_,
+            const float* dht, void* dq, void* dk, void* dv, void* dg, float* dbeta,
             float* dh0, void* ws, size_t ws_bytes, void* stream, bool saved = false,
             bool no_delta = false, const int* cu_seqlens = nullptr, int nseq = -1) {
   gdn::Problem p;
@@ -156,8 +158,8 @@ int run_bwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
   const size_t pre = seq_prefix(p);
   const size_t need = pre + (saved ? ctx_bytes(p) : bwd_ws(p));
   if (need > 0 && (!ws || ws_bytes < need)) return GDN_ERR_WORKSPACE;
-  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.do_ = do_; p.dht = dht;
-  p.dq = dq; p.dk_ = dk; p.dv_ = dv; p.dg = dg; p.dbeta = dbeta; p.dh0 = dh0;
+  p.q = q; p.k = k; p.v = v; p.g = static_cast<const float*>(g); p.beta = beta; p.h0 = h0; p.do_ = do_; p.dht = dht;
+  p.dq = dq; p.dk_ = dk; p.dv_ = dv; p.dg = static_cast<float*>(dg); p.dbeta = dbeta; p.dh0 = dh0;
   p.ws = static_cast<unsigned char*>(ws) + pre;
   p.ws_bytes = ws_bytes - pre;
   if (p.cu_seqlens) {
@@ -172,7 +174,7 @@ int run_bwd(const gdn_shape* shape, bool kda, const void* q, const void* k, cons
 }
 
 int run_decode(const gdn_shape* shape, bool kda, const void* q, const void* k, const void* v,
-               const float* g, const float* beta, const float* h0, void* o, float* ht,
+               const void* g, const float* beta, const float* h0, void* o, float* ht,
                void* stream) {
   gdn::Problem p;
   int rc = check_shape(shape, kda, &p);
@@ -188,7 +190,7 @@ int run_decode(const gdn_shape* shape, bool kda, const void* q, const void* k, c
     cudaError_t e = copy_state_or_zero(ht, h0, p, st);
     return e == cudaSuccess ? GDN_OK : fail_cuda(e);
   }
-  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.o = o; p.ht = ht;
+  p.q = q; p.k = k; p.v = v; p.g = static_cast<const float*>(g); p.beta = beta; p.h0 = h0; p.o = o; p.ht = ht;
   cudaError_t e = gdn::decode(p, st);
   return e == cudaSuccess ? GDN_OK : fail_cuda(e);
 }
@@ -290,7 +292,7 @@ int gdn_fwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
   return run_fwd(shape, false, q, k, v, g, beta, h0, o, ht, ws, ws_bytes, stream);
 }
 
-int kda_fwd(const gdn_shape* shape, const void* q, const void* k, const void* v, const float* g,
+int kda_fwd(const gdn_shape* shape, const void* q, const void* k, const void* v, const void* g,
             const float* beta, const float* h0, void* o, float* ht, void* ws, size_t ws_bytes,
             void* stream) {
   return run_fwd(shape, true, q, k, v, g, beta, h0, o, ht, ws, ws_bytes, stream);
@@ -304,9 +306,9 @@ int gdn_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
                  ws_bytes, stream);
 }
 
-int kda_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v, const float* g,
+int kda_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v, const void* g,
             const float* beta, const float* h0, const void* do_, const float* dht, void* dq,
-            void* dk, void* dv, float* dg, float* dbeta, float* dh0, void* ws, size_t ws_bytes,
+            void* dk, void* dv, void* dg, float* dbeta, float* dh0, void* ws, size_t ws_bytes,
             void* stream) {
   return run_bwd(shape, true, q, k, v, g, beta, h0, do_, dht, dq, dk, dv, dg, dbeta, dh0, ws,
                  ws_bytes, stream);
@@ -322,7 +324,7 @@ int gdn_fwd_save(const gdn_shape* shape, const void* q, const void* k, const voi
 }
 
 int kda_fwd_save(const gdn_shape* shape, const void* q, const void* k, const void* v,
-                 const float* g, const float* beta, const float* h0, void* o, float* ht,
+                 const void* g, const float* beta, const float* h0, void* o, float* ht,
                  void* ctx, size_t ctx_bytes, void* stream) {
   return run_fwd(shape, true, q, k, v, g, beta, h0, o, ht, ctx, ctx_bytes, stream, true);
 }
@@ -336,8 +338,8 @@ int gdn_bwd_saved(const gdn_shape* shape, const void* q, const void* k, const vo
 }
 
 int kda_bwd_saved(const gdn_shape* shape, const void* q, const void* k, const void* v,
-                  const float* g, const float* beta, const float* h0, const void* do_,
-                  const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                  const void* g, const float* beta, const float* h0, const void* do_,
+                  const float* dht, void* dq, void* dk, void* dv, void* dg, float* dbeta,
                   float* dh0, void* ctx, size_t ctx_bytes, void* stream) {
   return run_bwd(shape, true, q, k, v, g, beta, h0, do_, dht, dq, dk, dv, dg, dbeta, dh0, ctx,
                  ctx_bytes, stream, true);
@@ -350,7 +352,7 @@ int gdn_decode(const gdn_shape* shape, const void* q, const void* k, const void*
 }
 
 int kda_decode(const gdn_shape* shape, const void* q, const void* k, const void* v,
-               const float* g, const float* beta, const float* h0, void* o, float* ht,
+               const void* g, const float* beta, const float* h0, void* o, float* ht,
                void* stream) {
   return run_decode(shape, true, q, k, v, g, beta, h0, o, ht, stream);
 }
@@ -397,9 +399,9 @@ size_t mamba2_varlen_workspace(const gdn_shape* shape, int nseq, int backward) {
   return query_ws(shape, false, backward != 0, true, nseq);
 }
 
-#define GDN_VARLEN_PAIR(name, kda, nodelta)                                                        \
+#define GDN_VARLEN_PAIR(name, kda, nodelta, GT, DGT)                                               \
   int name##_fwd_varlen(const gdn_shape* shape, const int* cu_seqlens, int nseq, const void* q,  \
-                        const void* k, const void* v, const float* g, const float* beta,         \
+                        const void* k, const void* v, const GT* g, const float* beta,            \
                         const float* h0, void* o, float* ht, void* ws, size_t ws_bytes,          \
                         void* stream) {                                                          \
     if (nseq < 0) return GDN_ERR_SHAPE;                                                          \
@@ -407,17 +409,17 @@ size_t mamba2_varlen_workspace(const gdn_shape* shape, int nseq, int backward) {
                    nodelta, cu_seqlens, nseq);                                                    \
   }                                                                                              \
   int name##_bwd_varlen(const gdn_shape* shape, const int* cu_seqlens, int nseq, const void* q,  \
-                        const void* k, const void* v, const float* g, const float* beta,         \
+                        const void* k, const void* v, const GT* g, const float* beta,            \
                         const float* h0, const void* do_, const float* dht, void* dq, void* dk,  \
-                        void* dv, float* dg, float* dbeta, float* dh0, void* ws,                 \
+                        void* dv, DGT* dg, float* dbeta, float* dh0, void* ws,                   \
                         size_t ws_bytes, void* stream) {                                         \
     if (nseq < 0) return GDN_ERR_SHAPE;                                                          \
     return run_bwd(shape, kda, q, k, v, g, beta, h0, do_, dht, dq, dk, dv, dg, dbeta, dh0, ws,   \
                    ws_bytes, stream, false, nodelta, cu_seqlens, nseq);                           \
   }
-GDN_VARLEN_PAIR(gdn, false, false)
-GDN_VARLEN_PAIR(kda, true, false)
-GDN_VARLEN_PAIR(mamba2, false, true)
+GDN_VARLEN_PAIR(gdn, false, false, float, float)
+GDN_VARLEN_PAIR(kda, true, false, void, void)  // fp32 or bf16 gate (GDN_BF16_G16)
+GDN_VARLEN_PAIR(mamba2, false, true, float, float)
 #undef GDN_VARLEN_PAIR
 
 }  // extern "C"

@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(32 * kDecWarps) decode_kernel(Problem p) {
     for (int d = lane; d < kMaxD; d += 32) {  // zero past dk
       const bool in = d < dk;
       const float kd = in ? dld(k + tokh * dk + d) : 0.f, qd = in ? dld(q + tokh * dk + d) : 0.f;
-      const float ad = !in ? 0.f : KDA ? expf(p.g[tokh * dk + d]) : ag;
+      const float ad = !in ? 0.f : KDA ? expf(gate_load(p, tokh * dk + d)) : ag;
       kv[d] = kd;
       av[d] = ad;
       kav[d] = ad * kd;

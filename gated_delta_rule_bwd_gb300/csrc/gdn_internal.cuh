@@ -13,6 +13,7 @@ namespace gdn {
 struct Problem {
   int B, T, H, dk, dv, C, N;  // N = ceil(T / C) chunks per sequence
   bool kda, bf16;
+  bool g16;       // KDA gate g and dg in bf16 (carried in the float pointers below)
   bool no_delta;  // the Mamba2 mixer: the state only accumulates beta k v^T (no delta rule)
   const void *q, *k, *v, *do_;
   const float *g, *beta, *h0, *dht;
@@ -30,6 +31,17 @@ struct Problem {
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Element i of the gate g (fp32, or bf16 when g16) and a store into dg.
+__device__ __forceinline__ float gate_load(const Problem& p, size_t i) {
+  return p.g16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.g)[i]) : p.g[i];
+}
+__device__ __forceinline__ void dgate_store(const Problem& p, size_t i, float v) {
+  if (p.g16)
+    reinterpret_cast<__nv_bfloat16*>(p.dg)[i] = __float2bfloat16_rn(v);
+  else
+    p.dg[i] = v;
+}
 
 // Number of sequences (batch rows, or packed sequences).
 inline int num_seqs(const Problem& p) { return p.cu_seqlens ? p.nseq : p.B; }

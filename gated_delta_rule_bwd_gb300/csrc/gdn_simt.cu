@@ -171,7 +171,7 @@ __device__ void load_chunk_keys(const Problem& p, int b, int h, int t0, int n, f
   if (KDA) {
     for (int i = threadIdx.x; i < C * dk; i += kThreads) {
       const int r = i / dk, d = i % dk;
-      gm[r * lk + d] = r < n ? p.g[tok(p, b, t0 + r, h, dk) + d] : 0.f;
+      gm[r * lk + d] = r < n ? gate_load(p, tok(p, b, t0 + r, h, dk) + d) : 0.f;
     }
   } else {
     for (int r = threadIdx.x; r < C; r += kThreads)
@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_reduce_kernel(SimtArgs a) {
       float s = 0.f;
       for (int sp = 0; sp < a.nsplit; ++sp) s += a.part[PL.dgam + sp * tokh * GD + off];
       run += s;
-      p.dg[off] = run;
+      dgate_store(p, off, run);
     }
   }
 }

@@ -79,13 +79,14 @@ constexpr int kPrepSmemBytes = kP_BAR + 64 + 1024;
 static_assert(2 * (kPrepSmemBytes + 1024) <= 228 * 1024, "two prep CTAs per SM");
 
 struct KdaPrepParams {
-  const float* g;         // [B, T, H, dk]
+  const float* g;         // [B, T, H, dk] (bf16 when g16)
   const float* beta;      // [B, T, H]
   unsigned char* ktiles;  // [B*H][N][kKTBytes]
   int* skip;              // [sequences * H] flags, zero before the launch
   int B, T, H, N;
   Seqs sq;
   int nseq;
+  bool g16;
 };
 
 template <bool Packed>
@@ -132,12 +133,22 @@ kda_tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
   float gm[32];
   {
     const size_t stride = (size_t)p.H * D;
-    const float* src = p.g + (((size_t)b * p.T + t0) * p.H + h) * D + d;
+    const size_t o = (((size_t)b * p.T + t0) * p.H + h) * D + d;
     float mn = 0.f, mx = 0.f;
+    if (p.g16) {
+      const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(p.g) + o;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int r = 32 * rh + i;
-      gm[i] = r < n ? src[(size_t)r * stride] : 0.f;
+      for (int i = 0; i < 32; ++i) {
+        const int r = 32 * rh + i;
+        gm[i] = r < n ? __bfloat162float(src[(size_t)r * stride]) : 0.f;
+      }
+    } else {
+      const float* src = p.g + o;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int r = 32 * rh + i;
+        gm[i] = r < n ? src[(size_t)r * stride] : 0.f;
+      }
     }
 #pragma unroll
     for (int i = 1; i < 32; ++i) gm[i] += gm[i - 1];
@@ -754,7 +765,16 @@ __device__ __forceinline__ float* gate_elem(unsigned char* sm, int r, int d) {
   return reinterpret_cast<float*>(base + r * 128 + (d & 31) * 4);
 }
 
-template <bool Packed>
+// bf16 gate tile element as loaded by two TMA boxes of 64 dimensions: d 0-63
+// at the start of the V slot, d 64-127 at the start of the dZ halves (both
+// inside the fp32 tile's footprint, which the in-place dg sums reuse once
+// every thread has read its gate values)
+__device__ __forceinline__ float gate_elem16(const unsigned char* sm, int r, int d) {
+  const unsigned char* base = d < 64 ? sm + kB_V : sm + kB_ZO;
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + r * 128 + (d & 63) * 2));
+}
+
+template <bool Packed, bool G16>
 __global__ void __launch_bounds__(BT, 1)
 kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_dq,
@@ -1071,9 +1091,9 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
       }
       bulk_commit_group();
       // the gate tile, d 0-63 into the V slot (V is read for the last time)
-      mbar_arrive_expect_tx(bar_g, 32768);
+      mbar_arrive_expect_tx(bar_g, G16 ? 16384 : 32768);
       tma_load_4d(sm + kB_V, &tm_g, bar_g, 0, h, t0, b);
-      tma_load_4d(sm + kB_V + 8192, &tm_g, bar_g, 32, h, t0, b);
+      if (!G16) tma_load_4d(sm + kB_V + 8192, &tm_g, bar_g, 32, h, t0, b);
       ++g_issued;
       const uint32_t id = idesc_bf16(128, 64, false, true);
       for (int ks = 0; ks < 8; ++ks)
@@ -1087,7 +1107,7 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
     if (tid == 0) {
       // d 64-127 of the gate tile into the dZ halves (dZ is read for the last time)
       tma_load_4d(sm + kB_ZO, &tm_g, bar_g, 64, h, t0, b);
-      tma_load_4d(sm + kB_ZO + 16384, &tm_g, bar_g, 96, h, t0, b);
+      if (!G16) tma_load_4d(sm + kB_ZO + 16384, &tm_g, bar_g, 96, h, t0, b);
     }
     {
       float x[16];
@@ -1199,7 +1219,9 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
     float gam[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i)  // (a packed sequence's rows past its end hold the next one's gates)
-      gam[i] = (!Packed || cg * 16 + i < n) ? *gate_elem(sm, cg * 16 + i, d) : 0.f;
+      gam[i] = (!Packed || cg * 16 + i < n)
+                   ? (G16 ? gate_elem16(sm, cg * 16 + i, d) : *gate_elem(sm, cg * 16 + i, d))
+                   : 0.f;
 #pragma unroll
     for (int i = 1; i < 16; ++i) gam[i] += gam[i - 1];
     red[kR_TOT + cg * 128 + d] = gam[15];
@@ -1271,8 +1293,18 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
         off += red[kR_C2 + c2 * 128 + d];
         if (c2 > cg) off += red[kR_COL + c2 * 128 + d];
       }
+      if (G16) {
+        // dg straight to global memory in bf16 (32 lanes: 64 contiguous bytes per token)
+        __nv_bfloat16* dg16 = reinterpret_cast<__nv_bfloat16*>(p.dg) +
+                              (((size_t)b * p.T + t0) * p.H + h) * D + d;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) *gate_elem(sm, cg * 16 + i, d) += off;  // dg
+        for (int i = 0; i < 16; ++i)
+          if (cg * 16 + i < n)
+            dg16[(size_t)(cg * 16 + i) * p.H * D] = __float2bfloat16_rn(*gate_elem(sm, cg * 16 + i, d) + off);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) *gate_elem(sm, cg * 16 + i, d) += off;  // dg
+      }
     }
     fence_async_shared();
     cta_sync();
@@ -1280,20 +1312,23 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
       const size_t o0 = (((size_t)b * p.T + t0) * p.H + h) * D;
       store_rows_bf16(sm + kB_X, p.dq + o0, (size_t)p.H * D, n, tid, BT);
       store_rows_bf16(sm + kB_X + 16384, p.dk + o0, (size_t)p.H * D, n, tid, BT);
-      for (int i = tid; i < n * 32; i += BT) {  // dg: 16-byte pieces of the fp32 rows
-        const int r = i >> 5, c = i & 31;
-        const float4 v = *reinterpret_cast<const float4*>(gate_elem(sm, r, c * 4));
-        *reinterpret_cast<float4*>(p.dg + o0 + (size_t)r * p.H * D + c * 4) = v;
-      }
+      if (!G16)
+        for (int i = tid; i < n * 32; i += BT) {  // dg: 16-byte pieces of the fp32 rows
+          const int r = i >> 5, c = i & 31;
+          const float4 v = *reinterpret_cast<const float4*>(gate_elem(sm, r, c * 4));
+          *reinterpret_cast<float4*>(p.dg + o0 + (size_t)r * p.H * D + c * 4) = v;
+        }
     } else if (tid == 0) {
       tma_store_4d(&tm_dq, sm + kB_X, 0, h, t0, b);
       tma_store_4d(&tm_dq, sm + kB_X + 8192, 64, h, t0, b);
       tma_store_4d(&tm_dk, sm + kB_X + 16384, 0, h, t0, b);
       tma_store_4d(&tm_dk, sm + kB_X + 24576, 64, h, t0, b);
-      tma_store_4d(&tm_dg, sm + kB_V, 0, h, t0, b);
-      tma_store_4d(&tm_dg, sm + kB_V + 8192, 32, h, t0, b);
-      tma_store_4d(&tm_dg, sm + kB_ZO, 64, h, t0, b);
-      tma_store_4d(&tm_dg, sm + kB_ZO + 16384, 96, h, t0, b);
+      if (!G16) {
+        tma_store_4d(&tm_dg, sm + kB_V, 0, h, t0, b);
+        tma_store_4d(&tm_dg, sm + kB_V + 8192, 32, h, t0, b);
+        tma_store_4d(&tm_dg, sm + kB_ZO, 64, h, t0, b);
+        tma_store_4d(&tm_dg, sm + kB_ZO + 16384, 96, h, t0, b);
+      }
       bulk_commit_group();
     }
     if (tid < 64 && tid < n) p.dbeta[((size_t)b * p.T + t0 + tid) * p.H + h] = db1[tid] + db2[tid];
@@ -1350,14 +1385,18 @@ KdaLayout layout(const Problem& p, bool with_bwd) {
 // 4-D map over a [B, T, H, 128] fp32 tensor (the KDA gate and its gradient);
 // box = 32 dimensions x 1 head x 64 tokens x 1 batch row, no swizzle (128-byte
 // rows); rows past T read as zero and are not written.
+// With a bf16 gate (g16) the box is 64 dimensions (the same 128-byte rows).
 cudaError_t make_gate_map(CUtensorMap* m, const void* ptr, const Problem& p) {
   auto enc = get_encoder();
   if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t es_bytes = p.g16 ? 2 : 4;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)p.H, (cuuint64_t)p.T, (cuuint64_t)p.B};
-  cuuint64_t strides[3] = {(cuuint64_t)D * 4, (cuuint64_t)p.H * D * 4, (cuuint64_t)p.T * p.H * D * 4};
-  cuuint32_t box[4] = {32, 1, 64, 1};
+  cuuint64_t strides[3] = {(cuuint64_t)D * es_bytes, (cuuint64_t)p.H * D * es_bytes,
+                           (cuuint64_t)p.T * p.H * D * es_bytes};
+  cuuint32_t box[4] = {p.g16 ? 64u : 32u, 1, 64, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(ptr), dims, strides, box, es,
+  CUresult r = enc(m, p.g16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                   const_cast<void*>(ptr), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -1369,7 +1408,7 @@ cudaError_t launch_prep(const Problem& p, cudaStream_t s, const KdaLayout& L) {
   CUtensorMap mk, mq;
   if ((e = make_token_map(&mk, p.k, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mq, p.q, p)) != cudaSuccess) return e;
-  KdaPrepParams pp{p.g, p.beta, L.ktiles, L.skip, p.B, p.T, p.H, p.N, Seqs::of(p), p.nseq};
+  KdaPrepParams pp{p.g, p.beta, L.ktiles, L.skip, p.B, p.T, p.H, p.N, Seqs::of(p), p.nseq, p.g16};
   auto kern = p.cu_seqlens ? kda_tc_prep_kernel<true> : kda_tc_prep_kernel<false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmemBytes);
   if (e != cudaSuccess) return e;
@@ -1444,7 +1483,8 @@ cudaError_t kda_tc_bwd(const Problem& p, cudaStream_t s, bool saved) {
   KdaBwdParams bp{p.dht, L.ktiles, reinterpret_cast<const unsigned char*>(L.states), L.skip,
                   p.dbeta, p.dh0, static_cast<__nv_bfloat16*>(p.dq), static_cast<__nv_bfloat16*>(p.dk_),
                   static_cast<__nv_bfloat16*>(p.dv_), p.dg, p.B, p.T, p.H, p.N, Seqs::of(p)};
-  auto kern = p.cu_seqlens ? kda_tc_bwd_kernel<true> : kda_tc_bwd_kernel<false>;
+  auto kern = p.cu_seqlens ? (p.g16 ? kda_tc_bwd_kernel<true, true> : kda_tc_bwd_kernel<true, false>)
+                           : (p.g16 ? kda_tc_bwd_kernel<false, true> : kda_tc_bwd_kernel<false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemBytes);
   if (e != cudaSuccess) return e;
   prof_before(s);

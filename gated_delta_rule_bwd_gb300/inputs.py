@@ -19,7 +19,8 @@ dht (only if ``with_dht``).
 * h0 ~ N(0, h0_std) in fp32 when ``h0_std`` is given, else no initial state.
 
 q, k, v and dO are rounded to ``dtype`` (round-to-nearest-even for bf16);
-g, beta, h0 and dht stay fp32.  These are the pre-training shapes and value
+g, beta, h0 and dht stay fp32 (g is rounded to bf16 with ``g_dtype="bf16"``,
+KDA's bf16-gate variant).  These are the pre-training shapes and value
 ranges of the Primus hybrid-LLM pretraining blog (MI355X), sections "The
 models we trained" and "Recipe": bf16, sequence length 2048; the pages' own
 data set (FineWeb-Edu) is replaced by these synthetic draws.
@@ -71,7 +72,7 @@ _DT = {"bf16": torch.bfloat16, "f32": torch.float32, "fp32": torch.float32}
 def make_inputs(B: int, T: int, H: int, dk: int, dv: int, *, kda: bool = False,
                 dtype: str = "bf16", g_mean: float = 2.0, h0_std: float | None = None,
                 with_dht: bool = False, seed: int = 0, device="cpu",
-                t_slice: int = 1 << 16) -> MixerInputs:
+                t_slice: int = 1 << 16, g_dtype: str = "f32") -> MixerInputs:
     """Draw one seeded input set (see the module docstring for the recipe).
 
     Large tensors are drawn per batch row in slices of ``t_slice`` tokens so
@@ -104,7 +105,8 @@ def make_inputs(B: int, T: int, H: int, dk: int, dv: int, *, kda: bool = False,
     k = normal_tokens(dk, l2n(1.0), dt)
     v = normal_tokens(dv, lambda x: x, dt)
     beta = normal_tokens(0, torch.sigmoid, torch.float32)
-    g = normal_tokens(dk if kda else 0, F.logsigmoid, torch.float32, mean=g_mean)
+    # g_dtype "bf16" (KDA's bf16-gate variant): the same draws rounded to bf16
+    g = normal_tokens(dk if kda else 0, F.logsigmoid, _DT[g_dtype], mean=g_mean)
     h0 = None
     if h0_std is not None:
         h0 = (torch.randn((B, H, dk, dv), generator=gen, device=device) * h0_std).float()

@@ -29,6 +29,7 @@ class Workload:
     delta: bool = True  # False: the Mamba2 mixer (scalar gate, no delta rule)
     block: bool = False  # the mixer with its fused neighbours (short conv, gated norm)
     conv_width: int = 4
+    g_dtype: str = "f32"  # "bf16": KDA's bf16-gate variant (g and dg in bf16)
 
     @property
     def mixer(self) -> str:
@@ -50,13 +51,16 @@ class Workload:
         return make_inputs(self.B if B is None else B, self.T if T is None else T, self.H,
                            self.dk, self.dv, kda=self.kda, dtype=self.dtype,
                            g_mean=self.g_mean, h0_std=self.h0_std, with_dht=with_dht,
-                           seed=seed, device=device)
+                           seed=seed, device=device, g_dtype=self.g_dtype)
 
 
 GDN_TINY_FP32 = Workload("gdn_tiny_fp32_B1_T64_H2_d16_C16", 1, 64, 2, 16, 16, 16, dtype="f32")
 GDN_300M_BF16 = Workload("gdn_300m_bf16_B16_T2048_H8_d128_C64", 16, 2048, 8, 128, 128, 64)
 KDA_300M_BF16 = Workload("kda_300m_bf16_B16_T2048_H8_d128_C64", 16, 2048, 8, 128, 128, 64,
                          kda=True)
+# KDA with the gate and its gradient in bf16 (half the gate traffic).
+KDA_300M_BF16_G16 = Workload("kda_300m_bf16_g16_B16_T2048_H8_d128_C64", 16, 2048, 8, 128, 128,
+                             64, kda=True, g_dtype="bf16")
 # The Mamba2 mixer of the same model list (the scalar-gated state GDN extends
 # with the delta rule) at the 300M pre-training shape.
 MAMBA2_300M_BF16 = Workload("mamba2_300m_bf16_B16_T2048_H8_d128_C64", 16, 2048, 8, 128, 128, 64,
@@ -79,7 +83,8 @@ GDN_DECODE_BF16 = Workload("gdn_decode_bf16_B256_T1_H16_d128", 256, 1, 16, 128, 
 KDA_DECODE_BF16 = Workload("kda_decode_bf16_B256_T1_H16_d128", 256, 1, 16, 128, 128, 64,
                            kda=True, h0_std=0.02, fwd_only=True)
 
-ALL = [GDN_TINY_FP32, GDN_300M_BF16, KDA_300M_BF16, MAMBA2_300M_BF16, GDN_BLOCK_300M_BF16,
+ALL = [GDN_TINY_FP32, GDN_300M_BF16, KDA_300M_BF16, KDA_300M_BF16_G16, MAMBA2_300M_BF16,
+       GDN_BLOCK_300M_BF16,
        GDN_1B_BF16_H0,
        GDN_1M_FWD_BF16, GDN_DECODE_BF16, KDA_DECODE_BF16]
 BY_NAME = {w.name: w for w in ALL}

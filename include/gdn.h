@@ -28,7 +28,7 @@
  *   q, k, dq, dk          [B, T, H, dk]   dtype per gdn_shape.dtype
  *   v, o, do_, dv         [B, T, H, dv]   dtype per gdn_shape.dtype
  *   g, dg (GDN)           [B, T, H]       fp32, log forget gate (a = exp(g))
- *   g, dg (KDA)           [B, T, H, dk]   fp32
+ *   g, dg (KDA)           [B, T, H, dk]   fp32, or bf16 with GDN_BF16_G16
  *   beta, dbeta           [B, T, H]       fp32, used as given
  *   h0, ht, dht, dh0      [B, H, dk, dv]  fp32
  * No query scale and no normalisation is applied inside: gradients are with
@@ -83,7 +83,8 @@ typedef enum {
   GDN_OK = 0,
   GDN_ERR_ARG = -1,            /* NULL required pointer, bad enum value        */
   GDN_ERR_SHAPE = -2,          /* B,T,H < 0, dk/dv outside [1,128], bad chunk  */
-  GDN_ERR_DTYPE = -3,          /* dtype not GDN_F32 / GDN_BF16                 */
+  GDN_ERR_DTYPE = -3,          /* dtype not a gdn_dtype, or GDN_BF16_G16 with a
+                                  mixer other than KDA                         */
   GDN_ERR_ALIGN = -4,          /* a pointer is not 16-byte aligned             */
   GDN_ERR_WORKSPACE = -5,      /* workspace NULL or smaller than required      */
   GDN_ERR_CUDA = -6,           /* a CUDA call failed; see gdn_last_cuda_error  */
@@ -92,9 +93,15 @@ typedef enum {
                                   0 to T (found on the device; see *_varlen)   */
 } gdn_status;
 
-typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+/* GDN_BF16_G16 (KDA only): bf16 token tensors, and the per-key-dimension gate
+ * g and its gradient dg in bf16 too, which halves the gate's traffic (4 dk
+ * bytes per token and head in each direction otherwise).  The kernels read
+ * g as bf16, compute in fp32 exactly as with an fp32 gate holding the same
+ * values, and round dg to bf16 once. */
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_BF16_G16 = 2 } gdn_dtype;
 
-/* Problem shape.  dtype is the element type of q, k, v, o, do_, dq, dk, dv. */
+/* Problem shape.  dtype is the element type of q, k, v, o, do_, dq, dk, dv
+ * (GDN_BF16_G16: bf16, with a bf16 KDA gate). */
 typedef struct {
   int B, T, H;  /* batch, tokens per sequence, heads; each >= 0 (0 = no work) */
   int dk, dv;   /* key / value head dimension, 1..128                         */
@@ -132,14 +139,16 @@ GDN_API int gdn_bwd(const gdn_shape* shape, const void* q, const void* k, const 
             const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
             float* dh0, void* ws, size_t ws_bytes, void* stream);
 
-/* KDA forward / backward: as GDN, with g and dg of shape [B,T,H,dk]. */
+/* KDA forward / backward: as GDN, with g and dg of shape [B,T,H,dk], fp32
+ * (or bf16 when shape->dtype is GDN_BF16_G16; every kda_* call takes g and
+ * dg as untyped pointers for that reason). */
 GDN_API int kda_fwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
-            const float* g, const float* beta, const float* h0, void* o, float* ht,
+            const void* g, const float* beta, const float* h0, void* o, float* ht,
             void* ws, size_t ws_bytes, void* stream);
 
 GDN_API int kda_bwd(const gdn_shape* shape, const void* q, const void* k, const void* v,
-            const float* g, const float* beta, const float* h0, const void* do_,
-            const float* dht, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+            const void* g, const float* beta, const float* h0, const void* do_,
+            const float* dht, void* dq, void* dk, void* dv, void* dg, float* dbeta,
             float* dh0, void* ws, size_t ws_bytes, void* stream);
 
 /* Training step with a saved context.  The backward pass needs the state
@@ -180,12 +189,12 @@ GDN_API int gdn_bwd_saved(const gdn_shape* shape, const void* q, const void* k, 
                           float* dbeta, float* dh0, void* ctx, size_t ctx_bytes, void* stream);
 
 GDN_API int kda_fwd_save(const gdn_shape* shape, const void* q, const void* k, const void* v,
-                         const float* g, const float* beta, const float* h0, void* o, float* ht,
+                         const void* g, const float* beta, const float* h0, void* o, float* ht,
                          void* ctx, size_t ctx_bytes, void* stream);
 
 GDN_API int kda_bwd_saved(const gdn_shape* shape, const void* q, const void* k, const void* v,
-                          const float* g, const float* beta, const float* h0, const void* do_,
-                          const float* dht, void* dq, void* dk, void* dv, float* dg,
+                          const void* g, const float* beta, const float* h0, const void* do_,
+                          const float* dht, void* dq, void* dk, void* dv, void* dg,
                           float* dbeta, float* dh0, void* ctx, size_t ctx_bytes, void* stream);
 
 /* Mamba2: the mixer that GDN extends with the delta rule.  The Primus blog's
@@ -249,13 +258,13 @@ GDN_API int gdn_bwd_varlen(const gdn_shape* shape, const int* cu_seqlens, int ns
                            void* dk, void* dv, float* dg, float* dbeta, float* dh0, void* ws,
                            size_t ws_bytes, void* stream);
 GDN_API int kda_fwd_varlen(const gdn_shape* shape, const int* cu_seqlens, int nseq, const void* q,
-                           const void* k, const void* v, const float* g, const float* beta,
+                           const void* k, const void* v, const void* g, const float* beta,
                            const float* h0, void* o, float* ht, void* ws, size_t ws_bytes,
                            void* stream);
 GDN_API int kda_bwd_varlen(const gdn_shape* shape, const int* cu_seqlens, int nseq, const void* q,
-                           const void* k, const void* v, const float* g, const float* beta,
+                           const void* k, const void* v, const void* g, const float* beta,
                            const float* h0, const void* do_, const float* dht, void* dq,
-                           void* dk, void* dv, float* dg, float* dbeta, float* dh0, void* ws,
+                           void* dk, void* dv, void* dg, float* dbeta, float* dh0, void* ws,
                            size_t ws_bytes, void* stream);
 GDN_API int mamba2_fwd_varlen(const gdn_shape* shape, const int* cu_seqlens, int nseq,
                               const void* q, const void* k, const void* v, const float* g,
@@ -281,7 +290,7 @@ GDN_API int gdn_decode(const gdn_shape* shape, const void* q, const void* k, con
                        const float* g, const float* beta, const float* h0, void* o, float* ht,
                        void* stream);
 GDN_API int kda_decode(const gdn_shape* shape, const void* q, const void* k, const void* v,
-                       const float* g, const float* beta, const float* h0, void* o, float* ht,
+                       const void* g, const float* beta, const float* h0, void* o, float* ht,
                        void* stream);
 
 /* The mixer's fused neighbours (Primus hybrid-LLM pretraining blog, section

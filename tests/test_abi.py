@@ -312,3 +312,14 @@ def test_neighbour_binding_refuses_cpu_tensors(L):
         gdn.short_conv_fwd(x, torch.zeros(256, 4), H=2)
     with pytest.raises(gdn.GdnError):
         gdn.gated_rmsnorm_fwd(x, x, torch.ones(256))
+
+
+def test_bf16_gate_dtype_is_kda_only(L):
+    s = shape(B=1, T=64, H=2, dk=128, dv=128, chunk=64, dtype=2)
+    assert call_fwd(L, s) == GDN_ERR_DTYPE                      # GDN
+    assert call_fwd(L, s, kda=True, o=None) == GDN_ERR_ARG       # KDA: accepted, then NULL o
+    assert L.mamba2_fwd(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, None, 0,
+                        None) == GDN_ERR_DTYPE
+    assert L.kda_uses_tensor_cores(ctypes.byref(s)) == 1
+    assert L.kda_bwd_workspace(ctypes.byref(s)) == L.kda_bwd_workspace(
+        ctypes.byref(shape(B=1, T=64, H=2, dk=128, dv=128, chunk=64, dtype=1)))

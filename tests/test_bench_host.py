@@ -1,6 +1,7 @@
 """Host-side logic of bench.py (CPU only): the algorithmic work it divides by,
 the clock record it attaches, and the ncu traffic it reads from profiles/."""
 import datetime
+import json
 import os
 
 import pytest
@@ -82,12 +83,17 @@ def test_recorded_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
 
 
 def test_committed_profiles_parse():
-    # every committed summary names a source hash and a traffic figure
+    # every committed kernel summary names a source hash and a traffic figure;
+    # the bench record holds one parseable JSON line per workload
     root = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "profiles")
     names = [n for n in os.listdir(root) if n.endswith(".md")]
     assert names
     for n in names:
         text = open(os.path.join(root, n)).read()
+        if n.startswith("bench_"):
+            lines = [json.loads(l) for l in text.splitlines() if l.startswith("{")]
+            assert lines and all("roofline" in d and "clocks" in d for d in lines), n
+            continue
         assert "kernel_source_sha256_16:" in text and "traffic_bytes_per_launch:" in text, n
 
 

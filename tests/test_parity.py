@@ -640,3 +640,83 @@ def test_varlen_invalid_offsets_are_reported():
     o, ht = gdn.gdn_fwd_varlen(x.q, x.k, x.v, x.g, x.beta, good)
     torch.cuda.synchronize()
     assert gdn.device_status() == 0 and torch.isfinite(o.float()).all()
+
+
+# ----------------------------------------------------------- KDA with a bf16 gate
+
+def _as_f32_gate(x):
+    """The same inputs with the bf16 gate widened to fp32 (identical values)."""
+    import copy
+    y = copy.copy(x)
+    y.g = x.g.float()
+    return y
+
+
+BF16_GATE = [
+    # B, T, H, dk, dv, chunk, g_mean: path
+    (2, 200, 2, 128, 128, 64, 2.0),    # tensor cores, 8-token tail
+    (1, 37, 3, 128, 128, 64, 2.0),     # tensor cores, T < chunk
+    (1, 256, 2, 128, 128, 64, -3.0),   # gates past the factor range: CUDA-core fallback
+    (2, 100, 3, 64, 64, 32, 2.0),      # CUDA cores
+]
+
+
+@pytest.mark.parametrize("case", BF16_GATE, ids=lambda c: "x".join(map(str, c)))
+def test_kda_bf16_gate_matches_oracle_and_fp32_gate(case):
+    """KDA with g and dg in bf16 (GDN_BF16_G16): against the oracle on the
+    bf16 gate's values, and bit for bit against the fp32-gate call on the same
+    values (every output but dg equal; dg equal to the fp32 call's dg rounded
+    to bf16), with the saved-context pair equal to the recomputing one."""
+    B, T, H, dk, dv, chunk, g_mean = case
+    x = make_inputs(B, T, H, dk, dv, kda=True, dtype="bf16", g_mean=g_mean, h0_std=0.3,
+                    with_dht=True, seed=31, g_dtype="bf16")
+    assert x.g.dtype == torch.bfloat16
+    o, ht, gr = run_gpu(x, chunk)
+    assert gr["dg"].dtype == torch.bfloat16
+    compare(x, o, ht, gr, fp32=False)
+    o32, ht32, gr32 = run_gpu(_as_f32_gate(x), chunk)
+    assert torch.equal(o, o32) and torch.equal(ht, ht32)
+    for n in ("dq", "dk", "dv", "dbeta", "dh0"):
+        assert torch.equal(gr[n], gr32[n]), n
+    assert torch.equal(gr["dg"], gr32["dg"].to(torch.bfloat16))
+    d = x.to("cuda")
+    o2, ht2, ctx = gdn.kda_fwd_save(d.q, d.k, d.v, d.g, d.beta, d.h0, chunk=chunk)
+    gr2 = gdn.kda_bwd_saved(d.q, d.k, d.v, d.g, d.beta, d.h0, d.do, ctx, d.dht, chunk=chunk)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, o) and torch.equal(ht2, ht)
+    for n in gr:
+        assert torch.equal(gr2[n], gr[n]), n
+
+
+def test_kda_bf16_gate_varlen_and_decode():
+    """The bf16 gate through the packed-sequence calls and the decode step."""
+    lens = [1, 64, 100, 0, 77]
+    seqs = [make_inputs(1, L, 2, 128, 128, kda=True, dtype="bf16", h0_std=0.3, with_dht=True,
+                        seed=200 + i, g_dtype="bf16") for i, L in enumerate(lens)]
+    x, cu = _pack(seqs)
+    d = {n: (t.to("cuda") if t is not None else None) for n, t in x.items()}
+    cu_d = cu.to("cuda")
+    o, ht = gdn.kda_fwd_varlen(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_d, d["h0"])
+    gr = gdn.kda_bwd_varlen(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_d, d["h0"], d["do"],
+                            d["dht"])
+    torch.cuda.synchronize()
+    assert gdn.device_status() == 0 and gr["dg"].dtype == torch.bfloat16
+    for i, sq in enumerate(seqs):
+        a, b = int(cu[i]), int(cu[i + 1])
+        o_ref, ht_ref = oracle.fwd(sq.q, sq.k, sq.v, sq.g, sq.beta, sq.h0, kda=True)
+        check(f"ht[{i}]", ht[i:i + 1].cpu(), ht_ref, False)
+        if b == a:
+            continue
+        ref = oracle.bwd(sq.q, sq.k, sq.v, sq.g, sq.beta, sq.h0, sq.do, sq.dht, kda=True)
+        check(f"o[{i}]", o[:, a:b].cpu(), o_ref, False)
+        for n in ("dq", "dk", "dv", "dg", "dbeta"):
+            check(f"{n}[{i}]", gr[n][:, a:b].cpu(), ref[n], False)
+    # decode: four tokens of 16 sequences, state updated in place
+    y = make_inputs(16, 4, 2, 128, 128, kda=True, dtype="bf16", h0_std=0.3, seed=7, g_dtype="bf16")
+    dy = y.to("cuda")
+    state = dy.h0.clone()
+    od, _ = gdn.kda_decode(dy.q, dy.k, dy.v, dy.g, dy.beta, state)
+    torch.cuda.synchronize()
+    o_ref, ht_ref = oracle.fwd(y.q, y.k, y.v, y.g, y.beta, y.h0, kda=True)
+    check("decode o", od.cpu(), o_ref, False)
+    check("decode ht", state.cpu(), ht_ref, False)
