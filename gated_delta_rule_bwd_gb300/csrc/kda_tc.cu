@@ -89,7 +89,7 @@ struct KdaPrepParams {
   bool g16;
 };
 
-template <bool Packed>
+template <bool Packed, bool G16>
 __global__ void __launch_bounds__(PT)
 kda_tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                    KdaPrepParams p) {
@@ -135,7 +135,7 @@ kda_tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const size_t stride = (size_t)p.H * D;
     const size_t o = (((size_t)b * p.T + t0) * p.H + h) * D + d;
     float mn = 0.f, mx = 0.f;
-    if (p.g16) {
+    if (G16) {
       const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(p.g) + o;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -1409,7 +1409,8 @@ cudaError_t launch_prep(const Problem& p, cudaStream_t s, const KdaLayout& L) {
   if ((e = make_token_map(&mk, p.k, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mq, p.q, p)) != cudaSuccess) return e;
   KdaPrepParams pp{p.g, p.beta, L.ktiles, L.skip, p.B, p.T, p.H, p.N, Seqs::of(p), p.nseq, p.g16};
-  auto kern = p.cu_seqlens ? kda_tc_prep_kernel<true> : kda_tc_prep_kernel<false>;
+  auto kern = p.cu_seqlens ? (p.g16 ? kda_tc_prep_kernel<true, true> : kda_tc_prep_kernel<true, false>)
+                           : (p.g16 ? kda_tc_prep_kernel<false, true> : kda_tc_prep_kernel<false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmemBytes);
   if (e != cudaSuccess) return e;
   // an ordinary launch: it must follow the flags' reset in full

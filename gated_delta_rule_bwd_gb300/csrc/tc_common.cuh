@@ -270,6 +270,42 @@ __device__ __forceinline__ void group_sync_tc(int id) {
   tc_fence_after();
 }
 
+// n-column form of cta_sum_rows16 for any CTA of 128 x (64 / n) threads:
+// each thread holds v[i] for tile column (n cg + i) of its row (cg = warp / 4);
+// out[r] (r < 64) gets the sum over all 128 rows.  Within a warp log2(n)
+// halving exchanges leave lane l with column n cg + (l >> (5 - log2 n)),
+// summed over the lanes that differ in the low bits by the remaining xor
+// adds; across the four warps of a column group via red[(4 cg + quad) n + i].
+template <int n>
+__device__ __forceinline__ void cta_sum_rows(float (&v)[n], float* red, float* out) {
+  constexpr int steps = n == 16 ? 4 : n == 8 ? 3 : n == 4 ? 2 : 1;
+  const int l = threadIdx.x & 31, w = threadIdx.x >> 5, quad = w & 3, cg = w >> 2;
+#pragma unroll
+  for (int step = 0; step < steps; ++step) {
+    const int off = 16 >> step, half = (n / 2) >> step;
+    const bool up = (l & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      if (i < half) {
+        const float send = up ? v[i] : v[i + half];
+        const float keep = up ? v[i + half] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16 >> steps; off > 0; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+  constexpr int sh = 5 - steps;
+  if ((l & ((1 << sh) - 1)) == 0) red[(cg * 4 + quad) * n + (l >> sh)] = v[0];
+  __syncthreads();
+  if (threadIdx.x < 64) {
+    const int c = threadIdx.x / n, i = threadIdx.x % n;
+    out[threadIdx.x] = red[(c * 4 + 0) * n + i] + red[(c * 4 + 1) * n + i] +
+                       red[(c * 4 + 2) * n + i] + red[(c * 4 + 3) * n + i];
+  }
+  __syncthreads();
+}
+
 // Each thread holds v[i] for tile column (16 cg + i) of its row; returns in
 // out[r] (r < 64) the sum over all 128 rows.  Within a warp: four halving
 // exchanges and one pairwise add (lane l ends with column 16 cg + l/2); across

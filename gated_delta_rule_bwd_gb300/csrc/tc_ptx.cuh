@@ -224,6 +224,34 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Same, 16 columns.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// n-column forms of the loads and stores above (n = 8, 16 or 32).
+template <int n>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[n]) {
+  if constexpr (n == 8) tmem_ld8(taddr, v);
+  else if constexpr (n == 16) tmem_ld16(taddr, v);
+  else tmem_ld32(taddr, v);
+}
+template <int n>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[n]) {
+  if constexpr (n == 16) tmem_st16(taddr, v);
+  else tmem_st32(taddr, v);
+}
+
 // ------------------------------------------------------------------ named barriers
 
 // Barrier over the `count` threads (a multiple of 32) of one warp group.
