@@ -92,7 +92,7 @@ struct KdaPrepParams {
 template <bool Packed, bool G16>
 __global__ void __launch_bounds__(PT)
 kda_tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-                   KdaPrepParams p) {
+                   const __grid_constant__ CUtensorMap tm_g, KdaPrepParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -118,11 +118,14 @@ kda_tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     mbar_init(bar_ld, 1);
     mbar_init(bar_mma, 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(bar_ld, 32768);
+    mbar_arrive_expect_tx(bar_ld, G16 ? 32768 + 16384 : 32768);
     tma_load_4d(sm + kP_KQ + 0, &tm_k, bar_ld, 0, h, t0, b);
     tma_load_4d(sm + kP_KQ + 8192, &tm_q, bar_ld, 0, h, t0, b);
     tma_load_4d(sm + kP_KQ + 16384, &tm_k, bar_ld, 64, h, t0, b);
     tma_load_4d(sm + kP_KQ + 24576, &tm_q, bar_ld, 64, h, t0, b);
+    // bf16 gate: the chunk's [64 tokens][128 dims] tile into the A slot (free until
+    // the A product, long after the gates are read)
+    if (G16) tma_load_4d(sm + kP_A, &tm_g, bar_ld, 0, h, t0, b);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, 64);
@@ -136,11 +139,14 @@ kda_tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const size_t o = (((size_t)b * p.T + t0) * p.H + h) * D + d;
     float mn = 0.f, mx = 0.f;
     if (G16) {
-      const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(p.g) + o;
+      (void)o;
+      __syncthreads();  // the barrier is initialised (thread 0, above) before anyone polls it
+      __syncthreads_and(mbar_wait(bar_ld, 0));  // (a failed wait is reported below)
+      const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(sm + kP_A) + d;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int r = 32 * rh + i;
-        gm[i] = r < n ? __bfloat162float(src[(size_t)r * stride]) : 0.f;
+        gm[i] = r < n ? __bfloat162float(src[r * D]) : 0.f;
       }
     } else {
       const float* src = p.g + o;
@@ -1386,14 +1392,14 @@ KdaLayout layout(const Problem& p, bool with_bwd) {
 // box = 32 dimensions x 1 head x 64 tokens x 1 batch row, no swizzle (128-byte
 // rows); rows past T read as zero and are not written.
 // With a bf16 gate (g16) the box is 64 dimensions (the same 128-byte rows).
-cudaError_t make_gate_map(CUtensorMap* m, const void* ptr, const Problem& p) {
+cudaError_t make_gate_map(CUtensorMap* m, const void* ptr, const Problem& p, int box_d = 0) {
   auto enc = get_encoder();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t es_bytes = p.g16 ? 2 : 4;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)p.H, (cuuint64_t)p.T, (cuuint64_t)p.B};
   cuuint64_t strides[3] = {(cuuint64_t)D * es_bytes, (cuuint64_t)p.H * D * es_bytes,
                            (cuuint64_t)p.T * p.H * D * es_bytes};
-  cuuint32_t box[4] = {p.g16 ? 64u : 32u, 1, 64, 1};
+  cuuint32_t box[4] = {box_d ? (cuuint32_t)box_d : (p.g16 ? 64u : 32u), 1, 64, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = enc(m, p.g16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
                    const_cast<void*>(ptr), dims, strides, box, es,
@@ -1405,9 +1411,11 @@ cudaError_t make_gate_map(CUtensorMap* m, const void* ptr, const Problem& p) {
 cudaError_t launch_prep(const Problem& p, cudaStream_t s, const KdaLayout& L) {
   cudaError_t e = cudaMemsetAsync(L.skip, 0, (size_t)num_seqs(p) * p.H * sizeof(int), s);
   if (e != cudaSuccess) return e;
-  CUtensorMap mk, mq;
+  CUtensorMap mk, mq, mg;
   if ((e = make_token_map(&mk, p.k, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mq, p.q, p)) != cudaSuccess) return e;
+  if (p.g16 && (e = make_gate_map(&mg, p.g, p, 128)) != cudaSuccess) return e;
+  if (!p.g16) mg = mk;  // not read
   KdaPrepParams pp{p.g, p.beta, L.ktiles, L.skip, p.B, p.T, p.H, p.N, Seqs::of(p), p.nseq, p.g16};
   auto kern = p.cu_seqlens ? (p.g16 ? kda_tc_prep_kernel<true, true> : kda_tc_prep_kernel<true, false>)
                            : (p.g16 ? kda_tc_prep_kernel<false, true> : kda_tc_prep_kernel<false, false>);
@@ -1415,7 +1423,7 @@ cudaError_t launch_prep(const Problem& p, cudaStream_t s, const KdaLayout& L) {
   if (e != cudaSuccess) return e;
   // an ordinary launch: it must follow the flags' reset in full
   prof_before(s);
-  kern<<<(unsigned)(max_chunks(p) * p.H), PT, kPrepSmemBytes, s>>>(mk, mq, pp);
+  kern<<<(unsigned)(max_chunks(p) * p.H), PT, kPrepSmemBytes, s>>>(mk, mq, mg, pp);
   prof_after(s, kKdaPrep);
   return cudaGetLastError();
 }
