@@ -77,6 +77,7 @@ constexpr int kP_X = kP_S + kSolveScratch * 4;  // exchange: totals, minima, max
 constexpr int kP_BAR = kP_X + 3 * 256 * 4;
 constexpr int kPrepSmemBytes = kP_BAR + 64 + 1024;
 static_assert(2 * (kPrepSmemBytes + 1024) <= 228 * 1024, "two prep CTAs per SM");
+static_assert(kP_S - kP_A >= 64 * 128 * 4, "the fp32 gate tile fits in the A and T slots");
 
 struct KdaPrepParams {
   const float* g;         // [B, T, H, dk] (bf16 when g16)
@@ -118,14 +119,14 @@ kda_tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     mbar_init(bar_ld, 1);
     mbar_init(bar_mma, 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(bar_ld, G16 ? 32768 + 16384 : 32768);
+    mbar_arrive_expect_tx(bar_ld, 32768 + 64 * D * (G16 ? 2 : 4));
     tma_load_4d(sm + kP_KQ + 0, &tm_k, bar_ld, 0, h, t0, b);
     tma_load_4d(sm + kP_KQ + 8192, &tm_q, bar_ld, 0, h, t0, b);
     tma_load_4d(sm + kP_KQ + 16384, &tm_k, bar_ld, 64, h, t0, b);
     tma_load_4d(sm + kP_KQ + 24576, &tm_q, bar_ld, 64, h, t0, b);
-    // bf16 gate: the chunk's [64 tokens][128 dims] tile into the A slot (free until
-    // the A product, long after the gates are read)
-    if (G16) tma_load_4d(sm + kP_A, &tm_g, bar_ld, 0, h, t0, b);
+    // the chunk's gate tile [64 tokens][128 dims] (16 KB bf16 / 32 KB fp32) into the
+    // A and T slots, free until the A product, long after the gates are read
+    tma_load_4d(sm + kP_A, &tm_g, bar_ld, 0, h, t0, b);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, 64);
@@ -135,13 +136,10 @@ kda_tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
   const int d = tid & 127, rh = tid >> 7;
   float gm[32];
   {
-    const size_t stride = (size_t)p.H * D;
-    const size_t o = (((size_t)b * p.T + t0) * p.H + h) * D + d;
     float mn = 0.f, mx = 0.f;
+    __syncthreads();  // the barrier is initialised (thread 0, above) before anyone polls it
+    __syncthreads_and(mbar_wait(bar_ld, 0));  // (a failed wait is reported below)
     if (G16) {
-      (void)o;
-      __syncthreads();  // the barrier is initialised (thread 0, above) before anyone polls it
-      __syncthreads_and(mbar_wait(bar_ld, 0));  // (a failed wait is reported below)
       const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(sm + kP_A) + d;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -149,11 +147,11 @@ kda_tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         gm[i] = r < n ? __bfloat162float(src[r * D]) : 0.f;
       }
     } else {
-      const float* src = p.g + o;
+      const float* src = reinterpret_cast<const float*>(sm + kP_A) + d;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int r = 32 * rh + i;
-        gm[i] = r < n ? src[(size_t)r * stride] : 0.f;
+        gm[i] = r < n ? src[r * D] : 0.f;
       }
     }
 #pragma unroll
@@ -1414,8 +1412,7 @@ cudaError_t launch_prep(const Problem& p, cudaStream_t s, const KdaLayout& L) {
   CUtensorMap mk, mq, mg;
   if ((e = make_token_map(&mk, p.k, p)) != cudaSuccess) return e;
   if ((e = make_token_map(&mq, p.q, p)) != cudaSuccess) return e;
-  if (p.g16 && (e = make_gate_map(&mg, p.g, p, 128)) != cudaSuccess) return e;
-  if (!p.g16) mg = mk;  // not read
+  if ((e = make_gate_map(&mg, p.g, p, 128)) != cudaSuccess) return e;
   KdaPrepParams pp{p.g, p.beta, L.ktiles, L.skip, p.B, p.T, p.H, p.N, Seqs::of(p), p.nseq, p.g16};
   auto kern = p.cu_seqlens ? (p.g16 ? kda_tc_prep_kernel<true, true> : kda_tc_prep_kernel<true, false>)
                            : (p.g16 ? kda_tc_prep_kernel<false, true> : kda_tc_prep_kernel<false, false>);
