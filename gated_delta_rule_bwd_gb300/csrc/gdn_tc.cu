@@ -1189,13 +1189,15 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int r = cg * 16 + i;
         const float vr = tile_elem(sm + kB_V + half * 8192, r, cc);
         const float dr = bt[r] * z[i];
-        stage_bf16(sm + kB_T, r, row, dr);  // dv; T and P have been read for the last time
         acc[i] = fmaf(ee[r] * dr, rr[i], acc[i]);  // -e_r dR_rc (K H_in)_rc  (rr = -(K H_in)^T)
         rr[i] = z[i] * (vr + ee[r] * rr[i]);      // dZ_rc R_rc
-        *reinterpret_cast<__nv_bfloat16*>(sm + kB_ZO + half * 16384 + sw_row_off(r, cc >> 3) +
-                                          (cc & 7) * 2) = __float2bfloat16_rn(z[i]);
         z[i] = ee[r] * dr;
       }
+      // dv = dR (T and P have been read for the last time) and the dZ rows of the
+      // [dZ; dO] operand, token-major: transposed stores of this warp's block
+      const uint32_t tz = tmem + lb + kBtZ + cg * 16;
+      stage_tmem_block(sm + kB_T, 8192, tz, quad * 32, cg * 16, [&](int r, float zz) { return bt[r] * zz; });
+      stage_tmem_block(sm + kB_ZO, 16384, tz, quad * 32, cg * 16, [](int, float zz) { return zz; });
       store_chunks(sm + kB_X + 16384, row, cg * 2, z, 2);
       cta_sum_rows16(rr, red, db1);
     }
@@ -1361,19 +1363,12 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const float2 q2 = __bfloat1622float2(qv[i / 2]);
         acc[i] = fmaf((i & 1) ? q2.y : q2.x, x[i], acc[i]);  // e_r dO_r . (Q H_in)_r
       }
-      {
-        float y[16];
-        tmem_ld16(tmem + lb + kBtX2 + cg * 16, y);  // dQ^T intra-chunk term
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          stage_bf16(sm + kB_X, cg * 16 + i, row, x[i] + y[i]);  // dq (X0 is free once the products are done)
-      }
-      tmem_ld16(tmem + lb + kBtU + cg * 16, x);  // dK^T row d, columns j
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int j = cg * 16 + i;
-        stage_bf16(sm + kB_X + 16384, j, row, x[i]);  // dk (X1)
-      }
+      // dq = both dQ^T terms (X0 is free once the products are done), dk (X1):
+      // transposed stores of this warp's blocks
+      stage_tmem_block(sm + kB_X, 8192, tmem + lb + kBtR + cg * 16, quad * 32, cg * 16,
+                       [](int, float q) { return q; }, tmem + lb + kBtX2 + cg * 16);
+      stage_tmem_block(sm + kB_X + 16384, 8192, tmem + lb + kBtU + cg * 16, quad * 32, cg * 16,
+                       [](int, float q) { return q; });
     }
     fence_async_shared();
     cta_sum_rows16(acc, red, dlc);  // (its barriers also publish the staged dq, dk)

@@ -344,6 +344,45 @@ __device__ __forceinline__ void stage_bf16(unsigned char* tile2, int r, int d, f
                                     (d & 7) * 2) = __float2bfloat16_rn(x);
 }
 
+// Stages a warp's 32 x 16 block of a transposed tile -- TMEM lanes (features)
+// lane0 .. lane0 + 31, columns (tokens) col0 .. col0 + 15 -- as bf16 rows of a
+// [64 x 128] token-major staging tile made of two K-major 128-byte-swizzled
+// feature halves `half_stride` bytes apart (element (token r, feature d) at
+// tile2 + (d >> 6) half_stride + sw_row_off(r, (d & 63) >> 3) + (d & 7) 2),
+// with f(token, value) applied first: two 16x256b loads and two transposed
+// 4-matrix stores per 16 lanes instead of one scalar store per element.
+// With tmem_b != 0 the staged value is the sum of the two TMEM blocks.
+template <typename F>
+__device__ __forceinline__ void stage_tmem_block(unsigned char* tile2, int half_stride,
+                                                 uint32_t tmem_lane0_col0, int lane0, int col0,
+                                                 F f, uint32_t tmem_b = 0) {
+  const int t = threadIdx.x & 31;
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    float v[8];
+    tmem_ld16x16(tmem_lane0_col0 + ((uint32_t)(16 * hh) << 16), v);
+    if (tmem_b) {
+      float u[8];
+      tmem_ld16x16(tmem_b + ((uint32_t)(16 * hh) << 16), u);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] += u[i];
+    }
+    const int f0 = lane0 + 16 * hh;  // first feature of these 16 lanes
+    const int c = col0 + 2 * (t & 3);
+    uint32_t w[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {  // matrix m: features f0 + 8 (m & 1), tokens col0 + 8 (m >> 1)
+      const int tok = c + 8 * (m >> 1);
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(f(tok, v[2 * m]), f(tok + 1, v[2 * m + 1]));
+      w[m] = *reinterpret_cast<uint32_t*>(&b2);
+    }
+    // this thread's row address: matrix t / 8, stored row t % 8
+    const int m = t >> 3, tok = col0 + 8 * (m >> 1) + (t & 7), fe = f0 + 8 * (m & 1);
+    unsigned char* dst = tile2 + (fe >> 6) * half_stride + sw_row_off(tok, (fe & 63) >> 3);
+    stmatrix_x4_trans(smem_u32(dst), w[0], w[1], w[2], w[3]);
+  }
+}
+
 // Writes rows [0, n) of a [64 x 128] bf16 staging tile (two K-major
 // 128-byte-swizzled halves of 8 KB, features 0-63 and 64-127) to global rows
 // dst + r * row_stride (in elements), 16 bytes per store; t / nth: this

@@ -239,6 +239,34 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 16 TMEM lanes x 16 columns (shape 16x256b, two repetitions): thread t gets
+// v[0], v[1] = lane (t / 4), columns 2 (t % 4) + {0, 1}; v[2], v[3] = lane
+// 8 + t / 4, the same columns; v[4..7] the same for columns + 8 -- the
+// fragment layout of an 8 x 8 matrix per register pair, as stmatrix takes it.
+// The lane of taddr is the first of the 16 (within the warp's sub-partition).
+__device__ __forceinline__ void tmem_ld16x16(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Stores four 8 x 8 bf16 matrices transposed: register i of every thread holds
+// its fragment of matrix i (row t / 4, columns 2 (t % 4) + {0, 1}); thread t
+// gives the shared address of stored row t % 8 of matrix t / 8 (16 bytes, the
+// fragment's column t % 8).
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t r0, uint32_t r1,
+                                                  uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
 // n-column forms of the loads and stores above (n = 8, 16 or 32).
 template <int n>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[n]) {
