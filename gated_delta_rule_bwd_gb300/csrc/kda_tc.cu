@@ -1072,12 +1072,19 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
       for (int i = 0; i < 16; ++i) {
         const int j = cg * 16 + i;
         z[i] += u[i];                                // dZ = dU + (T - I)^T dU
-        const float dr = bt[j] * z[i];
-        stage_bf16(sm + kB_T, j, row, dr);          // dv (T and P are read for the last time)
-        *reinterpret_cast<__nv_bfloat16*>(sm + kB_ZO + hv * 16384 + sw_row_off(j, cc >> 3) + (cc & 7) * 2) =
-            __float2bfloat16_rn(z[i]);
         rr[i] *= z[i];                               // dZ_jc R_jc
-        z[i] = dr;
+        z[i] *= bt[j];                               // dR
+      }
+      {
+        // dv = dR (T and P are read for the last time) and the dZ rows of the
+        // [dZ; dO] operand, token-major: transposed stores of this warp's block
+        // (the same sum dZ = Z + X1 + X2, read again in the 16x256b layout)
+        const uint32_t tz = tmem + lb + kBtZ + cg * 16, t1 = tmem + lb + kBtX1 + cg * 16,
+                       t2 = tmem + lb + kBtX2 + cg * 16;
+        stage_tmem_block(sm + kB_T, 8192, tz, quad * 32, cg * 16,
+                         [&](int j, float zz) { return bt[j] * zz; }, t1, t2);
+        stage_tmem_block(sm + kB_ZO, 16384, tz, quad * 32, cg * 16, [](int, float zz) { return zz; }, t1,
+                         t2);
       }
       store_chunks(sm + kB_X + 16384, row, cg * 2, z, 2);  // dR^T
       cta_sum_rows16(rr, red + kR_SUM, db1);

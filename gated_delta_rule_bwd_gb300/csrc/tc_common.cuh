@@ -351,11 +351,11 @@ __device__ __forceinline__ void stage_bf16(unsigned char* tile2, int r, int d, f
 // tile2 + (d >> 6) half_stride + sw_row_off(r, (d & 63) >> 3) + (d & 7) 2),
 // with f(token, value) applied first: two 16x256b loads and two transposed
 // 4-matrix stores per 16 lanes instead of one scalar store per element.
-// With tmem_b != 0 the staged value is the sum of the two TMEM blocks.
+// With tmem_b (and tmem_c) != 0 the staged value is the sum of the TMEM blocks.
 template <typename F>
 __device__ __forceinline__ void stage_tmem_block(unsigned char* tile2, int half_stride,
                                                  uint32_t tmem_lane0_col0, int lane0, int col0,
-                                                 F f, uint32_t tmem_b = 0) {
+                                                 F f, uint32_t tmem_b = 0, uint32_t tmem_c = 0) {
   const int t = threadIdx.x & 31;
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
@@ -364,6 +364,12 @@ __device__ __forceinline__ void stage_tmem_block(unsigned char* tile2, int half_
     if (tmem_b) {
       float u[8];
       tmem_ld16x16(tmem_b + ((uint32_t)(16 * hh) << 16), u);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] += u[i];
+    }
+    if (tmem_c) {
+      float u[8];
+      tmem_ld16x16(tmem_c + ((uint32_t)(16 * hh) << 16), u);
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] += u[i];
     }
