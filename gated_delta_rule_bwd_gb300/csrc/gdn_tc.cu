@@ -900,16 +900,17 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const GateView GV{gam, ee, ff, bt, gam + 256, gam + 320, eC, gam + 576};
   uint64_t* bar_load = reinterpret_cast<uint64_t*>(sm + kB_BAR);
   uint64_t* bar_mma = bar_load + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma + 1);
-  const uint32_t sKQ = smem_u32(sm + kB_KQ), sZO = smem_u32(sm + kB_ZO);
-  const uint32_t sGI = smem_u32(sm + kB_GI), sDG = smem_u32(sm + kB_DG);
-  const uint32_t sT = smem_u32(sm + kB_T), sP = smem_u32(sm + kB_P);
-  const uint32_t sDP = sP, sM = sT;
-  const uint32_t sX0 = smem_u32(sm + kB_X), sX1 = sX0 + 16384, sX2 = sX0 + 32768;
+  uint64_t* bar_kq = bar_load + 2;  // K K^T, Q K^T done; later dO^T P done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_load + 3);
+  // operand descriptors: every tile's is a base descriptor plus its offset
+  const uint64_t dK0 = sw128_desc(smem_u32(sm), 16, 1024), dM0 = sw128_desc(smem_u32(sm), 16384, 1024);
+  auto kdesc = [&](uint32_t off) { return desc_at(dK0, off); };  // K-major tiles
+  auto mdesc = [&](uint32_t off) { return desc_at(dM0, off); };  // MN-major tiles
 
   if (tid == 0) {
     mbar_init(bar_load, 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_kq, 1);
     fence_barrier_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -969,7 +970,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (NN > 1) load_gates(NN - 2);
   }
 
-  uint32_t mma_phase = 0, load_phase = 0;
+  uint32_t mma_phase = 0, load_phase = 0, kq_phase = 0;
   bool ok = true;
   auto mma_wait = [&]() {
     ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
@@ -1055,44 +1056,66 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if ((r >> 3) == c8) reinterpret_cast<__nv_bfloat16*>(&pk)[r & 7] = __float2bfloat16_rn(1.f);
       *reinterpret_cast<uint4*>(sm + kB_T + sw_row_off(r, c8)) = pk;
     }
-    // ---- MMA1: [K;Q] K^T;  -G_in K^T (not formed without the delta rule);  dG K^T
+    // ---- MMA1: [K;Q] K^T, committed on its own so that the P epilogue runs
+    // while the tensor cores go on with -G_in K^T (not formed without the
+    // delta rule) and dG K^T
     if (tid == 0) {
       const uint32_t id = idesc_bf16(128, 64, false, false);
       const uint32_t idn = idesc_bf16(128, 64, false, false, true);
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
-        mma_bf16(tmem + kBtKQ, sw128_desc(sKQ + off, 16, 1024), sw128_desc(sKQ + off, 16, 1024), id,
-                 ks > 0);
+        mma_bf16(tmem + kBtKQ, kdesc(kB_KQ + off), kdesc(kB_KQ + off), id, ks > 0);
+      }
+      mma_commit(bar_kq);
+      #pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
         if (!NoDelta)
-          mma_bf16(tmem + kBtR, sw128_desc(sGI + off, 16, 1024), sw128_desc(sKQ + off, 16, 1024), idn,
-                   ks > 0);
-        mma_bf16(tmem + kBtX1, sw128_desc(sDG + off, 16, 1024), sw128_desc(sKQ + off, 16, 1024), id,
-                 ks > 0);
+          mma_bf16(tmem + kBtR, kdesc(kB_GI + off), kdesc(kB_KQ + off), idn, ks > 0);
+        mma_bf16(tmem + kBtX1, kdesc(kB_DG + off), kdesc(kB_KQ + off), id, ks > 0);
       }
       mma_commit(bar_mma);
     }
-    mma_wait();
-    if (!ok) break;
-    // P = lower(Q K^T o Gam) from TMEM lanes 64-127
-    if (row >= 64) {
-      const int r = row - 64;
-      float v[16];
-      tmem_ld16(tmem + lb + kBtKQ + cg * 16, v);
-      decay_row(v, GV, r, cg * 16, false, 1.f);
-      store_chunks(sm + kB_P, r, cg * 2, v, 2);
+    // P = lower(Q K^T o Gam) from TMEM lanes 64-127 (warps of the upper two
+    // lane quarters; the issuing thread is in the first)
+    {
+      bool okp = true;
+      if (row >= 64) {
+        okp = mbar_wait(bar_kq, kq_phase);
+        tc_fence_after();
+        if (okp) {
+          const int r = row - 64;
+          float v[16];
+          tmem_ld16(tmem + lb + kBtKQ + cg * 16, v);
+          decay_row(v, GV, r, cg * 16, false, 1.f);
+          store_chunks(sm + kB_P, r, cg * 2, v, 2);
+        }
+      }
+      kq_phase ^= 1;
+      fence_async_shared();
+      tc_fence_before();
+      ok = __syncthreads_and(okp);
+      tc_fence_after();
+      if (!ok) break;
     }
-    fence_async_shared();
-    cta_sync();
     // ---- dO^T P
     if (tid == 0) {
       const uint32_t idmm = idesc_bf16(128, 64, true, true);
+      #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + kBtX2, sw128_desc(sZO + 8192 + ks * 2048, 16384, 1024),
-                 sw128_desc(sP + ks * 2048, 16384, 1024), idmm, ks > 0);
-      mma_commit(bar_mma);
+        mma_bf16(tmem + kBtX2, mdesc(kB_ZO + 8192 + ks * 2048),
+                 mdesc(kB_P + ks * 2048), idmm, ks > 0);
+      mma_commit(bar_kq);
       bulk_wait_read_all();  // the previous chunk's dq / dk staging (X0, X1) has been read
     }
-    mma_wait();
+    // This commit arrives once every product issued so far is done, the rest of
+    // MMA1 included: its own phase on bar_mma is passed over (a later wait on
+    // bar_mma targets the newest phase, which completes after it).
+    ok = __syncthreads_and(mbar_wait(bar_kq, kq_phase));
+    kq_phase ^= 1;
+    mma_phase ^= 1;
+    tc_fence_after();
     if (!ok) break;
     // ---- E3: beta R^T -> X0, dU^T -> X1  (this thread: row c, columns 16 cg + i)
     {
@@ -1117,10 +1140,11 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (tid == 0) {
       const uint32_t id = idesc_bf16(128, 64, false, false);
       const uint32_t idm = idesc_bf16(128, 64, false, true);
+      #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        mma_bf16(tmem + kBtU, sw128_desc(sX0 + ks * 32, 16, 1024), sw128_desc(sT + ks * 32, 16, 1024), id,
+        mma_bf16(tmem + kBtU, kdesc(kB_X + ks * 32), kdesc(kB_T + ks * 32), id,
                  ks > 0);
-        mma_bf16(tmem + kBtZ, sw128_desc(sX1 + ks * 32, 16, 1024), sw128_desc(sT + ks * 2048, 16384, 1024),
+        mma_bf16(tmem + kBtZ, kdesc(kB_X + 16384 + ks * 32), mdesc(kB_T + ks * 2048),
                  idm, ks > 0);
       }
       mma_commit(bar_mma);
@@ -1216,9 +1240,10 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       bulk_commit_group();
       if (ci > 0) issue_v(ci - 1);  // V has been read for the last time
       const uint32_t id = idesc_bf16(128, 64, false, true);
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        mma_bf16(tmem + kBtX1, sw128_desc(sZO + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024),
-                 sw128_desc(sX0 + ks * 2048, 16384, 1024), id, ks > 0);
+        mma_bf16(tmem + kBtX1, kdesc(kB_ZO + (ks / 4) * 16384 + (ks % 4) * 32),
+                 mdesc(kB_X + ks * 2048), id, ks > 0);
       mma_commit(bar_mma);
       bulk_wait_read_all();  // the staged dv is read before M and dP o Gam overwrite it
     }
@@ -1291,41 +1316,50 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (tid == 0) {
       // G3 = (e dO)^T Q - (e dR)^T K   [c x d]
       const uint32_t idg = idesc_bf16(128, 128, true, true);
+      #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + kBtG3, sw128_desc(sZO + 8192 + ks * 2048, 16384, 1024),
-                 sw128_desc(sKQ + 8192 + ks * 2048, 16384, 1024), idg, 1);
+        mma_bf16(tmem + kBtG3, mdesc(kB_ZO + 8192 + ks * 2048),
+                 mdesc(kB_KQ + 8192 + ks * 2048), idg, 1);
       const uint32_t idgn = idesc_bf16(128, 128, false, true, true);
+      #pragma unroll
       for (int ks = 0; ks < (NoDelta ? 0 : 4); ++ks)
-        mma_bf16(tmem + kBtG3, sw128_desc(sX1 + ks * 32, 16, 1024), sw128_desc(sKQ + ks * 2048, 16384, 1024),
+        mma_bf16(tmem + kBtG3, kdesc(kB_X + 16384 + ks * 32), mdesc(kB_KQ + ks * 2048),
                  idgn, 1);
       // dQ^T = G_in^T (e dO)^T + K^T (dP o Gam)^T   [d x r], the two terms in
       // separate accumulators (R columns, X2 columns): q . (first term) is the
       // state's part of the log-gate gradient
       const uint32_t idq = idesc_bf16(128, 64, true, false);
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        mma_bf16(tmem + kBtR, sw128_desc(sGI + ks * 2048, 16384, 1024),
-                 sw128_desc(sZO + 8192 + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024), idq, ks > 0);
+        mma_bf16(tmem + kBtR, mdesc(kB_GI + ks * 2048),
+                 kdesc(kB_ZO + 8192 + (ks / 4) * 16384 + (ks % 4) * 32), idq, ks > 0);
+      #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + kBtX2, sw128_desc(sKQ + ks * 2048, 16384, 1024), sw128_desc(sDP + ks * 32, 16, 1024),
+        mma_bf16(tmem + kBtX2, mdesc(kB_KQ + ks * 2048), kdesc(kB_P + ks * 32),
                  idq, ks > 0);
       // dK^T  [d x j] -> U columns
       const uint32_t idmm = idesc_bf16(128, 64, true, true);
       const uint32_t idmmn = idesc_bf16(128, 64, true, true, true);
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        mma_bf16(tmem + kBtU, sw128_desc(sDG + ks * 2048, 16384, 1024), sw128_desc(sX2 + ks * 2048, 16384, 1024),
+        mma_bf16(tmem + kBtU, mdesc(kB_DG + ks * 2048), mdesc(kB_X + 32768 + ks * 2048),
                  idmm, ks > 0);
       const int nd = NoDelta ? 0 : 1;  // the R- and A-terms vanish without the delta rule
+      #pragma unroll
       for (int ks = 0; ks < 8 * nd; ++ks)
-        mma_bf16(tmem + kBtU, sw128_desc(sGI + ks * 2048, 16384, 1024), sw128_desc(sX1 + ks * 2048, 16384, 1024),
+        mma_bf16(tmem + kBtU, mdesc(kB_GI + ks * 2048), mdesc(kB_X + 16384 + ks * 2048),
                  idmmn, 1);
+      #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + kBtU, sw128_desc(sKQ + 8192 + ks * 2048, 16384, 1024),
-                 sw128_desc(sDP + ks * 2048, 16384, 1024), idmm, 1);
+        mma_bf16(tmem + kBtU, mdesc(kB_KQ + 8192 + ks * 2048),
+                 mdesc(kB_P + ks * 2048), idmm, 1);
+      #pragma unroll
       for (int ks = 0; ks < 4 * nd; ++ks)
-        mma_bf16(tmem + kBtU, sw128_desc(sKQ + ks * 2048, 16384, 1024), sw128_desc(sM + ks * 32, 16, 1024),
+        mma_bf16(tmem + kBtU, mdesc(kB_KQ + ks * 2048), kdesc(kB_T + ks * 32),
                  idq, 1);
+      #pragma unroll
       for (int ks = 0; ks < 4 * nd; ++ks)
-        mma_bf16(tmem + kBtU, sw128_desc(sKQ + ks * 2048, 16384, 1024), sw128_desc(sM + ks * 2048, 16384, 1024),
+        mma_bf16(tmem + kBtU, mdesc(kB_KQ + ks * 2048), mdesc(kB_T + ks * 2048),
                  idmm, 1);
       mma_commit(bar_mma);
     }

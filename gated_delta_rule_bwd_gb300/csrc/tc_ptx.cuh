@@ -315,6 +315,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_byte
   return d;
 }
 
+// The descriptor of the tile `off` bytes (a multiple of 16) after the one `d`
+// describes: the start address is bits 0-13 in 16-byte units, and shared
+// memory ends below 256 KB, so the add never carries into the next field.
+// One add per MMA instead of rebuilding the descriptor.
+__device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t off) { return d + (off >> 4); }
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
 // a_mn / b_mn: operand is MN-major (1) or K-major (0).
 __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, bool a_mn, bool b_mn,
