@@ -1020,20 +1020,6 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int t0 = tb + ci * C, n = min(C, slen - ci * C);
     const bool rowwise = Packed && n < C;  // a packed sequence's partial last chunk
     fence_async_shared();  // the dG tile written last chunk, for MMA1 (after the barrier below)
-    if (tid == 0 && ci > 0) {
-      // the next chunk in the reverse scan: start pulling its tiles into L2
-      const int tp = t0 - C;
-      tma_prefetch_l2_4d(&tm_k, 0, h, tp, b);
-      tma_prefetch_l2_4d(&tm_k, 64, h, tp, b);
-      tma_prefetch_l2_4d(&tm_q, 0, h, tp, b);
-      tma_prefetch_l2_4d(&tm_q, 64, h, tp, b);
-      tma_prefetch_l2_4d(&tm_do, 0, h, tp, b);
-      tma_prefetch_l2_4d(&tm_do, 64, h, tp, b);
-      tma_prefetch_l2_4d(&tm_v, 0, h, tp, b);
-      tma_prefetch_l2_4d(&tm_v, 64, h, tp, b);
-      bulk_prefetch_l2(p.states + rec_bh<Packed>(p.sq, p.N, bh, sq_s, h, ci - 1) * 32768, 32768);
-      if (!NoDelta) bulk_prefetch_l2(p.tiles + rec_bh<Packed>(p.sq, p.N, bh, sq_s, h, ci - 1) * 8192, 8192);
-    }
     ok = __syncthreads_and(mbar_wait(bar_load, load_phase));
     if (!ok) break;
     load_phase ^= 1;

@@ -929,18 +929,7 @@ kda_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
         bulk_wait_read_all();  // the last chunk's dg, dq, dk stores have read the V slot
         issue_v(ci);
       }
-      if (ci > 0) {
-        issue_vec(ci - 1);
-        // the next chunk of the reverse scan: start pulling its tiles into L2
-        const int tp = t0 - C;
-        bulk_prefetch_l2(blk(ci - 1), kKTBytes);
-        bulk_prefetch_l2(p.states + (Packed ? p.sq.template rec_t<true>(sqi, h, ci - 1) : (size_t)bh * p.N + ci - 1) * 32768, 32768);
-        tma_prefetch_l2_4d(&tm_do, 0, h, tp, b);
-        tma_prefetch_l2_4d(&tm_do, 64, h, tp, b);
-        tma_prefetch_l2_4d(&tm_v, 0, h, tp, b);
-        tma_prefetch_l2_4d(&tm_v, 64, h, tp, b);
-        for (int x = 0; x < 128; x += 32) tma_prefetch_l2_4d(&tm_g, x, h, tp, b);
-      }
+      if (ci > 0) issue_vec(ci - 1);
     }
     ok = __syncthreads_and(mbar_wait(bar_load, load_phase));
     if (!ok) break;
