@@ -971,6 +971,39 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
 
   uint32_t mma_phase = 0, load_phase = 0, kq_phase = 0;
+  // dbeta and dg of a finished chunk are written by warps 4 and 5 while the
+  // next chunk's first products run (their inputs, db1, db2, dlc and the
+  // reduction scratch, are not rewritten before that chunk's E4)
+  int pend_t0 = 0, pend_n = -1;
+  auto flush_pending = [&]() {
+    const size_t base = ((size_t)b * p.T + pend_t0) * p.H + h;
+    if (warp == 5) {
+      if (lane < pend_n) p.dbeta[base + (size_t)lane * p.H] = db1[lane] + db2[lane];
+      if (lane + 32 < pend_n) p.dbeta[base + (size_t)(lane + 32) * p.H] = db1[lane + 32] + db2[lane + 32];
+    } else if (warp == 4) {
+      // dg_t = sum_{s >= t, s in chunk} dgamma_s + <dH_out, H_out>
+      float carry = 0.f;
+#pragma unroll
+      for (int w = 0; w < BT / 32; ++w) carry += red[256 + w];
+      float a0 = dlc[lane] + red[kRedRow + lane], a1 = dlc[lane + 32] + red[kRedRow + lane + 32];
+      float s1 = a1;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_down_sync(0xffffffffu, s1, off);
+        if (lane + off < 32) s1 += y;
+      }
+      const float tot1 = __shfl_sync(0xffffffffu, s1, 0);
+      float s0 = a0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_down_sync(0xffffffffu, s0, off);
+        if (lane + off < 32) s0 += y;
+      }
+      s0 += tot1;
+      if (lane < pend_n) p.dg[base + (size_t)lane * p.H] = carry + s0;
+      if (lane + 32 < pend_n) p.dg[base + (size_t)(lane + 32) * p.H] = carry + s1;
+    }
+  };
   bool ok = true;
   auto mma_wait = [&]() {
     ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
@@ -1063,6 +1096,7 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       mma_commit(bar_mma);
     }
+    if (pend_n >= 0) flush_pending();  // the chunk before, in warps 4 and 5
     // P = lower(Q K^T o Gam) from TMEM lanes 64-127 (warps of the upper two
     // lane quarters; the issuing thread is in the first)
     {
@@ -1349,6 +1383,12 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                  idmm, 1);
       mma_commit(bar_mma);
     }
+    if (warp == 1 && ci > 0) {
+      // gates of the next chunk of the reverse scan, while the products run
+      // (nothing from here on in this chunk reads them)
+      chunk_gates_raw(GV, graw + ((ci - 1) & 1) * 128, lane);
+      if (ci > 1) load_gates(ci - 2);
+    }
     // this thread's Q values for the q . dq sums (bf16 pairs), read while the
     // products run so that Q can be reloaded as soon as they are done
     __nv_bfloat162 qv[8];
@@ -1403,41 +1443,11 @@ gdn_tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       tma_store_4d(&tm_dk, sm + kB_X + 24576, 64, h, t0, b);
       bulk_commit_group();
     }
-    if (warp == 1 && ci > 0) {
-      // gates of the next chunk of the reverse scan (this chunk's are no longer read)
-      chunk_gates_raw(GV, graw + ((ci - 1) & 1) * 128, lane);
-      if (ci > 1) load_gates(ci - 2);
-    }
-    if (tid < 64) {
-      const int r = tid;
-      if (r < n) p.dbeta[((size_t)b * p.T + t0 + r) * p.H + h] = db1[r] + db2[r];
-    }
-    if (warp == 0) {
-      // dg_t = sum_{s >= t, s in chunk} dgamma_s + <dH_out, H_out>
-      float carry = 0.f;
-#pragma unroll
-      for (int w = 0; w < BT / 32; ++w) carry += red[256 + w];
-      float a0 = dlc[lane] + red[kRedRow + lane], a1 = dlc[lane + 32] + red[kRedRow + lane + 32];
-      float s1 = a1;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float y = __shfl_down_sync(0xffffffffu, s1, off);
-        if (lane + off < 32) s1 += y;
-      }
-      const float tot1 = __shfl_sync(0xffffffffu, s1, 0);
-      float s0 = a0;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float y = __shfl_down_sync(0xffffffffu, s0, off);
-        if (lane + off < 32) s0 += y;
-      }
-      s0 += tot1;
-      const size_t base = ((size_t)b * p.T + t0) * p.H + h;
-      if (lane < n) p.dg[base + (size_t)lane * p.H] = carry + s0;
-      if (lane + 32 < n) p.dg[base + (size_t)(lane + 32) * p.H] = carry + s1;
-    }
+    pend_t0 = t0;
+    pend_n = n;
   }
 
+  if (ok && pend_n >= 0) flush_pending();  // the last chunk of the reverse scan
   if (!ok) {
     if (tid == 0) {
       report_timeout();
