@@ -256,6 +256,10 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   cta_sync();
   const uint32_t tmem = *tmem_slot;
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+  // operand descriptors: every tile's is a base descriptor plus its offset
+  const uint64_t dK0 = sw128_desc(smem_u32(sm), 16, 1024);     // K-major tiles
+  const uint64_t dM0 = sw128_desc(smem_u32(sm), 16384, 1024);  // MN-major, halves 16 KB apart
+  const uint64_t dV0 = sw128_desc(smem_u32(sm), 8192, 1024);   // MN-major, halves 8 KB apart
   grid_dep_wait();  // the previous kernel's results (and its reads of what this one writes)
   grid_dep_launch();
   {
@@ -365,21 +369,26 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       fence_async_shared();
       group_sync_tc(kBarChain);
       if (gt == 0) mbar_arrive(bar_wf);  // W^T has been copied: the next MMA2 may run
-      const uint32_t st_kq = smem_u32(sm + kF_KQ + s * 32768);
+      const uint32_t st_off = kF_KQ + s * 32768;  // this chunk's K|Q stage
       const uint32_t tmU = kTmU0 + 64 * s;
       if (gt == 0) {
         // MMA3b: U^T += -G W^T (A: G K-major M=c K=d; B: W MN-major N=r K=d);
         // without the delta rule U = diag(beta) V holds no state term
         const uint32_t id3 = idesc_bf16(128, 64, false, true, true);
-        for (int ks = 0; ks < (NoDelta ? 0 : 8); ++ks)
-          mma_bf16(tmem + tmU, sw128_desc(smem_u32(sm + kF_G) + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024),
-                   sw128_desc(smem_u32(sm + kF_W) + ks * 2048, 16384, 1024), id3, has_v || ks > 0);
+        if (!NoDelta) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_bf16(tmem + tmU, desc_at(dK0, kF_G + (ks / 4) * 16384 + (ks % 4) * 32),
+                     desc_at(dM0, kF_W + ks * 2048), id3, has_v || ks > 0);
+        }
         // MMA4a: O = (eQ) G^T  (M=64: A = eQ rows r, K=d; B = G tile rows c, K=d)
         const uint32_t id4 = idesc_bf16(64, 128, false, false);
-        for (int ks = 0; ks < (want_o ? 8 : 0); ++ks) {
-          const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
-          mma_bf16(tmem + kTmO, sw128_desc(st_kq + 8192 + off, 16, 1024),
-                   sw128_desc(smem_u32(sm + kF_G) + off, 16, 1024), id4, ks > 0);
+        if (want_o) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
+            mma_bf16(tmem + kTmO, desc_at(dK0, st_off + 8192 + off), desc_at(dK0, kF_G + off), id4, ks > 0);
+          }
         }
         mma_commit(bar_s);
         bulk_wait_read_all();  // the last output rows staged in the U^T slot have been read
@@ -398,14 +407,16 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (gt == 0) {
         // MMA4b: O += P U  (A = P rows r, K=j; B = U^T tile rows c, K=j)
         const uint32_t id4 = idesc_bf16(64, 128, false, false);
-        for (int ks = 0; ks < (want_o ? 4 : 0); ++ks)
-          mma_bf16(tmem + kTmO, sw128_desc(smem_u32(sm + kF_P + s * 8192) + ks * 32, 16, 1024),
-                   sw128_desc(smem_u32(sm + kF_U) + ks * 32, 16, 1024), id4, 1);
+        if (want_o) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + kTmO, desc_at(dK0, kF_P + s * 8192 + ks * 32), desc_at(dK0, kF_U + ks * 32), id4, 1);
+        }
         // MMA5: G += U^T (f K)  (B: K tile, rows scaled by f, MN-major N=d, K=j)
         const uint32_t id5 = idesc_bf16(128, 128, false, true);
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tmem + kTmG, sw128_desc(smem_u32(sm + kF_U) + ks * 32, 16, 1024),
-                   sw128_desc(st_kq + ks * 2048, 16384, 1024), id5, 1);
+          mma_bf16(tmem + kTmG, desc_at(dK0, kF_U + ks * 32), desc_at(dM0, st_off + ks * 2048), id5, 1);
         mma_commit(bar_s);
         bulk_wait_read_all();  // the last entry-state copy has read the tile E5 rewrites next
       }
@@ -500,12 +511,12 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (pt == 0) *early_mma1 = 0;
     auto issue_mma1 = [&](int cn) {
       // MMA1: [K;Q] K^T, M=128 N=64 K=128 on the stage of chunk cn
-      const uint32_t kq = smem_u32(sm + kF_KQ + (cn & 1) * 32768);
+      const uint32_t kq = kF_KQ + (cn & 1) * 32768;
       const uint32_t idesc = idesc_bf16(128, 64, false, false);
+#pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
-        mma_bf16(tmem + kTmKQ, sw128_desc(kq + off, 16, 1024), sw128_desc(kq + off, 16, 1024), idesc,
-                 ks > 0);
+        mma_bf16(tmem + kTmKQ, desc_at(dK0, kq + off), desc_at(dK0, kq + off), idesc, ks > 0);
       }
       mma_commit(bar_p1);
     };
@@ -517,8 +528,6 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         gates + 384, gates + 385};
       float* ee = GV.ee;
       float* bt = GV.bt;
-      unsigned char* st = sm + kF_KQ + s * 32768;
-      const uint32_t st_kq = smem_u32(st);
       ok = group_and(kBarPrep, kGroup, mbar_wait(&bar_kq[s], (ci >> 1) & 1) && !*abort_flag);
       if (!ok) break;
       if (pt == 0) cnt[2 + s] += 1;
@@ -608,13 +617,19 @@ gdn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (pt == 0) {
         // MMA2: W^T = K^T T'^T  (A: K tile MN-major, M=d; B: T' K-major, N=r)
         const uint32_t id2 = idesc_bf16(128, 64, true, false);
-        for (int ks = 0; ks < (NoDelta ? 0 : 4); ++ks)
-          mma_bf16(tmem + kTmW, sw128_desc(st_kq + ks * 2048, 16384, 1024),
-                   sw128_desc(smem_u32(sm + kF_T1) + ks * 32, 16, 1024), id2, ks > 0);
+        const uint32_t st_off = kF_KQ + s * 32768;
+        if (!NoDelta) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + kTmW, desc_at(dM0, st_off + ks * 2048), desc_at(dK0, kF_T1 + ks * 32), id2, ks > 0);
+        }
         // MMA3a: U^T = V^T T''^T  (A: V tile MN-major, M=c; B: T'' K-major, N=r)
-        for (int ks = 0; ks < (has_v ? 4 : 0); ++ks)
-          mma_bf16(tmem + kTmU0 + 64 * s, sw128_desc(smem_u32(sm + kF_V) + ks * 2048, 8192, 1024),
-                   sw128_desc(smem_u32(sm + kF_T0) + ks * 32, 16, 1024), id2, ks > 0);
+        if (has_v) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + kTmU0 + 64 * s, desc_at(dV0, kF_V + ks * 2048), desc_at(dK0, kF_T0 + ks * 32), id2,
+                     ks > 0);
+        }
         mma_commit(bar_p);
       }
       if (warp == 9 && ci + 1 < NL) {
@@ -739,11 +754,12 @@ gdn_tc_solve_kernel(const __grid_constant__ CUtensorMap tm_k, SolveParams p) {
   if (ok) {
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t sk = smem_u32(sm + kS_K);
+      const uint64_t dk = sw128_desc(smem_u32(sm + kS_K), 16, 1024);
       const uint32_t id = idesc_bf16(64, 64, false, false);
+#pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t off = (ks / 4) * 8192 + (ks % 4) * 32;
-        mma_bf16(tmem, sw128_desc(sk + off, 16, 1024), sw128_desc(sk + off, 16, 1024), id, ks > 0);
+        mma_bf16(tmem, desc_at(dk, off), desc_at(dk, off), id, ks > 0);
       }
       mma_commit(bar_mma);
     }

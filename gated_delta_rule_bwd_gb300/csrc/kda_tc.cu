@@ -218,10 +218,12 @@ kda_tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     // K K^T with the decays folded in: Kp Km^T (M = 64: row r in TMEM lane 32 (r / 16) + r % 16)
     tc_fence_after();
     const uint32_t id = idesc_bf16(64, 64, false, false);
-    const uint32_t skq = smem_u32(sm + kP_KQ), skm = smem_u32(sm + kP_KM);
+    const uint64_t dK0 = sw128_desc(smem_u32(sm), 16, 1024);
+#pragma unroll
+    #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
-      mma_bf16(tmem, sw128_desc(skq + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024),
-               sw128_desc(skm + (ks / 4) * 8192 + (ks % 4) * 32, 16, 1024), id, ks > 0);
+      mma_bf16(tmem, desc_at(dK0, kP_KQ + (ks / 4) * 16384 + (ks % 4) * 32),
+               desc_at(dK0, kP_KM + (ks / 4) * 8192 + (ks % 4) * 32), id, ks > 0);
     mma_commit(bar_mma);
   }
   const bool loaded = ok;
@@ -355,6 +357,10 @@ kda_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
   cta_sync();
   const uint32_t tmem = *tmem_slot;
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+  // operand descriptors: every tile's is a base descriptor plus its offset
+  const uint64_t dK0 = sw128_desc(smem_u32(sm), 16, 1024);     // K-major tiles
+  const uint64_t dM0 = sw128_desc(smem_u32(sm), 16384, 1024);  // MN-major, halves 16 KB apart
+  const uint64_t dV0 = sw128_desc(smem_u32(sm), 8192, 1024);   // MN-major, halves 8 KB apart
   grid_dep_wait();
   grid_dep_launch();
   p.sq.get_t<Packed>(sqi, b, tb, slen, NL);
@@ -445,15 +451,16 @@ kda_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
       if (gt == 0) {
         // MMA3b: U^T += -G~ W~^T
         const uint32_t id3 = idesc_bf16(128, 64, false, true, true);
+        #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          mma_bf16(tmem + tmU, sw128_desc(smem_u32(sm + kF_G) + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024),
-                   sw128_desc(smem_u32(sm + kF_W) + ks * 2048, 16384, 1024), id3, 1);
+          mma_bf16(tmem + tmU, desc_at(dK0, kF_G + (ks / 4) * 16384 + (ks % 4) * 32),
+                   desc_at(dM0, kF_W + ks * 2048), id3, 1);
         // MMA4a: O = Qp G~^T  (M = 64: A = Qp rows r; B = G~ tile rows c)
         const uint32_t id4 = idesc_bf16(64, 128, false, false);
         for (int ks = 0; ks < (want_o ? 8 : 0); ++ks) {
           const uint32_t off = (ks / 4) * 16384 + (ks % 4) * 32;
-          mma_bf16(tmem + kTmO, sw128_desc(st_kq + 8192 + off, 16, 1024),
-                   sw128_desc(smem_u32(sm + kF_G) + off, 16, 1024), id4, ks > 0);
+          mma_bf16(tmem + kTmO, desc_at(dK0, (kF_KQ + s * 32768) + 8192 + off),
+                   desc_at(dK0, kF_G + off), id4, ks > 0);
         }
         mma_commit(bar_s);
         bulk_wait_read_all();  // the last output rows staged in the U^T slot have been read
@@ -472,14 +479,16 @@ kda_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
       if (gt == 0) {
         // MMA4b: O += P U
         const uint32_t id4 = idesc_bf16(64, 128, false, false);
+        #pragma unroll
         for (int ks = 0; ks < (want_o ? 4 : 0); ++ks)
-          mma_bf16(tmem + kTmO, sw128_desc(smem_u32(sm + kF_P + s * 8192) + ks * 32, 16, 1024),
-                   sw128_desc(smem_u32(sm + kF_U) + ks * 32, 16, 1024), id4, 1);
+          mma_bf16(tmem + kTmO, desc_at(dK0, kF_P + s * 8192 + ks * 32),
+                   desc_at(dK0, kF_U + ks * 32), id4, 1);
         // MMA5: G~ += U^T Km  (B: Km tile, MN-major N = d, K = j)
         const uint32_t id5 = idesc_bf16(128, 128, false, true);
+        #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tmem + kTmG, sw128_desc(smem_u32(sm + kF_U) + ks * 32, 16, 1024),
-                   sw128_desc(st_km + ks * 2048, 8192, 1024), id5, 1);
+          mma_bf16(tmem + kTmG, desc_at(dK0, kF_U + ks * 32),
+                   desc_at(dV0, (kF_KM + s * 16384) + ks * 2048), id5, 1);
         mma_commit(bar_s);
         bulk_wait_read_all();  // the last entry-state copy has read the tile rewritten next
       }
@@ -561,9 +570,10 @@ kda_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
       const uint32_t kq = smem_u32(sm + kF_KQ + (cn & 1) * 32768);
       const uint32_t km = smem_u32(sm + kF_KM + (cn & 1) * 16384);
       const uint32_t idesc = idesc_bf16(128, 64, false, false);
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        mma_bf16(tmem + kTmKQ, sw128_desc(kq + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024),
-                 sw128_desc(km + (ks / 4) * 8192 + (ks % 4) * 32, 16, 1024), idesc, ks > 0);
+        mma_bf16(tmem + kTmKQ, desc_at(dK0, (kF_KQ + (cn & 1) * 32768) + (ks / 4) * 16384 + (ks % 4) * 32),
+                 desc_at(dK0, (kF_KM + (cn & 1) * 16384) + (ks / 4) * 8192 + (ks % 4) * 32), idesc, ks > 0);
       mma_commit(bar_p1);
     };
     uint32_t p_phase = 0;
@@ -630,13 +640,15 @@ kda_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constan
       if (pt == 0) {
         // MMA2: W~^T = Kp^T T''^T  (A: Kp MN-major, M = d; B: T'' K-major, N = r)
         const uint32_t id2 = idesc_bf16(128, 64, true, false);
+        #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tmem + kTmW, sw128_desc(st_kq + ks * 2048, 16384, 1024),
-                   sw128_desc(smem_u32(sm + kF_T0) + ks * 32, 16, 1024), id2, ks > 0);
+          mma_bf16(tmem + kTmW, desc_at(dM0, (kF_KQ + s * 32768) + ks * 2048),
+                   desc_at(dK0, kF_T0 + ks * 32), id2, ks > 0);
         // MMA3a: U^T = V^T T''^T
+        #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tmem + kTmU0 + 64 * s, sw128_desc(smem_u32(sm + kF_V) + ks * 2048, 8192, 1024),
-                   sw128_desc(smem_u32(sm + kF_T0) + ks * 32, 16, 1024), id2, ks > 0);
+          mma_bf16(tmem + kTmU0 + 64 * s, desc_at(dV0, kF_V + ks * 2048),
+                   desc_at(dK0, kF_T0 + ks * 32), id2, ks > 0);
         mma_commit(bar_p);
       }
       ok = group_and(kBarPrep, kGroup, mbar_wait(bar_p, p_phase));
