@@ -220,7 +220,6 @@ kda_tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const uint32_t id = idesc_bf16(64, 64, false, false);
     const uint64_t dK0 = sw128_desc(smem_u32(sm), 16, 1024);
 #pragma unroll
-    #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
       mma_bf16(tmem, desc_at(dK0, kP_KQ + (ks / 4) * 16384 + (ks % 4) * 32),
                desc_at(dK0, kP_KM + (ks / 4) * 8192 + (ks % 4) * 32), id, ks > 0);
