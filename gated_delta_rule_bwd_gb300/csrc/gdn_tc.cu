@@ -1682,18 +1682,27 @@ gdn_tc_combine_kernel(const float* M, const float* Nl, const float* h0, float* H
     for (int i = t; i < D * D; i += kCombineThreads) ht[(size_t)bh * D * D + i] = Hs[i];
 }
 
-// Chunks per segment of the forward pass, or 0 for no segments.  Segments
-// cost about three times the arithmetic, so they are used only when they
-// multiply the number of busy SMs by at least four; segments are at least 32
-// chunks long.
+// Chunks per segment of the forward pass, or 0 for no segments.  A pass over
+// nseg segments per sequence takes about waves x (chunks per segment) chunk
+// times, waves = ceil(seqs nseg / SMs) with one CTA per SM; the segmented
+// forward runs three such passes (transitions, local states, outputs).  The
+// count with the least time is taken (the smallest of equals), and segments
+// are used only when three passes beat one unsegmented pass by a third.
+// Segments are at least 32 chunks long.
 int fwd_seg_chunks(const Problem& p) {
   if (p.no_delta || p.cu_seqlens) return 0;  // segments: GDN batches only
   const long seqs = (long)p.B * p.H;
-  const int sms = sm_count();
-  if (seqs <= 0 || p.N < 128) return 0;
-  const long want = std::min<long>(sms / seqs, p.N / 32);
-  if (want < 4) return 0;
-  return (int)((p.N + want - 1) / want);
+  const long sms = sm_count();
+  if (seqs <= 0 || sms <= 0 || p.N < 128) return 0;
+  auto waves = [&](long ctas) { return (ctas + sms - 1) / sms; };
+  const long plain = waves(seqs) * p.N;
+  long best = 0, best_cost = 0;
+  for (long nseg = 2; nseg <= p.N / 32; ++nseg) {
+    const long cost = 3 * waves(seqs * nseg) * ((p.N + nseg - 1) / nseg);
+    if (best == 0 || cost < best_cost) best = nseg, best_cost = cost;
+  }
+  if (best == 0 || 3 * best_cost > 2 * plain) return 0;
+  return (int)((p.N + best - 1) / best);
 }
 
 size_t seg_state_bytes(const Problem& p, int seg_chunks) {
