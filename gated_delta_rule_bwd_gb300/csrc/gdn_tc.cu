@@ -1636,50 +1636,71 @@ cudaError_t launch_fwd(const Problem& p, cudaStream_t s, const unsigned char* ti
 // arithmetic of the plain forward, spread over B*H*nseg CTAs instead of B*H.
 
 constexpr int kCombineThreads = 256;
-constexpr int kCombineSmem = 2 * D * D * 4;  // H and M, fp32
+constexpr int kCombineSplit = 8;               // CTAs per sequence, each a block of H's columns
+constexpr int kCombineCols = D / kCombineSplit;  // 16 columns of H (dv) per CTA
+constexpr int kCombineLdM = D + 1;             // M row stride in shared memory (no bank conflicts)
+constexpr int kCombineSmem = (D * kCombineLdM + D * kCombineCols) * 4;  // M, then the H block, fp32
 
+// H_in(s + 1) = M_s H_in(s) + N_s acts on each column of H on its own, so
+// the columns are split over kCombineSplit CTAs per sequence.  Thread t
+// owns row d = t / 2 and columns 8 (t % 2) + [0, 8) of its CTA's block.
 __global__ void __launch_bounds__(kCombineThreads)
 gdn_tc_combine_kernel(const float* M, const float* Nl, const float* h0, float* Hin, float* ht,
                       int nseg) {
   extern __shared__ float csm[];
-  float* Hs = csm;           // [dk][dv]
-  float* Ms = csm + D * D;   // [dk][dk]
-  const int t = threadIdx.x, bh = blockIdx.x;
-  const int d0 = (t / 16) * 8, e0 = (t % 16) * 8;  // this thread's 8 x 8 block of H
-  for (int i = t; i < D * D; i += kCombineThreads) Hs[i] = h0 ? h0[(size_t)bh * D * D + i] : 0.f;
+  float* Ms = csm;                       // [dk][dk], row stride kCombineLdM
+  float* Hs = csm + D * kCombineLdM;     // [dk][kCombineCols]
+  const int t = threadIdx.x, bh = blockIdx.x / kCombineSplit;
+  const int c0 = (blockIdx.x % kCombineSplit) * kCombineCols;  // first column of H
+  const int d = t >> 1, e0 = (t & 1) * 8;
+  for (int i = t; i < D * kCombineCols; i += kCombineThreads) {
+    const int r = i / kCombineCols, c = i % kCombineCols;
+    Hs[i] = h0 ? h0[((size_t)bh * D + r) * D + c0 + c] : 0.f;
+  }
   __syncthreads();
   for (int sgi = 0; sgi < nseg; ++sgi) {
     const size_t base = ((size_t)bh * nseg + sgi) * D * D;
-    for (int i = t; i < D * D; i += kCombineThreads) {
-      Hin[base + i] = Hs[i];
-      Ms[i] = M[base + i];
+    for (int i = t; i < D * kCombineCols; i += kCombineThreads) {
+      const int r = i / kCombineCols, c = i % kCombineCols;
+      Hin[base + (size_t)r * D + c0 + c] = Hs[i];
     }
+    for (int i = t; i < D * D / 4; i += kCombineThreads) {
+      const float4 m4 = reinterpret_cast<const float4*>(M + base)[i];
+      const int r = (4 * i) / D, c = (4 * i) % D;
+      float* dst = Ms + r * kCombineLdM + c;
+      dst[0] = m4.x;
+      dst[1] = m4.y;
+      dst[2] = m4.z;
+      dst[3] = m4.w;
+    }
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = Nl[base + (size_t)d * D + c0 + e0 + j];
     __syncthreads();
-    float acc[8][8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = Nl[base + (size_t)(d0 + i) * D + e0 + j];
+#pragma unroll 4
     for (int k = 0; k < D; ++k) {
-      const float4 h_lo = *reinterpret_cast<const float4*>(Hs + k * D + e0);
-      const float4 h_hi = *reinterpret_cast<const float4*>(Hs + k * D + e0 + 4);
-      const float hv[8] = {h_lo.x, h_lo.y, h_lo.z, h_lo.w, h_hi.x, h_hi.y, h_hi.z, h_hi.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float m = Ms[(d0 + i) * D + k];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(m, hv[j], acc[i][j]);
-      }
+      const float m = Ms[d * kCombineLdM + k];
+      const float4 h_lo = *reinterpret_cast<const float4*>(Hs + k * kCombineCols + e0);
+      const float4 h_hi = *reinterpret_cast<const float4*>(Hs + k * kCombineCols + e0 + 4);
+      acc[0] = fmaf(m, h_lo.x, acc[0]);
+      acc[1] = fmaf(m, h_lo.y, acc[1]);
+      acc[2] = fmaf(m, h_lo.z, acc[2]);
+      acc[3] = fmaf(m, h_lo.w, acc[3]);
+      acc[4] = fmaf(m, h_hi.x, acc[4]);
+      acc[5] = fmaf(m, h_hi.y, acc[5]);
+      acc[6] = fmaf(m, h_hi.z, acc[6]);
+      acc[7] = fmaf(m, h_hi.w, acc[7]);
     }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) Hs[(d0 + i) * D + e0 + j] = acc[i][j];
+    for (int j = 0; j < 8; ++j) Hs[d * kCombineCols + e0 + j] = acc[j];
     __syncthreads();
   }
   if (ht)
-    for (int i = t; i < D * D; i += kCombineThreads) ht[(size_t)bh * D * D + i] = Hs[i];
+    for (int i = t; i < D * kCombineCols; i += kCombineThreads) {
+      const int r = i / kCombineCols, c = i % kCombineCols;
+      ht[((size_t)bh * D + r) * D + c0 + c] = Hs[i];
+    }
 }
 
 // Chunks per segment of the forward pass, or 0 for no segments.  A pass over
@@ -1787,7 +1808,7 @@ cudaError_t tc_fwd(const Problem& p, cudaStream_t s, bool save) {
                            kCombineSmem);
   if (e != cudaSuccess) return e;
   prof_before(s);
-  gdn_tc_combine_kernel<<<p.B * p.H, kCombineThreads, kCombineSmem, s>>>(Mt, Nl, p.h0, Hin, p.ht,
+  gdn_tc_combine_kernel<<<p.B * p.H * kCombineSplit, kCombineThreads, kCombineSmem, s>>>(Mt, Nl, p.h0, Hin, p.ht,
                                                                           nseg);
   prof_after(s, kTcCombine);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
