@@ -158,6 +158,21 @@ def test_segmented_forward_matches_oracle():
     compare(x, o, ht, None, fp32=False)
 
 
+def test_many_segments_forward_matches_oracle():
+    """One long sequence: the forward takes as many segments as the minimum
+    segment length allows (63 of 33 chunks here), so the combine chains 63
+    segment maps and its column blocks.  Output and final state against the
+    oracle, with an initial state and a ragged tail."""
+    x = make_inputs(1, 64 * 2048 + 5, 1, 128, 128, dtype="bf16", h0_std=0.3, seed=15)
+    d = x.to("cuda")
+    with gdn.KernelTimer() as t:
+        o, ht = gdn.gdn_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0)
+        torch.cuda.synchronize()
+    names = [n for n, _ in t.records()]
+    assert "tc_combine" in names and names.count("tc_fwd_segment") == 2, names
+    compare(x, o, ht, None, fp32=False)
+
+
 # ----------------------------------------------------------- fast-decaying gates
 
 # The workloads' gates are logsigmoid(N(2, 1)), about -0.13 a token.  These
